@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""HSQ decode-step benchmark on the Qwen3-8B-shaped 32K-context workload.
+
+One step = one decode step of one layer: routing + top-beta selection
+(hsq_route) and the union attention with the selected L3 groups gathered
+in-kernel from pinned host memory (hsq_decode_attn).  Steps run strictly in
+order; each step uses a fresh query (the workload's 512 queries, cycled).
+A 256 MiB device buffer is written between timed steps so every step starts
+with a cold L2 (the whole per-step working set would otherwise sit in L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hsq|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU
+oracle on the same workload (one KV head per step, scaled to a full step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "HSQ decode steps/s (Qwen3-8B shape, 32K ctx); effective GB/s vs HBM/link peak"
+UNIT = "steps/s"
+WORKLOAD = "qwen3_8b_32k"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["hsq", "reference"], default="hsq")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    p.add_argument("--n-splits", type=int, default=0)
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def input_rope(x, p, theta):
+    """Rotary embedding used only to build the planted-needle inputs
+    (rotate-half pairing, float64 angles)."""
+    x = np.asarray(x, dtype=np.float64)
+    h = x.shape[-1] // 2
+    ang = np.asarray(p, dtype=np.float64)[..., None] * theta ** (-2.0 * np.arange(h) / x.shape[-1])
+    c, s = np.cos(ang), np.sin(ang)
+    return np.concatenate([x[..., :h] * c - x[..., h:] * s, x[..., h:] * c + x[..., :h] * s], axis=-1)
+
+
+def workload_inputs(w, rope):
+    li = W.layer_inputs(w, rope=rope)
+    q, pos = W.queries(w, steps=w.steps)
+    return li, q, pos
+
+
+def algorithmic_bytes(w, l1_count: int, nonempty: int):
+    """Bytes the method must move once per layer-step (HBM and host link)."""
+    l1 = w.B * w.Hkv * l1_count * 2 * 68
+    l2 = w.B * w.Hkv * nonempty * 2 * 52
+    link = w.B * w.Hkv * w.beta * w.N * 136
+    return {"hbm": l1 + l2, "link": link, "l1": l1, "l2": l2,
+            "attn_hbm": l1 + w.B * w.Hkv * max(nonempty - w.beta, 0) * 2 * 52,
+            "route_hbm": w.B * w.Hkv * nonempty * 52}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"hsq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def link_peak(torch, nbytes=1 << 30, reps=5):
+    """Pinned host <-> device copy bandwidth (GB/s), best of `reps`."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        out[name] = nbytes / (best * 1e-3) / 1e9
+    del h, d
+    return out
+
+
+def cpu_oracle_sample(w, li, q, pos, seconds: float):
+    """The float64 oracle timed on the host cores: one KV head per decode step,
+    run for about `seconds`, scaled to the full B * Hkv step."""
+    import oracle as O
+    r = w.r
+    t0 = time.perf_counter()
+    cache = O.encode(li.K[:, :1], li.V[:, :1], li.l1_mask, li.signs, w.N, w.theta)
+    enc_s = time.perf_counter() - t0
+    n, spent = 0, 0.0
+    while spent < seconds and n < w.steps:
+        s = n % w.steps
+        t0 = time.perf_counter()
+        sel, _ = O.route(cache, q[s][:, :r], pos[s], w.beta)
+        O.decode_attn(cache, q[s][:, :r], pos[s], sel)
+        spent += time.perf_counter() - t0
+        n += 1
+    per_head = spent / n
+    full = per_head * w.B * w.Hkv
+    return {"value": 1.0 / full, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"KV head 0 of {w.name}: encode of that head ({enc_s:.2f} s, not in the value) then "
+                      f"{n} decode steps of that head ({spent:.1f} s); step time x {w.B * w.Hkv} heads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle as O
+    w = W.get_workload(WORKLOAD)
+    li, q, pos = workload_inputs(w, lambda x, p: O.rope(x, p, w.theta))
+    caches = {}
+
+    def step(s):
+        h = s % w.Hkv
+        if h not in caches:
+            caches[h] = O.encode(li.K[:, h:h + 1], li.V[:, h:h + 1], li.l1_mask, li.signs, w.N, w.theta)
+        c = caches[h]
+        qs = q[s % w.steps][:, h * w.r:(h + 1) * w.r]
+        t0 = time.perf_counter()
+        sel, _ = O.route(c, qs, pos[s % w.steps], w.beta)
+        O.decode_attn(c, qs, pos[s % w.steps], sel)
+        return time.perf_counter() - t0
+
+    for s in range(args.warmup):
+        step(s)
+    t = [step(args.warmup + s) for s in range(args.steps)]
+    per_head = sum(t) / len(t)
+    full = per_head * w.B * w.Hkv
+    value = 1.0 / full
+    cores = len(os.sched_getaffinity(0))
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta}",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"each step = one KV head of the {w.B * w.Hkv}-head decode step "
+                                   f"(round robin), scaled by {w.B * w.Hkv}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_hsq(args, rank, world, local):
+    import ctypes
+
+    import torch
+
+    import hierarchical_kv_cache_hsq_gb300 as H
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    H.load_library()
+    lib = H.load_library()
+    w = W.get_workload(WORKLOAD)
+    li, q, pos = workload_inputs(w, lambda x, p: input_rope(x, p, w.theta))
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
+                        args.n_splits)
+    ctx = H.Context(cfg)
+    caches = {"host": H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False),
+              "device": H.allocate_cache(ctx, w.B, w.T, l3_on_host=False, with_staging=False)}
+    for c in caches.values():
+        H.set_layer_inputs(c, li.l1_mask, li.signs)
+    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+
+    # encode (prefill of this layer), both L3 placements
+    enc = {}
+    for name, c in caches.items():
+        H.hsq_encode(ctx, c, K, V)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            H.hsq_encode(ctx, c, K, V)
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        enc[name] = statistics.median(ts)
+    assert H.hsq_sync_status(ctx) == 0
+    l1_count = int(caches["host"].view("l1_count").cpu()[0])
+    nonempty = int((caches["host"].view("l2_cnt").cpu() > 0).sum())
+    ab = algorithmic_bytes(w, l1_count, nonempty)
+    del K, V
+
+    qd = torch.from_numpy(q).cuda()          # [steps, B, Hq, 128]
+    pd = torch.from_numpy(pos).cuda()        # [steps, B]
+    q_host = torch.from_numpy(q).pin_memory()
+    p_host = torch.from_numpy(pos).pin_memory()
+    q_in = torch.empty_like(qd[0])
+    p_in = torch.empty_like(pd[0])
+    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    out_host = torch.empty((w.B, w.Hq, 128), pin_memory=True)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    structs = {k: c.struct() for k, c in caches.items()}
+
+    # needle sanity on step 0: the planted group is routed for every KV head
+    st = structs["host"]
+    lib.hsq_route(ctx.handle, ctypes.byref(st), qd[0].data_ptr(), pd[0].data_ptr(), sel.data_ptr(), None, sh)
+    torch.cuda.synchronize()
+    s0 = sel.cpu().numpy()
+    needle_ok = all(int(li.needle_group[0, h]) in s0[0, h] for h in range(w.Hkv))
+
+    def loop(cache_key, nsteps, e2e=False, timed=True):
+        stc = structs[cache_key]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsteps)] if timed else None
+        torch.cuda._sleep(20_000_000)   # let the host queue the steps ahead of the GPU
+        for i in range(nsteps):
+            s = i % w.steps
+            flush.fill_(i & 255)
+            if timed:
+                ev[i][0].record()
+            if e2e:
+                q_in.copy_(q_host[s], non_blocking=True)
+                p_in.copy_(p_host[s], non_blocking=True)
+                qp, pp = q_in.data_ptr(), p_in.data_ptr()
+            else:
+                qp, pp = qd[s].data_ptr(), pd[s].data_ptr()
+            lib.hsq_route(ctx.handle, ctypes.byref(stc), qp, pp, sel.data_ptr(), None, sh)
+            if timed:
+                ev[i][1].record()
+            lib.hsq_decode_attn(ctx.handle, ctypes.byref(stc), qp, pp, sel.data_ptr(), out.data_ptr(), 0, sh)
+            if e2e:
+                out_host.copy_(out, non_blocking=True)
+            if timed:
+                ev[i][2].record()
+        torch.cuda.synchronize()
+        if not timed:
+            return None
+        step = [e[0].elapsed_time(e[2]) for e in ev]
+        route = [e[0].elapsed_time(e[1]) for e in ev]
+        attn = [e[1].elapsed_time(e[2]) for e in ev]
+        return {"step_ms": step, "route_ms": route, "attn_ms": attn}
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    loop("host", args.warmup, timed=False)
+    barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall = time.perf_counter()
+    res = loop("host", args.steps)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    assert H.hsq_sync_status(ctx) == 0
+
+    loop("device", args.warmup, timed=False)
+    res_dev = loop("device", args.steps)
+    loop("host", args.warmup, e2e=True, timed=False)
+    res_e2e = loop("host", args.steps, e2e=True)
+    assert H.hsq_sync_status(ctx) == 0
+
+    tot = sum(res["step_ms"])
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([tot], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot = float(t.item())
+    ms_per_step = tot / args.steps
+    value = world * args.steps / (tot * 1e-3)
+    mean = lambda x: sum(x) / len(x)
+    t_route, t_attn = mean(res["route_ms"]), mean(res["attn_ms"])
+    hbm_peak, peak_src = measured_peaks()
+    lp = link_peak(torch)
+    link_gbs = lp["h2d_gbs"]
+    # whole-step roofline: t* = max(HBM bytes / HBM peak, link bytes / link peak)
+    t_star = max(ab["hbm"] / (hbm_peak * 1e9), ab["link"] / (link_gbs * 1e9))
+    dev_ms = mean(res_dev["step_ms"])
+    t_star_dev = (ab["hbm"] + ab["link"]) / (hbm_peak * 1e9)
+    attn_dev = mean(res_dev["attn_ms"])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta} "
+                               f"L1={l1_count} non-empty groups={nonempty}, L3 in pinned host memory",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{FLUSH_BYTES >> 20} MiB device write between timed steps (cold L2 each step)",
+                   "n_splits": args.n_splits or "auto"},
+        "roofline": {"bound": "link", "achieved": ab["link"] / (t_attn * 1e-3) / 1e9, "peak": link_gbs,
+                     "unit": "GB/s", "frac": ab["link"] / (t_attn * 1e-3) / 1e9 / link_gbs, "traffic": None,
+                     "kernel": "attn_kernel (fused L3 gather)", "peak_source": "measured pinned H2D copy in this run",
+                     "bytes_per_launch": ab["link"]},
+        "roofline_hbm_device_l3": {"bound": "hbm", "achieved": (ab["attn_hbm"] + ab["link"]) / (attn_dev * 1e-3) / 1e9,
+                                   "peak": hbm_peak, "unit": "GB/s",
+                                   "frac": (ab["attn_hbm"] + ab["link"]) / (attn_dev * 1e-3) / 1e9 / hbm_peak,
+                                   "traffic": None, "kernel": "attn_kernel, L3 in device memory",
+                                   "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+        "step_roofline": {"t_star_us": t_star * 1e6, "t_us": ms_per_step * 1e3, "frac": t_star / (ms_per_step * 1e-3),
+                          "hbm_bytes": ab["hbm"], "link_bytes": ab["link"],
+                          "hbm_gbs": ab["hbm"] / (ms_per_step * 1e-3) / 1e9,
+                          "link_gbs": ab["link"] / (ms_per_step * 1e-3) / 1e9},
+        "kernels_us": {"route": t_route * 1e3, "attn": t_attn * 1e3},
+        "device_l3": {"value": 1e3 / dev_ms, "unit": UNIT, "ms_per_step": dev_ms,
+                      "step_roofline_frac": t_star_dev / (dev_ms * 1e-3),
+                      "kernels_us": {"route": mean(res_dev["route_ms"]) * 1e3, "attn": attn_dev * 1e3}},
+        "e2e": {"value": 1e3 / mean(res_e2e["step_ms"]), "unit": UNIT,
+                "h2d_bytes_per_step": q_in.numel() * 4 + p_in.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 4},
+        "encode": {"ms_pinned_l3": enc["host"], "ms_device_l3": enc["device"],
+                   "tokens_per_s_pinned_l3": w.B * w.T / (enc["host"] * 1e-3),
+                   "input_gbs_pinned_l3": w.B * w.Hkv * w.T * 2 * 128 * 2 / (enc["host"] * 1e-3) / 1e9,
+                   "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
+        "link_peak": lp,
+        "gpu_launches": 2 * args.steps,
+        "tokens_per_s": value * w.B,
+        "needle_routed_step0": needle_ok,
+        "wall_s_timed_loop": wall,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, li, q, pos, args.cpu_baseline_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    ctx.close()
+    return line if rank == 0 else None
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_hsq(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

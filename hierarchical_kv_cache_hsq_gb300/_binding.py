@@ -1,0 +1,322 @@
+"""ctypes binding of the HSQ C ABI (``include/hsq.h``).
+
+Argument marshalling only: every step of the compressed-KV path runs in the
+CUDA kernels of ``_build/libhsq.so``.  torch supplies device / pinned memory
+and stream handles.  If the library has not been built the loader raises --
+there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import numpy as np
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+LIB_PATH = os.path.join(PKG, "_build", "libhsq.so")
+HEADER = os.path.join(ROOT, "include", "hsq.h")
+
+HSQ_OK, HSQ_ERR_INVALID, HSQ_ERR_CUDA, HSQ_ERR_NOMEM = 0, 1, 2, 3
+HSQ_ERR_TIMEOUT, HSQ_ERR_DEVICE_CHECK, HSQ_ERR_UNSUPPORTED = 4, 5, 6
+HSQ_DTYPE_F32, HSQ_DTYPE_BF16 = 0, 1
+HSQ_ATTN_FROM_STAGING = 1
+HSQ_FAULT_ALLOC, HSQ_FAULT_FETCH = 1, 2
+HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER = 1, 2, 4
+
+BUFFERS = ["l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc", "l2_kn",
+           "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging"]
+HSQ_NBUF = len(BUFFERS)
+
+
+class HSQError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"hsq status {status}: {msg}")
+        self.status = status
+
+
+class hsq_config(ctypes.Structure):
+    _fields_ = [
+        ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("group_n", ctypes.c_int), ("beta", ctypes.c_int), ("bits_l1l3", ctypes.c_int),
+        ("bits_l2", ctypes.c_int), ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int),
+        ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
+        ("n_splits", ctypes.c_int),
+    ]
+
+
+class hsq_cache(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("T", ctypes.c_int),
+        ("l1_kc", ctypes.c_void_p), ("l1_vc", ctypes.c_void_p), ("l1_kn", ctypes.c_void_p),
+        ("l1_vn", ctypes.c_void_p), ("l1_pos", ctypes.c_void_p), ("l1_count", ctypes.c_void_p),
+        ("l2_kc", ctypes.c_void_p), ("l2_vc", ctypes.c_void_p), ("l2_kn", ctypes.c_void_p),
+        ("l2_vn", ctypes.c_void_p), ("l2_cnt", ctypes.c_void_p),
+        ("l3", ctypes.c_void_p), ("l3_on_host", ctypes.c_int),
+        ("l1_bitmap", ctypes.c_void_p), ("signs", ctypes.c_void_p), ("staging", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_SIGS = {
+    "hsq_codebook": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _vp, _vp]),
+    "hsq_cache_sizes": (ctypes.c_int, [ctypes.POINTER(hsq_config), ctypes.c_int, ctypes.c_int, _vp]),
+    "hsq_create": (ctypes.c_int, [ctypes.POINTER(hsq_config), ctypes.POINTER(_vp)]),
+    "hsq_destroy": (ctypes.c_int, [_vp]),
+    "hsq_encode": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, ctypes.c_int, _vp]),
+    "hsq_route": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
+    "hsq_fetch_dequant": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
+    "hsq_decode_attn": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
+    "hsq_decode_step": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
+    "hsq_sync_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
+    "hsq_last_error": (ctypes.c_char_p, [_vp]),
+    "hsq_debug_set_fault": (ctypes.c_int, [ctypes.c_uint]),
+    "hsq_version": (ctypes.c_char_p, []),
+}
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libhsq.so (built by ``hierarchical_kv_cache_hsq_gb300.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"HSQ CUDA library not built ({p} missing): run "
+                           "`python -m hierarchical_kv_cache_hsq_gb300.build` first")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name, None)
+        if fn is None:
+            continue
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def declared_symbols() -> list:
+    """Function names declared in include/hsq.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hsq_[a-z_]+)\s*\(", text)))
+
+
+def _check(st: int, ctx=None):
+    if st != HSQ_OK:
+        lib = load_library()
+        msg = lib.hsq_last_error(ctx)
+        raise HSQError(st, msg.decode() if msg else "")
+
+
+# -- host-only calls --------------------------------------------------------------
+
+def hsq_codebook(bits: int, dim: int = 128):
+    lib = load_library()
+    c = np.zeros(1 << bits, np.float64)
+    t = np.zeros((1 << bits) - 1, np.float64)
+    _check(lib.hsq_codebook(bits, dim, c.ctypes.data, t.ctypes.data))
+    return c, t
+
+
+def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
+                max_pos: int, theta: float = 1.0e6, n_splits: int = 0) -> hsq_config:
+    return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
+                      bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
+                      max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits)
+
+
+def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:
+    lib = load_library()
+    out = (ctypes.c_size_t * HSQ_NBUF)()
+    _check(lib.hsq_cache_sizes(ctypes.byref(cfg), B, T, ctypes.cast(out, _vp)))
+    return {name: int(out[i]) for i, name in enumerate(BUFFERS)}
+
+
+def hsq_debug_set_fault(mask: int):
+    _check(load_library().hsq_debug_set_fault(mask))
+
+
+def hsq_version() -> str:
+    return load_library().hsq_version().decode()
+
+
+# -- context and cache ---------------------------------------------------------------
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Context:
+    """Owns an hsq_ctx (codebooks, RoPE tables, scratch) on the current device."""
+
+    def __init__(self, cfg: hsq_config):
+        self.cfg = cfg
+        self.lib = load_library()
+        h = _vp()
+        _check(self.lib.hsq_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self.handle = h
+
+    @property
+    def r(self) -> int:
+        return self.cfg.n_q_heads // self.cfg.n_kv_heads
+
+    def close(self):
+        if self.handle:
+            self.lib.hsq_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def last_error(self) -> str:
+        return self.lib.hsq_last_error(self.handle).decode()
+
+
+@dataclass
+class CacheBuffers:
+    """The caller-owned buffers of one layer's cache (torch tensors) and its C view."""
+    B: int
+    T: int
+    N: int
+    Hkv: int
+    max_l1: int
+    beta: int
+    tensors: Dict[str, "object"]
+    signs: "object"
+    l3_on_host: bool
+
+    @property
+    def G(self) -> int:
+        return -(-self.T // self.N)
+
+    def struct(self) -> hsq_cache:
+        t = self.tensors
+        c = hsq_cache(B=self.B, T=self.T, l3_on_host=1 if self.l3_on_host else 0)
+        for name in BUFFERS:
+            setattr(c, name, _ptr(t.get(name)))
+        c.signs = _ptr(self.signs)
+        return c
+
+    # shaped views (for tests and diagnostics)
+    def view(self, name: str):
+        t = self.tensors[name]
+        B, H, L1, G, N = self.B, self.Hkv, self.max_l1, self.G, self.N
+        shapes = {
+            "l1_kc": (B, H, L1, 64), "l1_vc": (B, H, L1, 64), "l1_kn": (B, H, L1), "l1_vn": (B, H, L1),
+            "l1_pos": (B, L1), "l1_count": (B,), "l2_kc": (B, H, G, 48), "l2_vc": (B, H, G, 48),
+            "l2_kn": (B, H, G), "l2_vn": (B, H, G), "l2_cnt": (B, G), "l3": (B, H, G, N * 136),
+            "l1_bitmap": (B, (self.T + 31) // 32), "staging": (B, H, self.beta, N * 136),
+        }
+        import torch
+        dt = {"l1_kn": torch.float32, "l1_vn": torch.float32, "l2_kn": torch.float32,
+              "l2_vn": torch.float32, "l1_pos": torch.int32, "l1_count": torch.int32,
+              "l1_bitmap": torch.int32}.get(name, torch.uint8)
+        return t.view(dt).view(shapes[name])
+
+
+def l1_bitmap_words(mask: np.ndarray) -> np.ndarray:
+    """[B, T] bool -> [B, ceil(T/32)] uint32, bit (t & 31) of word t >> 5."""
+    mask = np.asarray(mask, dtype=bool)
+    B, T = mask.shape
+    W = (T + 31) // 32
+    padded = np.zeros((B, W * 32), dtype=bool)
+    padded[:, :T] = mask
+    bits = padded.reshape(B, W, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)
+    return bits.sum(axis=2).astype(np.uint32)
+
+
+def allocate_cache(ctx: Context, B: int, T: int, l3_on_host: bool = True, with_staging: bool = True,
+                   device=None) -> CacheBuffers:
+    import torch
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    sizes = hsq_cache_sizes(ctx.cfg, B, T)
+    t = {}
+    for name in BUFFERS:
+        n = max(sizes[name], 16)
+        if name == "staging" and not with_staging:
+            continue
+        if name == "l3" and l3_on_host:
+            t[name] = torch.zeros(n, dtype=torch.uint8, pin_memory=True)
+        else:
+            t[name] = torch.zeros(n, dtype=torch.uint8, device=dev)
+    signs = torch.ones(128, dtype=torch.int8, device=dev)
+    return CacheBuffers(B=B, T=T, N=ctx.cfg.group_n, Hkv=ctx.cfg.n_kv_heads, max_l1=ctx.cfg.max_l1,
+                        beta=ctx.cfg.beta, tensors=t, signs=signs, l3_on_host=l3_on_host)
+
+
+def set_layer_inputs(cache: CacheBuffers, l1_mask: np.ndarray, signs: np.ndarray):
+    """Upload the L1 membership bitmap and the sign vector of a layer."""
+    import torch
+    words = l1_bitmap_words(l1_mask)
+    bm = cache.tensors["l1_bitmap"]
+    src = torch.from_numpy(words.view(np.uint8).reshape(-1).copy())
+    bm[: src.numel()].copy_(src)
+    cache.signs.copy_(torch.from_numpy(np.asarray(signs, np.int8)))
+
+
+# -- the four calls of the path (+ the fused step) ------------------------------------
+
+def hsq_encode(ctx: Context, cache: CacheBuffers, K, V, stream=None):
+    import torch
+    if K.dtype == torch.bfloat16:
+        dt = HSQ_DTYPE_BF16
+    elif K.dtype == torch.float32:
+        dt = HSQ_DTYPE_F32
+    else:
+        raise ValueError("K/V must be bfloat16 or float32")
+    if not (K.is_contiguous() and V.is_contiguous() and V.dtype == K.dtype):
+        raise ValueError("K and V must be contiguous and of one dtype")
+    c = cache.struct()
+    _check(ctx.lib.hsq_encode(ctx.handle, ctypes.byref(c), K.data_ptr(), V.data_ptr(), dt,
+                              _stream_handle(stream)), ctx.handle)
+
+
+def hsq_route(ctx: Context, cache: CacheBuffers, q, pos, sel, scores=None, stream=None):
+    c = cache.struct()
+    _check(ctx.lib.hsq_route(ctx.handle, ctypes.byref(c), q.data_ptr(), pos.data_ptr(), sel.data_ptr(),
+                             _ptr(scores), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_fetch_dequant(ctx: Context, cache: CacheBuffers, sel, k_out=None, v_out=None, valid=None,
+                      stream=None):
+    c = cache.struct()
+    _check(ctx.lib.hsq_fetch_dequant(ctx.handle, ctypes.byref(c), sel.data_ptr(), _ptr(k_out), _ptr(v_out),
+                                     _ptr(valid), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_decode_attn(ctx: Context, cache: CacheBuffers, q, pos, sel, out, flags: int = 0, stream=None):
+    c = cache.struct()
+    _check(ctx.lib.hsq_decode_attn(ctx.handle, ctypes.byref(c), q.data_ptr(), pos.data_ptr(), sel.data_ptr(),
+                                   out.data_ptr(), flags, _stream_handle(stream)), ctx.handle)
+
+
+def hsq_decode_step(ctx: Context, cache: CacheBuffers, q, pos, sel, out, stream=None):
+    c = cache.struct()
+    _check(ctx.lib.hsq_decode_step(ctx.handle, ctypes.byref(c), q.data_ptr(), pos.data_ptr(), sel.data_ptr(),
+                                   out.data_ptr(), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_sync_status(ctx: Context, stream=None) -> int:
+    """Synchronise, return the device error word (raises on a CUDA error only)."""
+    w = ctypes.c_int(0)
+    st = ctx.lib.hsq_sync_status(ctx.handle, _stream_handle(stream), ctypes.byref(w))
+    if st not in (HSQ_OK, HSQ_ERR_DEVICE_CHECK):
+        _check(st, ctx.handle)
+    return int(w.value)

@@ -1,0 +1,1404 @@
+// HSQ compressed-KV kernels for GB300 (sm_103a) and the C entry points that
+// launch them.
+//
+// Method: Tamarin (HSQ) technical summary (gist.science rs-10297225),
+// section 2: three-tier cache (L1 focal 4-bit, L2 3-bit group summaries,
+// L3 4-bit archive) and the decode process (route -> fetch + dequantise +
+// rotate to position -> attention over the union, fetched summaries
+// masked).  TurboQuant: "Ablation, Statistical Inference, and Validation
+// for KV-Cache Compression" (gist.science 2607.09683), experimental setup
+// item 1 (randomised Walsh-Hadamard transform + Beta Lloyd-Max codebook).
+//
+// Thread mapping.  Every 128-d vector is handled by one half-warp (16
+// lanes).  Lane l of the half holds dims {4l..4l+3} in v[0..3] and
+// {64+4l..64+4l+3} in v[4..7]:
+//   * RoPE pairs (i, i+64) sit in the same lane, so RoPE needs no shuffle;
+//   * the Walsh-Hadamard transform runs its index bits 0, 1 and 6 in
+//     registers and bits 2-5 as four xor-shuffles inside the half-warp;
+//   * 4-bit codes of a lane are two 16-bit words of the 64-byte record.
+// The two halves of a warp work independently (shuffles carry a 16-lane
+// mask), so a half-warp is the unit of work in every kernel.
+//
+// All arithmetic is fp32.  Softmax runs in the log2 domain (logits scaled by
+// log2(e)/sqrt(128), exp2).
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "hsq_internal.h"
+
+namespace {
+
+using hsq::kDim;
+
+constexpr float kRsqrtD = 0.08838834764831845f;                 // 1/sqrt(128)
+constexpr float kLogitScaleLog2 = 0.12751743074960003f;         // log2(e)/sqrt(128)
+constexpr int kThreads = 256;                                   // all kernels but encode
+constexpr int kHalves = kThreads / 16;
+constexpr int kRouteGroupsPerCta = 128;
+constexpr int kFetchBatchBytes = 17408;                          // fetched records staged per pass
+constexpr int kMaxFetchChunksPerThread = (kFetchBatchBytes / 16 + kThreads - 1) / kThreads;
+
+// ---------------------------------------------------------------------------
+// Parameter blocks (passed by value).
+// ---------------------------------------------------------------------------
+
+struct Tables {
+    const float* cb;        // c4[16] | t4[15] pad | c3[8] | t3[7] pad
+    const float* rope_hi;   // [n_hi][cos 64 | sin 64]
+    const float* rope_lo;   // [256][cos 64 | sin 64]
+    int max_pos;
+};
+
+struct CacheView {
+    int B, T, G, N, Hkv, Hq, beta, max_l1, W;
+    const uint8_t* l1_kc; const uint8_t* l1_vc; const float* l1_kn; const float* l1_vn;
+    const int32_t* l1_pos; const int32_t* l1_count;
+    const uint8_t* l2_kc; const uint8_t* l2_vc; const float* l2_kn; const float* l2_vn;
+    const uint8_t* l2_cnt;
+    const uint8_t* l3;
+    const uint32_t* l1_bitmap;
+    const int8_t* signs;
+    const uint8_t* staging;
+};
+
+// ---------------------------------------------------------------------------
+// Half-warp helpers.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned half_mask() { return 0xFFFFu << (threadIdx.x & 16); }
+__device__ __forceinline__ int hlane() { return threadIdx.x & 15; }
+
+__device__ __forceinline__ float half_sum(float v, unsigned m) {
+    v += __shfl_xor_sync(m, v, 1, 16);
+    v += __shfl_xor_sync(m, v, 2, 16);
+    v += __shfl_xor_sync(m, v, 4, 16);
+    v += __shfl_xor_sync(m, v, 8, 16);
+    return v;
+}
+
+// Unnormalised Sylvester-Hadamard transform of the half-warp's 128-vector.
+__device__ __forceinline__ void fwht(float v[8], unsigned m) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {  // index bit 0
+        float a = v[i], b = v[i + 1];
+        v[i] = a + b; v[i + 1] = a - b;
+    }
+#pragma unroll
+    for (int base = 0; base < 8; base += 4) {  // index bit 1
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            float a = v[base + k], b = v[base + k + 2];
+            v[base + k] = a + b; v[base + k + 2] = a - b;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // index bit 6
+        float a = v[k], b = v[k + 4];
+        v[k] = a + b; v[k + 4] = a - b;
+    }
+    const int l = hlane();
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1) {  // index bits 2..5 = lane bits 0..3
+        const bool upper = (l & s) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float p = __shfl_xor_sync(m, v[i], s, 16);
+            v[i] = upper ? (p - v[i]) : (v[i] + p);
+        }
+    }
+}
+
+__device__ __forceinline__ void load_signs(float s[8], const float* s_sign) {
+    const int l = hlane();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        s[k] = s_sign[4 * l + k];
+        s[4 + k] = s_sign[64 + 4 * l + k];
+    }
+}
+
+// RoPE at position p by angle addition: p = 256 a + c.
+__device__ __forceinline__ void rope(float v[8], int p, const Tables& tb) {
+    const int l = hlane();
+    const float* rh = tb.rope_hi + (size_t)(p >> 8) * kDim;
+    const float* rl = tb.rope_lo + (size_t)(p & 255) * kDim;
+    const float4 ch = __ldg(reinterpret_cast<const float4*>(rh + 4 * l));
+    const float4 sh = __ldg(reinterpret_cast<const float4*>(rh + 64 + 4 * l));
+    const float4 cl = __ldg(reinterpret_cast<const float4*>(rl + 4 * l));
+    const float4 sl = __ldg(reinterpret_cast<const float4*>(rl + 64 + 4 * l));
+    const float cA[4] = {ch.x, ch.y, ch.z, ch.w}, sA[4] = {sh.x, sh.y, sh.z, sh.w};
+    const float cB[4] = {cl.x, cl.y, cl.z, cl.w}, sB[4] = {sl.x, sl.y, sl.z, sl.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float c = fmaf(cA[k], cB[k], -sA[k] * sB[k]);
+        const float s = fmaf(sA[k], cB[k], cA[k] * sB[k]);
+        const float lo = v[k], hi = v[4 + k];
+        v[k] = fmaf(lo, c, -hi * s);
+        v[4 + k] = fmaf(hi, c, lo * s);
+    }
+}
+
+__device__ __forceinline__ int quant4(float y, const float* t) {
+    int c = (y > t[7]) ? 8 : 0;
+    c += (y > t[c + 3]) ? 4 : 0;
+    c += (y > t[c + 1]) ? 2 : 0;
+    c += (y > t[c]) ? 1 : 0;
+    return c;
+}
+
+__device__ __forceinline__ int quant3(float y, const float* t) {
+    int c = (y > t[3]) ? 4 : 0;
+    c += (y > t[c + 1]) ? 2 : 0;
+    c += (y > t[c]) ? 1 : 0;
+    return c;
+}
+
+// TurboQuant forward: y = Pi (x / n) with Pi = H diag(s) / sqrt(d).  Returns n.
+__device__ __forceinline__ float tq_rotate(float x[8], float y[8], const float sg[8], unsigned m) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+    ss = half_sum(ss, m);
+    const float n = sqrtf(ss);
+    const float inv = n > 0.f ? 1.0f / n : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = x[i] * inv * sg[i];
+    fwht(y, m);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] *= kRsqrtD;
+    return n;
+}
+
+// 4-bit codes of the lane's 8 coordinates as the two 16-bit words of the record.
+__device__ __forceinline__ void pack4(const float y[8], const float* t4, uint16_t& lo, uint16_t& hi) {
+    uint32_t a = 0, b = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        a |= (uint32_t)quant4(y[k], t4) << (4 * k);
+        b |= (uint32_t)quant4(y[4 + k], t4) << (4 * k);
+    }
+    lo = (uint16_t)a;
+    hi = (uint16_t)b;
+}
+
+__device__ __forceinline__ void unpack4(uint32_t lo, uint32_t hi, const float* c4, float scale, float v[8]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[k] = c4[(lo >> (4 * k)) & 15] * scale;
+        v[4 + k] = c4[(hi >> (4 * k)) & 15] * scale;
+    }
+}
+
+// 3-bit record (12 words): the lane's fields start at bits 12 l and 192 + 12 l.
+__device__ __forceinline__ void unpack3(const uint32_t* __restrict__ rec, const float* c3, float scale, float v[8]) {
+    const int l = hlane();
+    const int bit = 12 * l, w = bit >> 5, sh = bit & 31;
+    const int w1 = min(w + 1, 5);
+    const uint32_t a0 = __ldg(rec + w), a1 = __ldg(rec + w1);
+    const uint32_t b0 = __ldg(rec + 6 + w), b1 = __ldg(rec + 6 + w1);
+    const uint32_t fa = __funnelshift_r(a0, a1, sh) & 0xFFFu;
+    const uint32_t fb = __funnelshift_r(b0, b1, sh) & 0xFFFu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[k] = c3[(fa >> (3 * k)) & 7] * scale;
+        v[4 + k] = c3[(fb >> (3 * k)) & 7] * scale;
+    }
+}
+
+__device__ __forceinline__ void load_f32x8(const float* __restrict__ p, float v[8]) {
+    const int l = hlane();
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p + 4 * l));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 64 + 4 * l));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void load_bf16x8(const uint16_t* __restrict__ p, float v[8]) {
+    const int l = hlane();
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(p + 4 * l));
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(p + 64 + 4 * l));
+    v[0] = __uint_as_float(a.x << 16); v[1] = __uint_as_float(a.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xFFFF0000u);
+    v[4] = __uint_as_float(b.x << 16); v[5] = __uint_as_float(b.x & 0xFFFF0000u);
+    v[6] = __uint_as_float(b.y << 16); v[7] = __uint_as_float(b.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void store_f32x8(float* __restrict__ p, const float v[8]) {
+    const int l = hlane();
+    *reinterpret_cast<float4*>(p + 4 * l) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 64 + 4 * l) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+__device__ __forceinline__ void load_tables(float* s_cb, float* s_sign, const Tables& tb,
+                                            const int8_t* __restrict__ signs) {
+    for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = tb.cb[i];
+    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = (float)signs[i];
+}
+
+__device__ __forceinline__ int checked_pos(int p, const Tables& tb, int* err) {
+    if (p < 0 || p >= tb.max_pos) {
+        atomicOr(err, HSQ_DEVERR_POS);
+        p = p < 0 ? 0 : tb.max_pos - 1;
+    }
+    return p;
+}
+
+__device__ __forceinline__ bool in_l1(const CacheView& c, int b, int t) {
+    const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
+    return (w >> (t & 31)) & 1u;
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int* s_warp, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < nw) s_warp[lane] = t;
+    }
+    __syncthreads();
+    total = s_warp[nw - 1];
+    const int before = warp > 0 ? s_warp[warp - 1] : 0;
+    __syncthreads();
+    return before + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// Encode, stage 1: L1 slot prefix per bitmap word, L1 position list, counts.
+// One CTA per sequence.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(1024) l1_index_kernel(CacheView c, int32_t* __restrict__ l1_pos,
+                                                        int32_t* __restrict__ l1_count,
+                                                        int32_t* __restrict__ prefix, int* err) {
+    __shared__ int s_warp[32];
+    const int b = blockIdx.x;
+    const int W = c.W;
+    const int per = (W + blockDim.x - 1) / blockDim.x;
+    const int w0 = min(W, (int)threadIdx.x * per), w1 = min(W, w0 + per);
+    auto word = [&](int w) -> uint32_t {
+        uint32_t x = c.l1_bitmap[(size_t)b * W + w];
+        const int valid = c.T - 32 * w;
+        if (valid < 32) x &= (1u << valid) - 1u;
+        return x;
+    };
+    int local = 0;
+    for (int w = w0; w < w1; ++w) local += __popc(word(w));
+    int total;
+    int run = block_exclusive_scan(local, s_warp, total);
+    for (int w = w0; w < w1; ++w) {
+        uint32_t x = word(w);
+        prefix[(size_t)b * W + w] = run;
+        while (x) {
+            const int bit = __ffs(x) - 1;
+            x &= x - 1;
+            if (run < c.max_l1) l1_pos[(size_t)b * c.max_l1 + run] = 32 * w + bit;
+            ++run;
+        }
+    }
+    if (threadIdx.x == 0) {
+        l1_count[b] = min(total, c.max_l1);
+        if (total > c.max_l1) atomicOr(err, HSQ_DEVERR_L1_OVER);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Encode, stage 2: one CTA per (group g, KV head h, sequence b), one warp per
+// token: half 0 encodes the key, half 1 the value.
+// ---------------------------------------------------------------------------
+
+struct EncodeOut {
+    uint8_t* l1_kc; uint8_t* l1_vc; float* l1_kn; float* l1_vn;
+    uint8_t* l2_kc; uint8_t* l2_vc; float* l2_kn; float* l2_vn; uint8_t* l2_cnt;
+    uint8_t* l3;
+    const int32_t* prefix;
+};
+
+template <int N, bool kBF16>
+__global__ void __launch_bounds__(N * 32) encode_kernel(CacheView c, EncodeOut o, const void* __restrict__ Kp,
+                                                        const void* __restrict__ Vp, Tables tb) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) uint8_t s_rec[N * 136];
+    __shared__ __align__(16) float s_sum[N][2][kDim];
+    __shared__ int s_member[N];
+    __shared__ uint32_t s_l2[2][12];
+
+    const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1, l = hlane();
+    const unsigned m = half_mask();
+    load_tables(s_cb, s_sign, tb, c.signs);
+    if (threadIdx.x < 24) (&s_l2[0][0])[threadIdx.x] = 0u;
+    __syncthreads();
+    const float* t4 = s_cb + 16;
+    const float* t3 = s_cb + 40;
+    float sg[8];
+    load_signs(sg, s_sign);
+
+    const int t = g * N + warp;
+    const bool in_ctx = t < c.T;
+    bool is_l1 = false;
+    int slot = 0;
+    if (in_ctx) {
+        const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
+        is_l1 = (w >> (t & 31)) & 1u;
+        if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
+    }
+
+    float x[8];
+    if (in_ctx) {
+        const size_t off = (((size_t)b * c.Hkv + h) * c.T + t) * kDim;
+        if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? Vp : Kp) + off, x);
+        else load_f32x8(static_cast<const float*>(half ? Vp : Kp) + off, x);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.f;
+    }
+
+    // L3: TQ4 of the raw (pre-RoPE) key / value
+    float y[8];
+    const float n = tq_rotate(x, y, sg, m);
+    uint16_t lo, hi;
+    pack4(y, t4, lo, hi);
+    {
+        uint8_t* row = s_rec + (half ? N * 64 : 0) + warp * 64;
+        reinterpret_cast<uint16_t*>(row)[l] = lo;
+        reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
+        if (l == 0) reinterpret_cast<float*>(s_rec + N * 128)[half * N + warp] = n;
+    }
+
+    // RoPE'd key (half 0) for L1 and for the group summary; values as they are
+    float xr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xr[i] = x[i];
+    if (half == 0 && in_ctx) rope(xr, t, tb);
+
+    if (is_l1 && slot < c.max_l1) {
+        const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
+        if (half == 0) {
+            float yr[8];
+            tq_rotate(xr, yr, sg, m);  // same norm as the raw key (RoPE is norm preserving)
+            uint16_t klo, khi;
+            pack4(yr, t4, klo, khi);
+            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
+            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64 + 32)[l] = khi;
+            if (l == 0) o.l1_kn[so] = n;
+        } else {
+            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64)[l] = lo;
+            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64 + 32)[l] = hi;
+            if (l == 0) o.l1_vn[so] = n;
+        }
+    }
+
+    const bool member = in_ctx && !is_l1;
+    if (member) {
+        float* row = &s_sum[warp][half][0];
+        *reinterpret_cast<float4*>(row + 4 * l) = make_float4(xr[0], xr[1], xr[2], xr[3]);
+        *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(xr[4], xr[5], xr[6], xr[7]);
+    }
+    if (threadIdx.x == warp * 32) s_member[warp] = member ? 1 : 0;
+    __syncthreads();
+
+    // L3 record out (16-byte chunks; through the host link when L3 is pinned host memory)
+    {
+        uint4* dst = reinterpret_cast<uint4*>(o.l3 + (((size_t)b * c.Hkv + h) * c.G + g) * (N * 136));
+        const uint4* src = reinterpret_cast<const uint4*>(s_rec);
+        for (int i = threadIdx.x; i < N * 136 / 16; i += blockDim.x) dst[i] = src[i];
+    }
+
+    // L2 summary: mean over members in token order, then TQ3
+    if (warp == 0) {
+        int cnt = 0;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int k = 0; k < N; ++k) {
+            if (!s_member[k]) continue;
+            ++cnt;
+            const float* row = &s_sum[k][half][0];
+            const float4 a = *reinterpret_cast<const float4*>(row + 4 * l);
+            const float4 bq = *reinterpret_cast<const float4*>(row + 64 + 4 * l);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += bq.x; acc[5] += bq.y; acc[6] += bq.z; acc[7] += bq.w;
+        }
+        if (cnt > 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
+        }
+        float ys[8];
+        const float ns = tq_rotate(acc, ys, sg, m);
+        uint32_t fa = 0, fb = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            fa |= (uint32_t)quant3(ys[k], t3) << (3 * k);
+            fb |= (uint32_t)quant3(ys[4 + k], t3) << (3 * k);
+        }
+        uint32_t* w = s_l2[half];
+        const int bit = 12 * l, wi = bit >> 5, sh = bit & 31;
+        atomicOr(&w[wi], fa << sh);
+        if (sh > 20) atomicOr(&w[wi + 1], fa >> (32 - sh));
+        atomicOr(&w[6 + wi], fb << sh);
+        if (sh > 20) atomicOr(&w[6 + wi + 1], fb >> (32 - sh));
+        __syncwarp();
+        const size_t go = ((size_t)b * c.Hkv + h) * c.G + g;
+        uint32_t* dst = reinterpret_cast<uint32_t*>((half ? o.l2_vc : o.l2_kc) + go * 48);
+        if (l < 12) dst[l] = w[l];
+        if (l == 0) (half ? o.l2_vn : o.l2_kn)[go] = ns;
+        if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Route: score every group of a (b, h) against the aggregated rotated query,
+// then the last CTA of the (b, h) selects the top beta by radix select.
+// grid = (ceil(G / 128), B * Hkv).
+// ---------------------------------------------------------------------------
+
+struct RouteArgs {
+    const float* q; const int32_t* pos; int32_t* sel; float* scores; int* counters; int* err;
+};
+
+__device__ __forceinline__ uint32_t ordered_key(float s) {
+    if (s == -INFINITY) return 0u;
+    const uint32_t u = __float_as_uint(s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs a, Tables tb) {
+    extern __shared__ uint32_t s_keys[];
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) float s_q[R][kDim];
+    __shared__ int s_hist[256];
+    __shared__ int s_warp[32];
+    __shared__ int s_flag;
+    __shared__ uint32_t s_digit;
+    __shared__ int s_above;
+
+    const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    load_tables(s_cb, s_sign, tb, c.signs);
+    __syncthreads();
+    float sg[8];
+    load_signs(sg, s_sign);
+
+    // rotated, RoPE'd query of each query head of this KV head
+    if (hw < R) {
+        const int j = h * R + hw;
+        const int p = checked_pos(__ldg(a.pos + b), tb, a.err);
+        float x[8];
+        load_f32x8(a.q + ((size_t)b * c.Hq + j) * kDim, x);
+        rope(x, p, tb);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= sg[i];
+        fwht(x, m);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            s_q[hw][4 * l + k] = x[k] * kRsqrtD;
+            s_q[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
+        }
+    }
+    __syncthreads();
+    float gq[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < R; ++jj) {
+            s0 += s_q[jj][4 * l + k];
+            s1 += s_q[jj][64 + 4 * l + k];
+        }
+        gq[k] = s0;
+        gq[4 + k] = s1;
+    }
+
+    const int g_begin = blockIdx.x * kRouteGroupsPerCta;
+    const int g_end = min(c.G, g_begin + kRouteGroupsPerCta);
+    const float* c3 = s_cb + 32;
+    for (int g = g_begin + hw; g < g_end; g += kHalves) {
+        const int cnt = __ldg(c.l2_cnt + (size_t)b * c.G + g);
+        float score = -INFINITY;
+        if (cnt > 0) {
+            const size_t go = (size_t)bh * c.G + g;
+            float v[8];
+            unpack3(reinterpret_cast<const uint32_t*>(c.l2_kc + go * 48), c3, 1.0f, v);
+            float d = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d = fmaf(gq[i], v[i], d);
+            d = half_sum(d, m);
+            score = __ldg(c.l2_kn + go) * d;
+        }
+        if (l == 0) a.scores[(size_t)bh * c.G + g] = score;
+    }
+
+    // last CTA of this (b, h) selects
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(a.counters + bh, 1);
+        s_flag = (ticket == (int)gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+
+    const int G = c.G, beta = c.beta;
+    int ne_local = 0;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const uint32_t k = ordered_key(__ldcg(a.scores + (size_t)bh * G + g));
+        s_keys[g] = k;
+        ne_local += (k != 0u);
+    }
+    int ne;
+    block_exclusive_scan(ne_local, s_warp, ne);  // also a barrier for s_keys
+
+    uint32_t kstar = 0u;
+    int need = 0;
+    if (beta < ne) {
+        uint32_t prefix = 0u, pmask = 0u;
+        int remaining = beta;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            s_hist[threadIdx.x] = 0;  // blockDim == 256
+            __syncthreads();
+            for (int g = threadIdx.x; g < G; g += blockDim.x) {
+                const uint32_t k = s_keys[g];
+                if ((k & pmask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                // lane L owns digits 255-8L-7 .. 255-8L (descending)
+                const int lane = threadIdx.x;
+                int cnt[8], tot = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) { cnt[i] = s_hist[255 - 8 * lane - i]; tot += cnt[i]; }
+                int inc = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int exc = inc - tot;  // count in higher digits
+                const bool here = exc < remaining && inc >= remaining;
+                if (here) {
+                    int acc = exc;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (acc + cnt[i] >= remaining) {
+                            s_digit = (uint32_t)(255 - 8 * lane - i);
+                            s_above = acc;
+                            break;
+                        }
+                        acc += cnt[i];
+                    }
+                }
+            }
+            __syncthreads();
+            prefix |= s_digit << shift;
+            pmask |= 255u << shift;
+            remaining -= s_above;
+            __syncthreads();
+        }
+        kstar = prefix;
+        need = remaining;
+    }
+
+    // ascending compaction: key > kstar, or key == kstar among the first `need` in index order
+    const int per = (G + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(G, (int)threadIdx.x * per), i1 = min(G, i0 + per);
+    int eq_local = 0;
+    for (int g = i0; g < i1; ++g) eq_local += (s_keys[g] == kstar && kstar != 0u);
+    int eq_total;
+    int eq_before = block_exclusive_scan(eq_local, s_warp, eq_total);
+    int sel_local = 0;
+    {
+        int e = eq_before;
+        for (int g = i0; g < i1; ++g) {
+            const uint32_t k = s_keys[g];
+            bool take = k > kstar;
+            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
+            sel_local += take;
+        }
+    }
+    int sel_total;
+    int out = block_exclusive_scan(sel_local, s_warp, sel_total);
+    {
+        int e = eq_before;
+        for (int g = i0; g < i1; ++g) {
+            const uint32_t k = s_keys[g];
+            bool take = k > kstar;
+            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
+            if (take && out < beta) a.sel[(size_t)bh * beta + out++] = g;
+        }
+    }
+    for (int i = sel_total + threadIdx.x; i < beta; i += blockDim.x) a.sel[(size_t)bh * beta + i] = -1;
+    if (threadIdx.x == 0) a.counters[bh] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Selection validity: entries must be -1 or in [0, G), non-negative entries
+// strictly ascending and before any -1.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int valid_sel(const int32_t* __restrict__ row, int i, int G, int* err) {
+    const int g = __ldg(row + i);
+    if (g < 0) return -1;
+    bool ok = g < G;
+    if (i > 0) {
+        const int p = __ldg(row + i - 1);
+        ok = ok && p >= 0 && p < g;
+    }
+    if (!ok) {
+        atomicOr(err, HSQ_DEVERR_SEL);
+        return -1;
+    }
+    return g;
+}
+
+// ---------------------------------------------------------------------------
+// Fetch + dequantise (standalone): one CTA per (selected slot i, b*Hkv + h).
+// ---------------------------------------------------------------------------
+
+struct FetchArgs {
+    const int32_t* sel; float* k_out; float* v_out; uint8_t* valid; uint8_t* staging; int* err;
+};
+
+template <int N>
+__global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs a, Tables tb) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) uint8_t s_rec[N * 136];
+    __shared__ int s_g;
+
+    const int i = blockIdx.x, bh = blockIdx.y, b = bh / c.Hkv;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    load_tables(s_cb, s_sign, tb, c.signs);
+    if (threadIdx.x == 0) s_g = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
+    __syncthreads();
+    const int g = s_g;
+    constexpr int kChunks = N * 136 / 16;
+    uint4* srec = reinterpret_cast<uint4*>(s_rec);
+    for (int k = threadIdx.x; k < kChunks; k += blockDim.x) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (g >= 0) v = __ldcg(reinterpret_cast<const uint4*>(c.l3 + ((size_t)bh * c.G + g) * (N * 136)) + k);
+        srec[k] = v;
+        if (a.staging) reinterpret_cast<uint4*>(a.staging + ((size_t)bh * c.beta + i) * (N * 136))[k] = v;
+    }
+    __syncthreads();
+    if (hw >= N) return;
+    float sg[8];
+    load_signs(sg, s_sign);
+    const int t = g * N + hw;
+    const bool have = g >= 0 && t < c.T;
+    const size_t oo = (((size_t)bh * c.beta + i) * N + hw) * kDim;
+    float kx[8], vx[8];
+    if (have) {
+        const float* c4 = s_cb;
+        const float* norms = reinterpret_cast<const float*>(s_rec + N * 128);
+        const uint16_t* kr = reinterpret_cast<const uint16_t*>(s_rec + hw * 64);
+        const uint16_t* vr = reinterpret_cast<const uint16_t*>(s_rec + N * 64 + hw * 64);
+        unpack4(kr[l], kr[16 + l], c4, 1.0f, kx);
+        unpack4(vr[l], vr[16 + l], c4, 1.0f, vx);
+        fwht(kx, m);
+        fwht(vx, m);
+        const float kn = norms[hw] * kRsqrtD, vn = norms[N + hw] * kRsqrtD;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            kx[q] *= sg[q] * kn;
+            vx[q] *= sg[q] * vn;
+        }
+        rope(kx, t, tb);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) kx[q] = vx[q] = 0.f;
+    }
+    if (a.k_out) store_f32x8(a.k_out + oo, kx);
+    if (a.v_out) store_f32x8(a.v_out + oo, vx);
+    if (a.valid && l == 0)
+        a.valid[((size_t)bh * c.beta + i) * N + hw] = (uint8_t)(have && !in_l1(c, b, t));
+}
+
+// ---------------------------------------------------------------------------
+// Union attention: grid = (S splits, B * Hkv).  Split s owns the L1 slots,
+// L2 groups and selected records of its share; each half-warp keeps an
+// online softmax for the r query heads; the CTA merges its half-warps, and
+// the last CTA of a (b, h) merges the splits and rotates the output back.
+// ---------------------------------------------------------------------------
+
+struct AttnArgs {
+    const float* q; const int32_t* pos; const int32_t* sel; float* out;
+    float* part; int* counters; int* err; int S; int from_staging;
+};
+
+template <int R>
+struct Softmax {
+    float m[R], l[R], acc[R][8];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+        }
+    }
+    // add one entry with log2-domain logits x[j] and value v
+    __device__ __forceinline__ void add(const float x[R], const float v[8]) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (x[j] > m[j]) {
+                const float corr = exp2f(m[j] - x[j]);
+                l[j] *= corr;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[j][i] *= corr;
+                m[j] = x[j];
+            }
+            const float p = exp2f(x[j] - m[j]);
+            l[j] += p;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(p, v[i], acc[j][i]);
+        }
+    }
+};
+
+__device__ __forceinline__ float merge_weight(float mi, float M) {
+    return mi == -INFINITY ? 0.f : exp2f(mi - M);
+}
+
+template <int R, int N>
+__global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a, Tables tb) {
+    extern __shared__ __align__(16) uint8_t s_dyn[];
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) float s_qt[R][kDim];
+    __shared__ __align__(16) float s_qr[R][kDim];
+    __shared__ int s_warp[32];
+    __shared__ int s_fg[kFetchBatchBytes / (N * 136)];
+    __shared__ int s_flag;
+
+    constexpr int RB = N * 136;
+    constexpr int kBatchRecs = kFetchBatchBytes / RB;
+    constexpr int kRecChunks = RB / 16;
+
+    const int s = blockIdx.x, S = a.S;
+    const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    const int32_t* selrow = a.sel + (size_t)bh * c.beta;
+
+    // this split's share of the selected records, L2 groups and L1 slots
+    const int f0 = (int)((long long)c.beta * s / S), f1 = (int)((long long)c.beta * (s + 1) / S);
+    const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
+    const int cnt1 = min(__ldg(c.l1_count + b), c.max_l1);
+    const int e0 = (int)((long long)cnt1 * s / S), e1 = (int)((long long)cnt1 * (s + 1) / S);
+
+    // dynamic smem: staged records | selected-group bitmap of [g0, g1) | L2 entry list | CTA merge
+    uint8_t* s_rec = s_dyn;
+    uint32_t* s_selbits = reinterpret_cast<uint32_t*>(s_dyn + kFetchBatchBytes);
+    const int nselw = (g1 - g0 + 31) / 32;
+    int* s_list = reinterpret_cast<int*>(s_selbits + ((c.G + S - 1) / S + 31) / 32 + 1);
+
+    // 1. start gathering the first batch of selected records (register staged)
+    uint4 pre[kMaxFetchChunksPerThread];
+    auto issue = [&](int r0, int nrec) {
+#pragma unroll
+        for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
+            const int ch = threadIdx.x + k * kThreads;
+            pre[k] = make_uint4(0, 0, 0, 0);
+            if (ch < nrec * kRecChunks) {
+                const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
+                const int i = r0 + rec;
+                const int g = __ldg(selrow + i);
+                if (g >= 0 && g < c.G) {
+                    const uint8_t* base = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
+                                                         : c.l3 + ((size_t)bh * c.G + g) * RB;
+                    pre[k] = __ldcg(reinterpret_cast<const uint4*>(base) + off);
+                }
+            }
+        }
+    };
+    const int nfetch = f1 - f0;
+    int nb0 = min(nfetch, kBatchRecs);
+    if (nb0 > 0) issue(f0, nb0);
+
+    load_tables(s_cb, s_sign, tb, c.signs);
+    for (int i = threadIdx.x; i < nselw; i += kThreads) s_selbits[i] = 0u;
+    __syncthreads();
+    float sg[8];
+    load_signs(sg, s_sign);
+    const float* c4 = s_cb;
+    const float* c3 = s_cb + 32;
+
+    // 2. query heads of this KV head: RoPE'd (original frame) and rotated
+    const int pos = checked_pos(__ldg(a.pos + b), tb, a.err);
+    if (hw < R) {
+        const int j = h * R + hw;
+        float x[8];
+        load_f32x8(a.q + ((size_t)b * c.Hq + j) * kDim, x);
+        rope(x, pos, tb);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            s_qr[hw][4 * l + k] = x[k];
+            s_qr[hw][64 + 4 * l + k] = x[4 + k];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= sg[i];
+        fwht(x, m);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            s_qt[hw][4 * l + k] = x[k] * kRsqrtD;
+            s_qt[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
+        }
+    }
+    // selected groups that fall in this split's L2 range are masked
+    for (int i = threadIdx.x; i < c.beta; i += kThreads) {
+        const int g = valid_sel(selrow, i, c.G, a.err);
+        if (g >= g0 && g < g1) atomicOr(&s_selbits[(g - g0) >> 5], 1u << ((g - g0) & 31));
+    }
+    __syncthreads();
+
+    // L2 entries of this split: non-empty and not selected, in group order
+    int nl2 = 0;
+    {
+        const int span = g1 - g0;
+        const int per = (span + kThreads - 1) / kThreads;
+        const int i0 = min(span, (int)threadIdx.x * per), i1 = min(span, i0 + per);
+        int local = 0;
+        for (int i = i0; i < i1; ++i) {
+            const int g = g0 + i;
+            local += (__ldg(c.l2_cnt + (size_t)b * c.G + g) > 0) && !((s_selbits[i >> 5] >> (i & 31)) & 1u);
+        }
+        int o = block_exclusive_scan(local, s_warp, nl2);
+        for (int i = i0; i < i1; ++i) {
+            const int g = g0 + i;
+            if ((__ldg(c.l2_cnt + (size_t)b * c.G + g) > 0) && !((s_selbits[i >> 5] >> (i & 31)) & 1u))
+                s_list[o++] = g;
+        }
+    }
+    __syncthreads();
+
+    Softmax<R> sm;
+    sm.init();
+
+    // 3. L1 and L2 entries: logits in the rotated frame, q~ . (n c[codes])
+    {
+        float qt[R][8];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                qt[j][k] = s_qt[j][4 * l + k];
+                qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
+            }
+        }
+        const int nl1 = e1 - e0;
+        const int ne = nl1 + nl2;
+        for (int e = hw; e < ne; e += kHalves) {
+            float kv[8], vv[8];
+            if (e < nl1) {
+                const size_t so = (size_t)bh * c.max_l1 + e0 + e;
+                const uint16_t* kr = reinterpret_cast<const uint16_t*>(c.l1_kc + so * 64);
+                const uint16_t* vr = reinterpret_cast<const uint16_t*>(c.l1_vc + so * 64);
+                unpack4(__ldg(kr + l), __ldg(kr + 16 + l), c4, __ldg(c.l1_kn + so), kv);
+                unpack4(__ldg(vr + l), __ldg(vr + 16 + l), c4, __ldg(c.l1_vn + so), vv);
+            } else {
+                const size_t go = (size_t)bh * c.G + s_list[e - nl1];
+                unpack3(reinterpret_cast<const uint32_t*>(c.l2_kc + go * 48), c3, __ldg(c.l2_kn + go), kv);
+                unpack3(reinterpret_cast<const uint32_t*>(c.l2_vc + go * 48), c3, __ldg(c.l2_vn + go), vv);
+            }
+            float x[R];
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                float d = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) d = fmaf(qt[j][i], kv[i], d);
+                x[j] = half_sum(d, m) * kLogitScaleLog2;
+            }
+            sm.add(x, vv);
+        }
+    }
+
+    // 4. fetched tokens: recover RoPE(Pi^T n c4[codes], t); logits against the RoPE'd query
+    if (nfetch > 0) {
+        float qr[R][8];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                qr[j][k] = s_qr[j][4 * l + k];
+                qr[j][4 + k] = s_qr[j][64 + 4 * l + k];
+            }
+        }
+        for (int r0 = f0; r0 < f1; r0 += kBatchRecs) {
+            const int nb = min(kBatchRecs, f1 - r0);
+            __syncthreads();  // previous batch fully consumed
+#pragma unroll
+            for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
+                const int ch = threadIdx.x + k * kThreads;
+                if (ch < nb * kRecChunks) reinterpret_cast<uint4*>(s_rec)[ch] = pre[k];
+            }
+            for (int i = threadIdx.x; i < nb; i += kThreads) s_fg[i] = valid_sel(selrow, r0 + i, c.G, a.err);
+            __syncthreads();
+            if (r0 + kBatchRecs < f1) issue(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+            for (int u = hw; u < nb * N; u += kHalves) {
+                const int rec = u / N, n = u - rec * N;
+                const int g = s_fg[rec];
+                const int t = g * N + n;
+                if (g < 0 || t >= c.T || in_l1(c, b, t)) continue;
+                const uint8_t* rp = s_rec + rec * RB;
+                const float* norms = reinterpret_cast<const float*>(rp + N * 128);
+                const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
+                const uint16_t* vr = reinterpret_cast<const uint16_t*>(rp + N * 64 + n * 64);
+                float kv[8], vv[8];
+                unpack4(kr[l], kr[16 + l], c4, 1.0f, kv);
+                fwht(kv, m);
+                const float kn = norms[n] * kRsqrtD;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
+                rope(kv, t, tb);
+                unpack4(vr[l], vr[16 + l], c4, norms[N + n], vv);
+                float x[R];
+#pragma unroll
+                for (int j = 0; j < R; ++j) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d = fmaf(qr[j][i], kv[i], d);
+                    x[j] = half_sum(d, m) * kLogitScaleLog2;
+                }
+                sm.add(x, vv);
+            }
+        }
+    }
+
+    // 5. merge the two halves of each warp, then the warps, into this split's partial
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const float mo = __shfl_xor_sync(0xffffffffu, sm.m[j], 16);
+        const float lo = __shfl_xor_sync(0xffffffffu, sm.l[j], 16);
+        const float M = fmaxf(sm.m[j], mo);
+        const float ws = merge_weight(sm.m[j], M), wo = merge_weight(mo, M);
+        sm.l[j] = sm.l[j] * ws + lo * wo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float ao = __shfl_xor_sync(0xffffffffu, sm.acc[j][i], 16);
+            sm.acc[j][i] = sm.acc[j][i] * ws + ao * wo;
+        }
+        sm.m[j] = M;
+    }
+    __syncthreads();  // s_rec no longer needed: reuse for the warp partials
+    float* s_part = reinterpret_cast<float*>(s_dyn);  // [8 warps][R][132]
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 16) == 0) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            float* p = s_part + ((size_t)warp * R + j) * hsq::kPartStride;
+            *reinterpret_cast<float4*>(p + 4 * l) = make_float4(sm.acc[j][0], sm.acc[j][1], sm.acc[j][2], sm.acc[j][3]);
+            *reinterpret_cast<float4*>(p + 64 + 4 * l) = make_float4(sm.acc[j][4], sm.acc[j][5], sm.acc[j][6], sm.acc[j][7]);
+            if (l == 0) { p[128] = sm.m[j]; p[129] = sm.l[j]; }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < R * 32) {
+        const int j = threadIdx.x >> 5, q4 = threadIdx.x & 31;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, s_part[((size_t)w * R + j) * hsq::kPartStride + 128]);
+        float L = 0.f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const float* p = s_part + ((size_t)w * R + j) * hsq::kPartStride;
+            const float wt = merge_weight(p[128], M);
+            const float4 v = *reinterpret_cast<const float4*>(p + 4 * q4);
+            L += p[129] * wt;
+            A.x += v.x * wt; A.y += v.y * wt; A.z += v.z * wt; A.w += v.w * wt;
+        }
+        float* dst = a.part + (((size_t)bh * S + s) * R + j) * hsq::kPartStride;
+        __stcg(reinterpret_cast<float4*>(dst + 4 * q4), A);
+        if (q4 == 0) { __stcg(dst + 128, M); __stcg(dst + 129, L); }
+    }
+
+    // 6. the last split of this (b, h) merges all splits and writes the output
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(a.counters + bh, 1);
+        s_flag = (ticket == S - 1);
+    }
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    if (hw < R) {
+        const int j = hw;
+        const float* base = a.part + ((size_t)bh * S * R + j) * hsq::kPartStride;
+        float M = -INFINITY;
+        for (int k = 0; k < S; ++k) M = fmaxf(M, __ldcg(base + (size_t)k * R * hsq::kPartStride + 128));
+        float L = 0.f, o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = 0.f;
+        for (int k = 0; k < S; ++k) {
+            const float* p = base + (size_t)k * R * hsq::kPartStride;
+            const float wt = merge_weight(__ldcg(p + 128), M);
+            L += __ldcg(p + 129) * wt;
+            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p + 4 * l));
+            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(p + 64 + 4 * l));
+            o[0] += x0.x * wt; o[1] += x0.y * wt; o[2] += x0.z * wt; o[3] += x0.w * wt;
+            o[4] += x1.x * wt; o[5] += x1.y * wt; o[6] += x1.z * wt; o[7] += x1.w * wt;
+        }
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] *= inv;
+        fwht(o, m);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] *= sg[i] * kRsqrtD;
+        store_f32x8(a.out + ((size_t)b * c.Hq + h * R + j) * kDim, o);
+    }
+    if (threadIdx.x == 0) a.counters[bh] = 0;
+}
+
+}  // namespace
+
+// ===========================================================================
+// Host side: context and entry points.
+// ===========================================================================
+
+struct hsq_ctx {
+    hsq_config cfg;
+    int r = 1, num_sms = 0, device = 0;
+    int G_max = 0, W_max = 0;
+    float* d_cb = nullptr;
+    float* d_rope_hi = nullptr;
+    float* d_rope_lo = nullptr;
+    float* d_scores = nullptr;
+    float* d_part = nullptr;
+    int* d_route_ctr = nullptr;
+    int* d_attn_ctr = nullptr;
+    int* d_prefix = nullptr;
+    int* d_err = nullptr;
+    std::string last_error;
+};
+
+namespace {
+
+hsq_status fail(hsq_ctx* ctx, hsq_status st, const std::string& msg) {
+    if (ctx) ctx->last_error = msg;
+    hsq::set_process_error(msg);
+    return st;
+}
+
+hsq_status cuda_fail(hsq_ctx* ctx, cudaError_t e, const char* where) {
+    return fail(ctx, HSQ_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define HSQ_CUDA(ctx, call)                                   \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+    } while (0)
+
+bool r_supported(int r) { return r == 1 || r == 2 || r == 4 || r == 5 || r == 8; }
+
+CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
+    CacheView v{};
+    v.B = c->B; v.T = c->T; v.N = ctx->cfg.group_n; v.G = hsq::groups_of(c->T, v.N);
+    v.Hkv = ctx->cfg.n_kv_heads; v.Hq = ctx->cfg.n_q_heads; v.beta = ctx->cfg.beta;
+    v.max_l1 = ctx->cfg.max_l1; v.W = hsq::bitmap_words(c->T);
+    v.l1_kc = c->l1_kc; v.l1_vc = c->l1_vc; v.l1_kn = c->l1_kn; v.l1_vn = c->l1_vn;
+    v.l1_pos = c->l1_pos; v.l1_count = c->l1_count;
+    v.l2_kc = c->l2_kc; v.l2_vc = c->l2_vc; v.l2_kn = c->l2_kn; v.l2_vn = c->l2_vn; v.l2_cnt = c->l2_cnt;
+    v.l3 = c->l3; v.l1_bitmap = c->l1_bitmap; v.signs = c->signs; v.staging = c->staging;
+    return v;
+}
+
+Tables make_tables(const hsq_ctx* ctx) {
+    Tables t{};
+    t.cb = ctx->d_cb; t.rope_hi = ctx->d_rope_hi; t.rope_lo = ctx->d_rope_lo; t.max_pos = ctx->cfg.max_pos;
+    return t;
+}
+
+int attn_splits(const hsq_ctx* ctx, int B) {
+    if (ctx->cfg.n_splits > 0) return ctx->cfg.n_splits;
+    const int bh = B * ctx->cfg.n_kv_heads;
+    int S = (2 * ctx->num_sms + bh - 1) / bh;
+    return S < 1 ? 1 : (S > HSQ_MAX_SPLITS ? HSQ_MAX_SPLITS : S);
+}
+
+size_t attn_smem_bytes(int G, int S, int R) {
+    const int span = (G + S - 1) / S;
+    const size_t sel_words = (size_t)(span + 31) / 32 + 1;
+    const size_t list = (size_t)span + 1;
+    const size_t a = kFetchBatchBytes + (sel_words + list) * 4;
+    const size_t b = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
+    return a > b ? a : b;
+}
+
+template <int R, int N>
+void set_attn_smem(size_t bytes) {
+    cudaFuncSetAttribute(attn_kernel<R, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int R>
+void set_route_smem(size_t bytes) {
+    cudaFuncSetAttribute(route_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int R>
+hsq_status launch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cudaStream_t st) {
+    dim3 grid((v.G + kRouteGroupsPerCta - 1) / kRouteGroupsPerCta, v.B * v.Hkv);
+    route_kernel<R><<<grid, kThreads, (size_t)v.G * 4, st>>>(v, a, make_tables(ctx));
+    return HSQ_OK;
+}
+
+template <int R, int N>
+hsq_status launch_attn(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
+    dim3 grid(a.S, v.B * v.Hkv);
+    attn_kernel<R, N><<<grid, kThreads, attn_smem_bytes(v.G, a.S, R), st>>>(v, a, make_tables(ctx));
+    return HSQ_OK;
+}
+
+template <int R>
+hsq_status dispatch_attn_n(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
+    return v.N == 8 ? launch_attn<R, 8>(ctx, v, a, st) : launch_attn<R, 16>(ctx, v, a, st);
+}
+
+hsq_status dispatch_attn(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
+    switch (ctx->r) {
+        case 1: return dispatch_attn_n<1>(ctx, v, a, st);
+        case 2: return dispatch_attn_n<2>(ctx, v, a, st);
+        case 4: return dispatch_attn_n<4>(ctx, v, a, st);
+        case 5: return dispatch_attn_n<5>(ctx, v, a, st);
+        case 8: return dispatch_attn_n<8>(ctx, v, a, st);
+    }
+    return HSQ_ERR_UNSUPPORTED;
+}
+
+hsq_status dispatch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cudaStream_t st) {
+    switch (ctx->r) {
+        case 1: return launch_route<1>(ctx, v, a, st);
+        case 2: return launch_route<2>(ctx, v, a, st);
+        case 4: return launch_route<4>(ctx, v, a, st);
+        case 5: return launch_route<5>(ctx, v, a, st);
+        case 8: return launch_route<8>(ctx, v, a, st);
+    }
+    return HSQ_ERR_UNSUPPORTED;
+}
+
+hsq_status after_launch(hsq_ctx* ctx, const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(ctx, e, what);
+    return HSQ_OK;
+}
+
+hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
+    if (!ctx) return fail(nullptr, HSQ_ERR_INVALID, "context is NULL");
+    std::string why = hsq::check_cache_shape(&ctx->cfg, cache);
+    if (!why.empty()) return fail(ctx, HSQ_ERR_INVALID, why);
+    return HSQ_OK;
+}
+
+void free_ctx(hsq_ctx* c) {
+    cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
+    cudaFree(c->d_part); cudaFree(c->d_route_ctr); cudaFree(c->d_attn_ctr); cudaFree(c->d_prefix);
+    cudaFree(c->d_err);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
+    if (!out) return fail(nullptr, HSQ_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    std::string why = hsq::check_config(cfg);
+    if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
+    if (hsq::fault_mask() & HSQ_FAULT_ALLOC) return fail(nullptr, HSQ_ERR_NOMEM, "injected allocation failure");
+    const int r = cfg->n_q_heads / cfg->n_kv_heads;
+    if (!r_supported(r)) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "r = Hq/Hkv must be 1, 2, 4, 5 or 8");
+
+    hsq_ctx* c = new hsq_ctx();
+    c->cfg = *cfg;
+    c->r = r;
+    auto bail = [&](cudaError_t e, const char* where) {
+        hsq_status st = (e == cudaErrorMemoryAllocation) ? HSQ_ERR_NOMEM : HSQ_ERR_CUDA;
+        std::string msg = std::string(where) + ": " + cudaGetErrorString(e);
+        free_ctx(c);
+        return fail(nullptr, st, msg);
+    };
+    cudaError_t e;
+    if ((e = cudaGetDevice(&c->device)) != cudaSuccess) return bail(e, "cudaGetDevice");
+    if ((e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device)) != cudaSuccess)
+        return bail(e, "cudaDeviceGetAttribute");
+
+    float cb[hsq::kCodebookFloats];
+    hsq::device_codebook(cb);
+    std::vector<float> hi, lo;
+    hsq::rope_tables(cfg->rope_theta, cfg->max_pos, hi, lo);
+    c->G_max = hsq::groups_of(cfg->max_ctx, cfg->group_n);
+    c->W_max = hsq::bitmap_words(cfg->max_ctx);
+    const size_t bh = (size_t)cfg->max_batch * cfg->n_kv_heads;
+
+    if ((e = cudaMalloc(&c->d_cb, sizeof(cb))) != cudaSuccess) return bail(e, "cudaMalloc(codebook)");
+    if ((e = cudaMalloc(&c->d_rope_hi, hi.size() * 4)) != cudaSuccess) return bail(e, "cudaMalloc(rope)");
+    if ((e = cudaMalloc(&c->d_rope_lo, lo.size() * 4)) != cudaSuccess) return bail(e, "cudaMalloc(rope)");
+    if ((e = cudaMalloc(&c->d_scores, bh * c->G_max * 4)) != cudaSuccess) return bail(e, "cudaMalloc(scores)");
+    if ((e = cudaMalloc(&c->d_part, bh * HSQ_MAX_SPLITS * r * hsq::kPartStride * 4)) != cudaSuccess)
+        return bail(e, "cudaMalloc(partials)");
+    if ((e = cudaMalloc(&c->d_route_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
+    if ((e = cudaMalloc(&c->d_attn_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
+    if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
+        return bail(e, "cudaMalloc(prefix)");
+    if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
+    if ((e = cudaMemcpy(c->d_cb, cb, sizeof(cb), cudaMemcpyHostToDevice)) != cudaSuccess) return bail(e, "upload");
+    if ((e = cudaMemcpy(c->d_rope_hi, hi.data(), hi.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return bail(e, "upload");
+    if ((e = cudaMemcpy(c->d_rope_lo, lo.data(), lo.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return bail(e, "upload");
+    if ((e = cudaMemset(c->d_route_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMemset(c->d_attn_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMemset(c->d_err, 0, 4)) != cudaSuccess) return bail(e, "cudaMemset");
+
+    // dynamic shared memory ceilings for the largest G this context can see
+    const size_t route_smem = (size_t)c->G_max * 4;
+    size_t attn_smem = 0;
+    for (int S = 1; S <= HSQ_MAX_SPLITS; ++S) {
+        size_t b2 = attn_smem_bytes(c->G_max, S, r);
+        attn_smem = b2 > attn_smem ? b2 : attn_smem;
+    }
+    switch (r) {
+        case 1: set_route_smem<1>(route_smem); set_attn_smem<1, 8>(attn_smem); set_attn_smem<1, 16>(attn_smem); break;
+        case 2: set_route_smem<2>(route_smem); set_attn_smem<2, 8>(attn_smem); set_attn_smem<2, 16>(attn_smem); break;
+        case 4: set_route_smem<4>(route_smem); set_attn_smem<4, 8>(attn_smem); set_attn_smem<4, 16>(attn_smem); break;
+        case 5: set_route_smem<5>(route_smem); set_attn_smem<5, 8>(attn_smem); set_attn_smem<5, 16>(attn_smem); break;
+        case 8: set_route_smem<8>(route_smem); set_attn_smem<8, 8>(attn_smem); set_attn_smem<8, 16>(attn_smem); break;
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return bail(e, "cudaFuncSetAttribute");
+    *out = c;
+    return HSQ_OK;
+}
+
+hsq_status hsq_destroy(hsq_ctx* ctx) {
+    if (!ctx) return HSQ_OK;
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return HSQ_OK;
+}
+
+hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const void* V,
+                      hsq_dtype dtype, hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!K || !V) return fail(ctx, HSQ_ERR_INVALID, "K or V is NULL");
+    if (dtype != HSQ_DTYPE_F32 && dtype != HSQ_DTYPE_BF16) return fail(ctx, HSQ_ERR_INVALID, "bad dtype");
+    cudaPointerAttributes pa;
+    HSQ_CUDA(ctx, cudaPointerGetAttributes(&pa, cache->l3));
+    const bool on_host = pa.type == cudaMemoryTypeHost;
+    if (on_host != (cache->l3_on_host != 0))
+        return fail(ctx, HSQ_ERR_INVALID, "l3 location does not match l3_on_host");
+    if (on_host && pa.devicePointer != (void*)cache->l3)
+        return fail(ctx, HSQ_ERR_INVALID, "host l3 is not mapped at the same address on the device");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CacheView v = make_view(ctx, cache);
+    l1_index_kernel<<<v.B, 1024, 0, s>>>(v, cache->l1_pos, cache->l1_count, ctx->d_prefix, ctx->d_err);
+    EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
+                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix};
+    dim3 grid(v.G, v.Hkv, v.B);
+    const Tables tb = make_tables(ctx);
+    if (v.N == 16) {
+        if (dtype == HSQ_DTYPE_BF16) encode_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, o, K, V, tb);
+        else encode_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, o, K, V, tb);
+    } else {
+        if (dtype == HSQ_DTYPE_BF16) encode_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, o, K, V, tb);
+        else encode_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, o, K, V, tb);
+    }
+    return after_launch(ctx, "encode");
+}
+
+hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
+                     int32_t* sel, float* scores_opt, hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!q || !pos || !sel) return fail(ctx, HSQ_ERR_INVALID, "q, pos or sel is NULL");
+    CacheView v = make_view(ctx, cache);
+    RouteArgs a{q, pos, sel, scores_opt ? scores_opt : ctx->d_scores, ctx->d_route_ctr, ctx->d_err};
+    st = dispatch_route(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
+    if (st != HSQ_OK) return fail(ctx, st, "unsupported head ratio");
+    return after_launch(ctx, "route");
+}
+
+hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t* sel,
+                             float* k_out_opt, float* v_out_opt, uint8_t* valid_opt, hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!sel) return fail(ctx, HSQ_ERR_INVALID, "sel is NULL");
+    if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
+    CacheView v = make_view(ctx, cache);
+    FetchArgs a{sel, k_out_opt, v_out_opt, valid_opt, cache->staging, ctx->d_err};
+    dim3 grid(v.beta, v.B * v.Hkv);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (v.N == 16) fetch_kernel<16><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
+    else fetch_kernel<8><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
+    return after_launch(ctx, "fetch_dequant");
+}
+
+hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
+                           const int32_t* sel, float* out, int flags, hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!q || !pos || !sel || !out) return fail(ctx, HSQ_ERR_INVALID, "q, pos, sel or out is NULL");
+    if (flags & ~HSQ_ATTN_FROM_STAGING) return fail(ctx, HSQ_ERR_INVALID, "unknown flags");
+    const bool staged = (flags & HSQ_ATTN_FROM_STAGING) != 0;
+    if (staged && !cache->staging) return fail(ctx, HSQ_ERR_INVALID, "staging is NULL");
+    if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
+    CacheView v = make_view(ctx, cache);
+    AttnArgs a{q, pos, sel, out, ctx->d_part, ctx->d_attn_ctr, ctx->d_err, attn_splits(ctx, v.B), staged ? 1 : 0};
+    st = dispatch_attn(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
+    if (st != HSQ_OK) return fail(ctx, st, "unsupported head ratio");
+    return after_launch(ctx, "decode_attn");
+}
+
+hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
+                           int32_t* sel, float* out, hsq_stream_t stream) {
+    hsq_status st = hsq_route(ctx, cache, q, pos, sel, nullptr, stream);
+    if (st != HSQ_OK) return st;
+    return hsq_decode_attn(ctx, cache, q, pos, sel, out, 0, stream);
+}
+
+hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word) {
+    if (!ctx) return fail(nullptr, HSQ_ERR_INVALID, "context is NULL");
+    HSQ_CUDA(ctx, cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    int w = 0;
+    HSQ_CUDA(ctx, cudaMemcpy(&w, ctx->d_err, 4, cudaMemcpyDeviceToHost));
+    HSQ_CUDA(ctx, cudaMemset(ctx->d_err, 0, 4));
+    if (device_word) *device_word = w;
+    if (w) return fail(ctx, HSQ_ERR_DEVICE_CHECK, "device-side check failed (word " + std::to_string(w) + ")");
+    return HSQ_OK;
+}
+
+const char* hsq_last_error(const hsq_ctx* ctx) {
+    return ctx ? ctx->last_error.c_str() : hsq::process_error();
+}
+
+}  // extern "C"

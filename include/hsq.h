@@ -1,0 +1,279 @@
+/*
+ * hsq.h -- C ABI of the HSQ (Hierarchical Semantic Quantization, "Tamarin")
+ * compressed-KV library for GB300 (sm_103a).
+ *
+ * The operations follow the decode process of the Tamarin (HSQ) technical
+ * summary (gist.science rs-10297225), section 2 "Method":
+ *   - three-tier cache: L1 focal tier (GPU, 4-bit), L2 summary tier (GPU,
+ *     3-bit, one key/value pair per group of N in {8, 16}), L3 archive of
+ *     4-bit originals of every compressed token in host RAM;
+ *   - decode: (1) a per-head router scores the L2 summary keys against the
+ *     current query, (2) the top-beta groups' originals are fetched from L3,
+ *     dequantised on the GPU and rotated to their positions, (3) attention
+ *     runs over L1 tokens, L2 summaries and the recovered originals, with the
+ *     summaries of fetched groups masked out.
+ * Quantisation is TurboQuant as described in "Ablation, Statistical
+ * Inference, and Validation for KV-Cache Compression" (gist.science
+ * 2607.09683), experimental setup item 1: a randomised Walsh-Hadamard
+ * rotation, then a data-oblivious Beta Lloyd-Max scalar codebook.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - head_dim d = 128.  Hq query heads, Hkv KV heads, r = Hq / Hkv; query
+ *    head j reads KV head j / r.
+ *  - A stored vector x is (n, codes): n = ||x|| as float32, codes = the
+ *    b-bit indices of Pi (x / n), Pi = H diag(s) / sqrt(d), H the Sylvester
+ *    Hadamard matrix and s the layer's +-1 sign vector.  A code is the number
+ *    of codebook boundaries strictly below the coordinate.  A zero vector is
+ *    n = 0 with every code 2^(b-1) - 1.
+ *  - Codes are packed as a little-endian bit string: code i occupies bits
+ *    [b*i, b*i + b).  A 4-bit vector takes 64 bytes, a 3-bit vector 48.
+ *  - Keys enter pre-RoPE; RoPE is the rotate-half form pairing (i, i + 64)
+ *    with omega_i = theta^(-2i/d).
+ *  - Groups are positional blocks [gN, gN + N) over the whole context,
+ *    G = ceil(T / N).  A group's members are its tokens outside L1; a group
+ *    without members is empty and is never routed.
+ *  - Every pointer in hsq_cache and every array argument is caller-owned.
+ *    The library owns only the context (codebooks, RoPE tables, scratch).
+ *  - Every call is asynchronous on the given stream and returns a status;
+ *    none aborts, asserts or traps.  Argument errors are reported before
+ *    anything is enqueued.  Device-side checks (bad selection indices, a
+ *    position outside the RoPE tables, an L1 set over capacity) set a
+ *    context error word that hsq_sync_status() reports.
+ *  - One context serves one stream at a time: its scratch is shared by the
+ *    calls made with it.
+ */
+#ifndef HSQ_H
+#define HSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t / cudaEvent_t compatible handles (NULL = legacy default stream). */
+typedef struct CUstream_st* hsq_stream_t;
+
+typedef enum {
+    HSQ_OK = 0,
+    HSQ_ERR_INVALID = 1,      /* bad argument or configuration */
+    HSQ_ERR_CUDA = 2,         /* a CUDA runtime call failed (see hsq_last_error) */
+    HSQ_ERR_NOMEM = 3,        /* device allocation failed at hsq_create */
+    HSQ_ERR_TIMEOUT = 4,      /* reserved: a bounded device wait ran out */
+    HSQ_ERR_DEVICE_CHECK = 5, /* a device-side check failed (see hsq_sync_status) */
+    HSQ_ERR_UNSUPPORTED = 6   /* valid but not built (e.g. an r outside {1,2,4,5,8}) */
+} hsq_status;
+
+typedef enum { HSQ_DTYPE_F32 = 0, HSQ_DTYPE_BF16 = 1 } hsq_dtype;
+
+enum { HSQ_HEAD_DIM = 128, HSQ_MAX_BETA = 512, HSQ_MAX_SPLITS = 64 };
+
+/* Bits of the device error word (hsq_sync_status fills *device_word). */
+enum {
+    HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
+    HSQ_DEVERR_POS = 2,       /* position outside [0, max_pos): clamped */
+    HSQ_DEVERR_L1_OVER = 4    /* more L1 tokens than max_l1: extra tokens dropped from L1 */
+};
+
+/* Flags of hsq_decode_attn. */
+enum {
+    HSQ_ATTN_FROM_STAGING = 1 /* read fetched records from cache->staging (filled by
+                                 hsq_fetch_dequant) instead of gathering them from L3 */
+};
+
+/* Host-only fault injection (hsq_debug_set_fault). */
+enum {
+    HSQ_FAULT_ALLOC = 1,      /* hsq_create fails with HSQ_ERR_NOMEM before any CUDA call */
+    HSQ_FAULT_FETCH = 2       /* hsq_fetch_dequant / hsq_decode_attn return HSQ_ERR_CUDA
+                                 without launching */
+};
+
+typedef struct hsq_config {
+    int n_q_heads;      /* Hq >= 1 */
+    int n_kv_heads;     /* Hkv >= 1, Hq % Hkv == 0, r = Hq / Hkv in {1, 2, 4, 5, 8} */
+    int head_dim;       /* must be 128 */
+    int group_n;        /* N: 8 or 16 (group size of the L2 tier) */
+    int beta;           /* groups fetched per KV head per step, 1..HSQ_MAX_BETA */
+    int bits_l1l3;      /* must be 4 (L1 and L3 precision) */
+    int bits_l2;        /* must be 3 (L2 summary precision) */
+    double rope_theta;  /* RoPE base, > 0 */
+    int max_batch;      /* largest B any cache of this context has */
+    int max_ctx;        /* largest T */
+    int max_l1;         /* L1 slots per sequence */
+    int max_pos;        /* exclusive bound on positions (context + decode steps), <= 2^24 */
+    int n_splits;       /* decode-attention splits per (b, KV head); 0 = automatic */
+} hsq_config;
+
+/*
+ * Cache buffers of one layer.  Sizes in bytes come from hsq_cache_sizes(),
+ * in the order of enum hsq_buffer.  All device buffers are plain device
+ * memory; l3 is either device memory or page-locked host memory mapped into
+ * the device address space (cudaHostAlloc / torch pin_memory), read by the
+ * GPU in place (zero copy).
+ */
+typedef struct hsq_cache {
+    int B;                    /* sequences in this cache, 1..max_batch */
+    int T;                    /* tokens per sequence, positions 0..T-1, 1..max_ctx */
+    /* L1 focal tier */
+    uint8_t* l1_kc;           /* [B][Hkv][max_l1][64]  4-bit codes of RoPE(k_t, t) */
+    uint8_t* l1_vc;           /* [B][Hkv][max_l1][64]  4-bit codes of v_t */
+    float* l1_kn;             /* [B][Hkv][max_l1]      key norms */
+    float* l1_vn;             /* [B][Hkv][max_l1]      value norms */
+    int32_t* l1_pos;          /* [B][max_l1]           ascending L1 positions */
+    int32_t* l1_count;        /* [B]                   L1 size per sequence */
+    /* L2 summary tier */
+    uint8_t* l2_kc;           /* [B][Hkv][G][48]  3-bit codes of the members' mean RoPE'd key */
+    uint8_t* l2_vc;           /* [B][Hkv][G][48]  3-bit codes of the members' mean value */
+    float* l2_kn;             /* [B][Hkv][G] */
+    float* l2_vn;             /* [B][Hkv][G] */
+    uint8_t* l2_cnt;          /* [B][G] members per group (0 = empty) */
+    /* L3 archive: group-major records, one per (b, h, g), of N*136 bytes:
+       K codes [N][64] | V codes [N][64] | K norms [N] f32 | V norms [N] f32.
+       Slots past T hold the zero-vector encoding. */
+    uint8_t* l3;
+    int l3_on_host;           /* 1 = page-locked host memory, 0 = device memory */
+    /* L1 membership: bit (t & 31) of word [b][t >> 5]; bits at t >= T are ignored */
+    const uint32_t* l1_bitmap;/* [B][ceil(T/32)] device */
+    const int8_t* signs;      /* [128] device, +-1: the layer's Walsh-Hadamard sign vector */
+    uint8_t* staging;         /* [B][Hkv][beta][N*136] device, or NULL (only needed for the
+                                 staged fetch path) */
+} hsq_cache;
+
+typedef enum {
+    HSQ_BUF_L1_KC = 0, HSQ_BUF_L1_VC, HSQ_BUF_L1_KN, HSQ_BUF_L1_VN, HSQ_BUF_L1_POS,
+    HSQ_BUF_L1_COUNT, HSQ_BUF_L2_KC, HSQ_BUF_L2_VC, HSQ_BUF_L2_KN, HSQ_BUF_L2_VN,
+    HSQ_BUF_L2_CNT, HSQ_BUF_L3, HSQ_BUF_L1_BITMAP, HSQ_BUF_STAGING, HSQ_NBUF
+} hsq_buffer;
+
+typedef struct hsq_ctx hsq_ctx;   /* opaque, library-owned */
+
+/*
+ * hsq_codebook -- the TurboQuant Beta Lloyd-Max codebook (host only, float64).
+ *   Lloyd-Max for the law of one coordinate of a uniform unit vector in R^dim
+ *   (Y^2 ~ Beta(1/2, (dim-1)/2)), iterated to convergence; symmetric, so the
+ *   middle boundary is 0.  ("Ablation, Statistical Inference, and Validation
+ *   for KV-Cache Compression", experimental setup item 1.)
+ *   centroids: [2^bits] ascending; boundaries: [2^bits - 1], midpoints.
+ *   bits in 1..8, dim >= 4.  Needs no GPU.  Errors: HSQ_ERR_INVALID.
+ */
+hsq_status hsq_codebook(int bits, int dim, double* centroids, double* boundaries);
+
+/*
+ * hsq_cache_sizes -- bytes of each buffer of a cache with B sequences of T
+ *   tokens under cfg, indexed by enum hsq_buffer.  Needs no GPU.
+ *   Errors: HSQ_ERR_INVALID (bad cfg, B or T).
+ */
+hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ_NBUF]);
+
+/*
+ * hsq_create -- validate cfg, build both codebooks (float64, rounded to
+ *   float32 for the device) and the RoPE angle tables (float64 angles,
+ *   float32 cos/sin of 256*a*omega and c*omega, combined on the device by
+ *   angle addition), allocate scratch on the current device.
+ *   *out receives the context.  Errors: HSQ_ERR_INVALID, HSQ_ERR_NOMEM,
+ *   HSQ_ERR_CUDA, HSQ_ERR_UNSUPPORTED.
+ */
+hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out);
+
+/* hsq_destroy -- free the context (synchronises its device work). NULL is a no-op. */
+hsq_status hsq_destroy(hsq_ctx* ctx);
+
+/*
+ * hsq_encode -- build the three tiers of one layer from pre-RoPE K and V
+ *   (Tamarin summary, section 2, three-tier architecture; TurboQuant encode).
+ *   K, V: device [B][Hkv][T][128] of dtype (bf16 or f32), positions 0..T-1.
+ *   Reads cache->l1_bitmap and cache->signs; writes every L1, L2 and L3
+ *   buffer:
+ *     L3 record slot t: TQ4(k_t) and TQ4(v_t) for every token;
+ *     L1 slot i (ascending position order): TQ4(RoPE(k_t, t)), TQ4(v_t);
+ *     L2 group g: TQ3(mean of RoPE(k_t, t)), TQ3(mean of v_t) over members,
+ *       count in l2_cnt; an empty group stores the zero vector.
+ *   If l3_on_host, the records are written through the host link.
+ *   Errors: HSQ_ERR_INVALID (null pointer, B/T out of range, L3 location not
+ *   matching l3_on_host), HSQ_ERR_CUDA.  An L1 set larger than max_l1 sets
+ *   HSQ_DEVERR_L1_OVER.
+ */
+hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const void* V,
+                      hsq_dtype dtype, hsq_stream_t stream);
+
+/*
+ * hsq_route -- per-head routing and top-beta group selection (decode
+ *   process, steps 1-2).  For each (b, KV head h):
+ *     s_g = sum over the head's query heads j of RoPE(q_j, pos_b) . k_hat_g
+ *   (k_hat_g the dequantised summary key), computed in the rotated frame as
+ *   n_g * (sum_j Pi RoPE(q_j, pos_b)) . c3[codes_g]; empty groups score -inf.
+ *   sel[b][h][0..beta) = the beta largest scores, ties to the lower group,
+ *   listed in ascending group order, -1 padded when fewer are non-empty.
+ *   q: device [B][Hq][128] f32; pos: device [B] int32 (query positions);
+ *   sel: device [B][Hkv][beta] int32; scores_opt: device [B][Hkv][G] f32 or
+ *   NULL.  Errors: HSQ_ERR_INVALID, HSQ_ERR_CUDA.
+ */
+hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
+                     int32_t* sel, float* scores_opt, hsq_stream_t stream);
+
+/*
+ * hsq_fetch_dequant -- fetch the selected groups' L3 records and recover the
+ *   originals (decode process, step 2).  Copies record (b, h, sel[b][h][i])
+ *   to cache->staging[b][h][i] when staging is not NULL, and optionally
+ *   writes, for token t = g*N + n:
+ *     k_out_opt [B][Hkv][beta][N][128] f32: RoPE(Pi^T n c4[codes], t), original frame;
+ *     v_out_opt [same] f32: Pi^T n c4[codes], original frame;
+ *     valid_opt [B][Hkv][beta][N] u8: 1 unless sel = -1, t >= T or t in L1.
+ *   Slots with sel = -1 or t >= T are written as zeros.  All outputs device.
+ *   Errors: HSQ_ERR_INVALID, HSQ_ERR_CUDA.
+ */
+hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t* sel,
+                             float* k_out_opt, float* v_out_opt, uint8_t* valid_opt,
+                             hsq_stream_t stream);
+
+/*
+ * hsq_decode_attn -- union attention of one decode step (decode process,
+ *   step 3).  For each query head j of KV head h, one softmax with scale
+ *   1/sqrt(128) over
+ *     L1 tokens (key RoPE'd at encode),
+ *     non-empty groups not in sel (one entry each: summary key and value),
+ *     tokens t of the groups in sel that are not in L1 (key RoPE(k_t, t)
+ *     recovered from L3, value v_t),
+ *   split over the entries (flash-decoding) and merged by log-sum-exp.
+ *   out: device [B][Hq][128] f32 in the original frame.  q, pos, sel as in
+ *   hsq_route.  By default the kernel gathers the selected L3 records itself
+ *   (zero-copy when L3 is on the host); with HSQ_ATTN_FROM_STAGING it reads
+ *   cache->staging, which a prior hsq_fetch_dequant filled (order the two
+ *   with the caller's events when they run on different streams).
+ *   Errors: HSQ_ERR_INVALID, HSQ_ERR_CUDA; bad sel entries set HSQ_DEVERR_SEL.
+ */
+hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
+                           const int32_t* pos, const int32_t* sel, float* out, int flags,
+                           hsq_stream_t stream);
+
+/*
+ * hsq_decode_step -- hsq_route followed by hsq_decode_attn (fused gather) on
+ *   one stream: one whole decode step of one layer.  sel is written as by
+ *   hsq_route and then consumed.  Errors as the two calls.
+ */
+hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
+                           const int32_t* pos, int32_t* sel, float* out, hsq_stream_t stream);
+
+/*
+ * hsq_sync_status -- synchronise `stream`, read and clear the device error
+ *   word.  Returns HSQ_ERR_DEVICE_CHECK if any bit was set (the bits go to
+ *   *device_word when it is not NULL), HSQ_ERR_CUDA on a CUDA error.
+ */
+hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word);
+
+/* hsq_last_error -- text of the last error of ctx (or of the process when ctx is NULL). */
+const char* hsq_last_error(const hsq_ctx* ctx);
+
+/* hsq_debug_set_fault -- process-wide host-side fault injection mask (HSQ_FAULT_*). */
+hsq_status hsq_debug_set_fault(unsigned mask);
+
+/* hsq_version -- library version string. */
+const char* hsq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSQ_H */
