@@ -228,7 +228,8 @@ class CacheBuffers:
         dt = {"l1_kn": torch.float32, "l1_vn": torch.float32, "l2_kn": torch.float32,
               "l2_vn": torch.float32, "l1_pos": torch.int32, "l1_count": torch.int32,
               "l1_bitmap": torch.int32}.get(name, torch.uint8)
-        return t.view(dt).view(shapes[name])
+        n = int(np.prod(shapes[name]))
+        return t.view(dt)[:n].view(shapes[name])
 
 
 def l1_bitmap_words(mask: np.ndarray) -> np.ndarray:

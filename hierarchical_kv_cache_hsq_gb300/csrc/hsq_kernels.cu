@@ -1154,14 +1154,32 @@ size_t attn_smem_bytes(int G, int S, int R) {
     return a > b ? a : b;
 }
 
-template <int R, int N>
-void set_attn_smem(size_t bytes) {
-    cudaFuncSetAttribute(attn_kernel<R, N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+// The dynamic shared-memory ceiling is a property of the kernel (per device),
+// shared by every context of the process: only ever raise it.
+std::mutex g_smem_mu;
+std::vector<std::pair<std::pair<const void*, int>, size_t>> g_smem_limits;
+
+cudaError_t raise_smem_limit(const void* fn, int device, size_t bytes) {
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    for (auto& e : g_smem_limits) {
+        if (e.first.first == fn && e.first.second == device) {
+            if (e.second >= bytes) return cudaSuccess;
+            cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (err == cudaSuccess) e.second = bytes;
+            return err;
+        }
+    }
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess) g_smem_limits.push_back({{fn, device}, bytes});
+    return err;
 }
 
 template <int R>
-void set_route_smem(size_t bytes) {
-    cudaFuncSetAttribute(route_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+cudaError_t set_smem_limits(int device, size_t route_bytes, size_t attn_bytes) {
+    cudaError_t e = raise_smem_limit((const void*)route_kernel<R>, device, route_bytes);
+    if (e == cudaSuccess) e = raise_smem_limit((const void*)attn_kernel<R, 8>, device, attn_bytes);
+    if (e == cudaSuccess) e = raise_smem_limit((const void*)attn_kernel<R, 16>, device, attn_bytes);
+    return e;
 }
 
 template <int R>
@@ -1288,13 +1306,13 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
         attn_smem = b2 > attn_smem ? b2 : attn_smem;
     }
     switch (r) {
-        case 1: set_route_smem<1>(route_smem); set_attn_smem<1, 8>(attn_smem); set_attn_smem<1, 16>(attn_smem); break;
-        case 2: set_route_smem<2>(route_smem); set_attn_smem<2, 8>(attn_smem); set_attn_smem<2, 16>(attn_smem); break;
-        case 4: set_route_smem<4>(route_smem); set_attn_smem<4, 8>(attn_smem); set_attn_smem<4, 16>(attn_smem); break;
-        case 5: set_route_smem<5>(route_smem); set_attn_smem<5, 8>(attn_smem); set_attn_smem<5, 16>(attn_smem); break;
-        case 8: set_route_smem<8>(route_smem); set_attn_smem<8, 8>(attn_smem); set_attn_smem<8, 16>(attn_smem); break;
+        case 1: e = set_smem_limits<1>(c->device, route_smem, attn_smem); break;
+        case 2: e = set_smem_limits<2>(c->device, route_smem, attn_smem); break;
+        case 4: e = set_smem_limits<4>(c->device, route_smem, attn_smem); break;
+        case 5: e = set_smem_limits<5>(c->device, route_smem, attn_smem); break;
+        default: e = set_smem_limits<8>(c->device, route_smem, attn_smem); break;
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) return bail(e, "cudaFuncSetAttribute");
+    if (e != cudaSuccess) return bail(e, "cudaFuncSetAttribute");
     *out = c;
     return HSQ_OK;
 }

@@ -60,10 +60,16 @@ def oracle_view(bufs, li: W.LayerInputs, w: W.Workload) -> O.OracleCache:
     return O.cache_from_abi(bufs, li.l1_mask, li.signs, w.N, w.T, w.theta)
 
 
-def code_mismatch(gpu_codes: np.ndarray, ora_codes: np.ndarray, y: np.ndarray, bits: int):
-    """(mismatches outside the near-tie band, near-tie coordinates that differ, near-tie count)."""
+def code_mismatch(gpu_codes: np.ndarray, ora_codes: np.ndarray, y: np.ndarray, bits: int,
+                  norms: Optional[np.ndarray] = None):
+    """(mismatches outside the near-tie band, near-tie coordinates that differ, near-tie count).
+
+    Zero vectors (norm 0, e.g. empty groups) are encoded by definition, not
+    by a boundary decision, so they never count as near-ties."""
     diff = gpu_codes != ora_codes
     tie = O.near_boundary(y, bits)
+    if norms is not None:
+        tie &= (np.asarray(norms) > 0)[..., None]
     return int(np.sum(diff & ~tie)), int(np.sum(diff & tie)), int(np.sum(tie))
 
 

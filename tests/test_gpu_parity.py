@@ -88,11 +88,11 @@ def test_encode_parity(name):
             bad = tie_diff = ties = 0
             for b in range(w.B):
                 n = int(ora.l1_count[b])
-                r = code_mismatch(go.codes[b, :, :n], oo.codes[b, :, :n], oo.y[b, :, :n], bits)
+                r = code_mismatch(go.codes[b, :, :n], oo.codes[b, :, :n], oo.y[b, :, :n], bits, oo.norms[b, :, :n])
                 bad, tie_diff, ties = bad + r[0], tie_diff + r[1], ties + r[2]
                 np.testing.assert_allclose(go.norms[b, :, :n], oo.norms[b, :, :n], rtol=2e-6)
         else:
-            bad, tie_diff, ties = code_mismatch(go.codes, oo.codes, oo.y, bits)
+            bad, tie_diff, ties = code_mismatch(go.codes, oo.codes, oo.y, bits, oo.norms)
             np.testing.assert_allclose(go.norms, oo.norms, rtol=2e-6 if tier.startswith("l3") else 1e-5,
                                        atol=1e-30)
         report[tier] = (tie_diff, ties)
@@ -289,6 +289,27 @@ def test_degenerate_caches(kw):
         o = out.cpu().numpy()
         assert np.all(np.isfinite(o))
         assert np.all(rel_l2(o, ref) <= 1e-3)
+
+
+def test_contexts_of_different_sizes_coexist():
+    # a small context created after a large one (same head ratio) must not
+    # shrink the large one's launch limits
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    big = layer("qwen3_0p6b_4k")
+    small = WL["tiny_1k"].with_(Hq=16, Hkv=8, seed_tag=30)
+    ctx_small = make_ctx(small)
+    cache_small = gpu_encode(ctx_small, small, W.layer_inputs(small))
+    w = big.w
+    q, pos = W.queries(w, steps=1)
+    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    H.hsq_decode_step(big.ctx, big.cache, torch.from_numpy(q[0]).cuda(), torch.from_numpy(pos[0]).cuda(), sel, out)
+    assert H.hsq_sync_status(big.ctx) == 0
+    ref = O.decode_attn(big.gview, q[0], pos[0], sel.cpu().numpy().astype(np.int64))
+    assert np.all(rel_l2(out.cpu().numpy(), ref) <= 1e-3)
+    del cache_small
+    ctx_small.close()
 
 
 def test_invalid_selection_is_flagged_not_faulted():
