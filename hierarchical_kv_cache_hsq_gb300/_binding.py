@@ -74,6 +74,7 @@ _SIGS = {
     "hsq_decode_attn": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
     "hsq_decode_step": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
     "hsq_sync_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
+    "hsq_route_noalloc": (ctypes.c_int, [ctypes.POINTER(hsq_config), ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp]),
     "hsq_last_error": (ctypes.c_char_p, [_vp]),
     "hsq_debug_set_fault": (ctypes.c_int, [ctypes.c_uint]),
     "hsq_version": (ctypes.c_char_p, []),
@@ -312,6 +313,14 @@ def hsq_decode_step(ctx: Context, cache: CacheBuffers, q, pos, sel, out, stream=
     c = cache.struct()
     _check(ctx.lib.hsq_decode_step(ctx.handle, ctypes.byref(c), q.data_ptr(), pos.data_ptr(), sel.data_ptr(),
                                    out.data_ptr(), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_route_noalloc(cfg: hsq_config, cache: CacheBuffers, q, pos, sel, stream=None):
+    """Routing through the entry point that allocates no device memory."""
+    lib = load_library()
+    c = cache.struct()
+    _check(lib.hsq_route_noalloc(ctypes.byref(cfg), ctypes.byref(c), q.data_ptr(), pos.data_ptr(),
+                                 sel.data_ptr(), _stream_handle(stream)))
 
 
 def hsq_sync_status(ctx: Context, stream=None) -> int:

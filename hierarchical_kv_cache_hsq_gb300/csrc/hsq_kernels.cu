@@ -1420,3 +1420,291 @@ const char* hsq_last_error(const hsq_ctx* ctx) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Routing that allocates nothing.
+//
+// Some callers cannot call cudaMalloc: a serving runtime that reserves all
+// device memory for its own pool at start-up and fails any later allocation,
+// or a host that must not let a library call synchronise the device (a
+// cudaMalloc may).  hsq_route_noalloc serves them.  It needs no context: the
+// routing scores and the per-(b, h) tickets live in a fixed-size file-scope
+// device array (every GPU that loads this library holds it until the process
+// exits), the codebook in a small file-scope array filled once per device,
+// and the query's RoPE angles are evaluated in float64 inside the kernel
+// instead of being read from a context's tables.
+// ===========================================================================
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HSQ_NOALLOC_SCRATCH_BYTES];
+static __device__ float g_noalloc_codebook[hsq::kCodebookFloats];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// Query RoPE from float64 angles p * theta^(-2i/d).
+__device__ __forceinline__ void rope_f64(float v[8], int p, double theta) {
+    const int l = hlane();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = 4 * l + k;
+        const double ang = (double)p * pow(theta, -2.0 * i / kDim);
+        double sd, cd;
+        sincos(ang, &sd, &cd);
+        const float c = (float)cd, s = (float)sd;
+        const float lo = v[k], hi = v[4 + k];
+        v[k] = fmaf(lo, c, -hi * s);
+        v[4 + k] = fmaf(hi, c, lo * s);
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, RouteArgs a, double theta) {
+    extern __shared__ uint32_t s_keys[];
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) float s_q[R][kDim];
+    __shared__ int s_hist[256];
+    __shared__ int s_warp[32];
+    __shared__ int s_flag;
+    __shared__ uint32_t s_digit;
+    __shared__ int s_above;
+
+    const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = g_noalloc_codebook[i];
+    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = (float)c.signs[i];
+    __syncthreads();
+    float sg[8];
+    load_signs(sg, s_sign);
+
+    if (hw < R) {
+        const int j = h * R + hw;
+        float x[8];
+        load_f32x8(a.q + ((size_t)b * c.Hq + j) * kDim, x);
+        rope_f64(x, __ldg(a.pos + b), theta);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] *= sg[i];
+        fwht(x, m);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            s_q[hw][4 * l + k] = x[k] * kRsqrtD;
+            s_q[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
+        }
+    }
+    __syncthreads();
+    float gq[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < R; ++jj) {
+            s0 += s_q[jj][4 * l + k];
+            s1 += s_q[jj][64 + 4 * l + k];
+        }
+        gq[k] = s0;
+        gq[4 + k] = s1;
+    }
+
+    const int g_begin = blockIdx.x * kRouteGroupsPerCta;
+    const int g_end = min(c.G, g_begin + kRouteGroupsPerCta);
+    const float* c3 = s_cb + 32;
+    for (int g = g_begin + hw; g < g_end; g += kHalves) {
+        const int cnt = __ldg(c.l2_cnt + (size_t)b * c.G + g);
+        float score = -INFINITY;
+        if (cnt > 0) {
+            const size_t go = (size_t)bh * c.G + g;
+            float v[8];
+            unpack3(reinterpret_cast<const uint32_t*>(c.l2_kc + go * 48), c3, 1.0f, v);
+            float d = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d = fmaf(gq[i], v[i], d);
+            d = half_sum(d, m);
+            score = __ldg(c.l2_kn + go) * d;
+        }
+        if (l == 0) a.scores[(size_t)bh * c.G + g] = score;
+    }
+
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(a.counters + bh, 1);
+        s_flag = (ticket == (int)gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+
+    const int G = c.G, beta = c.beta;
+    int ne_local = 0;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        const uint32_t k = ordered_key(__ldcg(a.scores + (size_t)bh * G + g));
+        s_keys[g] = k;
+        ne_local += (k != 0u);
+    }
+    int ne;
+    block_exclusive_scan(ne_local, s_warp, ne);
+
+    uint32_t kstar = 0u;
+    int need = 0;
+    if (beta < ne) {
+        uint32_t prefix = 0u, pmask = 0u;
+        int remaining = beta;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            s_hist[threadIdx.x] = 0;
+            __syncthreads();
+            for (int g = threadIdx.x; g < G; g += blockDim.x) {
+                const uint32_t k = s_keys[g];
+                if ((k & pmask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1);
+            }
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                const int lane = threadIdx.x;
+                int cnt[8], tot = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) { cnt[i] = s_hist[255 - 8 * lane - i]; tot += cnt[i]; }
+                int inc = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int exc = inc - tot;
+                if (exc < remaining && inc >= remaining) {
+                    int acc = exc;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (acc + cnt[i] >= remaining) {
+                            s_digit = (uint32_t)(255 - 8 * lane - i);
+                            s_above = acc;
+                            break;
+                        }
+                        acc += cnt[i];
+                    }
+                }
+            }
+            __syncthreads();
+            prefix |= s_digit << shift;
+            pmask |= 255u << shift;
+            remaining -= s_above;
+            __syncthreads();
+        }
+        kstar = prefix;
+        need = remaining;
+    }
+
+    const int per = (G + blockDim.x - 1) / blockDim.x;
+    const int i0 = min(G, (int)threadIdx.x * per), i1 = min(G, i0 + per);
+    int eq_local = 0;
+    for (int g = i0; g < i1; ++g) eq_local += (s_keys[g] == kstar && kstar != 0u);
+    int eq_total;
+    const int eq_before = block_exclusive_scan(eq_local, s_warp, eq_total);
+    int sel_local = 0;
+    {
+        int e = eq_before;
+        for (int g = i0; g < i1; ++g) {
+            const uint32_t k = s_keys[g];
+            bool take = k > kstar;
+            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
+            sel_local += take;
+        }
+    }
+    int sel_total;
+    int out = block_exclusive_scan(sel_local, s_warp, sel_total);
+    {
+        int e = eq_before;
+        for (int g = i0; g < i1; ++g) {
+            const uint32_t k = s_keys[g];
+            bool take = k > kstar;
+            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
+            if (take && out < beta) a.sel[(size_t)bh * beta + out++] = g;
+        }
+    }
+    for (int i = sel_total + threadIdx.x; i < beta; i += blockDim.x) a.sel[(size_t)bh * beta + i] = -1;
+    if (threadIdx.x == 0) a.counters[bh] = 0;
+}
+
+// One-time set-up of the current device: the scratch array's device address
+// (a host-side use of the symbol name itself would not be a device address)
+// and the codebook upload.  Synchronous, so it must not run under stream capture.
+hsq_status noalloc_setup(unsigned char** scratch) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoallocMaxDevices) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "device ordinal above 63");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetSymbolAddress(scratch)");
+        float cb[hsq::kCodebookFloats];
+        hsq::device_codebook(cb);
+        e = cudaMemcpyToSymbol(g_noalloc_codebook, cb, sizeof(cb));
+        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemcpyToSymbol(codebook)");
+        g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+    }
+    *scratch = g_noalloc_ptr[dev];
+    return HSQ_OK;
+}
+
+template <int R>
+hsq_status launch_route_noalloc(const CacheView& v, const RouteArgs& a, double theta, cudaStream_t st, int dev) {
+    const size_t smem = (size_t)v.G * 4;
+    if (smem > 48 * 1024) {
+        cudaError_t e = raise_smem_limit((const void*)route_noalloc_kernel<R>, dev, smem);
+        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaFuncSetAttribute");
+    }
+    dim3 grid((v.G + kRouteGroupsPerCta - 1) / kRouteGroupsPerCta, v.B * v.Hkv);
+    route_noalloc_kernel<R><<<grid, kThreads, smem, st>>>(v, a, theta);
+    return HSQ_OK;
+}
+
+}  // namespace
+
+extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* cache, const float* q,
+                                        const int32_t* pos, int32_t* sel, hsq_stream_t stream) {
+    std::string why = hsq::check_config(cfg);
+    if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
+    why = hsq::check_cache_shape(cfg, cache);
+    if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
+    if (!q || !pos || !sel) return fail(nullptr, HSQ_ERR_INVALID, "q, pos or sel is NULL");
+    const int r = cfg->n_q_heads / cfg->n_kv_heads;
+    if (!r_supported(r)) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "r = Hq/Hkv must be 1, 2, 4, 5 or 8");
+    const size_t bh = (size_t)cache->B * cfg->n_kv_heads;
+    const size_t G = (size_t)hsq::groups_of(cache->T, cfg->group_n);
+    const size_t ticket_bytes = (bh * 4 + 255) / 256 * 256;
+    if (ticket_bytes + bh * G * 4 > (size_t)HSQ_NOALLOC_SCRATCH_BYTES)
+        return fail(nullptr, HSQ_ERR_INVALID,
+                    "B * n_kv_heads * ceil(T / group_n) too large for the fixed 4 MiB scratch of hsq_route_noalloc");
+    if (G * 4 > 200 * 1024) return fail(nullptr, HSQ_ERR_INVALID, "ceil(T / group_n) above 51200");
+    unsigned char* scratch = nullptr;
+    hsq_status st = noalloc_setup(&scratch);
+    if (st != HSQ_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the tickets must start at zero on every call (the array keeps the last call's contents)
+    cudaError_t e = cudaMemsetAsync(scratch, 0, ticket_bytes, s);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemsetAsync(tickets)");
+    CacheView v{};
+    v.B = cache->B; v.T = cache->T; v.N = cfg->group_n; v.G = (int)G;
+    v.Hkv = cfg->n_kv_heads; v.Hq = cfg->n_q_heads; v.beta = cfg->beta;
+    v.max_l1 = cfg->max_l1; v.W = hsq::bitmap_words(cache->T);
+    v.l2_kc = cache->l2_kc; v.l2_kn = cache->l2_kn; v.l2_cnt = cache->l2_cnt; v.signs = cache->signs;
+    RouteArgs a{q, pos, sel, reinterpret_cast<float*>(scratch + ticket_bytes),
+                reinterpret_cast<int*>(scratch), nullptr};
+    switch (r) {
+        case 1: st = launch_route_noalloc<1>(v, a, cfg->rope_theta, s, dev); break;
+        case 2: st = launch_route_noalloc<2>(v, a, cfg->rope_theta, s, dev); break;
+        case 4: st = launch_route_noalloc<4>(v, a, cfg->rope_theta, s, dev); break;
+        case 5: st = launch_route_noalloc<5>(v, a, cfg->rope_theta, s, dev); break;
+        default: st = launch_route_noalloc<8>(v, a, cfg->rope_theta, s, dev); break;
+    }
+    if (st != HSQ_OK) return st;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "route_noalloc");
+    return HSQ_OK;
+}

@@ -263,6 +263,34 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  */
 hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word);
 
+/*
+ * hsq_route_noalloc -- hsq_route for callers that cannot allocate device memory.
+ *   The pages have no counterpart: this is an interface of this library only.
+ *   Who needs it: a caller that owns all device memory through its own pool
+ *   and fails any later cudaMalloc, or one that must not let a library call
+ *   synchronise the device (cudaMalloc may).  It takes no context and calls
+ *   no cudaMalloc, cudaFree or other allocating routine.
+ *   Same inputs and output as hsq_route (cfg describes the cache; scores are
+ *   not returned).  The query's RoPE angles are evaluated in float64 inside
+ *   the kernel, so scores agree with hsq_route to fp32 rounding and sel is
+ *   identical except for near-ties of the beta-th score.
+ *   Scratch: a fixed array of HSQ_NOALLOC_SCRATCH_BYTES in device memory,
+ *   defined in the library and held by every GPU that loads it until the
+ *   process exits.  It holds 256-byte-rounded B*Hkv tickets plus the
+ *   B*Hkv*ceil(T/N) float32 scores; larger caches are rejected with
+ *   HSQ_ERR_INVALID before anything is enqueued.  Every call shares that
+ *   array: calls whose kernels overlap on the GPU (other streams, other
+ *   threads) race and must be ordered by the caller.  The tickets are
+ *   cleared (cudaMemsetAsync on `stream`) at the start of each call.
+ *   The first call on a device sets that device up (looks up the array's
+ *   device address and uploads the codebook, synchronously); make that first
+ *   call outside any stream capture.  Errors: HSQ_ERR_INVALID,
+ *   HSQ_ERR_UNSUPPORTED, HSQ_ERR_CUDA (text via hsq_last_error(NULL)).
+ */
+enum { HSQ_NOALLOC_SCRATCH_BYTES = 4 << 20 };
+hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* cache, const float* q,
+                             const int32_t* pos, int32_t* sel, hsq_stream_t stream);
+
 /* hsq_last_error -- text of the last error of ctx (or of the process when ctx is NULL). */
 const char* hsq_last_error(const hsq_ctx* ctx);
 
