@@ -5,8 +5,10 @@ One step = one decode step of one layer: routing + top-beta selection
 (hsq_route) and the union attention with the selected L3 groups gathered
 in-kernel from pinned host memory (hsq_decode_attn).  Steps run strictly in
 order; each step uses a fresh query (the workload's 512 queries, cycled).
-A 256 MiB device buffer is written between timed steps so every step starts
-with a cold L2 (the whole per-step working set would otherwise sit in L2).
+Between timed steps a 256 MiB device buffer is written (evicting L2) and a
+second 256 MiB buffer is read, so every step starts with a cold L2 that holds
+only clean lines -- as after a model's weight reads -- and no write-back of
+the flush drains into the timed step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hsq|reference]
 
@@ -47,6 +49,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     p.add_argument("--n-splits", type=int, default=0)
+    p.add_argument("--quick", action="store_true",
+                   help="only the pinned-L3 decode loop (no variants, no link peak): for profiler captures")
     return p.parse_args()
 
 
@@ -284,6 +288,12 @@ def run_hsq(args, rank, world, local):
     out = torch.empty((w.B, w.Hq, 128), device="cuda")
     out_host = torch.empty((w.B, w.Hq, 128), pin_memory=True)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def cold_l2(i):
+        flush.fill_(i & 255)               # evict: write more than L2 holds
+        torch.sum(clean, dim=0, out=sink)  # refill L2 with clean lines (no write-back left over)
     stream = torch.cuda.current_stream()
     sh = ctypes.c_void_p(stream.cuda_stream)
     structs = {k: c.struct() for k, c in caches.items()}
@@ -297,11 +307,11 @@ def run_hsq(args, rank, world, local):
 
     def loop(cache_key, nsteps, e2e=False, timed=True):
         stc = structs[cache_key]
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsteps)] if timed else None
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nsteps)] if timed else None
         torch.cuda._sleep(20_000_000)   # let the host queue the steps ahead of the GPU
         for i in range(nsteps):
             s = i % w.steps
-            flush.fill_(i & 255)
+            cold_l2(i)
             if timed:
                 ev[i][0].record()
             if e2e:
@@ -310,21 +320,15 @@ def run_hsq(args, rank, world, local):
                 qp, pp = q_in.data_ptr(), p_in.data_ptr()
             else:
                 qp, pp = qd[s].data_ptr(), pd[s].data_ptr()
-            lib.hsq_route(ctx.handle, ctypes.byref(stc), qp, pp, sel.data_ptr(), None, sh)
-            if timed:
-                ev[i][1].record()
-            lib.hsq_decode_attn(ctx.handle, ctypes.byref(stc), qp, pp, sel.data_ptr(), out.data_ptr(), 0, sh)
+            lib.hsq_decode_step(ctx.handle, ctypes.byref(stc), qp, pp, sel.data_ptr(), out.data_ptr(), sh)
             if e2e:
                 out_host.copy_(out, non_blocking=True)
             if timed:
-                ev[i][2].record()
+                ev[i][1].record()
         torch.cuda.synchronize()
         if not timed:
             return None
-        step = [e[0].elapsed_time(e[2]) for e in ev]
-        route = [e[0].elapsed_time(e[1]) for e in ev]
-        attn = [e[1].elapsed_time(e[2]) for e in ev]
-        return {"step_ms": step, "route_ms": route, "attn_ms": attn}
+        return {"step_ms": [e[0].elapsed_time(e[1]) for e in ev]}
 
     def barrier():
         if world > 1:
@@ -343,10 +347,15 @@ def run_hsq(args, rank, world, local):
     clk = clocks.stop()
     assert H.hsq_sync_status(ctx) == 0
 
-    loop("device", args.warmup, timed=False)
-    res_dev = loop("device", args.steps)
-    loop("host", args.warmup, e2e=True, timed=False)
-    res_e2e = loop("host", args.steps, e2e=True)
+    if args.quick:
+        res_dev, res_e2e = res, res
+        lp = {"h2d_gbs": float("nan"), "d2h_gbs": float("nan")}
+    else:
+        loop("device", args.warmup, timed=False)
+        res_dev = loop("device", args.steps)
+        loop("host", args.warmup, e2e=True, timed=False)
+        res_e2e = loop("host", args.steps, e2e=True)
+        lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
 
     tot = sum(res["step_ms"])
@@ -358,15 +367,14 @@ def run_hsq(args, rank, world, local):
     ms_per_step = tot / args.steps
     value = world * args.steps / (tot * 1e-3)
     mean = lambda x: sum(x) / len(x)
-    t_route, t_attn = mean(res["route_ms"]), mean(res["attn_ms"])
     hbm_peak, peak_src = measured_peaks()
-    lp = link_peak(torch)
     link_gbs = lp["h2d_gbs"]
     # whole-step roofline: t* = max(HBM bytes / HBM peak, link bytes / link peak)
     t_star = max(ab["hbm"] / (hbm_peak * 1e9), ab["link"] / (link_gbs * 1e9))
     dev_ms = mean(res_dev["step_ms"])
     t_star_dev = (ab["hbm"] + ab["link"]) / (hbm_peak * 1e9)
-    attn_dev = mean(res_dev["attn_ms"])
+    link_achieved = ab["link"] / (ms_per_step * 1e-3) / 1e9
+    hbm_dev_achieved = (ab["hbm"] + ab["link"]) / (dev_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -374,25 +382,23 @@ def run_hsq(args, rank, world, local):
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta} "
                                f"L1={l1_count} non-empty groups={nonempty}, L3 in pinned host memory",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"{FLUSH_BYTES >> 20} MiB device write between timed steps (cold L2 each step)",
+                   "l2": f"cold and clean at every step: {FLUSH_BYTES >> 20} MiB device write, then a "
+                         f"{FLUSH_BYTES >> 20} MiB read, between timed steps (outside the step events)",
                    "n_splits": args.n_splits or "auto"},
-        "roofline": {"bound": "link", "achieved": ab["link"] / (t_attn * 1e-3) / 1e9, "peak": link_gbs,
-                     "unit": "GB/s", "frac": ab["link"] / (t_attn * 1e-3) / 1e9 / link_gbs, "traffic": None,
-                     "kernel": "attn_kernel (fused L3 gather)", "peak_source": "measured pinned H2D copy in this run",
-                     "bytes_per_launch": ab["link"]},
-        "roofline_hbm_device_l3": {"bound": "hbm", "achieved": (ab["attn_hbm"] + ab["link"]) / (attn_dev * 1e-3) / 1e9,
-                                   "peak": hbm_peak, "unit": "GB/s",
-                                   "frac": (ab["attn_hbm"] + ab["link"]) / (attn_dev * 1e-3) / 1e9 / hbm_peak,
-                                   "traffic": None, "kernel": "attn_kernel, L3 in device memory",
+        "roofline": {"bound": "link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
+                     "frac": link_achieved / link_gbs, "traffic": None,
+                     "kernel": "decode_kernel (whole step: route, select, L3 gather, attention)",
+                     "peak_source": "pinned host-to-device copy measured in this run",
+                     "bytes_per_launch": ab["link"], "hbm_bytes_per_launch": ab["hbm"]},
+        "roofline_hbm_device_l3": {"bound": "hbm", "achieved": hbm_dev_achieved, "peak": hbm_peak,
+                                   "unit": "GB/s", "frac": hbm_dev_achieved / hbm_peak, "traffic": None,
+                                   "kernel": "decode_kernel, L3 in device memory",
                                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
         "step_roofline": {"t_star_us": t_star * 1e6, "t_us": ms_per_step * 1e3, "frac": t_star / (ms_per_step * 1e-3),
                           "hbm_bytes": ab["hbm"], "link_bytes": ab["link"],
-                          "hbm_gbs": ab["hbm"] / (ms_per_step * 1e-3) / 1e9,
-                          "link_gbs": ab["link"] / (ms_per_step * 1e-3) / 1e9},
-        "kernels_us": {"route": t_route * 1e3, "attn": t_attn * 1e3},
+                          "hbm_gbs": ab["hbm"] / (ms_per_step * 1e-3) / 1e9, "link_gbs": link_achieved},
         "device_l3": {"value": 1e3 / dev_ms, "unit": UNIT, "ms_per_step": dev_ms,
-                      "step_roofline_frac": t_star_dev / (dev_ms * 1e-3),
-                      "kernels_us": {"route": mean(res_dev["route_ms"]) * 1e3, "attn": attn_dev * 1e3}},
+                      "step_roofline_frac": t_star_dev / (dev_ms * 1e-3)},
         "e2e": {"value": 1e3 / mean(res_e2e["step_ms"]), "unit": UNIT,
                 "h2d_bytes_per_step": q_in.numel() * 4 + p_in.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 4},
@@ -401,13 +407,13 @@ def run_hsq(args, rank, world, local):
                    "input_gbs_pinned_l3": w.B * w.Hkv * w.T * 2 * 128 * 2 / (enc["host"] * 1e-3) / 1e9,
                    "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
         "link_peak": lp,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,
         "wall_s_timed_loop": wall,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         line["cpu_baseline"] = cpu_oracle_sample(w, li, q, pos, args.cpu_baseline_seconds)
     if world > 1:
         import torch.distributed as dist

@@ -26,7 +26,7 @@ HSQ_ERR_TIMEOUT, HSQ_ERR_DEVICE_CHECK, HSQ_ERR_UNSUPPORTED = 4, 5, 6
 HSQ_DTYPE_F32, HSQ_DTYPE_BF16 = 0, 1
 HSQ_ATTN_FROM_STAGING = 1
 HSQ_FAULT_ALLOC, HSQ_FAULT_FETCH = 1, 2
-HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER = 1, 2, 4
+HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER, HSQ_DEVERR_WAIT = 1, 2, 4, 8
 
 BUFFERS = ["l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc", "l2_kn",
            "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging"]

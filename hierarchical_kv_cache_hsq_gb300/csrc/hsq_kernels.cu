@@ -27,7 +27,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
+#include <type_traits>
 #include <string>
 #include <vector>
 
@@ -106,11 +108,11 @@ __device__ __forceinline__ void fwht(float v[8], unsigned m) {
     const int l = hlane();
 #pragma unroll
     for (int s = 1; s < 16; s <<= 1) {  // index bits 2..5 = lane bits 0..3
-        const bool upper = (l & s) != 0;
+        const float sgn = (l & s) ? -1.f : 1.f;  // upper lane: p - v, lower lane: v + p
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float p = __shfl_xor_sync(m, v[i], s, 16);
-            v[i] = upper ? (p - v[i]) : (v[i] + p);
+            const float p = __shfl_xor_sync(m, v[i], s, 16);
+            v[i] = fmaf(sgn, v[i], p);
         }
     }
 }
@@ -228,6 +230,14 @@ __device__ __forceinline__ void load_bf16x8(const uint16_t* __restrict__ p, floa
     v[2] = __uint_as_float(a.y << 16); v[3] = __uint_as_float(a.y & 0xFFFF0000u);
     v[4] = __uint_as_float(b.x << 16); v[5] = __uint_as_float(b.x & 0xFFFF0000u);
     v[6] = __uint_as_float(b.y << 16); v[7] = __uint_as_float(b.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void load_f32x8_smem(const float* p, float v[8]) {
+    const int l = hlane();
+    const float4 a = *reinterpret_cast<const float4*>(p + 4 * l);
+    const float4 b = *reinterpret_cast<const float4*>(p + 64 + 4 * l);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 __device__ __forceinline__ void store_f32x8(float* __restrict__ p, const float v[8]) {
@@ -468,9 +478,64 @@ __global__ void __launch_bounds__(N * 32) encode_kernel(CacheView c, EncodeOut o
 }
 
 // ---------------------------------------------------------------------------
-// Route: score every group of a (b, h) against the aggregated rotated query,
-// then the last CTA of the (b, h) selects the top beta by radix select.
-// grid = (ceil(G / 128), B * Hkv).
+// Asynchronous global -> shared staging of device-resident inputs.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// bytes: a multiple of 16, both addresses 16-byte aligned
+__device__ __forceinline__ void stage16(void* dst, const void* src, int bytes) {
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    const uint8_t* s = static_cast<const uint8_t*>(src);
+    for (int i = threadIdx.x * 16; i < bytes; i += blockDim.x * 16) cp_async16(d + i, s + i);
+}
+
+__device__ __forceinline__ void stage4(float* dst, const float* src, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) cp_async4(dst + i, src + i);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// signs of the lane's 8 dims straight from global memory
+__device__ __forceinline__ void load_signs_global(float s[8], const int8_t* __restrict__ signs) {
+    const int l = hlane();
+    const char4 a = *reinterpret_cast<const char4*>(signs + 4 * l);
+    const char4 b = *reinterpret_cast<const char4*>(signs + 64 + 4 * l);
+    s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+    s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+}
+
+// 3-bit record held in shared memory
+__device__ __forceinline__ void unpack3_smem(const uint8_t* rec8, const float* c3, float scale, float v[8]) {
+    const uint32_t* rec = reinterpret_cast<const uint32_t*>(rec8);
+    const int l = hlane();
+    const int bit = 12 * l, w = bit >> 5, sh = bit & 31;
+    const int w1 = min(w + 1, 5);
+    const uint32_t fa = __funnelshift_r(rec[w], rec[w1], sh) & 0xFFFu;
+    const uint32_t fb = __funnelshift_r(rec[6 + w], rec[6 + w1], sh) & 0xFFFu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[k] = c3[(fa >> (3 * k)) & 7] * scale;
+        v[4 + k] = c3[(fb >> (3 * k)) & 7] * scale;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Top-beta selection by radix select over order-preserving score keys.
 // ---------------------------------------------------------------------------
 
 struct RouteArgs {
@@ -483,25 +548,232 @@ __device__ __forceinline__ uint32_t ordered_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+constexpr int kSelBins = 2048;          // histogram bins of the bucket select (8 per thread)
+constexpr int kSelMaxGroups = 32768;
+constexpr int kSelCand = 32;            // boundary candidates ranked in one warp
+
+struct __align__(16) SelectSmem {
+    int hist[kSelBins];
+    uint32_t taken[kSelMaxGroups / 32];
+    uint32_t cand_key[kSelCand];
+    int cand_g[kSelCand];
+    uint32_t red[3][8];
+    int warp[32];
+    int bstar, above, bcnt, ncand;
+};
+
+// Top-beta selection by the whole block (256 threads).  s_keys[0..G) are
+// order-preserving keys of the fp32 group scores (0 = empty group, never
+// selected).  The beta largest keys (ties to the lower group) go, in ascending
+// group order and -1 padded, to sel_row (global) and, when s_out is not null,
+// to s_out (shared).
+//
+// Bucket select: the keys still in play, [lo, hi], are histogrammed (first
+// pass: kSelBins equal-width bins of the fp32 score; later passes: power-of-
+// two-wide bins of the key), a blocked scan from the top finds the bin that
+// holds the beta-th key, every key of a higher bin is taken, and the
+// boundary bin's keys are ranked exactly (key, then group index) when there
+// are at most 32 of them; otherwise [lo, hi] shrinks to that bin and the
+// pass repeats.  If all keys left are equal, the lowest groups are taken.
+// Both bin functions are monotone in the key, so a bin is a contiguous key
+// range and the result is exact.
+__device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int32_t* __restrict__ sel_row,
+                                int* s_out, SelectSmem& ss) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+    const unsigned full = 0xffffffffu;
+
+    // count, max and min of the non-empty keys (every thread reduces the per-warp values itself)
+    int ne;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    {
+        int c = 0;
+        uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+        for (int g = tid; g < G; g += nt) {
+            const uint32_t v = s_keys[g];
+            if (v != 0u) { ++c; mx = max(mx, v); mn = min(mn, v); }
+        }
+        c = __reduce_add_sync(full, c);
+        mx = __reduce_max_sync(full, mx);
+        mn = __reduce_min_sync(full, mn);
+        if (lane == 0) { ss.red[0][warp] = (uint32_t)c; ss.red[1][warp] = mx; ss.red[2][warp] = mn; }
+        for (int g = tid; g < (G + 31) / 32; g += nt) ss.taken[g] = 0u;
+        __syncthreads();
+        ne = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            ne += (int)ss.red[0][w];
+            hi = max(hi, ss.red[1][w]);
+            lo = min(lo, ss.red[2][w]);
+        }
+    }
+
+    // mode 0: take every non-empty group; 1: keys > bhi plus the ranked
+    // boundary candidates; 2: keys > kstar plus the first `need` equal to kstar
+    int mode = 0, above = 0, need = 0;
+    uint32_t bhi = 0u, kstar = 0u;
+    if (ne > beta) {
+        const float smin = key_to_float(lo), smax = key_to_float(hi);
+        const float fscale = (float)kSelBins / (smax - smin);
+        const bool float_ok = isfinite(fscale) && smax > smin;
+        for (int level = 0; level < 8; ++level) {
+            if (lo == hi) { mode = 2; kstar = lo; need = beta - above; break; }
+            const bool fl = level == 0 && float_ok;
+            const uint32_t span = hi - lo;
+            const int bits = 32 - __clz(span);
+            const int shift = bits > 11 ? bits - 11 : 0;
+            auto bin_of = [&](uint32_t v) -> int {
+                if (fl) return min(max((int)((key_to_float(v) - smin) * fscale), 0), kSelBins - 1);
+                return (int)((v - lo) >> shift);
+            };
+            for (int i = tid; i < kSelBins; i += nt) ss.hist[i] = 0;
+            __syncthreads();
+            for (int g = tid; g < G; g += nt) {
+                const uint32_t v = s_keys[g];
+                if (v != 0u && v >= lo && v <= hi) atomicAdd(&ss.hist[bin_of(v)], 1);
+            }
+            __syncthreads();
+            // blocked scan from the top: thread t owns bins [B - 8(t+1), B - 8t)
+            const int top = kSelBins - 8 * tid;
+            const int4 h0 = *reinterpret_cast<const int4*>(&ss.hist[top - 8]);
+            const int4 h1 = *reinterpret_cast<const int4*>(&ss.hist[top - 4]);
+            const int hv[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};  // descending bins
+            int local = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) local += hv[i];
+            int tot;
+            int run = above + block_exclusive_scan(local, ss.warp, tot);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (run < beta && run + hv[i] >= beta) { ss.bstar = top - 1 - i; ss.above = run; ss.bcnt = hv[i]; }
+                run += hv[i];
+            }
+            if (tid == 0) ss.ncand = 0;
+            __syncthreads();
+            const int bstar = ss.bstar, bcnt = ss.bcnt;
+            above = ss.above;
+            need = beta - above;
+            // the boundary bin's members: gather (when few) and their exact key range
+            uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+            for (int g = tid; g < G; g += nt) {
+                const uint32_t v = s_keys[g];
+                if (v != 0u && v >= lo && v <= hi && bin_of(v) == bstar) {
+                    bmx = max(bmx, v);
+                    bmn = min(bmn, v);
+                    if (bcnt <= kSelCand) {
+                        const int slot = atomicAdd(&ss.ncand, 1);
+                        ss.cand_key[slot] = v;
+                        ss.cand_g[slot] = g;
+                    }
+                }
+            }
+            bmx = __reduce_max_sync(full, bmx);
+            bmn = __reduce_min_sync(full, bmn);
+            if (lane == 0) { ss.red[1][warp] = bmx; ss.red[2][warp] = bmn; }
+            __syncthreads();
+            uint32_t blo_b = 0xFFFFFFFFu, bhi_b = 0u;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                bhi_b = max(bhi_b, ss.red[1][w]);
+                blo_b = min(blo_b, ss.red[2][w]);
+            }
+            if (bcnt <= kSelCand) {
+                if (warp == 0) {
+                    const uint32_t ck = lane < bcnt ? ss.cand_key[lane] : 0u;
+                    const int cg = lane < bcnt ? ss.cand_g[lane] : -1;
+                    int rank = 0;
+                    for (int j = 0; j < bcnt; ++j) {
+                        const uint32_t kj = __shfl_sync(full, ck, j);
+                        const int gj = __shfl_sync(full, cg, j);
+                        rank += (kj > ck) || (kj == ck && gj < cg);
+                    }
+                    if (lane < bcnt && rank < need) atomicOr(&ss.taken[cg >> 5], 1u << (cg & 31));
+                }
+                mode = 1;
+                bhi = bhi_b;
+                __syncthreads();
+                break;
+            }
+            lo = blo_b;  // crowded boundary bin: continue inside it
+            hi = bhi_b;
+            __syncthreads();
+        }
+    }
+
+    // ordered placement: thread t owns the contiguous groups [per*t, per*t + per)
+    const int per = (G + nt - 1) / nt;
+    const int i0 = min(G, tid * per), i1 = min(G, i0 + per);
+    auto take_of = [&](int g, uint32_t v, int eq_rank) -> bool {
+        if (mode == 0) return v != 0u;
+        if (mode == 1) return v > bhi || (v != 0u && ((ss.taken[g >> 5] >> (g & 31)) & 1u));
+        return v > kstar || (v == kstar && eq_rank < need);
+    };
+    int nsel = 0, neq = 0;
+    for (int g = i0; g < i1; ++g) {
+        const uint32_t v = s_keys[g];
+        if (mode == 2) { nsel += (v > kstar); neq += (v == kstar); }
+        else nsel += take_of(g, v, 0);
+    }
+    int total;
+    const int packed = block_exclusive_scan(nsel | (neq << 16), ss.warp, total);
+    int pos_gt = packed & 0xFFFF, eq_before = packed >> 16;
+    for (int g = i0; g < i1; ++g) {
+        const uint32_t v = s_keys[g];
+        const bool take = take_of(g, v, eq_before);
+        const int pos = mode == 2 ? pos_gt + min(eq_before, need) : pos_gt;
+        if (take && pos < beta) {
+            sel_row[pos] = g;
+            if (s_out) s_out[pos] = g;
+        }
+        if (mode == 2) { pos_gt += (v > kstar); eq_before += (v == kstar); }
+        else pos_gt += take;
+    }
+    const int n_sel = mode == 0 ? ne : beta;
+    for (int i = n_sel + tid; i < beta; i += nt) {
+        sel_row[i] = -1;
+        if (s_out) s_out[i] = -1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Route (standalone call): grid = (ceil(G / 128), B * Hkv).  Each CTA stages
+// its 128 groups' summary keys in shared memory, scores them against the
+// aggregated rotated query, and the last CTA of a (b, h) selects.
+// ---------------------------------------------------------------------------
+
+__host__ __device__ inline unsigned al16(size_t x) { return (unsigned)((x + 15) & ~(size_t)15); }
+
+__host__ __device__ inline unsigned route_smem_bytes(int G) {
+    return al16((size_t)G * 4) + kRouteGroupsPerCta * (48 + 4 + 1);
+}
+
 template <int R>
 __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs a, Tables tb) {
-    extern __shared__ uint32_t s_keys[];
-    __shared__ float s_cb[hsq::kCodebookFloats];
-    __shared__ float s_sign[kDim];
+    extern __shared__ __align__(16) uint8_t s_dyn[];
+    __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
     __shared__ __align__(16) float s_q[R][kDim];
-    __shared__ int s_hist[256];
-    __shared__ int s_warp[32];
+    __shared__ SelectSmem s_ss;
     __shared__ int s_flag;
-    __shared__ uint32_t s_digit;
-    __shared__ int s_above;
 
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
-    const int hw = threadIdx.x >> 4, l = hlane();
+    const int tid = threadIdx.x, hw = tid >> 4, l = hlane();
     const unsigned m = half_mask();
-    load_tables(s_cb, s_sign, tb, c.signs);
-    __syncthreads();
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_dyn);
+    uint8_t* s_codes = s_dyn + al16((size_t)c.G * 4);
+    float* s_kn = reinterpret_cast<float*>(s_codes + kRouteGroupsPerCta * 48);
+    uint8_t* s_cnt = reinterpret_cast<uint8_t*>(s_kn + kRouteGroupsPerCta);
+
+    const int g_begin = blockIdx.x * kRouteGroupsPerCta;
+    const int ng = min(c.G, g_begin + kRouteGroupsPerCta) - g_begin;
+    stage16(s_codes, c.l2_kc + ((size_t)bh * c.G + g_begin) * 48, ng * 48);
+    stage4(s_kn, c.l2_kn + (size_t)bh * c.G + g_begin, ng);
+    if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
+    for (int i = tid; i < ng; i += kThreads) s_cnt[i] = __ldg(c.l2_cnt + (size_t)b * c.G + g_begin + i);
     float sg[8];
-    load_signs(sg, s_sign);
+    load_signs_global(sg, c.signs);
 
     // rotated, RoPE'd query of each query head of this KV head
     if (hw < R) {
@@ -519,6 +791,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
             s_q[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
         }
     }
+    cp_async_wait_all();
     __syncthreads();
     float gq[8];
 #pragma unroll
@@ -532,127 +805,34 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
         gq[k] = s0;
         gq[4 + k] = s1;
     }
-
-    const int g_begin = blockIdx.x * kRouteGroupsPerCta;
-    const int g_end = min(c.G, g_begin + kRouteGroupsPerCta);
     const float* c3 = s_cb + 32;
-    for (int g = g_begin + hw; g < g_end; g += kHalves) {
-        const int cnt = __ldg(c.l2_cnt + (size_t)b * c.G + g);
+    for (int i = hw; i < ng; i += kHalves) {
         float score = -INFINITY;
-        if (cnt > 0) {
-            const size_t go = (size_t)bh * c.G + g;
+        if (s_cnt[i] > 0) {
             float v[8];
-            unpack3(reinterpret_cast<const uint32_t*>(c.l2_kc + go * 48), c3, 1.0f, v);
+            unpack3_smem(s_codes + i * 48, c3, 1.0f, v);
             float d = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) d = fmaf(gq[i], v[i], d);
+            for (int k = 0; k < 8; ++k) d = fmaf(gq[k], v[k], d);
             d = half_sum(d, m);
-            score = __ldg(c.l2_kn + go) * d;
+            score = s_kn[i] * d;
         }
-        if (l == 0) a.scores[(size_t)bh * c.G + g] = score;
+        if (l == 0) a.scores[(size_t)bh * c.G + g_begin + i] = score;
     }
 
-    // last CTA of this (b, h) selects
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         __threadfence();
         const int ticket = atomicAdd(a.counters + bh, 1);
         s_flag = (ticket == (int)gridDim.x - 1);
+        if (s_flag) __threadfence();
     }
     __syncthreads();
     if (!s_flag) return;
-    __threadfence();
-
-    const int G = c.G, beta = c.beta;
-    int ne_local = 0;
-    for (int g = threadIdx.x; g < G; g += blockDim.x) {
-        const uint32_t k = ordered_key(__ldcg(a.scores + (size_t)bh * G + g));
-        s_keys[g] = k;
-        ne_local += (k != 0u);
-    }
-    int ne;
-    block_exclusive_scan(ne_local, s_warp, ne);  // also a barrier for s_keys
-
-    uint32_t kstar = 0u;
-    int need = 0;
-    if (beta < ne) {
-        uint32_t prefix = 0u, pmask = 0u;
-        int remaining = beta;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            s_hist[threadIdx.x] = 0;  // blockDim == 256
-            __syncthreads();
-            for (int g = threadIdx.x; g < G; g += blockDim.x) {
-                const uint32_t k = s_keys[g];
-                if ((k & pmask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1);
-            }
-            __syncthreads();
-            if (threadIdx.x < 32) {
-                // lane L owns digits 255-8L-7 .. 255-8L (descending)
-                const int lane = threadIdx.x;
-                int cnt[8], tot = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) { cnt[i] = s_hist[255 - 8 * lane - i]; tot += cnt[i]; }
-                int inc = tot;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    int y = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += y;
-                }
-                const int exc = inc - tot;  // count in higher digits
-                const bool here = exc < remaining && inc >= remaining;
-                if (here) {
-                    int acc = exc;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (acc + cnt[i] >= remaining) {
-                            s_digit = (uint32_t)(255 - 8 * lane - i);
-                            s_above = acc;
-                            break;
-                        }
-                        acc += cnt[i];
-                    }
-                }
-            }
-            __syncthreads();
-            prefix |= s_digit << shift;
-            pmask |= 255u << shift;
-            remaining -= s_above;
-            __syncthreads();
-        }
-        kstar = prefix;
-        need = remaining;
-    }
-
-    // ascending compaction: key > kstar, or key == kstar among the first `need` in index order
-    const int per = (G + blockDim.x - 1) / blockDim.x;
-    const int i0 = min(G, (int)threadIdx.x * per), i1 = min(G, i0 + per);
-    int eq_local = 0;
-    for (int g = i0; g < i1; ++g) eq_local += (s_keys[g] == kstar && kstar != 0u);
-    int eq_total;
-    int eq_before = block_exclusive_scan(eq_local, s_warp, eq_total);
-    int sel_local = 0;
-    {
-        int e = eq_before;
-        for (int g = i0; g < i1; ++g) {
-            const uint32_t k = s_keys[g];
-            bool take = k > kstar;
-            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
-            sel_local += take;
-        }
-    }
-    int sel_total;
-    int out = block_exclusive_scan(sel_local, s_warp, sel_total);
-    {
-        int e = eq_before;
-        for (int g = i0; g < i1; ++g) {
-            const uint32_t k = s_keys[g];
-            bool take = k > kstar;
-            if (k == kstar && kstar != 0u) { take = e < need; ++e; }
-            if (take && out < beta) a.sel[(size_t)bh * beta + out++] = g;
-        }
-    }
-    for (int i = sel_total + threadIdx.x; i < beta; i += blockDim.x) a.sel[(size_t)bh * beta + i] = -1;
-    if (threadIdx.x == 0) a.counters[bh] = 0;
+    for (int g = tid; g < c.G; g += kThreads) s_keys[g] = ordered_key(__ldcg(a.scores + (size_t)bh * c.G + g));
+    __syncthreads();
+    select_top_beta(s_keys, c.G, c.beta, a.sel + (size_t)bh * c.beta, nullptr, s_ss);
+    if (tid == 0) a.counters[bh] = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -740,16 +920,76 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
 }
 
 // ---------------------------------------------------------------------------
-// Union attention: grid = (S splits, B * Hkv).  Split s owns the L1 slots,
-// L2 groups and selected records of its share; each half-warp keeps an
-// online softmax for the r query heads; the CTA merges its half-warps, and
-// the last CTA of a (b, h) merges the splits and rotates the output back.
+// Decode step: grid = (S splits, B * Hkv), 256 threads.  Split s of (b, h)
+// owns a contiguous share of the L2 groups, of the L1 slots and of the
+// selected records.
+//   1. stage its L2 summary keys/values, its L1 tokens, the codebook and the
+//      small-offset RoPE rows in shared memory (cp.async, one round trip);
+//   2. rotate the query heads;
+//   3. per-head logits of its L2 groups (kept in shared memory) and, with
+//      kRoute, the routing score n_g * (sum_j q~_j) . c3[codes] (same
+//      arithmetic as the standalone route kernel, so the selection agrees);
+//   4. L1 tokens into the online softmax (they never depend on routing);
+//   5. kRoute: the splits of (b, h) meet at a counter; the last one selects
+//      the top beta and releases the others through a generation word
+//      (bounded wait: cooperative launch keeps every CTA resident);
+//      otherwise the caller's selection is validated and read;
+//   6. starts gathering its selected records (register staged, zero-copy
+//      when L3 is host memory) and, while they travel, adds the unselected
+//      non-empty summaries;
+//   7. recovered tokens: 4-bit dequantise, inverse WHT, RoPE at the token's
+//      position (group base angle + small offset), logits against RoPE'd q;
+//   8. CTA merge; the last split of (b, h) merges all splits and rotates the
+//      output back to the original frame.
+// Each half-warp runs its own online softmax over its entries.
 // ---------------------------------------------------------------------------
 
-struct AttnArgs {
-    const float* q; const int32_t* pos; const int32_t* sel; float* out;
-    float* part; int* counters; int* err; int S; int from_staging;
+struct DecodeArgs {
+    const float* q; const int32_t* pos; int32_t* sel; float* out; float* scores;
+    float* part; int* merge_ctr; int* arrive; int* gen; int* err; int S; int from_staging;
 };
+
+struct DecodeLayout {
+    int span, l1span;
+    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, sel, mask, base, rbits, off, rec, keys, total;
+};
+
+template <int R, int N>
+__host__ __device__ inline DecodeLayout decode_layout(int G, int S, int max_l1, int beta, bool route) {
+    DecodeLayout L;
+    L.span = (G + S - 1) / S;
+    L.l1span = (max_l1 + S - 1) / S;
+    constexpr int kBatchRecs = kFetchBatchBytes / (N * 136);
+    size_t o = 0;
+    L.l2k = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+    L.l2v = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+    L.l2kn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+    L.l2vn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+    L.cnt = (unsigned)o; o = al16(o + (size_t)L.span);
+    L.l1k = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+    L.l1v = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+    L.l1kn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+    L.l1vn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+    L.logit = (unsigned)o; o = al16(o + (size_t)L.span * R * 4);
+    L.sel = (unsigned)o; o = al16(o + (size_t)beta * 4);
+    L.mask = (unsigned)o; o = al16(o + (size_t)((L.span + 31) / 32) * 4);
+    L.base = (unsigned)o; o = al16(o + (size_t)kBatchRecs * kDim * 4);
+    L.rbits = (unsigned)o; o = al16(o + (size_t)kBatchRecs * 4);
+    L.off = (unsigned)o; o = al16(o + (size_t)N * kDim * 4);
+    const size_t merge = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
+    L.rec = (unsigned)o; o = al16(o + (kFetchBatchBytes > merge ? (size_t)kFetchBatchBytes : merge));
+    L.keys = (unsigned)o;
+    if (route) o = al16(o + (size_t)G * 4);
+    L.total = (unsigned)o;
+    return L;
+}
+
+// 2^x by the special-function unit (relative error about 2^-22); -inf gives 0
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 template <int R>
 struct Softmax {
@@ -763,39 +1003,43 @@ struct Softmax {
             for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
         }
     }
-    // add one entry with log2-domain logits x[j] and value v
-    __device__ __forceinline__ void add(const float x[R], const float v[8]) {
+    // add up to two entries with log2-domain logits xa[j], xb[j] and values va, vb
+    __device__ __forceinline__ void add2(const float xa[R], const float va[8], bool oka, const float xb[R],
+                                         const float vb[8], bool okb) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            if (x[j] > m[j]) {
-                const float corr = exp2f(m[j] - x[j]);
+            const float a = oka ? xa[j] : -INFINITY, b = okb ? xb[j] : -INFINITY;
+            const float mn = fmaxf(m[j], fmaxf(a, b));
+            if (mn > m[j]) {
+                const float corr = fast_exp2(m[j] - mn);
                 l[j] *= corr;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[j][i] *= corr;
-                m[j] = x[j];
+                m[j] = mn;
             }
-            const float p = exp2f(x[j] - m[j]);
-            l[j] += p;
+            const float pa = oka ? fast_exp2(a - m[j]) : 0.f;
+            const float pb = okb ? fast_exp2(b - m[j]) : 0.f;
+            l[j] += pa + pb;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(p, v[i], acc[j][i]);
+            for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(pa, va[i], fmaf(pb, vb[i], acc[j][i]));
         }
     }
 };
 
 __device__ __forceinline__ float merge_weight(float mi, float M) {
-    return mi == -INFINITY ? 0.f : exp2f(mi - M);
+    return mi == -INFINITY ? 0.f : fast_exp2(mi - M);
 }
 
-template <int R, int N>
-__global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a, Tables tb) {
+constexpr int kSpinLimit = 1 << 21;
+
+template <int R, int N, bool kRoute>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
     extern __shared__ __align__(16) uint8_t s_dyn[];
-    __shared__ float s_cb[hsq::kCodebookFloats];
-    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
     __shared__ __align__(16) float s_qt[R][kDim];
     __shared__ __align__(16) float s_qr[R][kDim];
-    __shared__ int s_warp[32];
-    __shared__ int s_fg[kFetchBatchBytes / (N * 136)];
-    __shared__ int s_flag;
+    __shared__ SelectSmem s_ss;
+    __shared__ int s_flag, s_gen;
 
     constexpr int RB = N * 136;
     constexpr int kBatchRecs = kFetchBatchBytes / RB;
@@ -803,52 +1047,50 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
 
     const int s = blockIdx.x, S = a.S;
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
-    const int hw = threadIdx.x >> 4, l = hlane();
+    const int tid = threadIdx.x, hw = tid >> 4, l = hlane();
     const unsigned m = half_mask();
-    const int32_t* selrow = a.sel + (size_t)bh * c.beta;
+    const DecodeLayout L = decode_layout<R, N>(c.G, S, c.max_l1, c.beta, kRoute);
+    uint8_t* s_l2k = s_dyn + L.l2k;
+    uint8_t* s_l2v = s_dyn + L.l2v;
+    float* s_l2kn = reinterpret_cast<float*>(s_dyn + L.l2kn);
+    float* s_l2vn = reinterpret_cast<float*>(s_dyn + L.l2vn);
+    uint8_t* s_cnt = s_dyn + L.cnt;
+    uint8_t* s_l1k = s_dyn + L.l1k;
+    uint8_t* s_l1v = s_dyn + L.l1v;
+    float* s_l1kn = reinterpret_cast<float*>(s_dyn + L.l1kn);
+    float* s_l1vn = reinterpret_cast<float*>(s_dyn + L.l1vn);
+    float* s_logit = reinterpret_cast<float*>(s_dyn + L.logit);
+    int* s_sel = reinterpret_cast<int*>(s_dyn + L.sel);
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + L.mask);
+    float* s_base = reinterpret_cast<float*>(s_dyn + L.base);
+    uint32_t* s_rbits = reinterpret_cast<uint32_t*>(s_dyn + L.rbits);
+    float* s_off = reinterpret_cast<float*>(s_dyn + L.off);
+    uint8_t* s_rec = s_dyn + L.rec;
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_dyn + L.keys);
 
-    // this split's share of the selected records, L2 groups and L1 slots
-    const int f0 = (int)((long long)c.beta * s / S), f1 = (int)((long long)c.beta * (s + 1) / S);
     const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
+    const int n2 = g1 - g0;
     const int cnt1 = min(__ldg(c.l1_count + b), c.max_l1);
     const int e0 = (int)((long long)cnt1 * s / S), e1 = (int)((long long)cnt1 * (s + 1) / S);
-
-    // dynamic smem: staged records | selected-group bitmap of [g0, g1) | L2 entry list | CTA merge
-    uint8_t* s_rec = s_dyn;
-    uint32_t* s_selbits = reinterpret_cast<uint32_t*>(s_dyn + kFetchBatchBytes);
-    const int nselw = (g1 - g0 + 31) / 32;
-    int* s_list = reinterpret_cast<int*>(s_selbits + ((c.G + S - 1) / S + 31) / 32 + 1);
-
-    // 1. start gathering the first batch of selected records (register staged)
-    uint4 pre[kMaxFetchChunksPerThread];
-    auto issue = [&](int r0, int nrec) {
-#pragma unroll
-        for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
-            const int ch = threadIdx.x + k * kThreads;
-            pre[k] = make_uint4(0, 0, 0, 0);
-            if (ch < nrec * kRecChunks) {
-                const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
-                const int i = r0 + rec;
-                const int g = __ldg(selrow + i);
-                if (g >= 0 && g < c.G) {
-                    const uint8_t* base = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
-                                                         : c.l3 + ((size_t)bh * c.G + g) * RB;
-                    pre[k] = __ldcg(reinterpret_cast<const uint4*>(base) + off);
-                }
-            }
-        }
-    };
+    const int n1 = e1 - e0;
+    const int f0 = (int)((long long)c.beta * s / S), f1 = (int)((long long)c.beta * (s + 1) / S);
     const int nfetch = f1 - f0;
-    int nb0 = min(nfetch, kBatchRecs);
-    if (nb0 > 0) issue(f0, nb0);
 
-    load_tables(s_cb, s_sign, tb, c.signs);
-    for (int i = threadIdx.x; i < nselw; i += kThreads) s_selbits[i] = 0u;
-    __syncthreads();
+    // 1. stage the device-resident inputs of this split
+    stage16(s_l2k, c.l2_kc + ((size_t)bh * c.G + g0) * 48, n2 * 48);
+    stage16(s_l2v, c.l2_vc + ((size_t)bh * c.G + g0) * 48, n2 * 48);
+    stage4(s_l2kn, c.l2_kn + (size_t)bh * c.G + g0, n2);
+    stage4(s_l2vn, c.l2_vn + (size_t)bh * c.G + g0, n2);
+    stage16(s_l1k, c.l1_kc + ((size_t)bh * c.max_l1 + e0) * 64, n1 * 64);
+    stage16(s_l1v, c.l1_vc + ((size_t)bh * c.max_l1 + e0) * 64, n1 * 64);
+    stage4(s_l1kn, c.l1_kn + (size_t)bh * c.max_l1 + e0, n1);
+    stage4(s_l1vn, c.l1_vn + (size_t)bh * c.max_l1 + e0, n1);
+    if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
+    stage16(s_off, tb.rope_lo, N * kDim * 4);  // cos/sin of n * omega, n < N
+    for (int i = tid; i < n2; i += kThreads) s_cnt[i] = __ldg(c.l2_cnt + (size_t)b * c.G + g0 + i);
+    for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
     float sg[8];
-    load_signs(sg, s_sign);
-    const float* c4 = s_cb;
-    const float* c3 = s_cb + 32;
+    load_signs_global(sg, c.signs);
 
     // 2. query heads of this KV head: RoPE'd (original frame) and rotated
     const int pos = checked_pos(__ldg(a.pos + b), tb, a.err);
@@ -871,37 +1113,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
             s_qt[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
         }
     }
-    // selected groups that fall in this split's L2 range are masked
-    for (int i = threadIdx.x; i < c.beta; i += kThreads) {
-        const int g = valid_sel(selrow, i, c.G, a.err);
-        if (g >= g0 && g < g1) atomicOr(&s_selbits[(g - g0) >> 5], 1u << ((g - g0) & 31));
-    }
+    cp_async_wait_all();
     __syncthreads();
 
-    // L2 entries of this split: non-empty and not selected, in group order
-    int nl2 = 0;
-    {
-        const int span = g1 - g0;
-        const int per = (span + kThreads - 1) / kThreads;
-        const int i0 = min(span, (int)threadIdx.x * per), i1 = min(span, i0 + per);
-        int local = 0;
-        for (int i = i0; i < i1; ++i) {
-            const int g = g0 + i;
-            local += (__ldg(c.l2_cnt + (size_t)b * c.G + g) > 0) && !((s_selbits[i >> 5] >> (i & 31)) & 1u);
-        }
-        int o = block_exclusive_scan(local, s_warp, nl2);
-        for (int i = i0; i < i1; ++i) {
-            const int g = g0 + i;
-            if ((__ldg(c.l2_cnt + (size_t)b * c.G + g) > 0) && !((s_selbits[i >> 5] >> (i & 31)) & 1u))
-                s_list[o++] = g;
-        }
-    }
-    __syncthreads();
-
+    const float* c4 = s_cb;
+    const float* c3 = s_cb + 32;
     Softmax<R> sm;
     sm.init();
-
-    // 3. L1 and L2 entries: logits in the rotated frame, q~ . (n c[codes])
     {
         float qt[R][8];
 #pragma unroll
@@ -912,34 +1130,231 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
                 qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
             }
         }
-        const int nl1 = e1 - e0;
-        const int ne = nl1 + nl2;
-        for (int e = hw; e < ne; e += kHalves) {
-            float kv[8], vv[8];
-            if (e < nl1) {
-                const size_t so = (size_t)bh * c.max_l1 + e0 + e;
-                const uint16_t* kr = reinterpret_cast<const uint16_t*>(c.l1_kc + so * 64);
-                const uint16_t* vr = reinterpret_cast<const uint16_t*>(c.l1_vc + so * 64);
-                unpack4(__ldg(kr + l), __ldg(kr + 16 + l), c4, __ldg(c.l1_kn + so), kv);
-                unpack4(__ldg(vr + l), __ldg(vr + 16 + l), c4, __ldg(c.l1_vn + so), vv);
-            } else {
-                const size_t go = (size_t)bh * c.G + s_list[e - nl1];
-                unpack3(reinterpret_cast<const uint32_t*>(c.l2_kc + go * 48), c3, __ldg(c.l2_kn + go), kv);
-                unpack3(reinterpret_cast<const uint32_t*>(c.l2_vc + go * 48), c3, __ldg(c.l2_vn + go), vv);
+        // 3. L2 logits per query head, and the routing score
+        float gq[8];
+        if (kRoute) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < R; ++jj) {
+                    s0 += s_qt[jj][4 * l + k];
+                    s1 += s_qt[jj][64 + 4 * l + k];
+                }
+                gq[k] = s0;
+                gq[4 + k] = s1;
             }
-            float x[R];
+        }
+        // two groups per half-warp per iteration (independent instruction streams)
+        for (int i = hw; i < n2; i += 2 * kHalves) {
+            const int ib = i + kHalves;
+            const bool hb = ib < n2;
+            const int ibs = hb ? ib : i;
+            const bool nea = s_cnt[i] > 0, neb = hb && s_cnt[ibs] > 0;
+            float va[8], vb[8];
+            unpack3_smem(s_l2k + i * 48, c3, 1.0f, va);
+            unpack3_smem(s_l2k + ibs * 48, c3, 1.0f, vb);
+            const float kna = s_l2kn[i], knb = s_l2kn[ibs];
+            if (kRoute) {
+                float da = 0.f, db = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    da = fmaf(gq[k], va[k], da);
+                    db = fmaf(gq[k], vb[k], db);
+                }
+                da = half_sum(da, m);
+                db = half_sum(db, m);
+                if (l == 0) {
+                    a.scores[(size_t)bh * c.G + g0 + i] = nea ? kna * da : -INFINITY;
+                    if (hb) a.scores[(size_t)bh * c.G + g0 + ib] = neb ? knb * db : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                float da = 0.f, db = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    da = fmaf(qt[j][k], va[k], da);
+                    db = fmaf(qt[j][k], vb[k], db);
+                }
+                da = half_sum(da, m);
+                db = half_sum(db, m);
+                if (l == 0) {
+                    if (nea) s_logit[i * R + j] = kna * da * kLogitScaleLog2;
+                    if (neb) s_logit[ib * R + j] = knb * db * kLogitScaleLog2;
+                }
+            }
+        }
+    }
+    // 4. L1 tokens (independent of routing: with kRoute they run while the selection is made)
+    auto l1_tokens = [&]() {
+        float qt[R][8];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                qt[j][k] = s_qt[j][4 * l + k];
+                qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
+            }
+        }
+        auto entry = [&](int e, float x[R], float vv[8]) {
+            const uint16_t* kr = reinterpret_cast<const uint16_t*>(s_l1k + e * 64);
+            const uint16_t* vr = reinterpret_cast<const uint16_t*>(s_l1v + e * 64);
+            float kv[8];
+            unpack4(kr[l], kr[16 + l], c4, s_l1kn[e], kv);
+            unpack4(vr[l], vr[16 + l], c4, s_l1vn[e], vv);
 #pragma unroll
             for (int j = 0; j < R; ++j) {
                 float d = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) d = fmaf(qt[j][i], kv[i], d);
+                for (int k = 0; k < 8; ++k) d = fmaf(qt[j][k], kv[k], d);
                 x[j] = half_sum(d, m) * kLogitScaleLog2;
             }
-            sm.add(x, vv);
+        };
+        for (int e = hw; e < n1; e += 2 * kHalves) {
+            const int eb = e + kHalves;
+            const bool hb = eb < n1;
+            float xa[R], xb[R], va[8], vb[8];
+            entry(e, xa, va);
+            entry(hb ? eb : e, xb, vb);
+            sm.add2(xa, va, true, xb, vb, hb);
         }
+    };
+
+    // 5. the selection of this (b, h)
+    const int32_t* selrow = a.sel + (size_t)bh * c.beta;
+    if (kRoute) {
+        __syncthreads();  // this split's scores are written
+        if (tid == 0) {
+            const int gcur = ld_acquire_gpu(a.gen + bh);
+            __threadfence();
+            const int ticket = atomicAdd(a.arrive + bh, 1);
+            s_gen = gcur;
+            s_flag = (ticket == S - 1);
+            if (s_flag) __threadfence();
+        }
+        __syncthreads();
+        if (s_flag) {
+            // last split to arrive: select for everyone, release them, then do its own L1 tokens
+            for (int g = tid; g < c.G; g += kThreads) s_keys[g] = ordered_key(__ldcg(a.scores + (size_t)bh * c.G + g));
+            __syncthreads();
+            select_top_beta(s_keys, c.G, c.beta, a.sel + (size_t)bh * c.beta, s_sel, s_ss);
+            __syncthreads();
+            if (tid == 0) {
+                a.arrive[bh] = 0;
+                __threadfence();
+                atomicAdd(a.gen + bh, 1);
+            }
+            l1_tokens();
+        } else {
+            l1_tokens();
+            if (tid == 0) {
+                int it = 0;
+                while (ld_acquire_gpu(a.gen + bh) == s_gen) {
+                    if (++it > kSpinLimit) {
+                        atomicOr(a.err, HSQ_DEVERR_WAIT);
+                        break;
+                    }
+                    __nanosleep(32);
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < c.beta; i += kThreads) {
+                const int g = __ldcg(selrow + i);
+                s_sel[i] = (g >= 0 && g < c.G) ? g : -1;
+            }
+        }
+    } else {
+        l1_tokens();
+        for (int i = tid; i < c.beta; i += kThreads) s_sel[i] = valid_sel(selrow, i, c.G, a.err);
+    }
+    __syncthreads();
+
+    // 6. start the gather of the first batch of this split's records
+    uint4 pre[kMaxFetchChunksPerThread];
+    auto issue = [&](int r0, int nrec) {
+#pragma unroll
+        for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
+            const int ch = tid + k * kThreads;
+            pre[k] = make_uint4(0, 0, 0, 0);
+            if (ch < nrec * kRecChunks) {
+                const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
+                const int i = r0 + rec;
+                const int g = s_sel[i];
+                if (g >= 0) {
+                    const uint8_t* base = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
+                                                         : c.l3 + ((size_t)bh * c.G + g) * RB;
+                    pre[k] = __ldcg(reinterpret_cast<const uint4*>(base) + off);
+                }
+            }
+        }
+    };
+    // per record: cos/sin of the group's base angle g*N*omega and its L1 bits.  The device
+    // loads are issued before the host gather so they do not queue behind it.
+    float4 mch, msh, mcl, msl;
+    uint32_t mword = 0u;
+    auto meta_load = [&](int r0, int nrec) {
+        if (hw < nrec) {
+            const int g = s_sel[r0 + hw];
+            if (g >= 0) {
+                const int p0 = g * N;
+                const float* rh = tb.rope_hi + (size_t)(p0 >> 8) * kDim;
+                const float* rl = tb.rope_lo + (size_t)(p0 & 255) * kDim;
+                mch = __ldg(reinterpret_cast<const float4*>(rh + 4 * l));
+                msh = __ldg(reinterpret_cast<const float4*>(rh + 64 + 4 * l));
+                mcl = __ldg(reinterpret_cast<const float4*>(rl + 4 * l));
+                msl = __ldg(reinterpret_cast<const float4*>(rl + 64 + 4 * l));
+                if (l == 0) mword = __ldg(c.l1_bitmap + (size_t)b * c.W + (p0 >> 5));
+            }
+        }
+    };
+    auto meta_store = [&](int r0, int nrec) {
+        if (hw < nrec) {
+            const int g = s_sel[r0 + hw];
+            if (g >= 0) {
+                const int p0 = g * N;
+                float* bp = s_base + hw * kDim;
+                *reinterpret_cast<float4*>(bp + 4 * l) =
+                    make_float4(fmaf(mch.x, mcl.x, -msh.x * msl.x), fmaf(mch.y, mcl.y, -msh.y * msl.y),
+                                fmaf(mch.z, mcl.z, -msh.z * msl.z), fmaf(mch.w, mcl.w, -msh.w * msl.w));
+                *reinterpret_cast<float4*>(bp + 64 + 4 * l) =
+                    make_float4(fmaf(msh.x, mcl.x, mch.x * msl.x), fmaf(msh.y, mcl.y, mch.y * msl.y),
+                                fmaf(msh.z, mcl.z, mch.z * msl.z), fmaf(msh.w, mcl.w, mch.w * msl.w));
+                if (l == 0) s_rbits[hw] = (mword >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
+            }
+        }
+    };
+    const int nb0 = min(nfetch, kBatchRecs);
+    if (nb0 > 0) {
+        meta_load(f0, nb0);
+        issue(f0, nb0);
+        meta_store(f0, nb0);
+    }
+    for (int i = tid; i < c.beta; i += kThreads) {
+        const int g = s_sel[i];
+        if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
+    }
+    __syncthreads();
+
+    // unselected non-empty summaries: one entry each, two per half-warp per iteration
+    for (int i = hw; i < n2; i += 2 * kHalves) {
+        const int ib = i + kHalves;
+        const int ibs = ib < n2 ? ib : i;
+        const bool oka = s_cnt[i] > 0 && !((s_mask[i >> 5] >> (i & 31)) & 1u);
+        const bool okb = ib < n2 && s_cnt[ibs] > 0 && !((s_mask[ibs >> 5] >> (ibs & 31)) & 1u);
+        if (!oka && !okb) continue;
+        float va[8], vb[8], xa[R], xb[R];
+        unpack3_smem(s_l2v + i * 48, c3, s_l2vn[i], va);
+        unpack3_smem(s_l2v + ibs * 48, c3, s_l2vn[ibs], vb);
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            xa[j] = s_logit[i * R + j];
+            xb[j] = s_logit[ibs * R + j];
+        }
+        sm.add2(xa, va, oka, xb, vb, okb);
     }
 
-    // 4. fetched tokens: recover RoPE(Pi^T n c4[codes], t); logits against the RoPE'd query
+    // 7. recovered tokens of the selected groups
     if (nfetch > 0) {
         float qr[R][8];
 #pragma unroll
@@ -952,33 +1367,50 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
         }
         for (int r0 = f0; r0 < f1; r0 += kBatchRecs) {
             const int nb = min(kBatchRecs, f1 - r0);
-            __syncthreads();  // previous batch fully consumed
+            __syncthreads();  // previous batch consumed, this batch's meta written
 #pragma unroll
             for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
-                const int ch = threadIdx.x + k * kThreads;
+                const int ch = tid + k * kThreads;
                 if (ch < nb * kRecChunks) reinterpret_cast<uint4*>(s_rec)[ch] = pre[k];
             }
-            for (int i = threadIdx.x; i < nb; i += kThreads) s_fg[i] = valid_sel(selrow, r0 + i, c.G, a.err);
             __syncthreads();
-            if (r0 + kBatchRecs < f1) issue(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
-            for (int u = hw; u < nb * N; u += kHalves) {
+            const bool more = r0 + kBatchRecs < f1;
+            if (more) issue(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+            // one recovered token: validity, logits against the RoPE'd queries, rotated-frame value
+            auto token = [&](int u, float x[R], float vv[8]) -> bool {
                 const int rec = u / N, n = u - rec * N;
-                const int g = s_fg[rec];
+                const int g = s_sel[r0 + rec];
                 const int t = g * N + n;
-                if (g < 0 || t >= c.T || in_l1(c, b, t)) continue;
+                const bool ok = g >= 0 && t < c.T && !((s_rbits[rec] >> n) & 1u);
                 const uint8_t* rp = s_rec + rec * RB;
                 const float* norms = reinterpret_cast<const float*>(rp + N * 128);
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
                 const uint16_t* vr = reinterpret_cast<const uint16_t*>(rp + N * 64 + n * 64);
-                float kv[8], vv[8];
+                float kv[8];
                 unpack4(kr[l], kr[16 + l], c4, 1.0f, kv);
                 fwht(kv, m);
                 const float kn = norms[n] * kRsqrtD;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
-                rope(kv, t, tb);
+                {   // RoPE at t = g*N + n: base angle (per record) plus offset n*omega
+                    const float* bp = s_base + rec * kDim;
+                    const float* op = s_off + n * kDim;
+                    const float4 cb = *reinterpret_cast<const float4*>(bp + 4 * l);
+                    const float4 sb = *reinterpret_cast<const float4*>(bp + 64 + 4 * l);
+                    const float4 co = *reinterpret_cast<const float4*>(op + 4 * l);
+                    const float4 so = *reinterpret_cast<const float4*>(op + 64 + 4 * l);
+                    const float cbv[4] = {cb.x, cb.y, cb.z, cb.w}, sbv[4] = {sb.x, sb.y, sb.z, sb.w};
+                    const float cov[4] = {co.x, co.y, co.z, co.w}, sov[4] = {so.x, so.y, so.z, so.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float cs = fmaf(cbv[k], cov[k], -sbv[k] * sov[k]);
+                        const float sn = fmaf(sbv[k], cov[k], cbv[k] * sov[k]);
+                        const float lo = kv[k], hi = kv[4 + k];
+                        kv[k] = fmaf(lo, cs, -hi * sn);
+                        kv[4 + k] = fmaf(hi, cs, lo * sn);
+                    }
+                }
                 unpack4(vr[l], vr[16 + l], c4, norms[N + n], vv);
-                float x[R];
 #pragma unroll
                 for (int j = 0; j < R; ++j) {
                     float d = 0.f;
@@ -986,12 +1418,25 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
                     for (int i = 0; i < 8; ++i) d = fmaf(qr[j][i], kv[i], d);
                     x[j] = half_sum(d, m) * kLogitScaleLog2;
                 }
-                sm.add(x, vv);
+                return ok;
+            };
+            for (int u = hw; u < nb * N; u += 2 * kHalves) {
+                const int ub = u + kHalves;
+                const bool hb = ub < nb * N;
+                float xa[R], xb[R], va[8], vb[8];
+                const bool oka = token(u, xa, va);
+                const bool okb = token(hb ? ub : u, xb, vb) && hb;
+                sm.add2(xa, va, oka, xb, vb, okb);
+            }
+            if (more) {
+                __syncthreads();
+                meta_load(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+                meta_store(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
             }
         }
     }
 
-    // 5. merge the two halves of each warp, then the warps, into this split's partial
+    // 8. merge the two halves of each warp, then the warps, into this split's partial
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < R; ++j) {
@@ -1007,10 +1452,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
         }
         sm.m[j] = M;
     }
-    __syncthreads();  // s_rec no longer needed: reuse for the warp partials
-    float* s_part = reinterpret_cast<float*>(s_dyn);  // [8 warps][R][132]
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 16) == 0) {
+    __syncthreads();  // the record staging area becomes the warp-partial area
+    float* s_part = reinterpret_cast<float*>(s_rec);  // [8 warps][R][132]
+    const int warp = tid >> 5;
+    if ((tid & 16) == 0) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
             float* p = s_part + ((size_t)warp * R + j) * hsq::kPartStride;
@@ -1020,62 +1465,74 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(CacheView c, AttnArgs a,
         }
     }
     __syncthreads();
-    if (threadIdx.x < R * 32) {
-        const int j = threadIdx.x >> 5, q4 = threadIdx.x & 31;
+    if (tid < R * 32) {
+        const int j = tid >> 5, q4 = tid & 31;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, s_part[((size_t)w * R + j) * hsq::kPartStride + 128]);
-        float L = 0.f;
+        float Lsum = 0.f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kThreads / 32; ++w) {
             const float* p = s_part + ((size_t)w * R + j) * hsq::kPartStride;
             const float wt = merge_weight(p[128], M);
             const float4 v = *reinterpret_cast<const float4*>(p + 4 * q4);
-            L += p[129] * wt;
+            Lsum += p[129] * wt;
             A.x += v.x * wt; A.y += v.y * wt; A.z += v.z * wt; A.w += v.w * wt;
         }
         float* dst = a.part + (((size_t)bh * S + s) * R + j) * hsq::kPartStride;
         __stcg(reinterpret_cast<float4*>(dst + 4 * q4), A);
-        if (q4 == 0) { __stcg(dst + 128, M); __stcg(dst + 129, L); }
+        if (q4 == 0) { __stcg(dst + 128, M); __stcg(dst + 129, Lsum); }
     }
-
-    // 6. the last split of this (b, h) merges all splits and writes the output
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         __threadfence();
-        const int ticket = atomicAdd(a.counters + bh, 1);
+        const int ticket = atomicAdd(a.merge_ctr + bh, 1);
         s_flag = (ticket == S - 1);
+        if (s_flag) __threadfence();
     }
     __syncthreads();
     if (!s_flag) return;
-    __threadfence();
-    if (hw < R) {
-        const int j = hw;
-        const float* base = a.part + ((size_t)bh * S * R + j) * hsq::kPartStride;
+    // stage every split's partial of this (b, h) in shared memory with one sweep
+    const float* pbase = a.part + (size_t)bh * S * R * hsq::kPartStride;
+    const size_t pbytes = (size_t)S * R * hsq::kPartStride * 4;
+    const bool staged = pbytes <= L.total;
+    float* s_all = reinterpret_cast<float*>(s_dyn);
+    if (staged) {
+        stage16(s_all, pbase, (int)pbytes);
+        cp_async_wait_all();
+        __syncthreads();
+    }
+    float* s_o = s_qr[0];  // [R][128]: merged outputs (the RoPE'd queries are no longer needed)
+    if (tid < R * 32) {
+        const int j = tid >> 5, q4 = tid & 31;
+        const float* base = (staged ? s_all : pbase) + (size_t)j * hsq::kPartStride;
+        auto ld = [&](const float* p) { return staged ? *p : __ldcg(p); };
         float M = -INFINITY;
-        for (int k = 0; k < S; ++k) M = fmaxf(M, __ldcg(base + (size_t)k * R * hsq::kPartStride + 128));
-        float L = 0.f, o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = 0.f;
+        for (int k = 0; k < S; ++k) M = fmaxf(M, ld(base + (size_t)k * R * hsq::kPartStride + 128));
+        float Lsum = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k = 0; k < S; ++k) {
             const float* p = base + (size_t)k * R * hsq::kPartStride;
-            const float wt = merge_weight(__ldcg(p + 128), M);
-            L += __ldcg(p + 129) * wt;
-            const float4 x0 = __ldcg(reinterpret_cast<const float4*>(p + 4 * l));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4*>(p + 64 + 4 * l));
-            o[0] += x0.x * wt; o[1] += x0.y * wt; o[2] += x0.z * wt; o[3] += x0.w * wt;
-            o[4] += x1.x * wt; o[5] += x1.y * wt; o[6] += x1.z * wt; o[7] += x1.w * wt;
+            const float wt = merge_weight(ld(p + 128), M);
+            Lsum += ld(p + 129) * wt;
+            const float4 x = staged ? *reinterpret_cast<const float4*>(p + 4 * q4)
+                                    : __ldcg(reinterpret_cast<const float4*>(p + 4 * q4));
+            o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
         }
-        const float inv = L > 0.f ? 1.0f / L : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] *= inv;
+        const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+        *reinterpret_cast<float4*>(s_o + j * kDim + 4 * q4) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    }
+    __syncthreads();
+    if (hw < R) {
+        float o[8];
+        load_f32x8_smem(s_o + hw * kDim, o);
         fwht(o, m);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] *= sg[i] * kRsqrtD;
-        store_f32x8(a.out + ((size_t)b * c.Hq + h * R + j) * kDim, o);
+        store_f32x8(a.out + ((size_t)b * c.Hq + h * R + hw) * kDim, o);
     }
-    if (threadIdx.x == 0) a.counters[bh] = 0;
+    if (tid == 0) a.merge_ctr[bh] = 0;
 }
 
 }  // namespace
@@ -1094,9 +1551,13 @@ struct hsq_ctx {
     float* d_scores = nullptr;
     float* d_part = nullptr;
     int* d_route_ctr = nullptr;
-    int* d_attn_ctr = nullptr;
+    int* d_attn_ctr = nullptr;   // merge tickets of the decode kernel
+    int* d_arrive = nullptr;     // selection barrier: arrivals per (b, h)
+    int* d_gen = nullptr;        // selection barrier: generation per (b, h)
     int* d_prefix = nullptr;
     int* d_err = nullptr;
+    struct Split { int B, G, route, S; };
+    std::vector<Split> splits;   // chosen split counts per cache shape
     std::string last_error;
 };
 
@@ -1138,22 +1599,6 @@ Tables make_tables(const hsq_ctx* ctx) {
     return t;
 }
 
-int attn_splits(const hsq_ctx* ctx, int B) {
-    if (ctx->cfg.n_splits > 0) return ctx->cfg.n_splits;
-    const int bh = B * ctx->cfg.n_kv_heads;
-    int S = (2 * ctx->num_sms + bh - 1) / bh;
-    return S < 1 ? 1 : (S > HSQ_MAX_SPLITS ? HSQ_MAX_SPLITS : S);
-}
-
-size_t attn_smem_bytes(int G, int S, int R) {
-    const int span = (G + S - 1) / S;
-    const size_t sel_words = (size_t)(span + 31) / 32 + 1;
-    const size_t list = (size_t)span + 1;
-    const size_t a = kFetchBatchBytes + (sel_words + list) * 4;
-    const size_t b = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
-    return a > b ? a : b;
-}
-
 // The dynamic shared-memory ceiling is a property of the kernel (per device),
 // shared by every context of the process: only ever raise it.
 std::mutex g_smem_mu;
@@ -1174,42 +1619,76 @@ cudaError_t raise_smem_limit(const void* fn, int device, size_t bytes) {
     return err;
 }
 
-template <int R>
-cudaError_t set_smem_limits(int device, size_t route_bytes, size_t attn_bytes) {
-    cudaError_t e = raise_smem_limit((const void*)route_kernel<R>, device, route_bytes);
-    if (e == cudaSuccess) e = raise_smem_limit((const void*)attn_kernel<R, 8>, device, attn_bytes);
-    if (e == cudaSuccess) e = raise_smem_limit((const void*)attn_kernel<R, 16>, device, attn_bytes);
-    return e;
+template <int V>
+using IC = std::integral_constant<int, V>;
+
+// Calls f(IC<R>{}, IC<N>{}) for the context's head ratio and group size.
+template <class F>
+hsq_status dispatch_rn(int r, int n, F&& f) {
+    const bool n8 = n == 8;
+    switch (r) {
+        case 1: return n8 ? f(IC<1>{}, IC<8>{}) : f(IC<1>{}, IC<16>{});
+        case 2: return n8 ? f(IC<2>{}, IC<8>{}) : f(IC<2>{}, IC<16>{});
+        case 4: return n8 ? f(IC<4>{}, IC<8>{}) : f(IC<4>{}, IC<16>{});
+        case 5: return n8 ? f(IC<5>{}, IC<8>{}) : f(IC<5>{}, IC<16>{});
+        case 8: return n8 ? f(IC<8>{}, IC<8>{}) : f(IC<8>{}, IC<16>{});
+    }
+    return HSQ_ERR_UNSUPPORTED;
+}
+
+// Split count of the decode kernel for B sequences of G groups: one CTA per SM
+// across the B * Hkv heads.  With the routing barrier (kRoute) the whole grid
+// must be co-resident; 0 means it cannot be.
+template <int R, int N, bool kRoute>
+int fit_splits(hsq_ctx* ctx, int B, int G) {
+    for (const auto& e : ctx->splits)
+        if (e.B == B && e.G == G && e.route == (int)kRoute) return e.S;
+    const int bh = B * ctx->cfg.n_kv_heads;
+    auto fn = decode_kernel<R, N, kRoute>;
+    int S0 = ctx->cfg.n_splits > 0 ? ctx->cfg.n_splits : ctx->num_sms / bh;
+    S0 = std::max(1, std::min(std::min(S0, (int)HSQ_MAX_SPLITS), G));
+    int chosen = kRoute ? 0 : S0;
+    for (int S = S0; S >= 1; --S) {
+        const size_t smem = decode_layout<R, N>(G, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute).total;
+        if (raise_smem_limit((const void*)fn, ctx->device, smem) != cudaSuccess) continue;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, smem) != cudaSuccess) continue;
+        if (!kRoute) { chosen = S; break; }
+        if ((long long)S * bh <= (long long)occ * ctx->num_sms) { chosen = S; break; }
+        if (ctx->cfg.n_splits > 0) break;  // a fixed split count that does not fit: no fused step
+    }
+    cudaGetLastError();
+    ctx->splits.push_back({B, G, (int)kRoute, chosen});
+    return chosen;
+}
+
+template <int R, int N, bool kRoute>
+hsq_status launch_decode(hsq_ctx* ctx, CacheView v, DecodeArgs a, cudaStream_t st) {
+    const DecodeLayout L = decode_layout<R, N>(v.G, a.S, v.max_l1, v.beta, kRoute);
+    auto fn = decode_kernel<R, N, kRoute>;
+    cudaError_t e = raise_smem_limit((const void*)fn, ctx->device, L.total);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
+    dim3 grid(a.S, v.B * v.Hkv);
+    Tables tb = make_tables(ctx);
+    if (kRoute) {
+        void* args[] = {&v, &a, &tb};
+        e = cudaLaunchCooperativeKernel((const void*)fn, grid, dim3(kThreads), args, L.total, st);
+    } else {
+        fn<<<grid, kThreads, L.total, st>>>(v, a, tb);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "decode launch");
+    return HSQ_OK;
 }
 
 template <int R>
 hsq_status launch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cudaStream_t st) {
+    const unsigned smem = route_smem_bytes(v.G);
+    cudaError_t e = raise_smem_limit((const void*)route_kernel<R>, ctx->device, smem);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(route)");
     dim3 grid((v.G + kRouteGroupsPerCta - 1) / kRouteGroupsPerCta, v.B * v.Hkv);
-    route_kernel<R><<<grid, kThreads, (size_t)v.G * 4, st>>>(v, a, make_tables(ctx));
+    route_kernel<R><<<grid, kThreads, smem, st>>>(v, a, make_tables(ctx));
     return HSQ_OK;
-}
-
-template <int R, int N>
-hsq_status launch_attn(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
-    dim3 grid(a.S, v.B * v.Hkv);
-    attn_kernel<R, N><<<grid, kThreads, attn_smem_bytes(v.G, a.S, R), st>>>(v, a, make_tables(ctx));
-    return HSQ_OK;
-}
-
-template <int R>
-hsq_status dispatch_attn_n(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
-    return v.N == 8 ? launch_attn<R, 8>(ctx, v, a, st) : launch_attn<R, 16>(ctx, v, a, st);
-}
-
-hsq_status dispatch_attn(hsq_ctx* ctx, const CacheView& v, const AttnArgs& a, cudaStream_t st) {
-    switch (ctx->r) {
-        case 1: return dispatch_attn_n<1>(ctx, v, a, st);
-        case 2: return dispatch_attn_n<2>(ctx, v, a, st);
-        case 4: return dispatch_attn_n<4>(ctx, v, a, st);
-        case 5: return dispatch_attn_n<5>(ctx, v, a, st);
-        case 8: return dispatch_attn_n<8>(ctx, v, a, st);
-    }
-    return HSQ_ERR_UNSUPPORTED;
 }
 
 hsq_status dispatch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cudaStream_t st) {
@@ -1239,6 +1718,7 @@ hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
 void free_ctx(hsq_ctx* c) {
     cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
     cudaFree(c->d_part); cudaFree(c->d_route_ctr); cudaFree(c->d_attn_ctr); cudaFree(c->d_prefix);
+    cudaFree(c->d_arrive); cudaFree(c->d_gen);
     cudaFree(c->d_err);
     delete c;
 }
@@ -1286,6 +1766,8 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
         return bail(e, "cudaMalloc(partials)");
     if ((e = cudaMalloc(&c->d_route_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
     if ((e = cudaMalloc(&c->d_attn_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
+    if ((e = cudaMalloc(&c->d_arrive, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
+    if ((e = cudaMalloc(&c->d_gen, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
     if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(prefix)");
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
@@ -1296,23 +1778,10 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
         return bail(e, "upload");
     if ((e = cudaMemset(c->d_route_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMemset(c->d_attn_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMemset(c->d_arrive, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
+    if ((e = cudaMemset(c->d_gen, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMemset(c->d_err, 0, 4)) != cudaSuccess) return bail(e, "cudaMemset");
 
-    // dynamic shared memory ceilings for the largest G this context can see
-    const size_t route_smem = (size_t)c->G_max * 4;
-    size_t attn_smem = 0;
-    for (int S = 1; S <= HSQ_MAX_SPLITS; ++S) {
-        size_t b2 = attn_smem_bytes(c->G_max, S, r);
-        attn_smem = b2 > attn_smem ? b2 : attn_smem;
-    }
-    switch (r) {
-        case 1: e = set_smem_limits<1>(c->device, route_smem, attn_smem); break;
-        case 2: e = set_smem_limits<2>(c->device, route_smem, attn_smem); break;
-        case 4: e = set_smem_limits<4>(c->device, route_smem, attn_smem); break;
-        case 5: e = set_smem_limits<5>(c->device, route_smem, attn_smem); break;
-        default: e = set_smem_limits<8>(c->device, route_smem, attn_smem); break;
-    }
-    if (e != cudaSuccess) return bail(e, "cudaFuncSetAttribute");
     *out = c;
     return HSQ_OK;
 }
@@ -1390,16 +1859,36 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     const bool staged = (flags & HSQ_ATTN_FROM_STAGING) != 0;
     if (staged && !cache->staging) return fail(ctx, HSQ_ERR_INVALID, "staging is NULL");
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
-    CacheView v = make_view(ctx, cache);
-    AttnArgs a{q, pos, sel, out, ctx->d_part, ctx->d_attn_ctr, ctx->d_err, attn_splits(ctx, v.B), staged ? 1 : 0};
-    st = dispatch_attn(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
-    if (st != HSQ_OK) return fail(ctx, st, "unsupported head ratio");
-    return after_launch(ctx, "decode_attn");
+    const CacheView v = make_view(ctx, cache);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return dispatch_rn(ctx->r, v.N, [&](auto Ri, auto Ni) -> hsq_status {
+        constexpr int R = decltype(Ri)::value, N = decltype(Ni)::value;
+        DecodeArgs a{q, pos, const_cast<int32_t*>(sel), out, nullptr, ctx->d_part, ctx->d_attn_ctr,
+                     ctx->d_arrive, ctx->d_gen, ctx->d_err, fit_splits<R, N, false>(ctx, v.B, v.G), staged ? 1 : 0};
+        return launch_decode<R, N, false>(ctx, v, a, s);
+    });
 }
 
 hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
                            int32_t* sel, float* out, hsq_stream_t stream) {
-    hsq_status st = hsq_route(ctx, cache, q, pos, sel, nullptr, stream);
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!q || !pos || !sel || !out) return fail(ctx, HSQ_ERR_INVALID, "q, pos, sel or out is NULL");
+    if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
+    const CacheView v = make_view(ctx, cache);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool fused = false;
+    st = dispatch_rn(ctx->r, v.N, [&](auto Ri, auto Ni) -> hsq_status {
+        constexpr int R = decltype(Ri)::value, N = decltype(Ni)::value;
+        const int S = fit_splits<R, N, true>(ctx, v.B, v.G);
+        if (S == 0) return HSQ_OK;  // the grid cannot be co-resident: two kernels below
+        fused = true;
+        DecodeArgs a{q, pos, sel, out, ctx->d_scores, ctx->d_part, ctx->d_attn_ctr, ctx->d_arrive, ctx->d_gen,
+                     ctx->d_err, S, 0};
+        return launch_decode<R, N, true>(ctx, v, a, s);
+    });
+    if (st != HSQ_OK || fused) return st;
+    st = hsq_route(ctx, cache, q, pos, sel, nullptr, stream);
     if (st != HSQ_OK) return st;
     return hsq_decode_attn(ctx, cache, q, pos, sel, out, 0, stream);
 }

@@ -74,7 +74,9 @@ enum { HSQ_HEAD_DIM = 128, HSQ_MAX_BETA = 512, HSQ_MAX_SPLITS = 64 };
 enum {
     HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
     HSQ_DEVERR_POS = 2,       /* position outside [0, max_pos): clamped */
-    HSQ_DEVERR_L1_OVER = 4    /* more L1 tokens than max_l1: extra tokens dropped from L1 */
+    HSQ_DEVERR_L1_OVER = 4,   /* more L1 tokens than max_l1: extra tokens dropped from L1 */
+    HSQ_DEVERR_WAIT = 8       /* the decode step's wait for its selection ran out (bounded):
+                                 that step's output is not valid */
 };
 
 /* Flags of hsq_decode_attn. */
@@ -249,9 +251,14 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
                            hsq_stream_t stream);
 
 /*
- * hsq_decode_step -- hsq_route followed by hsq_decode_attn (fused gather) on
- *   one stream: one whole decode step of one layer.  sel is written as by
- *   hsq_route and then consumed.  Errors as the two calls.
+ * hsq_decode_step -- one whole decode step of one layer: routing, top-beta
+ *   selection, gather of the selected L3 records and the union attention.
+ *   sel is written exactly as hsq_route writes it (same scores, same
+ *   selection) and out as hsq_decode_attn computes it.  When the B*Hkv*S
+ *   split grid fits on the GPU at once this is a single cooperative kernel
+ *   (the splits of a (b, h) meet at a bounded device-side wait for their
+ *   selection); otherwise it runs hsq_route then hsq_decode_attn.
+ *   Errors as the two calls; a wait that runs out sets HSQ_DEVERR_WAIT.
  */
 hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
                            const int32_t* pos, int32_t* sel, float* out, hsq_stream_t stream);

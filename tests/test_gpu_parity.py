@@ -183,6 +183,15 @@ def test_decode_attn_parity(name):
         out = torch.empty((w.B, w.Hq, 128), device="cuda")
         H.hsq_decode_step(L.ctx, L.cache, qd, pd, sel, out)
         assert H.hsq_sync_status(L.ctx) == 0
+        # the fused step selects exactly what the routing call selects ...
+        sel_r = torch.empty_like(sel)
+        H.hsq_route(L.ctx, L.cache, qd, pd, sel_r)
+        # ... and attends exactly like the attention call given that selection
+        out_a = torch.empty_like(out)
+        H.hsq_decode_attn(L.ctx, L.cache, qd, pd, sel_r, out_a)
+        assert H.hsq_sync_status(L.ctx) == 0
+        assert torch.equal(sel, sel_r)
+        assert np.all(rel_l2(out.cpu().numpy(), out_a.cpu().numpy()) <= 1e-5)
         gsel = sel.cpu().numpy().astype(np.int64)
         ref = O.decode_attn(L.gview, q[s], pos[s], gsel)          # conditional: GPU cache + GPU sel
         err = rel_l2(out.cpu().numpy(), ref)
