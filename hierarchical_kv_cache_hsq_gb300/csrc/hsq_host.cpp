@@ -172,7 +172,7 @@ std::string check_config(const hsq_config* c) {
     if (c->max_pos < c->max_ctx || c->max_pos > (1 << 24)) return "max_pos must be in [max_ctx, 2^24]";
     if ((long long)c->max_ctx > (1LL << 24)) return "max_ctx too large";
     if ((c->max_ctx + c->group_n - 1) / c->group_n > 32768) return "more than 32768 groups per sequence";
-    if (c->n_splits < 0 || c->n_splits > HSQ_MAX_SPLITS) return "n_splits must be in [0, 64]";
+    if (c->n_splits < 0 || c->n_splits > HSQ_MAX_SPLITS) return "n_splits must be in [0, 16]";
     return "";
 }
 

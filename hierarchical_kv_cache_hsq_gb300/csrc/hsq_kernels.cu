@@ -22,6 +22,7 @@
 // All arithmetic is fp32.  Softmax runs in the log2 domain (logits scaled by
 // log2(e)/sqrt(128), exp2).
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -504,12 +505,6 @@ __device__ __forceinline__ void stage4(float* dst, const float* src, int n) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) cp_async4(dst + i, src + i);
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // signs of the lane's 8 dims straight from global memory
 __device__ __forceinline__ void load_signs_global(float s[8], const int8_t* __restrict__ signs) {
     const int l = hlane();
@@ -920,66 +915,93 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
 }
 
 // ---------------------------------------------------------------------------
-// Decode step: grid = (S splits, B * Hkv), 256 threads.  Split s of (b, h)
-// owns a contiguous share of the L2 groups, of the L1 slots and of the
-// selected records.
-//   1. stage its L2 summary keys/values, its L1 tokens, the codebook and the
-//      small-offset RoPE rows in shared memory (cp.async, one round trip);
-//   2. rotate the query heads;
-//   3. per-head logits of its L2 groups (kept in shared memory) and, with
-//      kRoute, the routing score n_g * (sum_j q~_j) . c3[codes] (same
-//      arithmetic as the standalone route kernel, so the selection agrees);
-//   4. L1 tokens into the online softmax (they never depend on routing);
-//   5. kRoute: the splits of (b, h) meet at a counter; the last one selects
-//      the top beta and releases the others through a generation word
-//      (bounded wait: cooperative launch keeps every CTA resident);
-//      otherwise the caller's selection is validated and read;
-//   6. starts gathering its selected records (register staged, zero-copy
-//      when L3 is host memory) and, while they travel, adds the unselected
-//      non-empty summaries;
-//   7. recovered tokens: 4-bit dequantise, inverse WHT, RoPE at the token's
-//      position (group base angle + small offset), logits against RoPE'd q;
-//   8. CTA merge; the last split of (b, h) merges all splits and rotates the
-//      output back to the original frame.
+// Decode step: one thread-block cluster per (b, KV head).  grid = (S, B*Hkv),
+// cluster = (S, 1, 1), 256 threads per CTA.  Split s owns a contiguous share
+// of the L2 groups and of the L1 slots of its (b, h) and an even share of the
+// selected records.  The splits of a (b, h) exchange what they must through
+// distributed shared memory and cluster barriers; nothing goes through
+// global scratch.
+//   1. stage the split's L2 summaries, L1 tokens, the sequence's L1 bitmap,
+//      the codebook and the RoPE angle rows it may need (cp.async);
+//   2. rotate the query heads; per-head logits of the split's L2 groups and,
+//      with kRoute, the routing score n_g * (sum_j q~_j) . c3[codes] (the
+//      arithmetic of the routing kernel, so both select the same groups);
+//   3. kRoute: distributed top-beta over the splits' scores (cluster_select);
+//      otherwise the caller's selection is validated and used;
+//   4. gather this split's share of the selected L3 records (zero copy when
+//      L3 is host memory) and, while they travel, add the L1 tokens and the
+//      unselected non-empty summaries;
+//   5. recovered tokens: dequantise, inverse WHT, RoPE at the token's
+//      position (per-record base angle plus a small offset), logits against
+//      the RoPE'd queries, values kept in the rotated frame;
+//   6. the CTA's softmax partial per query head is published; query head j is
+//      merged by split j mod S, rotated back to the original frame, stored.
 // Each half-warp runs its own online softmax over its entries.
+//
+// Inputs that do not fit in shared memory (very long contexts) are read in
+// place from global memory instead of being staged (the flags below).
 // ---------------------------------------------------------------------------
 
+constexpr int kMaxSplits = 16;   // largest (non-portable) cluster
+enum : int { kStageL2 = 1, kKeepLogits = 2, kStageL1 = 4, kStageBitmap = 8 };
+
 struct DecodeArgs {
-    const float* q; const int32_t* pos; int32_t* sel; float* out; float* scores;
-    float* part; int* merge_ctr; int* arrive; int* gen; int* err; int S; int from_staging;
+    const float* q; const int32_t* pos; int32_t* sel; float* out; int* err; int from_staging; int flags;
 };
 
 struct DecodeLayout {
-    int span, l1span;
-    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, sel, mask, base, rbits, off, rec, keys, total;
+    int span, l1span, nlev, nb0;
+    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, keys, sel, mask, bitmap;
+    unsigned lev, b0, off, base, rbits, rec, total;
 };
 
+// 4-bit digits of p >> 8 for cache positions p < T
+__host__ __device__ inline int rope_levels(int T) {
+    int hi = (T - 1) >> 8, n = 0;
+    while (hi > 0) {
+        ++n;
+        hi >>= 4;
+    }
+    return n;
+}
+
 template <int R, int N>
-__host__ __device__ inline DecodeLayout decode_layout(int G, int S, int max_l1, int beta, bool route) {
+__host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int max_l1, int beta, bool route,
+                                                      int flags) {
     DecodeLayout L;
     L.span = (G + S - 1) / S;
     L.l1span = (max_l1 + S - 1) / S;
+    L.nlev = rope_levels(T);
+    L.nb0 = 256 / N;
     constexpr int kBatchRecs = kFetchBatchBytes / (N * 136);
+    const size_t row = (size_t)kDim * 4;
     size_t o = 0;
-    L.l2k = (unsigned)o; o = al16(o + (size_t)L.span * 48);
-    L.l2v = (unsigned)o; o = al16(o + (size_t)L.span * 48);
-    L.l2kn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
-    L.l2vn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
-    L.cnt = (unsigned)o; o = al16(o + (size_t)L.span);
-    L.l1k = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
-    L.l1v = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
-    L.l1kn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
-    L.l1vn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
-    L.logit = (unsigned)o; o = al16(o + (size_t)L.span * R * 4);
+    L.l2k = L.l2v = L.l2kn = L.l2vn = L.cnt = L.l1k = L.l1v = L.l1kn = L.l1vn = L.logit = L.keys = L.bitmap = 0;
+    if (flags & kStageL2) {
+        L.l2k = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+        L.l2v = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+        L.l2kn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+        L.l2vn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+        L.cnt = (unsigned)o; o = al16(o + (size_t)L.span);
+    }
+    if (flags & kStageL1) {
+        L.l1k = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+        L.l1v = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+        L.l1kn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+        L.l1vn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+    }
+    if (flags & kKeepLogits) { L.logit = (unsigned)o; o = al16(o + (size_t)L.span * R * 4); }
+    if (route) { L.keys = (unsigned)o; o = al16(o + (size_t)L.span * 4); }
+    if (flags & kStageBitmap) { L.bitmap = (unsigned)o; o = al16(o + (size_t)((T + 31) / 32) * 4); }
     L.sel = (unsigned)o; o = al16(o + (size_t)beta * 4);
     L.mask = (unsigned)o; o = al16(o + (size_t)((L.span + 31) / 32) * 4);
-    L.base = (unsigned)o; o = al16(o + (size_t)kBatchRecs * kDim * 4);
+    L.lev = (unsigned)o; o = al16(o + (size_t)L.nlev * 16 * row);
+    L.b0 = (unsigned)o; o = al16(o + (size_t)L.nb0 * row);
+    L.off = (unsigned)o; o = al16(o + (size_t)N * row);
+    L.base = (unsigned)o; o = al16(o + (size_t)kBatchRecs * row);
     L.rbits = (unsigned)o; o = al16(o + (size_t)kBatchRecs * 4);
-    L.off = (unsigned)o; o = al16(o + (size_t)N * kDim * 4);
     const size_t merge = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
     L.rec = (unsigned)o; o = al16(o + (kFetchBatchBytes > merge ? (size_t)kFetchBatchBytes : merge));
-    L.keys = (unsigned)o;
-    if (route) o = al16(o + (size_t)G * 4);
     L.total = (unsigned)o;
     return L;
 }
@@ -1030,43 +1052,372 @@ __device__ __forceinline__ float merge_weight(float mi, float M) {
     return mi == -INFINITY ? 0.f : fast_exp2(mi - M);
 }
 
-constexpr int kSpinLimit = 1 << 21;
+// (c1, s1) <- cos/sin of the sum of the two angles, 4 frequencies
+__device__ __forceinline__ void angle_add4(float4& c1, float4& s1, const float4 c2, const float4 s2) {
+    const float4 c = make_float4(fmaf(c1.x, c2.x, -s1.x * s2.x), fmaf(c1.y, c2.y, -s1.y * s2.y),
+                                 fmaf(c1.z, c2.z, -s1.z * s2.z), fmaf(c1.w, c2.w, -s1.w * s2.w));
+    const float4 s = make_float4(fmaf(s1.x, c2.x, c1.x * s2.x), fmaf(s1.y, c2.y, c1.y * s2.y),
+                                 fmaf(s1.z, c2.z, c1.z * s2.z), fmaf(s1.w, c2.w, c1.w * s2.w));
+    c1 = c;
+    s1 = s;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Distributed top-beta.  What a split publishes to the others of its cluster,
+// and its private scratch.
+// ---------------------------------------------------------------------------
+
+struct __align__(16) SelPub {
+    int ne, n_cand, n_eq, n_mine;
+    uint32_t kmin, kmax, bmin, bmax;
+    int hist_coarse[kSelBins / 32];
+    int hist[kSelBins];
+    uint32_t cand_key[kSelCand];
+    int cand_g[kSelCand];
+    int mine[HSQ_MAX_BETA];
+};
+
+struct SelLocal {
+    uint32_t red[3][kThreads / 32];
+    int warp[32];
+    int g[8];
+    int off[kMaxSplits + 1];
+};
+
+// Every split holds the keys of its own groups [g0, g0 + n) in s_keys (order-
+// preserving keys of the fp32 routing scores, 0 = empty group).  On return,
+// in every split, s_sel[0..beta) holds the groups of the beta largest keys
+// over the whole cluster (ties to the lower group) in ascending order, -1
+// padded, and bit i of s_mark is set iff group g0 + i is selected.  The
+// result equals select_top_beta over all keys: the same bins at every level
+// (float-linear over the score range first, then power-of-two key bins inside
+// the boundary bin), with the histograms summed over the splits.  Every split
+// computes the same boundary from the same totals, so all of them take the
+// same branches and meet at every cluster barrier.
+__device__ void cluster_select(const uint32_t* s_keys, int n, int g0, int beta, int* s_sel, uint32_t* s_mark,
+                               SelPub& pub, SelLocal& sl) {
+    namespace cgx = cooperative_groups;
+    cgx::cluster_group cluster = cgx::this_cluster();
+    const int S = (int)cluster.num_blocks(), s = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned full = 0xffffffffu;
+    // contiguous groups of this thread, for ordered passes
+    const int per = (n + kThreads - 1) / kThreads;
+    const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+
+    // count, max and min of the non-empty keys of the cluster
+    {
+        int c = 0;
+        uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+        for (int i = tid; i < n; i += kThreads) {
+            const uint32_t v = s_keys[i];
+            if (v != 0u) { ++c; mx = max(mx, v); mn = min(mn, v); }
+        }
+        c = __reduce_add_sync(full, c);
+        mx = __reduce_max_sync(full, mx);
+        mn = __reduce_min_sync(full, mn);
+        if (lane == 0) { sl.red[0][warp] = (uint32_t)c; sl.red[1][warp] = mx; sl.red[2][warp] = mn; }
+        __syncthreads();
+        if (tid == 0) {
+            int t = 0;
+            uint32_t hx = 0u, lx = 0xFFFFFFFFu;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                t += (int)sl.red[0][w];
+                hx = max(hx, sl.red[1][w]);
+                lx = min(lx, sl.red[2][w]);
+            }
+            pub.ne = t; pub.kmax = hx; pub.kmin = lx;
+        }
+    }
+    cluster.sync();
+    if (warp == 0) {
+        int t = 0;
+        uint32_t hx = 0u, lx = 0xFFFFFFFFu;
+        if (lane < S) {
+            const SelPub* rp = cluster.map_shared_rank(&pub, lane);
+            t = rp->ne; hx = rp->kmax; lx = rp->kmin;
+        }
+        t = __reduce_add_sync(full, t);
+        hx = __reduce_max_sync(full, hx);
+        lx = __reduce_min_sync(full, lx);
+        if (lane == 0) { sl.g[0] = t; sl.g[1] = (int)hx; sl.g[2] = (int)lx; }
+    }
+    __syncthreads();
+    const int NE = sl.g[0];
+    uint32_t hi = (uint32_t)sl.g[1], lo = (uint32_t)sl.g[2];
+
+    auto mark = [&](int i) { atomicOr(&s_mark[i >> 5], 1u << (i & 31)); };
+
+    // mode 0: every non-empty group; 1: boundary bin ranked exactly; 2: all keys left equal
+    int mode = 0, above = 0, need = 0;
+    uint32_t kstar = 0u;
+    if (NE > beta) {
+        const float smin = key_to_float(lo), smax = key_to_float(hi);
+        const float fscale = (float)kSelBins / (smax - smin);
+        const bool float_ok = isfinite(fscale) && smax > smin;
+        for (int level = 0; level < 8; ++level) {
+            if (lo == hi) { mode = 2; kstar = lo; need = beta - above; break; }
+            const bool fl = level == 0 && float_ok;
+            const int bits = 32 - __clz(hi - lo);
+            const int shift = bits > 11 ? bits - 11 : 0;
+            auto bin_of = [&](uint32_t v) -> int {
+                if (fl) return min(max((int)((key_to_float(v) - smin) * fscale), 0), kSelBins - 1);
+                return (int)((v - lo) >> shift);
+            };
+            for (int i = tid; i < kSelBins; i += kThreads) pub.hist[i] = 0;
+            if (tid < kSelBins / 32) pub.hist_coarse[tid] = 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t v = s_keys[i];
+                if (v != 0u && v >= lo && v <= hi) {
+                    const int bn = bin_of(v);
+                    atomicAdd(&pub.hist[bn], 1);
+                    atomicAdd(&pub.hist_coarse[bn >> 5], 1);
+                }
+            }
+            cluster.sync();  // every split's histogram is complete
+            if (warp == 0) {
+                // coarse bins (32 fine bins each), two per lane, descending, summed over the splits
+                int ca = 0, cb = 0;
+#pragma unroll
+                for (int r = 0; r < kMaxSplits; ++r) {
+                    if (r < S) {
+                        const SelPub* rp = cluster.map_shared_rank(&pub, r);
+                        ca += rp->hist_coarse[63 - 2 * lane];
+                        cb += rp->hist_coarse[62 - 2 * lane];
+                    }
+                }
+                int incl = ca + cb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(full, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int need_here = beta - above;
+                const unsigned hit = __ballot_sync(full, incl >= need_here);
+                const int f = __ffs(hit) - 1;
+                const int ex_f = __shfl_sync(full, incl - ca - cb, f), ca_f = __shfl_sync(full, ca, f);
+                const bool upper = ex_f + ca_f >= need_here;
+                const int cbin = upper ? 63 - 2 * f : 62 - 2 * f;
+                const int above_c = upper ? ex_f : ex_f + ca_f;
+                // the 32 fine bins of that coarse bin, descending by lane
+                const int fb = cbin * 32 + 31 - lane;
+                int hcnt = 0;
+#pragma unroll
+                for (int r = 0; r < kMaxSplits; ++r)
+                    if (r < S) hcnt += cluster.map_shared_rank(&pub, r)->hist[fb];
+                int fin = hcnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(full, fin, o);
+                    if (lane >= o) fin += y;
+                }
+                const unsigned fhit = __ballot_sync(full, above_c + fin >= need_here);
+                const int ff = __ffs(fhit) - 1;
+                const int fin_f = __shfl_sync(full, fin, ff), h_f = __shfl_sync(full, hcnt, ff);
+                if (lane == 0) {
+                    sl.g[3] = cbin * 32 + 31 - ff;
+                    sl.g[4] = above + above_c + fin_f - h_f;
+                    sl.g[5] = h_f;
+                }
+            }
+            __syncthreads();
+            const int bstar = sl.g[3], above_new = sl.g[4], bcnt = sl.g[5];
+            if (bcnt <= kSelCand) {
+                mode = 1;
+                above = above_new;
+                need = beta - above;
+                // keys above the range or in a higher bin are taken; the boundary bin's keys are candidates
+                int nc = 0;
+                for (int i = i0; i < i1; ++i) {
+                    const uint32_t v = s_keys[i];
+                    nc += v != 0u && v >= lo && v <= hi && bin_of(v) == bstar;
+                }
+                int tot;
+                int pc = block_exclusive_scan(nc, sl.warp, tot);
+                for (int i = i0; i < i1; ++i) {
+                    const uint32_t v = s_keys[i];
+                    if (v == 0u) continue;
+                    if (v > hi || (v >= lo && bin_of(v) > bstar)) mark(i);
+                    else if (v >= lo && bin_of(v) == bstar) {
+                        pub.cand_key[pc] = v;
+                        pub.cand_g[pc] = g0 + i;
+                        ++pc;
+                    }
+                }
+                if (tid == 0) pub.n_cand = tot;
+                break;
+            }
+            // crowded boundary bin: continue inside its exact key range
+            uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+            for (int i = tid; i < n; i += kThreads) {
+                const uint32_t v = s_keys[i];
+                if (v != 0u && v >= lo && v <= hi && bin_of(v) == bstar) { bmx = max(bmx, v); bmn = min(bmn, v); }
+            }
+            bmx = __reduce_max_sync(full, bmx);
+            bmn = __reduce_min_sync(full, bmn);
+            if (lane == 0) { sl.red[1][warp] = bmx; sl.red[2][warp] = bmn; }
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t hx = 0u, lx = 0xFFFFFFFFu;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) { hx = max(hx, sl.red[1][w]); lx = min(lx, sl.red[2][w]); }
+                pub.bmax = hx; pub.bmin = lx;
+            }
+            cluster.sync();  // also: every split is done reading this level's histograms
+            if (warp == 0) {
+                uint32_t hx = 0u, lx = 0xFFFFFFFFu;
+                if (lane < S) {
+                    const SelPub* rp = cluster.map_shared_rank(&pub, lane);
+                    hx = rp->bmax; lx = rp->bmin;
+                }
+                hx = __reduce_max_sync(full, hx);
+                lx = __reduce_min_sync(full, lx);
+                if (lane == 0) { sl.g[6] = (int)hx; sl.g[7] = (int)lx; }
+            }
+            __syncthreads();
+            hi = (uint32_t)sl.g[6];
+            lo = (uint32_t)sl.g[7];
+            above = above_new;
+        }
+    }
+
+    if (mode == 1) {
+        cluster.sync();  // every split's candidates are published
+        if (warp == 0) {
+            // the candidates of all splits, one per lane, in split (= group) order
+            const int ncr = lane < S ? cluster.map_shared_rank(&pub, lane)->n_cand : 0;
+            int cpre = ncr;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(full, cpre, o);
+                if (lane >= o) cpre += y;
+            }
+            const int ctot = __shfl_sync(full, cpre, 31);
+            int r = 0;
+            for (int j = 0; j < S; ++j) r += __shfl_sync(full, cpre, j) <= lane;
+            const int start = __shfl_sync(full, cpre - ncr, min(r, 31));
+            uint32_t ck = 0u;
+            int cg = -1;
+            if (lane < ctot) {
+                const SelPub* rp = cluster.map_shared_rank(&pub, r);
+                ck = rp->cand_key[lane - start];
+                cg = rp->cand_g[lane - start];
+            }
+            int rank = 0;
+            for (int j = 0; j < ctot; ++j) {
+                const uint32_t kj = __shfl_sync(full, ck, j);
+                const int gj = __shfl_sync(full, cg, j);
+                rank += (kj > ck) || (kj == ck && gj < cg);
+            }
+            if (lane < ctot && rank < need && r == s) mark(cg - g0);
+        }
+    } else if (mode == 2) {
+        // keys above kstar are taken, then the first `need` keys equal to kstar in group order
+        int neq = 0;
+        for (int i = i0; i < i1; ++i) neq += s_keys[i] == kstar;
+        int tot;
+        int eq_before = block_exclusive_scan(neq, sl.warp, tot);
+        if (tid == 0) pub.n_eq = tot;
+        cluster.sync();  // every split's count of equal keys is published
+        if (warp == 0) {
+            int t = lane < s ? cluster.map_shared_rank(&pub, lane)->n_eq : 0;
+            t = __reduce_add_sync(full, t);
+            if (lane == 0) sl.g[0] = t;
+        }
+        __syncthreads();
+        const int take = min(max(need - sl.g[0], 0), tot);
+        for (int i = i0; i < i1; ++i) {
+            const uint32_t v = s_keys[i];
+            if (v > kstar) mark(i);
+            else if (v == kstar) {
+                if (eq_before < take) mark(i);
+                ++eq_before;
+            }
+        }
+    } else {
+        for (int i = tid; i < n; i += kThreads)
+            if (s_keys[i] != 0u) mark(i);
+    }
+    __syncthreads();
+
+    // this split's selected groups, ascending, then the concatenation over the splits
+    {
+        int c = 0;
+        for (int i = i0; i < i1; ++i) c += (s_mark[i >> 5] >> (i & 31)) & 1u;
+        int tot;
+        int p = block_exclusive_scan(c, sl.warp, tot);
+        for (int i = i0; i < i1; ++i) {
+            if ((s_mark[i >> 5] >> (i & 31)) & 1u) {
+                if (p < HSQ_MAX_BETA) pub.mine[p] = g0 + i;
+                ++p;
+            }
+        }
+        if (tid == 0) pub.n_mine = min(tot, beta);
+    }
+    cluster.sync();  // every split's list is published
+    if (warp == 0) {
+        const int nm = lane < S ? cluster.map_shared_rank(&pub, lane)->n_mine : 0;
+        int incl = nm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(full, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane < S) sl.off[lane + 1] = incl;
+        if (lane == 0) sl.off[0] = 0;
+    }
+    __syncthreads();
+    const int total = min(sl.off[S], beta);
+    for (int i = tid; i < beta; i += kThreads) {
+        int g = -1;
+        if (i < total) {
+            int r = 0;
+            while (sl.off[r + 1] <= i) ++r;
+            g = cluster.map_shared_rank(&pub, r)->mine[i - sl.off[r]];
+        }
+        s_sel[i] = g;
+    }
+    __syncthreads();
+}
 
 template <int R, int N, bool kRoute>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
+    namespace cgx = cooperative_groups;
     extern __shared__ __align__(16) uint8_t s_dyn[];
     __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
     __shared__ __align__(16) float s_qt[R][kDim];
     __shared__ __align__(16) float s_qr[R][kDim];
-    __shared__ SelectSmem s_ss;
-    __shared__ int s_flag, s_gen;
+    __shared__ __align__(16) float s_ppart[R][hsq::kPartStride];  // this split's partial, read by the others
+    __shared__ SelPub s_pub;
+    __shared__ SelLocal s_sl;
 
     constexpr int RB = N * 136;
     constexpr int kBatchRecs = kFetchBatchBytes / RB;
     constexpr int kRecChunks = RB / 16;
 
-    const int s = blockIdx.x, S = a.S;
+    cgx::cluster_group cluster = cgx::this_cluster();
+    const int S = (int)cluster.num_blocks();
+    const int s = (int)cluster.block_rank();
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
-    const int tid = threadIdx.x, hw = tid >> 4, l = hlane();
+    const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
     const unsigned m = half_mask();
-    const DecodeLayout L = decode_layout<R, N>(c.G, S, c.max_l1, c.beta, kRoute);
-    uint8_t* s_l2k = s_dyn + L.l2k;
-    uint8_t* s_l2v = s_dyn + L.l2v;
-    float* s_l2kn = reinterpret_cast<float*>(s_dyn + L.l2kn);
-    float* s_l2vn = reinterpret_cast<float*>(s_dyn + L.l2vn);
-    uint8_t* s_cnt = s_dyn + L.cnt;
-    uint8_t* s_l1k = s_dyn + L.l1k;
-    uint8_t* s_l1v = s_dyn + L.l1v;
-    float* s_l1kn = reinterpret_cast<float*>(s_dyn + L.l1kn);
-    float* s_l1vn = reinterpret_cast<float*>(s_dyn + L.l1vn);
-    float* s_logit = reinterpret_cast<float*>(s_dyn + L.logit);
-    int* s_sel = reinterpret_cast<int*>(s_dyn + L.sel);
-    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + L.mask);
-    float* s_base = reinterpret_cast<float*>(s_dyn + L.base);
-    uint32_t* s_rbits = reinterpret_cast<uint32_t*>(s_dyn + L.rbits);
-    float* s_off = reinterpret_cast<float*>(s_dyn + L.off);
-    uint8_t* s_rec = s_dyn + L.rec;
-    uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_dyn + L.keys);
+    const unsigned full = 0xffffffffu;
+    const int fl = a.flags;
+    const DecodeLayout L = decode_layout<R, N>(c.G, c.T, S, c.max_l1, c.beta, kRoute, fl);
 
     const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
     const int n2 = g1 - g0;
@@ -1076,18 +1427,65 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     const int f0 = (int)((long long)c.beta * s / S), f1 = (int)((long long)c.beta * (s + 1) / S);
     const int nfetch = f1 - f0;
 
+    // inputs: staged copies in shared memory, or read in place
+    const uint8_t* g_l2k = c.l2_kc + ((size_t)bh * c.G + g0) * 48;
+    const uint8_t* g_l2v = c.l2_vc + ((size_t)bh * c.G + g0) * 48;
+    const float* g_l2kn = c.l2_kn + (size_t)bh * c.G + g0;
+    const float* g_l2vn = c.l2_vn + (size_t)bh * c.G + g0;
+    const uint8_t* g_cnt = c.l2_cnt + (size_t)b * c.G + g0;
+    const uint8_t* g_l1k = c.l1_kc + ((size_t)bh * c.max_l1 + e0) * 64;
+    const uint8_t* g_l1v = c.l1_vc + ((size_t)bh * c.max_l1 + e0) * 64;
+    const float* g_l1kn = c.l1_kn + (size_t)bh * c.max_l1 + e0;
+    const float* g_l1vn = c.l1_vn + (size_t)bh * c.max_l1 + e0;
+    const uint32_t* g_bitmap = c.l1_bitmap + (size_t)b * c.W;
+    const bool st2 = fl & kStageL2, st1 = fl & kStageL1, stb = fl & kStageBitmap, keep = fl & kKeepLogits;
+    const uint8_t* p_l2k = st2 ? s_dyn + L.l2k : g_l2k;
+    const uint8_t* p_l2v = st2 ? s_dyn + L.l2v : g_l2v;
+    const float* p_l2kn = st2 ? reinterpret_cast<const float*>(s_dyn + L.l2kn) : g_l2kn;
+    const float* p_l2vn = st2 ? reinterpret_cast<const float*>(s_dyn + L.l2vn) : g_l2vn;
+    const uint8_t* p_cnt = st2 ? s_dyn + L.cnt : g_cnt;
+    const uint8_t* p_l1k = st1 ? s_dyn + L.l1k : g_l1k;
+    const uint8_t* p_l1v = st1 ? s_dyn + L.l1v : g_l1v;
+    const float* p_l1kn = st1 ? reinterpret_cast<const float*>(s_dyn + L.l1kn) : g_l1kn;
+    const float* p_l1vn = st1 ? reinterpret_cast<const float*>(s_dyn + L.l1vn) : g_l1vn;
+    const uint32_t* p_bitmap = stb ? reinterpret_cast<const uint32_t*>(s_dyn + L.bitmap) : g_bitmap;
+    float* s_logit = reinterpret_cast<float*>(s_dyn + L.logit);
+    uint32_t* s_keys = reinterpret_cast<uint32_t*>(s_dyn + L.keys);
+    int* s_sel = reinterpret_cast<int*>(s_dyn + L.sel);
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + L.mask);
+    float* s_lev = reinterpret_cast<float*>(s_dyn + L.lev);
+    float* s_b0 = reinterpret_cast<float*>(s_dyn + L.b0);
+    float* s_off = reinterpret_cast<float*>(s_dyn + L.off);
+    float* s_base = reinterpret_cast<float*>(s_dyn + L.base);
+    uint32_t* s_rbits = reinterpret_cast<uint32_t*>(s_dyn + L.rbits);
+    uint8_t* s_rec = s_dyn + L.rec;
+
     // 1. stage the device-resident inputs of this split
-    stage16(s_l2k, c.l2_kc + ((size_t)bh * c.G + g0) * 48, n2 * 48);
-    stage16(s_l2v, c.l2_vc + ((size_t)bh * c.G + g0) * 48, n2 * 48);
-    stage4(s_l2kn, c.l2_kn + (size_t)bh * c.G + g0, n2);
-    stage4(s_l2vn, c.l2_vn + (size_t)bh * c.G + g0, n2);
-    stage16(s_l1k, c.l1_kc + ((size_t)bh * c.max_l1 + e0) * 64, n1 * 64);
-    stage16(s_l1v, c.l1_vc + ((size_t)bh * c.max_l1 + e0) * 64, n1 * 64);
-    stage4(s_l1kn, c.l1_kn + (size_t)bh * c.max_l1 + e0, n1);
-    stage4(s_l1vn, c.l1_vn + (size_t)bh * c.max_l1 + e0, n1);
+    if (st2) {
+        stage16(s_dyn + L.l2k, g_l2k, n2 * 48);
+        stage16(s_dyn + L.l2v, g_l2v, n2 * 48);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l2kn), g_l2kn, n2);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l2vn), g_l2vn, n2);
+        for (int i = tid; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
+    }
+    if (st1) {
+        stage16(s_dyn + L.l1k, g_l1k, n1 * 64);
+        stage16(s_dyn + L.l1v, g_l1v, n1 * 64);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l1kn), g_l1kn, n1);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l1vn), g_l1vn, n1);
+    }
+    if (stb) stage4(reinterpret_cast<float*>(s_dyn + L.bitmap), reinterpret_cast<const float*>(g_bitmap), c.W);
     if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
-    stage16(s_off, tb.rope_lo, N * kDim * 4);  // cos/sin of n * omega, n < N
-    for (int i = tid; i < n2; i += kThreads) s_cnt[i] = __ldg(c.l2_cnt + (size_t)b * c.G + g0 + i);
+    // RoPE rows: level k row j = hi[j * 16^k] (angle 256 j 16^k omega), b0 row j = lo[N j], off row n = lo[n]
+    const int n_hi = (tb.max_pos + 255) / 256;
+    for (int i = tid; i < L.nlev * 16 * 32; i += kThreads) {
+        const int rowi = i >> 5, k = rowi >> 4, j = rowi & 15;
+        const int src = j << (4 * k);
+        if (src < n_hi) cp_async16(s_lev + 4 * i, tb.rope_hi + (size_t)src * kDim + 4 * (i & 31));
+    }
+    for (int i = tid; i < L.nb0 * 32; i += kThreads)
+        cp_async16(s_b0 + 4 * i, tb.rope_lo + (size_t)(N * (i >> 5)) * kDim + 4 * (i & 31));
+    stage16(s_off, tb.rope_lo, N * kDim * 4);
     for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
     float sg[8];
     load_signs_global(sg, c.signs);
@@ -1118,19 +1516,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
 
     const float* c4 = s_cb;
     const float* c3 = s_cb + 32;
-    Softmax<R> sm;
-    sm.init();
-    {
-        float qt[R][8];
+    float qt[R][8];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            qt[j][k] = s_qt[j][4 * l + k];
+            qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
+        }
+    }
+    // log2-domain logits of L2 groups i and ib against every query head
+    auto l2_logits = [&](int i, int ib, float xa[R], float xb[R]) {
+        float va[8], vb[8];
+        unpack3_smem(p_l2k + i * 48, c3, 1.0f, va);
+        unpack3_smem(p_l2k + ib * 48, c3, 1.0f, vb);
+        const float kna = p_l2kn[i], knb = p_l2kn[ib];
 #pragma unroll
         for (int j = 0; j < R; ++j) {
+            float da = 0.f, db = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                qt[j][k] = s_qt[j][4 * l + k];
-                qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
+            for (int k = 0; k < 8; ++k) {
+                da = fmaf(qt[j][k], va[k], da);
+                db = fmaf(qt[j][k], vb[k], db);
             }
+            xa[j] = kna * half_sum(da, m) * kLogitScaleLog2;
+            xb[j] = knb * half_sum(db, m) * kLogitScaleLog2;
         }
-        // 3. L2 logits per query head, and the routing score
+    };
+    if (kRoute || keep) {
         float gq[8];
         if (kRoute) {
 #pragma unroll
@@ -1150,12 +1563,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             const int ib = i + kHalves;
             const bool hb = ib < n2;
             const int ibs = hb ? ib : i;
-            const bool nea = s_cnt[i] > 0, neb = hb && s_cnt[ibs] > 0;
-            float va[8], vb[8];
-            unpack3_smem(s_l2k + i * 48, c3, 1.0f, va);
-            unpack3_smem(s_l2k + ibs * 48, c3, 1.0f, vb);
-            const float kna = s_l2kn[i], knb = s_l2kn[ibs];
             if (kRoute) {
+                float va[8], vb[8];
+                unpack3_smem(p_l2k + i * 48, c3, 1.0f, va);
+                unpack3_smem(p_l2k + ibs * 48, c3, 1.0f, vb);
                 float da = 0.f, db = 0.f;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -1165,112 +1576,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
                 da = half_sum(da, m);
                 db = half_sum(db, m);
                 if (l == 0) {
-                    a.scores[(size_t)bh * c.G + g0 + i] = nea ? kna * da : -INFINITY;
-                    if (hb) a.scores[(size_t)bh * c.G + g0 + ib] = neb ? knb * db : -INFINITY;
+                    s_keys[i] = p_cnt[i] > 0 ? ordered_key(p_l2kn[i] * da) : 0u;
+                    if (hb) s_keys[ib] = p_cnt[ib] > 0 ? ordered_key(p_l2kn[ib] * db) : 0u;
                 }
             }
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                float da = 0.f, db = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    da = fmaf(qt[j][k], va[k], da);
-                    db = fmaf(qt[j][k], vb[k], db);
-                }
-                da = half_sum(da, m);
-                db = half_sum(db, m);
+            if (keep) {
+                float xa[R], xb[R];
+                l2_logits(i, ibs, xa, xb);
                 if (l == 0) {
-                    if (nea) s_logit[i * R + j] = kna * da * kLogitScaleLog2;
-                    if (neb) s_logit[ib * R + j] = knb * db * kLogitScaleLog2;
-                }
-            }
-        }
-    }
-    // 4. L1 tokens (independent of routing: with kRoute they run while the selection is made)
-    auto l1_tokens = [&]() {
-        float qt[R][8];
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                qt[j][k] = s_qt[j][4 * l + k];
-                qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
-            }
-        }
-        auto entry = [&](int e, float x[R], float vv[8]) {
-            const uint16_t* kr = reinterpret_cast<const uint16_t*>(s_l1k + e * 64);
-            const uint16_t* vr = reinterpret_cast<const uint16_t*>(s_l1v + e * 64);
-            float kv[8];
-            unpack4(kr[l], kr[16 + l], c4, s_l1kn[e], kv);
-            unpack4(vr[l], vr[16 + l], c4, s_l1vn[e], vv);
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                float d = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) d = fmaf(qt[j][k], kv[k], d);
-                x[j] = half_sum(d, m) * kLogitScaleLog2;
-            }
-        };
-        for (int e = hw; e < n1; e += 2 * kHalves) {
-            const int eb = e + kHalves;
-            const bool hb = eb < n1;
-            float xa[R], xb[R], va[8], vb[8];
-            entry(e, xa, va);
-            entry(hb ? eb : e, xb, vb);
-            sm.add2(xa, va, true, xb, vb, hb);
-        }
-    };
-
-    // 5. the selection of this (b, h)
-    const int32_t* selrow = a.sel + (size_t)bh * c.beta;
-    if (kRoute) {
-        __syncthreads();  // this split's scores are written
-        if (tid == 0) {
-            const int gcur = ld_acquire_gpu(a.gen + bh);
-            __threadfence();
-            const int ticket = atomicAdd(a.arrive + bh, 1);
-            s_gen = gcur;
-            s_flag = (ticket == S - 1);
-            if (s_flag) __threadfence();
-        }
-        __syncthreads();
-        if (s_flag) {
-            // last split to arrive: select for everyone, release them, then do its own L1 tokens
-            for (int g = tid; g < c.G; g += kThreads) s_keys[g] = ordered_key(__ldcg(a.scores + (size_t)bh * c.G + g));
-            __syncthreads();
-            select_top_beta(s_keys, c.G, c.beta, a.sel + (size_t)bh * c.beta, s_sel, s_ss);
-            __syncthreads();
-            if (tid == 0) {
-                a.arrive[bh] = 0;
-                __threadfence();
-                atomicAdd(a.gen + bh, 1);
-            }
-            l1_tokens();
-        } else {
-            l1_tokens();
-            if (tid == 0) {
-                int it = 0;
-                while (ld_acquire_gpu(a.gen + bh) == s_gen) {
-                    if (++it > kSpinLimit) {
-                        atomicOr(a.err, HSQ_DEVERR_WAIT);
-                        break;
+                    for (int j = 0; j < R; ++j) {
+                        s_logit[i * R + j] = xa[j];
+                        if (hb) s_logit[ib * R + j] = xb[j];
                     }
-                    __nanosleep(32);
                 }
             }
-            __syncthreads();
-            for (int i = tid; i < c.beta; i += kThreads) {
-                const int g = __ldcg(selrow + i);
-                s_sel[i] = (g >= 0 && g < c.G) ? g : -1;
-            }
         }
-    } else {
-        l1_tokens();
-        for (int i = tid; i < c.beta; i += kThreads) s_sel[i] = valid_sel(selrow, i, c.G, a.err);
     }
-    __syncthreads();
 
-    // 6. start the gather of the first batch of this split's records
+    // 3. the selection of this (b, h)
+    if (kRoute) {
+        __syncthreads();  // this split's keys are written
+        cluster_select(s_keys, n2, g0, c.beta, s_sel, s_mask, s_pub, s_sl);
+        if (s == 0)
+            for (int i = tid; i < c.beta; i += kThreads) a.sel[(size_t)bh * c.beta + i] = s_sel[i];
+    } else {
+        for (int i = tid; i < c.beta; i += kThreads) s_sel[i] = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
+        __syncthreads();
+        for (int i = tid; i < c.beta; i += kThreads) {
+            const int g = s_sel[i];
+            if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
+        }
+    }
+
+    // 4. gather this split's records; meanwhile L1 tokens and unselected summaries
     uint4 pre[kMaxFetchChunksPerThread];
     auto issue = [&](int r0, int nrec) {
 #pragma unroll
@@ -1289,72 +1628,86 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             }
         }
     };
-    // per record: cos/sin of the group's base angle g*N*omega and its L1 bits.  The device
-    // loads are issued before the host gather so they do not queue behind it.
-    float4 mch, msh, mcl, msl;
-    uint32_t mword = 0u;
-    auto meta_load = [&](int r0, int nrec) {
+    // per record: cos/sin of its base angle g N omega (staged rows only) and its L1 bits
+    auto meta = [&](int r0, int nrec) {
         if (hw < nrec) {
             const int g = s_sel[r0 + hw];
             if (g >= 0) {
                 const int p0 = g * N;
-                const float* rh = tb.rope_hi + (size_t)(p0 >> 8) * kDim;
-                const float* rl = tb.rope_lo + (size_t)(p0 & 255) * kDim;
-                mch = __ldg(reinterpret_cast<const float4*>(rh + 4 * l));
-                msh = __ldg(reinterpret_cast<const float4*>(rh + 64 + 4 * l));
-                mcl = __ldg(reinterpret_cast<const float4*>(rl + 4 * l));
-                msl = __ldg(reinterpret_cast<const float4*>(rl + 64 + 4 * l));
-                if (l == 0) mword = __ldg(c.l1_bitmap + (size_t)b * c.W + (p0 >> 5));
-            }
-        }
-    };
-    auto meta_store = [&](int r0, int nrec) {
-        if (hw < nrec) {
-            const int g = s_sel[r0 + hw];
-            if (g >= 0) {
-                const int p0 = g * N;
-                float* bp = s_base + hw * kDim;
-                *reinterpret_cast<float4*>(bp + 4 * l) =
-                    make_float4(fmaf(mch.x, mcl.x, -msh.x * msl.x), fmaf(mch.y, mcl.y, -msh.y * msl.y),
-                                fmaf(mch.z, mcl.z, -msh.z * msl.z), fmaf(mch.w, mcl.w, -msh.w * msl.w));
-                *reinterpret_cast<float4*>(bp + 64 + 4 * l) =
-                    make_float4(fmaf(msh.x, mcl.x, mch.x * msl.x), fmaf(msh.y, mcl.y, mch.y * msl.y),
-                                fmaf(msh.z, mcl.z, mch.z * msl.z), fmaf(msh.w, mcl.w, mch.w * msl.w));
-                if (l == 0) s_rbits[hw] = (mword >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
+                const float* br = s_b0 + ((p0 & 255) / N) * kDim;
+                float4 cs = *reinterpret_cast<const float4*>(br + 4 * l);
+                float4 sn = *reinterpret_cast<const float4*>(br + 64 + 4 * l);
+                int rest = p0 >> 8;
+                for (int k = 0; rest > 0; ++k, rest >>= 4) {
+                    const int j = rest & 15;
+                    if (j) {
+                        const float* lr = s_lev + (k * 16 + j) * kDim;
+                        angle_add4(cs, sn, *reinterpret_cast<const float4*>(lr + 4 * l),
+                                   *reinterpret_cast<const float4*>(lr + 64 + 4 * l));
+                    }
+                }
+                *reinterpret_cast<float4*>(s_base + hw * kDim + 4 * l) = cs;
+                *reinterpret_cast<float4*>(s_base + hw * kDim + 64 + 4 * l) = sn;
+                if (l == 0)
+                    s_rbits[hw] = (p_bitmap[p0 >> 5] >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
             }
         }
     };
     const int nb0 = min(nfetch, kBatchRecs);
     if (nb0 > 0) {
-        meta_load(f0, nb0);
         issue(f0, nb0);
-        meta_store(f0, nb0);
+        meta(f0, nb0);
     }
-    for (int i = tid; i < c.beta; i += kThreads) {
-        const int g = s_sel[i];
-        if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
-    }
-    __syncthreads();
+    __syncthreads();  // s_mask complete (kRoute: marked by the selection)
 
-    // unselected non-empty summaries: one entry each, two per half-warp per iteration
+    Softmax<R> sm;
+    sm.init();
+    {
+        auto entry = [&](int e, float x[R], float vv[8]) {
+            const uint16_t* kr = reinterpret_cast<const uint16_t*>(p_l1k + e * 64);
+            const uint16_t* vr = reinterpret_cast<const uint16_t*>(p_l1v + e * 64);
+            float kv[8];
+            unpack4(kr[l], kr[16 + l], c4, p_l1kn[e], kv);
+            unpack4(vr[l], vr[16 + l], c4, p_l1vn[e], vv);
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                float d = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d = fmaf(qt[j][k], kv[k], d);
+                x[j] = half_sum(d, m) * kLogitScaleLog2;
+            }
+        };
+        for (int e = hw; e < n1; e += 2 * kHalves) {
+            const int eb = e + kHalves;
+            const bool hb = eb < n1;
+            float xa[R], xb[R], va[8], vb[8];
+            entry(e, xa, va);
+            entry(hb ? eb : e, xb, vb);
+            sm.add2(xa, va, true, xb, vb, hb);
+        }
+    }
     for (int i = hw; i < n2; i += 2 * kHalves) {
         const int ib = i + kHalves;
         const int ibs = ib < n2 ? ib : i;
-        const bool oka = s_cnt[i] > 0 && !((s_mask[i >> 5] >> (i & 31)) & 1u);
-        const bool okb = ib < n2 && s_cnt[ibs] > 0 && !((s_mask[ibs >> 5] >> (ibs & 31)) & 1u);
+        const bool oka = p_cnt[i] > 0 && !((s_mask[i >> 5] >> (i & 31)) & 1u);
+        const bool okb = ib < n2 && p_cnt[ibs] > 0 && !((s_mask[ibs >> 5] >> (ibs & 31)) & 1u);
         if (!oka && !okb) continue;
         float va[8], vb[8], xa[R], xb[R];
-        unpack3_smem(s_l2v + i * 48, c3, s_l2vn[i], va);
-        unpack3_smem(s_l2v + ibs * 48, c3, s_l2vn[ibs], vb);
+        unpack3_smem(p_l2v + i * 48, c3, p_l2vn[i], va);
+        unpack3_smem(p_l2v + ibs * 48, c3, p_l2vn[ibs], vb);
+        if (keep) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-            xa[j] = s_logit[i * R + j];
-            xb[j] = s_logit[ibs * R + j];
+            for (int j = 0; j < R; ++j) {
+                xa[j] = s_logit[i * R + j];
+                xb[j] = s_logit[ibs * R + j];
+            }
+        } else {
+            l2_logits(i, ibs, xa, xb);
         }
         sm.add2(xa, va, oka, xb, vb, okb);
     }
 
-    // 7. recovered tokens of the selected groups
+    // 5. recovered tokens of the selected groups
     if (nfetch > 0) {
         float qr[R][8];
 #pragma unroll
@@ -1392,22 +1745,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
                 const float kn = norms[n] * kRsqrtD;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
-                {   // RoPE at t = g*N + n: base angle (per record) plus offset n*omega
-                    const float* bp = s_base + rec * kDim;
-                    const float* op = s_off + n * kDim;
-                    const float4 cb = *reinterpret_cast<const float4*>(bp + 4 * l);
-                    const float4 sb = *reinterpret_cast<const float4*>(bp + 64 + 4 * l);
-                    const float4 co = *reinterpret_cast<const float4*>(op + 4 * l);
-                    const float4 so = *reinterpret_cast<const float4*>(op + 64 + 4 * l);
-                    const float cbv[4] = {cb.x, cb.y, cb.z, cb.w}, sbv[4] = {sb.x, sb.y, sb.z, sb.w};
-                    const float cov[4] = {co.x, co.y, co.z, co.w}, sov[4] = {so.x, so.y, so.z, so.w};
+                {   // RoPE at t = g N + n: base angle (per record) plus offset n omega
+                    float4 cs = *reinterpret_cast<const float4*>(s_base + rec * kDim + 4 * l);
+                    float4 sn = *reinterpret_cast<const float4*>(s_base + rec * kDim + 64 + 4 * l);
+                    angle_add4(cs, sn, *reinterpret_cast<const float4*>(s_off + n * kDim + 4 * l),
+                               *reinterpret_cast<const float4*>(s_off + n * kDim + 64 + 4 * l));
+                    const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float cs = fmaf(cbv[k], cov[k], -sbv[k] * sov[k]);
-                        const float sn = fmaf(sbv[k], cov[k], cbv[k] * sov[k]);
                         const float lo = kv[k], hi = kv[4 + k];
-                        kv[k] = fmaf(lo, cs, -hi * sn);
-                        kv[4 + k] = fmaf(hi, cs, lo * sn);
+                        kv[k] = fmaf(lo, cv[k], -hi * sv[k]);
+                        kv[4 + k] = fmaf(hi, cv[k], lo * sv[k]);
                     }
                 }
                 unpack4(vr[l], vr[16 + l], c4, norms[N + n], vv);
@@ -1430,31 +1778,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             }
             if (more) {
                 __syncthreads();
-                meta_load(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
-                meta_store(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+                meta(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
             }
         }
     }
 
-    // 8. merge the two halves of each warp, then the warps, into this split's partial
+    // 6. merge the two halves of each warp, then the warps, into this split's published partial
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-        const float mo = __shfl_xor_sync(0xffffffffu, sm.m[j], 16);
-        const float lo = __shfl_xor_sync(0xffffffffu, sm.l[j], 16);
+        const float mo = __shfl_xor_sync(full, sm.m[j], 16);
+        const float lo = __shfl_xor_sync(full, sm.l[j], 16);
         const float M = fmaxf(sm.m[j], mo);
         const float ws = merge_weight(sm.m[j], M), wo = merge_weight(mo, M);
         sm.l[j] = sm.l[j] * ws + lo * wo;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float ao = __shfl_xor_sync(0xffffffffu, sm.acc[j][i], 16);
+            const float ao = __shfl_xor_sync(full, sm.acc[j][i], 16);
             sm.acc[j][i] = sm.acc[j][i] * ws + ao * wo;
         }
         sm.m[j] = M;
     }
     __syncthreads();  // the record staging area becomes the warp-partial area
     float* s_part = reinterpret_cast<float*>(s_rec);  // [8 warps][R][132]
-    const int warp = tid >> 5;
     if ((tid & 16) == 0) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
@@ -1480,59 +1826,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             Lsum += p[129] * wt;
             A.x += v.x * wt; A.y += v.y * wt; A.z += v.z * wt; A.w += v.w * wt;
         }
-        float* dst = a.part + (((size_t)bh * S + s) * R + j) * hsq::kPartStride;
-        __stcg(reinterpret_cast<float4*>(dst + 4 * q4), A);
-        if (q4 == 0) { __stcg(dst + 128, M); __stcg(dst + 129, Lsum); }
+        *reinterpret_cast<float4*>(&s_ppart[j][4 * q4]) = A;
+        if (q4 == 0) { s_ppart[j][128] = M; s_ppart[j][129] = Lsum; }
     }
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        const int ticket = atomicAdd(a.merge_ctr + bh, 1);
-        s_flag = (ticket == S - 1);
-        if (s_flag) __threadfence();
-    }
-    __syncthreads();
-    if (!s_flag) return;
-    // stage every split's partial of this (b, h) in shared memory with one sweep
-    const float* pbase = a.part + (size_t)bh * S * R * hsq::kPartStride;
-    const size_t pbytes = (size_t)S * R * hsq::kPartStride * 4;
-    const bool staged = pbytes <= L.total;
-    float* s_all = reinterpret_cast<float*>(s_dyn);
-    if (staged) {
-        stage16(s_all, pbase, (int)pbytes);
-        cp_async_wait_all();
-        __syncthreads();
-    }
-    float* s_o = s_qr[0];  // [R][128]: merged outputs (the RoPE'd queries are no longer needed)
-    if (tid < R * 32) {
-        const int j = tid >> 5, q4 = tid & 31;
-        const float* base = (staged ? s_all : pbase) + (size_t)j * hsq::kPartStride;
-        auto ld = [&](const float* p) { return staged ? *p : __ldcg(p); };
-        float M = -INFINITY;
-        for (int k = 0; k < S; ++k) M = fmaxf(M, ld(base + (size_t)k * R * hsq::kPartStride + 128));
-        float Lsum = 0.f;
+    cluster.sync();  // every split's partial is published
+
+    // query head j is merged by split j mod S (warp w: head s + w S), then rotated back by one half-warp
+    float* s_o = s_qr[0];  // [R][128]; the RoPE'd queries are no longer needed
+    const int nmine = (R - s + S - 1) / S;
+    if (warp < nmine) {
+        const int j = s + warp * S;
+        float mr = -INFINITY, lr = 0.f;
+        if (lane < S) {
+            const float* pp = cluster.map_shared_rank(&s_ppart[j][0], lane);
+            mr = pp[128];
+            lr = pp[129];
+        }
+        const float M = warp_max(mr);
+        const float wr = merge_weight(mr, M);
+        const float Lsum = warp_sum(lr * wr);
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < S; ++k) {
-            const float* p = base + (size_t)k * R * hsq::kPartStride;
-            const float wt = merge_weight(ld(p + 128), M);
-            Lsum += ld(p + 129) * wt;
-            const float4 x = staged ? *reinterpret_cast<const float4*>(p + 4 * q4)
-                                    : __ldcg(reinterpret_cast<const float4*>(p + 4 * q4));
-            o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
+#pragma unroll
+        for (int r = 0; r < kMaxSplits; ++r) {
+            const float wt = __shfl_sync(full, wr, r);
+            if (r < S) {
+                const float4 x = *reinterpret_cast<const float4*>(cluster.map_shared_rank(&s_ppart[j][0], r) + 4 * lane);
+                o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
+            }
         }
         const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-        *reinterpret_cast<float4*>(s_o + j * kDim + 4 * q4) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        *reinterpret_cast<float4*>(s_o + j * kDim + 4 * lane) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
     __syncthreads();
-    if (hw < R) {
+    if (hw < 2 * nmine && (hw & 1) == 0) {
+        const int j = s + (hw >> 1) * S;
         float o[8];
-        load_f32x8_smem(s_o + hw * kDim, o);
+        load_f32x8_smem(s_o + j * kDim, o);
         fwht(o, m);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] *= sg[i] * kRsqrtD;
-        store_f32x8(a.out + ((size_t)b * c.Hq + h * R + hw) * kDim, o);
+        store_f32x8(a.out + ((size_t)b * c.Hq + h * R + j) * kDim, o);
     }
-    if (tid == 0) a.merge_ctr[bh] = 0;
+    cluster.sync();  // this split's shared memory stays alive until every reader is done
 }
 
 }  // namespace
@@ -1543,21 +1878,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
 
 struct hsq_ctx {
     hsq_config cfg;
-    int r = 1, num_sms = 0, device = 0;
+    int r = 1, num_sms = 0, device = 0, smem_optin = 0;
     int G_max = 0, W_max = 0;
     float* d_cb = nullptr;
     float* d_rope_hi = nullptr;
     float* d_rope_lo = nullptr;
     float* d_scores = nullptr;
-    float* d_part = nullptr;
     int* d_route_ctr = nullptr;
-    int* d_attn_ctr = nullptr;   // merge tickets of the decode kernel
-    int* d_arrive = nullptr;     // selection barrier: arrivals per (b, h)
-    int* d_gen = nullptr;        // selection barrier: generation per (b, h)
     int* d_prefix = nullptr;
     int* d_err = nullptr;
-    struct Split { int B, G, route, S; };
-    std::vector<Split> splits;   // chosen split counts per cache shape
+    // decode launch plan per cache shape: cluster size S (0 = cannot launch) and staging flags
+    struct Plan { int B, T, route, S, flags; };
+    std::vector<Plan> plans;
     std::string last_error;
 };
 
@@ -1636,47 +1968,88 @@ hsq_status dispatch_rn(int r, int n, F&& f) {
     return HSQ_ERR_UNSUPPORTED;
 }
 
-// Split count of the decode kernel for B sequences of G groups: one CTA per SM
-// across the B * Hkv heads.  With the routing barrier (kRoute) the whole grid
-// must be co-resident; 0 means it cannot be.
+// Kernels allowed to run in 16-CTA clusters (the portable limit is 8).
+std::vector<std::pair<const void*, int>> g_big_clusters;
+
+cudaError_t allow_big_clusters(const void* fn, int device) {
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    for (auto& e : g_big_clusters)
+        if (e.first == fn && e.second == device) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err == cudaSuccess) g_big_clusters.push_back({fn, device});
+    return err;
+}
+
+cudaLaunchConfig_t decode_config(int S, int bh, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(S, bh, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return lc;
+}
+
+// Cluster size of the decode kernel for B sequences of T tokens: the largest
+// S <= 16 whose B * Hkv clusters are all resident at once (one wave); when no
+// S gives one wave, S = 1 (least per-head overhead across waves).  A fixed
+// n_splits is an upper bound.  Inputs that do not fit in shared memory are
+// left in global memory, dropping first the kept L2 logits, then the L1
+// slice, then the bitmap row, then the L2 slice.
 template <int R, int N, bool kRoute>
-int fit_splits(hsq_ctx* ctx, int B, int G) {
-    for (const auto& e : ctx->splits)
-        if (e.B == B && e.G == G && e.route == (int)kRoute) return e.S;
+hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T) {
+    for (const auto& e : ctx->plans)
+        if (e.B == B && e.T == T && e.route == (int)kRoute) return e;
+    const int G = hsq::groups_of(T, N);
     const int bh = B * ctx->cfg.n_kv_heads;
-    auto fn = decode_kernel<R, N, kRoute>;
-    int S0 = ctx->cfg.n_splits > 0 ? ctx->cfg.n_splits : ctx->num_sms / bh;
-    S0 = std::max(1, std::min(std::min(S0, (int)HSQ_MAX_SPLITS), G));
-    int chosen = kRoute ? 0 : S0;
-    for (int S = S0; S >= 1; --S) {
-        const size_t smem = decode_layout<R, N>(G, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute).total;
-        if (raise_smem_limit((const void*)fn, ctx->device, smem) != cudaSuccess) continue;
-        int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, smem) != cudaSuccess) continue;
-        if (!kRoute) { chosen = S; break; }
-        if ((long long)S * bh <= (long long)occ * ctx->num_sms) { chosen = S; break; }
-        if (ctx->cfg.n_splits > 0) break;  // a fixed split count that does not fit: no fused step
+    const void* fn = (const void*)decode_kernel<R, N, kRoute>;
+    hsq_ctx::Plan plan{B, T, (int)kRoute, 0, 0};
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess && allow_big_clusters(fn, ctx->device) == cudaSuccess) {
+        const size_t cap = (size_t)ctx->smem_optin > fa.sharedSizeBytes ? ctx->smem_optin - fa.sharedSizeBytes : 0;
+        const int fixed = ctx->cfg.n_splits;
+        const int s_hi = std::max(1, std::min(fixed > 0 ? fixed : kMaxSplits, std::max(G, 1)));
+        static const int kFlagOrder[] = {kStageL2 | kKeepLogits | kStageL1 | kStageBitmap,
+                                         kStageL2 | kStageL1 | kStageBitmap, kStageL2 | kStageBitmap, kStageL2, 0};
+        for (int S = s_hi; S >= 1; --S) {
+            int flags = -1;
+            size_t smem = 0;
+            for (int f : kFlagOrder) {
+                smem = decode_layout<R, N>(G, T, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute, f).total;
+                if (smem <= cap) { flags = f; break; }
+            }
+            if (flags < 0) continue;
+            if (raise_smem_limit(fn, ctx->device, smem) != cudaSuccess) continue;
+            cudaLaunchAttribute at[1];
+            cudaLaunchConfig_t lc = decode_config(S, bh, smem, 0, at);
+            int nc = 0;
+            if (cudaOccupancyMaxActiveClusters(&nc, fn, &lc) != cudaSuccess || nc < 1) continue;
+            plan.S = S;
+            plan.flags = flags;
+            if (fixed > 0 || nc >= bh) break;  // otherwise keep going down to S = 1
+        }
     }
     cudaGetLastError();
-    ctx->splits.push_back({B, G, (int)kRoute, chosen});
-    return chosen;
+    ctx->plans.push_back(plan);
+    return plan;
 }
 
 template <int R, int N, bool kRoute>
-hsq_status launch_decode(hsq_ctx* ctx, CacheView v, DecodeArgs a, cudaStream_t st) {
-    const DecodeLayout L = decode_layout<R, N>(v.G, a.S, v.max_l1, v.beta, kRoute);
-    auto fn = decode_kernel<R, N, kRoute>;
-    cudaError_t e = raise_smem_limit((const void*)fn, ctx->device, L.total);
+hsq_status launch_decode(hsq_ctx* ctx, CacheView v, DecodeArgs a, const hsq_ctx::Plan& p, cudaStream_t st) {
+    a.flags = p.flags;
+    const DecodeLayout L = decode_layout<R, N>(v.G, v.T, p.S, v.max_l1, v.beta, kRoute, p.flags);
+    const void* fn = (const void*)decode_kernel<R, N, kRoute>;
+    cudaError_t e = raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
-    dim3 grid(a.S, v.B * v.Hkv);
-    Tables tb = make_tables(ctx);
-    if (kRoute) {
-        void* args[] = {&v, &a, &tb};
-        e = cudaLaunchCooperativeKernel((const void*)fn, grid, dim3(kThreads), args, L.total, st);
-    } else {
-        fn<<<grid, kThreads, L.total, st>>>(v, a, tb);
-        e = cudaGetLastError();
-    }
+    cudaLaunchAttribute at[1];
+    const cudaLaunchConfig_t lc = decode_config(p.S, v.B * v.Hkv, L.total, st, at);
+    const Tables tb = make_tables(ctx);
+    e = cudaLaunchKernelEx(&lc, decode_kernel<R, N, kRoute>, v, a, tb);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "decode launch");
     return HSQ_OK;
 }
@@ -1717,9 +2090,7 @@ hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
 
 void free_ctx(hsq_ctx* c) {
     cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
-    cudaFree(c->d_part); cudaFree(c->d_route_ctr); cudaFree(c->d_attn_ctr); cudaFree(c->d_prefix);
-    cudaFree(c->d_arrive); cudaFree(c->d_gen);
-    cudaFree(c->d_err);
+    cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err);
     delete c;
 }
 
@@ -1749,6 +2120,9 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaGetDevice(&c->device)) != cudaSuccess) return bail(e, "cudaGetDevice");
     if ((e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device)) != cudaSuccess)
         return bail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&c->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device)) !=
+        cudaSuccess)
+        return bail(e, "cudaDeviceGetAttribute");
 
     float cb[hsq::kCodebookFloats];
     hsq::device_codebook(cb);
@@ -1762,12 +2136,7 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMalloc(&c->d_rope_hi, hi.size() * 4)) != cudaSuccess) return bail(e, "cudaMalloc(rope)");
     if ((e = cudaMalloc(&c->d_rope_lo, lo.size() * 4)) != cudaSuccess) return bail(e, "cudaMalloc(rope)");
     if ((e = cudaMalloc(&c->d_scores, bh * c->G_max * 4)) != cudaSuccess) return bail(e, "cudaMalloc(scores)");
-    if ((e = cudaMalloc(&c->d_part, bh * HSQ_MAX_SPLITS * r * hsq::kPartStride * 4)) != cudaSuccess)
-        return bail(e, "cudaMalloc(partials)");
     if ((e = cudaMalloc(&c->d_route_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
-    if ((e = cudaMalloc(&c->d_attn_ctr, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
-    if ((e = cudaMalloc(&c->d_arrive, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
-    if ((e = cudaMalloc(&c->d_gen, bh * 4)) != cudaSuccess) return bail(e, "cudaMalloc(counters)");
     if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(prefix)");
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
@@ -1777,9 +2146,6 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMemcpy(c->d_rope_lo, lo.data(), lo.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(e, "upload");
     if ((e = cudaMemset(c->d_route_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
-    if ((e = cudaMemset(c->d_attn_ctr, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
-    if ((e = cudaMemset(c->d_arrive, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
-    if ((e = cudaMemset(c->d_gen, 0, bh * 4)) != cudaSuccess) return bail(e, "cudaMemset");
     if ((e = cudaMemset(c->d_err, 0, 4)) != cudaSuccess) return bail(e, "cudaMemset");
 
     *out = c;
@@ -1863,9 +2229,10 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dispatch_rn(ctx->r, v.N, [&](auto Ri, auto Ni) -> hsq_status {
         constexpr int R = decltype(Ri)::value, N = decltype(Ni)::value;
-        DecodeArgs a{q, pos, const_cast<int32_t*>(sel), out, nullptr, ctx->d_part, ctx->d_attn_ctr,
-                     ctx->d_arrive, ctx->d_gen, ctx->d_err, fit_splits<R, N, false>(ctx, v.B, v.G), staged ? 1 : 0};
-        return launch_decode<R, N, false>(ctx, v, a, s);
+        const hsq_ctx::Plan p = decode_plan<R, N, false>(ctx, v.B, v.T);
+        if (p.S == 0) return fail(ctx, HSQ_ERR_UNSUPPORTED, "decode kernel cannot be launched for this shape");
+        DecodeArgs a{q, pos, const_cast<int32_t*>(sel), out, ctx->d_err, staged ? 1 : 0, 0};
+        return launch_decode<R, N, false>(ctx, v, a, p, s);
     });
 }
 
@@ -1880,12 +2247,11 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     bool fused = false;
     st = dispatch_rn(ctx->r, v.N, [&](auto Ri, auto Ni) -> hsq_status {
         constexpr int R = decltype(Ri)::value, N = decltype(Ni)::value;
-        const int S = fit_splits<R, N, true>(ctx, v.B, v.G);
-        if (S == 0) return HSQ_OK;  // the grid cannot be co-resident: two kernels below
+        const hsq_ctx::Plan p = decode_plan<R, N, true>(ctx, v.B, v.T);
+        if (p.S == 0) return HSQ_OK;  // no launchable cluster shape: two kernels below
         fused = true;
-        DecodeArgs a{q, pos, sel, out, ctx->d_scores, ctx->d_part, ctx->d_attn_ctr, ctx->d_arrive, ctx->d_gen,
-                     ctx->d_err, S, 0};
-        return launch_decode<R, N, true>(ctx, v, a, s);
+        DecodeArgs a{q, pos, sel, out, ctx->d_err, 0, 0};
+        return launch_decode<R, N, true>(ctx, v, a, p, s);
     });
     if (st != HSQ_OK || fused) return st;
     st = hsq_route(ctx, cache, q, pos, sel, nullptr, stream);

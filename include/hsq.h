@@ -68,15 +68,15 @@ typedef enum {
 
 typedef enum { HSQ_DTYPE_F32 = 0, HSQ_DTYPE_BF16 = 1 } hsq_dtype;
 
-enum { HSQ_HEAD_DIM = 128, HSQ_MAX_BETA = 512, HSQ_MAX_SPLITS = 64 };
+enum { HSQ_HEAD_DIM = 128, HSQ_MAX_BETA = 512, HSQ_MAX_SPLITS = 16 };
 
 /* Bits of the device error word (hsq_sync_status fills *device_word). */
 enum {
     HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
     HSQ_DEVERR_POS = 2,       /* position outside [0, max_pos): clamped */
     HSQ_DEVERR_L1_OVER = 4,   /* more L1 tokens than max_l1: extra tokens dropped from L1 */
-    HSQ_DEVERR_WAIT = 8       /* the decode step's wait for its selection ran out (bounded):
-                                 that step's output is not valid */
+    HSQ_DEVERR_WAIT = 8       /* reserved: no kernel of this version waits on another CTA
+                                 outside its own thread-block cluster */
 };
 
 /* Flags of hsq_decode_attn. */
@@ -105,7 +105,8 @@ typedef struct hsq_config {
     int max_ctx;        /* largest T */
     int max_l1;         /* L1 slots per sequence */
     int max_pos;        /* exclusive bound on positions (context + decode steps), <= 2^24 */
-    int n_splits;       /* decode-attention splits per (b, KV head); 0 = automatic */
+    int n_splits;       /* decode splits (CTAs of one thread-block cluster) per (b, KV head):
+                           0 = automatic, else an upper bound in [1, HSQ_MAX_SPLITS] */
 } hsq_config;
 
 /*
@@ -254,11 +255,12 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  * hsq_decode_step -- one whole decode step of one layer: routing, top-beta
  *   selection, gather of the selected L3 records and the union attention.
  *   sel is written exactly as hsq_route writes it (same scores, same
- *   selection) and out as hsq_decode_attn computes it.  When the B*Hkv*S
- *   split grid fits on the GPU at once this is a single cooperative kernel
- *   (the splits of a (b, h) meet at a bounded device-side wait for their
- *   selection); otherwise it runs hsq_route then hsq_decode_attn.
- *   Errors as the two calls; a wait that runs out sets HSQ_DEVERR_WAIT.
+ *   selection) and out as hsq_decode_attn computes it.  One kernel: the S
+ *   splits of a (b, h) form one thread-block cluster and select the top
+ *   beta together through distributed shared memory, so no CTA waits on a
+ *   CTA outside its cluster and the grid need not be co-resident.  Only if
+ *   no cluster shape can be launched does it run hsq_route then
+ *   hsq_decode_attn.  Errors as the two calls.
  */
 hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
                            const int32_t* pos, int32_t* sel, float* out, hsq_stream_t stream);

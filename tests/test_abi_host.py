@@ -66,7 +66,7 @@ def test_cache_sizes(H):
 
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 64), ("group_n", 12), ("beta", 0), ("beta", 513), ("bits_l1l3", 8),
-    ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 65),
+    ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 17),
     ("n_q_heads", 12),
 ])
 def test_invalid_config_rejected(H, field, value):
