@@ -1,8 +1,8 @@
 """Build the HSQ CUDA library in-tree: ``_build/libhsq.so`` next to this file.
 
-Two translation units (host C++ and the sm_103a kernels) are compiled in
-parallel with nvcc and linked into one shared library with a C ABI
-(``include/hsq.h``).  Run as ``python -m hierarchical_kv_cache_hsq_gb300.build``.
+The translation units (host C++, the sm_103a kernels, and the decode step
+once per head ratio) are compiled in parallel with nvcc and linked into one
+shared library with a C ABI (``include/hsq.h``).  Run as ``python -m hierarchical_kv_cache_hsq_gb300.build``.
 """
 
 from __future__ import annotations
@@ -22,7 +22,8 @@ LIB = os.path.join(BUILD, "libhsq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["hsq_host.cpp", "hsq_kernels.cu"]
+SOURCES = ["hsq_kernels.cu", "hsq_decode_r4.cu", "hsq_decode_r8.cu", "hsq_decode_r5.cu", "hsq_decode_r2.cu",
+           "hsq_decode_r1.cu", "hsq_host.cpp"]
 
 
 def nvcc() -> str:

@@ -1,0 +1,779 @@
+// The fused decode-step kernel (one thread-block cluster per (b, KV head))
+// and its host-side launch plan.  Included once per head ratio by
+// hsq_decode_r<R>.cu, which instantiates it for R (and both group sizes).
+//
+// Decode process: Tamarin (HSQ) technical summary (gist.science
+// rs-10297225), section 2 (route against the L2 summaries, fetch and
+// dequantise the selected L3 originals, re-rotate to position, attend over
+// the union with the fetched summaries masked).
+#pragma once
+
+#include <algorithm>
+
+#include "hsq_device.cuh"
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Decode step: one thread-block cluster per (b, KV head).  grid = (S, B*Hkv),
+// cluster = (S, 1, 1), 256 threads per CTA.  Split s owns a contiguous share
+// of the L2 groups and of the L1 slots of its (b, h) and an even share of the
+// selected records.  The splits of a (b, h) exchange data only through
+// distributed shared memory, by pushing (remote stores), each exchange
+// closed by one cluster barrier:
+//   1. stage the split's L2 summaries, L1 tokens, the sequence's L1 bitmap,
+//      the codebook and the RoPE angle rows it may need (cp.async);
+//   2. rotate the query heads; per-head logits of the split's L2 groups and,
+//      with kRoute, the routing score n_g * (sum_j q~_j) . c3[codes] (the
+//      arithmetic of the routing kernel, so both select the same groups),
+//      whose key is pushed into every split's copy of the score array;
+//   3. kRoute: after one barrier every split holds all G keys and runs the
+//      same block-wide top-beta (identical result in every split);
+//      otherwise the caller's selection is validated and used;
+//   4. gather this split's share of the selected L3 records (zero copy when
+//      L3 is host memory) and, while they travel, add the L1 tokens and the
+//      unselected non-empty summaries;
+//   5. recovered tokens: dequantise, inverse WHT, RoPE at the token's
+//      position (per-record base angle plus a small offset), logits against
+//      the RoPE'd queries, values kept in the rotated frame;
+//   6. the CTA's softmax partial of query head j is pushed to split j mod S,
+//      which merges the S partials after the last barrier, rotates the
+//      output back to the original frame and stores it.
+// Each half-warp runs its own online softmax over its entries, two entries
+// per step.  Every loop has warp-uniform bounds (entries past the end are
+// computed on a clamped index and masked), so all shuffles run on full
+// warps.  kStaged: the split's L2 / L1 slices, the L1 bitmap row and the
+// split's L2 logits live in shared memory; without it (contexts too long for
+// shared memory) they are read in place from global memory and the L2
+// logits are recomputed.
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxSplits = 16;   // largest (non-portable) cluster
+enum : int { kStageL2 = 1, kKeepLogits = 2, kStageL1 = 4, kStageBitmap = 8 };
+
+struct DecodeArgs {
+    const float* q; const int32_t* pos; int32_t* sel; float* out; int* err; int from_staging;
+};
+
+constexpr int kStagedFlags = kStageL2 | kKeepLogits | kStageL1 | kStageBitmap;
+
+struct DecodeLayout {
+    int span, l1span, nlev, nb0;
+    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, sel, mask, bitmap;
+    unsigned lev, b0, off, base, rbits, inbox, rec, total;
+};
+
+// 4-bit digits of p >> 8 for cache positions p < T
+__host__ __device__ inline int rope_levels(int T) {
+    int hi = (T - 1) >> 8, n = 0;
+    while (hi > 0) {
+        ++n;
+        hi >>= 4;
+    }
+    return n;
+}
+
+template <int R, int N>
+__host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int max_l1, int beta, bool route,
+                                                      int flags) {
+    DecodeLayout L;
+    L.span = (G + S - 1) / S;
+    L.l1span = (max_l1 + S - 1) / S;
+    L.nlev = rope_levels(T);
+    L.nb0 = 256 / N;
+    constexpr int kBatchRecs = kFetchBatchBytes / (N * 136);
+    const size_t row = (size_t)kDim * 4;
+    size_t o = 0;
+    L.l2k = L.l2v = L.l2kn = L.l2vn = L.cnt = L.l1k = L.l1v = L.l1kn = L.l1vn = L.logit = L.bitmap = 0;
+    if (flags & kStageL2) {
+        L.l2k = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+        L.l2v = (unsigned)o; o = al16(o + (size_t)L.span * 48);
+        L.l2kn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+        L.l2vn = (unsigned)o; o = al16(o + (size_t)L.span * 4);
+        L.cnt = (unsigned)o; o = al16(o + (size_t)L.span);
+    }
+    if (flags & kStageL1) {
+        L.l1k = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+        L.l1v = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
+        L.l1kn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+        L.l1vn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+    }
+    if (flags & kKeepLogits) { L.logit = (unsigned)o; o = al16(o + (size_t)L.span * R * 4); }
+    if (flags & kStageBitmap) { L.bitmap = (unsigned)o; o = al16(o + (size_t)((T + 31) / 32) * 4); }
+    L.sel = (unsigned)o; o = al16(o + (size_t)beta * 4);
+    L.mask = (unsigned)o; o = al16(o + (size_t)((L.span + 31) / 32) * 4);
+    L.lev = (unsigned)o; o = al16(o + (size_t)L.nlev * 16 * row);
+    L.b0 = (unsigned)o; o = al16(o + (size_t)L.nb0 * row);
+    L.off = (unsigned)o; o = al16(o + (size_t)N * row);
+    L.base = (unsigned)o; o = al16(o + (size_t)kBatchRecs * row);
+    L.rbits = (unsigned)o; o = al16(o + (size_t)kBatchRecs * 4);
+    L.inbox = (unsigned)o; o = al16(o + (size_t)((R + S - 1) / S) * S * hsq::kPartStride * 4);
+    // one region, used in turn for: every split's routing keys (until the
+    // selection is made), the gathered L3 records, the warp partials
+    size_t rec = kFetchBatchBytes;
+    const size_t merge = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
+    if (merge > rec) rec = merge;
+    if (route && (size_t)G * 4 > rec) rec = (size_t)G * 4;
+    L.rec = (unsigned)o; o = al16(o + rec);
+    L.total = (unsigned)o;
+    return L;
+}
+
+// 2^x by the special-function unit (relative error about 2^-22); -inf gives 0
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int R>
+struct Softmax {
+    float m[R], l[R], acc[R][8];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = 0.f;
+        }
+    }
+    // add up to two entries with log2-domain logits xa[j], xb[j] and values va, vb
+    __device__ __forceinline__ void add2(const float xa[R], const float va[8], bool oka, const float xb[R],
+                                         const float vb[8], bool okb) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const float a = oka ? xa[j] : -INFINITY, b = okb ? xb[j] : -INFINITY;
+            const float mn = fmaxf(m[j], fmaxf(a, b));
+            if (mn > m[j]) {
+                const float corr = fast_exp2(m[j] - mn);
+                l[j] *= corr;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[j][i] *= corr;
+                m[j] = mn;
+            }
+            const float pa = oka ? fast_exp2(a - m[j]) : 0.f;
+            const float pb = okb ? fast_exp2(b - m[j]) : 0.f;
+            l[j] += pa + pb;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(pa, va[i], fmaf(pb, vb[i], acc[j][i]));
+        }
+    }
+};
+
+__device__ __forceinline__ float merge_weight(float mi, float M) {
+    return mi == -INFINITY ? 0.f : fast_exp2(mi - M);
+}
+
+// (c1, s1) <- cos/sin of the sum of the two angles, 4 frequencies
+__device__ __forceinline__ void angle_add4(float4& c1, float4& s1, const float4 c2, const float4 s2) {
+    const float4 c = make_float4(fmaf(c1.x, c2.x, -s1.x * s2.x), fmaf(c1.y, c2.y, -s1.y * s2.y),
+                                 fmaf(c1.z, c2.z, -s1.z * s2.z), fmaf(c1.w, c2.w, -s1.w * s2.w));
+    const float4 s = make_float4(fmaf(s1.x, c2.x, c1.x * s2.x), fmaf(s1.y, c2.y, c1.y * s2.y),
+                                 fmaf(s1.z, c2.z, c1.z * s2.z), fmaf(s1.w, c2.w, c1.w * s2.w));
+    c1 = c;
+    s1 = s;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Dot products of two 128-vectors (a, b; this lane's 8 dims each) with the R
+// query heads.  Returns the lane's share of the 2R sums (spread_sum): index
+// idx < R is head idx of a, R <= idx < 2R head idx - R of b, idx >= 2R unused.
+template <int R>
+__device__ __forceinline__ float pair_dots(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
+                                           int& idx) {
+    constexpr int K = pow2_ceil(2 * R);
+    float p[K];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float da = 0.f, db = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            da = fmaf(q[j][k], ka[k], da);
+            db = fmaf(q[j][k], kb[k], db);
+        }
+        p[j] = da;
+        p[R + j] = db;
+    }
+#pragma unroll
+    for (int j = 2 * R; j < K; ++j) p[j] = 0.f;
+    idx = spread_index<K>(hlane());
+    return spread_sum<K>(p);
+}
+
+// The 2R logits of a pair in every lane: xa[j] = scale * (q_j . ka), xb likewise.
+// xs: this half-warp's 16-float scratch in shared memory.
+template <int R>
+__device__ __forceinline__ void pair_logits(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
+                                            float scale, float* xs, float (&xa)[R], float (&xb)[R]) {
+    int idx;
+    const float d = pair_dots<R>(q, ka, kb, idx);
+    __syncwarp();  // the previous pair's reads are done
+    if (idx < 2 * R) xs[idx] = d * scale;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        xa[j] = xs[j];
+        xb[j] = xs[R + j];
+    }
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+}
+
+template <int R, int N, bool kRoute, bool kStaged>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
+    namespace cgx = cooperative_groups;
+    extern __shared__ __align__(16) uint8_t s_dyn[];
+    __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
+    __shared__ __align__(16) float s_qt[R][kDim];
+    __shared__ __align__(16) float s_qr[R][kDim];
+    __shared__ __align__(16) float s_x[kHalves][16];
+    __shared__ SelectSmem s_ss;
+
+    constexpr int RB = N * 136;
+    constexpr int kBatchRecs = kFetchBatchBytes / RB;
+    constexpr int kRecChunks = RB / 16;
+
+    // first phase of the cluster barrier: every CTA of the cluster has started
+    // (completed by cluster_wait before the first remote store)
+    cluster_arrive_relaxed();
+    cgx::cluster_group cluster = cgx::this_cluster();
+    const int S = (int)cluster.num_blocks();
+    const int s = (int)cluster.block_rank();
+    const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
+    const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
+    constexpr int fl = kStaged ? kStagedFlags : 0;
+    const DecodeLayout L = decode_layout<R, N>(c.G, c.T, S, c.max_l1, c.beta, kRoute, fl);
+
+    const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
+    const int n2 = g1 - g0;
+    const int cnt1 = min(__ldg(c.l1_count + b), c.max_l1);
+    const int e0 = (int)((long long)cnt1 * s / S), e1 = (int)((long long)cnt1 * (s + 1) / S);
+    const int n1 = e1 - e0;
+    const int f0 = (int)((long long)c.beta * s / S), f1 = (int)((long long)c.beta * (s + 1) / S);
+    const int nfetch = f1 - f0;
+
+    // inputs: staged copies in shared memory, or read in place
+    const uint8_t* g_l2k = c.l2_kc + ((size_t)bh * c.G + g0) * 48;
+    const uint8_t* g_l2v = c.l2_vc + ((size_t)bh * c.G + g0) * 48;
+    const float* g_l2kn = c.l2_kn + (size_t)bh * c.G + g0;
+    const float* g_l2vn = c.l2_vn + (size_t)bh * c.G + g0;
+    const uint8_t* g_cnt = c.l2_cnt + (size_t)b * c.G + g0;
+    const uint8_t* g_l1k = c.l1_kc + ((size_t)bh * c.max_l1 + e0) * 64;
+    const uint8_t* g_l1v = c.l1_vc + ((size_t)bh * c.max_l1 + e0) * 64;
+    const float* g_l1kn = c.l1_kn + (size_t)bh * c.max_l1 + e0;
+    const float* g_l1vn = c.l1_vn + (size_t)bh * c.max_l1 + e0;
+    const uint32_t* g_bitmap = c.l1_bitmap + (size_t)b * c.W;
+    constexpr bool st2 = kStaged, st1 = kStaged, stb = kStaged, keep = kStaged;
+    const uint8_t* p_l2k = st2 ? s_dyn + L.l2k : g_l2k;
+    const uint8_t* p_l2v = st2 ? s_dyn + L.l2v : g_l2v;
+    const float* p_l2kn = st2 ? reinterpret_cast<const float*>(s_dyn + L.l2kn) : g_l2kn;
+    const float* p_l2vn = st2 ? reinterpret_cast<const float*>(s_dyn + L.l2vn) : g_l2vn;
+    const uint8_t* p_cnt = st2 ? s_dyn + L.cnt : g_cnt;
+    const uint8_t* p_l1k = st1 ? s_dyn + L.l1k : g_l1k;
+    const uint8_t* p_l1v = st1 ? s_dyn + L.l1v : g_l1v;
+    const float* p_l1kn = st1 ? reinterpret_cast<const float*>(s_dyn + L.l1kn) : g_l1kn;
+    const float* p_l1vn = st1 ? reinterpret_cast<const float*>(s_dyn + L.l1vn) : g_l1vn;
+    const uint32_t* p_bitmap = stb ? reinterpret_cast<const uint32_t*>(s_dyn + L.bitmap) : g_bitmap;
+    float* s_logit = reinterpret_cast<float*>(s_dyn + L.logit);
+    int* s_sel = reinterpret_cast<int*>(s_dyn + L.sel);
+    uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_dyn + L.mask);
+    float* s_lev = reinterpret_cast<float*>(s_dyn + L.lev);
+    float* s_b0 = reinterpret_cast<float*>(s_dyn + L.b0);
+    float* s_off = reinterpret_cast<float*>(s_dyn + L.off);
+    float* s_base = reinterpret_cast<float*>(s_dyn + L.base);
+    uint32_t* s_rbits = reinterpret_cast<uint32_t*>(s_dyn + L.rbits);
+    float* s_inbox = reinterpret_cast<float*>(s_dyn + L.inbox);
+    uint8_t* s_rec = s_dyn + L.rec;
+    uint32_t* s_all = reinterpret_cast<uint32_t*>(s_dyn + L.rec);  // routing keys of all splits
+    float* xs = &s_x[hw][0];
+
+    // 1. stage the device-resident inputs of this split
+    if constexpr (st2) {
+        stage16(s_dyn + L.l2k, g_l2k, n2 * 48);
+        stage16(s_dyn + L.l2v, g_l2v, n2 * 48);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l2kn), g_l2kn, n2);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l2vn), g_l2vn, n2);
+        for (int i = tid; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
+    }
+    if constexpr (st1) {
+        stage16(s_dyn + L.l1k, g_l1k, n1 * 64);
+        stage16(s_dyn + L.l1v, g_l1v, n1 * 64);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l1kn), g_l1kn, n1);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l1vn), g_l1vn, n1);
+    }
+    if constexpr (stb) stage4(reinterpret_cast<float*>(s_dyn + L.bitmap), reinterpret_cast<const float*>(g_bitmap), c.W);
+    if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
+    // RoPE rows: level k row j = hi[j * 16^k] (angle 256 j 16^k omega), b0 row j = lo[N j], off row n = lo[n]
+    const int n_hi = (tb.max_pos + 255) / 256;
+#pragma unroll 1
+    for (int i = tid; i < L.nlev * 16 * 32; i += kThreads) {
+        const int rowi = i >> 5, k = rowi >> 4, j = rowi & 15;
+        const int src = j << (4 * k);
+        if (src < n_hi) cp_async16(s_lev + 4 * i, tb.rope_hi + (size_t)src * kDim + 4 * (i & 31));
+    }
+#pragma unroll 1
+    for (int i = tid; i < L.nb0 * 32; i += kThreads)
+        cp_async16(s_b0 + 4 * i, tb.rope_lo + (size_t)(N * (i >> 5)) * kDim + 4 * (i & 31));
+    stage16(s_off, tb.rope_lo, N * kDim * 4);
+    for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
+    float sg[8];
+    load_signs_global(sg, c.signs);
+
+    // 2. query heads of this KV head: RoPE'd (original frame) and rotated
+    const int pos = checked_pos(__ldg(a.pos + b), tb, a.err);
+    prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, pos, sg, tb, s_qt, s_qr);
+    cp_async_wait_all();
+    __syncthreads();
+
+    const float* c4 = s_cb;
+    const float* c3 = s_cb + 32;
+    float qt[R][8];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            qt[j][k] = s_qt[j][4 * l + k];
+            qt[j][4 + k] = s_qt[j][64 + 4 * l + k];
+        }
+    }
+    if (kRoute) cluster_wait();  // every CTA of the cluster runs: remote stores may start
+    if constexpr (kRoute || keep) {
+        float gq[8];
+        if (kRoute) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < R; ++jj) {
+                    s0 += s_qt[jj][4 * l + k];
+                    s1 += s_qt[jj][64 + 4 * l + k];
+                }
+                gq[k] = s0;
+                gq[4 + k] = s1;
+            }
+        }
+        uint32_t* dst = kRoute && l < S ? cluster.map_shared_rank(s_all, l) + g0 : nullptr;
+#pragma unroll 1
+        for (int blk = 0; blk < n2; blk += 2 * kHalves) {
+            const int ia = blk + hw, ib = ia + kHalves;
+            const int ja = min(ia, n2 - 1), jb = min(ib, n2 - 1);
+            float va[8], vb[8];
+            unpack3_smem(p_l2k + ja * 48, c3, 1.0f, va);
+            unpack3_smem(p_l2k + jb * 48, c3, 1.0f, vb);
+            const float kna = p_l2kn[ja], knb = p_l2kn[jb];
+            if (kRoute) {
+                float sa, sb;
+                route_pair(gq, va, vb, sa, sb);
+                const uint32_t ka = p_cnt[ja] > 0 ? ordered_key(kna * sa) : 0u;
+                const uint32_t kb = p_cnt[jb] > 0 ? ordered_key(knb * sb) : 0u;
+                if (dst) {  // lane l < S writes this pair's keys into split l
+                    if (ia < n2) dst[ia] = ka;
+                    if (ib < n2) dst[ib] = kb;
+                }
+            }
+            if constexpr (keep) {
+                int idx;
+                const float d = pair_dots<R>(qt, va, vb, idx);
+                if (idx < R) {
+                    if (ia < n2) s_logit[ia * R + idx] = kna * d * kLogitScaleLog2;
+                } else if (idx < 2 * R) {
+                    if (ib < n2) s_logit[ib * R + idx - R] = knb * d * kLogitScaleLog2;
+                }
+            }
+        }
+    }
+
+    // 3. the selection of this (b, h)
+    if (kRoute) {
+        cluster.sync();  // every split's keys are in every split
+        select_top_beta(s_all, c.G, c.beta, s_sel, s_ss);
+        __syncthreads();
+        if (s == 0)
+            for (int i = tid; i < c.beta; i += kThreads) a.sel[(size_t)bh * c.beta + i] = s_sel[i];
+    } else {
+        for (int i = tid; i < c.beta; i += kThreads) s_sel[i] = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
+        __syncthreads();
+    }
+    for (int i = tid; i < c.beta; i += kThreads) {
+        const int g = s_sel[i];
+        if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
+    }
+
+    // 4. gather this split's records; meanwhile L1 tokens and unselected summaries
+    uint4 pre[kMaxFetchChunksPerThread];
+    auto issue = [&](int r0, int nrec) {
+#pragma unroll
+        for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
+            const int ch = tid + k * kThreads;
+            pre[k] = make_uint4(0, 0, 0, 0);
+            if (ch < nrec * kRecChunks) {
+                const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
+                const int i = r0 + rec;
+                const int g = s_sel[i];
+                if (g >= 0) {
+                    const uint8_t* base = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
+                                                         : c.l3 + ((size_t)bh * c.G + g) * RB;
+                    pre[k] = __ldcg(reinterpret_cast<const uint4*>(base) + off);
+                }
+            }
+        }
+    };
+    // per record: cos/sin of its base angle g N omega (staged rows only) and its L1 bits
+    auto meta = [&](int r0, int nrec) {
+        if (hw < nrec) {
+            const int g = s_sel[r0 + hw];
+            if (g >= 0) {
+                const int p0 = g * N;
+                const float* br = s_b0 + ((p0 & 255) / N) * kDim;
+                float4 cs = *reinterpret_cast<const float4*>(br + 4 * l);
+                float4 sn = *reinterpret_cast<const float4*>(br + 64 + 4 * l);
+#pragma unroll 1
+                for (int k = 0; k < L.nlev; ++k) {  // one 4-bit digit of p0 >> 8 per level
+                    const int j = (p0 >> (8 + 4 * k)) & 15;
+                    if (j) {
+                        const float* lr = s_lev + (k * 16 + j) * kDim;
+                        angle_add4(cs, sn, *reinterpret_cast<const float4*>(lr + 4 * l),
+                                   *reinterpret_cast<const float4*>(lr + 64 + 4 * l));
+                    }
+                }
+                *reinterpret_cast<float4*>(s_base + hw * kDim + 4 * l) = cs;
+                *reinterpret_cast<float4*>(s_base + hw * kDim + 64 + 4 * l) = sn;
+                if (l == 0)
+                    s_rbits[hw] = (p_bitmap[p0 >> 5] >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
+            }
+        }
+    };
+    const int nb0 = min(nfetch, kBatchRecs);
+    if (nb0 > 0) {
+        issue(f0, nb0);
+        meta(f0, nb0);
+    }
+    __syncthreads();  // s_mask complete
+
+    Softmax<R> sm;
+    sm.init();
+#pragma unroll 1
+    for (int blk = 0; blk < n1; blk += 2 * kHalves) {
+        const int ea = blk + hw, eb = ea + kHalves;
+        const int ja = min(ea, n1 - 1), jb = min(eb, n1 - 1);
+        float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
+        const uint16_t* kra = reinterpret_cast<const uint16_t*>(p_l1k + ja * 64);
+        const uint16_t* krb = reinterpret_cast<const uint16_t*>(p_l1k + jb * 64);
+        const uint16_t* vra = reinterpret_cast<const uint16_t*>(p_l1v + ja * 64);
+        const uint16_t* vrb = reinterpret_cast<const uint16_t*>(p_l1v + jb * 64);
+        unpack4(kra[l], kra[16 + l], c4, p_l1kn[ja], ka);
+        unpack4(krb[l], krb[16 + l], c4, p_l1kn[jb], kb);
+        pair_logits<R>(qt, ka, kb, kLogitScaleLog2, xs, xa, xb);
+        unpack4(vra[l], vra[16 + l], c4, p_l1vn[ja], va);
+        unpack4(vrb[l], vrb[16 + l], c4, p_l1vn[jb], vb);
+        sm.add2(xa, va, ea < n1, xb, vb, eb < n1);
+    }
+#pragma unroll 1
+    for (int blk = 0; blk < n2; blk += 2 * kHalves) {
+        const int ia = blk + hw, ib = ia + kHalves;
+        const int ja = min(ia, n2 - 1), jb = min(ib, n2 - 1);
+        const bool oka = ia < n2 && p_cnt[ja] > 0 && !((s_mask[ja >> 5] >> (ja & 31)) & 1u);
+        const bool okb = ib < n2 && p_cnt[jb] > 0 && !((s_mask[jb >> 5] >> (jb & 31)) & 1u);
+        if (!__any_sync(kFull, oka || okb)) continue;
+        float va[8], vb[8], xa[R], xb[R];
+        if constexpr (keep) {
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                xa[j] = s_logit[ja * R + j];
+                xb[j] = s_logit[jb * R + j];
+            }
+        } else {
+            float ka[8], kb[8];
+            unpack3_smem(p_l2k + ja * 48, c3, p_l2kn[ja], ka);
+            unpack3_smem(p_l2k + jb * 48, c3, p_l2kn[jb], kb);
+            pair_logits<R>(qt, ka, kb, kLogitScaleLog2, xs, xa, xb);
+        }
+        unpack3_smem(p_l2v + ja * 48, c3, p_l2vn[ja], va);
+        unpack3_smem(p_l2v + jb * 48, c3, p_l2vn[jb], vb);
+        sm.add2(xa, va, oka, xb, vb, okb);
+    }
+
+    // 5. recovered tokens of the selected groups
+    if (nfetch > 0) {
+        float qr[R][8];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                qr[j][k] = s_qr[j][4 * l + k];
+                qr[j][4 + k] = s_qr[j][64 + 4 * l + k];
+            }
+        }
+#pragma unroll 1
+        for (int r0 = f0; r0 < f1; r0 += kBatchRecs) {
+            const int nb = min(kBatchRecs, f1 - r0);
+            __syncthreads();  // previous batch consumed, this batch's meta written
+#pragma unroll
+            for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
+                const int ch = tid + k * kThreads;
+                if (ch < nb * kRecChunks) reinterpret_cast<uint4*>(s_rec)[ch] = pre[k];
+            }
+            __syncthreads();
+            issue(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));  // no-op past the last batch
+            // one recovered token: validity, RoPE'd key and rotated-frame value
+            auto token = [&](int u, float kv[8], float vv[8]) -> bool {
+                const int rec = u / N, n = u - rec * N;
+                const int g = s_sel[r0 + rec];
+                const int t = g * N + n;
+                const bool ok = g >= 0 && t < c.T && !((s_rbits[rec] >> n) & 1u);
+                const uint8_t* rp = s_rec + rec * RB;
+                const float* norms = reinterpret_cast<const float*>(rp + N * 128);
+                const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
+                const uint16_t* vr = reinterpret_cast<const uint16_t*>(rp + N * 64 + n * 64);
+                unpack4(kr[l], kr[16 + l], c4, 1.0f, kv);
+                fwht(kv, kFull);
+                const float kn = norms[n] * kRsqrtD;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
+                {   // RoPE at t = g N + n: base angle (per record) plus offset n omega
+                    float4 cs = *reinterpret_cast<const float4*>(s_base + rec * kDim + 4 * l);
+                    float4 sn = *reinterpret_cast<const float4*>(s_base + rec * kDim + 64 + 4 * l);
+                    angle_add4(cs, sn, *reinterpret_cast<const float4*>(s_off + n * kDim + 4 * l),
+                               *reinterpret_cast<const float4*>(s_off + n * kDim + 64 + 4 * l));
+                    const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float lo = kv[k], hi = kv[4 + k];
+                        kv[k] = fmaf(lo, cv[k], -hi * sv[k]);
+                        kv[4 + k] = fmaf(hi, cv[k], lo * sv[k]);
+                    }
+                }
+                unpack4(vr[l], vr[16 + l], c4, norms[N + n], vv);
+                return ok;
+            };
+            const int nt = nb * N;
+#pragma unroll 1
+            for (int blk = 0; blk < nt; blk += 2 * kHalves) {
+                const int ua = blk + hw, ub = ua + kHalves;
+                float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
+                const bool oka = token(min(ua, nt - 1), ka, va) && ua < nt;
+                const bool okb = token(min(ub, nt - 1), kb, vb) && ub < nt;
+                pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
+                sm.add2(xa, va, oka, xb, vb, okb);
+            }
+            __syncthreads();  // (a barrier under a condition costs code size even when uniform)
+            meta(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+        }
+    }
+
+    // 6. merge the two halves of each warp, then the warps, into this split's
+    //    partial, and push query head j's partial to split j mod S
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const float mo = __shfl_xor_sync(kFull, sm.m[j], 16);
+        const float lo = __shfl_xor_sync(kFull, sm.l[j], 16);
+        const float M = fmaxf(sm.m[j], mo);
+        const float ws = merge_weight(sm.m[j], M), wo = merge_weight(mo, M);
+        sm.l[j] = sm.l[j] * ws + lo * wo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float ao = __shfl_xor_sync(kFull, sm.acc[j][i], 16);
+            sm.acc[j][i] = sm.acc[j][i] * ws + ao * wo;
+        }
+        sm.m[j] = M;
+    }
+    __syncthreads();  // the record staging area becomes the warp-partial area
+    float* s_part = reinterpret_cast<float*>(s_rec);  // [8 warps][R][132]
+    if ((tid & 16) == 0) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            float* p = s_part + ((size_t)warp * R + j) * hsq::kPartStride;
+            *reinterpret_cast<float4*>(p + 4 * l) = make_float4(sm.acc[j][0], sm.acc[j][1], sm.acc[j][2], sm.acc[j][3]);
+            *reinterpret_cast<float4*>(p + 64 + 4 * l) = make_float4(sm.acc[j][4], sm.acc[j][5], sm.acc[j][6], sm.acc[j][7]);
+            if (l == 0) { p[128] = sm.m[j]; p[129] = sm.l[j]; }
+        }
+    }
+    __syncthreads();
+    if (!kRoute) cluster_wait();  // every CTA of the cluster runs: remote stores may start
+    if (tid < R * 32) {
+        const int j = tid >> 5, q4 = tid & 31;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, s_part[((size_t)w * R + j) * hsq::kPartStride + 128]);
+        float Lsum = 0.f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const float* p = s_part + ((size_t)w * R + j) * hsq::kPartStride;
+            const float wt = merge_weight(p[128], M);
+            const float4 v = *reinterpret_cast<const float4*>(p + 4 * q4);
+            Lsum += p[129] * wt;
+            A.x += v.x * wt; A.y += v.y * wt; A.z += v.z * wt; A.w += v.w * wt;
+        }
+        float* dst = cluster.map_shared_rank(s_inbox, j % S) + ((size_t)(j / S) * S + s) * hsq::kPartStride;
+        *reinterpret_cast<float4*>(dst + 4 * q4) = A;
+        if (q4 == 0) { dst[128] = M; dst[129] = Lsum; }
+    }
+    cluster.sync();  // every partial is in its owner's inbox; no remote access follows
+
+    // query heads s, s + S, ...: merge the S partials (warp k: head s + k S, 4 dims per lane)
+    float* s_o = s_qr[0];  // [R][128]; the RoPE'd queries are no longer needed
+    const int nmine = (R - s + S - 1) / S;
+    if (nmine > 0) {
+        const int k = min(warp, nmine - 1);
+        const float* in = s_inbox + (size_t)k * S * hsq::kPartStride;
+        const float mr = lane < S ? in[lane * hsq::kPartStride + 128] : -INFINITY;
+        const float lr = lane < S ? in[lane * hsq::kPartStride + 129] : 0.f;
+        const float M = warp_max(mr);
+        const float wr = merge_weight(mr, M);
+        const float Lsum = warp_sum(lr * wr);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int r = 0; r < S; ++r) {
+            const float wt = __shfl_sync(kFull, wr, r);
+            const float4 x = *reinterpret_cast<const float4*>(in + r * hsq::kPartStride + 4 * lane);
+            o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
+        }
+        const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+        if (warp < nmine)
+            *reinterpret_cast<float4*>(s_o + k * kDim + 4 * lane) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        __syncthreads();
+        const int kk = min(hw, nmine - 1);
+        float ov[8];
+        load_f32x8_smem(s_o + kk * kDim, ov);
+        fwht(ov, kFull);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ov[i] *= sg[i] * kRsqrtD;
+        if (hw < nmine) store_f32x8(a.out + ((size_t)b * c.Hq + h * R + s + kk * S) * kDim, ov);
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Host side: launch plan and launch.
+// ---------------------------------------------------------------------------
+
+cudaLaunchConfig_t decode_config(int S, int bh, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(S, bh, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = st;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    return lc;
+}
+
+// Best cluster size for one kernel variant: the largest S <= s_hi whose
+// bh clusters are all resident at once (one wave); when none gives one wave,
+// the smallest S that can launch (least per-head overhead across waves).  A
+// fixed n_splits takes the largest launchable S.  0: nothing launchable.
+template <int R, int N, bool kRoute, bool kStaged>
+int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
+    const void* fn = (const void*)decode_kernel<R, N, kRoute, kStaged>;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
+    if (hsq::allow_big_clusters(fn, ctx->device) != cudaSuccess) return 0;
+    const size_t cap = (size_t)ctx->smem_optin > fa.sharedSizeBytes ? ctx->smem_optin - fa.sharedSizeBytes : 0;
+    const int fl = kStaged ? kStagedFlags : 0;
+    int last = 0;
+    for (int S = s_hi; S >= 1; --S) {
+        const size_t smem = decode_layout<R, N>(G, T, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute, fl).total;
+        if (smem > cap) continue;
+        if (hsq::raise_smem_limit(fn, ctx->device, smem) != cudaSuccess) continue;
+        cudaLaunchAttribute at[1];
+        cudaLaunchConfig_t lc = decode_config(S, bh, smem, 0, at);
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, fn, &lc) != cudaSuccess || nc < 1) continue;
+        if (ctx->cfg.n_splits > 0 || nc >= bh) return S;
+        last = S;
+    }
+    return last;
+}
+
+// Launch plan for B sequences of T tokens (cached per shape): staged inputs
+// when some cluster size fits shared memory, else in place.
+template <int R, int N, bool kRoute>
+hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T) {
+    for (const auto& e : ctx->plans)
+        if (e.B == B && e.T == T && e.route == (int)kRoute) return e;
+    const int G = hsq::groups_of(T, N);
+    const int bh = B * ctx->cfg.n_kv_heads;
+    const int fixed = ctx->cfg.n_splits;
+    const int s_hi = std::max(1, std::min(fixed > 0 ? fixed : kMaxSplits, std::max(G, 1)));
+    hsq_ctx::Plan plan{B, T, (int)kRoute, 0, 1};
+    plan.S = best_splits<R, N, kRoute, true>(ctx, G, T, bh, s_hi);
+    if (plan.S == 0) {
+        plan.staged = 0;
+        plan.S = best_splits<R, N, kRoute, false>(ctx, G, T, bh, s_hi);
+    }
+    cudaGetLastError();
+    ctx->plans.push_back(plan);
+    return plan;
+}
+
+template <int R, int N, bool kRoute, bool kStaged>
+hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
+    const DecodeLayout L =
+        decode_layout<R, N>(v.G, v.T, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
+    const void* fn = (const void*)decode_kernel<R, N, kRoute, kStaged>;
+    cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
+    if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
+    cudaLaunchAttribute at[1];
+    const cudaLaunchConfig_t lc = decode_config(S, v.B * v.Hkv, L.total, st, at);
+    const Tables tb = make_tables(ctx);
+    e = cudaLaunchKernelEx(&lc, decode_kernel<R, N, kRoute, kStaged>, v, a, tb);
+    if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "decode launch");
+    return HSQ_OK;
+}
+
+template <int R, int N>
+hsq_status decode_run_n(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, bool route, cudaStream_t st,
+                        bool* launched) {
+    *launched = false;
+    const hsq_ctx::Plan p = route ? decode_plan<R, N, true>(ctx, v.B, v.T) : decode_plan<R, N, false>(ctx, v.B, v.T);
+    if (p.S == 0) return HSQ_OK;
+    *launched = true;
+    if (route) return p.staged ? launch_decode<R, N, true, true>(ctx, v, a, p.S, st)
+                               : launch_decode<R, N, true, false>(ctx, v, a, p.S, st);
+    return p.staged ? launch_decode<R, N, false, true>(ctx, v, a, p.S, st)
+                    : launch_decode<R, N, false, false>(ctx, v, a, p.S, st);
+}
+
+template <int R>
+hsq_status decode_run(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos, int32_t* sel,
+                      float* out, bool route, bool from_staging, cudaStream_t st, bool* launched) {
+    const CacheView v = make_view(ctx, cache);
+    const DecodeArgs a{q, pos, sel, out, ctx->d_err, from_staging ? 1 : 0};
+    return v.N == 16 ? decode_run_n<R, 16>(ctx, v, a, route, st, launched)
+                     : decode_run_n<R, 8>(ctx, v, a, route, st, launched);
+}
+
+}  // namespace
+
+// Instantiates the decode step for head ratio R as hsq::decode_run_r<R>.
+#define HSQ_DEFINE_DECODE(R)                                                                              \
+    namespace hsq {                                                                                       \
+    hsq_status decode_run_r##R(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,  \
+                               int32_t* sel, float* out, bool route, bool from_staging, cudaStream_t st,   \
+                               bool* launched) {                                                          \
+        return decode_run<R>(ctx, cache, q, pos, sel, out, route, from_staging, st, launched);            \
+    }                                                                                                     \
+    }
