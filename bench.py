@@ -1,10 +1,11 @@
 #!/usr/bin/env python
 """HSQ decode-step benchmark on the Qwen3-8B-shaped 32K-context workload.
 
-One step = one decode step of one layer: routing + top-beta selection
-(hsq_route) and the union attention with the selected L3 groups gathered
-in-kernel from pinned host memory (hsq_decode_attn).  Steps run strictly in
-order; each step uses a fresh query (the workload's 512 queries, cycled).
+One step = one decode step of one layer through hsq_decode_step: routing,
+top-beta selection, the gather of the selected L3 groups from pinned host
+memory and the union attention, all in one kernel launch.  Steps run
+strictly in order; each step uses a fresh query (the workload's 512
+queries, cycled).
 Between timed steps a 256 MiB device buffer is written (evicting L2) and a
 second 256 MiB buffer is read, so every step starts with a cold L2 that holds
 only clean lines -- as after a model's weight reads -- and no write-back of
@@ -24,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -97,7 +99,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join("/tmp", f"hsq_clocks_{os.getpid()}.csv")
+        fd, self.path = tempfile.mkstemp(prefix="hsq_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
@@ -149,6 +152,35 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_qwen3_8b_32k.traffic.txt")
+KERNEL_SOURCES = ("hsq_device.cuh", "hsq_decode.cuh")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "hierarchical_kv_cache_hsq_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when the kernel source has changed since the capture."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu capture recorded"
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_sources_sha256") != kernel_source_hash():
+        return None, "kernel changed since the last ncu capture"
+    return float(kv["dram_bytes_per_launch"]), "ncu dram__bytes_read.sum + dram__bytes_write.sum (profiles/)"
+
+
 def link_peak(torch, nbytes=1 << 30, reps=5):
     """Pinned host <-> device copy bandwidth (GB/s), best of `reps`."""
     h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
@@ -192,6 +224,18 @@ def cpu_oracle_sample(w, li, q, pos, seconds: float):
     return {"value": 1.0 / full, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"KV head 0 of {w.name}: encode of that head ({enc_s:.2f} s, not in the value) then "
                       f"{n} decode steps of that head ({spent:.1f} s); step time x {w.B * w.Hkv} heads"}
+
+
+def aggregate(total_ms: float, steps: int, world: int, device=None):
+    """Whole-job timing: the slowest rank's timed total (max over ranks), as
+    ms per step and whole-job steps/s (every rank runs `steps` steps)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms / steps, world * steps / (total_ms * 1e-3)
 
 
 def run_reference(args, rank, world):
@@ -358,14 +402,7 @@ def run_hsq(args, rank, world, local):
         lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
 
-    tot = sum(res["step_ms"])
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([tot], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot = float(t.item())
-    ms_per_step = tot / args.steps
-    value = world * args.steps / (tot * 1e-3)
+    ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
     mean = lambda x: sum(x) / len(x)
     hbm_peak, peak_src = measured_peaks()
     link_gbs = lp["h2d_gbs"]
@@ -374,6 +411,8 @@ def run_hsq(args, rank, world, local):
     dev_ms = mean(res_dev["step_ms"])
     t_star_dev = (ab["hbm"] + ab["link"]) / (hbm_peak * 1e9)
     link_achieved = ab["link"] / (ms_per_step * 1e-3) / 1e9
+    hbm_achieved = ab["hbm"] / (ms_per_step * 1e-3) / 1e9
+    traffic, traffic_src = profiled_traffic()
     hbm_dev_achieved = (ab["hbm"] + ab["link"]) / (dev_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -385,14 +424,18 @@ def run_hsq(args, rank, world, local):
                    "l2": f"cold and clean at every step: {FLUSH_BYTES >> 20} MiB device write, then a "
                          f"{FLUSH_BYTES >> 20} MiB read, between timed steps (outside the step events)",
                    "n_splits": args.n_splits or "auto"},
-        "roofline": {"bound": "link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
-                     "frac": link_achieved / link_gbs, "traffic": None,
-                     "kernel": "decode_kernel (whole step: route, select, L3 gather, attention)",
-                     "peak_source": "pinned host-to-device copy measured in this run",
-                     "bytes_per_launch": ab["link"], "hbm_bytes_per_launch": ab["hbm"]},
+        "roofline": {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": hbm_achieved / hbm_peak, "traffic": traffic,
+                     "kernel": "decode_kernel (whole step: route, select, L3 gather, attention), L3 in pinned host memory",
+                     "bytes_per_launch": ab["hbm"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic_source": traffic_src},
+        "roofline_link": {"bound": "host link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
+                          "frac": link_achieved / link_gbs, "bytes_per_launch": ab["link"],
+                          "peak_source": "pinned host-to-device copy measured in this run"},
         "roofline_hbm_device_l3": {"bound": "hbm", "achieved": hbm_dev_achieved, "peak": hbm_peak,
-                                   "unit": "GB/s", "frac": hbm_dev_achieved / hbm_peak, "traffic": None,
-                                   "kernel": "decode_kernel, L3 in device memory",
+                                   "unit": "GB/s", "frac": hbm_dev_achieved / hbm_peak,
+                                   "kernel": "decode_kernel, L3 in device memory (L3 bytes counted as HBM bytes)",
                                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
         "step_roofline": {"t_star_us": t_star * 1e6, "t_us": ms_per_step * 1e3, "frac": t_star / (ms_per_step * 1e-3),
                           "hbm_bytes": ab["hbm"], "link_bytes": ab["link"],

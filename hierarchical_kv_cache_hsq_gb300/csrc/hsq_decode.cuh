@@ -105,12 +105,12 @@ __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int m
     L.lev = (unsigned)o; o = al16(o + (size_t)L.nlev * 16 * row);
     L.b0 = (unsigned)o; o = al16(o + (size_t)L.nb0 * row);
     L.off = (unsigned)o; o = al16(o + (size_t)N * row);
-    L.base = (unsigned)o; o = al16(o + (size_t)kBatchRecs * row);
-    L.rbits = (unsigned)o; o = al16(o + (size_t)kBatchRecs * 4);
+    L.base = (unsigned)o; o = al16(o + (size_t)2 * kBatchRecs * row);   // two batches in flight
+    L.rbits = (unsigned)o; o = al16(o + (size_t)2 * kBatchRecs * 4);
     L.inbox = (unsigned)o; o = al16(o + (size_t)((R + S - 1) / S) * S * hsq::kPartStride * 4);
     // one region, used in turn for: every split's routing keys (until the
-    // selection is made), the gathered L3 records, the warp partials
-    size_t rec = kFetchBatchBytes;
+    // selection is made), two batches of gathered L3 records, the warp partials
+    size_t rec = 2 * (size_t)kFetchBatchBytes;
     const size_t merge = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
     if (merge > rec) rec = merge;
     if (route && (size_t)G * 4 > rec) rec = (size_t)G * 4;
@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     __shared__ __align__(16) float s_qr[R][kDim];
     __shared__ __align__(16) float s_x[kHalves][16];
     __shared__ SelectSmem s_ss;
+    __shared__ __align__(16) uint32_t s_stats[kMaxSplits][4];  // per split: non-empty keys, max key, min key
 
     constexpr int RB = N * 136;
     constexpr int kBatchRecs = kFetchBatchBytes / RB;
@@ -305,13 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     uint32_t* s_all = reinterpret_cast<uint32_t*>(s_dyn + L.rec);  // routing keys of all splits
     float* xs = &s_x[hw][0];
 
-    // 1. stage the device-resident inputs of this split
+    // 1. stage the device-resident inputs of this split: first what the L2
+    //    pass needs (one cp.async group), then the rest (a second group)
     if constexpr (st2) {
         stage16(s_dyn + L.l2k, g_l2k, n2 * 48);
-        stage16(s_dyn + L.l2v, g_l2v, n2 * 48);
         stage4(reinterpret_cast<float*>(s_dyn + L.l2kn), g_l2kn, n2);
-        stage4(reinterpret_cast<float*>(s_dyn + L.l2vn), g_l2vn, n2);
         for (int i = tid; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
+    }
+    if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
+    cp_async_commit();
+    if constexpr (st2) {
+        stage16(s_dyn + L.l2v, g_l2v, n2 * 48);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l2vn), g_l2vn, n2);
     }
     if constexpr (st1) {
         stage16(s_dyn + L.l1k, g_l1k, n1 * 64);
@@ -320,7 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
         stage4(reinterpret_cast<float*>(s_dyn + L.l1vn), g_l1vn, n1);
     }
     if constexpr (stb) stage4(reinterpret_cast<float*>(s_dyn + L.bitmap), reinterpret_cast<const float*>(g_bitmap), c.W);
-    if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
     // RoPE rows: level k row j = hi[j * 16^k] (angle 256 j 16^k omega), b0 row j = lo[N j], off row n = lo[n]
     const int n_hi = (tb.max_pos + 255) / 256;
 #pragma unroll 1
@@ -333,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     for (int i = tid; i < L.nb0 * 32; i += kThreads)
         cp_async16(s_b0 + 4 * i, tb.rope_lo + (size_t)(N * (i >> 5)) * kDim + 4 * (i & 31));
     stage16(s_off, tb.rope_lo, N * kDim * 4);
+    cp_async_commit();
     for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
     float sg[8];
     load_signs_global(sg, c.signs);
@@ -340,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     // 2. query heads of this KV head: RoPE'd (original frame) and rotated
     const int pos = checked_pos(__ldg(a.pos + b), tb, a.err);
     prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, pos, sg, tb, s_qt, s_qr);
-    cp_async_wait_all();
+    cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
 
     const float* c4 = s_cb;
@@ -356,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     }
     if (kRoute) cluster_wait();  // every CTA of the cluster runs: remote stores may start
     if constexpr (kRoute || keep) {
+        // routing keys (each goes to every split, and so do this split's key
+        // statistics) and the L2 logits per query head, one pass
         float gq[8];
-        if (kRoute) {
+        if constexpr (kRoute) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 float s0 = 0.f, s1 = 0.f;
@@ -371,6 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             }
         }
         uint32_t* dst = kRoute && l < S ? cluster.map_shared_rank(s_all, l) + g0 : nullptr;
+        int cn = 0;
+        uint32_t mx = 0u, mn = 0xFFFFFFFFu;
 #pragma unroll 1
         for (int blk = 0; blk < n2; blk += 2 * kHalves) {
             const int ia = blk + hw, ib = ia + kHalves;
@@ -378,33 +388,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             float va[8], vb[8];
             unpack3_smem(p_l2k + ja * 48, c3, 1.0f, va);
             unpack3_smem(p_l2k + jb * 48, c3, 1.0f, vb);
-            const float kna = p_l2kn[ja], knb = p_l2kn[jb];
-            if (kRoute) {
+            if constexpr (kRoute) {
                 float sa, sb;
                 route_pair(gq, va, vb, sa, sb);
-                const uint32_t ka = p_cnt[ja] > 0 ? ordered_key(kna * sa) : 0u;
-                const uint32_t kb = p_cnt[jb] > 0 ? ordered_key(knb * sb) : 0u;
+                const uint32_t ka = ia < n2 && p_cnt[ja] > 0 ? ordered_key(p_l2kn[ja] * sa) : 0u;
+                const uint32_t kb = ib < n2 && p_cnt[jb] > 0 ? ordered_key(p_l2kn[jb] * sb) : 0u;
                 if (dst) {  // lane l < S writes this pair's keys into split l
                     if (ia < n2) dst[ia] = ka;
                     if (ib < n2) dst[ib] = kb;
+                }
+                if (l == 0) {
+                    cn += (ka != 0u) + (kb != 0u);
+                    mx = max(mx, max(ka, kb));
+                    mn = min(mn, min(ka ? ka : 0xFFFFFFFFu, kb ? kb : 0xFFFFFFFFu));
                 }
             }
             if constexpr (keep) {
                 int idx;
                 const float d = pair_dots<R>(qt, va, vb, idx);
                 if (idx < R) {
-                    if (ia < n2) s_logit[ia * R + idx] = kna * d * kLogitScaleLog2;
+                    if (ia < n2) s_logit[ia * R + idx] = p_l2kn[ja] * d * kLogitScaleLog2;
                 } else if (idx < 2 * R) {
-                    if (ib < n2) s_logit[ib * R + idx - R] = knb * d * kLogitScaleLog2;
+                    if (ib < n2) s_logit[ib * R + idx - R] = p_l2kn[jb] * d * kLogitScaleLog2;
                 }
+            }
+        }
+        if constexpr (kRoute) {
+            cn = __reduce_add_sync(kFull, cn);
+            mx = __reduce_max_sync(kFull, mx);
+            mn = __reduce_min_sync(kFull, mn);
+            if (lane == 0) { s_ss.red[0][warp] = (uint32_t)cn; s_ss.red[1][warp] = mx; s_ss.red[2][warp] = mn; }
+            __syncthreads();
+            if (tid < S) {
+                uint32_t t = 0u, hx = 0u, lx = 0xFFFFFFFFu;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    t += s_ss.red[0][w];
+                    hx = max(hx, s_ss.red[1][w]);
+                    lx = min(lx, s_ss.red[2][w]);
+                }
+                *reinterpret_cast<uint4*>(cluster.map_shared_rank(&s_stats[s][0], tid)) = make_uint4(t, hx, lx, 0u);
             }
         }
     }
 
     // 3. the selection of this (b, h)
+    cp_async_wait_group<0>();  // everything staged (visible after the next barrier)
     if (kRoute) {
-        cluster.sync();  // every split's keys are in every split
-        select_top_beta(s_all, c.G, c.beta, s_sel, s_ss);
+        cluster.sync();  // every split's keys and statistics are in every split
+        select_top_beta(s_all, c.G, c.beta, s_sel, s_ss, &s_stats[0][0], S);
         __syncthreads();
         if (s == 0)
             for (int i = tid; i < c.beta; i += kThreads) a.sel[(size_t)bh * c.beta + i] = s_sel[i];
@@ -417,27 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
         if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
     }
 
-    // 4. gather this split's records; meanwhile L1 tokens and unselected summaries
+    // 4. gather this split's records (batch k: records f0 + k B .., loaded into
+    //    registers one batch ahead -- zero-copy loads from host memory -- and
+    //    stored to buffer k & 1 when consumed); meanwhile the L1 tokens and the
+    //    unselected summaries.  Per record, its base angle g N omega (staged
+    //    rows only) and its L1 bits go to slot k & 1.
     uint4 pre[kMaxFetchChunksPerThread];
-    auto issue = [&](int r0, int nrec) {
+    auto issue = [&](int k) {
+        const int r0 = f0 + k * kBatchRecs;
+        const int nrec = min(kBatchRecs, f1 - r0);
 #pragma unroll
-        for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
-            const int ch = tid + k * kThreads;
-            pre[k] = make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kMaxFetchChunksPerThread; ++u) {
+            const int ch = tid + u * kThreads;
+            pre[u] = make_uint4(0u, 0u, 0u, 0u);
             if (ch < nrec * kRecChunks) {
                 const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
                 const int i = r0 + rec;
                 const int g = s_sel[i];
                 if (g >= 0) {
-                    const uint8_t* base = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
-                                                         : c.l3 + ((size_t)bh * c.G + g) * RB;
-                    pre[k] = __ldcg(reinterpret_cast<const uint4*>(base) + off);
+                    const uint8_t* src = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
+                                                        : c.l3 + ((size_t)bh * c.G + g) * RB;
+                    pre[u] = __ldcg(reinterpret_cast<const uint4*>(src) + off);
                 }
             }
         }
-    };
-    // per record: cos/sin of its base angle g N omega (staged rows only) and its L1 bits
-    auto meta = [&](int r0, int nrec) {
         if (hw < nrec) {
             const int g = s_sel[r0 + hw];
             if (g >= 0) {
@@ -446,26 +481,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
                 float4 cs = *reinterpret_cast<const float4*>(br + 4 * l);
                 float4 sn = *reinterpret_cast<const float4*>(br + 64 + 4 * l);
 #pragma unroll 1
-                for (int k = 0; k < L.nlev; ++k) {  // one 4-bit digit of p0 >> 8 per level
-                    const int j = (p0 >> (8 + 4 * k)) & 15;
+                for (int k2 = 0; k2 < L.nlev; ++k2) {  // one 4-bit digit of p0 >> 8 per level
+                    const int j = (p0 >> (8 + 4 * k2)) & 15;
                     if (j) {
-                        const float* lr = s_lev + (k * 16 + j) * kDim;
+                        const float* lr = s_lev + (k2 * 16 + j) * kDim;
                         angle_add4(cs, sn, *reinterpret_cast<const float4*>(lr + 4 * l),
                                    *reinterpret_cast<const float4*>(lr + 64 + 4 * l));
                     }
                 }
-                *reinterpret_cast<float4*>(s_base + hw * kDim + 4 * l) = cs;
-                *reinterpret_cast<float4*>(s_base + hw * kDim + 64 + 4 * l) = sn;
+                float* sb = s_base + ((k & 1) * kBatchRecs + hw) * kDim;
+                *reinterpret_cast<float4*>(sb + 4 * l) = cs;
+                *reinterpret_cast<float4*>(sb + 64 + 4 * l) = sn;
                 if (l == 0)
-                    s_rbits[hw] = (p_bitmap[p0 >> 5] >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
+                    s_rbits[(k & 1) * kBatchRecs + hw] =
+                        (p_bitmap[p0 >> 5] >> (p0 & 31)) & ((N == 32) ? 0xFFFFFFFFu : ((1u << N) - 1u));
             }
         }
     };
-    const int nb0 = min(nfetch, kBatchRecs);
-    if (nb0 > 0) {
-        issue(f0, nb0);
-        meta(f0, nb0);
-    }
+    const int nbatch = (nfetch + kBatchRecs - 1) / kBatchRecs;
+    issue(0);
     __syncthreads();  // s_mask complete
 
     Softmax<R> sm;
@@ -512,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     }
 
     // 5. recovered tokens of the selected groups
-    if (nfetch > 0) {
+    {
         float qr[R][8];
 #pragma unroll
         for (int j = 0; j < R; ++j) {
@@ -523,23 +557,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             }
         }
 #pragma unroll 1
-        for (int r0 = f0; r0 < f1; r0 += kBatchRecs) {
-            const int nb = min(kBatchRecs, f1 - r0);
-            __syncthreads();  // previous batch consumed, this batch's meta written
+        for (int kb_ = 0; kb_ < nbatch; ++kb_) {
+            {   // batch kb_ lands in buffer kb_ & 1 (the loads were issued one batch ahead)
+                uint4* dstb = reinterpret_cast<uint4*>(s_rec + (kb_ & 1) * kFetchBatchBytes);
 #pragma unroll
-            for (int k = 0; k < kMaxFetchChunksPerThread; ++k) {
-                const int ch = tid + k * kThreads;
-                if (ch < nb * kRecChunks) reinterpret_cast<uint4*>(s_rec)[ch] = pre[k];
+                for (int u = 0; u < kMaxFetchChunksPerThread; ++u) {
+                    const int ch = tid + u * kThreads;
+                    if (ch < kFetchBatchBytes / 16) dstb[ch] = pre[u];
+                }
             }
-            __syncthreads();
-            issue(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));  // no-op past the last batch
+            __syncthreads();  // batch kb_ and its meta are in shared memory
+            issue(kb_ + 1);  // the next batch (nothing past the last)
+            const int r0 = f0 + kb_ * kBatchRecs;
+            const int nb = min(kBatchRecs, f1 - r0);
+            const uint8_t* buf = s_rec + (kb_ & 1) * kFetchBatchBytes;
+            const float* sbase = s_base + (kb_ & 1) * kBatchRecs * kDim;
+            const uint32_t* rbits = s_rbits + (kb_ & 1) * kBatchRecs;
             // one recovered token: validity, RoPE'd key and rotated-frame value
             auto token = [&](int u, float kv[8], float vv[8]) -> bool {
                 const int rec = u / N, n = u - rec * N;
                 const int g = s_sel[r0 + rec];
                 const int t = g * N + n;
-                const bool ok = g >= 0 && t < c.T && !((s_rbits[rec] >> n) & 1u);
-                const uint8_t* rp = s_rec + rec * RB;
+                const bool ok = g >= 0 && t < c.T && !((rbits[rec] >> n) & 1u);
+                const uint8_t* rp = buf + rec * RB;
                 const float* norms = reinterpret_cast<const float*>(rp + N * 128);
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
                 const uint16_t* vr = reinterpret_cast<const uint16_t*>(rp + N * 64 + n * 64);
@@ -549,8 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
 #pragma unroll
                 for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
                 {   // RoPE at t = g N + n: base angle (per record) plus offset n omega
-                    float4 cs = *reinterpret_cast<const float4*>(s_base + rec * kDim + 4 * l);
-                    float4 sn = *reinterpret_cast<const float4*>(s_base + rec * kDim + 64 + 4 * l);
+                    float4 cs = *reinterpret_cast<const float4*>(sbase + rec * kDim + 4 * l);
+                    float4 sn = *reinterpret_cast<const float4*>(sbase + rec * kDim + 64 + 4 * l);
                     angle_add4(cs, sn, *reinterpret_cast<const float4*>(s_off + n * kDim + 4 * l),
                                *reinterpret_cast<const float4*>(s_off + n * kDim + 64 + 4 * l));
                     const float cv[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
@@ -574,8 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
                 pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
                 sm.add2(xa, va, oka, xb, vb, okb);
             }
-            __syncthreads();  // (a barrier under a condition costs code size even when uniform)
-            meta(r0 + kBatchRecs, min(kBatchRecs, f1 - r0 - kBatchRecs));
+            __syncthreads();  // batch kb_ consumed: its buffer may be refilled
         }
     }
 

@@ -351,6 +351,10 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// wait until at most n committed groups of this thread are still in flight
+template <int n>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory"); }
 
 // bytes: a multiple of 16, both addresses 16-byte aligned
 __device__ __forceinline__ void stage16(void* dst, const void* src, int bytes) {
@@ -446,7 +450,10 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
 // order-preserving keys of the fp32 group scores (0 = empty group, never
 // selected).  The groups of the beta largest keys (ties to the lower group)
 // go to out[0..beta) in ascending group order, -1 padded (out may be shared
-// or global memory; the caller synchronises before reading it).
+// or global memory; the caller synchronises before reading it).  stats, when
+// not null, holds nstats partial (count, max, min) statistics of the
+// non-empty keys (4 words each) that together cover all G keys; otherwise
+// they are computed here.
 //
 // Bucket select: the keys still in play, [lo, hi], are histogrammed (first
 // pass: kSelBins equal-width bins of the fp32 score; later passes: power-of-
@@ -462,7 +469,8 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
 // step j of a warp reads keys w W + 32 j + lane (conflict-free), and the
 // ordered placement counts with one ballot per step.  Every loop bound is
 // uniform, so all warp-level operations are converged.
-__device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* out, SelectSmem& ss) {
+__device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* out, SelectSmem& ss,
+                                const uint32_t* stats = nullptr, int nstats = 0) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kpw = (G + kThreads - 1) / kThreads;  // steps per warp
     const int wbase = warp * 32 * kpw;
@@ -474,7 +482,17 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     // count, max and min of the non-empty keys
     int ne = 0;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    {
+    if (stats) {
+#pragma unroll 1
+        for (int w = tid; w < (G + 31) / 32; w += kThreads) ss.taken[w] = 0u;
+#pragma unroll 1
+        for (int r = 0; r < nstats; ++r) {
+            ne += (int)stats[4 * r];
+            hi = max(hi, stats[4 * r + 1]);
+            lo = min(lo, stats[4 * r + 2]);
+        }
+        __syncthreads();
+    } else {
         int cn = 0;
         uint32_t mx = 0u, mn = 0xFFFFFFFFu;
 #pragma unroll 1
