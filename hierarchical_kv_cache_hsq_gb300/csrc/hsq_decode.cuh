@@ -391,26 +391,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             if constexpr (kRoute) {
                 float sa, sb;
                 route_pair(gq, va, vb, sa, sb);
-                const uint32_t ka = ia < n2 && p_cnt[ja] > 0 ? ordered_key(p_l2kn[ja] * sa) : 0u;
-                const uint32_t kb = ib < n2 && p_cnt[jb] > 0 ? ordered_key(p_l2kn[jb] * sb) : 0u;
-                if (dst) {  // lane l < S writes this pair's keys into split l
-                    if (ia < n2) dst[ia] = ka;
-                    if (ib < n2) dst[ib] = kb;
-                }
-                if (l == 0) {
-                    cn += (ka != 0u) + (kb != 0u);
-                    mx = max(mx, max(ka, kb));
-                    mn = min(mn, min(ka ? ka : 0xFFFFFFFFu, kb ? kb : 0xFFFFFFFFu));
-                }
+                // (flags are bitwise: no branch around the loads)
+                const uint32_t ka = ((ia < n2) & (p_cnt[ja] > 0)) ? ordered_key(p_l2kn[ja] * sa) : 0u;
+                const uint32_t kb = ((ib < n2) & (p_cnt[jb] > 0)) ? ordered_key(p_l2kn[jb] * sb) : 0u;
+                if (dst && ia < n2) dst[ia] = ka;  // lane l < S writes this pair's keys into split l
+                if (dst && ib < n2) dst[ib] = kb;
+                const bool l0 = l == 0;
+                cn += l0 ? (ka != 0u) + (kb != 0u) : 0;
+                mx = max(mx, l0 ? max(ka, kb) : 0u);
+                mn = min(mn, l0 ? min(ka ? ka : 0xFFFFFFFFu, kb ? kb : 0xFFFFFFFFu) : 0xFFFFFFFFu);
             }
             if constexpr (keep) {
                 int idx;
                 const float d = pair_dots<R>(qt, va, vb, idx);
-                if (idx < R) {
-                    if (ia < n2) s_logit[ia * R + idx] = p_l2kn[ja] * d * kLogitScaleLog2;
-                } else if (idx < 2 * R) {
-                    if (ib < n2) s_logit[ib * R + idx - R] = p_l2kn[jb] * d * kLogitScaleLog2;
-                }
+                const bool first = idx < R;
+                const int e = first ? ia : ib;
+                const float kn = first ? p_l2kn[ja] : p_l2kn[jb];
+                if ((idx < 2 * R) & (e < n2)) s_logit[e * R + (first ? idx : idx - R)] = kn * d * kLogitScaleLog2;
             }
         }
         if constexpr (kRoute) {
@@ -524,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     for (int blk = 0; blk < n2; blk += 2 * kHalves) {
         const int ia = blk + hw, ib = ia + kHalves;
         const int ja = min(ia, n2 - 1), jb = min(ib, n2 - 1);
-        const bool oka = ia < n2 && p_cnt[ja] > 0 && !((s_mask[ja >> 5] >> (ja & 31)) & 1u);
-        const bool okb = ib < n2 && p_cnt[jb] > 0 && !((s_mask[jb >> 5] >> (jb & 31)) & 1u);
+        const bool oka = (ia < n2) & (p_cnt[ja] > 0) & (((s_mask[ja >> 5] >> (ja & 31)) & 1u) == 0u);
+        const bool okb = (ib < n2) & (p_cnt[jb] > 0) & (((s_mask[jb >> 5] >> (jb & 31)) & 1u) == 0u);
         if (!__any_sync(kFull, oka || okb)) continue;
         float va[8], vb[8], xa[R], xb[R];
         if constexpr (keep) {
@@ -578,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
                 const int rec = u / N, n = u - rec * N;
                 const int g = s_sel[r0 + rec];
                 const int t = g * N + n;
-                const bool ok = g >= 0 && t < c.T && !((rbits[rec] >> n) & 1u);
+                const bool ok = (g >= 0) & (t < c.T) & (((rbits[rec] >> n) & 1u) == 0u);
                 const uint8_t* rp = buf + rec * RB;
                 const float* norms = reinterpret_cast<const float*>(rp + N * 128);
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);

@@ -414,7 +414,7 @@ constexpr int kSelMaxGroups = 32768;
 constexpr int kSelCand = 32;            // boundary candidates ranked by one warp
 
 struct __align__(16) SelectSmem {
-    int hist[kSelBins];
+    int hist[kSelBins + 4];  // + a sink bin for keys out of play (branch-free histogram)
     uint32_t taken[kSelMaxGroups / 32];
     uint32_t cand_key[kSelCand];
     int cand_g[kSelCand];
@@ -468,7 +468,9 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
 // Layout: warp w owns the contiguous keys [w W, (w + 1) W), W = 32 kpw;
 // step j of a warp reads keys w W + 32 j + lane (conflict-free), and the
 // ordered placement counts with one ballot per step.  Every loop bound is
-// uniform, so all warp-level operations are converged.
+// uniform, so all warp-level operations are converged, and the per-key work
+// is branch-free (clamped loads, bitwise flags, a sink bin): a divergent
+// branch around a load or an atomic costs several hundred cycles per step.
 __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* out, SelectSmem& ss,
                                 const uint32_t* stats = nullptr, int nstats = 0) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -476,7 +478,8 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     const int wbase = warp * 32 * kpw;
     auto key_at = [&](int j, int& i) -> uint32_t {
         i = wbase + 32 * j + lane;
-        return i < G ? s_keys[i] : 0u;
+        const uint32_t v = s_keys[min(i, G - 1)];
+        return i < G ? v : 0u;
     };
 
     // count, max and min of the non-empty keys
@@ -499,7 +502,9 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         for (int j = 0; j < kpw; ++j) {
             int i;
             const uint32_t v = key_at(j, i);
-            if (v != 0u) { ++cn; mx = max(mx, v); mn = min(mn, v); }
+            cn += v != 0u;
+            mx = max(mx, v);
+            mn = min(mn, v != 0u ? v : 0xFFFFFFFFu);
         }
         cn = __reduce_add_sync(kFull, cn);
         mx = __reduce_max_sync(kFull, mx);
@@ -541,7 +546,8 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             for (int j = 0; j < kpw; ++j) {
                 int i;
                 const uint32_t v = key_at(j, i);
-                if (v != 0u && v >= lo && v <= hi) atomicAdd(&ss.hist[bin_of(v)], 1);
+                const bool play = (v != 0u) & (v >= lo) & (v <= hi);
+                atomicAdd(&ss.hist[play ? bin_of(v) : kSelBins], 1);
             }
             __syncthreads();
             // blocked scan from the top: thread t owns bins [B - 8(t+1), B - 8t)
@@ -570,11 +576,15 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             for (int j = 0; j < kpw; ++j) {
                 int i;
                 const uint32_t v = key_at(j, i);
-                if (v != 0u && v >= lo && v <= hi && bin_of(v) == bstar) {
-                    bmx = max(bmx, v);
-                    bmn = min(bmn, v);
-                    if (bcnt <= kSelCand) {
-                        const int slot = atomicAdd(&ss.ncand, 1);
+                const bool inb = (v != 0u) & (v >= lo) & (v <= hi) & (bin_of(v) == bstar);
+                bmx = max(bmx, inb ? v : 0u);
+                bmn = min(bmn, inb ? v : 0xFFFFFFFFu);
+                const unsigned bm = __ballot_sync(kFull, inb);
+                if (bm != 0u && bcnt <= kSelCand) {  // rare: the boundary bin's few keys
+                    int slot = 0;
+                    if (lane == 0) slot = atomicAdd(&ss.ncand, __popc(bm));
+                    slot = __shfl_sync(kFull, slot, 0) + __popc(bm & ((1u << lane) - 1u));
+                    if (inb) {
                         ss.cand_key[slot] = v;
                         ss.cand_g[slot] = i;
                     }
@@ -615,13 +625,14 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
 
     // ordered placement: per step a ballot of taken (mode 2: greater) and of
     // equal keys; a warp's counts, then one exclusive scan over the warps
+    // (mode is uniform; the per-key expressions are bitwise, without branches)
+    const uint32_t thr = mode == 0 ? 0u : mode == 1 ? bhi : kstar;
     auto flags_at = [&](int j, int& i, bool& gt, bool& eq) {
         const uint32_t v = key_at(j, i);
-        if (mode == 2) { gt = v > kstar; eq = v == kstar; }
-        else {
-            gt = mode == 0 ? v != 0u : (v > bhi || (v != 0u && ((ss.taken[i >> 5] >> (i & 31)) & 1u)));
-            eq = false;
-        }
+        const uint32_t tw = ss.taken[min(i, G - 1) >> 5];
+        const bool tk = (mode == 1) & (v != 0u) & (((tw >> (i & 31)) & 1u) != 0u);
+        gt = (v > thr) | tk;
+        eq = (mode == 2) & (v == kstar);
     };
     int wgt = 0, weq = 0;
 #pragma unroll 1
@@ -643,12 +654,9 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         flags_at(j, i, gt, eq);
         const unsigned bg = __ballot_sync(kFull, gt), be = __ballot_sync(kFull, eq);
         const int pg = pos_gt + __popc(bg & lt), pe = eq_before + __popc(be & lt);
-        if (mode == 2) {
-            if (gt && pg + min(pe, need) < beta) out[pg + min(pe, need)] = i;
-            else if (eq && pe < need && pg + pe < beta) out[pg + pe] = i;
-        } else if (gt && pg < beta) {
-            out[pg] = i;
-        }
+        const int p = gt ? pg + (mode == 2 ? min(pe, need) : 0) : pg + pe;
+        const bool put = (gt | (eq & (pe < need))) & (p < beta);
+        if (put) out[p] = i;
         pos_gt += __popc(bg);
         eq_before += __popc(be);
     }
