@@ -143,17 +143,16 @@ struct Softmax {
                                          const float vb[8], bool okb) {
 #pragma unroll
         for (int j = 0; j < R; ++j) {
+            // rescale by selects, not a branch (the two half-warps of a warp diverge here)
             const float a = oka ? xa[j] : -INFINITY, b = okb ? xb[j] : -INFINITY;
             const float mn = fmaxf(m[j], fmaxf(a, b));
-            if (mn > m[j]) {
-                const float corr = fast_exp2(m[j] - mn);
-                l[j] *= corr;
+            const float corr = mn > m[j] ? fast_exp2(m[j] - mn) : 1.f;
+            l[j] *= corr;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[j][i] *= corr;
-                m[j] = mn;
-            }
-            const float pa = oka ? fast_exp2(a - m[j]) : 0.f;
-            const float pb = okb ? fast_exp2(b - m[j]) : 0.f;
+            for (int i = 0; i < 8; ++i) acc[j][i] *= corr;
+            m[j] = mn;
+            const float pa = oka ? fast_exp2(a - mn) : 0.f;
+            const float pb = okb ? fast_exp2(b - mn) : 0.f;
             l[j] += pa + pb;
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(pa, va[i], fmaf(pb, vb[i], acc[j][i]));
@@ -306,12 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     uint32_t* s_all = reinterpret_cast<uint32_t*>(s_dyn + L.rec);  // routing keys of all splits
     float* xs = &s_x[hw][0];
 
+    // 0. the few values read straight into registers, issued before anything
+    //    waits on them: position, this half-warp's query head, signs, counts
+    const int pos_raw = __ldg(a.pos + b);
+    float qx[8];
+    load_f32x8(a.q + ((size_t)b * c.Hq + h * R + min(hw, R - 1)) * kDim, qx);
+    float sg[8];
+    load_signs_global(sg, c.signs);
+    const uint8_t cnt0 = st2 && tid < n2 ? __ldg(g_cnt + tid) : (uint8_t)0;
+
     // 1. stage the device-resident inputs of this split: first what the L2
     //    pass needs (one cp.async group), then the rest (a second group)
     if constexpr (st2) {
         stage16(s_dyn + L.l2k, g_l2k, n2 * 48);
         stage4(reinterpret_cast<float*>(s_dyn + L.l2kn), g_l2kn, n2);
-        for (int i = tid; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
     }
     if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
     cp_async_commit();
@@ -340,12 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     stage16(s_off, tb.rope_lo, N * kDim * 4);
     cp_async_commit();
     for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
-    float sg[8];
-    load_signs_global(sg, c.signs);
+    if constexpr (st2) {
+        if (tid < n2) s_dyn[L.cnt + tid] = cnt0;
+#pragma unroll 1
+        for (int i = tid + kThreads; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
+    }
 
     // 2. query heads of this KV head: RoPE'd (original frame) and rotated
-    const int pos = checked_pos(__ldg(a.pos + b), tb, a.err);
-    prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, pos, sg, tb, s_qt, s_qr);
+    const int pos = checked_pos(pos_raw, tb, a.err);
+    prepare_queries<R>(qx, pos, sg, tb, s_qt, s_qr);
     cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
 

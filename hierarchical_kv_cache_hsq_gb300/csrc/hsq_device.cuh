@@ -360,10 +360,12 @@ __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.w
 __device__ __forceinline__ void stage16(void* dst, const void* src, int bytes) {
     uint8_t* d = static_cast<uint8_t*>(dst);
     const uint8_t* s = static_cast<const uint8_t*>(src);
+#pragma unroll 1
     for (int i = threadIdx.x * 16; i < bytes; i += blockDim.x * 16) cp_async16(d + i, s + i);
 }
 
 __device__ __forceinline__ void stage4(float* dst, const float* src, int n) {
+#pragma unroll 1
     for (int i = threadIdx.x; i < n; i += blockDim.x) cp_async4(dst + i, src + i);
 }
 
@@ -523,7 +525,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
 
     // mode 0: take every non-empty group; 1: keys > bhi plus the ranked
     // boundary candidates; 2: keys > kstar plus the first `need` equal to kstar
-    int mode = 0, above = 0, need = 0;
+    int mode = 0, above = 0, need = 0, mode1_base = 0;
     uint32_t bhi = 0u, kstar = 0u;
     if (ne > beta) {
         const float smin = key_to_float(lo), smax = key_to_float(hi);
@@ -570,13 +572,18 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             const int bstar = ss.bstar, bcnt = ss.bcnt;
             above = ss.above;
             need = beta - above;
-            // the boundary bin's members: gathered (when few) and their exact key range
+            // the boundary bin's members: gathered (when few) and their exact key
+            // range; and per warp the keys above the boundary bin (all taken)
             uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+            int wsure = 0;
 #pragma unroll 1
             for (int j = 0; j < kpw; ++j) {
                 int i;
                 const uint32_t v = key_at(j, i);
-                const bool inb = (v != 0u) & (v >= lo) & (v <= hi) & (bin_of(v) == bstar);
+                const bool inr = (v != 0u) & (v >= lo) & (v <= hi);
+                const int bn = bin_of(v);
+                const bool inb = inr & (bn == bstar);
+                wsure += __popc(__ballot_sync(kFull, (v > hi) | (inr & (bn > bstar))));
                 bmx = max(bmx, inb ? v : 0u);
                 bmn = min(bmn, inb ? v : 0xFFFFFFFFu);
                 const unsigned bm = __ballot_sync(kFull, inb);
@@ -592,7 +599,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             }
             bmx = __reduce_max_sync(kFull, bmx);
             bmn = __reduce_min_sync(kFull, bmn);
-            if (lane == 0) { ss.red[1][warp] = bmx; ss.red[2][warp] = bmn; }
+            if (lane == 0) { ss.red[0][warp] = (uint32_t)wsure; ss.red[1][warp] = bmx; ss.red[2][warp] = bmn; }
             __syncthreads();
             uint32_t blo_b = 0xFFFFFFFFu, bhi_b = 0u;
 #pragma unroll
@@ -611,7 +618,18 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                     const int gj = __shfl_sync(kFull, cg, j);
                     rank += (kj > ck) || (kj == ck && gj < cg);
                 }
-                if (warp == 0 && lane < bcnt && rank < need) atomicOr(&ss.taken[cg >> 5], 1u << (cg & 31));
+                const bool tk = lane < bcnt && rank < need;
+                if (warp == 0 && tk) atomicOr(&ss.taken[cg >> 5], 1u << (cg & 31));
+                // where this warp's taken keys start: keys above the bin plus taken
+                // candidates, over the warps before it (the placement needs no count pass)
+                const int ow = cg >= 0 ? cg / (32 * kpw) : -1;
+                int base = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    const int cw = (int)ss.red[0][w] + __popc(__ballot_sync(kFull, tk & (ow == w)));
+                    base += w < warp ? cw : 0;
+                }
+                mode1_base = base;
                 mode = 1;
                 bhi = bhi_b;
                 __syncthreads();
@@ -634,18 +652,22 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         gt = (v > thr) | tk;
         eq = (mode == 2) & (v == kstar);
     };
-    int wgt = 0, weq = 0;
+    int pos_gt = mode1_base, eq_before = 0;
+    if (mode != 1) {
+        int wgt = 0, weq = 0;
 #pragma unroll 1
-    for (int j = 0; j < kpw; ++j) {
-        int i;
-        bool gt, eq;
-        flags_at(j, i, gt, eq);
-        wgt += __popc(__ballot_sync(kFull, gt));
-        weq += __popc(__ballot_sync(kFull, eq));
+        for (int j = 0; j < kpw; ++j) {
+            int i;
+            bool gt, eq;
+            flags_at(j, i, gt, eq);
+            wgt += __popc(__ballot_sync(kFull, gt));
+            weq += __popc(__ballot_sync(kFull, eq));
+        }
+        int total;
+        const int packed = block_scan_1(lane == 0 ? (wgt | (weq << 16)) : 0, ss.wsum, total);
+        pos_gt = __shfl_sync(kFull, packed, 0) & 0xFFFF;
+        eq_before = __shfl_sync(kFull, packed, 0) >> 16;
     }
-    int total;
-    const int packed = block_scan_1(lane == 0 ? (wgt | (weq << 16)) : 0, ss.wsum, total);
-    int pos_gt = __shfl_sync(kFull, packed, 0) & 0xFFFF, eq_before = __shfl_sync(kFull, packed, 0) >> 16;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll 1
     for (int j = 0; j < kpw; ++j) {
@@ -683,14 +705,13 @@ __device__ __forceinline__ void route_pair(const float (&gq)[8], const float (&v
 
 // Rotated, RoPE'd query heads of KV head h: every half-warp computes head
 // min(hw, R - 1) (all warps stay converged); half-warps hw < R store it.
-// With qr, the RoPE'd query in the original frame is stored too.
+// x: that head's query (this lane's 8 dims).  With qr, the RoPE'd query in
+// the original frame is stored too.
 template <int R>
-__device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int pos, const float sg[8],
-                                                const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim]) {
+__device__ __forceinline__ void prepare_queries(float (&x)[8], int pos, const float sg[8], const Tables& tb,
+                                                float (*s_qt)[kDim], float (*s_qr)[kDim]) {
     const int hw = threadIdx.x >> 4, l = hlane();
     const int j = min(hw, R - 1);
-    float x[8];
-    load_f32x8(q + (size_t)j * kDim, x);
     rope(x, pos, tb);
     if (s_qr && hw < R) {
 #pragma unroll
@@ -709,6 +730,15 @@ __device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int
             s_qt[j][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
         }
     }
+}
+
+// The same, loading the query heads (q: the KV head's first query head).
+template <int R>
+__device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int pos, const float sg[8],
+                                                const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim]) {
+    float x[8];
+    load_f32x8(q + (size_t)min((int)threadIdx.x >> 4, R - 1) * kDim, x);
+    prepare_queries<R>(x, pos, sg, tb, s_qt, s_qr);
 }
 
 __host__ __device__ inline unsigned al16(size_t x) { return (unsigned)((x + 15) & ~(size_t)15); }
