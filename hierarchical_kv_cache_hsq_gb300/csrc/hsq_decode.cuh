@@ -49,6 +49,11 @@ namespace {
 // ---------------------------------------------------------------------------
 
 constexpr int kMaxSplits = 16;   // largest (non-portable) cluster
+
+// Threads per CTA of the decode kernel.  8 warps: 12 warps (384 threads,
+// which still fit the R <= 5 softmax state in registers) measured slower.
+template <int R>
+__host__ __device__ constexpr int dec_threads() { return 256; }
 enum : int { kStageL2 = 1, kKeepLogits = 2, kStageL1 = 4, kStageBitmap = 8 };
 
 struct DecodeArgs {
@@ -111,7 +116,7 @@ __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int m
     // one region, used in turn for: every split's routing keys (until the
     // selection is made), two batches of gathered L3 records, the warp partials
     size_t rec = 2 * (size_t)kFetchBatchBytes;
-    const size_t merge = (size_t)(kThreads / 32) * R * hsq::kPartStride * 4;
+    const size_t merge = (size_t)(dec_threads<R>() / 32) * R * hsq::kPartStride * 4;
     if (merge > rec) rec = merge;
     if (route && (size_t)G * 4 > rec) rec = (size_t)G * 4;
     L.rec = (unsigned)o; o = al16(o + rec);
@@ -237,13 +242,15 @@ __device__ __forceinline__ void cluster_wait() {
 }
 
 template <int R, int N, bool kRoute, bool kStaged>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
+__global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
     namespace cgx = cooperative_groups;
+    constexpr int NT = dec_threads<R>(), NH = NT / 16, NW = NT / 32;
+    constexpr int kChunksPT = (kFetchBatchBytes / 16 + NT - 1) / NT;  // gathered 16-B chunks per thread
     extern __shared__ __align__(16) uint8_t s_dyn[];
     __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
     __shared__ __align__(16) float s_qt[R][kDim];
     __shared__ __align__(16) float s_qr[R][kDim];
-    __shared__ __align__(16) float s_x[kHalves][16];
+    __shared__ __align__(16) float s_x[NH][16];
     __shared__ SelectSmem s_ss;
     __shared__ __align__(16) uint32_t s_stats[kMaxSplits][4];  // per split: non-empty keys, max key, min key
 
@@ -336,21 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     // RoPE rows: level k row j = hi[j * 16^k] (angle 256 j 16^k omega), b0 row j = lo[N j], off row n = lo[n]
     const int n_hi = (tb.max_pos + 255) / 256;
 #pragma unroll 1
-    for (int i = tid; i < L.nlev * 16 * 32; i += kThreads) {
+    for (int i = tid; i < L.nlev * 16 * 32; i += NT) {
         const int rowi = i >> 5, k = rowi >> 4, j = rowi & 15;
         const int src = j << (4 * k);
         if (src < n_hi) cp_async16(s_lev + 4 * i, tb.rope_hi + (size_t)src * kDim + 4 * (i & 31));
     }
 #pragma unroll 1
-    for (int i = tid; i < L.nb0 * 32; i += kThreads)
+    for (int i = tid; i < L.nb0 * 32; i += NT)
         cp_async16(s_b0 + 4 * i, tb.rope_lo + (size_t)(N * (i >> 5)) * kDim + 4 * (i & 31));
     stage16(s_off, tb.rope_lo, N * kDim * 4);
     cp_async_commit();
-    for (int i = tid; i < (L.span + 31) / 32; i += kThreads) s_mask[i] = 0u;
+    for (int i = tid; i < (L.span + 31) / 32; i += NT) s_mask[i] = 0u;
     if constexpr (st2) {
         if (tid < n2) s_dyn[L.cnt + tid] = cnt0;
 #pragma unroll 1
-        for (int i = tid + kThreads; i < n2; i += kThreads) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
+        for (int i = tid + NT; i < n2; i += NT) s_dyn[L.cnt + i] = __ldg(g_cnt + i);
     }
 
     // 2. query heads of this KV head: RoPE'd (original frame) and rotated
@@ -392,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
         int cn = 0;
         uint32_t mx = 0u, mn = 0xFFFFFFFFu;
 #pragma unroll 1
-        for (int blk = 0; blk < n2; blk += 2 * kHalves) {
-            const int ia = blk + hw, ib = ia + kHalves;
+        for (int blk = 0; blk < n2; blk += 2 * NH) {
+            const int ia = blk + hw, ib = ia + NH;
             const int ja = min(ia, n2 - 1), jb = min(ib, n2 - 1);
             float va[8], vb[8];
             unpack3_smem(p_l2k + ja * 48, c3, 1.0f, va);
@@ -429,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             if (tid < S) {
                 uint32_t t = 0u, hx = 0u, lx = 0xFFFFFFFFu;
 #pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) {
+                for (int w = 0; w < NW; ++w) {
                     t += s_ss.red[0][w];
                     hx = max(hx, s_ss.red[1][w]);
                     lx = min(lx, s_ss.red[2][w]);
@@ -443,15 +450,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     cp_async_wait_group<0>();  // everything staged (visible after the next barrier)
     if (kRoute) {
         cluster.sync();  // every split's keys and statistics are in every split
-        select_top_beta(s_all, c.G, c.beta, s_sel, s_ss, &s_stats[0][0], S);
+        select_top_beta<NT>(s_all, c.G, c.beta, s_sel, s_ss, &s_stats[0][0], S);
         __syncthreads();
         if (s == 0)
-            for (int i = tid; i < c.beta; i += kThreads) a.sel[(size_t)bh * c.beta + i] = s_sel[i];
+            for (int i = tid; i < c.beta; i += NT) a.sel[(size_t)bh * c.beta + i] = s_sel[i];
     } else {
-        for (int i = tid; i < c.beta; i += kThreads) s_sel[i] = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
+        for (int i = tid; i < c.beta; i += NT) s_sel[i] = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
         __syncthreads();
     }
-    for (int i = tid; i < c.beta; i += kThreads) {
+    for (int i = tid; i < c.beta; i += NT) {
         const int g = s_sel[i];
         if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
     }
@@ -461,13 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     //    stored to buffer k & 1 when consumed); meanwhile the L1 tokens and the
     //    unselected summaries.  Per record, its base angle g N omega (staged
     //    rows only) and its L1 bits go to slot k & 1.
-    uint4 pre[kMaxFetchChunksPerThread];
+    uint4 pre[kChunksPT];
     auto issue = [&](int k) {
         const int r0 = f0 + k * kBatchRecs;
         const int nrec = min(kBatchRecs, f1 - r0);
 #pragma unroll
-        for (int u = 0; u < kMaxFetchChunksPerThread; ++u) {
-            const int ch = tid + u * kThreads;
+        for (int u = 0; u < kChunksPT; ++u) {
+            const int ch = tid + u * NT;
             pre[u] = make_uint4(0u, 0u, 0u, 0u);
             if (ch < nrec * kRecChunks) {
                 const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
@@ -512,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
     Softmax<R> sm;
     sm.init();
 #pragma unroll 1
-    for (int blk = 0; blk < n1; blk += 2 * kHalves) {
-        const int ea = blk + hw, eb = ea + kHalves;
+    for (int blk = 0; blk < n1; blk += 2 * NH) {
+        const int ea = blk + hw, eb = ea + NH;
         const int ja = min(ea, n1 - 1), jb = min(eb, n1 - 1);
         float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
         const uint16_t* kra = reinterpret_cast<const uint16_t*>(p_l1k + ja * 64);
@@ -528,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
         sm.add2(xa, va, ea < n1, xb, vb, eb < n1);
     }
 #pragma unroll 1
-    for (int blk = 0; blk < n2; blk += 2 * kHalves) {
-        const int ia = blk + hw, ib = ia + kHalves;
+    for (int blk = 0; blk < n2; blk += 2 * NH) {
+        const int ia = blk + hw, ib = ia + NH;
         const int ja = min(ia, n2 - 1), jb = min(ib, n2 - 1);
         const bool oka = (ia < n2) & (p_cnt[ja] > 0) & (((s_mask[ja >> 5] >> (ja & 31)) & 1u) == 0u);
         const bool okb = (ib < n2) & (p_cnt[jb] > 0) & (((s_mask[jb >> 5] >> (jb & 31)) & 1u) == 0u);
@@ -568,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             {   // batch kb_ lands in buffer kb_ & 1 (the loads were issued one batch ahead)
                 uint4* dstb = reinterpret_cast<uint4*>(s_rec + (kb_ & 1) * kFetchBatchBytes);
 #pragma unroll
-                for (int u = 0; u < kMaxFetchChunksPerThread; ++u) {
-                    const int ch = tid + u * kThreads;
+                for (int u = 0; u < kChunksPT; ++u) {
+                    const int ch = tid + u * NT;
                     if (ch < kFetchBatchBytes / 16) dstb[ch] = pre[u];
                 }
             }
@@ -613,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
             };
             const int nt = nb * N;
 #pragma unroll 1
-            for (int blk = 0; blk < nt; blk += 2 * kHalves) {
-                const int ua = blk + hw, ub = ua + kHalves;
+            for (int blk = 0; blk < nt; blk += 2 * NH) {
+                const int ua = blk + hw, ub = ua + NH;
                 float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
                 const bool oka = token(min(ua, nt - 1), ka, va) && ua < nt;
                 const bool okb = token(min(ub, nt - 1), kb, vb) && ub < nt;
@@ -658,11 +665,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
         const int j = tid >> 5, q4 = tid & 31;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, s_part[((size_t)w * R + j) * hsq::kPartStride + 128]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, s_part[((size_t)w * R + j) * hsq::kPartStride + 128]);
         float Lsum = 0.f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const float* p = s_part + ((size_t)w * R + j) * hsq::kPartStride;
             const float wt = merge_weight(p[128], M);
             const float4 v = *reinterpret_cast<const float4*>(p + 4 * q4);
@@ -712,10 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(CacheView c, Decode
 // Host side: launch plan and launch.
 // ---------------------------------------------------------------------------
 
-cudaLaunchConfig_t decode_config(int S, int bh, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
+cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(S, bh, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.blockDim = dim3(threads, 1, 1);
     lc.dynamicSmemBytes = smem;
     lc.stream = st;
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -745,7 +752,7 @@ int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
         if (smem > cap) continue;
         if (hsq::raise_smem_limit(fn, ctx->device, smem) != cudaSuccess) continue;
         cudaLaunchAttribute at[1];
-        cudaLaunchConfig_t lc = decode_config(S, bh, smem, 0, at);
+        cudaLaunchConfig_t lc = decode_config(S, bh, dec_threads<R>(), smem, 0, at);
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, fn, &lc) != cudaSuccess || nc < 1) continue;
         if (ctx->cfg.n_splits > 0 || nc >= bh) return S;
@@ -783,7 +790,7 @@ hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, 
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
     cudaLaunchAttribute at[1];
-    const cudaLaunchConfig_t lc = decode_config(S, v.B * v.Hkv, L.total, st, at);
+    const cudaLaunchConfig_t lc = decode_config(S, v.B * v.Hkv, dec_threads<R>(), L.total, st, at);
     const Tables tb = make_tables(ctx);
     e = cudaLaunchKernelEx(&lc, decode_kernel<R, N, kRoute, kStaged>, v, a, tb);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "decode launch");

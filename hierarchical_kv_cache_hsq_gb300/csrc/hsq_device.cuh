@@ -420,13 +420,14 @@ struct __align__(16) SelectSmem {
     uint32_t taken[kSelMaxGroups / 32];
     uint32_t cand_key[kSelCand];
     int cand_g[kSelCand];
-    uint32_t red[3][kThreads / 32];
-    int wsum[kThreads / 32];
+    uint32_t red[3][32];  // per warp (up to 32 warps)
+    int wsum[32];
     int bstar, above, bcnt, ncand;
 };
 
-// Block-wide exclusive scan of one int per thread with a single barrier.
-// `wsum` must not be written again before the block's next __syncthreads.
+// Block-wide exclusive scan of one int per thread (NT threads) with a single
+// barrier.  `wsum` must not be written again before the block's next __syncthreads.
+template <int NT>
 __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -439,7 +440,7 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
     __syncthreads();
     int before = 0, t = 0;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         const int s = wsum[w];
         before += w < warp ? s : 0;
         t += s;
@@ -448,7 +449,8 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
     return before + x - v;
 }
 
-// Top-beta selection by the whole block (256 threads).  s_keys[0..G) are
+// Top-beta selection by the whole block (NT threads, a multiple of 32, at
+// least 256).  s_keys[0..G) are
 // order-preserving keys of the fp32 group scores (0 = empty group, never
 // selected).  The groups of the beta largest keys (ties to the lower group)
 // go to out[0..beta) in ascending group order, -1 padded (out may be shared
@@ -473,10 +475,13 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
 // uniform, so all warp-level operations are converged, and the per-key work
 // is branch-free (clamped loads, bitwise flags, a sink bin): a divergent
 // branch around a load or an atomic costs several hundred cycles per step.
+template <int NT>
 __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* out, SelectSmem& ss,
                                 const uint32_t* stats = nullptr, int nstats = 0) {
+    static_assert(NT % 32 == 0 && NT >= kSelBins / 8, "block size");
+    constexpr int NW = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int kpw = (G + kThreads - 1) / kThreads;  // steps per warp
+    const int kpw = (G + NT - 1) / NT;  // steps per warp
     const int wbase = warp * 32 * kpw;
     auto key_at = [&](int j, int& i) -> uint32_t {
         i = wbase + 32 * j + lane;
@@ -489,7 +494,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     if (stats) {
 #pragma unroll 1
-        for (int w = tid; w < (G + 31) / 32; w += kThreads) ss.taken[w] = 0u;
+        for (int w = tid; w < (G + 31) / 32; w += NT) ss.taken[w] = 0u;
 #pragma unroll 1
         for (int r = 0; r < nstats; ++r) {
             ne += (int)stats[4 * r];
@@ -513,10 +518,10 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         mn = __reduce_min_sync(kFull, mn);
         if (lane == 0) { ss.red[0][warp] = (uint32_t)cn; ss.red[1][warp] = mx; ss.red[2][warp] = mn; }
 #pragma unroll 1
-        for (int w = tid; w < (G + 31) / 32; w += kThreads) ss.taken[w] = 0u;
+        for (int w = tid; w < (G + 31) / 32; w += NT) ss.taken[w] = 0u;
         __syncthreads();
 #pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < NW; ++w) {
             ne += (int)ss.red[0][w];
             hi = max(hi, ss.red[1][w]);
             lo = min(lo, ss.red[2][w]);
@@ -541,8 +546,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                 if (fl) return min(max((int)((key_to_float(v) - smin) * fscale), 0), kSelBins - 1);
                 return (int)((v - lo) >> shift);
             };
-            reinterpret_cast<int4*>(ss.hist)[2 * tid] = make_int4(0, 0, 0, 0);
-            reinterpret_cast<int4*>(ss.hist)[2 * tid + 1] = make_int4(0, 0, 0, 0);
+            for (int q = tid; q < kSelBins / 4; q += NT) reinterpret_cast<int4*>(ss.hist)[q] = make_int4(0, 0, 0, 0);
             __syncthreads();
 #pragma unroll 1
             for (int j = 0; j < kpw; ++j) {
@@ -552,16 +556,20 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                 atomicAdd(&ss.hist[play ? bin_of(v) : kSelBins], 1);
             }
             __syncthreads();
-            // blocked scan from the top: thread t owns bins [B - 8(t+1), B - 8t)
-            const int top = kSelBins - 8 * tid;
+            // blocked scan from the top: thread t < B/8 owns bins [B - 8(t+1), B - 8t)
+            const bool owns = tid < kSelBins / 8;
+            const int top = kSelBins - 8 * min(tid, kSelBins / 8 - 1);
             const int4 h0 = *reinterpret_cast<const int4*>(&ss.hist[top - 8]);
             const int4 h1 = *reinterpret_cast<const int4*>(&ss.hist[top - 4]);
-            const int hv[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};  // descending bins
+            int hv[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};  // descending bins
             int local = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) local += hv[i];
+            for (int i = 0; i < 8; ++i) {
+                hv[i] = owns ? hv[i] : 0;
+                local += hv[i];
+            }
             int tot;
-            int run = above + block_scan_1(local, ss.wsum, tot);
+            int run = above + block_scan_1<NT>(local, ss.wsum, tot);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 if (run < beta && run + hv[i] >= beta) { ss.bstar = top - 1 - i; ss.above = run; ss.bcnt = hv[i]; }
@@ -603,7 +611,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             __syncthreads();
             uint32_t blo_b = 0xFFFFFFFFu, bhi_b = 0u;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 bhi_b = max(bhi_b, ss.red[1][w]);
                 blo_b = min(blo_b, ss.red[2][w]);
             }
@@ -625,7 +633,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                 const int ow = cg >= 0 ? cg / (32 * kpw) : -1;
                 int base = 0;
 #pragma unroll
-                for (int w = 0; w < kThreads / 32; ++w) {
+                for (int w = 0; w < NW; ++w) {
                     const int cw = (int)ss.red[0][w] + __popc(__ballot_sync(kFull, tk & (ow == w)));
                     base += w < warp ? cw : 0;
                 }
@@ -664,7 +672,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
             weq += __popc(__ballot_sync(kFull, eq));
         }
         int total;
-        const int packed = block_scan_1(lane == 0 ? (wgt | (weq << 16)) : 0, ss.wsum, total);
+        const int packed = block_scan_1<NT>(lane == 0 ? (wgt | (weq << 16)) : 0, ss.wsum, total);
         pos_gt = __shfl_sync(kFull, packed, 0) & 0xFFFF;
         eq_before = __shfl_sync(kFull, packed, 0) >> 16;
     }
@@ -684,7 +692,7 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     }
     const int n_sel = mode == 0 ? ne : beta;
 #pragma unroll 1
-    for (int i = n_sel + tid; i < beta; i += kThreads) out[i] = -1;
+    for (int i = n_sel + tid; i < beta; i += NT) out[i] = -1;
 }
 
 // Routing scores of two groups a and b: (sum_j q~_j) . c3[codes], every lane

@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
     if (!s_flag) return;
     for (int g = tid; g < c.G; g += kThreads) s_keys[g] = ordered_key(__ldcg(a.scores + (size_t)bh * c.G + g));
     __syncthreads();
-    select_top_beta(s_keys, c.G, c.beta, a.sel + (size_t)bh * c.beta, s_ss);
+    select_top_beta<kThreads>(s_keys, c.G, c.beta, a.sel + (size_t)bh * c.beta, s_ss);
     if (tid == 0) a.counters[bh] = 0;
 }
 
