@@ -24,6 +24,7 @@ struct hsq_ctx {
     // shape) and whether the split's inputs are staged in shared memory.
     struct Plan { int B, T, route, S, staged; };
     std::vector<Plan> plans;
+    std::vector<const void*> accessible;  // caller pointers already checked (device or mapped host)
     std::string last_error;
 };
 

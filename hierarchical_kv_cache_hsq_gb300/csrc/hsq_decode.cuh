@@ -314,9 +314,9 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 
     // 0. the few values read straight into registers, issued before anything
     //    waits on them: position, this half-warp's query head, signs, counts
-    const int pos_raw = __ldg(a.pos + b);
+    const int pos_raw = __ldcg(a.pos + b);  // (q, pos, sel, out may be host-mapped)
     float qx[8];
-    load_f32x8(a.q + ((size_t)b * c.Hq + h * R + min(hw, R - 1)) * kDim, qx);
+    load_f32x8_cg(a.q + ((size_t)b * c.Hq + h * R + min(hw, R - 1)) * kDim, qx);
     float sg[8];
     load_signs_global(sg, c.signs);
     const uint8_t cnt0 = st2 && tid < n2 ? __ldg(g_cnt + tid) : (uint8_t)0;

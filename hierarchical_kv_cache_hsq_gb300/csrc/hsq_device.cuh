@@ -276,6 +276,16 @@ __device__ __forceinline__ void load_bf16x8(const uint16_t* __restrict__ p, floa
     v[6] = __uint_as_float(b.y << 16); v[7] = __uint_as_float(b.y & 0xFFFF0000u);
 }
 
+// The same through L2 only (ld.global.cg): for caller buffers that may be
+// page-locked host memory read in place over the host link.
+__device__ __forceinline__ void load_f32x8_cg(const float* p, float v[8]) {
+    const int l = hlane();
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p + 4 * l));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p + 64 + 4 * l));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 __device__ __forceinline__ void load_f32x8_smem(const float* p, float v[8]) {
     const int l = hlane();
     const float4 a = *reinterpret_cast<const float4*>(p + 4 * l);
@@ -745,7 +755,7 @@ template <int R>
 __device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int pos, const float sg[8],
                                                 const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim]) {
     float x[8];
-    load_f32x8(q + (size_t)min((int)threadIdx.x >> 4, R - 1) * kDim, x);
+    load_f32x8_cg(q + (size_t)min((int)threadIdx.x >> 4, R - 1) * kDim, x);
     prepare_queries<R>(x, pos, sg, tb, s_qt, s_qr);
 }
 
@@ -761,11 +771,11 @@ __host__ __device__ inline unsigned route_smem_bytes(int G) {
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ int valid_sel(const int32_t* __restrict__ row, int i, int G, int* err) {
-    const int g = __ldg(row + i);
+    const int g = __ldcg(row + i);
     if (g < 0) return -1;
     bool ok = g < G;
     if (i > 0) {
-        const int p = __ldg(row + i - 1);
+        const int p = __ldcg(row + i - 1);
         ok = ok && p >= 0 && p < g;
     }
     if (!ok) {

@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
     for (int i = tid; i < ng; i += kThreads) s_cnt[i] = __ldg(c.l2_cnt + (size_t)b * c.G + g_begin + i);
     float sg[8];
     load_signs_global(sg, c.signs);
-    const int p = checked_pos(__ldg(a.pos + b), tb, a.err);
+    const int p = checked_pos(__ldcg(a.pos + b), tb, a.err);
     prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, p, sg, tb, s_q, nullptr);
     cp_async_wait_all();
     __syncthreads();
@@ -450,6 +450,35 @@ hsq_status decode_run(hsq_ctx* ctx, const hsq_cache* cache, const float* q, cons
     return fail(ctx, HSQ_ERR_UNSUPPORTED, "unsupported head ratio");
 }
 
+// q, pos, sel and out may be device memory or page-locked host memory mapped
+// into the device address space; anything else (pageable host memory) is
+// refused here rather than faulting in a kernel.
+hsq_status check_accessible(hsq_ctx* ctx, const void* p, const char* what) {
+    for (const void* q : ctx->accessible)
+        if (q == p) return HSQ_OK;
+    cudaPointerAttributes pa;
+    cudaError_t e = cudaPointerGetAttributes(&pa, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, HSQ_ERR_INVALID, std::string(what) + " is not a device or page-locked host pointer");
+    }
+    const bool ok = pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged ||
+                    (pa.type == cudaMemoryTypeHost && pa.devicePointer == p);
+    if (!ok) return fail(ctx, HSQ_ERR_INVALID, std::string(what) + " is not device-accessible at this address");
+    if (ctx->accessible.size() >= 64) ctx->accessible.erase(ctx->accessible.begin());
+    ctx->accessible.push_back(p);
+    return HSQ_OK;
+}
+
+hsq_status check_io(hsq_ctx* ctx, const float* q, const int32_t* pos, const int32_t* sel, const float* out) {
+    hsq_status st;
+    if ((st = check_accessible(ctx, q, "q")) != HSQ_OK) return st;
+    if ((st = check_accessible(ctx, pos, "pos")) != HSQ_OK) return st;
+    if (sel && (st = check_accessible(ctx, sel, "sel")) != HSQ_OK) return st;
+    if (out && (st = check_accessible(ctx, out, "out")) != HSQ_OK) return st;
+    return HSQ_OK;
+}
+
 hsq_status after_launch(hsq_ctx* ctx, const char* what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(ctx, e, what);
@@ -569,6 +598,7 @@ hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const
     hsq_status st = check_common(ctx, cache);
     if (st != HSQ_OK) return st;
     if (!q || !pos || !sel) return fail(ctx, HSQ_ERR_INVALID, "q, pos or sel is NULL");
+    if ((st = check_io(ctx, q, pos, sel, nullptr)) != HSQ_OK) return st;
     CacheView v = make_view(ctx, cache);
     RouteArgs a{q, pos, sel, scores_opt ? scores_opt : ctx->d_scores, ctx->d_route_ctr, ctx->d_err};
     st = dispatch_route(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
@@ -596,6 +626,7 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     hsq_status st = check_common(ctx, cache);
     if (st != HSQ_OK) return st;
     if (!q || !pos || !sel || !out) return fail(ctx, HSQ_ERR_INVALID, "q, pos, sel or out is NULL");
+    if ((st = check_io(ctx, q, pos, sel, out)) != HSQ_OK) return st;
     if (flags & ~HSQ_ATTN_FROM_STAGING) return fail(ctx, HSQ_ERR_INVALID, "unknown flags");
     const bool staged = (flags & HSQ_ATTN_FROM_STAGING) != 0;
     if (staged && !cache->staging) return fail(ctx, HSQ_ERR_INVALID, "staging is NULL");
@@ -613,6 +644,7 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     hsq_status st = check_common(ctx, cache);
     if (st != HSQ_OK) return st;
     if (!q || !pos || !sel || !out) return fail(ctx, HSQ_ERR_INVALID, "q, pos, sel or out is NULL");
+    if ((st = check_io(ctx, q, pos, sel, out)) != HSQ_OK) return st;
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool fused = false;

@@ -209,9 +209,11 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
  *   n_g * (sum_j Pi RoPE(q_j, pos_b)) . c3[codes_g]; empty groups score -inf.
  *   sel[b][h][0..beta) = the beta largest scores, ties to the lower group,
  *   listed in ascending group order, -1 padded when fewer are non-empty.
- *   q: device [B][Hq][128] f32; pos: device [B] int32 (query positions);
- *   sel: device [B][Hkv][beta] int32; scores_opt: device [B][Hkv][G] f32 or
- *   NULL.  Errors: HSQ_ERR_INVALID, HSQ_ERR_CUDA.
+ *   q: [B][Hq][128] f32; pos: [B] int32 (query positions); sel:
+ *   [B][Hkv][beta] int32 -- each device memory or page-locked host memory
+ *   mapped at the same address (read / written in place over the host link);
+ *   scores_opt: device [B][Hkv][G] f32 or NULL.  Errors: HSQ_ERR_INVALID
+ *   (also for a pageable host pointer), HSQ_ERR_CUDA.
  */
 hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
                      int32_t* sel, float* scores_opt, hsq_stream_t stream);
@@ -240,7 +242,8 @@ hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t
  *     tokens t of the groups in sel that are not in L1 (key RoPE(k_t, t)
  *     recovered from L3, value v_t),
  *   split over the entries (flash-decoding) and merged by log-sum-exp.
- *   out: device [B][Hq][128] f32 in the original frame.  q, pos, sel as in
+ *   out: [B][Hq][128] f32 in the original frame, device memory or mapped
+ *   page-locked host memory (written in place).  q, pos, sel as in
  *   hsq_route.  By default the kernel gathers the selected L3 records itself
  *   (zero-copy when L3 is on the host); with HSQ_ATTN_FROM_STAGING it reads
  *   cache->staging, which a prior hsq_fetch_dequant filled (order the two
@@ -260,7 +263,9 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  *   beta together through distributed shared memory, so no CTA waits on a
  *   CTA outside its cluster and the grid need not be co-resident.  Only if
  *   no cluster shape can be launched does it run hsq_route then
- *   hsq_decode_attn.  Errors as the two calls.
+ *   hsq_decode_attn.  q, pos, sel, out: as for those calls (device memory,
+ *   or mapped page-locked host memory for a step with no separate copies).
+ *   Errors as the two calls.
  */
 hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
                            const int32_t* pos, int32_t* sel, float* out, hsq_stream_t stream);

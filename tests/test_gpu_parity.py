@@ -386,3 +386,42 @@ def test_l3_location_mismatch_rejected():
     with pytest.raises(H.HSQError) as ei:
         H.hsq_encode(ctx, cache, K, K)
     assert ei.value.status == 1
+
+
+def test_host_mapped_io_matches_device_io():
+    # q, pos, sel and out in page-locked host memory are read and written in
+    # place by the kernel; the step is the same as with device buffers
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    L = layer("qwen3_0p6b_4k")
+    w = L.w
+    q, pos = W.queries(w, steps=2)
+    for s in range(2):
+        qd, pd = torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda()
+        sel_d = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        out_d = torch.empty((w.B, w.Hq, 128), device="cuda")
+        H.hsq_decode_step(L.ctx, L.cache, qd, pd, sel_d, out_d)
+        qh, ph = torch.from_numpy(q[s]).pin_memory(), torch.from_numpy(pos[s]).pin_memory()
+        sel_h = torch.full((w.B, w.Hkv, w.beta), 7, dtype=torch.int32).pin_memory()
+        out_h = torch.full((w.B, w.Hq, 128), 7.0).pin_memory()
+        H.hsq_decode_step(L.ctx, L.cache, qh, ph, sel_h, out_h)
+        assert H.hsq_sync_status(L.ctx) == 0
+        assert torch.equal(sel_h, sel_d.cpu())
+        assert torch.equal(out_h, out_d.cpu())
+
+
+def test_pageable_host_buffer_is_refused():
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    from hierarchical_kv_cache_hsq_gb300 import _binding as B
+    L = layer("tiny_1k")
+    w = L.w
+    q, pos = W.queries(w, steps=1)
+    qh = torch.from_numpy(q[0])  # ordinary (pageable) host memory
+    pd = torch.from_numpy(pos[0]).cuda()
+    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    with pytest.raises(B.HSQError) as ei:
+        H.hsq_decode_step(L.ctx, L.cache, qh, pd, sel, out)
+    assert ei.value.status == B.HSQ_ERR_INVALID
+    assert H.hsq_sync_status(L.ctx) == 0
