@@ -39,6 +39,7 @@ import workloads as W  # noqa: E402
 METRIC = "HSQ decode steps/s (Qwen3-8B shape, 32K ctx); effective GB/s vs HBM/link peak"
 UNIT = "steps/s"
 WORKLOAD = "qwen3_8b_32k"
+LAYERED = ("qwen3_4b_b16_8k", "qwen3_14b_b4_32k")  # multi-layer batch workloads
 FLUSH_BYTES = 256 << 20
 
 
@@ -53,6 +54,10 @@ def parse_args():
     p.add_argument("--n-splits", type=int, default=0)
     p.add_argument("--quick", action="store_true",
                    help="only the pinned-L3 decode loop (no variants, no link peak): for profiler captures")
+    p.add_argument("--workload", choices=[WORKLOAD, *LAYERED], default=WORKLOAD,
+                   help="the batch workloads run every layer of a decode step back to back "
+                        "and report a per-layer roofline (not the headline line)")
+    p.add_argument("--layers", type=int, default=0, help="layers per step (0: the workload's)")
     return p.parse_args()
 
 
@@ -467,11 +472,149 @@ def run_hsq(args, rank, world, local):
     return line if rank == 0 else None
 
 
+def layer_bytes(w, beta: int, l1_counts, nonempty):
+    """Bytes one layer-step must move once: the device tiers (L1 entries and
+    non-empty L2 summaries, keys and values, over all sequences and KV heads)
+    and the fetched L3 records (whole groups, masked L1 members included)."""
+    hbm = w.Hkv * (int(sum(l1_counts)) * 2 * 68 + int(sum(nonempty)) * 2 * 52)
+    link = w.B * w.Hkv * beta * w.N * 136
+    return hbm, link
+
+
+def run_layers(args, rank, world, local):
+    """A decode step of a multi-layer batch workload: every layer's
+    hsq_decode_step back to back (layers are serialised, as in a model),
+    an L2 flush between steps (outside the step events), and per layer the
+    time against its roofline.  All layers share layer 0's K/V draw and have
+    their own seeded L1 membership and sign vector, hence their own codes,
+    summaries, L3 records and selections."""
+    import torch
+
+    import hierarchical_kv_cache_hsq_gb300 as H
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    H.load_library()
+    w = W.get_workload(args.workload)
+    L = args.layers or w.layers
+    betas = tuple(w.betas) or (w.beta,)
+    placements = ("host", "device") if w.name == "qwen3_4b_b16_8k" else ("host",)
+    li = W.layer_inputs(w)
+    q, pos = W.queries(w, steps=w.steps)
+    cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
+                             args.n_splits) for b in betas}
+    ctxs = {b: H.Context(c) for b, c in cfgs.items()}
+    ctx0 = ctxs[betas[0]]
+    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+    caches = {pl: [] for pl in placements}
+    enc_ms = []
+    for l in range(L):
+        mask, signs = (li.l1_mask, li.signs) if l == 0 else W.layer_meta(w, l)
+        for pl in placements:
+            c = H.allocate_cache(ctx0, w.B, w.T, l3_on_host=pl == "host", with_staging=False)
+            H.set_layer_inputs(c, mask, signs)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            H.hsq_encode(ctx0, c, K, V)
+            b.record()
+            b.synchronize()
+            if pl == "host" and l > 0:  # (layer 0: first touch of the pinned pages)
+                enc_ms.append(a.elapsed_time(b))
+            caches[pl].append(c)
+    assert H.hsq_sync_status(ctx0) == 0
+    del K, V
+    l1c = [caches["host"][l].view("l1_count").cpu().numpy() for l in range(L)]
+    ne = [(caches["host"][l].view("l2_cnt").cpu().numpy() > 0).sum(axis=1) for l in range(L)]
+
+    qd, pd = torch.from_numpy(q).cuda(), torch.from_numpy(pos).cuda()
+    sel = torch.empty((w.B, w.Hkv, max(betas)), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def loop(beta, pl, nsteps, timed=True):
+        ctx, cl = ctxs[beta], caches[pl]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nsteps)]
+        torch.cuda._sleep(20_000_000)
+        for i in range(nsteps):
+            s = i % w.steps
+            flush.fill_(i & 255)
+            torch.sum(clean, dim=0, out=sink)
+            ev[i][0].record()
+            for c in cl:
+                H.hsq_decode_step(ctx, c, qd[s], pd[s], sel, out)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return [e[0].elapsed_time(e[1]) for e in ev] if timed else None
+
+    hbm_peak, peak_src = measured_peaks()
+    lp = link_peak(torch)
+    clocks = ClockSampler(local)
+    rows = []
+    for beta in betas:
+        for pl in placements:
+            loop(beta, pl, args.warmup, timed=False)
+            if not rows:
+                clocks.start()
+            ts = loop(beta, pl, args.steps)
+            ms, _ = aggregate(sum(ts), args.steps, world, device="cuda")
+            hbm = [layer_bytes(w, beta, l1c[l], ne[l])[0] for l in range(L)]
+            link = layer_bytes(w, beta, l1c[0], ne[0])[1]
+            hbm_avg = sum(hbm) / L
+            t_layer = ms * 1e-3 / L
+            if pl == "host":
+                t_star = max(hbm_avg / (hbm_peak * 1e9), link / (lp["h2d_gbs"] * 1e9))
+                bound = "host link" if link / lp["h2d_gbs"] > hbm_avg / hbm_peak else "hbm"
+            else:
+                t_star = (hbm_avg + link) / (hbm_peak * 1e9)
+                bound = "hbm"
+            rows.append({"beta": beta, "l3": "pinned host" if pl == "host" else "device",
+                         "ms_per_step": ms, "steps_per_s": world * 1e3 / ms, "us_per_layer": t_layer * 1e6,
+                         "hbm_bytes_per_layer": hbm_avg, "l3_bytes_per_layer": link,
+                         "hbm_gbs": hbm_avg / t_layer / 1e9, "l3_gbs": link / t_layer / 1e9,
+                         "t_star_us_per_layer": t_star * 1e6, "bound": bound, "frac": t_star / t_layer})
+    clk = clocks.stop()
+    assert H.hsq_sync_status(ctx0) == 0
+    head = rows[0] if len(betas) == 1 else next(r for r in rows if r["beta"] == w.beta)
+    enc = statistics.median(enc_ms) if enc_ms else float("nan")
+    line = {
+        "metric": f"HSQ decode steps/s ({w.name}, {L} layers per step)", "value": head["steps_per_s"],
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} L1={w.l1_size} "
+                               f"{L} layers, beta {'/'.join(map(str, betas))}",
+                   "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
+                   "l2": "cold and clean at every step (256 MiB write + 256 MiB read between steps, "
+                         "outside the step events); layers of a step back to back"},
+        "per_layer": rows,
+        "peaks": {"hbm_gbs": hbm_peak, "hbm_source": peak_src, "h2d_gbs": lp["h2d_gbs"],
+                  "h2d_source": "pinned host-to-device copy measured in this run"},
+        "encode": {"ms_per_layer": enc, "tokens_per_s": w.B * w.T / (enc * 1e-3),
+                   "input_gbs": w.B * w.Hkv * w.T * 2 * 128 * 2 / (enc * 1e-3) / 1e9,
+                   "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc * 1e-3) / 1e9},
+        "gpu_launches": args.steps * L * len(rows),
+        "clocks": clk,
+    }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    for c in ctxs.values():
+        c.close()
+    return line if rank == 0 else None
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.workload != WORKLOAD:
+        line = run_layers(args, rank, world, local)
     else:
         line = run_hsq(args, rank, world, local)
     if line is not None:

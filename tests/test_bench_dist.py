@@ -1,5 +1,6 @@
-"""bench.py's multi-rank aggregation on CPU: two gloo ranks, each with its own
-timed total; both get the slowest rank's time and the whole-job rate."""
+"""bench.py host logic on CPU: the multi-rank aggregation (two gloo ranks, each with its own
+timed total; both get the slowest rank's time and the whole-job rate) and the
+per-layer byte counts of the multi-layer mode."""
 
 import os
 import sys
@@ -49,3 +50,31 @@ def test_aggregate_single_rank_is_local():
     ms, value = bench.aggregate(20.0, 50, 1)
     assert ms == pytest.approx(0.4)
     assert value == pytest.approx(50 / 0.02)
+
+
+def test_layer_bytes_counts_every_sequence_and_head():
+    import bench
+    import workloads as W
+    w = W.get_workload("qwen3_4b_b16_8k")
+    l1 = [213] * w.B
+    ne = [1000] * w.B
+    hbm, link = bench.layer_bytes(w, 48, l1, ne)
+    # 68 B per 4-bit entry and 52 B per 3-bit summary, keys and values, per KV head
+    assert hbm == w.Hkv * w.B * (213 * 2 * 68 + 1000 * 2 * 52)
+    # whole group records of N tokens, 136 B each, beta per (sequence, KV head)
+    assert link == w.B * w.Hkv * 48 * w.N * 136
+    # uneven sequences are summed, not multiplied from the first
+    hbm2, _ = bench.layer_bytes(w, 48, [0] * (w.B - 1) + [213], [0] * (w.B - 1) + [1000])
+    assert hbm2 == w.Hkv * (213 * 2 * 68 + 1000 * 2 * 52)
+
+
+def test_layer_meta_matches_layer_inputs():
+    import numpy as np
+    import workloads as W
+    w = W.get_workload("tiny_1k")
+    li = W.layer_inputs(w, layer=2)
+    mask, signs = W.layer_meta(w, layer=2)
+    np.testing.assert_array_equal(mask, li.l1_mask)
+    np.testing.assert_array_equal(signs, li.signs)
+    m3, s3 = W.layer_meta(w, layer=3)
+    assert not np.array_equal(s3, signs) or not np.array_equal(m3, mask)

@@ -12,6 +12,7 @@ from .configs import WORKLOADS, Workload, get_workload
 from .generate import (
     LayerInputs,
     layer_inputs,
+    layer_meta,
     queries,
     needle_groups,
     plant_needle,
@@ -25,6 +26,7 @@ __all__ = [
     "get_workload",
     "LayerInputs",
     "layer_inputs",
+    "layer_meta",
     "queries",
     "needle_groups",
     "plant_needle",

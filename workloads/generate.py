@@ -30,7 +30,7 @@ Recipes (stated readings of the workload text):
 from __future__ import annotations
 
 from dataclasses import dataclass
-from typing import Callable, Optional, Sequence
+from typing import Tuple, Callable, Optional, Sequence
 
 import numpy as np
 
@@ -120,6 +120,13 @@ def _l1_mask(w: Workload, seed: int, layer: int, b: int) -> np.ndarray:
 def _signs(w: Workload, seed: int, layer: int) -> np.ndarray:
     bits = _rng(w, seed, layer, "signs").integers(0, 2, size=w.d)
     return np.where(bits == 1, 1, -1).astype(np.int8)
+
+
+def layer_meta(w: Workload, layer: int = 0, seed: int = 0,
+               batch: Optional[Sequence[int]] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """L1 membership [nb, T] and sign vector [d] of one layer, without its K/V."""
+    bs = list(range(w.B)) if batch is None else list(batch)
+    return np.stack([_l1_mask(w, seed, layer, b) for b in bs]), _signs(w, seed, layer)
 
 
 def queries(w: Workload, layer: int = 0, steps: Optional[int] = None, seed: int = 0,
