@@ -76,8 +76,11 @@ struct EncodeOut {
     const int32_t* prefix;
 };
 
+// (48 resident warps per SM -- 3 CTAs of 16 warps or 6 of 8, 40 registers: the
+// kernel is issue bound and the extra warps hide its memory and shared-memory
+// latencies; 32 warps measured 20 % slower)
 template <int N, bool kBF16>
-__global__ void __launch_bounds__(N * 32) encode_kernel(CacheView c, EncodeOut o, const void* __restrict__ Kp,
+__global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c, EncodeOut o, const void* __restrict__ Kp,
                                                         const void* __restrict__ Vp, Tables tb) {
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
