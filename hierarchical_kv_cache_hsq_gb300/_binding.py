@@ -26,10 +26,10 @@ HSQ_ERR_TIMEOUT, HSQ_ERR_DEVICE_CHECK, HSQ_ERR_UNSUPPORTED = 4, 5, 6
 HSQ_DTYPE_F32, HSQ_DTYPE_BF16 = 0, 1
 HSQ_ATTN_FROM_STAGING = 1
 HSQ_FAULT_ALLOC, HSQ_FAULT_FETCH = 1, 2
-HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER, HSQ_DEVERR_WAIT = 1, 2, 4, 8
+HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER, HSQ_DEVERR_WAIT, HSQ_DEVERR_GROW = 1, 2, 4, 8, 16
 
 BUFFERS = ["l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc", "l2_kn",
-           "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging"]
+           "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging", "win_kv", "gsum"]
 HSQ_NBUF = len(BUFFERS)
 
 
@@ -45,7 +45,7 @@ class hsq_config(ctypes.Structure):
         ("group_n", ctypes.c_int), ("beta", ctypes.c_int), ("bits_l1l3", ctypes.c_int),
         ("bits_l2", ctypes.c_int), ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int),
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
-        ("n_splits", ctypes.c_int),
+        ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
     ]
 
 
@@ -58,6 +58,7 @@ class hsq_cache(ctypes.Structure):
         ("l2_vn", ctypes.c_void_p), ("l2_cnt", ctypes.c_void_p),
         ("l3", ctypes.c_void_p), ("l3_on_host", ctypes.c_int),
         ("l1_bitmap", ctypes.c_void_p), ("signs", ctypes.c_void_p), ("staging", ctypes.c_void_p),
+        ("t_cap", ctypes.c_int), ("win_kv", ctypes.c_void_p), ("gsum", ctypes.c_void_p),
     ]
 
 
@@ -73,6 +74,7 @@ _SIGS = {
     "hsq_fetch_dequant": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
     "hsq_decode_attn": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
     "hsq_decode_step": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
+    "hsq_append": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, ctypes.c_int, _vp]),
     "hsq_sync_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "hsq_route_noalloc": (ctypes.c_int, [ctypes.POINTER(hsq_config), ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp]),
     "hsq_last_error": (ctypes.c_char_p, [_vp]),
@@ -128,10 +130,14 @@ def hsq_codebook(bits: int, dim: int = 128):
 
 
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
-                max_pos: int, theta: float = 1.0e6, n_splits: int = 0) -> hsq_config:
+                max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
+                recent: int = 0) -> hsq_config:
+    """recent > 0 makes caches of this context growable (hsq_append) with an
+    L1 recent window of that length and `sinks` permanent sink positions."""
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
                       bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
-                      max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits)
+                      max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
+                      l1_sinks=sinks, l1_recent=recent)
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:
@@ -202,14 +208,21 @@ class CacheBuffers:
     tensors: Dict[str, "object"]
     signs: "object"
     l3_on_host: bool
+    t_cap: int = 0       # layout capacity in tokens (0: T)
+    recent: int = 0      # recent-window length of a growable cache
+
+    @property
+    def cap(self) -> int:
+        return self.t_cap or self.T
 
     @property
     def G(self) -> int:
-        return -(-self.T // self.N)
+        """Groups of the layout (of the capacity; those past T are empty)."""
+        return -(-self.cap // self.N)
 
     def struct(self) -> hsq_cache:
         t = self.tensors
-        c = hsq_cache(B=self.B, T=self.T, l3_on_host=1 if self.l3_on_host else 0)
+        c = hsq_cache(B=self.B, T=self.T, l3_on_host=1 if self.l3_on_host else 0, t_cap=self.t_cap)
         for name in BUFFERS:
             setattr(c, name, _ptr(t.get(name)))
         c.signs = _ptr(self.signs)
@@ -223,12 +236,13 @@ class CacheBuffers:
             "l1_kc": (B, H, L1, 64), "l1_vc": (B, H, L1, 64), "l1_kn": (B, H, L1), "l1_vn": (B, H, L1),
             "l1_pos": (B, L1), "l1_count": (B,), "l2_kc": (B, H, G, 48), "l2_vc": (B, H, G, 48),
             "l2_kn": (B, H, G), "l2_vn": (B, H, G), "l2_cnt": (B, G), "l3": (B, H, G, N * 136),
-            "l1_bitmap": (B, (self.T + 31) // 32), "staging": (B, H, self.beta, N * 136),
+            "l1_bitmap": (B, (self.cap + 31) // 32), "staging": (B, H, self.beta, N * 136),
+            "win_kv": (B, H, self.recent, 2, 128), "gsum": (B, H, 260),
         }
         import torch
         dt = {"l1_kn": torch.float32, "l1_vn": torch.float32, "l2_kn": torch.float32,
               "l2_vn": torch.float32, "l1_pos": torch.int32, "l1_count": torch.int32,
-              "l1_bitmap": torch.int32}.get(name, torch.uint8)
+              "l1_bitmap": torch.int32, "win_kv": torch.float32, "gsum": torch.float32}.get(name, torch.uint8)
         n = int(np.prod(shapes[name]))
         return t.view(dt)[:n].view(shapes[name])
 
@@ -245,14 +259,19 @@ def l1_bitmap_words(mask: np.ndarray) -> np.ndarray:
 
 
 def allocate_cache(ctx: Context, B: int, T: int, l3_on_host: bool = True, with_staging: bool = True,
-                   device=None) -> CacheBuffers:
+                   device=None, t_cap: Optional[int] = None) -> CacheBuffers:
+    """Buffers for B sequences of T tokens, laid out for t_cap tokens (default T;
+    a growable cache -- ctx.cfg.l1_recent > 0 -- gets its growth state too)."""
     import torch
     dev = torch.device("cuda") if device is None else torch.device(device)
-    sizes = hsq_cache_sizes(ctx.cfg, B, T)
+    cap = T if t_cap is None else t_cap
+    sizes = hsq_cache_sizes(ctx.cfg, B, cap)
     t = {}
     for name in BUFFERS:
         n = max(sizes[name], 16)
         if name == "staging" and not with_staging:
+            continue
+        if name in ("win_kv", "gsum") and sizes[name] == 0:
             continue
         if name == "l3" and l3_on_host:
             t[name] = torch.zeros(n, dtype=torch.uint8, pin_memory=True)
@@ -260,15 +279,21 @@ def allocate_cache(ctx: Context, B: int, T: int, l3_on_host: bool = True, with_s
             t[name] = torch.zeros(n, dtype=torch.uint8, device=dev)
     signs = torch.ones(128, dtype=torch.int8, device=dev)
     return CacheBuffers(B=B, T=T, N=ctx.cfg.group_n, Hkv=ctx.cfg.n_kv_heads, max_l1=ctx.cfg.max_l1,
-                        beta=ctx.cfg.beta, tensors=t, signs=signs, l3_on_host=l3_on_host)
+                        beta=ctx.cfg.beta, tensors=t, signs=signs, l3_on_host=l3_on_host,
+                        t_cap=0 if cap == T else cap, recent=ctx.cfg.l1_recent)
 
 
 def set_layer_inputs(cache: CacheBuffers, l1_mask: np.ndarray, signs: np.ndarray):
     """Upload the L1 membership bitmap and the sign vector of a layer."""
     import torch
     words = l1_bitmap_words(l1_mask)
+    Wc = (cache.cap + 31) // 32  # one row per sequence at the layout's stride
+    if words.shape[1] > Wc:
+        raise ValueError("L1 mask longer than the cache capacity")
+    rows = np.zeros((words.shape[0], Wc), np.uint32)
+    rows[:, : words.shape[1]] = words
     bm = cache.tensors["l1_bitmap"]
-    src = torch.from_numpy(words.view(np.uint8).reshape(-1).copy())
+    src = torch.from_numpy(rows.view(np.uint8).reshape(-1).copy())
     bm[: src.numel()].copy_(src)
     cache.signs.copy_(torch.from_numpy(np.asarray(signs, np.int8)))
 
@@ -288,6 +313,24 @@ def hsq_encode(ctx: Context, cache: CacheBuffers, K, V, stream=None):
     c = cache.struct()
     _check(ctx.lib.hsq_encode(ctx.handle, ctypes.byref(c), K.data_ptr(), V.data_ptr(), dt,
                               _stream_handle(stream)), ctx.handle)
+
+
+def hsq_append(ctx: Context, cache: CacheBuffers, k, v, stream=None):
+    """Append one token per sequence (k, v: [B, Hkv, 128], pre-RoPE) at position
+    cache.T; cache.T grows by one."""
+    import torch
+    if k.dtype == torch.bfloat16:
+        dt = HSQ_DTYPE_BF16
+    elif k.dtype == torch.float32:
+        dt = HSQ_DTYPE_F32
+    else:
+        raise ValueError("k/v must be bfloat16 or float32")
+    if not (k.is_contiguous() and v.is_contiguous() and v.dtype == k.dtype):
+        raise ValueError("k and v must be contiguous and of one dtype")
+    c = cache.struct()
+    _check(ctx.lib.hsq_append(ctx.handle, ctypes.byref(c), k.data_ptr(), v.data_ptr(), dt,
+                              _stream_handle(stream)), ctx.handle)
+    cache.T = c.T
 
 
 def hsq_route(ctx: Context, cache: CacheBuffers, q, pos, sel, scores=None, stream=None):

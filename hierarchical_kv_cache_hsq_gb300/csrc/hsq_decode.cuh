@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
     const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
     constexpr int fl = kStaged ? kStagedFlags : 0;
-    const DecodeLayout L = decode_layout<R, N>(c.G, c.T, S, c.max_l1, c.beta, kRoute, fl);
+    const DecodeLayout L = decode_layout<R, N>(c.G, c.cap, S, c.max_l1, c.beta, kRoute, fl);
 
     const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
     const int n2 = g1 - g0;
@@ -761,8 +761,8 @@ int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
     return last;
 }
 
-// Launch plan for B sequences of T tokens (cached per shape): staged inputs
-// when some cluster size fits shared memory, else in place.
+// Launch plan for B sequences laid out for T tokens (the capacity; cached per
+// shape): staged inputs when some cluster size fits shared memory, else in place.
 template <int R, int N, bool kRoute>
 hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T) {
     for (const auto& e : ctx->plans)
@@ -785,7 +785,7 @@ hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T) {
 template <int R, int N, bool kRoute, bool kStaged>
 hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
     const DecodeLayout L =
-        decode_layout<R, N>(v.G, v.T, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
+        decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
     const void* fn = (const void*)decode_kernel<R, N, kRoute, kStaged>;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
@@ -801,7 +801,7 @@ template <int R, int N>
 hsq_status decode_run_n(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, bool route, cudaStream_t st,
                         bool* launched) {
     *launched = false;
-    const hsq_ctx::Plan p = route ? decode_plan<R, N, true>(ctx, v.B, v.T) : decode_plan<R, N, false>(ctx, v.B, v.T);
+    const hsq_ctx::Plan p = route ? decode_plan<R, N, true>(ctx, v.B, v.cap) : decode_plan<R, N, false>(ctx, v.B, v.cap);
     if (p.S == 0) return HSQ_OK;
     *launched = true;
     if (route) return p.staged ? launch_decode<R, N, true, true>(ctx, v, a, p.S, st)

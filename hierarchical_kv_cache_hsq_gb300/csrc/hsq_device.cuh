@@ -56,6 +56,7 @@ struct Tables {
 
 struct CacheView {
     int B, T, G, N, Hkv, Hq, beta, max_l1, W;
+    int cap;  // tokens the layout is sized for (G = ceil(cap / N) groups, W = ceil(cap / 32) words)
     const uint8_t* l1_kc; const uint8_t* l1_vc; const float* l1_kn; const float* l1_vn;
     const int32_t* l1_pos; const int32_t* l1_count;
     const uint8_t* l2_kc; const uint8_t* l2_vc; const float* l2_kn; const float* l2_vn;
@@ -789,9 +790,11 @@ __device__ __forceinline__ int valid_sel(const int32_t* __restrict__ row, int i,
 // Kernel-side views of a context and a cache (host helpers).
 inline CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
     CacheView v{};
-    v.B = c->B; v.T = c->T; v.N = ctx->cfg.group_n; v.G = hsq::groups_of(c->T, v.N);
+    // layout strides follow the capacity; groups and bitmap words past T are empty
+    const int cap = c->t_cap > 0 ? c->t_cap : c->T;
+    v.B = c->B; v.T = c->T; v.N = ctx->cfg.group_n; v.G = hsq::groups_of(cap, v.N);
     v.Hkv = ctx->cfg.n_kv_heads; v.Hq = ctx->cfg.n_q_heads; v.beta = ctx->cfg.beta;
-    v.max_l1 = ctx->cfg.max_l1; v.W = hsq::bitmap_words(c->T);
+    v.max_l1 = ctx->cfg.max_l1; v.W = hsq::bitmap_words(cap); v.cap = cap;
     v.l1_kc = c->l1_kc; v.l1_vc = c->l1_vc; v.l1_kn = c->l1_kn; v.l1_vn = c->l1_vn;
     v.l1_pos = c->l1_pos; v.l1_count = c->l1_count;
     v.l2_kc = c->l2_kc; v.l2_vc = c->l2_vc; v.l2_kn = c->l2_kn; v.l2_vn = c->l2_vn; v.l2_cnt = c->l2_cnt;

@@ -173,6 +173,9 @@ std::string check_config(const hsq_config* c) {
     if ((long long)c->max_ctx > (1LL << 24)) return "max_ctx too large";
     if ((c->max_ctx + c->group_n - 1) / c->group_n > 32768) return "more than 32768 groups per sequence";
     if (c->n_splits < 0 || c->n_splits > HSQ_MAX_SPLITS) return "n_splits must be in [0, 16]";
+    if (c->l1_sinks < 0 || c->l1_recent < 0) return "l1_sinks and l1_recent must be >= 0";
+    if (c->l1_recent > 0 && (long long)c->l1_sinks + c->l1_recent > c->max_l1)
+        return "l1_sinks + l1_recent must fit max_l1";
     return "";
 }
 
@@ -180,6 +183,7 @@ std::string check_cache_shape(const hsq_config* cfg, const hsq_cache* c) {
     if (!c) return "cache is NULL";
     if (c->B < 1 || c->B > cfg->max_batch) return "cache B out of range";
     if (c->T < 1 || c->T > cfg->max_ctx) return "cache T out of range";
+    if (c->t_cap != 0 && (c->t_cap < c->T || c->t_cap > cfg->max_ctx)) return "cache t_cap out of range";
     if (!c->l1_kc || !c->l1_vc || !c->l1_kn || !c->l1_vn || !c->l1_pos || !c->l1_count)
         return "an L1 buffer is NULL";
     if (!c->l2_kc || !c->l2_vc || !c->l2_kn || !c->l2_vn || !c->l2_cnt) return "an L2 buffer is NULL";
@@ -229,6 +233,8 @@ hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ
     bytes[HSQ_BUF_L3] = B * H * G * hsq::record_bytes((int)N);
     bytes[HSQ_BUF_L1_BITMAP] = (size_t)B * hsq::bitmap_words(T) * 4;
     bytes[HSQ_BUF_STAGING] = B * H * (size_t)cfg->beta * hsq::record_bytes((int)N);
+    bytes[HSQ_BUF_WIN_KV] = B * H * (size_t)cfg->l1_recent * 2 * hsq::kDim * 4;
+    bytes[HSQ_BUF_GSUM] = cfg->l1_recent > 0 ? B * H * (size_t)hsq::kGsumFloats * 4 : 0;
     return HSQ_OK;
 }
 

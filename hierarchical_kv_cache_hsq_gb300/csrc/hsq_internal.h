@@ -15,6 +15,7 @@ constexpr int kDim = 128;
 constexpr int kRopeLoRows = 256;            // positions p & 255
 constexpr int kRopeRowFloats = kDim;        // cos[64] | sin[64]
 constexpr int kCodebookFloats = 48;         // c4[16] | t4[15] pad | c3[8] | t3[7] pad
+constexpr int kGsumFloats = 2 * 128 + 4;    // growth sums: RoPE'd keys | values | count | pad
 constexpr int kPartStride = 132;            // acc[128] | m | l | pad | pad
 
 inline int groups_of(int T, int N) { return (T + N - 1) / N; }

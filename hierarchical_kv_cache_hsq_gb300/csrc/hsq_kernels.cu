@@ -38,10 +38,10 @@ __global__ void __launch_bounds__(1024) l1_index_kernel(CacheView c, int32_t* __
     const int W = c.W;
     const int per = (W + blockDim.x - 1) / blockDim.x;
     const int w0 = min(W, (int)threadIdx.x * per), w1 = min(W, w0 + per);
-    auto word = [&](int w) -> uint32_t {
+    auto word = [&](int w) -> uint32_t {  // bits at t >= T (up to the capacity) do not count
         uint32_t x = c.l1_bitmap[(size_t)b * W + w];
         const int valid = c.T - 32 * w;
-        if (valid < 32) x &= (1u << valid) - 1u;
+        if (valid < 32) x = valid <= 0 ? 0u : x & ((1u << valid) - 1u);
         return x;
     };
     int local = 0;
@@ -74,7 +74,32 @@ struct EncodeOut {
     uint8_t* l2_kc; uint8_t* l2_vc; float* l2_kn; float* l2_vn; uint8_t* l2_cnt;
     uint8_t* l3;
     const int32_t* prefix;
+    float* win_kv; float* gsum; int recent;  // growth state (win_kv NULL: none)
 };
+
+// TQ3 of one group summary (this half-warp's 8 dims of the mean; x is
+// overwritten) into its 48-byte code row and its norm.  w: this half's 12
+// shared words, zero on entry; the whole warp is converged (both halves call it).
+__device__ __forceinline__ void write_summary(float x[8], const float sg[8], unsigned m, const float* t3,
+                                              uint32_t* w, uint8_t* codes, float* norm) {
+    const int l = hlane();
+    float ys[8];
+    const float ns = tq_rotate(x, ys, sg, m);
+    uint32_t fa = 0, fb = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        fa |= (uint32_t)quant3(ys[k], t3) << (3 * k);
+        fb |= (uint32_t)quant3(ys[4 + k], t3) << (3 * k);
+    }
+    const int bit = 12 * l, wi = bit >> 5, sh = bit & 31;
+    atomicOr(&w[wi], fa << sh);
+    if (sh > 20) atomicOr(&w[wi + 1], fa >> (32 - sh));
+    atomicOr(&w[6 + wi], fb << sh);
+    if (sh > 20) atomicOr(&w[6 + wi + 1], fb >> (32 - sh));
+    __syncwarp();
+    if (l < 12) reinterpret_cast<uint32_t*>(codes)[l] = w[l];
+    if (l == 0) *norm = ns;
+}
 
 // (48 resident warps per SM -- 3 CTAs of 16 warps or 6 of 8, 40 registers: the
 // kernel is issue bound and the extra warps hide its memory and shared-memory
@@ -118,6 +143,13 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = 0.f;
+    }
+
+    // the recent window's inputs, for decode-time growth (slot t mod recent)
+    if (o.win_kv && in_ctx && t >= c.T - o.recent) {
+        float* wp = o.win_kv + ((((size_t)b * c.Hkv + h) * o.recent + t % o.recent) * 2 + half) * kDim;
+        *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
     }
 
     // L3: TQ4 of the raw (pre-RoPE) key / value
@@ -186,31 +218,171 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
             acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
             acc[4] += bq.x; acc[5] += bq.y; acc[6] += bq.z; acc[7] += bq.w;
         }
+        // growth: the running sums of the group holding position T - recent
+        // (its members below that position; zero when no token has left yet)
+        const int p_next = c.T - o.recent;
+        if (o.win_kv && (p_next >= 0 ? g == p_next / N : g == 0)) {
+            float* gs = o.gsum + ((size_t)b * c.Hkv + h) * hsq::kGsumFloats;
+            const bool keep = p_next >= 0;
+            *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) =
+                keep ? make_float4(acc[0], acc[1], acc[2], acc[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) =
+                keep ? make_float4(acc[4], acc[5], acc[6], acc[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (threadIdx.x == 0) gs[2 * kDim] = keep ? (float)cnt : 0.f;
+        }
         if (cnt > 0) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         }
-        float ys[8];
-        const float ns = tq_rotate(acc, ys, sg, m);
-        uint32_t fa = 0, fb = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            fa |= (uint32_t)quant3(ys[k], t3) << (3 * k);
-            fb |= (uint32_t)quant3(ys[4 + k], t3) << (3 * k);
-        }
-        uint32_t* w = s_l2[half];
-        const int bit = 12 * l, wi = bit >> 5, sh = bit & 31;
-        atomicOr(&w[wi], fa << sh);
-        if (sh > 20) atomicOr(&w[wi + 1], fa >> (32 - sh));
-        atomicOr(&w[6 + wi], fb << sh);
-        if (sh > 20) atomicOr(&w[6 + wi + 1], fb >> (32 - sh));
-        __syncwarp();
         const size_t go = ((size_t)b * c.Hkv + h) * c.G + g;
-        uint32_t* dst = reinterpret_cast<uint32_t*>((half ? o.l2_vc : o.l2_kc) + go * 48);
-        if (l < 12) dst[l] = w[l];
-        if (l == 0) (half ? o.l2_vn : o.l2_kn)[go] = ns;
+        write_summary(acc, sg, m, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+                      (half ? o.l2_vn : o.l2_kn) + go);
         if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
     }
+}
+
+// ---------------------------------------------------------------------------
+// Decode-time growth (append one token per sequence at position T).
+// Stage 1, one warp per sequence: the L1 slot of the new token -- the slot of
+// the token p = T - recent that leaves the window (found in l1_pos), or a new
+// slot when nothing leaves -- and the bitmap and position-list updates.
+// slot_out[b] = slot | (leaves << 30), or -1 when L1 is left unchanged.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(32) append_index_kernel(CacheView c, int32_t* l1_pos, int32_t* l1_count,
+                                                          uint32_t* l1_bitmap, int sinks, int recent,
+                                                          int* slot_out, int* err) {
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int t = c.T, p = t - recent;
+    int32_t* pos = l1_pos + (size_t)b * c.max_l1;
+    const int cnt = min(__ldcg(l1_count + b), c.max_l1);
+    int slot = -1, leaves = 0;
+    if (p >= 0 && p >= sinks) {
+        int found = -1;
+#pragma unroll 1
+        for (int i0 = 0; i0 < cnt; i0 += 32) {  // warp-uniform bound
+            const int i = i0 + lane;
+            const unsigned hit = __ballot_sync(kFull, i < cnt && __ldcg(pos + min(i, cnt - 1)) == p);
+            if (hit) {
+                found = i0 + __ffs(hit) - 1;
+                break;
+            }
+        }
+        if (found >= 0) {
+            slot = found;
+            leaves = 1;
+        } else if (lane == 0) {
+            atomicOr(err, HSQ_DEVERR_GROW);
+        }
+    } else if (cnt < c.max_l1) {
+        slot = cnt;
+        if (lane == 0) l1_count[b] = cnt + 1;
+    } else if (lane == 0) {
+        atomicOr(err, HSQ_DEVERR_L1_OVER);
+    }
+    if (lane == 0) {
+        uint32_t* bm = l1_bitmap + (size_t)b * c.W;
+        if (slot >= 0) {
+            pos[slot] = t;
+            atomicOr(bm + (t >> 5), 1u << (t & 31));
+        }
+        if (leaves) atomicAnd(bm + (p >> 5), ~(1u << (p & 31)));
+        slot_out[b] = slot >= 0 ? (slot | (leaves << 30)) : -1;
+    }
+}
+
+// Stage 2, one warp per (KV head h, sequence b); half 0 takes the key, half 1
+// the value: the new token's L3 record slot and L1 entry, then -- when p
+// leaves the window -- p joins group p / N: its input (from the window ring)
+// is added to the group's running sums in position order and the summary is
+// re-quantised, as the encode of the longer context computes it.
+template <int N, bool kBF16>
+__global__ void __launch_bounds__(32) append_kernel(CacheView c, EncodeOut o, const void* __restrict__ kp,
+                                                    const void* __restrict__ vp, Tables tb, int recent,
+                                                    const int* __restrict__ slot_in) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ uint32_t s_l2[2][12];
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int half = (threadIdx.x >> 4) & 1, l = hlane();
+    const unsigned m = half_mask();
+    load_tables(s_cb, s_sign, tb, c.signs);
+    if (threadIdx.x < 24) (&s_l2[0][0])[threadIdx.x] = 0u;
+    __syncthreads();
+    const float* t4 = s_cb + 16;
+    const float* t3 = s_cb + 40;
+    float sg[8];
+    load_signs(sg, s_sign);
+    const int t = c.T, p = t - recent;
+    const int sc = __ldcg(slot_in + b);
+    const int slot = sc < 0 ? -1 : (sc & 0x3FFFFFFF);
+    const bool leaves = sc >= 0 && ((sc >> 30) & 1);
+    const size_t bh = (size_t)b * c.Hkv + h;
+
+    float x[8];
+    if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? vp : kp) + bh * kDim, x);
+    else load_f32x8(static_cast<const float*>(half ? vp : kp) + bh * kDim, x);
+
+    // L3 record slot t: TQ4 of the raw key / value
+    float y[8];
+    const float n = tq_rotate(x, y, sg, m);
+    uint16_t lo, hi;
+    pack4(y, t4, lo, hi);
+    {
+        uint8_t* rec = o.l3 + (bh * c.G + t / N) * (N * 136);
+        uint8_t* row = rec + (half ? N * 64 : 0) + (t % N) * 64;
+        reinterpret_cast<uint16_t*>(row)[l] = lo;
+        reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
+        if (l == 0) reinterpret_cast<float*>(rec + N * 128)[half * N + t % N] = n;
+    }
+    // L1 entry (RoPE'd key, value as coded for L3)
+    if (slot >= 0) {
+        const size_t so = bh * c.max_l1 + slot;
+        if (half == 0) {
+            float xr[8], yr[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xr[i] = x[i];
+            rope(xr, t, tb);
+            tq_rotate(xr, yr, sg, m);
+            uint16_t klo, khi;
+            pack4(yr, t4, klo, khi);
+            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
+            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64 + 32)[l] = khi;
+            if (l == 0) o.l1_kn[so] = n;
+        } else {
+            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64)[l] = lo;
+            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64 + 32)[l] = hi;
+            if (l == 0) o.l1_vn[so] = n;
+        }
+    }
+    float* wp = o.win_kv + ((bh * recent + (size_t)(t % recent)) * 2 + half) * kDim;  // = p's slot
+    if (leaves) {
+        float xp[8];
+        load_f32x8_cg(wp, xp);
+        if (half == 0) rope(xp, p, tb);
+        float* gs = o.gsum + bh * hsq::kGsumFloats;
+        const bool fresh = p % N == 0;  // p opens its group: nothing summed before it
+        float acc[8];
+        float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 4 * l));
+        float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
+                          : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 64 + 4 * l));
+        acc[0] = a.x + xp[0]; acc[1] = a.y + xp[1]; acc[2] = a.z + xp[2]; acc[3] = a.w + xp[3];
+        acc[4] = bq.x + xp[4]; acc[5] = bq.y + xp[5]; acc[6] = bq.z + xp[6]; acc[7] = bq.w + xp[7];
+        const int cnt = (fresh ? 0 : (int)__ldcg(gs + 2 * kDim)) + 1;
+        __syncwarp();  // every lane has read the count before lane 0 rewrites it
+        *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if (threadIdx.x == 0) gs[2 * kDim] = (float)cnt;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
+        const int gp = p / N;
+        const size_t go = bh * c.G + gp;
+        write_summary(acc, sg, m, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48, (half ? o.l2_vn : o.l2_kn) + go);
+        if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
+    }
+    __syncwarp();  // p's inputs are read before t's replace them
+    *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
 }
 
 // ---------------------------------------------------------------------------
@@ -496,7 +668,7 @@ hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
 }
 
 void free_ctx(hsq_ctx* c) {
-    cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
+    cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores); cudaFree(c->d_slot);
     cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err);
     delete c;
 }
@@ -547,6 +719,7 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(prefix)");
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
+    if ((e = cudaMalloc(&c->d_slot, (size_t)cfg->max_batch * 4)) != cudaSuccess) return bail(e, "cudaMalloc(slots)");
     if ((e = cudaMemcpy(c->d_cb, cb, sizeof(cb), cudaMemcpyHostToDevice)) != cudaSuccess) return bail(e, "upload");
     if ((e = cudaMemcpy(c->d_rope_hi, hi.data(), hi.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(e, "upload");
@@ -582,8 +755,10 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     CacheView v = make_view(ctx, cache);
     l1_index_kernel<<<v.B, 1024, 0, s>>>(v, cache->l1_pos, cache->l1_count, ctx->d_prefix, ctx->d_err);
+    const bool grow = ctx->cfg.l1_recent > 0 && cache->win_kv && cache->gsum;
     EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
-                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix};
+                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix,
+                grow ? cache->win_kv : nullptr, grow ? cache->gsum : nullptr, ctx->cfg.l1_recent};
     dim3 grid(v.G, v.Hkv, v.B);
     const Tables tb = make_tables(ctx);
     if (v.N == 16) {
@@ -594,6 +769,40 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
         else encode_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, o, K, V, tb);
     }
     return after_launch(ctx, "encode");
+}
+
+hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void* v, hsq_dtype dtype,
+                      hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!k || !v) return fail(ctx, HSQ_ERR_INVALID, "k or v is NULL");
+    if (dtype != HSQ_DTYPE_F32 && dtype != HSQ_DTYPE_BF16) return fail(ctx, HSQ_ERR_INVALID, "bad dtype");
+    const int recent = ctx->cfg.l1_recent;
+    if (recent < 1) return fail(ctx, HSQ_ERR_INVALID, "the context has no recent window (l1_recent = 0)");
+    if (!cache->win_kv || !cache->gsum) return fail(ctx, HSQ_ERR_INVALID, "win_kv or gsum is NULL");
+    const int cap = cache->t_cap > 0 ? cache->t_cap : cache->T;
+    if (cache->T >= cap) return fail(ctx, HSQ_ERR_INVALID, "the cache is full (T == t_cap)");
+    if (cache->T >= ctx->cfg.max_pos) return fail(ctx, HSQ_ERR_INVALID, "position T reaches max_pos");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const CacheView vw = make_view(ctx, cache);
+    append_index_kernel<<<vw.B, 32, 0, s>>>(vw, cache->l1_pos, cache->l1_count, cache->l1_bitmap,
+                                            ctx->cfg.l1_sinks, recent, ctx->d_slot, ctx->d_err);
+    EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
+                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, nullptr, cache->win_kv, cache->gsum,
+                recent};
+    const dim3 grid(vw.Hkv, vw.B);
+    const Tables tb = make_tables(ctx);
+    const bool bf = dtype == HSQ_DTYPE_BF16;
+    if (vw.N == 16) {
+        if (bf) append_kernel<16, true><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+        else append_kernel<16, false><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+    } else {
+        if (bf) append_kernel<8, true><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+        else append_kernel<8, false><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+    }
+    st = after_launch(ctx, "append");
+    if (st == HSQ_OK) cache->T += 1;
+    return st;
 }
 
 hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
@@ -928,7 +1137,8 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     const int r = cfg->n_q_heads / cfg->n_kv_heads;
     if (!r_supported(r)) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "r = Hq/Hkv must be 1, 2, 4, 5 or 8");
     const size_t bh = (size_t)cache->B * cfg->n_kv_heads;
-    const size_t G = (size_t)hsq::groups_of(cache->T, cfg->group_n);
+    const int cap = cache->t_cap > 0 ? cache->t_cap : cache->T;  // the layout's capacity
+    const size_t G = (size_t)hsq::groups_of(cap, cfg->group_n);
     const size_t ticket_bytes = (bh * 4 + 255) / 256 * 256;
     if (ticket_bytes + bh * G * 4 > (size_t)HSQ_NOALLOC_SCRATCH_BYTES)
         return fail(nullptr, HSQ_ERR_INVALID,
@@ -946,7 +1156,7 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     CacheView v{};
     v.B = cache->B; v.T = cache->T; v.N = cfg->group_n; v.G = (int)G;
     v.Hkv = cfg->n_kv_heads; v.Hq = cfg->n_q_heads; v.beta = cfg->beta;
-    v.max_l1 = cfg->max_l1; v.W = hsq::bitmap_words(cache->T);
+    v.max_l1 = cfg->max_l1; v.W = hsq::bitmap_words(cap); v.cap = cap;
     v.l2_kc = cache->l2_kc; v.l2_kn = cache->l2_kn; v.l2_cnt = cache->l2_cnt; v.signs = cache->signs;
     RouteArgs a{q, pos, sel, reinterpret_cast<float*>(scratch + ticket_bytes),
                 reinterpret_cast<int*>(scratch), nullptr};

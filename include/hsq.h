@@ -75,8 +75,10 @@ enum {
     HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
     HSQ_DEVERR_POS = 2,       /* position outside [0, max_pos): clamped */
     HSQ_DEVERR_L1_OVER = 4,   /* more L1 tokens than max_l1: extra tokens dropped from L1 */
-    HSQ_DEVERR_WAIT = 8       /* reserved: no kernel of this version waits on another CTA
+    HSQ_DEVERR_WAIT = 8,      /* reserved: no kernel of this version waits on another CTA
                                  outside its own thread-block cluster */
+    HSQ_DEVERR_GROW = 16      /* hsq_append: the token leaving the recent window was not in L1
+                                 (the cache was not encoded with that window): L1 left as is */
 };
 
 /* Flags of hsq_decode_attn. */
@@ -107,6 +109,11 @@ typedef struct hsq_config {
     int max_pos;        /* exclusive bound on positions (context + decode steps), <= 2^24 */
     int n_splits;       /* decode splits (CTAs of one thread-block cluster) per (b, KV head):
                            0 = automatic, else an upper bound in [1, HSQ_MAX_SPLITS] */
+    /* Decode-time growth (hsq_append).  The L1 set then is: positions below
+       l1_sinks, the positions marked at encode time, and the recent window
+       [T - l1_recent, T), which slides by one with every appended token. */
+    int l1_sinks;       /* >= 0 */
+    int l1_recent;      /* >= 0; 0 = caches of this context do not grow */
 } hsq_config;
 
 /*
@@ -124,7 +131,7 @@ typedef struct hsq_cache {
     uint8_t* l1_vc;           /* [B][Hkv][max_l1][64]  4-bit codes of v_t */
     float* l1_kn;             /* [B][Hkv][max_l1]      key norms */
     float* l1_vn;             /* [B][Hkv][max_l1]      value norms */
-    int32_t* l1_pos;          /* [B][max_l1]           ascending L1 positions */
+    int32_t* l1_pos;          /* [B][max_l1]           L1 positions (ascending after encode) */
     int32_t* l1_count;        /* [B]                   L1 size per sequence */
     /* L2 summary tier */
     uint8_t* l2_kc;           /* [B][Hkv][G][48]  3-bit codes of the members' mean RoPE'd key */
@@ -138,16 +145,28 @@ typedef struct hsq_cache {
     uint8_t* l3;
     int l3_on_host;           /* 1 = page-locked host memory, 0 = device memory */
     /* L1 membership: bit (t & 31) of word [b][t >> 5]; bits at t >= T are ignored */
-    const uint32_t* l1_bitmap;/* [B][ceil(T/32)] device */
+    uint32_t* l1_bitmap;      /* [B][ceil(t_cap/32)] device (hsq_append updates it) */
     const int8_t* signs;      /* [128] device, +-1: the layer's Walsh-Hadamard sign vector */
     uint8_t* staging;         /* [B][Hkv][beta][N*136] device, or NULL (only needed for the
                                  staged fetch path) */
+    /* Capacity and decode-time growth state (hsq_append). */
+    int t_cap;                /* tokens the buffers are laid out for, T <= t_cap <= max_ctx
+                                 (0 = T): every G above is ceil(t_cap / N) and the bitmap has
+                                 ceil(t_cap / 32) words per sequence; groups past T are empty */
+    float* win_kv;            /* [B][Hkv][l1_recent][2][128] device, or NULL: the input (pre-RoPE)
+                                 key and the value of each recent-window token, slot p mod
+                                 l1_recent; written by hsq_encode, read and written by hsq_append */
+    float* gsum;              /* [B][Hkv][260] device, or NULL: for the group holding position
+                                 T - l1_recent, the float sums, in position order, of its members
+                                 below that position: RoPE'd keys [128] | values [128] | member
+                                 count | pad [3] */
 } hsq_cache;
 
 typedef enum {
     HSQ_BUF_L1_KC = 0, HSQ_BUF_L1_VC, HSQ_BUF_L1_KN, HSQ_BUF_L1_VN, HSQ_BUF_L1_POS,
     HSQ_BUF_L1_COUNT, HSQ_BUF_L2_KC, HSQ_BUF_L2_VC, HSQ_BUF_L2_KN, HSQ_BUF_L2_VN,
-    HSQ_BUF_L2_CNT, HSQ_BUF_L3, HSQ_BUF_L1_BITMAP, HSQ_BUF_STAGING, HSQ_NBUF
+    HSQ_BUF_L2_CNT, HSQ_BUF_L3, HSQ_BUF_L1_BITMAP, HSQ_BUF_STAGING, HSQ_BUF_WIN_KV,
+    HSQ_BUF_GSUM, HSQ_NBUF
 } hsq_buffer;
 
 typedef struct hsq_ctx hsq_ctx;   /* opaque, library-owned */
@@ -165,7 +184,9 @@ hsq_status hsq_codebook(int bits, int dim, double* centroids, double* boundaries
 
 /*
  * hsq_cache_sizes -- bytes of each buffer of a cache with B sequences of T
- *   tokens under cfg, indexed by enum hsq_buffer.  Needs no GPU.
+ *   tokens under cfg, indexed by enum hsq_buffer (for a cache that grows, T
+ *   is its capacity t_cap; the growth buffers are 0 bytes when l1_recent is
+ *   0).  Needs no GPU.
  *   Errors: HSQ_ERR_INVALID (bad cfg, B or T).
  */
 hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ_NBUF]);
@@ -193,13 +214,39 @@ hsq_status hsq_destroy(hsq_ctx* ctx);
  *     L1 slot i (ascending position order): TQ4(RoPE(k_t, t)), TQ4(v_t);
  *     L2 group g: TQ3(mean of RoPE(k_t, t)), TQ3(mean of v_t) over members,
  *       count in l2_cnt; an empty group stores the zero vector.
- *   If l3_on_host, the records are written through the host link.
+ *   If l3_on_host, the records are written through the host link.  With
+ *   cfg.l1_recent > 0 and win_kv / gsum set, it also stores the growth state
+ *   that hsq_append continues from (the recent window's inputs and the
+ *   running sums of the group at the window's trailing edge).  Groups and
+ *   records past T (up to t_cap) are written empty.
  *   Errors: HSQ_ERR_INVALID (null pointer, B/T out of range, L3 location not
  *   matching l3_on_host), HSQ_ERR_CUDA.  An L1 set larger than max_l1 sets
  *   HSQ_DEVERR_L1_OVER.
  */
 hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const void* V,
                       hsq_dtype dtype, hsq_stream_t stream);
+
+/*
+ * hsq_append -- decode-time growth: append one token per sequence at
+ *   position T (cache->T, the same for all B sequences), then T += 1 in
+ *   *cache.  The pages build the three tiers from a context and leave their
+ *   growth open; this call keeps the cache equal to what hsq_encode would
+ *   build from the longer context with the L1 set of hsq_config (sinks,
+ *   marked positions, and the recent window [T + 1 - l1_recent, T + 1)):
+ *     L3 record slot T: TQ4(k) and TQ4(v);
+ *     L1: TQ4(RoPE(k, T)) and TQ4(v) in the slot of the token p = T - l1_recent
+ *       that leaves the window (a new slot when p < max(l1_sinks, 0));
+ *     p joins group p / N: its summary is re-quantised from the members'
+ *       running float sums (position order, as hsq_encode sums them);
+ *     the L1 bitmap, positions and counts and l2_cnt follow.
+ *   k, v: device [B][Hkv][128] of dtype, pre-RoPE.  Needs cfg.l1_recent > 0,
+ *   cache->win_kv and cache->gsum (filled by hsq_encode under this cfg),
+ *   T < t_cap and T < max_pos.  L1 slots are then no longer in position
+ *   order (l1_pos holds each slot's position).  Errors: HSQ_ERR_INVALID,
+ *   HSQ_ERR_CUDA; device checks HSQ_DEVERR_GROW, HSQ_DEVERR_L1_OVER.
+ */
+hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void* v, hsq_dtype dtype,
+                      hsq_stream_t stream);
 
 /*
  * hsq_route -- per-head routing and top-beta group selection (decode

@@ -44,7 +44,12 @@ Readings where the pages are silent (each also listed in the design notes):
   * Attention: for each query head, one softmax (scale 1/sqrt(d)) over L1
     tokens, unselected non-empty summaries (one entry each, no count bias)
     and the selected groups' non-L1 tokens recovered from L3 and rotated to
-    their positions.  The cache is frozen after encode.
+    their positions.
+  * Decode-time growth (the pages describe the tiers of a context and leave
+    their growth open): a cache grown by appended tokens is, by definition,
+    the encode of the longer context under the grown L1 set (grown_l1_mask):
+    sinks, the positions marked at encode time, and the recent window at
+    the new length.  The oracle therefore grows a cache by encoding again.
 """
 
 from __future__ import annotations
@@ -58,6 +63,7 @@ from scipy import special
 
 __all__ = [
     "D",
+    "grown_l1_mask",
     "coordinate_pdf",
     "coordinate_cdf",
     "coordinate_cell_mass",
@@ -375,6 +381,25 @@ def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray,
         l3_k=_store(K, 4, Pi, quantize), l3_v=_store(V, 4, Pi, quantize),
         quantized=quantize,
     )
+
+
+def grown_l1_mask(l1_mask: np.ndarray, T_new: int, sinks: int, recent: int) -> np.ndarray:
+    """[HSQ] three-tier architecture, L1 focal tier (attention sinks, an
+    optional recent window, reader-marked tokens), after the context grows
+    from T = l1_mask.shape[1] to T_new tokens: the sinks [0, sinks), every
+    L1 position of the encode-time mask below the encode-time window
+    [T - recent, T) (the marked ones), and the window [T_new - recent, T_new)."""
+    l1_mask = np.asarray(l1_mask, dtype=bool)
+    B, T = l1_mask.shape
+    if T_new < T:
+        raise ValueError("a cache only grows")
+    out = np.zeros((B, T_new), dtype=bool)
+    kept = l1_mask.copy()
+    kept[:, max(T - recent, 0):] = False          # the old window slides on
+    out[:, :T] = kept
+    out[:, : min(sinks, T_new)] = True
+    out[:, max(T_new - recent, 0):] = True
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -62,12 +62,16 @@ def test_cache_sizes(H):
     assert s["staging"] == 2 * 8 * 64 * 2176
     s2 = H.hsq_cache_sizes(cfg, 1, 1000)  # ragged: G = ceil(1000 / 16) = 63
     assert s2["l2_kc"] == 8 * 63 * 48 and s2["l1_bitmap"] == 32 * 4
+    assert s["win_kv"] == 0 and s["gsum"] == 0  # not growable: no growth state
+    g = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 32768, 600, 40000, sinks=4, recent=256), 2, 32768)
+    assert g["win_kv"] == 2 * 8 * 256 * 2 * 128 * 4  # the window's input K and V, float
+    assert g["gsum"] == 2 * 8 * 260 * 4              # 128 + 128 sums, the count, padding
 
 
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 64), ("group_n", 12), ("beta", 0), ("beta", 513), ("bits_l1l3", 8),
     ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 17),
-    ("n_q_heads", 12),
+    ("n_q_heads", 12), ("l1_sinks", -1), ("l1_recent", -1), ("l1_recent", 101),
 ])
 def test_invalid_config_rejected(H, field, value):
     cfg = H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000)
@@ -114,6 +118,7 @@ def test_null_context_calls_fail_cleanly(H):
     assert lib.hsq_route(None, ctypes.byref(c), None, None, None, None, None) == 1
     assert lib.hsq_decode_attn(None, ctypes.byref(c), None, None, None, None, 0, None) == 1
     assert lib.hsq_fetch_dequant(None, ctypes.byref(c), None, None, None, None, None) == 1
+    assert lib.hsq_append(None, ctypes.byref(c), None, None, 0, None) == 1
     assert lib.hsq_destroy(None) == 0
 
 
