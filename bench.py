@@ -282,6 +282,54 @@ def run_reference(args, rank, world):
     }
 
 
+GROW_STEPS = 64
+
+
+def measure_growth(H, torch, w, li, flush, clean, sink):
+    """Decode with cache growth on the same layer: a growable copy of the cache
+    (recent window and sinks of the workload, capacity T + GROW_STEPS), then
+    per step hsq_append of the new token's K/V (seeded N(0,1) draws) followed
+    by the decode step of that token (query at the new position); L2 flushed
+    before every step, outside the events."""
+    n = GROW_STEPS
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T + n, w.l1_size, w.T + n + 1, w.theta, 0,
+                        sinks=w.sinks, recent=w.recent)
+    gctx = H.Context(cfg)
+    cache = H.allocate_cache(gctx, w.B, w.T, l3_on_host=True, with_staging=False, t_cap=w.T + n)
+    H.set_layer_inputs(cache, li.l1_mask, li.signs)
+    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+    H.hsq_encode(gctx, cache, K, V)
+    del K, V
+    rng = np.random.default_rng(12345)
+    kv = torch.from_numpy(rng.standard_normal((n, 2, w.B, w.Hkv, 128)).astype(np.float32)).cuda().to(torch.bfloat16)
+    q = torch.from_numpy(rng.standard_normal((n, w.B, w.Hq, 128)).astype(np.float32)).cuda()
+    pos = torch.arange(w.T, w.T + n, dtype=torch.int32, device="cuda").view(n, 1).expand(n, w.B).contiguous()
+    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    t_app, t_step = [], []
+    for i in range(n):
+        flush.fill_(i & 255)
+        torch.sum(clean, dim=0, out=sink)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        H.hsq_append(gctx, cache, kv[i, 0], kv[i, 1])
+        e[1].record()
+        H.hsq_decode_step(gctx, cache, q[i], pos[i], sel, out)
+        e[2].record()
+        e[2].synchronize()
+        if i >= 4:
+            t_app.append(e[0].elapsed_time(e[1]) * 1e3)
+            t_step.append(e[0].elapsed_time(e[2]) * 1e3)
+    assert H.hsq_sync_status(gctx) == 0 and cache.T == w.T + n
+    gctx.close()
+    med = statistics.median
+    return {"append_us": med(t_app), "append_plus_step_us": med(t_step),
+            "steps_per_s_with_append": 1e6 / med(t_step), "steps": n - 4,
+            "how": f"hsq_append (one kernel) then hsq_decode_step per token, {n} tokens appended to the "
+                   f"{w.T}-token layer (capacity {w.T + n}), recent window {w.recent}, L2 flushed per step"}
+
+
 def run_hsq(args, rank, world, local):
     import ctypes
 
@@ -406,6 +454,7 @@ def run_hsq(args, rank, world, local):
         res_e2e = loop("host", args.steps, e2e=True)
         lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
+    growth = None if args.quick else measure_growth(H, torch, w, li, flush, clean, sink)
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
     mean = lambda x: sum(x) / len(x)
@@ -457,6 +506,7 @@ def run_hsq(args, rank, world, local):
                    "input_gbs_pinned_l3": w.B * w.Hkv * w.T * 2 * 128 * 2 / (enc["host"] * 1e-3) / 1e9,
                    "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
         "link_peak": lp,
+        "growth": growth,
         "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,

@@ -20,7 +20,6 @@ struct hsq_ctx {
     int* d_route_ctr = nullptr;
     int* d_prefix = nullptr;
     int* d_err = nullptr;
-    int* d_slot = nullptr;  // hsq_append: the new token's L1 slot per sequence
     // Decode launch plan per cache shape: cluster size S (0 = no launchable
     // shape) and whether the split's inputs are staged in shared memory.
     struct Plan { int B, T, route, S, staged; };

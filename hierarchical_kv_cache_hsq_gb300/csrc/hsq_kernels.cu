@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
                 keep ? make_float4(acc[0], acc[1], acc[2], acc[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) =
                 keep ? make_float4(acc[4], acc[5], acc[6], acc[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (threadIdx.x == 0) gs[2 * kDim] = keep ? (float)cnt : 0.f;
+            if (threadIdx.x == 0) {
+                gs[2 * kDim] = keep ? (float)cnt : 0.f;
+                gs[2 * kDim + 1] = (float)p_next;  // the window's first position at encode
+            }
         }
         if (cnt > 0) {
 #pragma unroll
@@ -242,86 +245,89 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 }
 
 // ---------------------------------------------------------------------------
-// Decode-time growth (append one token per sequence at position T).
-// Stage 1, one warp per sequence: the L1 slot of the new token -- the slot of
-// the token p = T - recent that leaves the window (found in l1_pos), or a new
-// slot when nothing leaves -- and the bitmap and position-list updates.
-// slot_out[b] = slot | (leaves << 30), or -1 when L1 is left unchanged.
+// Decode-time growth: append one token per sequence at position T.  One CTA
+// per sequence b, one warp per KV head.  Warp 0 first finds the L1 slot of the
+// new token -- the slot of the token p = T - recent that leaves the window,
+// or a new slot when nothing leaves -- and updates the sequence's L1 list,
+// count and bitmap (no other CTA touches them).  Then warp h (half 0 the key,
+// half 1 the value) writes the new token's L3 record slot and L1 entry, and,
+// when p leaves, adds p's input (from the window ring) to the running sums
+// of its group in position order and re-quantises the group's summary, as the
+// encode of the longer context computes it.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(32) append_index_kernel(CacheView c, int32_t* l1_pos, int32_t* l1_count,
-                                                          uint32_t* l1_bitmap, int sinks, int recent,
-                                                          int* slot_out, int* err) {
-    const int b = blockIdx.x, lane = threadIdx.x;
-    const int t = c.T, p = t - recent;
-    int32_t* pos = l1_pos + (size_t)b * c.max_l1;
-    const int cnt = min(__ldcg(l1_count + b), c.max_l1);
-    int slot = -1, leaves = 0;
-    if (p >= 0 && p >= sinks) {
-        int found = -1;
-#pragma unroll 1
-        for (int i0 = 0; i0 < cnt; i0 += 32) {  // warp-uniform bound
-            const int i = i0 + lane;
-            const unsigned hit = __ballot_sync(kFull, i < cnt && __ldcg(pos + min(i, cnt - 1)) == p);
-            if (hit) {
-                found = i0 + __ffs(hit) - 1;
-                break;
-            }
-        }
-        if (found >= 0) {
-            slot = found;
-            leaves = 1;
-        } else if (lane == 0) {
-            atomicOr(err, HSQ_DEVERR_GROW);
-        }
-    } else if (cnt < c.max_l1) {
-        slot = cnt;
-        if (lane == 0) l1_count[b] = cnt + 1;
-    } else if (lane == 0) {
-        atomicOr(err, HSQ_DEVERR_L1_OVER);
-    }
-    if (lane == 0) {
-        uint32_t* bm = l1_bitmap + (size_t)b * c.W;
-        if (slot >= 0) {
-            pos[slot] = t;
-            atomicOr(bm + (t >> 5), 1u << (t & 31));
-        }
-        if (leaves) atomicAnd(bm + (p >> 5), ~(1u << (p & 31)));
-        slot_out[b] = slot >= 0 ? (slot | (leaves << 30)) : -1;
-    }
-}
-
-// Stage 2, one warp per (KV head h, sequence b); half 0 takes the key, half 1
-// the value: the new token's L3 record slot and L1 entry, then -- when p
-// leaves the window -- p joins group p / N: its input (from the window ring)
-// is added to the group's running sums in position order and the summary is
-// re-quantised, as the encode of the longer context computes it.
 template <int N, bool kBF16>
-__global__ void __launch_bounds__(32) append_kernel(CacheView c, EncodeOut o, const void* __restrict__ kp,
-                                                    const void* __restrict__ vp, Tables tb, int recent,
-                                                    const int* __restrict__ slot_in) {
+__global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, int32_t* l1_pos, int32_t* l1_count,
+                                                      uint32_t* l1_bitmap, const void* __restrict__ kp,
+                                                      const void* __restrict__ vp, Tables tb, int sinks,
+                                                      int recent, int* err) {
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
-    __shared__ uint32_t s_l2[2][12];
-    const int h = blockIdx.x, b = blockIdx.y;
+    __shared__ uint32_t s_l2[32][2][12];
+    __shared__ int s_slot;
+    const int b = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = (threadIdx.x >> 4) & 1, l = hlane();
     const unsigned m = half_mask();
+    const int t = c.T, p = t - recent;
+    const size_t bh = (size_t)b * c.Hkv + h;
+    // loads that depend on nothing, issued first
+    float x[8];
+    if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? vp : kp) + bh * kDim, x);
+    else load_f32x8(static_cast<const float*>(half ? vp : kp) + bh * kDim, x);
+    float* wp = o.win_kv + ((bh * recent + (size_t)(t % recent)) * 2 + half) * kDim;  // = p's ring slot
+    float xp[8];
+    load_f32x8_cg(wp, xp);
     load_tables(s_cb, s_sign, tb, c.signs);
-    if (threadIdx.x < 24) (&s_l2[0][0])[threadIdx.x] = 0u;
+    if (threadIdx.x < 24 * c.Hkv) (&s_l2[0][0][0])[threadIdx.x] = 0u;
+
+    if (h == 0) {  // the slot, and the sequence's L1 bookkeeping
+        int32_t* pos = l1_pos + (size_t)b * c.max_l1;
+        const int cnt = min(__ldcg(l1_count + b), c.max_l1);
+        int slot = -1, leaves = 0;
+        if (p >= 0 && p >= sinks) {
+            // the window fills the last `recent` slots, rotated: the token at
+            // position x0 + j (x0 its first position at encode) is in slot
+            // cnt - recent + j mod recent -- checked, else every slot is scanned
+            const int x0 = (int)__ldcg(o.gsum + (size_t)b * c.Hkv * hsq::kGsumFloats + 2 * kDim + 1);
+            const int pred = x0 >= 0 && p >= x0 && cnt >= recent ? cnt - recent + (p - x0) % recent : -1;
+            int found = pred >= 0 && __ldcg(pos + pred) == p ? pred : -1;
+            if (found < 0) {
+                int f = -1;
+#pragma unroll 4
+                for (int i = lane; i < cnt; i += 32)  // independent loads, no early exit
+                    f = __ldcg(pos + i) == p ? i : f;
+                found = __reduce_max_sync(kFull, f);
+            }
+            if (found >= 0) {
+                slot = found;
+                leaves = 1;
+            } else if (lane == 0) {
+                atomicOr(err, HSQ_DEVERR_GROW);
+            }
+        } else if (cnt < c.max_l1) {
+            slot = cnt;
+            if (lane == 0) l1_count[b] = cnt + 1;
+        } else if (lane == 0) {
+            atomicOr(err, HSQ_DEVERR_L1_OVER);
+        }
+        if (lane == 0) {
+            uint32_t* bm = l1_bitmap + (size_t)b * c.W;
+            if (slot >= 0) {
+                pos[slot] = t;
+                atomicOr(bm + (t >> 5), 1u << (t & 31));
+            }
+            if (leaves) atomicAnd(bm + (p >> 5), ~(1u << (p & 31)));
+            s_slot = slot >= 0 ? (slot | (leaves << 30)) : -1;
+        }
+    }
     __syncthreads();
     const float* t4 = s_cb + 16;
     const float* t3 = s_cb + 40;
     float sg[8];
     load_signs(sg, s_sign);
-    const int t = c.T, p = t - recent;
-    const int sc = __ldcg(slot_in + b);
+    const int sc = s_slot;
     const int slot = sc < 0 ? -1 : (sc & 0x3FFFFFFF);
     const bool leaves = sc >= 0 && ((sc >> 30) & 1);
-    const size_t bh = (size_t)b * c.Hkv + h;
-
-    float x[8];
-    if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? vp : kp) + bh * kDim, x);
-    else load_f32x8(static_cast<const float*>(half ? vp : kp) + bh * kDim, x);
 
     // L3 record slot t: TQ4 of the raw key / value
     float y[8];
@@ -355,32 +361,31 @@ __global__ void __launch_bounds__(32) append_kernel(CacheView c, EncodeOut o, co
             if (l == 0) o.l1_vn[so] = n;
         }
     }
-    float* wp = o.win_kv + ((bh * recent + (size_t)(t % recent)) * 2 + half) * kDim;  // = p's slot
     if (leaves) {
-        float xp[8];
-        load_f32x8_cg(wp, xp);
         if (half == 0) rope(xp, p, tb);
         float* gs = o.gsum + bh * hsq::kGsumFloats;
         const bool fresh = p % N == 0;  // p opens its group: nothing summed before it
         float acc[8];
-        float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 4 * l));
-        float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
-                          : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 64 + 4 * l));
+        const float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 4 * l));
+        const float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 64 + 4 * l));
         acc[0] = a.x + xp[0]; acc[1] = a.y + xp[1]; acc[2] = a.z + xp[2]; acc[3] = a.w + xp[3];
         acc[4] = bq.x + xp[4]; acc[5] = bq.y + xp[5]; acc[6] = bq.z + xp[6]; acc[7] = bq.w + xp[7];
         const int cnt = (fresh ? 0 : (int)__ldcg(gs + 2 * kDim)) + 1;
         __syncwarp();  // every lane has read the count before lane 0 rewrites it
         *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        if (threadIdx.x == 0) gs[2 * kDim] = (float)cnt;
+        if (lane == 0) gs[2 * kDim] = (float)cnt;
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         const int gp = p / N;
         const size_t go = bh * c.G + gp;
-        write_summary(acc, sg, m, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48, (half ? o.l2_vn : o.l2_kn) + go);
-        if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
+        write_summary(acc, sg, m, t3, s_l2[h][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+                      (half ? o.l2_vn : o.l2_kn) + go);
+        if (lane == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
     }
-    __syncwarp();  // p's inputs are read before t's replace them
+    // t's inputs replace p's in the ring (p's were read at the start)
     *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
     *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
 }
@@ -668,7 +673,7 @@ hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
 }
 
 void free_ctx(hsq_ctx* c) {
-    cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores); cudaFree(c->d_slot);
+    cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
     cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err);
     delete c;
 }
@@ -719,7 +724,6 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(prefix)");
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
-    if ((e = cudaMalloc(&c->d_slot, (size_t)cfg->max_batch * 4)) != cudaSuccess) return bail(e, "cudaMalloc(slots)");
     if ((e = cudaMemcpy(c->d_cb, cb, sizeof(cb), cudaMemcpyHostToDevice)) != cudaSuccess) return bail(e, "upload");
     if ((e = cudaMemcpy(c->d_rope_hi, hi.data(), hi.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(e, "upload");
@@ -785,20 +789,22 @@ hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void*
     if (cache->T >= ctx->cfg.max_pos) return fail(ctx, HSQ_ERR_INVALID, "position T reaches max_pos");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const CacheView vw = make_view(ctx, cache);
-    append_index_kernel<<<vw.B, 32, 0, s>>>(vw, cache->l1_pos, cache->l1_count, cache->l1_bitmap,
-                                            ctx->cfg.l1_sinks, recent, ctx->d_slot, ctx->d_err);
+    if (vw.Hkv > 32) return fail(ctx, HSQ_ERR_UNSUPPORTED, "hsq_append handles at most 32 KV heads");
     EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
                 cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, nullptr, cache->win_kv, cache->gsum,
                 recent};
-    const dim3 grid(vw.Hkv, vw.B);
     const Tables tb = make_tables(ctx);
     const bool bf = dtype == HSQ_DTYPE_BF16;
+    const int threads = 32 * vw.Hkv, sinks = ctx->cfg.l1_sinks;
+    int32_t* pos = cache->l1_pos;
+    int32_t* cnt = cache->l1_count;
+    uint32_t* bm = cache->l1_bitmap;
     if (vw.N == 16) {
-        if (bf) append_kernel<16, true><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
-        else append_kernel<16, false><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+        if (bf) append_kernel<16, true><<<vw.B, threads, 0, s>>>(vw, o, pos, cnt, bm, k, v, tb, sinks, recent, ctx->d_err);
+        else append_kernel<16, false><<<vw.B, threads, 0, s>>>(vw, o, pos, cnt, bm, k, v, tb, sinks, recent, ctx->d_err);
     } else {
-        if (bf) append_kernel<8, true><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
-        else append_kernel<8, false><<<grid, 32, 0, s>>>(vw, o, k, v, tb, recent, ctx->d_slot);
+        if (bf) append_kernel<8, true><<<vw.B, threads, 0, s>>>(vw, o, pos, cnt, bm, k, v, tb, sinks, recent, ctx->d_err);
+        else append_kernel<8, false><<<vw.B, threads, 0, s>>>(vw, o, pos, cnt, bm, k, v, tb, sinks, recent, ctx->d_err);
     }
     st = after_launch(ctx, "append");
     if (st == HSQ_OK) cache->T += 1;

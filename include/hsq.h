@@ -159,7 +159,7 @@ typedef struct hsq_cache {
     float* gsum;              /* [B][Hkv][260] device, or NULL: for the group holding position
                                  T - l1_recent, the float sums, in position order, of its members
                                  below that position: RoPE'd keys [128] | values [128] | member
-                                 count | pad [3] */
+                                 count | the window's first position at encode | pad [2] */
 } hsq_cache;
 
 typedef enum {

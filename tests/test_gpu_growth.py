@@ -4,7 +4,7 @@ A cache encoded at length T0 and grown by s appended tokens must be the
 encode of the T0 + s context under the grown L1 set (oracle.grown_l1_mask):
   * bit-exact against the GPU's own encode of the longer context: L3
     records, L2 codes, norms and counts, the L1 bitmap and count, the
-    window ring and the running sums, and the L1 entries as a set keyed by
+    window ring, the running sums and counts, and the L1 entries as a set keyed by
     position (an appended token takes the slot of the token that leaves);
   * within the encode parity bar against the oracle's encode of the longer
     context (codes bit-exact except near-ties);
@@ -100,8 +100,10 @@ def _l1_by_position(cache, b):
 @pytest.mark.parametrize("name", list(CASES))
 def test_append_equals_encode_of_longer_context(name):
     g = grown(name)
-    for buf in ("l3", "l2_kc", "l2_vc", "l2_kn", "l2_vn", "l2_cnt", "l1_bitmap", "l1_count", "win_kv", "gsum"):
+    for buf in ("l3", "l2_kc", "l2_vc", "l2_kn", "l2_vn", "l2_cnt", "l1_bitmap", "l1_count", "win_kv"):
         np.testing.assert_array_equal(_np(g.a, buf), _np(g.b, buf), err_msg=buf)
+    # the running sums and member count (the last word is each cache's own slot bookkeeping)
+    np.testing.assert_array_equal(_np(g.a, "gsum")[..., :257], _np(g.b, "gsum")[..., :257])
     for b in range(g.w.B):
         pa, pb = _l1_by_position(g.a, b), _l1_by_position(g.b, b)
         assert sorted(pa) == sorted(pb) == list(np.nonzero(g.mask1[b])[0])
