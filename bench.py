@@ -58,6 +58,9 @@ def parse_args():
                    help="the batch workloads run every layer of a decode step back to back "
                         "and report a per-layer roofline (not the headline line)")
     p.add_argument("--layers", type=int, default=0, help="layers per step (0: the workload's)")
+    p.add_argument("--betas", type=str, default="",
+                   help="comma-separated beta sweep for the per-layer mode (any workload)")
+    p.add_argument("--group-n", type=int, default=0, help="group size N override for the per-layer mode")
     return p.parse_args()
 
 
@@ -548,10 +551,12 @@ def run_layers(args, rank, world, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     H.load_library()
     w = W.get_workload(args.workload)
+    if args.group_n:
+        w = w.with_(N=args.group_n)
     L = args.layers or w.layers
-    betas = tuple(w.betas) or (w.beta,)
+    betas = tuple(int(b) for b in args.betas.split(",")) if args.betas else (tuple(w.betas) or (w.beta,))
     placements = ("host", "device") if w.name == "qwen3_4b_b16_8k" else ("host",)
-    li = W.layer_inputs(w)
+    li = W.layer_inputs(w, rope=lambda x, p: input_rope(x, p, w.theta))
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
                              args.n_splits) for b in betas}
@@ -622,14 +627,20 @@ def run_layers(args, rank, world, local):
             else:
                 t_star = (hbm_avg + link) / (hbm_peak * 1e9)
                 bound = "hbm"
-            rows.append({"beta": beta, "l3": "pinned host" if pl == "host" else "device",
+            needle = None
+            if w.needle:  # the planted group is routed at step 0 for every (b, KV head)
+                s_r = torch.empty((w.B, w.Hkv, beta), dtype=torch.int32, device="cuda")
+                H.hsq_route(ctxs[beta], caches[pl][0], qd[0], pd[0], s_r)
+                s0 = s_r.cpu().numpy()
+                needle = all(int(li.needle_group[b, h]) in s0[b, h] for b in range(w.B) for h in range(w.Hkv))
+            rows.append({"beta": beta, "l3": "pinned host" if pl == "host" else "device", "needle_routed": needle,
                          "ms_per_step": ms, "steps_per_s": world * 1e3 / ms, "us_per_layer": t_layer * 1e6,
                          "hbm_bytes_per_layer": hbm_avg, "l3_bytes_per_layer": link,
                          "hbm_gbs": hbm_avg / t_layer / 1e9, "l3_gbs": link / t_layer / 1e9,
                          "t_star_us_per_layer": t_star * 1e6, "bound": bound, "frac": t_star / t_layer})
     clk = clocks.stop()
     assert H.hsq_sync_status(ctx0) == 0
-    head = rows[0] if len(betas) == 1 else next(r for r in rows if r["beta"] == w.beta)
+    head = next((r for r in rows if r["beta"] == w.beta), rows[0])
     enc = statistics.median(enc_ms) if enc_ms else float("nan")
     line = {
         "metric": f"HSQ decode steps/s ({w.name}, {L} layers per step)", "value": head["steps_per_s"],
@@ -663,7 +674,7 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
-    elif args.workload != WORKLOAD:
+    elif args.workload != WORKLOAD or args.betas or args.group_n or args.layers:
         line = run_layers(args, rank, world, local)
     else:
         line = run_hsq(args, rank, world, local)
