@@ -46,6 +46,7 @@ class hsq_config(ctypes.Structure):
         ("bits_l2", ctypes.c_int), ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int),
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
         ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
+        ("route_max", ctypes.c_int),
     ]
 
 
@@ -131,13 +132,14 @@ def hsq_codebook(bits: int, dim: int = 128):
 
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
                 max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
-                recent: int = 0) -> hsq_config:
+                recent: int = 0, route_max: bool = False) -> hsq_config:
     """recent > 0 makes caches of this context growable (hsq_append) with an
-    L1 recent window of that length and `sinks` permanent sink positions."""
+    L1 recent window of that length and `sinks` permanent sink positions;
+    route_max scores a group by its best query head instead of their sum."""
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
                       bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
                       max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
-                      l1_sinks=sinks, l1_recent=recent)
+                      l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0)
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:

@@ -191,31 +191,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Dot products of two 128-vectors (a, b; this lane's 8 dims each) with the R
-// query heads.  Returns the lane's share of the 2R sums (spread_sum): index
-// idx < R is head idx of a, R <= idx < 2R head idx - R of b, idx >= 2R unused.
-template <int R>
-__device__ __forceinline__ float pair_dots(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
-                                           int& idx) {
-    constexpr int K = pow2_ceil(2 * R);
-    float p[K];
-#pragma unroll
-    for (int j = 0; j < R; ++j) {
-        float da = 0.f, db = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            da = fmaf(q[j][k], ka[k], da);
-            db = fmaf(q[j][k], kb[k], db);
-        }
-        p[j] = da;
-        p[R + j] = db;
-    }
-#pragma unroll
-    for (int j = 2 * R; j < K; ++j) p[j] = 0.f;
-    idx = spread_index<K>(hlane());
-    return spread_sum<K>(p);
-}
-
 // The 2R logits of a pair in every lane: xa[j] = scale * (q_j . ka), xb likewise.
 // xs: this half-warp's 16-float scratch in shared memory.
 template <int R>

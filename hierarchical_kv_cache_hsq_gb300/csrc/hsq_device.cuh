@@ -410,6 +410,7 @@ __device__ __forceinline__ void unpack3_smem(const uint8_t* rec8, const float* c
 
 struct RouteArgs {
     const float* q; const int32_t* pos; int32_t* sel; float* scores; int* counters; int* err;
+    int agg_max;  // score = max over the query heads instead of their sum
 };
 
 __device__ __forceinline__ uint32_t ordered_key(float s) {
@@ -704,6 +705,31 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     const int n_sel = mode == 0 ? ne : beta;
 #pragma unroll 1
     for (int i = n_sel + tid; i < beta; i += NT) out[i] = -1;
+}
+
+// Dot products of two 128-vectors (a, b; this lane's 8 dims each) with the R
+// query heads.  Returns the lane's share of the 2R sums (spread_sum): index
+// idx < R is head idx of a, R <= idx < 2R head idx - R of b, idx >= 2R unused.
+template <int R>
+__device__ __forceinline__ float pair_dots(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
+                                           int& idx) {
+    constexpr int K = pow2_ceil(2 * R);
+    float p[K];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float da = 0.f, db = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            da = fmaf(q[j][k], ka[k], da);
+            db = fmaf(q[j][k], kb[k], db);
+        }
+        p[j] = da;
+        p[R + j] = db;
+    }
+#pragma unroll
+    for (int j = 2 * R; j < K; ++j) p[j] = 0.f;
+    idx = spread_index<K>(hlane());
+    return spread_sum<K>(p);
 }
 
 // Routing scores of two groups a and b: (sum_j q~_j) . c3[codes], every lane

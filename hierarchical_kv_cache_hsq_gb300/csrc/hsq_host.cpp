@@ -176,6 +176,7 @@ std::string check_config(const hsq_config* c) {
     if (c->l1_sinks < 0 || c->l1_recent < 0) return "l1_sinks and l1_recent must be >= 0";
     if (c->l1_recent > 0 && (long long)c->l1_sinks + c->l1_recent > c->max_l1)
         return "l1_sinks + l1_recent must fit max_l1";
+    if (c->route_max != 0 && c->route_max != 1) return "route_max must be 0 or 1";
     return "";
 }
 

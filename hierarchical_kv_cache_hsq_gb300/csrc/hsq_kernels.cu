@@ -437,6 +437,15 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
     }
     const float* c3 = s_cb + 32;
     const size_t base = (size_t)bh * c.G + g_begin;
+    float qt[R][8];  // the rotated query heads (max aggregation)
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            qt[j][k] = s_q[j][4 * l + k];
+            qt[j][4 + k] = s_q[j][64 + 4 * l + k];
+        }
+    }
 #pragma unroll 1
     for (int blk = 0; blk < ng; blk += 2 * kHalves) {
         const int ia = blk + hw, ib = ia + kHalves;
@@ -445,7 +454,19 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
         unpack3_smem(s_codes + ja * 48, c3, 1.0f, va);
         unpack3_smem(s_codes + jb * 48, c3, 1.0f, vb);
         float sa, sb;
-        route_pair(gq, va, vb, sa, sb);
+        if (a.agg_max) {  // per-head dots, then their maximum (a uniform branch)
+            int idx;
+            const float d = pair_dots<R>(qt, va, vb, idx);
+            sa = idx < R ? d : -INFINITY;
+            sb = (idx >= R) & (idx < 2 * R) ? d : -INFINITY;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                sa = fmaxf(sa, __shfl_xor_sync(kFull, sa, o, 16));
+                sb = fmaxf(sb, __shfl_xor_sync(kFull, sb, o, 16));
+            }
+        } else {
+            route_pair(gq, va, vb, sa, sb);
+        }
         if (l == 0) {
             if (ia < ng) a.scores[base + ia] = s_cnt[ja] > 0 ? s_kn[ja] * sa : -INFINITY;
             if (ib < ng) a.scores[base + ib] = s_cnt[jb] > 0 ? s_kn[jb] * sb : -INFINITY;
@@ -818,7 +839,8 @@ hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const
     if (!q || !pos || !sel) return fail(ctx, HSQ_ERR_INVALID, "q, pos or sel is NULL");
     if ((st = check_io(ctx, q, pos, sel, nullptr)) != HSQ_OK) return st;
     CacheView v = make_view(ctx, cache);
-    RouteArgs a{q, pos, sel, scores_opt ? scores_opt : ctx->d_scores, ctx->d_route_ctr, ctx->d_err};
+    RouteArgs a{q, pos, sel, scores_opt ? scores_opt : ctx->d_scores, ctx->d_route_ctr, ctx->d_err,
+                ctx->cfg.route_max};
     st = dispatch_route(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
     if (st != HSQ_OK) return fail(ctx, st, "unsupported head ratio");
     return after_launch(ctx, "route");
@@ -866,8 +888,10 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool fused = false;
-    st = decode_run(ctx, cache, q, pos, sel, out, true, false, s, &fused);
-    if (st != HSQ_OK || fused) return st;
+    if (!ctx->cfg.route_max) {  // (the fused kernel routes by the sum over the query heads)
+        st = decode_run(ctx, cache, q, pos, sel, out, true, false, s, &fused);
+        if (st != HSQ_OK || fused) return st;
+    }
     st = hsq_route(ctx, cache, q, pos, sel, nullptr, stream);
     if (st != HSQ_OK) return st;
     return hsq_decode_attn(ctx, cache, q, pos, sel, out, 0, stream);
@@ -1139,6 +1163,7 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
     why = hsq::check_cache_shape(cfg, cache);
     if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
+    if (cfg->route_max) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "hsq_route_noalloc routes by the sum only");
     if (!q || !pos || !sel) return fail(nullptr, HSQ_ERR_INVALID, "q, pos or sel is NULL");
     const int r = cfg->n_q_heads / cfg->n_kv_heads;
     if (!r_supported(r)) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "r = Hq/Hkv must be 1, 2, 4, 5 or 8");

@@ -114,6 +114,10 @@ typedef struct hsq_config {
        [T - l1_recent, T), which slides by one with every appended token. */
     int l1_sinks;       /* >= 0 */
     int l1_recent;      /* >= 0; 0 = caches of this context do not grow */
+    /* How a KV head's routing score combines its query heads: 0 = their sum
+       (one dot with the summed rotated queries), 1 = their maximum (a group
+       counts as much as it does for its best query head). */
+    int route_max;
 } hsq_config;
 
 /*
@@ -253,7 +257,10 @@ hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void*
  *   process, steps 1-2).  For each (b, KV head h):
  *     s_g = sum over the head's query heads j of RoPE(q_j, pos_b) . k_hat_g
  *   (k_hat_g the dequantised summary key), computed in the rotated frame as
- *   n_g * (sum_j Pi RoPE(q_j, pos_b)) . c3[codes_g]; empty groups score -inf.
+ *   n_g * (sum_j Pi RoPE(q_j, pos_b)) . c3[codes_g]; with cfg.route_max the
+ *   maximum over j of n_g * (Pi RoPE(q_j, pos_b)) . c3[codes_g] instead
+ *   (hsq_decode_step then runs hsq_route and hsq_decode_attn; the no-alloc
+ *   routing call refuses it); empty groups score -inf.
  *   sel[b][h][0..beta) = the beta largest scores, ties to the lower group,
  *   listed in ascending group order, -1 padded when fewer are non-empty.
  *   q: [B][Hq][128] f32; pos: [B] int32 (query positions); sel:

@@ -422,9 +422,14 @@ def select_top_beta(scores32: np.ndarray, nonempty: np.ndarray, beta: int) -> np
     return out
 
 
-def route(cache: OracleCache, q: np.ndarray, pos: np.ndarray, beta: int):
+def route(cache: OracleCache, q: np.ndarray, pos: np.ndarray, beta: int, agg: str = "sum"):
     """Per-KV-head routing scores [B, Hkv, G] (float64, -inf for empty groups)
-    and the selection sel [B, Hkv, beta]."""
+    and the selection sel [B, Hkv, beta].  [HSQ] decode process, step 1 (a
+    per-head router scores the summary keys against the current query).
+    agg: how a KV head combines its query heads' scores -- "sum" (the reading
+    the library defaults to) or "max" (the group's score for its best head)."""
+    if agg not in ("sum", "max"):
+        raise ValueError("agg must be 'sum' or 'max'")
     B, Hq, d = q.shape
     Hkv = cache.Hkv
     qr = rope(np.asarray(q, dtype=np.float64), np.asarray(pos)[:, None], cache.theta)
@@ -434,7 +439,10 @@ def route(cache: OracleCache, q: np.ndarray, pos: np.ndarray, beta: int):
     for b in range(B):
         ne = cache.l2_cnt[b] > 0
         for h, js in enumerate(_heads(Hq, Hkv)):
-            s = khat[b, h] @ qr[b, js].sum(axis=0)
+            if agg == "sum":
+                s = khat[b, h] @ qr[b, js].sum(axis=0)
+            else:
+                s = (khat[b, h] @ qr[b, js].T).max(axis=1)           # best of the KV head's query heads
             scores[b, h] = np.where(ne, s, -np.inf)
             sel[b, h] = select_top_beta(scores[b, h].astype(np.float32), ne, beta)
     return sel, scores

@@ -233,3 +233,36 @@ def test_needle_group_is_routed_first_step():
         g = li.needle_group[0, h]
         assert g in sel[0, h]
         assert scores[0, h, g] == np.max(scores[0, h])
+
+
+# -- routing by the best query head (route_max) ------------------------------------
+
+def test_max_routing_is_the_best_single_head():
+    """A KV head's max score is, group by group, the largest of the scores its
+    query heads get when each routes alone (one query head per KV head, where
+    sum and max coincide)."""
+    w = _small(Hq=8, Hkv=2)
+    li, cache, q, pos = _setup(w)
+    r = w.Hq // w.Hkv
+    sel_max, s_max = O.route(cache, q[0], pos[0], w.beta, agg="max")
+    singles = []
+    for j in range(r):
+        qj = q[0][:, [h * r + j for h in range(w.Hkv)]]      # head j of every KV head
+        singles.append(O.route(cache, qj, pos[0], w.beta, agg="sum")[1])
+    np.testing.assert_allclose(s_max, np.max(singles, axis=0), rtol=1e-12, atol=0)
+    # and the selection is the top-beta of those scores
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            ne = cache.l2_cnt[b] > 0
+            np.testing.assert_array_equal(sel_max[b, h], _brute_select(s_max[b, h].astype(np.float32), ne, w.beta))
+
+
+def test_max_and_sum_routing_agree_with_one_query_head_per_kv_head():
+    w = _small(Hq=2, Hkv=2)
+    li, cache, q, pos = _setup(w)
+    a = O.route(cache, q[0], pos[0], w.beta, agg="sum")
+    b = O.route(cache, q[0], pos[0], w.beta, agg="max")
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_allclose(a[1], b[1], rtol=1e-15, atol=0)
+    with pytest.raises(ValueError):
+        O.route(cache, q[0], pos[0], w.beta, agg="mean")
