@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--betas", type=str, default="",
                    help="comma-separated beta sweep for the per-layer mode (any workload)")
     p.add_argument("--group-n", type=int, default=0, help="group size N override for the per-layer mode")
+    p.add_argument("--route-max", action="store_true",
+                   help="per-layer mode: route by each KV head's best query head (route + attention)")
     return p.parse_args()
 
 
@@ -559,7 +561,7 @@ def run_layers(args, rank, world, local):
     li = W.layer_inputs(w, rope=lambda x, p: input_rope(x, p, w.theta))
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                             args.n_splits) for b in betas}
+                             args.n_splits, route_max=args.route_max) for b in betas}
     ctxs = {b: H.Context(c) for b, c in cfgs.items()}
     ctx0 = ctxs[betas[0]]
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
@@ -650,6 +652,8 @@ def run_layers(args, rank, world, local):
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} L1={w.l1_size} "
                                f"{L} layers, beta {'/'.join(map(str, betas))}",
                    "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
+                   "routing": "max over each KV head's query heads (route + attention)" if args.route_max
+                              else "sum over each KV head's query heads (fused step)",
                    "l2": "cold and clean at every step (256 MiB write + 256 MiB read between steps, "
                          "outside the step events); layers of a step back to back"},
         "per_layer": rows,
@@ -674,7 +678,7 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
-    elif args.workload != WORKLOAD or args.betas or args.group_n or args.layers:
+    elif args.workload != WORKLOAD or args.betas or args.group_n or args.layers or args.route_max:
         line = run_layers(args, rank, world, local)
     else:
         line = run_hsq(args, rank, world, local)
