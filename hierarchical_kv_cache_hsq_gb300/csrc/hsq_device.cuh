@@ -172,16 +172,29 @@ __device__ __forceinline__ void load_signs(float s[8], const float* s_sign) {
 }
 
 // RoPE at position p by angle addition: p = 256 a + c.
-__device__ __forceinline__ void rope(float v[8], int p, const Tables& tb) {
+// The two table rows RoPE at position p combines (p = 256 a + c: cos/sin of
+// 256 a omega and of c omega, this lane's 4 frequencies), loaded ahead of use.
+struct RopeRows {
+    float4 ch, sh, cl, sl;
+};
+
+__device__ __forceinline__ RopeRows rope_rows(int p, const Tables& tb) {
     const int l = hlane();
     const float* rh = tb.rope_hi + (size_t)(p >> 8) * kDim;
     const float* rl = tb.rope_lo + (size_t)(p & 255) * kDim;
-    const float4 ch = __ldg(reinterpret_cast<const float4*>(rh + 4 * l));
-    const float4 sh = __ldg(reinterpret_cast<const float4*>(rh + 64 + 4 * l));
-    const float4 cl = __ldg(reinterpret_cast<const float4*>(rl + 4 * l));
-    const float4 sl = __ldg(reinterpret_cast<const float4*>(rl + 64 + 4 * l));
-    const float cA[4] = {ch.x, ch.y, ch.z, ch.w}, sA[4] = {sh.x, sh.y, sh.z, sh.w};
-    const float cB[4] = {cl.x, cl.y, cl.z, cl.w}, sB[4] = {sl.x, sl.y, sl.z, sl.w};
+    RopeRows r;
+    r.ch = __ldg(reinterpret_cast<const float4*>(rh + 4 * l));
+    r.sh = __ldg(reinterpret_cast<const float4*>(rh + 64 + 4 * l));
+    r.cl = __ldg(reinterpret_cast<const float4*>(rl + 4 * l));
+    r.sl = __ldg(reinterpret_cast<const float4*>(rl + 64 + 4 * l));
+    return r;
+}
+
+// Rotate-half RoPE of this lane's dims (i, i + 64), the angle by addition:
+// cos(A + B) = cA cB - sA sB, sin(A + B) = sA cB + cA sB.
+__device__ __forceinline__ void rope_apply(float v[8], const RopeRows& r) {
+    const float cA[4] = {r.ch.x, r.ch.y, r.ch.z, r.ch.w}, sA[4] = {r.sh.x, r.sh.y, r.sh.z, r.sh.w};
+    const float cB[4] = {r.cl.x, r.cl.y, r.cl.z, r.cl.w}, sB[4] = {r.sl.x, r.sl.y, r.sl.z, r.sl.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float c = fmaf(cA[k], cB[k], -sA[k] * sB[k]);
@@ -191,6 +204,8 @@ __device__ __forceinline__ void rope(float v[8], int p, const Tables& tb) {
         v[4 + k] = fmaf(hi, c, lo * s);
     }
 }
+
+__device__ __forceinline__ void rope(float v[8], int p, const Tables& tb) { rope_apply(v, rope_rows(p, tb)); }
 
 __device__ __forceinline__ int quant4(float y, const float* t) {
     int c = (y > t[7]) ? 8 : 0;

@@ -277,6 +277,12 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
     float* wp = o.win_kv + ((bh * recent + (size_t)(t % recent)) * 2 + half) * kDim;  // = p's ring slot
     float xp[8];
     load_f32x8_cg(wp, xp);
+    // the RoPE rows of t and p and the running sums, none waiting on the slot
+    const RopeRows rope_t = rope_rows(t, tb), rope_p = rope_rows(max(p, 0), tb);
+    const float* gs0 = o.gsum + bh * hsq::kGsumFloats;
+    const float4 gs_a = __ldcg(reinterpret_cast<const float4*>(gs0 + half * kDim + 4 * l));
+    const float4 gs_b = __ldcg(reinterpret_cast<const float4*>(gs0 + half * kDim + 64 + 4 * l));
+    const float gs_n = __ldcg(gs0 + 2 * kDim);
     load_tables(s_cb, s_sign, tb, c.signs);
     if (threadIdx.x < 24 * c.Hkv) (&s_l2[0][0][0])[threadIdx.x] = 0u;
 
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
             float xr[8], yr[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) xr[i] = x[i];
-            rope(xr, t, tb);
+            rope_apply(xr, rope_t);
             tq_rotate(xr, yr, sg, m);
             uint16_t klo, khi;
             pack4(yr, t4, klo, khi);
@@ -362,17 +368,15 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
         }
     }
     if (leaves) {
-        if (half == 0) rope(xp, p, tb);
+        if (half == 0) rope_apply(xp, rope_p);
         float* gs = o.gsum + bh * hsq::kGsumFloats;
         const bool fresh = p % N == 0;  // p opens its group: nothing summed before it
         float acc[8];
-        const float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
-                               : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 4 * l));
-        const float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : __ldcg(reinterpret_cast<const float4*>(gs + half * kDim + 64 + 4 * l));
+        const float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_a;
+        const float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_b;
         acc[0] = a.x + xp[0]; acc[1] = a.y + xp[1]; acc[2] = a.z + xp[2]; acc[3] = a.w + xp[3];
         acc[4] = bq.x + xp[4]; acc[5] = bq.y + xp[5]; acc[6] = bq.z + xp[6]; acc[7] = bq.w + xp[7];
-        const int cnt = (fresh ? 0 : (int)__ldcg(gs + 2 * kDim)) + 1;
+        const int cnt = (fresh ? 0 : (int)gs_n) + 1;
         __syncwarp();  // every lane has read the count before lane 0 rewrites it
         *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) = make_float4(acc[4], acc[5], acc[6], acc[7]);

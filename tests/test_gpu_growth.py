@@ -17,7 +17,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from hsq_harness import code_mismatch, ensure_built, rel_l2
+from hsq_harness import code_mismatch, ensure_built, rel_l2, sel_mismatch
 
 pytestmark = pytest.mark.gpu
 
@@ -181,3 +181,41 @@ def test_append_refuses_full_cache_and_static_context():
     c = H.allocate_cache(static, w.B, 100, with_staging=False, t_cap=200)
     with pytest.raises(H.HSQError):
         H.hsq_append(static, c, k, k)  # no recent window in this context
+
+
+@pytest.mark.parametrize("spare", [16, 200])
+def test_spare_capacity_is_invisible(spare):
+    """A cache laid out for T + spare tokens (empty trailing groups and bitmap
+    words) routes and attends like the oracle's cache of T tokens."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = W.get_workload("tiny_1k").with_(B=2, T=1000, steps=3)
+    li = W.layer_inputs(w)
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T + spare, w.l1_size, w.T + spare + 8, w.theta)
+    ctx = H.Context(cfg)
+    cache = H.allocate_cache(ctx, w.B, w.T, with_staging=False, t_cap=w.T + spare)
+    H.set_layer_inputs(cache, li.l1_mask, li.signs)
+    H.hsq_encode(ctx, cache, torch.from_numpy(li.K).cuda().contiguous(), torch.from_numpy(li.V).cuda().contiguous())
+    G = -(-w.T // w.N)
+    assert (cache.view("l2_cnt").cpu().numpy()[:, G:] == 0).all()
+    bufs = {k: _np(cache, k) for k in ("l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc",
+                                        "l2_kn", "l2_vn", "l2_cnt", "l3")}
+    for k in ("l2_kc", "l2_vc", "l2_kn", "l2_vn", "l3"):
+        bufs[k] = bufs[k][:, :, :G]
+    bufs["l2_cnt"] = bufs["l2_cnt"][:, :G]
+    gv = O.cache_from_abi(bufs, li.l1_mask, li.signs, w.N, w.T, w.theta)
+    q, pos = W.queries(w, steps=3)
+    for s in range(3):
+        qd, pd = torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda()
+        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        out = torch.empty((w.B, w.Hq, 128), device="cuda")
+        H.hsq_decode_step(ctx, cache, qd, pd, sel, out)
+        assert H.hsq_sync_status(ctx) == 0
+        gsel = sel.cpu().numpy().astype(np.int64)
+        assert gsel.max() < G
+        osel, oscores = O.route(gv, q[s], pos[s], w.beta)
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                assert sel_mismatch(gsel[b, h], osel[b, h], oscores[b, h], w.beta)[0] == 0
+        err = rel_l2(out.cpu().numpy(), O.decode_attn(gv, q[s], pos[s], gsel))
+        assert np.all(err <= 1e-3), f"step {s}: rel L2 {err.max():.3e}"
