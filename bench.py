@@ -61,6 +61,8 @@ def parse_args():
     p.add_argument("--betas", type=str, default="",
                    help="comma-separated beta sweep for the per-layer mode (any workload)")
     p.add_argument("--group-n", type=int, default=0, help="group size N override for the per-layer mode")
+    p.add_argument("--graph", action="store_true",
+                   help="per-layer mode: replay each decode step (all layers) as one captured CUDA graph")
     p.add_argument("--route-max", action="store_true",
                    help="per-layer mode: route by each KV head's best query head (route + attention)")
     return p.parse_args()
@@ -593,17 +595,45 @@ def run_layers(args, rank, world, local):
     clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     sink = torch.empty((), dtype=torch.float32, device="cuda")
 
+    q_in = torch.empty_like(qd[0])
+    p_in = torch.empty_like(pd[0])
+    graphs = {}
+
+    def step_graph(beta, pl):
+        """One decode step (every layer's hsq_decode_step) captured once as a CUDA
+        graph reading the static query buffers q_in / p_in."""
+        if (beta, pl) not in graphs:
+            ctx, cl = ctxs[beta], caches[pl]
+            q_in.copy_(qd[0])
+            p_in.copy_(pd[0])
+            for c in cl:  # the launch plans are made (and cached) outside the capture
+                H.hsq_decode_step(ctx, c, q_in, p_in, sel, out)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for c in cl:
+                    H.hsq_decode_step(ctx, c, q_in, p_in, sel, out)
+            graphs[(beta, pl)] = g
+        return graphs[(beta, pl)]
+
     def loop(beta, pl, nsteps, timed=True):
         ctx, cl = ctxs[beta], caches[pl]
+        g = step_graph(beta, pl) if args.graph else None
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nsteps)]
         torch.cuda._sleep(20_000_000)
         for i in range(nsteps):
             s = i % w.steps
+            if g is not None:  # the step's query goes to the graph's input buffers first
+                q_in.copy_(qd[s])
+                p_in.copy_(pd[s])
             flush.fill_(i & 255)
             torch.sum(clean, dim=0, out=sink)
             ev[i][0].record()
-            for c in cl:
-                H.hsq_decode_step(ctx, c, qd[s], pd[s], sel, out)
+            if g is not None:
+                g.replay()
+            else:
+                for c in cl:
+                    H.hsq_decode_step(ctx, c, qd[s], pd[s], sel, out)
             ev[i][1].record()
         torch.cuda.synchronize()
         return [e[0].elapsed_time(e[1]) for e in ev] if timed else None
@@ -652,6 +682,7 @@ def run_layers(args, rank, world, local):
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} L1={w.l1_size} "
                                f"{L} layers, beta {'/'.join(map(str, betas))}",
                    "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
+                   "launch": "one CUDA graph per step (all layers)" if args.graph else "one call per layer",
                    "routing": "max over each KV head's query heads (route + attention)" if args.route_max
                               else "sum over each KV head's query heads (fused step)",
                    "l2": "cold and clean at every step (256 MiB write + 256 MiB read between steps, "
