@@ -45,6 +45,14 @@ Readings where the pages are silent (each also listed in the design notes):
     tokens, unselected non-empty summaries (one entry each, no count bias)
     and the selected groups' non-L1 tokens recovered from L3 and rotated to
     their positions.
+  * Codec (an ablation on the [TQ] page, "Plain-KV": scalar quantisation
+    without the rotation): codec "plain" replaces Pi by the identity in every
+    tier and keeps everything else (fp32 norm, the same codebook applied to
+    the unrotated unit vector, packing, tiers, routing, attention).
+  * Codec diagnostics ([TQ] metrics: relMSE with the K / V split, and the
+    direction error as cosine similarity): relMSE = sum_t |x^_t - x_t|^2 /
+    sum_t |x_t|^2 over a set of vectors; cosine = the mean over vectors of
+    nonzero norm of x^_t . x_t / (|x^_t| |x_t|).
   * Decode-time growth (the pages describe the tiers of a context and leave
     their growth open): a cache grown by appended tokens is, by definition,
     the encode of the longer context under the grown L1 set (grown_l1_mask):
@@ -89,6 +97,9 @@ __all__ = [
     "cache_to_abi",
     "cache_from_abi",
     "record_bytes",
+    "codec_rotation",
+    "codec_errors",
+    "CODECS",
 ]
 
 D = 128
@@ -196,6 +207,18 @@ def rotation_matrix(signs: np.ndarray) -> np.ndarray:
     return sylvester_hadamard(d) * s[None, :] / np.sqrt(d)
 
 
+CODECS = ("tq", "plain")
+
+
+def codec_rotation(signs: np.ndarray, codec: str = "tq") -> np.ndarray:
+    """The codec's rotation: Pi for TurboQuant, the identity for Plain-KV."""
+    if codec == "tq":
+        return rotation_matrix(signs)
+    if codec == "plain":
+        return np.eye(len(signs))
+    raise ValueError(f"unknown codec {codec!r}")
+
+
 # ---------------------------------------------------------------------------
 # RoPE: the fetched originals are "rotated to their positions" ([HSQ] decode
 # process, step 2).  Rotate-half pairing, float64 angles.
@@ -268,6 +291,20 @@ def unpack_codes(packed: np.ndarray, bits: int, d: int = D) -> np.ndarray:
     return (planes << np.arange(bits, dtype=np.uint8)).sum(axis=-1).astype(np.uint8)
 
 
+def codec_errors(x: np.ndarray, x_hat: np.ndarray) -> dict:
+    """[TQ] metrics over the vectors x[..., d] and their reconstructions:
+    relMSE = sum |x^ - x|^2 / sum |x|^2 and the mean cosine similarity over
+    vectors where both norms are nonzero (float64)."""
+    x = np.asarray(x, dtype=np.float64).reshape(-1, np.shape(x)[-1])
+    xh = np.asarray(x_hat, dtype=np.float64).reshape(x.shape)
+    den = float(np.sum(x * x))
+    rel = float(np.sum((xh - x) ** 2)) / den if den > 0 else 0.0
+    nx, nh = np.linalg.norm(x, axis=1), np.linalg.norm(xh, axis=1)
+    ok = (nx > 0) & (nh > 0)
+    cos = float(np.mean(np.sum(x[ok] * xh[ok], axis=1) / (nx[ok] * nh[ok]))) if ok.any() else 1.0
+    return {"relmse": rel, "cosine": cos}
+
+
 # ---------------------------------------------------------------------------
 # Tiers ([HSQ] three-tier architecture).
 # ---------------------------------------------------------------------------
@@ -311,10 +348,11 @@ class OracleCache:
     l3_k: _Store               # [B, Hkv, T, d] pre-RoPE keys
     l3_v: _Store               # [B, Hkv, T, d]
     quantized: bool = True
+    codec: str = "tq"
 
     @property
     def Pi(self) -> np.ndarray:
-        return rotation_matrix(self.signs)
+        return codec_rotation(self.signs, self.codec)
 
     @property
     def G(self) -> int:
@@ -331,13 +369,14 @@ class OracleCache:
 
 
 def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray, N: int,
-           theta: float = 1.0e6, quantize: bool = True, max_l1: Optional[int] = None) -> OracleCache:
+           theta: float = 1.0e6, quantize: bool = True, max_l1: Optional[int] = None,
+           codec: str = "tq") -> OracleCache:
     """Build the three tiers from pre-RoPE K, V [B, Hkv, T, d] at positions 0..T-1."""
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)
     B, Hkv, T, d = K.shape
     G = -(-T // N)
-    Pi = rotation_matrix(signs)
+    Pi = codec_rotation(signs, codec)
     l1_mask = np.asarray(l1_mask, dtype=bool)
     counts = l1_mask.sum(axis=1)
     L1max = int(counts.max()) if max_l1 is None else int(max_l1)
@@ -379,7 +418,7 @@ def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray,
         l2_cnt=l2_cnt,
         l2_k=_store(l2_kx, 3, Pi, quantize), l2_v=_store(l2_vx, 3, Pi, quantize),
         l3_k=_store(K, 4, Pi, quantize), l3_v=_store(V, 4, Pi, quantize),
-        quantized=quantize,
+        quantized=quantize, codec=codec,
     )
 
 
@@ -588,7 +627,7 @@ def cache_to_abi(cache: OracleCache, max_l1: Optional[int] = None) -> dict:
 
 
 def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T: int,
-                   theta: float = 1.0e6) -> OracleCache:
+                   theta: float = 1.0e6, codec: str = "tq") -> OracleCache:
     """Read a cache back from the library's buffer layout (numpy copies of the buffers)."""
     rec = np.asarray(bufs["l3"], dtype=np.uint8)
     B, Hkv, G, _ = rec.shape
@@ -613,5 +652,5 @@ def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T
         l2_v=_Store(3, codes=unpack_codes(bufs["l2_vc"], 3, d), norms=np.asarray(bufs["l2_vn"])),
         l3_k=_Store(4, codes=kc[:, :, :T], norms=kn[:, :, :T]),
         l3_v=_Store(4, codes=vc[:, :, :T], norms=vn[:, :, :T]),
-        quantized=True,
+        quantized=True, codec=codec,
     )
