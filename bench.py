@@ -337,6 +337,48 @@ def measure_growth(H, torch, w, li, flush, clean, sink):
                    f"{w.T}-token layer (capacity {w.T + n}), recent window {w.recent}, L2 flushed per step"}
 
 
+def measure_codecs(H, torch, w, li):
+    """Codec diagnostics (relMSE_K, relMSE_V and cosine of every token
+    recovered from L3 by hsq_recover against the encoder's bf16 input) for
+    TurboQuant and Plain-KV, on this layer and on heavy-tailed and low-rank
+    key regimes of the same head shape (one sequence of 4096 tokens each)."""
+    def one(wl, lay):
+        K = torch.from_numpy(np.ascontiguousarray(lay.K, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        V = torch.from_numpy(np.ascontiguousarray(lay.V, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        G = -(-wl.T // wl.N)
+        res = {}
+        for codec in ("tq", "plain"):
+            cfg = H.make_config(wl.Hq, wl.Hkv, wl.N, wl.beta, wl.B, wl.T, max(wl.l1_size, 1), wl.T + 1,
+                                wl.theta, codec=codec)
+            cctx = H.Context(cfg)
+            cache = H.allocate_cache(cctx, wl.B, wl.T, l3_on_host=False, with_staging=False)
+            H.set_layer_inputs(cache, lay.l1_mask, lay.signs)
+            H.hsq_encode(cctx, cache, K, V)
+            kh = torch.empty((wl.B, wl.Hkv, G * wl.N, 128), device="cuda")
+            vh = torch.empty_like(kh)
+            H.hsq_recover(cctx, cache, 0, G, kh, vh)
+            assert H.hsq_sync_status(cctx) == 0
+            row = {}
+            for nm, x, xh in (("k", K, kh), ("v", V, vh)):
+                x = x.double().reshape(-1, 128)
+                xh = xh[:, :, : wl.T].double().reshape(-1, 128)
+                row[f"relmse_{nm}"] = float(((xh - x) ** 2).sum() / (x * x).sum())
+                cos = (x * xh).sum(1) / (x.norm(dim=1) * xh.norm(dim=1))
+                row[f"cosine_{nm}"] = float(cos[torch.isfinite(cos)].mean())
+            res[codec] = row
+            del cache
+            cctx.close()
+        return res
+
+    out = {f"{w.name} ({w.key_law} keys)": one(w, li)}
+    for law in ("student_t", "lowrank"):
+        wl = w.with_(name=f"{w.name}_{law}", B=1, T=4096, key_law=law, needle=False, seed_tag=w.seed_tag + 40)
+        out[f"{law} keys, B1 T4096"] = one(wl, W.layer_inputs(wl))
+    out["how"] = ("hsq_recover of every group after hsq_encode (4-bit L3), against the bf16 input; "
+                  "relMSE = sum |x^ - x|^2 / sum |x|^2, cosine = mean over tokens")
+    return out
+
+
 def run_hsq(args, rank, world, local):
     import ctypes
 
@@ -462,6 +504,7 @@ def run_hsq(args, rank, world, local):
         lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
     growth = None if args.quick else measure_growth(H, torch, w, li, flush, clean, sink)
+    codecs = None if args.quick else measure_codecs(H, torch, w, li)
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
     mean = lambda x: sum(x) / len(x)
@@ -514,6 +557,7 @@ def run_hsq(args, rank, world, local):
                    "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
         "link_peak": lp,
         "growth": growth,
+        "codec": codecs,
         "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,

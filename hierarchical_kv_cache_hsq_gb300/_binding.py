@@ -31,6 +31,7 @@ HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER, HSQ_DEVERR_WAIT, HSQ_DEVERR_
 BUFFERS = ["l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc", "l2_kn",
            "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging", "win_kv", "gsum"]
 HSQ_NBUF = len(BUFFERS)
+CODECS = {"tq": 0, "plain": 1}  # hsq_codec
 
 
 class HSQError(RuntimeError):
@@ -46,7 +47,7 @@ class hsq_config(ctypes.Structure):
         ("bits_l2", ctypes.c_int), ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int),
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
         ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
-        ("route_max", ctypes.c_int),
+        ("route_max", ctypes.c_int), ("codec", ctypes.c_int),
     ]
 
 
@@ -73,6 +74,7 @@ _SIGS = {
     "hsq_encode": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, ctypes.c_int, _vp]),
     "hsq_route": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
     "hsq_fetch_dequant": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
+    "hsq_recover": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "hsq_decode_attn": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, ctypes.c_int, _vp]),
     "hsq_decode_step": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp, _vp]),
     "hsq_append": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, ctypes.c_int, _vp]),
@@ -132,14 +134,19 @@ def hsq_codebook(bits: int, dim: int = 128):
 
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
                 max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
-                recent: int = 0, route_max: bool = False) -> hsq_config:
+                recent: int = 0, route_max: bool = False, codec: str = "tq") -> hsq_config:
     """recent > 0 makes caches of this context growable (hsq_append) with an
     L1 recent window of that length and `sinks` permanent sink positions;
-    route_max scores a group by its best query head instead of their sum."""
+    route_max scores a group by its best query head instead of their sum;
+    codec "plain" quantises the unrotated unit vectors (Plain-KV) instead of
+    TurboQuant's rotated ones."""
+    if codec not in CODECS:
+        raise ValueError(f"codec must be one of {tuple(CODECS)}")
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
                       bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
                       max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
-                      l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0)
+                      l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0,
+                      codec=CODECS[codec])
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:
@@ -346,6 +353,12 @@ def hsq_fetch_dequant(ctx: Context, cache: CacheBuffers, sel, k_out=None, v_out=
     c = cache.struct()
     _check(ctx.lib.hsq_fetch_dequant(ctx.handle, ctypes.byref(c), sel.data_ptr(), _ptr(k_out), _ptr(v_out),
                                      _ptr(valid), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_recover(ctx: Context, cache: CacheBuffers, g0: int, ng: int, k_out=None, v_out=None, stream=None):
+    c = cache.struct()
+    _check(ctx.lib.hsq_recover(ctx.handle, ctypes.byref(c), int(g0), int(ng), _ptr(k_out), _ptr(v_out),
+                               _stream_handle(stream)), ctx.handle)
 
 
 def hsq_decode_attn(ctx: Context, cache: CacheBuffers, q, pos, sel, out, flags: int = 0, stream=None):

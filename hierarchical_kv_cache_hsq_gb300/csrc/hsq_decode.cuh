@@ -216,7 +216,8 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
 }
 
-template <int R, int N, bool kRoute, bool kStaged>
+// kRot: TurboQuant (rotated frame); false: Plain-KV (identity, no signs).
+template <int R, int N, bool kRoute, bool kStaged, bool kRot>
 __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
     namespace cgx = cooperative_groups;
     constexpr int NT = dec_threads<R>(), NH = NT / 16, NW = NT / 32;
@@ -293,7 +294,12 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     float qx[8];
     load_f32x8_cg(a.q + ((size_t)b * c.Hq + h * R + min(hw, R - 1)) * kDim, qx);
     float sg[8];
-    load_signs_global(sg, c.signs);
+    if constexpr (kRot) {
+        load_signs_global(sg, c.signs);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sg[i] = 1.f;
+    }
     const uint8_t cnt0 = st2 && tid < n2 ? __ldg(g_cnt + tid) : (uint8_t)0;
 
     // 1. stage the device-resident inputs of this split: first what the L2
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 
     // 2. query heads of this KV head: RoPE'd (original frame) and rotated
     const int pos = checked_pos(pos_raw, tb, a.err);
-    prepare_queries<R>(qx, pos, sg, tb, s_qt, s_qr);
+    prepare_queries<R>(qx, pos, sg, tb, s_qt, s_qr, kRot);
     cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
 
@@ -573,8 +579,8 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
                 const uint16_t* vr = reinterpret_cast<const uint16_t*>(rp + N * 64 + n * 64);
                 unpack4(kr[l], kr[16 + l], c4, 1.0f, kv);
-                fwht(kv, kFull);
-                const float kn = norms[n] * kRsqrtD;
+                if constexpr (kRot) fwht(kv, kFull);
+                const float kn = norms[n] * (kRot ? kRsqrtD : 1.f);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) kv[i] *= sg[i] * kn;
                 {   // RoPE at t = g N + n: base angle (per record) plus offset n omega
@@ -682,9 +688,10 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
         const int kk = min(hw, nmine - 1);
         float ov[8];
         load_f32x8_smem(s_o + kk * kDim, ov);
-        fwht(ov, kFull);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
+        if constexpr (kRot) fwht(ov, kFull);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
+        const float sc = kRot ? kRsqrtD : 1.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ov[i] *= sg[i] * kRsqrtD;
+        for (int i = 0; i < 8; ++i) ov[i] *= sg[i] * sc;
         if (hw < nmine) store_f32x8(a.out + ((size_t)b * c.Hq + h * R + s + kk * S) * kDim, ov);
     }
 }
@@ -693,6 +700,8 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 // ---------------------------------------------------------------------------
 // Host side: launch plan and launch.
 // ---------------------------------------------------------------------------
+
+using DecodeFn = void (*)(CacheView, DecodeArgs, Tables);
 
 cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
     cudaLaunchConfig_t lc = {};
@@ -713,9 +722,15 @@ cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaSt
 // bh clusters are all resident at once (one wave); when none gives one wave,
 // the smallest S that can launch (least per-head overhead across waves).  A
 // fixed n_splits takes the largest launchable S.  0: nothing launchable.
+// The kernel variant of the context's codec.
+template <int R, int N, bool kRoute, bool kStaged>
+DecodeFn decode_fn(bool rot) {
+    return rot ? decode_kernel<R, N, kRoute, kStaged, true> : decode_kernel<R, N, kRoute, kStaged, false>;
+}
+
 template <int R, int N, bool kRoute, bool kStaged>
 int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
-    const void* fn = (const void*)decode_kernel<R, N, kRoute, kStaged>;
+    const void* fn = (const void*)decode_fn<R, N, kRoute, kStaged>(ctx->cfg.codec != HSQ_CODEC_PLAIN);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
     if (hsq::allow_big_clusters(fn, ctx->device) != cudaSuccess) return 0;
@@ -761,13 +776,14 @@ template <int R, int N, bool kRoute, bool kStaged>
 hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
     const DecodeLayout L =
         decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
-    const void* fn = (const void*)decode_kernel<R, N, kRoute, kStaged>;
+    const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0);
+    const void* fn = (const void*)kern;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
     cudaLaunchAttribute at[1];
     const cudaLaunchConfig_t lc = decode_config(S, v.B * v.Hkv, dec_threads<R>(), L.total, st, at);
     const Tables tb = make_tables(ctx);
-    e = cudaLaunchKernelEx(&lc, decode_kernel<R, N, kRoute, kStaged>, v, a, tb);
+    e = cudaLaunchKernelEx(&lc, kern, v, a, tb);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "decode launch");
     return HSQ_OK;
 }

@@ -57,6 +57,7 @@ struct Tables {
 struct CacheView {
     int B, T, G, N, Hkv, Hq, beta, max_l1, W;
     int cap;  // tokens the layout is sized for (G = ceil(cap / N) groups, W = ceil(cap / 32) words)
+    int rot;  // 1: TurboQuant rotation Pi; 0: Plain-KV (identity, signs NULL)
     const uint8_t* l1_kc; const uint8_t* l1_vc; const float* l1_kn; const float* l1_vn;
     const int32_t* l1_pos; const int32_t* l1_count;
     const uint8_t* l2_kc; const uint8_t* l2_vc; const float* l2_kn; const float* l2_vn;
@@ -222,8 +223,9 @@ __device__ __forceinline__ int quant3(float y, const float* t) {
     return c;
 }
 
-// TurboQuant forward: y = Pi (x / n) with Pi = H diag(s) / sqrt(d).  Returns n.
-__device__ __forceinline__ float tq_rotate(float x[8], float y[8], const float sg[8], unsigned m) {
+// Codec forward: y = Pi (x / n) with Pi = H diag(s) / sqrt(d) (TurboQuant),
+// or y = x / n (Plain-KV, rot false).  Returns n.
+__device__ __forceinline__ float tq_rotate(float x[8], float y[8], const float sg[8], unsigned m, bool rot) {
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
@@ -231,10 +233,14 @@ __device__ __forceinline__ float tq_rotate(float x[8], float y[8], const float s
     const float n = sqrtf(ss);
     const float inv = n > 0.f ? 1.0f / n : 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = x[i] * inv * sg[i];
-    fwht(y, m);
+    for (int i = 0; i < 8; ++i) y[i] = x[i] * inv;
+    if (rot) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] *= kRsqrtD;
+        for (int i = 0; i < 8; ++i) y[i] *= sg[i];
+        fwht(y, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] *= kRsqrtD;
+    }
     return n;
 }
 
@@ -319,7 +325,7 @@ __device__ __forceinline__ void store_f32x8(float* __restrict__ p, const float v
 __device__ __forceinline__ void load_tables(float* s_cb, float* s_sign, const Tables& tb,
                                             const int8_t* __restrict__ signs) {
     for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = tb.cb[i];
-    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = (float)signs[i];
+    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = signs ? (float)signs[i] : 1.f;
 }
 
 __device__ __forceinline__ int checked_pos(int p, const Tables& tb, int* err) {
@@ -395,9 +401,14 @@ __device__ __forceinline__ void stage4(float* dst, const float* src, int n) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) cp_async4(dst + i, src + i);
 }
 
-// signs of the lane's 8 dims straight from global memory
+// signs of the lane's 8 dims straight from global memory (all +1 without signs)
 __device__ __forceinline__ void load_signs_global(float s[8], const int8_t* __restrict__ signs) {
     const int l = hlane();
+    if (!signs) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s[i] = 1.f;
+        return;
+    }
     const char4 a = *reinterpret_cast<const char4*>(signs + 4 * l);
     const char4 b = *reinterpret_cast<const char4*>(signs + 64 + 4 * l);
     s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
@@ -766,10 +777,10 @@ __device__ __forceinline__ void route_pair(const float (&gq)[8], const float (&v
 // Rotated, RoPE'd query heads of KV head h: every half-warp computes head
 // min(hw, R - 1) (all warps stay converged); half-warps hw < R store it.
 // x: that head's query (this lane's 8 dims).  With qr, the RoPE'd query in
-// the original frame is stored too.
+// the original frame is stored too.  rot false (Plain-KV): no rotation.
 template <int R>
 __device__ __forceinline__ void prepare_queries(float (&x)[8], int pos, const float sg[8], const Tables& tb,
-                                                float (*s_qt)[kDim], float (*s_qr)[kDim]) {
+                                                float (*s_qt)[kDim], float (*s_qr)[kDim], bool rot) {
     const int hw = threadIdx.x >> 4, l = hlane();
     const int j = min(hw, R - 1);
     rope(x, pos, tb);
@@ -782,12 +793,13 @@ __device__ __forceinline__ void prepare_queries(float (&x)[8], int pos, const fl
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] *= sg[i];
-    fwht(x, kFull);
+    if (rot) fwht(x, kFull);
+    const float sc = rot ? kRsqrtD : 1.f;
     if (hw < R) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            s_qt[j][4 * l + k] = x[k] * kRsqrtD;
-            s_qt[j][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
+            s_qt[j][4 * l + k] = x[k] * sc;
+            s_qt[j][64 + 4 * l + k] = x[4 + k] * sc;
         }
     }
 }
@@ -795,10 +807,11 @@ __device__ __forceinline__ void prepare_queries(float (&x)[8], int pos, const fl
 // The same, loading the query heads (q: the KV head's first query head).
 template <int R>
 __device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int pos, const float sg[8],
-                                                const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim]) {
+                                                const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim],
+                                                bool rot) {
     float x[8];
     load_f32x8_cg(q + (size_t)min((int)threadIdx.x >> 4, R - 1) * kDim, x);
-    prepare_queries<R>(x, pos, sg, tb, s_qt, s_qr);
+    prepare_queries<R>(x, pos, sg, tb, s_qt, s_qr, rot);
 }
 
 __host__ __device__ inline unsigned al16(size_t x) { return (unsigned)((x + 15) & ~(size_t)15); }
@@ -839,7 +852,9 @@ inline CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
     v.l1_kc = c->l1_kc; v.l1_vc = c->l1_vc; v.l1_kn = c->l1_kn; v.l1_vn = c->l1_vn;
     v.l1_pos = c->l1_pos; v.l1_count = c->l1_count;
     v.l2_kc = c->l2_kc; v.l2_vc = c->l2_vc; v.l2_kn = c->l2_kn; v.l2_vn = c->l2_vn; v.l2_cnt = c->l2_cnt;
-    v.l3 = c->l3; v.l1_bitmap = c->l1_bitmap; v.signs = c->signs; v.staging = c->staging;
+    v.l3 = c->l3; v.l1_bitmap = c->l1_bitmap; v.staging = c->staging;
+    v.rot = ctx->cfg.codec == HSQ_CODEC_PLAIN ? 0 : 1;
+    v.signs = v.rot ? c->signs : nullptr;
     return v;
 }
 

@@ -177,6 +177,7 @@ std::string check_config(const hsq_config* c) {
     if (c->l1_recent > 0 && (long long)c->l1_sinks + c->l1_recent > c->max_l1)
         return "l1_sinks + l1_recent must fit max_l1";
     if (c->route_max != 0 && c->route_max != 1) return "route_max must be 0 or 1";
+    if (c->codec != HSQ_CODEC_TQ && c->codec != HSQ_CODEC_PLAIN) return "codec must be HSQ_CODEC_TQ or HSQ_CODEC_PLAIN";
     return "";
 }
 
@@ -190,7 +191,7 @@ std::string check_cache_shape(const hsq_config* cfg, const hsq_cache* c) {
     if (!c->l2_kc || !c->l2_vc || !c->l2_kn || !c->l2_vn || !c->l2_cnt) return "an L2 buffer is NULL";
     if (!c->l3) return "l3 is NULL";
     if (!c->l1_bitmap) return "l1_bitmap is NULL";
-    if (!c->signs) return "signs is NULL";
+    if (!c->signs && cfg->codec != HSQ_CODEC_PLAIN) return "signs is NULL";
     return "";
 }
 

@@ -80,11 +80,11 @@ struct EncodeOut {
 // TQ3 of one group summary (this half-warp's 8 dims of the mean; x is
 // overwritten) into its 48-byte code row and its norm.  w: this half's 12
 // shared words, zero on entry; the whole warp is converged (both halves call it).
-__device__ __forceinline__ void write_summary(float x[8], const float sg[8], unsigned m, const float* t3,
+__device__ __forceinline__ void write_summary(float x[8], const float sg[8], unsigned m, bool rot, const float* t3,
                                               uint32_t* w, uint8_t* codes, float* norm) {
     const int l = hlane();
     float ys[8];
-    const float ns = tq_rotate(x, ys, sg, m);
+    const float ns = tq_rotate(x, ys, sg, m, rot);
     uint32_t fa = 0, fb = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 
     // L3: TQ4 of the raw (pre-RoPE) key / value
     float y[8];
-    const float n = tq_rotate(x, y, sg, m);
+    const float n = tq_rotate(x, y, sg, m, c.rot);
     uint16_t lo, hi;
     pack4(y, t4, lo, hi);
     {
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
         const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
         if (half == 0) {
             float yr[8];
-            tq_rotate(xr, yr, sg, m);  // same norm as the raw key (RoPE is norm preserving)
+            tq_rotate(xr, yr, sg, m, c.rot);  // same norm as the raw key (RoPE is norm preserving)
             uint16_t klo, khi;
             pack4(yr, t4, klo, khi);
             reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
             for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         }
         const size_t go = ((size_t)b * c.Hkv + h) * c.G + g;
-        write_summary(acc, sg, m, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+        write_summary(acc, sg, m, c.rot, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
                       (half ? o.l2_vn : o.l2_kn) + go);
         if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
     }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
 
     // L3 record slot t: TQ4 of the raw key / value
     float y[8];
-    const float n = tq_rotate(x, y, sg, m);
+    const float n = tq_rotate(x, y, sg, m, c.rot);
     uint16_t lo, hi;
     pack4(y, t4, lo, hi);
     {
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
 #pragma unroll
             for (int i = 0; i < 8; ++i) xr[i] = x[i];
             rope_apply(xr, rope_t);
-            tq_rotate(xr, yr, sg, m);
+            tq_rotate(xr, yr, sg, m, c.rot);
             uint16_t klo, khi;
             pack4(yr, t4, klo, khi);
             reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
         for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         const int gp = p / N;
         const size_t go = bh * c.G + gp;
-        write_summary(acc, sg, m, t3, s_l2[h][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+        write_summary(acc, sg, m, c.rot, t3, s_l2[h][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
                       (half ? o.l2_vn : o.l2_kn) + go);
         if (lane == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
     }
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
     float sg[8];
     load_signs_global(sg, c.signs);
     const int p = checked_pos(__ldcg(a.pos + b), tb, a.err);
-    prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, p, sg, tb, s_q, nullptr);
+    prepare_queries<R>(a.q + ((size_t)b * c.Hq + h * R) * kDim, p, sg, tb, s_q, nullptr, c.rot);
     cp_async_wait_all();
     __syncthreads();
     float gq[8];
@@ -496,8 +496,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
 // Fetch + dequantise (standalone): one CTA per (selected slot i, b*Hkv + h).
 // ---------------------------------------------------------------------------
 
+// Slot i of (b, h) holds group sel[b][h][i] (fetch), or g0 + i when sel is
+// NULL (recover: keys stay pre-RoPE).  Outputs have nslot slots per (b, h).
 struct FetchArgs {
     const int32_t* sel; float* k_out; float* v_out; uint8_t* valid; uint8_t* staging; int* err;
+    int g0; int nslot;
 };
 
 template <int N>
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
     const int hw = threadIdx.x >> 4, l = hlane();
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
-    if (threadIdx.x == 0) s_g = valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err);
+    if (threadIdx.x == 0) s_g = a.sel ? valid_sel(a.sel + (size_t)bh * c.beta, i, c.G, a.err) : a.g0 + i;
     __syncthreads();
     const int g = s_g;
     constexpr int kChunks = N * 136 / 16;
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
         uint4 v = make_uint4(0, 0, 0, 0);
         if (g >= 0) v = __ldcg(reinterpret_cast<const uint4*>(c.l3 + ((size_t)bh * c.G + g) * (N * 136)) + k);
         srec[k] = v;
-        if (a.staging) reinterpret_cast<uint4*>(a.staging + ((size_t)bh * c.beta + i) * (N * 136))[k] = v;
+        if (a.staging) reinterpret_cast<uint4*>(a.staging + ((size_t)bh * a.nslot + i) * (N * 136))[k] = v;
     }
     __syncthreads();
     if (hw >= N) return;
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
     load_signs(sg, s_sign);
     const int t = g * N + hw;
     const bool have = g >= 0 && t < c.T;
-    const size_t oo = (((size_t)bh * c.beta + i) * N + hw) * kDim;
+    const size_t oo = (((size_t)bh * a.nslot + i) * N + hw) * kDim;
     float kx[8], vx[8];
     if (have) {
         const float* c4 = s_cb;
@@ -537,15 +540,18 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
         const uint16_t* vr = reinterpret_cast<const uint16_t*>(s_rec + N * 64 + hw * 64);
         unpack4(kr[l], kr[16 + l], c4, 1.0f, kx);
         unpack4(vr[l], vr[16 + l], c4, 1.0f, vx);
-        fwht(kx, m);
-        fwht(vx, m);
-        const float kn = norms[hw] * kRsqrtD, vn = norms[N + hw] * kRsqrtD;
+        if (c.rot) {
+            fwht(kx, m);
+            fwht(vx, m);
+        }
+        const float sc = c.rot ? kRsqrtD : 1.f;
+        const float kn = norms[hw] * sc, vn = norms[N + hw] * sc;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             kx[q] *= sg[q] * kn;
             vx[q] *= sg[q] * vn;
         }
-        rope(kx, t, tb);
+        if (a.sel) rope(kx, t, tb);
     } else {
 #pragma unroll
         for (int q = 0; q < 8; ++q) kx[q] = vx[q] = 0.f;
@@ -553,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
     if (a.k_out) store_f32x8(a.k_out + oo, kx);
     if (a.v_out) store_f32x8(a.v_out + oo, vx);
     if (a.valid && l == 0)
-        a.valid[((size_t)bh * c.beta + i) * N + hw] = (uint8_t)(have && !in_l1(c, b, t));
+        a.valid[((size_t)bh * a.nslot + i) * N + hw] = (uint8_t)(have && !in_l1(c, b, t));
 }
 
 }  // namespace
@@ -857,12 +863,31 @@ hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t
     if (!sel) return fail(ctx, HSQ_ERR_INVALID, "sel is NULL");
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
     CacheView v = make_view(ctx, cache);
-    FetchArgs a{sel, k_out_opt, v_out_opt, valid_opt, cache->staging, ctx->d_err};
+    FetchArgs a{sel, k_out_opt, v_out_opt, valid_opt, cache->staging, ctx->d_err, 0, v.beta};
     dim3 grid(v.beta, v.B * v.Hkv);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (v.N == 16) fetch_kernel<16><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
     else fetch_kernel<8><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
     return after_launch(ctx, "fetch_dequant");
+}
+
+hsq_status hsq_recover(hsq_ctx* ctx, const hsq_cache* cache, int g0, int ng, float* k_out_opt,
+                       float* v_out_opt, hsq_stream_t stream) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    const int groups = hsq::groups_of(cache->T, ctx->cfg.group_n);
+    if (g0 < 0 || ng < 1 || (long long)g0 + ng > groups)
+        return fail(ctx, HSQ_ERR_INVALID, "groups [g0, g0 + ng) must lie in [0, ceil(T / N))");
+    if (!k_out_opt && !v_out_opt) return fail(ctx, HSQ_ERR_INVALID, "no output");
+    if (k_out_opt && (st = check_accessible(ctx, k_out_opt, "k_out")) != HSQ_OK) return st;
+    if (v_out_opt && (st = check_accessible(ctx, v_out_opt, "v_out")) != HSQ_OK) return st;
+    CacheView v = make_view(ctx, cache);
+    FetchArgs a{nullptr, k_out_opt, v_out_opt, nullptr, nullptr, ctx->d_err, g0, ng};
+    dim3 grid(ng, v.B * v.Hkv);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (v.N == 16) fetch_kernel<16><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
+    else fetch_kernel<8><<<grid, kThreads, 0, s>>>(v, a, make_tables(ctx));
+    return after_launch(ctx, "recover");
 }
 
 hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos,
@@ -973,7 +998,7 @@ __global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, Ro
     const int hw = threadIdx.x >> 4, l = hlane();
     const unsigned m = half_mask();
     for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = g_noalloc_codebook[i];
-    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = (float)c.signs[i];
+    for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = c.signs ? (float)c.signs[i] : 1.f;
     __syncthreads();
     float sg[8];
     load_signs(sg, s_sign);
@@ -985,11 +1010,12 @@ __global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, Ro
         rope_f64(x, __ldg(a.pos + b), theta);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] *= sg[i];
-        fwht(x, m);
+        if (c.rot) fwht(x, m);
+        const float sc = c.rot ? kRsqrtD : 1.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            s_q[hw][4 * l + k] = x[k] * kRsqrtD;
-            s_q[hw][64 + 4 * l + k] = x[4 + k] * kRsqrtD;
+            s_q[hw][4 * l + k] = x[k] * sc;
+            s_q[hw][64 + 4 * l + k] = x[4 + k] * sc;
         }
     }
     __syncthreads();
@@ -1192,7 +1218,9 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     v.B = cache->B; v.T = cache->T; v.N = cfg->group_n; v.G = (int)G;
     v.Hkv = cfg->n_kv_heads; v.Hq = cfg->n_q_heads; v.beta = cfg->beta;
     v.max_l1 = cfg->max_l1; v.W = hsq::bitmap_words(cap); v.cap = cap;
-    v.l2_kc = cache->l2_kc; v.l2_kn = cache->l2_kn; v.l2_cnt = cache->l2_cnt; v.signs = cache->signs;
+    v.l2_kc = cache->l2_kc; v.l2_kn = cache->l2_kn; v.l2_cnt = cache->l2_cnt;
+    v.rot = cfg->codec == HSQ_CODEC_PLAIN ? 0 : 1;
+    v.signs = v.rot ? cache->signs : nullptr;
     RouteArgs a{q, pos, sel, reinterpret_cast<float*>(scratch + ticket_bytes),
                 reinterpret_cast<int*>(scratch), nullptr};
     switch (r) {

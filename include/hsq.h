@@ -70,6 +70,8 @@ typedef enum { HSQ_DTYPE_F32 = 0, HSQ_DTYPE_BF16 = 1 } hsq_dtype;
 
 enum { HSQ_HEAD_DIM = 128, HSQ_MAX_BETA = 512, HSQ_MAX_SPLITS = 16 };
 
+typedef enum { HSQ_CODEC_TQ = 0, HSQ_CODEC_PLAIN = 1 } hsq_codec;
+
 /* Bits of the device error word (hsq_sync_status fills *device_word). */
 enum {
     HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
@@ -118,6 +120,14 @@ typedef struct hsq_config {
        (one dot with the summed rotated queries), 1 = their maximum (a group
        counts as much as it does for its best query head). */
     int route_max;
+    /* Codec of every tier (hsq_codec).  HSQ_CODEC_TQ: TurboQuant, the unit
+       vector rotated by Pi = H diag(s) / sqrt(128) before the codebook
+       ("Tamarin (HSQ)", key components; "Ablation, Statistical Inference, and
+       Validation for KV-Cache Compression", experimental setup, item 1).
+       HSQ_CODEC_PLAIN: Plain-KV, the same codebook on the unrotated unit
+       vector (the second page's scalar quantisation without rotation); the
+       signs buffer is then not read. */
+    int codec;
 } hsq_config;
 
 /*
@@ -286,6 +296,22 @@ hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const
 hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t* sel,
                              float* k_out_opt, float* v_out_opt, uint8_t* valid_opt,
                              hsq_stream_t stream);
+
+/*
+ * hsq_recover -- recover the originals of groups [g0, g0 + ng) from L3
+ *   ("Tamarin (HSQ) - reversible hierarchical KV-cache compression": the
+ *   archive keeps every compressed token recoverable).  For token
+ *   t = g*N + n, slot i = g - g0:
+ *     k_out_opt [B][Hkv][ng][N][128] f32: Pi^T n c4[codes] of the key, pre-RoPE;
+ *     v_out_opt [same] f32: the same for the value;
+ *   both in the original frame; tokens t >= T are written as zeros.  L1
+ *   tokens are recovered too (L3 holds every token).  Outputs: device
+ *   memory or mapped page-locked host memory, at least one not NULL.
+ *   Errors: HSQ_ERR_INVALID (g0 < 0, ng < 1, g0 + ng > ceil(T / N), no
+ *   output), HSQ_ERR_CUDA.
+ */
+hsq_status hsq_recover(hsq_ctx* ctx, const hsq_cache* cache, int g0, int ng, float* k_out_opt,
+                       float* v_out_opt, hsq_stream_t stream);
 
 /*
  * hsq_decode_attn -- union attention of one decode step (decode process,

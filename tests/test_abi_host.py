@@ -72,6 +72,7 @@ def test_cache_sizes(H):
     ("head_dim", 64), ("group_n", 12), ("beta", 0), ("beta", 513), ("bits_l1l3", 8),
     ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 17),
     ("n_q_heads", 12), ("l1_sinks", -1), ("l1_recent", -1), ("l1_recent", 101),
+    ("route_max", 2), ("codec", 2), ("codec", -1),
 ])
 def test_invalid_config_rejected(H, field, value):
     cfg = H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000)
@@ -130,3 +131,14 @@ def test_bitmap_packing_matches_definition(H):
     for b in range(3):
         for t in range(70):
             assert bool((int(words[b, t >> 5]) >> (t & 31)) & 1) == mask[b, t]
+
+
+def test_codec_names(H):
+    assert H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000).codec == 0
+    assert H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000, codec="plain").codec == 1
+    with pytest.raises(ValueError):
+        H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000, codec="spectral")
+    # the cache layout does not depend on the codec
+    a = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000), 2, 4096)
+    b = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, codec="plain"), 2, 4096)
+    assert a == b
