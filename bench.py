@@ -63,6 +63,8 @@ def parse_args():
     p.add_argument("--group-n", type=int, default=0, help="group size N override for the per-layer mode")
     p.add_argument("--graph", action="store_true",
                    help="per-layer mode: replay each decode step (all layers) as one captured CUDA graph")
+    p.add_argument("--codec", choices=["tq", "plain"], default="tq",
+                   help="codec of the timed caches: TurboQuant (default) or Plain-KV (no rotation)")
     p.add_argument("--route-max", action="store_true",
                    help="per-layer mode: route by each KV head's best query head (route + attention)")
     return p.parse_args()
@@ -395,7 +397,7 @@ def run_hsq(args, rank, world, local):
     w = W.get_workload(WORKLOAD)
     li, q, pos = workload_inputs(w, lambda x, p: input_rope(x, p, w.theta))
     cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                        args.n_splits)
+                        args.n_splits, codec=args.codec)
     ctx = H.Context(cfg)
     caches = {"host": H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False),
               "device": H.allocate_cache(ctx, w.B, w.T, l3_on_host=False, with_staging=False)}
@@ -527,7 +529,7 @@ def run_hsq(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"cold and clean at every step: {FLUSH_BYTES >> 20} MiB device write, then a "
                          f"{FLUSH_BYTES >> 20} MiB read, between timed steps (outside the step events)",
-                   "n_splits": args.n_splits or "auto"},
+                   "n_splits": args.n_splits or "auto", "codec": args.codec},
         "roofline": {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": hbm_achieved / hbm_peak, "traffic": traffic,
                      "kernel": "decode_kernel (whole step: route, select, L3 gather, attention), L3 in pinned host memory",
@@ -607,7 +609,7 @@ def run_layers(args, rank, world, local):
     li = W.layer_inputs(w, rope=lambda x, p: input_rope(x, p, w.theta))
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                             args.n_splits, route_max=args.route_max) for b in betas}
+                             args.n_splits, route_max=args.route_max, codec=args.codec) for b in betas}
     ctxs = {b: H.Context(c) for b, c in cfgs.items()}
     ctx0 = ctxs[betas[0]]
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
@@ -727,6 +729,7 @@ def run_layers(args, rank, world, local):
                                f"{L} layers, beta {'/'.join(map(str, betas))}",
                    "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
                    "launch": "one CUDA graph per step (all layers)" if args.graph else "one call per layer",
+                   "codec": args.codec,
                    "routing": "max over each KV head's query heads (route + attention)" if args.route_max
                               else "sum over each KV head's query heads (fused step)",
                    "l2": "cold and clean at every step (256 MiB write + 256 MiB read between steps, "
