@@ -40,7 +40,10 @@ Readings where the pages are silent (each also listed in the design notes):
   * Routing: per KV head, s_g = sum over the head's query heads j of
     RoPE(q_j, pos) . k_hat_g; the beta largest (fp32 score, ties to the lower
     group index) are selected and listed in ascending group order, padded
-    with -1 when fewer groups are non-empty.
+    with -1 when fewer groups are non-empty.  Variants: the maximum over
+    the query heads instead of the sum, and per-query-head routing (each
+    query head selects its own beta groups with its own score and attends
+    with that selection: the router's per-head wording taken literally).
   * Attention: for each query head, one softmax (scale 1/sqrt(d)) over L1
     tokens, unselected non-empty summaries (one entry each, no count bias)
     and the selected groups' non-L1 tokens recovered from L3 and rotated to
@@ -462,22 +465,31 @@ def select_top_beta(scores32: np.ndarray, nonempty: np.ndarray, beta: int) -> np
 
 
 def route(cache: OracleCache, q: np.ndarray, pos: np.ndarray, beta: int, agg: str = "sum"):
-    """Per-KV-head routing scores [B, Hkv, G] (float64, -inf for empty groups)
-    and the selection sel [B, Hkv, beta].  [HSQ] decode process, step 1 (a
-    per-head router scores the summary keys against the current query).
-    agg: how a KV head combines its query heads' scores -- "sum" (the reading
-    the library defaults to) or "max" (the group's score for its best head)."""
-    if agg not in ("sum", "max"):
-        raise ValueError("agg must be 'sum' or 'max'")
+    """Routing scores (float64, -inf for empty groups) and the selection.
+    [HSQ] decode process, step 1 (a per-head router scores the summary keys
+    against the current query).  agg:
+      "sum"  -- per KV head, the sum of its query heads' scores (the reading
+                the library defaults to): scores [B, Hkv, G], sel [B, Hkv, beta];
+      "max"  -- per KV head, the group's score for its best query head;
+      "head" -- per query head, its own score against its KV head's
+                summaries: scores [B, Hq, G], sel [B, Hq, beta]."""
+    if agg not in ("sum", "max", "head"):
+        raise ValueError("agg must be 'sum', 'max' or 'head'")
     B, Hq, d = q.shape
     Hkv = cache.Hkv
     qr = rope(np.asarray(q, dtype=np.float64), np.asarray(pos)[:, None], cache.theta)
     khat = cache.l2_k.vectors(cache.Pi)                              # [B, Hkv, G, d]
-    scores = np.full((B, Hkv, cache.G), -np.inf)
-    sel = np.full((B, Hkv, beta), -1, dtype=np.int64)
+    rows = Hq if agg == "head" else Hkv
+    scores = np.full((B, rows, cache.G), -np.inf)
+    sel = np.full((B, rows, beta), -1, dtype=np.int64)
     for b in range(B):
         ne = cache.l2_cnt[b] > 0
         for h, js in enumerate(_heads(Hq, Hkv)):
+            if agg == "head":
+                for j in js:
+                    scores[b, j] = np.where(ne, khat[b, h] @ qr[b, j], -np.inf)
+                    sel[b, j] = select_top_beta(scores[b, j].astype(np.float32), ne, beta)
+                continue
             if agg == "sum":
                 s = khat[b, h] @ qr[b, js].sum(axis=0)
             else:
@@ -518,13 +530,16 @@ def fetch_dequant(cache: OracleCache, sel: np.ndarray):
     return k, v, valid
 
 
-def attention_entries(cache: OracleCache, sel: np.ndarray, b: int, h: int):
-    """Keys, values and provenance of the softmax entry set for one (b, h).
+def attention_entries(cache: OracleCache, sel: np.ndarray, b: int, h: int, kv_head: Optional[int] = None):
+    """Keys, values and provenance of the softmax entry set for selection row
+    sel[b, h] over the tiers of KV head kv_head (default h).
 
     provenance rows: (kind, index) with kind 1 = L1 slot, 2 = summary group,
     3 = fetched token position.
     """
     Pi = cache.Pi
+    s_row = sel[b, h]
+    h = h if kv_head is None else kv_head
     N, T = cache.N, cache.T
     keys, vals, prov = [], [], []
     c = int(cache.l1_count[b])
@@ -532,7 +547,7 @@ def attention_entries(cache: OracleCache, sel: np.ndarray, b: int, h: int):
         keys.append(cache.l1_k.vectors(Pi)[b, h, :c])
         vals.append(cache.l1_v.vectors(Pi)[b, h, :c])
         prov += [(1, i) for i in range(c)]
-    chosen = set(int(g) for g in sel[b, h] if g >= 0)
+    chosen = set(int(g) for g in s_row if g >= 0)
     groups = [g for g in range(cache.G) if cache.l2_cnt[b, g] > 0 and g not in chosen]
     if groups:
         keys.append(cache.l2_k.vectors(Pi)[b, h, groups])
@@ -553,17 +568,24 @@ def attention_entries(cache: OracleCache, sel: np.ndarray, b: int, h: int):
 
 
 def decode_attn(cache: OracleCache, q: np.ndarray, pos: np.ndarray, sel: np.ndarray) -> np.ndarray:
-    """out [B, Hq, d] float64: softmax(q_r . k / sqrt(d)) v over the entry set."""
+    """out [B, Hq, d] float64: softmax(q_r . k / sqrt(d)) v over the entry set.
+
+    sel [B, Hkv, beta]: one selection per KV head, shared by its query heads;
+    sel [B, Hq, beta] with Hq > Hkv: each query head attends with its own."""
     B, Hq, d = q.shape
-    Hkv = sel.shape[1]
+    Hkv = cache.Hkv
+    per_head = sel.shape[1] == Hq and Hq != Hkv
+    if sel.shape[1] != (Hq if per_head else Hkv):
+        raise ValueError("sel must have Hkv or Hq rows")
     qr = rope(np.asarray(q, dtype=np.float64), np.asarray(pos)[:, None], cache.theta)
     out = np.zeros((B, Hq, d))
     for b in range(B):
         for h, js in enumerate(_heads(Hq, Hkv)):
-            keys, vals, _ = attention_entries(cache, sel, b, h)
-            if len(keys) == 0:
-                continue
+            shared = None if per_head else attention_entries(cache, sel, b, h)
             for j in js:
+                keys, vals, _ = attention_entries(cache, sel, b, j, kv_head=h) if per_head else shared
+                if len(keys) == 0:
+                    continue
                 logits = keys @ qr[b, j] / np.sqrt(d)
                 w = np.exp(logits - logits.max())
                 out[b, j] = (w / w.sum()) @ vals

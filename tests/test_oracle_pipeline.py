@@ -266,3 +266,55 @@ def test_max_and_sum_routing_agree_with_one_query_head_per_kv_head():
     np.testing.assert_allclose(a[1], b[1], rtol=1e-15, atol=0)
     with pytest.raises(ValueError):
         O.route(cache, q[0], pos[0], w.beta, agg="mean")
+
+
+# -- per-query-head routing (each query head selects and attends by itself) ---------
+
+def test_per_head_routing_is_single_head_routing_of_each_query_head():
+    """Query head j's scores and selection equal the default routing of a
+    context with one query head per KV head made of head j alone, and its
+    attention output equals that context's output for head j."""
+    w = _small(Hq=8, Hkv=2)
+    li, cache, q, pos = _setup(w)
+    r = w.Hq // w.Hkv
+    sel, scores = O.route(cache, q[0], pos[0], w.beta, agg="head")
+    assert sel.shape == (w.B, w.Hq, w.beta) and scores.shape == (w.B, w.Hq, cache.G)
+    out = O.decode_attn(cache, q[0], pos[0], sel)
+    for j in range(r):
+        heads = [h * r + j for h in range(w.Hkv)]
+        s1, sc1 = O.route(cache, q[0][:, heads], pos[0], w.beta, agg="sum")
+        np.testing.assert_array_equal(sel[:, heads], s1)
+        np.testing.assert_allclose(scores[:, heads], sc1, rtol=1e-15, atol=0)
+        o1 = O.decode_attn(cache, q[0][:, heads], pos[0], s1)
+        np.testing.assert_allclose(out[:, heads], o1, rtol=1e-13, atol=1e-15)
+
+
+def test_per_head_routing_of_identical_query_heads_is_the_shared_routing():
+    """With the query heads of a KV head all equal (r a power of two, so the
+    float32 scores scale exactly), every head selects what the sum selects
+    and the outputs are the shared selection's outputs."""
+    w = _small(Hq=8, Hkv=2)
+    li, cache, q, pos = _setup(w)
+    r = w.Hq // w.Hkv
+    qs = np.repeat(q[0][:, ::r], r, axis=1)               # head h*r of each KV head, repeated
+    shared, _ = O.route(cache, qs, pos[0], w.beta, agg="sum")
+    per, _ = O.route(cache, qs, pos[0], w.beta, agg="head")
+    np.testing.assert_array_equal(per, np.repeat(shared, r, axis=1))
+    np.testing.assert_allclose(O.decode_attn(cache, qs, pos[0], per),
+                               O.decode_attn(cache, qs, pos[0], shared), rtol=1e-13, atol=1e-15)
+
+
+def test_per_head_selection_is_the_brute_force_top_beta_of_its_dots():
+    w = _small(Hq=4, Hkv=2, T=200, N=8, beta=5)
+    li, cache, q, pos = _setup(w)
+    sel, scores = O.route(cache, q[0], pos[0], w.beta, agg="head")
+    khat = cache.l2_k.vectors(cache.Pi)
+    for b in range(w.B):
+        for j in range(w.Hq):
+            h = j // (w.Hq // w.Hkv)
+            qr = O.rope(q[0][b, j].astype(np.float64), pos[0][b], w.theta)
+            ne = cache.l2_cnt[b] > 0
+            dots = np.array([sum(khat[b, h, g, i] * qr[i] for i in range(128)) for g in range(cache.G)])
+            np.testing.assert_allclose(scores[b, j][ne], dots[ne], rtol=1e-12, atol=1e-12)
+            assert np.all(np.isneginf(scores[b, j][~ne]))
+            np.testing.assert_array_equal(sel[b, j], _brute_select(scores[b, j].astype(np.float32), ne, w.beta))
