@@ -47,7 +47,7 @@ class hsq_config(ctypes.Structure):
         ("bits_l2", ctypes.c_int), ("rope_theta", ctypes.c_double), ("max_batch", ctypes.c_int),
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
         ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
-        ("route_max", ctypes.c_int), ("codec", ctypes.c_int),
+        ("route_max", ctypes.c_int), ("codec", ctypes.c_int), ("route_per_head", ctypes.c_int),
     ]
 
 
@@ -134,19 +134,21 @@ def hsq_codebook(bits: int, dim: int = 128):
 
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
                 max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
-                recent: int = 0, route_max: bool = False, codec: str = "tq") -> hsq_config:
+                recent: int = 0, route_max: bool = False, codec: str = "tq",
+                route_per_head: bool = False) -> hsq_config:
     """recent > 0 makes caches of this context growable (hsq_append) with an
     L1 recent window of that length and `sinks` permanent sink positions;
     route_max scores a group by its best query head instead of their sum;
     codec "plain" quantises the unrotated unit vectors (Plain-KV) instead of
-    TurboQuant's rotated ones."""
+    TurboQuant's rotated ones; route_per_head gives every query head its own
+    selection (sel [B, Hq, beta])."""
     if codec not in CODECS:
         raise ValueError(f"codec must be one of {tuple(CODECS)}")
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
                       bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
                       max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
                       l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0,
-                      codec=CODECS[codec])
+                      codec=CODECS[codec], route_per_head=1 if route_per_head else 0)
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:
@@ -219,6 +221,7 @@ class CacheBuffers:
     l3_on_host: bool
     t_cap: int = 0       # layout capacity in tokens (0: T)
     recent: int = 0      # recent-window length of a growable cache
+    sel_heads: int = 0   # selection rows per sequence (Hq under per-query-head routing; 0: Hkv)
 
     @property
     def cap(self) -> int:
@@ -245,7 +248,8 @@ class CacheBuffers:
             "l1_kc": (B, H, L1, 64), "l1_vc": (B, H, L1, 64), "l1_kn": (B, H, L1), "l1_vn": (B, H, L1),
             "l1_pos": (B, L1), "l1_count": (B,), "l2_kc": (B, H, G, 48), "l2_vc": (B, H, G, 48),
             "l2_kn": (B, H, G), "l2_vn": (B, H, G), "l2_cnt": (B, G), "l3": (B, H, G, N * 136),
-            "l1_bitmap": (B, (self.cap + 31) // 32), "staging": (B, H, self.beta, N * 136),
+            "l1_bitmap": (B, (self.cap + 31) // 32),
+            "staging": (B, self.sel_heads or H, self.beta, N * 136),
             "win_kv": (B, H, self.recent, 2, 128), "gsum": (B, H, 260),
         }
         import torch
@@ -289,7 +293,8 @@ def allocate_cache(ctx: Context, B: int, T: int, l3_on_host: bool = True, with_s
     signs = torch.ones(128, dtype=torch.int8, device=dev)
     return CacheBuffers(B=B, T=T, N=ctx.cfg.group_n, Hkv=ctx.cfg.n_kv_heads, max_l1=ctx.cfg.max_l1,
                         beta=ctx.cfg.beta, tensors=t, signs=signs, l3_on_host=l3_on_host,
-                        t_cap=0 if cap == T else cap, recent=ctx.cfg.l1_recent)
+                        t_cap=0 if cap == T else cap, recent=ctx.cfg.l1_recent,
+                        sel_heads=ctx.cfg.n_q_heads if ctx.cfg.route_per_head else ctx.cfg.n_kv_heads)
 
 
 def set_layer_inputs(cache: CacheBuffers, l1_mask: np.ndarray, signs: np.ndarray):

@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     const int S = (int)cluster.num_blocks();
     const int s = (int)cluster.block_rank();
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
+    const size_t bb = buf_head(c, b, h);  // tier buffers of this head (bh unless routing per query head)
     const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
     constexpr int fl = kStaged ? kStagedFlags : 0;
     const DecodeLayout L = decode_layout<R, N>(c.G, c.cap, S, c.max_l1, c.beta, kRoute, fl);
@@ -254,15 +255,15 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     const int nfetch = f1 - f0;
 
     // inputs: staged copies in shared memory, or read in place
-    const uint8_t* g_l2k = c.l2_kc + ((size_t)bh * c.G + g0) * 48;
-    const uint8_t* g_l2v = c.l2_vc + ((size_t)bh * c.G + g0) * 48;
-    const float* g_l2kn = c.l2_kn + (size_t)bh * c.G + g0;
-    const float* g_l2vn = c.l2_vn + (size_t)bh * c.G + g0;
+    const uint8_t* g_l2k = c.l2_kc + (bb * c.G + g0) * 48;
+    const uint8_t* g_l2v = c.l2_vc + (bb * c.G + g0) * 48;
+    const float* g_l2kn = c.l2_kn + bb * c.G + g0;
+    const float* g_l2vn = c.l2_vn + bb * c.G + g0;
     const uint8_t* g_cnt = c.l2_cnt + (size_t)b * c.G + g0;
-    const uint8_t* g_l1k = c.l1_kc + ((size_t)bh * c.max_l1 + e0) * 64;
-    const uint8_t* g_l1v = c.l1_vc + ((size_t)bh * c.max_l1 + e0) * 64;
-    const float* g_l1kn = c.l1_kn + (size_t)bh * c.max_l1 + e0;
-    const float* g_l1vn = c.l1_vn + (size_t)bh * c.max_l1 + e0;
+    const uint8_t* g_l1k = c.l1_kc + (bb * c.max_l1 + e0) * 64;
+    const uint8_t* g_l1v = c.l1_vc + (bb * c.max_l1 + e0) * 64;
+    const float* g_l1kn = c.l1_kn + bb * c.max_l1 + e0;
+    const float* g_l1vn = c.l1_vn + bb * c.max_l1 + e0;
     const uint32_t* g_bitmap = c.l1_bitmap + (size_t)b * c.W;
     constexpr bool st2 = kStaged, st1 = kStaged, stb = kStaged, keep = kStaged;
     const uint8_t* p_l2k = st2 ? s_dyn + L.l2k : g_l2k;
@@ -463,7 +464,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                 const int g = s_sel[i];
                 if (g >= 0) {
                     const uint8_t* src = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
-                                                        : c.l3 + ((size_t)bh * c.G + g) * RB;
+                                                        : c.l3 + (bb * c.G + g) * RB;
                     pre[u] = __ldcg(reinterpret_cast<const uint4*>(src) + off);
                 }
             }
@@ -754,11 +755,11 @@ int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
 // Launch plan for B sequences laid out for T tokens (the capacity; cached per
 // shape): staged inputs when some cluster size fits shared memory, else in place.
 template <int R, int N, bool kRoute>
-hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T) {
+hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T, int heads) {
     for (const auto& e : ctx->plans)
         if (e.B == B && e.T == T && e.route == (int)kRoute) return e;
     const int G = hsq::groups_of(T, N);
-    const int bh = B * ctx->cfg.n_kv_heads;
+    const int bh = B * heads;
     const int fixed = ctx->cfg.n_splits;
     const int s_hi = std::max(1, std::min(fixed > 0 ? fixed : kMaxSplits, std::max(G, 1)));
     hsq_ctx::Plan plan{B, T, (int)kRoute, 0, 1};
@@ -792,7 +793,8 @@ template <int R, int N>
 hsq_status decode_run_n(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, bool route, cudaStream_t st,
                         bool* launched) {
     *launched = false;
-    const hsq_ctx::Plan p = route ? decode_plan<R, N, true>(ctx, v.B, v.cap) : decode_plan<R, N, false>(ctx, v.B, v.cap);
+    const hsq_ctx::Plan p = route ? decode_plan<R, N, true>(ctx, v.B, v.cap, v.Hkv)
+                                  : decode_plan<R, N, false>(ctx, v.B, v.cap, v.Hkv);
     if (p.S == 0) return HSQ_OK;
     *launched = true;
     if (route) return p.staged ? launch_decode<R, N, true, true>(ctx, v, a, p.S, st)
@@ -804,7 +806,7 @@ hsq_status decode_run_n(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, b
 template <int R>
 hsq_status decode_run(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos, int32_t* sel,
                       float* out, bool route, bool from_staging, cudaStream_t st, bool* launched) {
-    const CacheView v = make_view(ctx, cache);
+    const CacheView v = make_sel_view(ctx, cache);
     const DecodeArgs a{q, pos, sel, out, ctx->d_err, from_staging ? 1 : 0};
     return v.N == 16 ? decode_run_n<R, 16>(ctx, v, a, route, st, launched)
                      : decode_run_n<R, 8>(ctx, v, a, route, st, launched);

@@ -58,6 +58,11 @@ struct CacheView {
     int B, T, G, N, Hkv, Hq, beta, max_l1, W;
     int cap;  // tokens the layout is sized for (G = ceil(cap / N) groups, W = ceil(cap / 32) words)
     int rot;  // 1: TurboQuant rotation Pi; 0: Plain-KV (identity, signs NULL)
+    // Heads: the view has Hkv selection heads (per-(b, h) selections, scores,
+    // staging, CTAs); view head h reads the tiers of buffer head h / hdiv of
+    // Hb.  hdiv = 1, Hb = Hkv except under per-query-head routing, where the
+    // view heads are the query heads (Hkv = Hq, hdiv = Hq / Hb).
+    int hdiv, Hb;
     const uint8_t* l1_kc; const uint8_t* l1_vc; const float* l1_kn; const float* l1_vn;
     const int32_t* l1_pos; const int32_t* l1_count;
     const uint8_t* l2_kc; const uint8_t* l2_vc; const float* l2_kn; const float* l2_vn;
@@ -855,7 +860,24 @@ inline CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
     v.l3 = c->l3; v.l1_bitmap = c->l1_bitmap; v.staging = c->staging;
     v.rot = ctx->cfg.codec == HSQ_CODEC_PLAIN ? 0 : 1;
     v.signs = v.rot ? c->signs : nullptr;
+    v.hdiv = 1; v.Hb = v.Hkv;
     return v;
+}
+
+// The view the routing, fetch and decode kernels run on: one selection per
+// KV head, or per query head under per-query-head routing.
+inline CacheView make_sel_view(const hsq_ctx* ctx, const hsq_cache* c) {
+    CacheView v = make_view(ctx, c);
+    if (ctx->cfg.route_per_head) {
+        v.hdiv = v.Hq / v.Hkv;
+        v.Hkv = v.Hq;
+    }
+    return v;
+}
+
+// Row of the tier buffers that view head (b, h) reads.
+__device__ __forceinline__ size_t buf_head(const CacheView& c, int b, int h) {
+    return (size_t)b * c.Hb + h / c.hdiv;
 }
 
 inline Tables make_tables(const hsq_ctx* ctx) {

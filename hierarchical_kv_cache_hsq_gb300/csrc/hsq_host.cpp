@@ -178,6 +178,8 @@ std::string check_config(const hsq_config* c) {
         return "l1_sinks + l1_recent must fit max_l1";
     if (c->route_max != 0 && c->route_max != 1) return "route_max must be 0 or 1";
     if (c->codec != HSQ_CODEC_TQ && c->codec != HSQ_CODEC_PLAIN) return "codec must be HSQ_CODEC_TQ or HSQ_CODEC_PLAIN";
+    if (c->route_per_head != 0 && c->route_per_head != 1) return "route_per_head must be 0 or 1";
+    if (c->route_per_head && c->route_max) return "route_per_head and route_max exclude each other";
     return "";
 }
 
@@ -234,7 +236,8 @@ hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ
     bytes[HSQ_BUF_L2_CNT] = B * G;
     bytes[HSQ_BUF_L3] = B * H * G * hsq::record_bytes((int)N);
     bytes[HSQ_BUF_L1_BITMAP] = (size_t)B * hsq::bitmap_words(T) * 4;
-    bytes[HSQ_BUF_STAGING] = B * H * (size_t)cfg->beta * hsq::record_bytes((int)N);
+    const size_t Hs = cfg->route_per_head ? (size_t)cfg->n_q_heads : H;  // selection rows per sequence
+    bytes[HSQ_BUF_STAGING] = B * Hs * (size_t)cfg->beta * hsq::record_bytes((int)N);
     bytes[HSQ_BUF_WIN_KV] = B * H * (size_t)cfg->l1_recent * 2 * hsq::kDim * 4;
     bytes[HSQ_BUF_GSUM] = cfg->l1_recent > 0 ? B * H * (size_t)hsq::kGsumFloats * 4 : 0;
     return HSQ_OK;

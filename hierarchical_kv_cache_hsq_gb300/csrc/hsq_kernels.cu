@@ -417,8 +417,9 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
 
     const int g_begin = blockIdx.x * kRouteGroupsPerCta;
     const int ng = min(c.G, g_begin + kRouteGroupsPerCta) - g_begin;
-    stage16(s_codes, c.l2_kc + ((size_t)bh * c.G + g_begin) * 48, ng * 48);
-    stage4(s_kn, c.l2_kn + (size_t)bh * c.G + g_begin, ng);
+    const size_t bb = buf_head(c, b, h);  // tier buffers (bh unless routing per query head)
+    stage16(s_codes, c.l2_kc + (bb * c.G + g_begin) * 48, ng * 48);
+    stage4(s_kn, c.l2_kn + bb * c.G + g_begin, ng);
     if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
     for (int i = tid; i < ng; i += kThreads) s_cnt[i] = __ldg(c.l2_cnt + (size_t)b * c.G + g_begin + i);
     float sg[8];
@@ -511,6 +512,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
     __shared__ int s_g;
 
     const int i = blockIdx.x, bh = blockIdx.y, b = bh / c.Hkv;
+    const size_t bb = buf_head(c, b, bh % c.Hkv);  // tier buffers (bh unless routing per query head)
     const int hw = threadIdx.x >> 4, l = hlane();
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads) fetch_kernel(CacheView c, FetchArgs 
     uint4* srec = reinterpret_cast<uint4*>(s_rec);
     for (int k = threadIdx.x; k < kChunks; k += blockDim.x) {
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (g >= 0) v = __ldcg(reinterpret_cast<const uint4*>(c.l3 + ((size_t)bh * c.G + g) * (N * 136)) + k);
+        if (g >= 0) v = __ldcg(reinterpret_cast<const uint4*>(c.l3 + (bb * c.G + g) * (N * 136)) + k);
         srec[k] = v;
         if (a.staging) reinterpret_cast<uint4*>(a.staging + ((size_t)bh * a.nslot + i) * (N * 136))[k] = v;
     }
@@ -639,7 +641,7 @@ hsq_status launch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cu
 }
 
 hsq_status dispatch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, cudaStream_t st) {
-    switch (ctx->r) {
+    switch (v.Hq / v.Hkv) {  // 1 under per-query-head routing
         case 1: return launch_route<1>(ctx, v, a, st);
         case 2: return launch_route<2>(ctx, v, a, st);
         case 4: return launch_route<4>(ctx, v, a, st);
@@ -651,7 +653,7 @@ hsq_status dispatch_route(hsq_ctx* ctx, const CacheView& v, const RouteArgs& a, 
 
 hsq_status decode_run(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const int32_t* pos, int32_t* sel,
                       float* out, bool route, bool from_staging, cudaStream_t st, bool* launched) {
-    switch (ctx->r) {
+    switch (ctx->cfg.route_per_head ? 1 : ctx->r) {  // per query head: one head per view head
         case 1: return hsq::decode_run_r1(ctx, cache, q, pos, sel, out, route, from_staging, st, launched);
         case 2: return hsq::decode_run_r2(ctx, cache, q, pos, sel, out, route, from_staging, st, launched);
         case 4: return hsq::decode_run_r4(ctx, cache, q, pos, sel, out, route, from_staging, st, launched);
@@ -745,7 +747,8 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     hsq::rope_tables(cfg->rope_theta, cfg->max_pos, hi, lo);
     c->G_max = hsq::groups_of(cfg->max_ctx, cfg->group_n);
     c->W_max = hsq::bitmap_words(cfg->max_ctx);
-    const size_t bh = (size_t)cfg->max_batch * cfg->n_kv_heads;
+    // one routing row per KV head, or per query head under per-query-head routing
+    const size_t bh = (size_t)cfg->max_batch * (cfg->route_per_head ? cfg->n_q_heads : cfg->n_kv_heads);
 
     if ((e = cudaMalloc(&c->d_cb, sizeof(cb))) != cudaSuccess) return bail(e, "cudaMalloc(codebook)");
     if ((e = cudaMalloc(&c->d_rope_hi, hi.size() * 4)) != cudaSuccess) return bail(e, "cudaMalloc(rope)");
@@ -848,7 +851,7 @@ hsq_status hsq_route(hsq_ctx* ctx, const hsq_cache* cache, const float* q, const
     if (st != HSQ_OK) return st;
     if (!q || !pos || !sel) return fail(ctx, HSQ_ERR_INVALID, "q, pos or sel is NULL");
     if ((st = check_io(ctx, q, pos, sel, nullptr)) != HSQ_OK) return st;
-    CacheView v = make_view(ctx, cache);
+    CacheView v = make_sel_view(ctx, cache);
     RouteArgs a{q, pos, sel, scores_opt ? scores_opt : ctx->d_scores, ctx->d_route_ctr, ctx->d_err,
                 ctx->cfg.route_max};
     st = dispatch_route(ctx, v, a, reinterpret_cast<cudaStream_t>(stream));
@@ -862,7 +865,7 @@ hsq_status hsq_fetch_dequant(hsq_ctx* ctx, const hsq_cache* cache, const int32_t
     if (st != HSQ_OK) return st;
     if (!sel) return fail(ctx, HSQ_ERR_INVALID, "sel is NULL");
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
-    CacheView v = make_view(ctx, cache);
+    CacheView v = make_sel_view(ctx, cache);
     FetchArgs a{sel, k_out_opt, v_out_opt, valid_opt, cache->staging, ctx->d_err, 0, v.beta};
     dim3 grid(v.beta, v.B * v.Hkv);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1193,7 +1196,8 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
     why = hsq::check_cache_shape(cfg, cache);
     if (!why.empty()) return fail(nullptr, HSQ_ERR_INVALID, why);
-    if (cfg->route_max) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "hsq_route_noalloc routes by the sum only");
+    if (cfg->route_max || cfg->route_per_head)
+        return fail(nullptr, HSQ_ERR_UNSUPPORTED, "hsq_route_noalloc routes by the sum over the query heads only");
     if (!q || !pos || !sel) return fail(nullptr, HSQ_ERR_INVALID, "q, pos or sel is NULL");
     const int r = cfg->n_q_heads / cfg->n_kv_heads;
     if (!r_supported(r)) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "r = Hq/Hkv must be 1, 2, 4, 5 or 8");

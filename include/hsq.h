@@ -128,6 +128,14 @@ typedef struct hsq_config {
        vector (the second page's scalar quantisation without rotation); the
        signs buffer is then not read. */
     int codec;
+    /* 1: per-query-head routing -- every query head selects its own beta
+       groups by its own score against its KV head's summaries and attends
+       with that selection (the router of "Tamarin (HSQ)", decode process,
+       step 1, is per head).  sel, scores and staging then have one row per
+       query head ([B][Hq][...]) instead of one per KV head, and each query
+       head fetches its own records.  0: one selection per KV head.  Not
+       together with route_max. */
+    int route_per_head;
 } hsq_config;
 
 /*
@@ -161,7 +169,7 @@ typedef struct hsq_cache {
     /* L1 membership: bit (t & 31) of word [b][t >> 5]; bits at t >= T are ignored */
     uint32_t* l1_bitmap;      /* [B][ceil(t_cap/32)] device (hsq_append updates it) */
     const int8_t* signs;      /* [128] device, +-1: the layer's Walsh-Hadamard sign vector */
-    uint8_t* staging;         /* [B][Hkv][beta][N*136] device, or NULL (only needed for the
+    uint8_t* staging;         /* [B][Hkv or Hq (route_per_head)][beta][N*136] device, or NULL (only needed for the
                                  staged fetch path) */
     /* Capacity and decode-time growth state (hsq_append). */
     int t_cap;                /* tokens the buffers are laid out for, T <= t_cap <= max_ctx
@@ -270,7 +278,11 @@ hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void*
  *   n_g * (sum_j Pi RoPE(q_j, pos_b)) . c3[codes_g]; with cfg.route_max the
  *   maximum over j of n_g * (Pi RoPE(q_j, pos_b)) . c3[codes_g] instead
  *   (hsq_decode_step then runs hsq_route and hsq_decode_attn; the no-alloc
- *   routing call refuses it); empty groups score -inf.
+ *   routing call refuses it); empty groups score -inf.  With
+ *   cfg.route_per_head every query head j has its own row:
+ *   s_g = n_g * (Pi RoPE(q_j, pos_b)) . c3[codes_g] of its KV head, and sel,
+ *   scores_opt (and, in the calls below, staging and the fetched outputs)
+ *   have Hq rows in place of Hkv.
  *   sel[b][h][0..beta) = the beta largest scores, ties to the lower group,
  *   listed in ascending group order, -1 padded when fewer are non-empty.
  *   q: [B][Hq][128] f32; pos: [B] int32 (query positions); sel:

@@ -72,7 +72,7 @@ def test_cache_sizes(H):
     ("head_dim", 64), ("group_n", 12), ("beta", 0), ("beta", 513), ("bits_l1l3", 8),
     ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 17),
     ("n_q_heads", 12), ("l1_sinks", -1), ("l1_recent", -1), ("l1_recent", 101),
-    ("route_max", 2), ("codec", 2), ("codec", -1),
+    ("route_max", 2), ("codec", 2), ("codec", -1), ("route_per_head", 2),
 ])
 def test_invalid_config_rejected(H, field, value):
     cfg = H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000)
@@ -142,3 +142,13 @@ def test_codec_names(H):
     a = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000), 2, 4096)
     b = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, codec="plain"), 2, 4096)
     assert a == b
+
+
+def test_per_head_routing_sizes_and_exclusion(H):
+    base = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000), 2, 4096)
+    per = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, route_per_head=True), 2, 4096)
+    assert per["staging"] == 4 * base["staging"]  # one row per query head (r = 4)
+    assert {k: v for k, v in per.items() if k != "staging"} == {k: v for k, v in base.items() if k != "staging"}
+    with pytest.raises(H.HSQError):
+        H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, route_per_head=True,
+                                        route_max=True), 2, 4096)
