@@ -65,6 +65,8 @@ def parse_args():
                    help="per-layer mode: replay each decode step (all layers) as one captured CUDA graph")
     p.add_argument("--codec", choices=["tq", "plain"], default="tq",
                    help="codec of the timed caches: TurboQuant (default) or Plain-KV (no rotation)")
+    p.add_argument("--route-per-head", action="store_true",
+                   help="per-layer mode: every query head routes, fetches and attends with its own beta groups")
     p.add_argument("--route-max", action="store_true",
                    help="per-layer mode: route by each KV head's best query head (route + attention)")
     return p.parse_args()
@@ -609,7 +611,8 @@ def run_layers(args, rank, world, local):
     li = W.layer_inputs(w, rope=lambda x, p: input_rope(x, p, w.theta))
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                             args.n_splits, route_max=args.route_max, codec=args.codec) for b in betas}
+                             args.n_splits, route_max=args.route_max, codec=args.codec,
+                             route_per_head=args.route_per_head) for b in betas}
     ctxs = {b: H.Context(c) for b, c in cfgs.items()}
     ctx0 = ctxs[betas[0]]
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
@@ -635,7 +638,8 @@ def run_layers(args, rank, world, local):
     ne = [(caches["host"][l].view("l2_cnt").cpu().numpy() > 0).sum(axis=1) for l in range(L)]
 
     qd, pd = torch.from_numpy(q).cuda(), torch.from_numpy(pos).cuda()
-    sel = torch.empty((w.B, w.Hkv, max(betas)), dtype=torch.int32, device="cuda")
+    rows_sel = w.Hq if args.route_per_head else w.Hkv  # selection rows per sequence
+    sel = torch.empty((w.B, rows_sel, max(betas)), dtype=torch.int32, device="cuda")
     out = torch.empty((w.B, w.Hq, 128), device="cuda")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -696,7 +700,7 @@ def run_layers(args, rank, world, local):
             ts = loop(beta, pl, args.steps)
             ms, _ = aggregate(sum(ts), args.steps, world, device="cuda")
             hbm = [layer_bytes(w, beta, l1c[l], ne[l])[0] for l in range(L)]
-            link = layer_bytes(w, beta, l1c[0], ne[0])[1]
+            link = layer_bytes(w, beta, l1c[0], ne[0])[1] * (rows_sel // w.Hkv)  # records per selection row
             hbm_avg = sum(hbm) / L
             t_layer = ms * 1e-3 / L
             if pl == "host":
@@ -707,10 +711,11 @@ def run_layers(args, rank, world, local):
                 bound = "hbm"
             needle = None
             if w.needle:  # the planted group is routed at step 0 for every (b, KV head)
-                s_r = torch.empty((w.B, w.Hkv, beta), dtype=torch.int32, device="cuda")
+                s_r = torch.empty((w.B, rows_sel, beta), dtype=torch.int32, device="cuda")
                 H.hsq_route(ctxs[beta], caches[pl][0], qd[0], pd[0], s_r)
                 s0 = s_r.cpu().numpy()
-                needle = all(int(li.needle_group[b, h]) in s0[b, h] for b in range(w.B) for h in range(w.Hkv))
+                per = rows_sel // w.Hkv
+                needle = all(int(li.needle_group[b, j // per]) in s0[b, j] for b in range(w.B) for j in range(rows_sel))
             rows.append({"beta": beta, "l3": "pinned host" if pl == "host" else "device", "needle_routed": needle,
                          "ms_per_step": ms, "steps_per_s": world * 1e3 / ms, "us_per_layer": t_layer * 1e6,
                          "hbm_bytes_per_layer": hbm_avg, "l3_bytes_per_layer": link,
@@ -731,7 +736,8 @@ def run_layers(args, rank, world, local):
                    "launch": "one CUDA graph per step (all layers)" if args.graph else "one call per layer",
                    "codec": args.codec,
                    "routing": "max over each KV head's query heads (route + attention)" if args.route_max
-                              else "sum over each KV head's query heads (fused step)",
+                              else "per query head: own selection, fetch and attention (fused step)"
+                              if args.route_per_head else "sum over each KV head's query heads (fused step)",
                    "l2": "cold and clean at every step (256 MiB write + 256 MiB read between steps, "
                          "outside the step events); layers of a step back to back"},
         "per_layer": rows,
@@ -756,7 +762,8 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, rank, world)
-    elif args.workload != WORKLOAD or args.betas or args.group_n or args.layers or args.route_max:
+    elif (args.workload != WORKLOAD or args.betas or args.group_n or args.layers or args.route_max
+          or args.route_per_head):
         line = run_layers(args, rank, world, local)
     else:
         line = run_hsq(args, rank, world, local)

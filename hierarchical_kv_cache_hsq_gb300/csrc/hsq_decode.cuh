@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     const int S = (int)cluster.num_blocks();
     const int s = (int)cluster.block_rank();
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
-    const size_t bb = buf_head(c, b, h);  // tier buffers of this head (bh unless routing per query head)
+    // tier buffers of this head: bh, except under per-query-head routing (run with R = 1)
+    const size_t bb = R == 1 ? buf_head(c, b, h) : (size_t)bh;
     const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
     constexpr int fl = kStaged ? kStagedFlags : 0;
     const DecodeLayout L = decode_layout<R, N>(c.G, c.cap, S, c.max_l1, c.beta, kRoute, fl);

@@ -417,7 +417,8 @@ __global__ void __launch_bounds__(kThreads) route_kernel(CacheView c, RouteArgs 
 
     const int g_begin = blockIdx.x * kRouteGroupsPerCta;
     const int ng = min(c.G, g_begin + kRouteGroupsPerCta) - g_begin;
-    const size_t bb = buf_head(c, b, h);  // tier buffers (bh unless routing per query head)
+    // tier buffers: bh, except under per-query-head routing (run with R = 1)
+    const size_t bb = R == 1 ? buf_head(c, b, h) : (size_t)bh;
     stage16(s_codes, c.l2_kc + (bb * c.G + g_begin) * 48, ng * 48);
     stage4(s_kn, c.l2_kn + bb * c.G + g_begin, ng);
     if (tid < hsq::kCodebookFloats / 4) cp_async16(s_cb + 4 * tid, tb.cb + 4 * tid);
