@@ -11,7 +11,8 @@ sampled pair and step:
     GPU cache and selection (the acceptance of the small-size tests);
 and, for the planted-needle workload, the needle group is routed at step 0
 for every (sequence, KV head).  A further case forces the in-place variant of
-the decode kernel (inputs read from global memory, not staged)."""
+the decode kernel (inputs read from global memory, not staged); two more run
+the 8B/32K layer with the Plain-KV codec and with per-query-head routing."""
 
 import numpy as np
 import pytest
@@ -34,25 +35,26 @@ def _rope(w):
     return lambda x, p: O.rope(x, p, w.theta)
 
 
-def _sub_view(bufs, li, w, b, h):
+def _sub_view(bufs, li, w, b, h, codec="tq"):
     sub = {}
     for k, v in bufs.items():
         v = v[b:b + 1]
         sub[k] = v[:, h:h + 1] if k in PER_HEAD else v
-    return O.cache_from_abi(sub, li.l1_mask[b:b + 1], li.signs, w.N, w.T, w.theta)
+    return O.cache_from_abi(sub, li.l1_mask[b:b + 1], li.signs, w.N, w.T, w.theta, codec=codec)
 
 
-def _run_and_check(w, li, ctx, cache, steps, samples, needle=False):
+def _run_and_check(w, li, ctx, cache, steps, samples, needle=False, codec="tq", per_head=False):
     import torch
     import hierarchical_kv_cache_hsq_gb300 as H
     bufs = abi_buffers(cache)
-    views = {bh: _sub_view(bufs, li, w, *bh) for bh in samples}
+    views = {bh: _sub_view(bufs, li, w, *bh, codec=codec) for bh in samples}
     q, pos = W.queries(w, steps=steps)
     r = w.r
+    rows = w.Hq if per_head else w.Hkv   # selection rows per sequence
     worst = 0.0
     for s in range(steps):
         qd, pd = torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda()
-        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        sel = torch.empty((w.B, rows, w.beta), dtype=torch.int32, device="cuda")
         out = torch.empty((w.B, w.Hq, 128), device="cuda")
         H.hsq_decode_step(ctx, cache, qd, pd, sel, out)
         sel_r = torch.empty_like(sel)
@@ -64,14 +66,17 @@ def _run_and_check(w, li, ctx, cache, steps, samples, needle=False):
         assert np.all(np.isfinite(o))
         if needle and s == 0:
             for b in range(w.B):
-                for h in range(w.Hkv):
-                    assert li.needle_group[b, h] in gsel[b, h], f"needle of (b={b}, h={h}) not routed"
+                for i in range(rows):
+                    h = i // (rows // w.Hkv)
+                    assert li.needle_group[b, h] in gsel[b, i], f"needle of (b={b}, row {i}) not routed"
         for (b, h), view in views.items():
             qs, ps = q[s][b:b + 1, h * r:(h + 1) * r], pos[s][b:b + 1]
-            osel, oscores = O.route(view, qs, ps, w.beta)
-            bad, _ = sel_mismatch(gsel[b, h], osel[0, 0], oscores[0, 0], w.beta)
-            assert bad == 0, f"step {s} (b={b}, h={h}): selection differs beyond near-ties"
-            ref = O.decode_attn(view, qs, ps, gsel[b:b + 1, h:h + 1])
+            mine = slice(h * r, (h + 1) * r) if per_head else slice(h, h + 1)
+            osel, oscores = O.route(view, qs, ps, w.beta, agg="head" if per_head else "sum")
+            for i in range(osel.shape[1]):
+                bad, _ = sel_mismatch(gsel[b, mine][i], osel[0, i], oscores[0, i], w.beta)
+                assert bad == 0, f"step {s} (b={b}, h={h}, row {i}): selection differs beyond near-ties"
+            ref = O.decode_attn(view, qs, ps, gsel[b:b + 1, mine])
             err = rel_l2(o[b:b + 1, h * r:(h + 1) * r], ref)
             worst = max(worst, float(err.max()))
             assert np.all(err <= 1e-3), f"step {s} (b={b}, h={h}): rel L2 {err.max():.3e}"
@@ -85,6 +90,23 @@ def test_qwen3_8b_32k_full_size():
     cache = gpu_encode(ctx, w, li)
     worst = _run_and_check(w, li, ctx, cache, steps=3, samples=[(0, 0), (0, 5)], needle=True)
     print(f"[qwen3_8b_32k] worst sampled rel L2 {worst:.2e}")
+
+
+@pytest.mark.parametrize("variant", ["plain_codec", "per_head_routing"])
+def test_qwen3_8b_32k_variants_full_size(variant):
+    """The Plain-KV codec and per-query-head routing at the full 8B/32K size."""
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = W.get_workload("qwen3_8b_32k")
+    li = W.layer_inputs(w, rope=_rope(w))
+    codec = "plain" if variant == "plain_codec" else "tq"
+    per_head = variant == "per_head_routing"
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
+                        codec=codec, route_per_head=per_head)
+    ctx = H.Context(cfg)
+    cache = gpu_encode(ctx, w, li)
+    worst = _run_and_check(w, li, ctx, cache, steps=2, samples=[(0, 0), (0, 5)], needle=True, codec=codec,
+                           per_head=per_head)
+    print(f"[qwen3_8b_32k {variant}] worst sampled rel L2 {worst:.2e}")
 
 
 def test_qwen3_4b_b16_8k_full_size():
