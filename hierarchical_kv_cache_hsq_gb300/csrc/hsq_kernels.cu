@@ -104,7 +104,8 @@ __device__ __forceinline__ void write_summary(float x[8], const float sg[8], uns
 // (48 resident warps per SM -- 3 CTAs of 16 warps or 6 of 8, 40 registers: the
 // kernel is issue bound and the extra warps hide its memory and shared-memory
 // latencies; 32 warps measured 20 % slower)
-template <int N, bool kBF16>
+// kRot: TurboQuant rotation (false: Plain-KV), fixed at compile time
+template <int N, bool kBF16, bool kRot>
 __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c, EncodeOut o, const void* __restrict__ Kp,
                                                         const void* __restrict__ Vp, Tables tb) {
     __shared__ float s_cb[hsq::kCodebookFloats];
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 
     // L3: TQ4 of the raw (pre-RoPE) key / value
     float y[8];
-    const float n = tq_rotate(x, y, sg, m, c.rot);
+    const float n = tq_rotate(x, y, sg, m, kRot);
     uint16_t lo, hi;
     pack4(y, t4, lo, hi);
     {
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
         const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
         if (half == 0) {
             float yr[8];
-            tq_rotate(xr, yr, sg, m, c.rot);  // same norm as the raw key (RoPE is norm preserving)
+            tq_rotate(xr, yr, sg, m, kRot);  // same norm as the raw key (RoPE is norm preserving)
             uint16_t klo, khi;
             pack4(yr, t4, klo, khi);
             reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
             for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         }
         const size_t go = ((size_t)b * c.Hkv + h) * c.G + g;
-        write_summary(acc, sg, m, c.rot, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+        write_summary(acc, sg, m, kRot, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
                       (half ? o.l2_vn : o.l2_kn) + go);
         if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
     }
@@ -800,13 +801,16 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
                 grow ? cache->win_kv : nullptr, grow ? cache->gsum : nullptr, ctx->cfg.l1_recent};
     dim3 grid(v.G, v.Hkv, v.B);
     const Tables tb = make_tables(ctx);
-    if (v.N == 16) {
-        if (dtype == HSQ_DTYPE_BF16) encode_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, o, K, V, tb);
-        else encode_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, o, K, V, tb);
-    } else {
-        if (dtype == HSQ_DTYPE_BF16) encode_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, o, K, V, tb);
-        else encode_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, o, K, V, tb);
-    }
+    using EncodeFn = void (*)(CacheView, EncodeOut, const void*, const void*, Tables);
+    const bool bf = dtype == HSQ_DTYPE_BF16;
+    EncodeFn fn;  // the variant of the block size, input type and codec
+    if (v.N == 16)
+        fn = v.rot ? (bf ? encode_kernel<16, true, true> : encode_kernel<16, false, true>)
+                   : (bf ? encode_kernel<16, true, false> : encode_kernel<16, false, false>);
+    else
+        fn = v.rot ? (bf ? encode_kernel<8, true, true> : encode_kernel<8, false, true>)
+                   : (bf ? encode_kernel<8, true, false> : encode_kernel<8, false, false>);
+    fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
     return after_launch(ctx, "encode");
 }
 
