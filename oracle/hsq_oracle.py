@@ -52,6 +52,15 @@ Readings where the pages are silent (each also listed in the design notes):
     without the rotation): codec "plain" replaces Pi by the identity in every
     tier and keeps everything else (fp32 norm, the same codebook applied to
     the unrotated unit vector, packing, tiers, routing, attention).
+  * TQ-QKV ([TQ] key contributions, item 1: TurboQuant plus a 1-bit QJL
+    sketch of the key residual): with a sketch matrix S [m, d] (i.i.d.
+    N(0, 1), an input like the signs), every 4-bit key -- L1 and L3 -- keeps
+    bits = (S rho >= 0) and |rho| of its residual rho in the frame its logit
+    is taken in, rotated by the codec: rho = Pi (RoPE(k_t, t) - RoPE(k^_t, t))
+    for L3 (the fetched key is RoPE'd before its logit), rho = Pi (RoPE(k_t,
+    t) - k^) for L1.  A token entry's logit gets the unbiased estimate
+    sqrt(pi/2) / m |rho| sum_i (S Pi q^r)_i sign_i of q^r . (Pi^T rho) added
+    before the 1/sqrt(d) scale; summaries get none.
   * Codec diagnostics ([TQ] metrics: relMSE with the K / V split, and the
     direction error as cosine similarity): relMSE = sum_t |x^_t - x_t|^2 /
     sum_t |x_t|^2 over a set of vectors; cosine = the mean over vectors of
@@ -101,6 +110,11 @@ __all__ = [
     "cache_from_abi",
     "record_bytes",
     "codec_rotation",
+    "Sketch",
+    "qjl_sketch",
+    "qjl_estimate",
+    "entry_sketches",
+    "unpack_sketch_words",
     "codec_errors",
     "CODECS",
 ]
@@ -294,6 +308,29 @@ def unpack_codes(packed: np.ndarray, bits: int, d: int = D) -> np.ndarray:
     return (planes << np.arange(bits, dtype=np.uint8)).sum(axis=-1).astype(np.uint8)
 
 
+@dataclass
+class Sketch:
+    """1-bit sketches of key residuals: bits[..., i] = (S rho)_i >= 0, norm = |rho| (fp32)."""
+    bits: np.ndarray
+    norm: np.ndarray
+
+
+def qjl_sketch(rho: np.ndarray, S: np.ndarray) -> Sketch:
+    """[TQ] TQ-QKV: the 1-bit Johnson-Lindenstrauss sketch of a key's
+    quantisation residual rho[..., d] under the sketch matrix S [m, d]."""
+    rho = np.asarray(rho, dtype=np.float64)
+    return Sketch(bits=(rho @ np.asarray(S, np.float64).T) >= 0.0,
+                  norm=np.linalg.norm(rho, axis=-1).astype(np.float32))
+
+
+def qjl_estimate(Sq: np.ndarray, sk: Sketch) -> np.ndarray:
+    """Estimate of q . rho from the sketch: sqrt(pi/2) / m * |rho| * sum_i (S q)_i sign_i,
+    sign_i = +1 where the bit is set, else -1.  Sq [..., m] broadcasts against sk."""
+    m = sk.bits.shape[-1]
+    signs = np.where(sk.bits, 1.0, -1.0)
+    return np.sqrt(np.pi / 2.0) / m * sk.norm.astype(np.float64) * np.sum(signs * Sq, axis=-1)
+
+
 def codec_errors(x: np.ndarray, x_hat: np.ndarray) -> dict:
     """[TQ] metrics over the vectors x[..., d] and their reconstructions:
     relMSE = sum |x^ - x|^2 / sum |x|^2 and the mean cosine similarity over
@@ -352,6 +389,9 @@ class OracleCache:
     l3_v: _Store               # [B, Hkv, T, d]
     quantized: bool = True
     codec: str = "tq"
+    qjl_S: Optional[np.ndarray] = None     # [m, d] sketch matrix (TQ-QKV) or None
+    l1_qjl: Optional["Sketch"] = None      # [B, Hkv, L1max] key-residual sketches
+    l3_qjl: Optional["Sketch"] = None      # [B, Hkv, T]
 
     @property
     def Pi(self) -> np.ndarray:
@@ -373,7 +413,7 @@ class OracleCache:
 
 def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray, N: int,
            theta: float = 1.0e6, quantize: bool = True, max_l1: Optional[int] = None,
-           codec: str = "tq") -> OracleCache:
+           codec: str = "tq", qjl_S: Optional[np.ndarray] = None) -> OracleCache:
     """Build the three tiers from pre-RoPE K, V [B, Hkv, T, d] at positions 0..T-1."""
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)
@@ -414,7 +454,7 @@ def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray,
                 l2_kx[b, :, g] = K_rope[b][:, m].mean(axis=1)
                 l2_vx[b, :, g] = V[b][:, m].mean(axis=1)
 
-    return OracleCache(
+    cache = OracleCache(
         N=N, T=T, theta=theta, signs=np.asarray(signs, dtype=np.int8), l1_mask=l1_mask,
         l1_count=counts.astype(np.int64), l1_pos=l1_pos,
         l1_k=_store(l1_kx, 4, Pi, quantize), l1_v=_store(l1_vx, 4, Pi, quantize),
@@ -423,6 +463,16 @@ def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray,
         l3_k=_store(K, 4, Pi, quantize), l3_v=_store(V, 4, Pi, quantize),
         quantized=quantize, codec=codec,
     )
+    if qjl_S is not None:
+        if not quantize:
+            raise ValueError("the residual sketch needs quantised keys")
+        S = np.asarray(qjl_S, dtype=np.float64)
+        # L3: the key residual of every token, RoPE'd to its position, in the codec's frame
+        r3 = rope(K - cache.l3_k.vectors(Pi), t_all, theta) @ Pi.T
+        # L1: the residual of the stored post-RoPE key (zero rows past the count)
+        r1 = (l1_kx - cache.l1_k.vectors(Pi)) @ Pi.T
+        cache.qjl_S, cache.l3_qjl, cache.l1_qjl = S, qjl_sketch(r3, S), qjl_sketch(r1, S)
+    return cache
 
 
 def grown_l1_mask(l1_mask: np.ndarray, T_new: int, sinks: int, recent: int) -> np.ndarray:
@@ -567,6 +617,25 @@ def attention_entries(cache: OracleCache, sel: np.ndarray, b: int, h: int, kv_he
     return np.concatenate(keys), np.concatenate(vals), prov
 
 
+def entry_sketches(cache: OracleCache, sel: np.ndarray, b: int, h: int, kv_head: Optional[int] = None):
+    """The residual sketches of attention_entries(...)'s entries (None for a
+    cache without them): L1 slots and fetched tokens carry theirs; summaries
+    carry a zero norm (no correction)."""
+    if cache.qjl_S is None:
+        return None
+    _, _, prov = attention_entries(cache, sel, b, h, kv_head)
+    hb = h if kv_head is None else kv_head
+    m = cache.qjl_S.shape[0]
+    bits = np.zeros((len(prov), m), bool)
+    norm = np.zeros(len(prov), np.float32)
+    for e, (kind, idx) in enumerate(prov):
+        if kind == 1:
+            bits[e], norm[e] = cache.l1_qjl.bits[b, hb, idx], cache.l1_qjl.norm[b, hb, idx]
+        elif kind == 3:
+            bits[e], norm[e] = cache.l3_qjl.bits[b, hb, idx], cache.l3_qjl.norm[b, hb, idx]
+    return Sketch(bits=bits, norm=norm)
+
+
 def decode_attn(cache: OracleCache, q: np.ndarray, pos: np.ndarray, sel: np.ndarray) -> np.ndarray:
     """out [B, Hq, d] float64: softmax(q_r . k / sqrt(d)) v over the entry set.
 
@@ -582,11 +651,16 @@ def decode_attn(cache: OracleCache, q: np.ndarray, pos: np.ndarray, sel: np.ndar
     for b in range(B):
         for h, js in enumerate(_heads(Hq, Hkv)):
             shared = None if per_head else attention_entries(cache, sel, b, h)
+            shared_sk = None if per_head else entry_sketches(cache, sel, b, h)
             for j in js:
                 keys, vals, _ = attention_entries(cache, sel, b, j, kv_head=h) if per_head else shared
                 if len(keys) == 0:
                     continue
-                logits = keys @ qr[b, j] / np.sqrt(d)
+                dots = keys @ qr[b, j]
+                sk = entry_sketches(cache, sel, b, j, kv_head=h) if per_head else shared_sk
+                if sk is not None:  # TQ-QKV: + the sketch estimate of q . residual
+                    dots = dots + qjl_estimate(cache.qjl_S @ (cache.Pi @ qr[b, j]), sk)
+                logits = dots / np.sqrt(d)
                 w = np.exp(logits - logits.max())
                 out[b, j] = (w / w.sum()) @ vals
     return out
@@ -648,8 +722,14 @@ def cache_to_abi(cache: OracleCache, max_l1: Optional[int] = None) -> dict:
     return out
 
 
+def unpack_sketch_words(words: np.ndarray, m: int = D) -> np.ndarray:
+    """uint32 words [..., m/32] -> bits [..., m]: bit i is bit (i mod 32) of word i // 32."""
+    w = np.asarray(words, dtype=np.uint32)
+    return ((w[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1).astype(bool).reshape(w.shape[:-1] + (m,))
+
+
 def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T: int,
-                   theta: float = 1.0e6, codec: str = "tq") -> OracleCache:
+                   theta: float = 1.0e6, codec: str = "tq", qjl_S: Optional[np.ndarray] = None) -> OracleCache:
     """Read a cache back from the library's buffer layout (numpy copies of the buffers)."""
     rec = np.asarray(bufs["l3"], dtype=np.uint8)
     B, Hkv, G, _ = rec.shape
@@ -662,7 +742,7 @@ def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T
     counts = np.asarray(bufs["l1_count"]).astype(np.int64)
     L1max = int(counts.max()) if len(counts) else 0
     pos = np.asarray(bufs["l1_pos"])[:, :L1max].astype(np.int64)
-    return OracleCache(
+    out = OracleCache(
         N=N, T=T, theta=theta, signs=np.asarray(signs, np.int8),
         l1_mask=np.asarray(l1_mask, bool), l1_count=counts, l1_pos=pos,
         l1_k=_Store(4, codes=unpack_codes(bufs["l1_kc"][:, :, :L1max], 4, d),
@@ -676,3 +756,11 @@ def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T
         l3_v=_Store(4, codes=vc[:, :, :T], norms=vn[:, :, :T]),
         quantized=True, codec=codec,
     )
+    if qjl_S is not None:
+        out.qjl_S = np.asarray(qjl_S, np.float64)
+        m = out.qjl_S.shape[0]
+        out.l1_qjl = Sketch(bits=unpack_sketch_words(np.asarray(bufs["l1_qs"])[:, :, :L1max], m),
+                            norm=np.asarray(bufs["l1_qn"])[:, :, :L1max].astype(np.float32))
+        out.l3_qjl = Sketch(bits=unpack_sketch_words(np.asarray(bufs["l3_qs"])[:, :, :T], m),
+                            norm=np.asarray(bufs["l3_qn"])[:, :, :T].astype(np.float32))
+    return out

@@ -180,3 +180,77 @@ def test_plain_encode_tiers_and_abi_round_trip():
     sel, _ = O.route(ora, q[0], pos[0], w.beta)
     np.testing.assert_allclose(O.decode_attn(back, q[0], pos[0], sel), O.decode_attn(ora, q[0], pos[0], sel),
                                rtol=0, atol=1e-13)
+
+
+# -- TQ-QKV: the 1-bit residual sketch of the keys --------------------------------
+
+def test_qjl_estimator_is_unbiased_with_the_closed_form_variance():
+    """For S with i.i.d. N(0, 1) entries, sqrt(pi/2)/m |rho| <S q, sign(S rho)>
+    has mean q . rho and variance ((pi/2)|q|^2|rho|^2 - (q . rho)^2) / m."""
+    rng = np.random.default_rng(21)
+    q, rho = rng.standard_normal(D), rng.standard_normal(D)
+    rho = 0.7 * q + rho           # correlated, so q . rho is far from 0
+    m, draws = 128, 3000
+    est = []
+    for _ in range(draws // 500):
+        S = rng.standard_normal((500, m, D))
+        sk = O.Sketch(bits=np.einsum("kmd,d->km", S, rho) >= 0,
+                      norm=np.full(500, np.linalg.norm(rho), np.float32))
+        est.append(O.qjl_estimate(np.einsum("kmd,d->km", S, q), sk))
+    est = np.concatenate(est)
+    want = q @ rho
+    var = ((np.pi / 2) * (q @ q) * (rho @ rho) - want ** 2) / m
+    se = np.sqrt(var / draws)
+    assert abs(est.mean() - want) <= 4 * se, (est.mean(), want, se)
+    assert abs(est.var(ddof=1) / var - 1.0) <= 0.1, (est.var(ddof=1), var)
+    # one draw through qjl_sketch itself: the bit convention and the stored norm
+    S = rng.standard_normal((m, D))
+    sk = O.qjl_sketch(rho, S)
+    np.testing.assert_array_equal(sk.bits, S @ rho >= 0)
+    assert sk.norm == np.float32(np.linalg.norm(rho))
+    zero = O.qjl_sketch(np.zeros(D), S)
+    assert zero.norm == 0 and O.qjl_estimate(S @ q, zero) == 0.0
+
+
+def test_qjl_corrected_logits_are_unbiased_for_the_exact_logits():
+    """Averaged over sketch matrices, a token entry's corrected dot equals the
+    dot with the unquantised key (RoPE'd for fetched tokens) -- the residual is
+    sketched in the frame its logit is taken in -- while the uncorrected dot
+    keeps its fixed quantisation error."""
+    w = W.get_workload("tiny_1k").with_(T=96, B=1, Hkv=1, Hq=1, N=16, beta=6, sinks=4, recent=16, marked=4)
+    li = W.layer_inputs(w)
+    q, pos = W.queries(w, steps=1)
+    qr = O.rope(q[0][0, 0].astype(np.float64), pos[0][0], w.theta)
+    sel = np.arange(6, dtype=np.int64)[None, None]          # every group (G = 6)
+    rng = np.random.default_rng(5)
+    exact = None
+    diffs = []
+    for _ in range(400):
+        S = rng.standard_normal((128, D))
+        c = O.encode(li.K, li.V, li.l1_mask, li.signs, w.N, w.theta, qjl_S=S)
+        keys, _, prov = O.attention_entries(c, sel, 0, 0)
+        sk = O.entry_sketches(c, sel, 0, 0)
+        if exact is None:
+            K = li.K[0, 0].astype(np.float64)
+            exact = np.array([O.rope(K[idx if kind == 3 else c.l1_pos[0, idx]],
+                                     idx if kind == 3 else c.l1_pos[0, idx], w.theta) @ qr
+                              for kind, idx in prov])
+            plain = keys @ qr
+            tok = np.array([kind != 2 for kind, _ in prov])
+            assert tok.sum() == 96 and np.all(sk.norm[~tok] == 0)
+        diffs.append(keys @ qr + O.qjl_estimate(S @ (c.Pi @ qr), sk) - exact)
+    diffs = np.array(diffs)[:, tok]
+    se = diffs.std(axis=0, ddof=1) / np.sqrt(len(diffs))
+    z = diffs.mean(axis=0) / se
+    assert np.mean(np.abs(z) <= 3.5) >= 0.98, np.sort(np.abs(z))[-5:]
+    # the uncorrected quantisation error is systematic: far outside the same band
+    zq = (plain - exact)[tok] / se
+    assert np.mean(np.abs(zq) > 3.5) >= 0.5
+
+
+def test_qjl_sketch_words_round_trip():
+    rng = np.random.default_rng(4)
+    bits = rng.integers(0, 2, (3, 5, 128)).astype(bool)
+    words = (bits.reshape(3, 5, 4, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(-1).astype(np.uint32)
+    np.testing.assert_array_equal(O.unpack_sketch_words(words), bits)
+    assert O.unpack_sketch_words(np.array([1, 0, 0, 0x80000000], np.uint32))[[0, 127]].all()
