@@ -208,6 +208,24 @@ __device__ __forceinline__ void pair_logits(const float (&q)[R][8], const float 
     }
 }
 
+// pair_logits plus the residual-sketch terms of TQ-QKV:
+// xa[j] = scale * (q_j . ka + sq_j . ca), sq_j = S Pi q^r_j, ca the signed sketch of a.
+template <int R>
+__device__ __forceinline__ void pair_logits_qjl(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
+                                                const float (&sq)[R][8], const float (&ca)[8], const float (&cb)[8],
+                                                float scale, float* xs, float (&xa)[R], float (&xb)[R]) {
+    int idx, idx2;
+    const float d = pair_dots<R>(q, ka, kb, idx) + pair_dots<R>(sq, ca, cb, idx2);
+    __syncwarp();  // the previous pair's reads are done
+    if (idx < 2 * R) xs[idx] = d * scale;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        xa[j] = xs[j];
+        xb[j] = xs[R + j];
+    }
+}
+
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 }
@@ -217,7 +235,8 @@ __device__ __forceinline__ void cluster_wait() {
 }
 
 // kRot: TurboQuant (rotated frame); false: Plain-KV (identity, no signs).
-template <int R, int N, bool kRoute, bool kStaged, bool kRot>
+// kQJL: TQ-QKV, the logits of L1 and fetched tokens carry the residual-sketch term.
+template <int R, int N, bool kRoute, bool kStaged, bool kRot, bool kQJL = false>
 __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
     namespace cgx = cooperative_groups;
     constexpr int NT = dec_threads<R>(), NH = NT / 16, NW = NT / 32;
@@ -226,6 +245,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     __shared__ __align__(16) float s_cb[hsq::kCodebookFloats];
     __shared__ __align__(16) float s_qt[R][kDim];
     __shared__ __align__(16) float s_qr[R][kDim];
+    __shared__ __align__(16) float s_sq[kQJL ? R : 1][kDim];  // S Pi q^r_j (TQ-QKV)
     __shared__ __align__(16) float s_x[NH][16];
     __shared__ SelectSmem s_ss;
     __shared__ __align__(16) uint32_t s_stats[kMaxSplits][4];  // per split: non-empty keys, max key, min key
@@ -348,6 +368,24 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     prepare_queries<R>(qx, pos, sg, tb, s_qt, s_qr, kRot);
     cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
+    if constexpr (kQJL) {
+        // the sketched rotated queries S q~_j (read after the barriers that precede the L1 pass)
+#pragma unroll 1
+        for (int o = tid; o < R * kDim; o += NT) {
+            const int j = o / kDim, i = o % kDim;
+            const float4* srow = reinterpret_cast<const float4*>(c.qjl_s + (size_t)i * kDim);
+            float acc = 0.f;
+#pragma unroll 4
+            for (int d4 = 0; d4 < kDim / 4; ++d4) {
+                const float4 sv = __ldg(srow + d4);
+                acc = fmaf(sv.x, s_qt[j][4 * d4], acc);
+                acc = fmaf(sv.y, s_qt[j][4 * d4 + 1], acc);
+                acc = fmaf(sv.z, s_qt[j][4 * d4 + 2], acc);
+                acc = fmaf(sv.w, s_qt[j][4 * d4 + 3], acc);
+            }
+            s_sq[j][i] = acc;
+        }
+    }
 
     const float* c4 = s_cb;
     const float* c3 = s_cb + 32;
@@ -501,6 +539,17 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 
     Softmax<R> sm;
     sm.init();
+    float sq[kQJL ? R : 1][8];  // this lane's coordinates of S q~_j (TQ-QKV)
+    if constexpr (kQJL) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                sq[j][k] = s_sq[j][4 * l + k];
+                sq[j][4 + k] = s_sq[j][64 + 4 * l + k];
+            }
+        }
+    }
 #pragma unroll 1
     for (int blk = 0; blk < n1; blk += 2 * NH) {
         const int ea = blk + hw, eb = ea + NH;
@@ -512,7 +561,15 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
         const uint16_t* vrb = reinterpret_cast<const uint16_t*>(p_l1v + jb * 64);
         unpack4(kra[l], kra[16 + l], c4, p_l1kn[ja], ka);
         unpack4(krb[l], krb[16 + l], c4, p_l1kn[jb], kb);
-        pair_logits<R>(qt, ka, kb, kLogitScaleLog2, xs, xa, xb);
+        if constexpr (kQJL) {
+            const size_t ia = bb * c.max_l1 + e0 + ja, ib = bb * c.max_l1 + e0 + jb;
+            float ca[8], cb[8];
+            sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ia), kQjlScale * __ldg(c.l1_qn + ia), ca);
+            sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ib), kQjlScale * __ldg(c.l1_qn + ib), cb);
+            pair_logits_qjl<R>(qt, ka, kb, sq, ca, cb, kLogitScaleLog2, xs, xa, xb);
+        } else {
+            pair_logits<R>(qt, ka, kb, kLogitScaleLog2, xs, xa, xb);
+        }
         unpack4(vra[l], vra[16 + l], c4, p_l1vn[ja], va);
         unpack4(vrb[l], vrb[16 + l], c4, p_l1vn[jb], vb);
         sm.add2(xa, va, ea < n1, xb, vb, eb < n1);
@@ -570,12 +627,18 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
             const uint8_t* buf = s_rec + (kb_ & 1) * kFetchBatchBytes;
             const float* sbase = s_base + (kb_ & 1) * kBatchRecs * kDim;
             const uint32_t* rbits = s_rbits + (kb_ & 1) * kBatchRecs;
-            // one recovered token: validity, RoPE'd key and rotated-frame value
-            auto token = [&](int u, float kv[8], float vv[8]) -> bool {
+            // one recovered token: validity, RoPE'd key, rotated-frame value and
+            // (TQ-QKV) the signed residual sketch
+            auto token = [&](int u, float kv[8], float vv[8], float cv[8]) -> bool {
                 const int rec = u / N, n = u - rec * N;
                 const int g = s_sel[r0 + rec];
                 const int t = g * N + n;
                 const bool ok = (g >= 0) & (t < c.T) & (((rbits[rec] >> n) & 1u) == 0u);
+                if constexpr (kQJL) {
+                    const size_t ti = bb * (size_t)c.G * N + (size_t)(ok ? t : 0);
+                    sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l3_qs) + ti),
+                                 ok ? kQjlScale * __ldg(c.l3_qn + ti) : 0.f, cv);
+                }
                 const uint8_t* rp = buf + rec * RB;
                 const float* norms = reinterpret_cast<const float*>(rp + N * 128);
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
@@ -605,10 +668,11 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 #pragma unroll 1
             for (int blk = 0; blk < nt; blk += 2 * NH) {
                 const int ua = blk + hw, ub = ua + NH;
-                float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
-                const bool oka = token(min(ua, nt - 1), ka, va) && ua < nt;
-                const bool okb = token(min(ub, nt - 1), kb, vb) && ub < nt;
-                pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
+                float ka[8], kb[8], va[8], vb[8], xa[R], xb[R], ca[8], cb[8];
+                const bool oka = token(min(ua, nt - 1), ka, va, ca) && ua < nt;
+                const bool okb = token(min(ub, nt - 1), kb, vb, cb) && ub < nt;
+                if constexpr (kQJL) pair_logits_qjl<R>(qr, ka, kb, sq, ca, cb, kLogitScaleLog2, xs, xa, xb);
+                else pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
                 sm.add2(xa, va, oka, xb, vb, okb);
             }
             __syncthreads();  // batch kb_ consumed: its buffer may be refilled
@@ -726,13 +790,16 @@ cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaSt
 // fixed n_splits takes the largest launchable S.  0: nothing launchable.
 // The kernel variant of the context's codec.
 template <int R, int N, bool kRoute, bool kStaged>
-DecodeFn decode_fn(bool rot) {
+DecodeFn decode_fn(bool rot, bool qjl) {
+    if constexpr (!kRoute) {  // TQ-QKV (TurboQuant only) runs as route + attention
+        if (qjl) return decode_kernel<R, N, false, kStaged, true, true>;
+    }
     return rot ? decode_kernel<R, N, kRoute, kStaged, true> : decode_kernel<R, N, kRoute, kStaged, false>;
 }
 
 template <int R, int N, bool kRoute, bool kStaged>
 int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
-    const void* fn = (const void*)decode_fn<R, N, kRoute, kStaged>(ctx->cfg.codec != HSQ_CODEC_PLAIN);
+    const void* fn = (const void*)decode_fn<R, N, kRoute, kStaged>(ctx->cfg.codec != HSQ_CODEC_PLAIN, ctx->cfg.qjl != 0);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
     if (hsq::allow_big_clusters(fn, ctx->device) != cudaSuccess) return 0;
@@ -778,7 +845,7 @@ template <int R, int N, bool kRoute, bool kStaged>
 hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
     const DecodeLayout L =
         decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
-    const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0);
+    const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0, v.qjl_s != nullptr);
     const void* fn = (const void*)kern;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");

@@ -63,6 +63,8 @@ struct CacheView {
     // Hb.  hdiv = 1, Hb = Hkv except under per-query-head routing, where the
     // view heads are the query heads (Hkv = Hq, hdiv = Hq / Hb).
     int hdiv, Hb;
+    // TQ-QKV key-residual sketches (NULL unless cfg.qjl)
+    const float* qjl_s; const uint32_t* l1_qs; const float* l1_qn; const uint32_t* l3_qs; const float* l3_qn;
     const uint8_t* l1_kc; const uint8_t* l1_vc; const float* l1_kn; const float* l1_vn;
     const int32_t* l1_pos; const int32_t* l1_count;
     const uint8_t* l2_kc; const uint8_t* l2_vc; const float* l2_kn; const float* l2_vn;
@@ -861,6 +863,9 @@ inline CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
     v.rot = ctx->cfg.codec == HSQ_CODEC_PLAIN ? 0 : 1;
     v.signs = v.rot ? c->signs : nullptr;
     v.hdiv = 1; v.Hb = v.Hkv;
+    if (ctx->cfg.qjl) {
+        v.qjl_s = c->qjl_s; v.l1_qs = c->l1_qs; v.l1_qn = c->l1_qn; v.l3_qs = c->l3_qs; v.l3_qn = c->l3_qn;
+    }
     return v;
 }
 
@@ -873,6 +878,23 @@ inline CacheView make_sel_view(const hsq_ctx* ctx, const hsq_cache* c) {
         v.Hkv = v.Hq;
     }
     return v;
+}
+
+// sqrt(pi/2) / m for the m = 128-bit residual sketch: E[sign(s . rho) (s . q)] =
+// sqrt(2/pi) (q . rho) / |rho| for s ~ N(0, I).
+constexpr float kQjlScale = 0.0097915167f;
+
+// This lane's 8 sketch signs times w (coordinates 4l + k and 64 + 4l + k of
+// the 128-bit sketch in words wd): +w where the bit is set, else -w.
+__device__ __forceinline__ void sketch_signs(uint4 wd, float w, float s[8]) {
+    const int l = hlane();
+    const uint32_t lo = ((l >> 3) ? wd.y : wd.x) >> (4 * (l & 7));
+    const uint32_t hi = ((l >> 3) ? wd.w : wd.z) >> (4 * (l & 7));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        s[k] = ((lo >> k) & 1u) ? w : -w;
+        s[4 + k] = ((hi >> k) & 1u) ? w : -w;
+    }
 }
 
 // Row of the tier buffers that view head (b, h) reads.

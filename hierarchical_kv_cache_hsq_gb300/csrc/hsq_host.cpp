@@ -180,6 +180,8 @@ std::string check_config(const hsq_config* c) {
     if (c->codec != HSQ_CODEC_TQ && c->codec != HSQ_CODEC_PLAIN) return "codec must be HSQ_CODEC_TQ or HSQ_CODEC_PLAIN";
     if (c->route_per_head != 0 && c->route_per_head != 1) return "route_per_head must be 0 or 1";
     if (c->route_per_head && c->route_max) return "route_per_head and route_max exclude each other";
+    if (c->qjl != 0 && c->qjl != 1) return "qjl must be 0 or 1";
+    if (c->qjl && c->codec != HSQ_CODEC_TQ) return "qjl (TQ-QKV) needs the TurboQuant codec";
     return "";
 }
 
@@ -194,6 +196,8 @@ std::string check_cache_shape(const hsq_config* cfg, const hsq_cache* c) {
     if (!c->l3) return "l3 is NULL";
     if (!c->l1_bitmap) return "l1_bitmap is NULL";
     if (!c->signs && cfg->codec != HSQ_CODEC_PLAIN) return "signs is NULL";
+    if (cfg->qjl && (!c->qjl_s || !c->l1_qs || !c->l1_qn || !c->l3_qs || !c->l3_qn))
+        return "a key-residual sketch buffer is NULL (cfg.qjl)";
     return "";
 }
 
@@ -240,6 +244,11 @@ hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ
     bytes[HSQ_BUF_STAGING] = B * Hs * (size_t)cfg->beta * hsq::record_bytes((int)N);
     bytes[HSQ_BUF_WIN_KV] = B * H * (size_t)cfg->l1_recent * 2 * hsq::kDim * 4;
     bytes[HSQ_BUF_GSUM] = cfg->l1_recent > 0 ? B * H * (size_t)hsq::kGsumFloats * 4 : 0;
+    const size_t q = cfg->qjl ? 1 : 0;  // key-residual sketches: 16 B of bits + a float norm per key
+    bytes[HSQ_BUF_L1_QS] = q * B * H * L1 * 16;
+    bytes[HSQ_BUF_L1_QN] = q * B * H * L1 * 4;
+    bytes[HSQ_BUF_L3_QS] = q * B * H * G * N * 16;
+    bytes[HSQ_BUF_L3_QN] = q * B * H * G * N * 4;
     return HSQ_OK;
 }
 

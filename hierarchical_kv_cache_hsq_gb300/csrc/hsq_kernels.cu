@@ -246,6 +246,128 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 }
 
 // ---------------------------------------------------------------------------
+// TQ-QKV, encode side: the 1-bit sketches of the key residuals.  One CTA per
+// (group g, KV head h, sequence b), one warp per token: half 0 sketches the
+// L3 key's residual, half 1 the L1 key's when the token is in L1.  Both
+// halves redo the quantiser decision of encode_kernel with the same
+// arithmetic, so the residual is that of the stored codes.
+// ---------------------------------------------------------------------------
+
+struct SketchOut {
+    const float* S; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
+};
+
+template <int N, bool kBF16>
+__global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp, Tables tb) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) float s_rho[N][2][kDim];
+
+    const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1, l = hlane();
+    const unsigned m = half_mask();
+    load_tables(s_cb, s_sign, tb, c.signs);
+    __syncthreads();
+    const float* c4 = s_cb;
+    const float* t4 = s_cb + 16;
+    float sg[8];
+    load_signs(sg, s_sign);
+
+    const int t = g * N + warp;
+    const bool in_ctx = t < c.T;
+    bool is_l1 = false;
+    int slot = 0;
+    if (in_ctx) {
+        const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
+        is_l1 = (w >> (t & 31)) & 1u;
+        if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
+    }
+    const bool active = in_ctx && (half == 0 || (is_l1 && slot < c.max_l1));  // uniform per half-warp
+
+    float x[8];
+    if (in_ctx) {
+        const size_t off = (((size_t)b * c.Hkv + h) * c.T + t) * kDim;
+        if (kBF16) load_bf16x8(static_cast<const uint16_t*>(Kp) + off, x);
+        else load_f32x8(static_cast<const float*>(Kp) + off, x);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.f;
+    }
+    float rho[8];
+    if (half == 0) {
+        // L3: e = n (y - c4[code]) is Pi (k - k^); back to the original frame, RoPE to
+        // position t, and into the rotated frame again
+        float y[8];
+        const float n = tq_rotate(x, y, sg, m, true);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rho[i] = n * (y[i] - c4[quant4(y[i], t4)]);
+        fwht(rho, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rho[i] *= sg[i] * kRsqrtD;
+        rope(rho, in_ctx ? t : 0, tb);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rho[i] *= sg[i];
+        fwht(rho, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rho[i] *= kRsqrtD;
+    } else {
+        // L1: the stored key is TQ4 of RoPE(k, t) with the raw key's norm n
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+        const float n = sqrtf(half_sum(ss, m));
+        rope(x, in_ctx ? t : 0, tb);
+        float yr[8];
+        const float nr = tq_rotate(x, yr, sg, m, true);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rho[i] = nr * yr[i] - n * c4[quant4(yr[i], t4)];
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
+    const float gamma = sqrtf(half_sum(ss, m));
+    float* row = s_rho[warp][half];
+    *reinterpret_cast<float4*>(row + 4 * l) = make_float4(rho[0], rho[1], rho[2], rho[3]);
+    *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(rho[4], rho[5], rho[6], rho[7]);
+    __syncwarp();
+    // this lane's 8 sketch rows i = 4l + k and 64 + 4l + k: bit = (S_i . rho >= 0)
+    uint32_t lo = 0u, hi = 0u;
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+        const int i = k < 4 ? 4 * l + k : 64 + 4 * l + (k - 4);
+        const float4* srow = reinterpret_cast<const float4*>(o.S + (size_t)i * kDim);
+        float acc = 0.f;
+#pragma unroll 8
+        for (int d4 = 0; d4 < kDim / 4; ++d4) {
+            const float4 sv = __ldg(srow + d4);
+            const float4 rv = *reinterpret_cast<const float4*>(row + 4 * d4);
+            acc = fmaf(sv.x, rv.x, acc);
+            acc = fmaf(sv.y, rv.y, acc);
+            acc = fmaf(sv.z, rv.z, acc);
+            acc = fmaf(sv.w, rv.w, acc);
+        }
+        const uint32_t bit = acc >= 0.f ? 1u : 0u;
+        if (k < 4) lo |= bit << k;
+        else hi |= bit << (k - 4);
+    }
+    // words: nibble of lane l at bits 4 (l & 7) of word l >> 3 (low coordinates) or 2 + (l >> 3)
+    uint32_t wlo = lo << (4 * (l & 7)), whi = hi << (4 * (l & 7));
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+        wlo |= __shfl_xor_sync(m, wlo, off, 16);
+        whi |= __shfl_xor_sync(m, whi, off, 16);
+    }
+    if (active && (l & 7) == 0) {
+        const size_t e = half == 0 ? (((size_t)b * c.Hkv + h) * c.G * N + t)
+                                   : (((size_t)b * c.Hkv + h) * c.max_l1 + slot);
+        uint32_t* qs = (half == 0 ? o.l3_qs : o.l1_qs) + e * 4;
+        qs[l >> 3] = wlo;
+        qs[2 + (l >> 3)] = whi;
+        if (l == 0) (half == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Decode-time growth: append one token per sequence at position T.  One CTA
 // per sequence b, one warp per KV head.  Warp 0 first finds the L1 slot of the
 // new token -- the slot of the token p = T - recent that leaves the window,
@@ -811,6 +933,16 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
         fn = v.rot ? (bf ? encode_kernel<8, true, true> : encode_kernel<8, false, true>)
                    : (bf ? encode_kernel<8, true, false> : encode_kernel<8, false, false>);
     fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
+    if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
+        const SketchOut so{cache->qjl_s, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
+        if (v.N == 16) {
+            if (bf) qjl_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
+        } else {
+            if (bf) qjl_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
+        }
+    }
     return after_launch(ctx, "encode");
 }
 
@@ -820,6 +952,7 @@ hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void*
     if (st != HSQ_OK) return st;
     if (!k || !v) return fail(ctx, HSQ_ERR_INVALID, "k or v is NULL");
     if (dtype != HSQ_DTYPE_F32 && dtype != HSQ_DTYPE_BF16) return fail(ctx, HSQ_ERR_INVALID, "bad dtype");
+    if (ctx->cfg.qjl) return fail(ctx, HSQ_ERR_UNSUPPORTED, "hsq_append does not sketch key residuals (cfg.qjl)");
     const int recent = ctx->cfg.l1_recent;
     if (recent < 1) return fail(ctx, HSQ_ERR_INVALID, "the context has no recent window (l1_recent = 0)");
     if (!cache->win_kv || !cache->gsum) return fail(ctx, HSQ_ERR_INVALID, "win_kv or gsum is NULL");
@@ -925,7 +1058,7 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool fused = false;
-    if (!ctx->cfg.route_max) {  // (the fused kernel routes by the sum over the query heads)
+    if (!ctx->cfg.route_max && !ctx->cfg.qjl) {  // (the fused kernel: sum routing, TQ-KV logits)
         st = decode_run(ctx, cache, q, pos, sel, out, true, false, s, &fused);
         if (st != HSQ_OK || fused) return st;
     }

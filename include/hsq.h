@@ -136,6 +136,19 @@ typedef struct hsq_config {
        head fetches its own records.  0: one selection per KV head.  Not
        together with route_max. */
     int route_per_head;
+    /* 1: TQ-QKV ("Ablation, Statistical Inference, and Validation for
+       KV-Cache Compression", key contributions, item 1) -- every 4-bit key
+       (L1 and L3) also keeps a 1-bit Johnson-Lindenstrauss sketch of its
+       quantisation residual rho, taken in the frame its logit is computed in
+       and rotated by the codec (L3: Pi RoPE(k_t - k^_t, t); L1: Pi (RoPE(k_t, t)
+       - k^)): 128 bits (S rho >= 0) and |rho|, S = cache->qjl_s.  A token's
+       logit then adds sqrt(pi/2) / 128 * |rho| * sum_i (S Pi q^r)_i sign_i
+       before the 1/sqrt(128) scale (an unbiased estimate of q^r . residual).
+       Needs codec HSQ_CODEC_TQ.  hsq_encode writes the sketches (the key
+       input is read a second time); hsq_decode_step runs hsq_route +
+       hsq_decode_attn under it; hsq_append refuses it (HSQ_ERR_UNSUPPORTED).
+       0: TQ-KV. */
+    int qjl;
 } hsq_config;
 
 /*
@@ -182,13 +195,20 @@ typedef struct hsq_cache {
                                  T - l1_recent, the float sums, in position order, of its members
                                  below that position: RoPE'd keys [128] | values [128] | member
                                  count | the window's first position at encode | pad [2] */
+    /* Key-residual sketches (cfg.qjl = 1; else ignored).  Sketch words: bit i of
+       the 128-bit sketch is bit (i mod 32) of word i / 32. */
+    const float* qjl_s;       /* [128][128] device, row i = sketch direction i (i.i.d. N(0,1)) */
+    uint32_t* l1_qs;          /* [B][Hkv][max_l1][4] device: sketches of the L1 keys' residuals */
+    float* l1_qn;             /* [B][Hkv][max_l1] device: their norms */
+    uint32_t* l3_qs;          /* [B][Hkv][G*N][4] device: sketches of every token's key residual */
+    float* l3_qn;             /* [B][Hkv][G*N] device: their norms */
 } hsq_cache;
 
 typedef enum {
     HSQ_BUF_L1_KC = 0, HSQ_BUF_L1_VC, HSQ_BUF_L1_KN, HSQ_BUF_L1_VN, HSQ_BUF_L1_POS,
     HSQ_BUF_L1_COUNT, HSQ_BUF_L2_KC, HSQ_BUF_L2_VC, HSQ_BUF_L2_KN, HSQ_BUF_L2_VN,
     HSQ_BUF_L2_CNT, HSQ_BUF_L3, HSQ_BUF_L1_BITMAP, HSQ_BUF_STAGING, HSQ_BUF_WIN_KV,
-    HSQ_BUF_GSUM, HSQ_NBUF
+    HSQ_BUF_GSUM, HSQ_BUF_L1_QS, HSQ_BUF_L1_QN, HSQ_BUF_L3_QS, HSQ_BUF_L3_QN, HSQ_NBUF
 } hsq_buffer;
 
 typedef struct hsq_ctx hsq_ctx;   /* opaque, library-owned */

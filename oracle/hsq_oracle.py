@@ -115,6 +115,7 @@ __all__ = [
     "qjl_estimate",
     "entry_sketches",
     "unpack_sketch_words",
+    "key_residuals",
     "codec_errors",
     "CODECS",
 ]
@@ -467,12 +468,28 @@ def encode(K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray,
         if not quantize:
             raise ValueError("the residual sketch needs quantised keys")
         S = np.asarray(qjl_S, dtype=np.float64)
-        # L3: the key residual of every token, RoPE'd to its position, in the codec's frame
-        r3 = rope(K - cache.l3_k.vectors(Pi), t_all, theta) @ Pi.T
-        # L1: the residual of the stored post-RoPE key (zero rows past the count)
-        r1 = (l1_kx - cache.l1_k.vectors(Pi)) @ Pi.T
+        r3, r1 = key_residuals(cache, K)
         cache.qjl_S, cache.l3_qjl, cache.l1_qjl = S, qjl_sketch(r3, S), qjl_sketch(r1, S)
     return cache
+
+
+def key_residuals(cache: OracleCache, K: np.ndarray):
+    """TQ-QKV: the key residuals of a cache's stored codes against the input
+    keys K [B, Hkv, T, d], each in the frame its logit is taken in, rotated by
+    the codec: L3 [B, Hkv, T, d] = Pi RoPE(k_t - k^_t, t); L1 [B, Hkv, L1max, d]
+    = Pi (RoPE(k_t, t) - k^) for the L1 slots (zero rows past the count)."""
+    K = np.asarray(K, dtype=np.float64)
+    Pi = cache.Pi
+    T = cache.T
+    r3 = rope(K - cache.l3_k.vectors(Pi), np.arange(T), cache.theta) @ Pi.T
+    k1 = cache.l1_k.vectors(Pi)
+    x1 = np.zeros_like(k1)
+    for b in range(K.shape[0]):
+        c = int(cache.l1_count[b])
+        p = cache.l1_pos[b, :c]
+        x1[b, :, :c] = rope(K[b][:, p], p, cache.theta)
+        k1[b, :, c:] = 0.0
+    return r3, (x1 - k1) @ Pi.T
 
 
 def grown_l1_mask(l1_mask: np.ndarray, T_new: int, sinks: int, recent: int) -> np.ndarray:

@@ -72,7 +72,7 @@ def test_cache_sizes(H):
     ("head_dim", 64), ("group_n", 12), ("beta", 0), ("beta", 513), ("bits_l1l3", 8),
     ("bits_l2", 4), ("rope_theta", 0.0), ("max_batch", 0), ("max_pos", 10), ("n_splits", 17),
     ("n_q_heads", 12), ("l1_sinks", -1), ("l1_recent", -1), ("l1_recent", 101),
-    ("route_max", 2), ("codec", 2), ("codec", -1), ("route_per_head", 2),
+    ("route_max", 2), ("codec", 2), ("codec", -1), ("route_per_head", 2), ("qjl", 2),
 ])
 def test_invalid_config_rejected(H, field, value):
     cfg = H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000)
@@ -152,3 +152,13 @@ def test_per_head_routing_sizes_and_exclusion(H):
     with pytest.raises(H.HSQError):
         H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, route_per_head=True,
                                         route_max=True), 2, 4096)
+
+
+def test_qjl_sizes_and_codec_requirement(H):
+    base = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000), 2, 4096)
+    q = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, qjl=True), 2, 4096)
+    assert all(base[n] == 0 for n in ("l1_qs", "l1_qn", "l3_qs", "l3_qn"))
+    assert q["l3_qs"] == 2 * 8 * 256 * 16 * 16 and q["l3_qn"] == 2 * 8 * 256 * 16 * 4  # 16 B + 4 B per token
+    assert q["l1_qs"] == 2 * 8 * 100 * 16 and q["l1_qn"] == 2 * 8 * 100 * 4
+    with pytest.raises(H.HSQError):
+        H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, codec="plain", qjl=True), 2, 4096)

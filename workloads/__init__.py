@@ -13,6 +13,7 @@ from .generate import (
     LayerInputs,
     layer_inputs,
     layer_meta,
+    qjl_matrix,
     queries,
     needle_groups,
     plant_needle,
@@ -27,6 +28,7 @@ __all__ = [
     "LayerInputs",
     "layer_inputs",
     "layer_meta",
+    "qjl_matrix",
     "queries",
     "needle_groups",
     "plant_needle",

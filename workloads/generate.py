@@ -18,6 +18,7 @@ Recipes (stated readings of the workload text):
     without replacement from [sinks, T - recent), per (layer, b).
   * signs: one +-1 vector of length d per layer (shared by K, V, all tiers
     and heads).
+  * sketch matrix (TQ-QKV): one [128, d] float32 N(0, 1) matrix per layer.
   * queries: float32 N(0, 1) at position T + s for step s.  With a needle,
     q_s = sqrt(0.8) q_0 + sqrt(0.2) z_s for s >= 1, so the needle stays
     near alignment while the selection still moves from step to step.
@@ -47,6 +48,7 @@ _PURPOSE = {
     "key_scale": 8,
     "outlier_channels": 9,
     "lowrank_A": 10,
+    "qjl_sketch": 11,
 }
 
 
@@ -120,6 +122,11 @@ def _l1_mask(w: Workload, seed: int, layer: int, b: int) -> np.ndarray:
 def _signs(w: Workload, seed: int, layer: int) -> np.ndarray:
     bits = _rng(w, seed, layer, "signs").integers(0, 2, size=w.d)
     return np.where(bits == 1, 1, -1).astype(np.int8)
+
+
+def qjl_matrix(w: Workload, layer: int = 0, seed: int = 0, m: int = 128) -> np.ndarray:
+    """The [m, d] float32 sketch matrix of a layer, i.i.d. N(0, 1)."""
+    return _rng(w, seed, layer, "qjl_sketch").standard_normal((m, w.d)).astype(np.float32)
 
 
 def layer_meta(w: Workload, layer: int = 0, seed: int = 0,
