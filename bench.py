@@ -65,6 +65,8 @@ def parse_args():
                    help="per-layer mode: replay each decode step (all layers) as one captured CUDA graph")
     p.add_argument("--codec", choices=["tq", "plain"], default="tq",
                    help="codec of the timed caches: TurboQuant (default) or Plain-KV (no rotation)")
+    p.add_argument("--qjl", action="store_true",
+                   help="TQ-QKV: key-residual sketches and their logit correction (route + attention)")
     p.add_argument("--route-per-head", action="store_true",
                    help="per-layer mode: every query head routes, fetches and attends with its own beta groups")
     p.add_argument("--route-max", action="store_true",
@@ -80,8 +82,9 @@ def dist_env():
 
 
 def input_rope(x, p, theta):
-    """Rotary embedding used only to build the planted-needle inputs
-    (rotate-half pairing, float64 angles)."""
+    """Rotary embedding (rotate-half pairing, float64 angles) for the inputs
+    around the timed path: planting the needle, and the exact attention the
+    codec diagnostics compare against."""
     x = np.asarray(x, dtype=np.float64)
     h = x.shape[-1] // 2
     ang = np.asarray(p, dtype=np.float64)[..., None] * theta ** (-2.0 * np.arange(h) / x.shape[-1])
@@ -345,7 +348,9 @@ def measure_codecs(H, torch, w, li):
     """Codec diagnostics (relMSE_K, relMSE_V and cosine of every token
     recovered from L3 by hsq_recover against the encoder's bf16 input) for
     TurboQuant and Plain-KV, on this layer and on heavy-tailed and low-rank
-    key regimes of the same head shape (one sequence of 4096 tokens each)."""
+    key regimes of the same head shape (one sequence of 4096 tokens each); on
+    the latter also the attention error of TQ-KV and TQ-QKV against exact
+    attention."""
     def one(wl, lay):
         K = torch.from_numpy(np.ascontiguousarray(lay.K, np.float32)).cuda().to(torch.bfloat16).contiguous()
         V = torch.from_numpy(np.ascontiguousarray(lay.V, np.float32)).cuda().to(torch.bfloat16).contiguous()
@@ -374,12 +379,56 @@ def measure_codecs(H, torch, w, li):
             cctx.close()
         return res
 
+    def attention(wl, lay, steps=4):
+        """Attention output of TQ-KV and TQ-QKV with every group fetched (beta = G,
+        so no summary enters) against exact softmax attention over the bf16 inputs:
+        the mean over heads and steps of the relative L2 error."""
+        K = torch.from_numpy(np.ascontiguousarray(lay.K, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        V = torch.from_numpy(np.ascontiguousarray(lay.V, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        G = -(-wl.T // wl.N)
+        q, pos = W.queries(wl, steps=steps)
+        Kr = input_rope(K.float().cpu().numpy(), np.arange(wl.T), wl.theta)      # [B, Hkv, T, d]
+        Vx = V.float().cpu().numpy().astype(np.float64)
+        r = wl.Hq // wl.Hkv
+        exact = []
+        for s in range(steps):
+            qr = input_rope(q[s], pos[s][:, None], wl.theta)                      # [B, Hq, d]
+            lg = np.einsum("bhrd,bhtd->bhrt", qr.reshape(wl.B, wl.Hkv, r, 128), Kr) / np.sqrt(128.0)
+            p = np.exp(lg - lg.max(axis=-1, keepdims=True))
+            exact.append(np.einsum("bhrt,bhtd->bhrd", p / p.sum(axis=-1, keepdims=True), Vx)
+                         .reshape(wl.B, wl.Hq, 128))
+        res = {}
+        for name, qj in (("tq", False), ("tq+qjl", True)):
+            cfg = H.make_config(wl.Hq, wl.Hkv, wl.N, G, wl.B, wl.T, max(wl.l1_size, 1), wl.T + steps + 1,
+                                wl.theta, qjl=qj)
+            cctx = H.Context(cfg)
+            cache = H.allocate_cache(cctx, wl.B, wl.T, l3_on_host=False, with_staging=False)
+            H.set_layer_inputs(cache, lay.l1_mask, lay.signs)
+            if qj:
+                H.set_qjl_matrix(cache, W.qjl_matrix(wl))
+            H.hsq_encode(cctx, cache, K, V)
+            sel = torch.empty((wl.B, wl.Hkv, G), dtype=torch.int32, device="cuda")
+            o = torch.empty((wl.B, wl.Hq, 128), device="cuda")
+            errs = []
+            for s in range(steps):
+                H.hsq_decode_step(cctx, cache, torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda(), sel, o)
+                got = o.cpu().numpy().astype(np.float64)
+                errs.append(np.linalg.norm(got - exact[s], axis=-1) / np.linalg.norm(exact[s], axis=-1))
+            assert H.hsq_sync_status(cctx) == 0
+            res[name] = float(np.mean(errs))
+            del cache
+            cctx.close()
+        return res
+
     out = {f"{w.name} ({w.key_law} keys)": one(w, li)}
     for law in ("student_t", "lowrank"):
         wl = w.with_(name=f"{w.name}_{law}", B=1, T=4096, key_law=law, needle=False, seed_tag=w.seed_tag + 40)
-        out[f"{law} keys, B1 T4096"] = one(wl, W.layer_inputs(wl))
+        lay = W.layer_inputs(wl)
+        out[f"{law} keys, B1 T4096"] = one(wl, lay)
+        out[f"{law} keys, B1 T4096"]["attention_rel_l2_vs_exact"] = attention(wl, lay)
     out["how"] = ("hsq_recover of every group after hsq_encode (4-bit L3), against the bf16 input; "
-                  "relMSE = sum |x^ - x|^2 / sum |x|^2, cosine = mean over tokens")
+                  "relMSE = sum |x^ - x|^2 / sum |x|^2, cosine = mean over tokens; attention: every group "
+                  "fetched, mean relative L2 error against exact softmax attention (4 query steps)")
     return out
 
 
@@ -399,12 +448,14 @@ def run_hsq(args, rank, world, local):
     w = W.get_workload(WORKLOAD)
     li, q, pos = workload_inputs(w, lambda x, p: input_rope(x, p, w.theta))
     cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                        args.n_splits, codec=args.codec)
+                        args.n_splits, codec=args.codec, qjl=args.qjl)
     ctx = H.Context(cfg)
     caches = {"host": H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False),
               "device": H.allocate_cache(ctx, w.B, w.T, l3_on_host=False, with_staging=False)}
     for c in caches.values():
         H.set_layer_inputs(c, li.l1_mask, li.signs)
+        if args.qjl:
+            H.set_qjl_matrix(c, W.qjl_matrix(w))
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
     V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
 
@@ -521,6 +572,8 @@ def run_hsq(args, rank, world, local):
     link_achieved = ab["link"] / (ms_per_step * 1e-3) / 1e9
     hbm_achieved = ab["hbm"] / (ms_per_step * 1e-3) / 1e9
     traffic, traffic_src = profiled_traffic()
+    if args.codec != "tq" or args.qjl:  # the capture is of the TurboQuant fused step
+        traffic, traffic_src = None, "no ncu capture of this variant"
     hbm_dev_achieved = (ab["hbm"] + ab["link"]) / (dev_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -531,7 +584,7 @@ def run_hsq(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"cold and clean at every step: {FLUSH_BYTES >> 20} MiB device write, then a "
                          f"{FLUSH_BYTES >> 20} MiB read, between timed steps (outside the step events)",
-                   "n_splits": args.n_splits or "auto", "codec": args.codec},
+                   "n_splits": args.n_splits or "auto", "codec": args.codec + ("+qjl" if args.qjl else "")},
         "roofline": {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": hbm_achieved / hbm_peak, "traffic": traffic,
                      "kernel": "decode_kernel (whole step: route, select, L3 gather, attention), L3 in pinned host memory",
@@ -562,7 +615,7 @@ def run_hsq(args, rank, world, local):
         "link_peak": lp,
         "growth": growth,
         "codec": codecs,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.qjl else 1),  # TQ-QKV: route + attention per step
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,
         "wall_s_timed_loop": wall,

@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
     __shared__ __align__(16) float s_rho[N][2][kDim];
+    __shared__ long long s_dst[N][2];
 
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1, l = hlane();
@@ -329,41 +330,42 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
     float* row = s_rho[warp][half];
     *reinterpret_cast<float4*>(row + 4 * l) = make_float4(rho[0], rho[1], rho[2], rho[3]);
     *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(rho[4], rho[5], rho[6], rho[7]);
-    __syncwarp();
-    // this lane's 8 sketch rows i = 4l + k and 64 + 4l + k: bit = (S_i . rho >= 0)
-    uint32_t lo = 0u, hi = 0u;
-#pragma unroll 1
-    for (int k = 0; k < 8; ++k) {
-        const int i = k < 4 ? 4 * l + k : 64 + 4 * l + (k - 4);
-        const float4* srow = reinterpret_cast<const float4*>(o.S + (size_t)i * kDim);
-        float acc = 0.f;
-#pragma unroll 8
-        for (int d4 = 0; d4 < kDim / 4; ++d4) {
-            const float4 sv = __ldg(srow + d4);
-            const float4 rv = *reinterpret_cast<const float4*>(row + 4 * d4);
-            acc = fmaf(sv.x, rv.x, acc);
-            acc = fmaf(sv.y, rv.y, acc);
-            acc = fmaf(sv.z, rv.z, acc);
-            acc = fmaf(sv.w, rv.w, acc);
-        }
-        const uint32_t bit = acc >= 0.f ? 1u : 0u;
-        if (k < 4) lo |= bit << k;
-        else hi |= bit << (k - 4);
+    if (l == 0) {
+        long long e = -1;  // destination sketch slot of this (token, half), -1: none
+        if (active) e = half == 0 ? (((long long)b * c.Hkv + h) * c.G * N + t)
+                                  : (((long long)b * c.Hkv + h) * c.max_l1 + slot);
+        s_dst[warp][half] = e;
+        if (active) (half == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
     }
-    // words: nibble of lane l at bits 4 (l & 7) of word l >> 3 (low coordinates) or 2 + (l >> 3)
-    uint32_t wlo = lo << (4 * (l & 7)), whi = hi << (4 * (l & 7));
+    __syncthreads();
+    // S rho for all 2N residuals of the CTA: thread (i, grp) forms row i of S against
+    // 8 residuals, reading its row of S once; a warp's 32 consecutive rows are one
+    // sketch word per residual (ballot)
+    const int i = threadIdx.x & (kDim - 1), grp = threadIdx.x >> 7;
+    const float4* srow = reinterpret_cast<const float4*>(o.S + (size_t)i * kDim);
+    float acc[8];
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-        wlo |= __shfl_xor_sync(m, wlo, off, 16);
-        whi |= __shfl_xor_sync(m, whi, off, 16);
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 4
+    for (int d4 = 0; d4 < kDim / 4; ++d4) {
+        const float4 sv = __ldg(srow + d4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = grp * 8 + j;
+            const float4 rv = *reinterpret_cast<const float4*>(&s_rho[r >> 1][r & 1][4 * d4]);
+            acc[j] = fmaf(sv.x, rv.x, acc[j]);
+            acc[j] = fmaf(sv.y, rv.y, acc[j]);
+            acc[j] = fmaf(sv.z, rv.z, acc[j]);
+            acc[j] = fmaf(sv.w, rv.w, acc[j]);
+        }
     }
-    if (active && (l & 7) == 0) {
-        const size_t e = half == 0 ? (((size_t)b * c.Hkv + h) * c.G * N + t)
-                                   : (((size_t)b * c.Hkv + h) * c.max_l1 + slot);
-        uint32_t* qs = (half == 0 ? o.l3_qs : o.l1_qs) + e * 4;
-        qs[l >> 3] = wlo;
-        qs[2 + (l >> 3)] = whi;
-        if (l == 0) (half == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
+    const int lane = threadIdx.x & 31, word = i >> 5;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = __ballot_sync(kFull, acc[j] >= 0.f);
+        const int r = grp * 8 + j;
+        const long long e = s_dst[r >> 1][r & 1];
+        if (lane == 0 && e >= 0) ((r & 1) == 0 ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
     }
 }
 
