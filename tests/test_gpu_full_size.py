@@ -11,8 +11,9 @@ sampled pair and step:
     GPU cache and selection (the acceptance of the small-size tests);
 and, for the planted-needle workload, the needle group is routed at step 0
 for every (sequence, KV head).  A further case forces the in-place variant of
-the decode kernel (inputs read from global memory, not staged); two more run
-the 8B/32K layer with the Plain-KV codec and with per-query-head routing."""
+the decode kernel (inputs read from global memory, not staged); three more run
+the 8B/32K layer with the Plain-KV codec, with per-query-head routing and with
+TQ-QKV."""
 
 import numpy as np
 import pytest
@@ -23,7 +24,8 @@ from hsq_harness import abi_buffers, ensure_built, gpu_encode, make_ctx, rel_l2,
 
 pytestmark = pytest.mark.gpu
 
-PER_HEAD = {"l1_kc", "l1_vc", "l1_kn", "l1_vn", "l2_kc", "l2_vc", "l2_kn", "l2_vn", "l3"}
+PER_HEAD = {"l1_kc", "l1_vc", "l1_kn", "l1_vn", "l2_kc", "l2_vc", "l2_kn", "l2_vn", "l3", "l1_qs", "l1_qn",
+            "l3_qs", "l3_qn"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,19 +37,23 @@ def _rope(w):
     return lambda x, p: O.rope(x, p, w.theta)
 
 
-def _sub_view(bufs, li, w, b, h, codec="tq"):
+def _sub_view(bufs, li, w, b, h, codec="tq", qjl_S=None):
     sub = {}
     for k, v in bufs.items():
         v = v[b:b + 1]
         sub[k] = v[:, h:h + 1] if k in PER_HEAD else v
-    return O.cache_from_abi(sub, li.l1_mask[b:b + 1], li.signs, w.N, w.T, w.theta, codec=codec)
+    return O.cache_from_abi(sub, li.l1_mask[b:b + 1], li.signs, w.N, w.T, w.theta, codec=codec, qjl_S=qjl_S)
 
 
-def _run_and_check(w, li, ctx, cache, steps, samples, needle=False, codec="tq", per_head=False):
+def _run_and_check(w, li, ctx, cache, steps, samples, needle=False, codec="tq", per_head=False, qjl_S=None):
     import torch
     import hierarchical_kv_cache_hsq_gb300 as H
     bufs = abi_buffers(cache)
-    views = {bh: _sub_view(bufs, li, w, *bh, codec=codec) for bh in samples}
+    if qjl_S is not None:
+        for n in ("l1_qs", "l1_qn", "l3_qs", "l3_qn"):
+            bufs[n] = cache.view(n).cpu().numpy()
+        bufs["l1_qs"], bufs["l3_qs"] = bufs["l1_qs"].view(np.uint32), bufs["l3_qs"].view(np.uint32)
+    views = {bh: _sub_view(bufs, li, w, *bh, codec=codec, qjl_S=qjl_S) for bh in samples}
     q, pos = W.queries(w, steps=steps)
     r = w.r
     rows = w.Hq if per_head else w.Hkv   # selection rows per sequence
@@ -92,20 +98,32 @@ def test_qwen3_8b_32k_full_size():
     print(f"[qwen3_8b_32k] worst sampled rel L2 {worst:.2e}")
 
 
-@pytest.mark.parametrize("variant", ["plain_codec", "per_head_routing"])
+@pytest.mark.parametrize("variant", ["plain_codec", "per_head_routing", "tq_qkv"])
 def test_qwen3_8b_32k_variants_full_size(variant):
-    """The Plain-KV codec and per-query-head routing at the full 8B/32K size."""
+    """The Plain-KV codec, per-query-head routing and TQ-QKV at the full 8B/32K size."""
+    import torch
     import hierarchical_kv_cache_hsq_gb300 as H
     w = W.get_workload("qwen3_8b_32k")
     li = W.layer_inputs(w, rope=_rope(w))
     codec = "plain" if variant == "plain_codec" else "tq"
     per_head = variant == "per_head_routing"
+    qjl = variant == "tq_qkv"
     cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
-                        codec=codec, route_per_head=per_head)
+                        codec=codec, route_per_head=per_head, qjl=qjl)
     ctx = H.Context(cfg)
-    cache = gpu_encode(ctx, w, li)
+    S = W.qjl_matrix(w) if qjl else None
+    if qjl:
+        cache = H.allocate_cache(ctx, w.B, w.T)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        H.set_qjl_matrix(cache, S)
+        K = torch.from_numpy(np.ascontiguousarray(li.K, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        V = torch.from_numpy(np.ascontiguousarray(li.V, np.float32)).cuda().to(torch.bfloat16).contiguous()
+        H.hsq_encode(ctx, cache, K, V)
+        del K, V
+    else:
+        cache = gpu_encode(ctx, w, li)
     worst = _run_and_check(w, li, ctx, cache, steps=2, samples=[(0, 0), (0, 5)], needle=True, codec=codec,
-                           per_head=per_head)
+                           per_head=per_head, qjl_S=S)
     print(f"[qwen3_8b_32k {variant}] worst sampled rel L2 {worst:.2e}")
 
 
