@@ -66,7 +66,7 @@ def parse_args():
     p.add_argument("--codec", choices=["tq", "plain"], default="tq",
                    help="codec of the timed caches: TurboQuant (default) or Plain-KV (no rotation)")
     p.add_argument("--qjl", action="store_true",
-                   help="TQ-QKV: key-residual sketches and their logit correction (route + attention)")
+                   help="TQ-QKV: key-residual sketches and their logit correction")
     p.add_argument("--route-per-head", action="store_true",
                    help="per-layer mode: every query head routes, fetches and attends with its own beta groups")
     p.add_argument("--route-max", action="store_true",
@@ -615,7 +615,7 @@ def run_hsq(args, rank, world, local):
         "link_peak": lp,
         "growth": growth,
         "codec": codecs,
-        "gpu_launches": args.steps * (2 if args.qjl else 1),  # TQ-QKV: route + attention per step
+        "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,
         "wall_s_timed_loop": wall,

@@ -214,8 +214,8 @@ template <int R>
 __device__ __forceinline__ void pair_logits_qjl(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
                                                 const float (&sq)[R][8], const float (&ca)[8], const float (&cb)[8],
                                                 float scale, float* xs, float (&xa)[R], float (&xb)[R]) {
-    int idx, idx2;
-    const float d = pair_dots<R>(q, ka, kb, idx) + pair_dots<R>(sq, ca, cb, idx2);
+    int idx;
+    const float d = pair_dots2<R>(q, ka, kb, sq, ca, cb, idx);
     __syncwarp();  // the previous pair's reads are done
     if (idx < 2 * R) xs[idx] = d * scale;
     __syncwarp();
@@ -535,6 +535,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     };
     const int nbatch = (nfetch + kBatchRecs - 1) / kBatchRecs;
     issue(0);
+
     __syncthreads();  // s_mask complete
 
     Softmax<R> sm;
@@ -791,9 +792,7 @@ cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaSt
 // The kernel variant of the context's codec.
 template <int R, int N, bool kRoute, bool kStaged>
 DecodeFn decode_fn(bool rot, bool qjl) {
-    if constexpr (!kRoute) {  // TQ-QKV (TurboQuant only) runs as route + attention
-        if (qjl) return decode_kernel<R, N, false, kStaged, true, true>;
-    }
+    if (qjl) return decode_kernel<R, N, kRoute, kStaged, true, true>;  // TQ-QKV: TurboQuant only
     return rot ? decode_kernel<R, N, kRoute, kStaged, true> : decode_kernel<R, N, kRoute, kStaged, false>;
 }
 

@@ -765,6 +765,36 @@ __device__ __forceinline__ float pair_dots(const float (&q)[R][8], const float (
     return spread_sum<K>(p);
 }
 
+// pair_dots of (q, ka, kb) plus (q2, ka2, kb2) in one reduction: the lane
+// products of both are summed before the spread.
+template <int R>
+__device__ __forceinline__ float pair_dots2(const float (&q)[R][8], const float (&ka)[8], const float (&kb)[8],
+                                            const float (&q2)[R][8], const float (&ka2)[8], const float (&kb2)[8],
+                                            int& idx) {
+    constexpr int K = pow2_ceil(2 * R);
+    float p[K];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        float da = 0.f, db = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            da = fmaf(q[j][k], ka[k], da);
+            db = fmaf(q[j][k], kb[k], db);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            da = fmaf(q2[j][k], ka2[k], da);
+            db = fmaf(q2[j][k], kb2[k], db);
+        }
+        p[j] = da;
+        p[R + j] = db;
+    }
+#pragma unroll
+    for (int j = 2 * R; j < K; ++j) p[j] = 0.f;
+    idx = spread_index<K>(hlane());
+    return spread_sum<K>(p);
+}
+
 // Routing scores of two groups a and b: (sum_j q~_j) . c3[codes], every lane
 // gets both.  One fixed summation order, shared by the routing kernel and
 // the decode step, so both select the same groups.

@@ -1060,7 +1060,7 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
     if (hsq::fault_mask() & HSQ_FAULT_FETCH) return fail(ctx, HSQ_ERR_CUDA, "injected fetch failure");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     bool fused = false;
-    if (!ctx->cfg.route_max && !ctx->cfg.qjl) {  // (the fused kernel: sum routing, TQ-KV logits)
+    if (!ctx->cfg.route_max) {  // (the fused kernel routes by the sum over the query heads)
         st = decode_run(ctx, cache, q, pos, sel, out, true, false, s, &fused);
         if (st != HSQ_OK || fused) return st;
     }

@@ -145,8 +145,7 @@ typedef struct hsq_config {
        logit then adds sqrt(pi/2) / 128 * |rho| * sum_i (S Pi q^r)_i sign_i
        before the 1/sqrt(128) scale (an unbiased estimate of q^r . residual).
        Needs codec HSQ_CODEC_TQ.  hsq_encode writes the sketches (the key
-       input is read a second time); hsq_decode_step runs hsq_route +
-       hsq_decode_attn under it; hsq_append refuses it (HSQ_ERR_UNSUPPORTED).
+       input is read a second time); hsq_append refuses it (HSQ_ERR_UNSUPPORTED).
        0: TQ-KV. */
     int qjl;
 } hsq_config;

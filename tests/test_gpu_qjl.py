@@ -6,9 +6,9 @@ Against the oracle on the same seeded inputs and sketch matrix:
     S_i . rho lies within 1e-4 |S_i| |rho| of zero (counted), residual norms
     within 1e-4 relative -- taken against the residuals of the GPU's own
     codes (oracle.key_residuals), so a quantiser near-tie cannot cascade;
-  * the decode step's attention within 1e-3 relative L2 of the oracle's on
-    the GPU's cache, sketches and selection, and measurably different from
-    the TQ-KV output of the same cache;
+  * the fused decode step equal to route + attention, and its attention
+    within 1e-3 relative L2 of the oracle's on the GPU's cache, sketches and
+    selection, and measurably different from the TQ-KV output of the same cache;
   * hsq_append refuses the mode.
 """
 
@@ -127,6 +127,10 @@ def test_qjl_decode_parity(name):
         H.hsq_route(L.ctx, L.cache, qd, pd, sel_r)
         assert H.hsq_sync_status(L.ctx) == 0
         assert torch.equal(sel, sel_r)  # the sketch does not touch routing
+        out_a = torch.empty_like(out)  # the fused step attends like the attention call
+        H.hsq_decode_attn(L.ctx, L.cache, qd, pd, sel_r, out_a)
+        assert H.hsq_sync_status(L.ctx) == 0
+        assert np.all(rel_l2(out.cpu().numpy(), out_a.cpu().numpy()) <= 1e-5)
         gsel = sel.cpu().numpy().astype(np.int64)
         o = out.cpu().numpy()
         ref = O.decode_attn(L.gview, q[s], pos[s], gsel)
