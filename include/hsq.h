@@ -259,7 +259,10 @@ hsq_status hsq_destroy(hsq_ctx* ctx);
  *   cfg.l1_recent > 0 and win_kv / gsum set, it also stores the growth state
  *   that hsq_append continues from (the recent window's inputs and the
  *   running sums of the group at the window's trailing edge).  Groups and
- *   records past T (up to t_cap) are written empty.
+ *   records past T (up to t_cap) are written empty.  With cfg.qjl it also
+ *   writes the key-residual sketches (l1_qs / l1_qn, l3_qs / l3_qn) from
+ *   cache->qjl_s, reading K a second time.  Under HSQ_CODEC_PLAIN every "Pi"
+ *   here is the identity and signs is not read.
  *   Errors: HSQ_ERR_INVALID (null pointer, B/T out of range, L3 location not
  *   matching l3_on_host), HSQ_ERR_CUDA.  An L1 set larger than max_l1 sets
  *   HSQ_DEVERR_L1_OVER.
@@ -284,7 +287,8 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
  *   cache->win_kv and cache->gsum (filled by hsq_encode under this cfg),
  *   T < t_cap and T < max_pos.  L1 slots are then no longer in position
  *   order (l1_pos holds each slot's position).  Errors: HSQ_ERR_INVALID,
- *   HSQ_ERR_CUDA; device checks HSQ_DEVERR_GROW, HSQ_DEVERR_L1_OVER.
+ *   HSQ_ERR_UNSUPPORTED (cfg.qjl), HSQ_ERR_CUDA; device checks
+ *   HSQ_DEVERR_GROW, HSQ_DEVERR_L1_OVER.
  */
 hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void* v, hsq_dtype dtype,
                       hsq_stream_t stream);
@@ -353,6 +357,10 @@ hsq_status hsq_recover(hsq_ctx* ctx, const hsq_cache* cache, int g0, int ng, flo
  *     tokens t of the groups in sel that are not in L1 (key RoPE(k_t, t)
  *     recovered from L3, value v_t),
  *   split over the entries (flash-decoding) and merged by log-sum-exp.
+ *   With cfg.qjl the L1 and fetched-token logits carry the sketch term
+ *   (hsq_config.qjl); with cfg.route_per_head query head j attends with its
+ *   own row sel[b][j] (L1, the summaries of groups not in it, the tokens of
+ *   the groups in it).
  *   out: [B][Hq][128] f32 in the original frame, device memory or mapped
  *   page-locked host memory (written in place).  q, pos, sel as in
  *   hsq_route.  By default the kernel gathers the selected L3 records itself
@@ -372,9 +380,10 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  *   selection) and out as hsq_decode_attn computes it.  One kernel: the S
  *   splits of a (b, h) form one thread-block cluster and select the top
  *   beta together through distributed shared memory, so no CTA waits on a
- *   CTA outside its cluster and the grid need not be co-resident.  Only if
- *   no cluster shape can be launched does it run hsq_route then
- *   hsq_decode_attn.  q, pos, sel, out: as for those calls (device memory,
+ *   CTA outside its cluster and the grid need not be co-resident.  It runs
+ *   hsq_route then hsq_decode_attn under cfg.route_max, and when no
+ *   cluster shape can be launched.  Per-query-head routing and TQ-QKV stay
+ *   one launch.  q, pos, sel, out: as for those calls (device memory,
  *   or mapped page-locked host memory for a step with no separate copies).
  *   Errors as the two calls.
  */
