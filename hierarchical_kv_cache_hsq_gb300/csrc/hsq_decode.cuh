@@ -369,21 +369,37 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
     if constexpr (kQJL) {
-        // the sketched rotated queries S q~_j (read after the barriers that precede the L1 pass)
-#pragma unroll 1
-        for (int o = tid; o < R * kDim; o += NT) {
-            const int j = o / kDim, i = o % kDim;
-            const float4* srow = reinterpret_cast<const float4*>(c.qjl_s + (size_t)i * kDim);
-            float acc = 0.f;
-#pragma unroll 4
-            for (int d4 = 0; d4 < kDim / 4; ++d4) {
-                const float4 sv = __ldg(srow + d4);
-                acc = fmaf(sv.x, s_qt[j][4 * d4], acc);
-                acc = fmaf(sv.y, s_qt[j][4 * d4 + 1], acc);
-                acc = fmaf(sv.z, s_qt[j][4 * d4 + 2], acc);
-                acc = fmaf(sv.w, s_qt[j][4 * d4 + 3], acc);
+        // the sketched rotated queries S q~_j (read after the barriers that precede the
+        // L1 pass): thread t takes half of row t mod 128 of S for every head, its 16
+        // loads issued together; the two halves meet in shared memory
+        static_assert(NT == 2 * kDim, "one row half per thread");
+        const int i = tid & (kDim - 1), part = tid >> 7;
+        const float4* srow = reinterpret_cast<const float4*>(c.qjl_s + (size_t)i * kDim) + part * (kDim / 8);
+        float4 sv[kDim / 8];
+#pragma unroll
+        for (int k = 0; k < kDim / 8; ++k) sv[k] = __ldg(srow + k);
+        float acc[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const float* qj = s_qt[j] + part * (kDim / 2);
+            float a = 0.f;
+#pragma unroll
+            for (int k = 0; k < kDim / 8; ++k) {
+                a = fmaf(sv[k].x, qj[4 * k], a);
+                a = fmaf(sv[k].y, qj[4 * k + 1], a);
+                a = fmaf(sv[k].z, qj[4 * k + 2], a);
+                a = fmaf(sv[k].w, qj[4 * k + 3], a);
             }
-            s_sq[j][i] = acc;
+            acc[j] = a;
+        }
+        if (part == 1) {
+#pragma unroll
+            for (int j = 0; j < R; ++j) s_sq[j][i] = acc[j];
+        }
+        __syncthreads();
+        if (part == 0) {
+#pragma unroll
+            for (int j = 0; j < R; ++j) s_sq[j][i] += acc[j];
         }
     }
 
@@ -551,6 +567,20 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
             }
         }
     }
+    // TQ-QKV: the sketch words of a pair of L1 entries, loaded one step ahead
+    uint4 nwa = make_uint4(0, 0, 0, 0), nwb = nwa;
+    float nga = 0.f, ngb = 0.f;
+    auto l1_sketch = [&](int blk_) {
+        const size_t ia = bb * c.max_l1 + e0 + min(blk_ + hw, n1 - 1);
+        const size_t ib = bb * c.max_l1 + e0 + min(blk_ + hw + NH, n1 - 1);
+        nwa = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ia);
+        nwb = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ib);
+        nga = __ldg(c.l1_qn + ia);
+        ngb = __ldg(c.l1_qn + ib);
+    };
+    if constexpr (kQJL) {
+        if (n1 > 0) l1_sketch(0);
+    }
 #pragma unroll 1
     for (int blk = 0; blk < n1; blk += 2 * NH) {
         const int ea = blk + hw, eb = ea + NH;
@@ -563,10 +593,12 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
         unpack4(kra[l], kra[16 + l], c4, p_l1kn[ja], ka);
         unpack4(krb[l], krb[16 + l], c4, p_l1kn[jb], kb);
         if constexpr (kQJL) {
-            const size_t ia = bb * c.max_l1 + e0 + ja, ib = bb * c.max_l1 + e0 + jb;
+            const uint4 wa = nwa, wb = nwb;
+            const float ga = nga, gb = ngb;
+            if (blk + 2 * NH < n1) l1_sketch(blk + 2 * NH);
             float ca[8], cb[8];
-            sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ia), kQjlScale * __ldg(c.l1_qn + ia), ca);
-            sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ib), kQjlScale * __ldg(c.l1_qn + ib), cb);
+            sketch_signs(wa, kQjlScale * ga, ca);
+            sketch_signs(wb, kQjlScale * gb, cb);
             pair_logits_qjl<R>(qt, ka, kb, sq, ca, cb, kLogitScaleLog2, xs, xa, xb);
         } else {
             pair_logits<R>(qt, ka, kb, kLogitScaleLog2, xs, xa, xb);
@@ -628,18 +660,22 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
             const uint8_t* buf = s_rec + (kb_ & 1) * kFetchBatchBytes;
             const float* sbase = s_base + (kb_ & 1) * kBatchRecs * kDim;
             const uint32_t* rbits = s_rbits + (kb_ & 1) * kBatchRecs;
-            // one recovered token: validity, RoPE'd key, rotated-frame value and
-            // (TQ-QKV) the signed residual sketch
-            auto token = [&](int u, float kv[8], float vv[8], float cv[8]) -> bool {
+            // TQ-QKV: token u's sketch words and weight (0 for a slot that is no token)
+            auto tok_sketch = [&](int u, uint4& wd, float& wt) {
+                const int rec = u / N, n = u - rec * N;
+                const int g = s_sel[r0 + rec];
+                const int t = g * N + n;
+                const bool ok = (g >= 0) & (t < c.T);
+                const size_t ti = bb * (size_t)c.G * N + (size_t)(ok ? t : 0);
+                wd = __ldg(reinterpret_cast<const uint4*>(c.l3_qs) + ti);
+                wt = ok ? kQjlScale * __ldg(c.l3_qn + ti) : 0.f;
+            };
+            // one recovered token: validity, RoPE'd key and rotated-frame value
+            auto token = [&](int u, float kv[8], float vv[8]) -> bool {
                 const int rec = u / N, n = u - rec * N;
                 const int g = s_sel[r0 + rec];
                 const int t = g * N + n;
                 const bool ok = (g >= 0) & (t < c.T) & (((rbits[rec] >> n) & 1u) == 0u);
-                if constexpr (kQJL) {
-                    const size_t ti = bb * (size_t)c.G * N + (size_t)(ok ? t : 0);
-                    sketch_signs(__ldg(reinterpret_cast<const uint4*>(c.l3_qs) + ti),
-                                 ok ? kQjlScale * __ldg(c.l3_qn + ti) : 0.f, cv);
-                }
                 const uint8_t* rp = buf + rec * RB;
                 const float* norms = reinterpret_cast<const float*>(rp + N * 128);
                 const uint16_t* kr = reinterpret_cast<const uint16_t*>(rp + n * 64);
@@ -666,14 +702,32 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                 return ok;
             };
             const int nt = nb * N;
+            uint4 twa = make_uint4(0, 0, 0, 0), twb = twa;  // next pair's sketches (TQ-QKV)
+            float tga = 0.f, tgb = 0.f;
+            if constexpr (kQJL) {
+                tok_sketch(min(hw, nt - 1), twa, tga);
+                tok_sketch(min(hw + NH, nt - 1), twb, tgb);
+            }
 #pragma unroll 1
             for (int blk = 0; blk < nt; blk += 2 * NH) {
                 const int ua = blk + hw, ub = ua + NH;
-                float ka[8], kb[8], va[8], vb[8], xa[R], xb[R], ca[8], cb[8];
-                const bool oka = token(min(ua, nt - 1), ka, va, ca) && ua < nt;
-                const bool okb = token(min(ub, nt - 1), kb, vb, cb) && ub < nt;
-                if constexpr (kQJL) pair_logits_qjl<R>(qr, ka, kb, sq, ca, cb, kLogitScaleLog2, xs, xa, xb);
-                else pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
+                float ka[8], kb[8], va[8], vb[8], xa[R], xb[R];
+                const bool oka = token(min(ua, nt - 1), ka, va) && ua < nt;
+                const bool okb = token(min(ub, nt - 1), kb, vb) && ub < nt;
+                if constexpr (kQJL) {
+                    const uint4 wa = twa, wb = twb;
+                    const float ga = tga, gb = tgb;
+                    if (blk + 2 * NH < nt) {
+                        tok_sketch(min(ua + 2 * NH, nt - 1), twa, tga);
+                        tok_sketch(min(ub + 2 * NH, nt - 1), twb, tgb);
+                    }
+                    float ca[8], cb[8];
+                    sketch_signs(wa, ga, ca);
+                    sketch_signs(wb, gb, cb);
+                    pair_logits_qjl<R>(qr, ka, kb, sq, ca, cb, kLogitScaleLog2, xs, xa, xb);
+                } else {
+                    pair_logits<R>(qr, ka, kb, kLogitScaleLog2, xs, xa, xb);
+                }
                 sm.add2(xa, va, oka, xb, vb, okb);
             }
             __syncthreads();  // batch kb_ consumed: its buffer may be refilled
