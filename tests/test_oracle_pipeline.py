@@ -318,3 +318,24 @@ def test_per_head_selection_is_the_brute_force_top_beta_of_its_dots():
             np.testing.assert_allclose(scores[b, j][ne], dots[ne], rtol=1e-12, atol=1e-12)
             assert np.all(np.isneginf(scores[b, j][~ne]))
             np.testing.assert_array_equal(sel[b, j], _brute_select(scores[b, j].astype(np.float32), ne, w.beta))
+
+
+def test_per_head_routing_with_residual_sketches_is_single_head_attention():
+    """TQ-QKV under per-query-head routing: each query head's output equals the
+    shared-routing output of a one-head-per-KV-head context made of that head,
+    sketch terms included (the sketches follow the KV head, not the row)."""
+    w = _small(Hq=8, Hkv=2)
+    li = W.layer_inputs(w)
+    S = np.random.default_rng(3).standard_normal((128, 128))
+    cache = O.encode(li.K, li.V, li.l1_mask, li.signs, w.N, w.theta, qjl_S=S)
+    plain = O.encode(li.K, li.V, li.l1_mask, li.signs, w.N, w.theta)
+    q, pos = W.queries(w, steps=1)
+    r = w.Hq // w.Hkv
+    sel, _ = O.route(cache, q[0], pos[0], w.beta, agg="head")
+    out = O.decode_attn(cache, q[0], pos[0], sel)
+    for j in range(r):
+        heads = [h * r + j for h in range(w.Hkv)]
+        o1 = O.decode_attn(cache, q[0][:, heads], pos[0], sel[:, heads])
+        np.testing.assert_allclose(out[:, heads], o1, rtol=1e-13, atol=1e-15)
+    # and the sketch terms are in: the same selection without them gives another output
+    assert np.max(np.abs(out - O.decode_attn(plain, q[0], pos[0], sel))) > 1e-3
