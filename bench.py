@@ -98,6 +98,12 @@ def workload_inputs(w, rope):
     return li, q, pos
 
 
+def workload_desc(w, l1_count: int, nonempty: int) -> str:
+    """The workload as both arms print it (config.workload)."""
+    return (f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta} "
+            f"L1={l1_count} non-empty groups={nonempty}")
+
+
 def algorithmic_bytes(w, l1_count: int, nonempty: int):
     """Bytes the method must move once per layer-step (HBM and host link)."""
     l1 = w.B * w.Hkv * l1_count * 2 * 68
@@ -222,14 +228,66 @@ def link_peak(torch, nbytes=1 << 30, reps=5):
     return out
 
 
-def cpu_oracle_sample(w, li, q, pos, seconds: float):
+def _tie_counts(gview, ora, tiers, O):
+    """Per tier: coordinates whose code differs inside / outside the near-tie
+    band, coordinates inside the band, coordinates compared."""
+    out = {}
+    for tier, bits in tiers:
+        go, oo = getattr(gview, tier), getattr(ora, tier)
+        n = None
+        if tier.startswith("l1"):
+            n = int(ora.l1_count.max())
+        gc, oc, y, nm = go.codes, oo.codes, oo.y, oo.norms
+        if n is not None:
+            gc, oc, y, nm = gc[:, :, :n], oc[:, :, :n], y[:, :, :n], nm[:, :, :n]
+        diff = gc != oc
+        tie = O.near_boundary(y, bits) & (np.asarray(nm) > 0)[..., None]
+        out[tier] = {"differ_in_band": int(np.sum(diff & tie)), "differ_outside_band": int(np.sum(diff & ~tie)),
+                     "in_band": int(np.sum(tie)), "coordinates": int(diff.size)}
+    return out
+
+
+def _sel_tie_counts(gsel, osel, oscores, beta):
+    """Selected groups that differ, and how many of them (and of all groups)
+    lie within 1e-5 max(|s_beta|, rms(s)) of the beta-th oracle score."""
+    fin = np.isfinite(oscores)
+    s = oscores[fin].astype(np.float64)
+    band = np.zeros(len(oscores), bool)
+    if len(s) > beta:
+        sb = np.sort(s)[::-1][beta - 1]
+        tol = 1e-5 * max(abs(sb), float(np.sqrt(np.mean(s * s))))
+        band[fin] = np.abs(oscores[fin] - sb) <= tol
+    a = set(int(g) for g in gsel if g >= 0)
+    b = set(int(g) for g in osel if g >= 0)
+    d = sorted(a ^ b)
+    return {"differ": len(d), "differ_in_band": int(sum(band[g] for g in d)),
+            "differ_outside_band": int(sum(not band[g] for g in d)), "in_band": int(band.sum()),
+            "groups": int(fin.sum())}
+
+
+def cpu_oracle_sample(w, li, q, pos, seconds: float, gpu_head0=None, gpu_sel0=None):
     """The float64 oracle timed on the host cores: one KV head per decode step,
-    run for about `seconds`, scaled to the full B * Hkv step."""
+    run for about `seconds`, scaled to the full B * Hkv step.  Given the GPU
+    cache's buffers of KV head 0 and the GPU's step-0 selection, the oracle's
+    encode and routing of that head also give the near-tie counts of the
+    GPU's codes and selection (returned second)."""
     import oracle as O
     r = w.r
     t0 = time.perf_counter()
     cache = O.encode(li.K[:, :1], li.V[:, :1], li.l1_mask, li.signs, w.N, w.theta)
     enc_s = time.perf_counter() - t0
+    ties = None
+    if gpu_head0 is not None:
+        gview = O.cache_from_abi(gpu_head0, li.l1_mask, li.signs, w.N, w.T, w.theta)
+        tiers = (("l3_k", 4), ("l3_v", 4), ("l1_k", 4), ("l1_v", 4), ("l2_k", 3), ("l2_v", 3))
+        ties = {"codes": _tie_counts(gview, cache, tiers, O)}
+        if gpu_sel0 is not None:
+            osel, oscores = O.route(gview, q[0][:, :r], pos[0], w.beta)
+            ties["selection_step0"] = _sel_tie_counts(gpu_sel0, osel[0, 0], oscores[0, 0], w.beta)
+        ties["sample"] = (f"sequence 0, KV head 0 of {w.name}: GPU codes against the oracle's encode of that "
+                          f"head, GPU step-0 selection against the oracle's routing on the GPU's cache; band = "
+                          f"1e-5 max(|tau_k|, 1/sqrt(d)) of a boundary, 1e-5 max(|s_beta|, rms(s)) of the "
+                          f"beta-th score")
     n, spent = 0, 0.0
     while spent < seconds and n < w.steps:
         s = n % w.steps
@@ -240,9 +298,19 @@ def cpu_oracle_sample(w, li, q, pos, seconds: float):
         n += 1
     per_head = spent / n
     full = per_head * w.B * w.Hkv
-    return {"value": 1.0 / full, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"KV head 0 of {w.name}: encode of that head ({enc_s:.2f} s, not in the value) then "
-                      f"{n} decode steps of that head ({spent:.1f} s); step time x {w.B * w.Hkv} heads"}
+    return ({"value": 1.0 / full, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+             "blas_threads": blas_threads(),
+             "sample": f"KV head 0 of {w.name}: encode of that head ({enc_s:.2f} s, not in the value) then "
+                       f"{n} decode steps of that head ({spent:.1f} s); step time x {w.B * w.Hkv} heads"},
+            ties)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((int(i.get("num_threads", 0)) for i in threadpool_info()), default=None)
+    except Exception:
+        return None
 
 
 def aggregate(total_ms: float, steps: int, world: int, device=None):
@@ -263,7 +331,9 @@ def run_reference(args, rank, world):
     import oracle as O
     w = W.get_workload(WORKLOAD)
     li, q, pos = workload_inputs(w, lambda x, p: O.rope(x, p, w.theta))
-    caches = {}
+    caches = {0: O.encode(li.K[:, :1], li.V[:, :1], li.l1_mask, li.signs, w.N, w.theta)}
+    l1_count = int(caches[0].l1_count[0])
+    nonempty = int((caches[0].l2_cnt > 0).sum())
 
     def step(s):
         h = s % w.Hkv
@@ -287,9 +357,9 @@ def run_reference(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta}",
-                   "parallelism": "host cores"},
+        "config": {"workload": workload_desc(w, l1_count, nonempty), "parallelism": "host cores"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "blas_threads": blas_threads(),
                          "sample": f"each step = one KV head of the {w.B * w.Hkv}-head decode step "
                                    f"(round robin), scaled by {w.B * w.Hkv}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -432,6 +502,70 @@ def measure_codecs(H, torch, w, li):
     return out
 
 
+SMALL_WORKLOADS = ("tiny_1k", "qwen3_0p6b_4k")
+
+
+def measure_small_workloads(H, torch, lp, flush, clean, sink, steps, warmup, cpu_seconds):
+    """The two small single-layer workloads (tiny 1K, Qwen3-0.6B-shaped 4K):
+    the fused decode step with L3 in pinned host memory, timed per step
+    between CUDA events with the same cold-L2 rule as the headline, its
+    step roofline, and the float64 oracle timed beside it."""
+    hbm_peak, _ = measured_peaks()
+    out = {}
+    for name in SMALL_WORKLOADS:
+        w = W.get_workload(name)
+        li = W.layer_inputs(w)
+        q, pos = W.queries(w, steps=w.steps)
+        cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta)
+        ctx = H.Context(cfg)
+        cache = H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        dt = torch.bfloat16 if w.storage == "bf16" else torch.float32
+        K = torch.from_numpy(np.ascontiguousarray(li.K, np.float32)).cuda().to(dt).contiguous()
+        V = torch.from_numpy(np.ascontiguousarray(li.V, np.float32)).cuda().to(dt).contiguous()
+        H.hsq_encode(ctx, cache, K, V)
+        del K, V
+        l1_count = int(cache.view("l1_count").cpu()[0])
+        nonempty = int((cache.view("l2_cnt").cpu() > 0).sum())
+        ab = algorithmic_bytes(w, l1_count, nonempty)
+        qd, pd = torch.from_numpy(q).cuda(), torch.from_numpy(pos).cuda()
+        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        o = torch.empty((w.B, w.Hq, 128), device="cuda")
+
+        def run(n, timed):
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            torch.cuda._sleep(20_000_000)
+            for i in range(n):
+                s = i % w.steps
+                flush.fill_(i & 255)
+                torch.sum(clean, dim=0, out=sink)
+                ev[i][0].record()
+                H.hsq_decode_step(ctx, cache, qd[s], pd[s], sel, o)
+                ev[i][1].record()
+            torch.cuda.synchronize()
+            return [e[0].elapsed_time(e[1]) for e in ev] if timed else None
+
+        run(warmup, False)
+        ts = run(steps, True)
+        assert H.hsq_sync_status(ctx) == 0
+        ms = sum(ts) / len(ts)
+        t_star = max(ab["hbm"] / (hbm_peak * 1e9), ab["link"] / (lp["h2d_gbs"] * 1e9))
+        cpu = cpu_oracle_sample(w, li, q, pos, cpu_seconds)[0] if cpu_seconds > 0 else None
+        out[name] = {"workload": workload_desc(w, l1_count, nonempty), "steps": steps,
+                     "value": 1e3 / ms, "unit": UNIT, "ms_per_step": ms,
+                     "step_roofline": {"t_star_us": t_star * 1e6, "frac": t_star / (ms * 1e-3),
+                                       "bound": "host link" if ab["link"] / lp["h2d_gbs"] > ab["hbm"] / hbm_peak
+                                       else "hbm",
+                                       "hbm_bytes": ab["hbm"], "link_bytes": ab["link"]},
+                     "cpu_baseline": cpu}
+        del cache
+        ctx.close()
+    out["how"] = ("hsq_decode_step, L3 in pinned host memory, L2 flushed before every step (outside the step "
+                  "events); step roofline t* = max(HBM bytes / measured HBM peak, L3 bytes / pinned copy peak "
+                  "measured in this run); not a target for these latency-sized shapes")
+    return out
+
+
 def run_hsq(args, rank, world, local):
     import ctypes
 
@@ -505,6 +639,12 @@ def run_hsq(args, rank, world, local):
     torch.cuda.synchronize()
     s0 = sel.cpu().numpy()
     needle_ok = all(int(li.needle_group[0, h]) in s0[0, h] for h in range(w.Hkv))
+    # sequence 0 / KV head 0 of the pinned-L3 cache, for the near-tie counts
+    head0 = {}
+    for name in ("l1_kc", "l1_vc", "l1_kn", "l1_vn", "l2_kc", "l2_vc", "l2_kn", "l2_vn", "l3"):
+        head0[name] = caches["host"].view(name)[0:1, 0:1].cpu().numpy()
+    for name in ("l1_pos", "l1_count", "l2_cnt"):
+        head0[name] = caches["host"].view(name)[0:1].cpu().numpy()
 
     def loop(cache_key, nsteps, e2e=False, timed=True):
         stc = structs[cache_key]
@@ -531,6 +671,29 @@ def run_hsq(args, rank, world, local):
             return None
         return {"step_ms": [e[0].elapsed_time(e[1]) for e in ev]}
 
+    def e2e_wall(nsteps, timed=True):
+        """Host wall clock per step through the public call with page-locked
+        host buffers: launch hsq_decode_step (the kernel reads q and pos from
+        host memory and writes out there), wait for the stream, read the
+        output on the host.  The L2 flush and a synchronize precede each
+        step's clock."""
+        stc = structs["host"]
+        o_np = out_host.numpy()
+        ts, acc = [], 0.0
+        for i in range(nsteps):
+            s = i % w.steps
+            cold_l2(i)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            st = lib.hsq_decode_step(ctx.handle, ctypes.byref(stc), q_host[s].data_ptr(), p_host[s].data_ptr(),
+                                     sel.data_ptr(), out_host.data_ptr(), sh)
+            if st != 0:
+                raise RuntimeError(f"hsq_decode_step failed: {lib.hsq_last_error(ctx.handle).decode()}")
+            stream.synchronize()
+            acc += float(o_np[0, 0, 0])  # the host reads the step's result
+            ts.append(time.perf_counter() - t0)
+        return ts if timed else None
+
     def barrier():
         if world > 1:
             import torch.distributed as dist
@@ -550,15 +713,21 @@ def run_hsq(args, rank, world, local):
 
     if args.quick:
         res_dev, res_e2e = res, res
+        wall_e2e = [x * 1e-3 for x in res["step_ms"]]
         lp = {"h2d_gbs": float("nan"), "d2h_gbs": float("nan")}
     else:
         loop("device", args.warmup, timed=False)
         res_dev = loop("device", args.steps)
         loop("host", args.warmup, e2e=True, timed=False)
         res_e2e = loop("host", args.steps, e2e=True)
+        e2e_wall(args.warmup, timed=False)
+        wall_e2e = e2e_wall(args.steps)
         lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
     growth = None if args.quick else measure_growth(H, torch, w, li, flush, clean, sink)
+    small = None if args.quick or world > 1 else measure_small_workloads(
+        H, torch, lp, flush, clean, sink, min(args.steps, 200), max(args.warmup, 3),
+        0.0 if args.no_cpu_baseline else 3.0)
     codecs = None if args.quick else measure_codecs(H, torch, w, li)
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
@@ -575,45 +744,67 @@ def run_hsq(args, rank, world, local):
     if args.codec != "tq" or args.qjl:  # the capture is of the TurboQuant fused step
         traffic, traffic_src = None, "no ncu capture of this variant"
     hbm_dev_achieved = (ab["hbm"] + ab["link"]) / (dev_ms * 1e-3) / 1e9
+    link_ok = link_gbs == link_gbs and link_gbs > 0
+    link_bound = link_ok and ab["link"] / link_gbs > ab["hbm"] / hbm_peak
+    kern = "decode_kernel (whole step: route, select, L3 gather, attention), L3 in pinned host memory"
+    hbm_roof = {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": hbm_achieved / hbm_peak, "traffic": traffic, "kernel": kern,
+                "bytes_per_launch": ab["hbm"], "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic_source": traffic_src}
+    if link_bound:
+        # the step's binding resource: t* = max(HBM bytes / HBM peak, link bytes / link peak)
+        # is the link term, so achieved / peak on the link equals t* / t
+        roofline = {"bound": "host link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
+                    "frac": link_achieved / link_gbs, "kernel": kern,
+                    "bytes_per_launch": ab["link"], "t_star_us": t_star * 1e6, "t_us": ms_per_step * 1e3,
+                    "peak_source": "pinned host-to-device copy measured in this run (1 GiB copy_, best of 5, "
+                                   "CUDA events); MEASURED_PEAKS.json holds no host-link figure",
+                    "traffic": traffic, "traffic_source": traffic_src + " (DRAM bytes of the kernel)"}
+    else:
+        roofline = hbm_roof
+    wall_mean = sum(wall_e2e) / len(wall_e2e)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} beta{w.beta} "
-                               f"L1={l1_count} non-empty groups={nonempty}, L3 in pinned host memory",
+        "config": {"workload": workload_desc(w, l1_count, nonempty),
+                   "l3": "pinned host memory (read in place by the kernel over the host link)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"cold and clean at every step: {FLUSH_BYTES >> 20} MiB device write, then a "
                          f"{FLUSH_BYTES >> 20} MiB read, between timed steps (outside the step events)",
                    "n_splits": args.n_splits or "auto", "codec": args.codec + ("+qjl" if args.qjl else "")},
-        "roofline": {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": hbm_achieved / hbm_peak, "traffic": traffic,
-                     "kernel": "decode_kernel (whole step: route, select, L3 gather, attention), L3 in pinned host memory",
-                     "bytes_per_launch": ab["hbm"],
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic_source": traffic_src},
+        "roofline": roofline,
+        "roofline_hbm": hbm_roof,
         "roofline_link": {"bound": "host link", "achieved": link_achieved, "peak": link_gbs, "unit": "GB/s",
-                          "frac": link_achieved / link_gbs, "bytes_per_launch": ab["link"],
+                          "frac": link_achieved / link_gbs if link_ok else None, "bytes_per_launch": ab["link"],
                           "peak_source": "pinned host-to-device copy measured in this run"},
         "roofline_hbm_device_l3": {"bound": "hbm", "achieved": hbm_dev_achieved, "peak": hbm_peak,
                                    "unit": "GB/s", "frac": hbm_dev_achieved / hbm_peak,
                                    "kernel": "decode_kernel, L3 in device memory (L3 bytes counted as HBM bytes)",
                                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
-        "step_roofline": {"t_star_us": t_star * 1e6, "t_us": ms_per_step * 1e3, "frac": t_star / (ms_per_step * 1e-3),
+        "step_roofline": {"t_star_us": t_star * 1e6 if link_ok else None, "t_us": ms_per_step * 1e3,
+                          "frac": t_star / (ms_per_step * 1e-3) if link_ok else None,
                           "hbm_bytes": ab["hbm"], "link_bytes": ab["link"],
                           "hbm_gbs": ab["hbm"] / (ms_per_step * 1e-3) / 1e9, "link_gbs": link_achieved},
         "device_l3": {"value": 1e3 / dev_ms, "unit": UNIT, "ms_per_step": dev_ms,
                       "step_roofline_frac": t_star_dev / (dev_ms * 1e-3)},
-        "e2e": {"value": 1e3 / mean(res_e2e["step_ms"]), "unit": UNIT,
+        "e2e": {"value": 1.0 / wall_mean, "unit": UNIT,
                 "h2d_bytes_per_step": q_in.numel() * 4 + p_in.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 4,
-                "how": "hsq_decode_step given page-locked host q, pos and out (read and written by the "
-                       "kernel over the host link, inside the step events)"},
+                "us_per_step_mean": wall_mean * 1e6, "us_per_step_median": statistics.median(wall_e2e) * 1e6,
+                "how": "host wall clock per step: hsq_decode_step (C ABI) given page-locked host q, pos and out "
+                       "(read and written by the kernel over the host link), then a stream synchronize and a "
+                       "host read of out; L2 flushed and the device idle before each step's clock",
+                "device_events": {"value": 1e3 / mean(res_e2e["step_ms"]), "unit": UNIT,
+                                  "how": "the same call timed between CUDA events on the stream, steps queued "
+                                         "ahead (the host neither waits for nor reads a step inside the events)"}},
         "encode": {"ms_pinned_l3": enc["host"], "ms_device_l3": enc["device"],
                    "tokens_per_s_pinned_l3": w.B * w.T / (enc["host"] * 1e-3),
                    "input_gbs_pinned_l3": w.B * w.Hkv * w.T * 2 * 128 * 2 / (enc["host"] * 1e-3) / 1e9,
                    "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
         "link_peak": lp,
         "growth": growth,
+        "small_workloads": small,
         "codec": codecs,
         "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
@@ -622,7 +813,8 @@ def run_hsq(args, rank, world, local):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
-        line["cpu_baseline"] = cpu_oracle_sample(w, li, q, pos, args.cpu_baseline_seconds)
+        line["cpu_baseline"], line["near_ties"] = cpu_oracle_sample(w, li, q, pos, args.cpu_baseline_seconds,
+                                                                    head0, s0[0, 0])
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -637,6 +829,34 @@ def layer_bytes(w, beta: int, l1_counts, nonempty):
     hbm = w.Hkv * (int(sum(l1_counts)) * 2 * 68 + int(sum(nonempty)) * 2 * 52)
     link = w.B * w.Hkv * beta * w.N * 136
     return hbm, link
+
+
+def layers_oracle_sample(w, L, li, q, pos, beta, nsteps=4):
+    """The float64 oracle on the multi-layer workload's stated sample: one
+    full-layer encode (every sequence and KV head of layer 0) and `nsteps`
+    decode steps of layers 0 and L - 1 (every sequence and KV head, routing
+    and attention), reported per layer-step."""
+    import oracle as O
+    t0 = time.perf_counter()
+    caches = {0: O.encode(li.K, li.V, li.l1_mask, li.signs, w.N, w.theta)}
+    enc_s = time.perf_counter() - t0
+    if L > 1:
+        mask, signs = W.layer_meta(w, L - 1)
+        caches[L - 1] = O.encode(li.K, li.V, mask, signs, w.N, w.theta)
+    per = []
+    for l, c in caches.items():
+        for s in range(nsteps):
+            t0 = time.perf_counter()
+            sel, _ = O.route(c, q[s], pos[s], beta)
+            O.decode_attn(c, q[s], pos[s], sel)
+            per.append(time.perf_counter() - t0)
+    t_layer = sum(per) / len(per)
+    return {"value": 1.0 / (t_layer * L), "unit": UNIT, "us_per_layer": t_layer * 1e6,
+            "encode_s_per_layer": enc_s, "cores": len(os.sched_getaffinity(0)), "blas_threads": blas_threads(),
+            "kind": "oracle",
+            "sample": f"one full-layer encode of layer 0 ({w.B * w.Hkv} (sequence, KV head) pairs, {enc_s:.1f} s) "
+                      f"and {nsteps} decode steps of layers {sorted(caches)} (every pair, beta {beta}); "
+                      f"value = 1 / (mean layer-step time x {L} layers)"}
 
 
 def run_layers(args, rank, world, local):
@@ -777,6 +997,9 @@ def run_layers(args, rank, world, local):
     clk = clocks.stop()
     assert H.hsq_sync_status(ctx0) == 0
     head = next((r for r in rows if r["beta"] == w.beta), rows[0])
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = layers_oracle_sample(w, L, li, q, pos, head["beta"])
     enc = statistics.median(enc_ms) if enc_ms else float("nan")
     line = {
         "metric": f"HSQ decode steps/s ({w.name}, {L} layers per step)", "value": head["steps_per_s"],
@@ -802,6 +1025,8 @@ def run_layers(args, rank, world, local):
         "gpu_launches": args.steps * L * len(rows),
         "clocks": clk,
     }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -9,6 +9,7 @@
 // item 1.
 
 #include <cooperative_groups.h>
+#include <cuda.h>  // driver types only (CUcontext, CUresult): entry points are looked up at run time
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -1095,19 +1096,25 @@ const char* hsq_last_error(const hsq_ctx* ctx) {
 // cudaMalloc may).  hsq_route_noalloc serves them.  It needs no context: the
 // routing scores and the per-(b, h) tickets live in a fixed-size file-scope
 // device array (every GPU that loads this library holds it until the process
-// exits), the codebook in a small file-scope array filled once per device,
-// and the query's RoPE angles are evaluated in float64 inside the kernel
-// instead of being read from a context's tables.
+// exits), the codebook travels by value in the kernel's parameters, and the
+// query's RoPE angles are evaluated in float64 inside the kernel instead of
+// being read from a context's tables.
 // ===========================================================================
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[HSQ_NOALLOC_SCRATCH_BYTES];
-static __device__ float g_noalloc_codebook[hsq::kCodebookFloats];
+
+struct NoallocCodebook { float v[hsq::kCodebookFloats]; };
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
+// per device: the scratch array's device address and the CUDA context it was
+// looked up in (a device reset makes a new context and reloads the module)
 unsigned char* g_noalloc_ptr[kNoallocMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kNoallocMaxDevices] = {};
+bool g_noalloc_have_cb = false;
+NoallocCodebook g_noalloc_cb;
 
 // Query RoPE from float64 angles p * theta^(-2i/d).
 __device__ __forceinline__ void rope_f64(float v[8], int p, double theta) {
@@ -1126,7 +1133,8 @@ __device__ __forceinline__ void rope_f64(float v[8], int p, double theta) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, RouteArgs a, double theta) {
+__global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, RouteArgs a, double theta,
+                                                                  int max_pos, NoallocCodebook cb) {
     extern __shared__ uint32_t s_keys[];
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
@@ -1140,7 +1148,7 @@ __global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, Ro
     const int bh = blockIdx.y, b = bh / c.Hkv, h = bh % c.Hkv;
     const int hw = threadIdx.x >> 4, l = hlane();
     const unsigned m = half_mask();
-    for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = g_noalloc_codebook[i];
+    for (int i = threadIdx.x; i < hsq::kCodebookFloats; i += blockDim.x) s_cb[i] = cb.v[i];
     for (int i = threadIdx.x; i < kDim; i += blockDim.x) s_sign[i] = c.signs ? (float)c.signs[i] : 1.f;
     __syncthreads();
     float sg[8];
@@ -1150,7 +1158,9 @@ __global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, Ro
         const int j = h * R + hw;
         float x[8];
         load_f32x8(a.q + ((size_t)b * c.Hq + j) * kDim, x);
-        rope_f64(x, __ldg(a.pos + b), theta);
+        // out-of-range positions are clamped to [0, max_pos) as hsq_route clamps
+        // them (this entry point has no device error word to report them in)
+        rope_f64(x, min(max(__ldg(a.pos + b), 0), max_pos - 1), theta);
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] *= sg[i];
         if (c.rot) fwht(x, m);
@@ -1293,38 +1303,73 @@ __global__ void __launch_bounds__(kThreads) route_noalloc_kernel(CacheView c, Ro
     if (threadIdx.x == 0) a.counters[bh] = 0;
 }
 
-// One-time set-up of the current device: the scratch array's device address
-// (a host-side use of the symbol name itself would not be a device address)
-// and the codebook upload.  Synchronous, so it must not run under stream capture.
-hsq_status noalloc_setup(unsigned char** scratch) {
+// The unique id of the calling thread's current CUDA context (0 when none is
+// current or the driver does not say), through driver entry points looked up
+// once, so the library needs no link to the driver library.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        looked_up = true;
+    }
+    CUcontext cx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&cx) != CUDA_SUCCESS || !cx || get_id(cx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Set-up of the current device: the scratch array's device address (a
+// host-side use of the symbol name itself would not be a device address).
+// Done on the first call on a device, and again when the device's CUDA
+// context has changed since (after a device reset the module is reloaded
+// and the array has a new address).  Synchronous on first use of a context,
+// so such a call must not run under stream capture.  The codebook is
+// computed once per process on the host and passed by value.
+hsq_status noalloc_setup(unsigned char** scratch, NoallocCodebook* cb) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
     if (dev < 0 || dev >= kNoallocMaxDevices) return fail(nullptr, HSQ_ERR_UNSUPPORTED, "device ordinal above 63");
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_have_cb) {
+        hsq::device_codebook(g_noalloc_cb.v);
+        g_noalloc_have_cb = true;
+    }
+    const unsigned long long ctx_id = current_context_id();
+    if (!g_noalloc_ptr[dev] || ctx_id == 0 || ctx_id != g_noalloc_ctx[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetSymbolAddress(scratch)");
-        float cb[hsq::kCodebookFloats];
-        hsq::device_codebook(cb);
-        e = cudaMemcpyToSymbol(g_noalloc_codebook, cb, sizeof(cb));
-        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemcpyToSymbol(codebook)");
         g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+        g_noalloc_ctx[dev] = current_context_id();  // the context the lookup ran in
     }
     *scratch = g_noalloc_ptr[dev];
+    *cb = g_noalloc_cb;
     return HSQ_OK;
 }
 
 template <int R>
-hsq_status launch_route_noalloc(const CacheView& v, const RouteArgs& a, double theta, cudaStream_t st, int dev) {
+hsq_status launch_route_noalloc(const CacheView& v, const RouteArgs& a, double theta, int max_pos,
+                                const NoallocCodebook& cb, cudaStream_t st, int dev) {
     const size_t smem = (size_t)v.G * 4;
     if (smem > 48 * 1024) {
         cudaError_t e = raise_smem_limit((const void*)route_noalloc_kernel<R>, dev, smem);
         if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaFuncSetAttribute");
     }
     dim3 grid((v.G + kRouteGroupsPerCta - 1) / kRouteGroupsPerCta, v.B * v.Hkv);
-    route_noalloc_kernel<R><<<grid, kThreads, smem, st>>>(v, a, theta);
+    route_noalloc_kernel<R><<<grid, kThreads, smem, st>>>(v, a, theta, max_pos, cb);
     return HSQ_OK;
 }
 
@@ -1350,7 +1395,8 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
                     "B * n_kv_heads * ceil(T / group_n) too large for the fixed 4 MiB scratch of hsq_route_noalloc");
     if (G * 4 > 200 * 1024) return fail(nullptr, HSQ_ERR_INVALID, "ceil(T / group_n) above 51200");
     unsigned char* scratch = nullptr;
-    hsq_status st = noalloc_setup(&scratch);
+    NoallocCodebook cb;
+    hsq_status st = noalloc_setup(&scratch, &cb);
     if (st != HSQ_OK) return st;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1368,11 +1414,11 @@ extern "C" hsq_status hsq_route_noalloc(const hsq_config* cfg, const hsq_cache* 
     RouteArgs a{q, pos, sel, reinterpret_cast<float*>(scratch + ticket_bytes),
                 reinterpret_cast<int*>(scratch), nullptr};
     switch (r) {
-        case 1: st = launch_route_noalloc<1>(v, a, cfg->rope_theta, s, dev); break;
-        case 2: st = launch_route_noalloc<2>(v, a, cfg->rope_theta, s, dev); break;
-        case 4: st = launch_route_noalloc<4>(v, a, cfg->rope_theta, s, dev); break;
-        case 5: st = launch_route_noalloc<5>(v, a, cfg->rope_theta, s, dev); break;
-        default: st = launch_route_noalloc<8>(v, a, cfg->rope_theta, s, dev); break;
+        case 1: st = launch_route_noalloc<1>(v, a, cfg->rope_theta, cfg->max_pos, cb, s, dev); break;
+        case 2: st = launch_route_noalloc<2>(v, a, cfg->rope_theta, cfg->max_pos, cb, s, dev); break;
+        case 4: st = launch_route_noalloc<4>(v, a, cfg->rope_theta, cfg->max_pos, cb, s, dev); break;
+        case 5: st = launch_route_noalloc<5>(v, a, cfg->rope_theta, cfg->max_pos, cb, s, dev); break;
+        default: st = launch_route_noalloc<8>(v, a, cfg->rope_theta, cfg->max_pos, cb, s, dev); break;
     }
     if (st != HSQ_OK) return st;
     e = cudaGetLastError();

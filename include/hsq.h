@@ -407,7 +407,9 @@ hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word);
  *   Same inputs and output as hsq_route (cfg describes the cache; scores are
  *   not returned).  The query's RoPE angles are evaluated in float64 inside
  *   the kernel, so scores agree with hsq_route to fp32 rounding and sel is
- *   identical except for near-ties of the beta-th score.
+ *   identical except for near-ties of the beta-th score.  A position outside
+ *   [0, cfg->max_pos) is clamped into it, as hsq_route clamps it, but is not
+ *   reported (there is no device error word without a context).
  *   Scratch: a fixed array of HSQ_NOALLOC_SCRATCH_BYTES in device memory,
  *   defined in the library and held by every GPU that loads it until the
  *   process exits.  It holds 256-byte-rounded B*Hkv tickets plus the
@@ -417,8 +419,11 @@ hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word);
  *   threads) race and must be ordered by the caller.  The tickets are
  *   cleared (cudaMemsetAsync on `stream`) at the start of each call.
  *   The first call on a device sets that device up (looks up the array's
- *   device address and uploads the codebook, synchronously); make that first
- *   call outside any stream capture.  Errors: HSQ_ERR_INVALID,
+ *   device address, synchronously; the codebook is passed to the kernel by
+ *   value); make that first call outside any stream capture.  The set-up is
+ *   repeated when the device's CUDA context has changed since (after a
+ *   device reset), so the same rule holds for the first call after a reset.
+ *   Errors: HSQ_ERR_INVALID,
  *   HSQ_ERR_UNSUPPORTED, HSQ_ERR_CUDA (text via hsq_last_error(NULL)).
  */
 enum { HSQ_NOALLOC_SCRATCH_BYTES = 4 << 20 };

@@ -10,17 +10,19 @@ sampled pair and step:
   * the attention output is within 1e-3 relative L2 of the oracle's on the
     GPU cache and selection (the acceptance of the small-size tests);
 and, for the planted-needle workload, the needle group is routed at step 0
-for every (sequence, KV head).  A further case forces the in-place variant of
-the decode kernel (inputs read from global memory, not staged); three more run
-the 8B/32K layer with the Plain-KV codec, with per-query-head routing and with
-TQ-QKV."""
+for every (sequence, KV head).  The encode is checked on sampled pairs too:
+L1 count and positions, group member counts, and every tier's codes
+(bit-exact outside the near-tie band) and norms against the oracle's encode
+of the pair.  A further case forces the in-place variant of the decode kernel
+(inputs read from global memory, not staged); three more run the 8B/32K layer
+with the Plain-KV codec, with per-query-head routing and with TQ-QKV."""
 
 import numpy as np
 import pytest
 
 import oracle as O
 import workloads as W
-from hsq_harness import abi_buffers, ensure_built, gpu_encode, make_ctx, rel_l2, sel_mismatch
+from hsq_harness import abi_buffers, code_mismatch, ensure_built, gpu_encode, make_ctx, rel_l2, sel_mismatch
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +45,32 @@ def _sub_view(bufs, li, w, b, h, codec="tq", qjl_S=None):
         v = v[b:b + 1]
         sub[k] = v[:, h:h + 1] if k in PER_HEAD else v
     return O.cache_from_abi(sub, li.l1_mask[b:b + 1], li.signs, w.N, w.T, w.theta, codec=codec, qjl_S=qjl_S)
+
+
+def _check_encode(w, li, cache, samples):
+    """Full-size encode parity on sampled (sequence, KV head) pairs: the GPU
+    cache's L1 index (count, positions), group member counts, and the codes
+    and norms of every tier of the pair against the oracle's encode of that
+    pair's K/V, codes bit-exact outside the near-tie band."""
+    bufs = abi_buffers(cache)
+    report = {}
+    for b, h in samples:
+        ora = O.encode(li.K[b:b + 1, h:h + 1], li.V[b:b + 1, h:h + 1], li.l1_mask[b:b + 1], li.signs, w.N,
+                       w.theta)
+        g = _sub_view(bufs, li, w, b, h)
+        n = int(ora.l1_count[0])
+        assert int(bufs["l1_count"][b]) == n
+        np.testing.assert_array_equal(bufs["l1_pos"][b, :n], ora.l1_pos[0, :n])
+        np.testing.assert_array_equal(bufs["l2_cnt"][b], ora.l2_cnt[0])
+        for tier, bits in (("l3_k", 4), ("l3_v", 4), ("l1_k", 4), ("l1_v", 4), ("l2_k", 3), ("l2_v", 3)):
+            go, oo = getattr(g, tier), getattr(ora, tier)
+            sl = (slice(None), slice(None), slice(0, n)) if tier.startswith("l1") else (Ellipsis,)
+            bad, tie_diff, ties = code_mismatch(go.codes[sl], oo.codes[sl], oo.y[sl], bits, oo.norms[sl])
+            np.testing.assert_allclose(go.norms[sl], oo.norms[sl], rtol=1e-5 if tier.startswith("l2") else 2e-6,
+                                       atol=1e-30)
+            assert bad == 0, f"(b={b}, h={h}) {tier}: {bad} code mismatches outside the near-tie band"
+            report[(b, h, tier)] = (tie_diff, ties)
+    print(f"[{w.name}] encode near-tie coordinates (differing, total): {report}")
 
 
 def _run_and_check(w, li, ctx, cache, steps, samples, needle=False, codec="tq", per_head=False, qjl_S=None):
@@ -94,6 +122,7 @@ def test_qwen3_8b_32k_full_size():
     li = W.layer_inputs(w, rope=_rope(w))
     ctx = make_ctx(w)
     cache = gpu_encode(ctx, w, li)
+    _check_encode(w, li, cache, samples=[(0, 0), (0, 5)])
     worst = _run_and_check(w, li, ctx, cache, steps=3, samples=[(0, 0), (0, 5)], needle=True)
     print(f"[qwen3_8b_32k] worst sampled rel L2 {worst:.2e}")
 
@@ -132,6 +161,7 @@ def test_qwen3_4b_b16_8k_full_size():
     li = W.layer_inputs(w, rope=_rope(w))
     ctx = make_ctx(w)
     cache = gpu_encode(ctx, w, li)
+    _check_encode(w, li, cache, samples=[(0, 0), (7, 3), (15, 7)])
     worst = _run_and_check(w, li, ctx, cache, steps=2, samples=[(0, 0), (7, 3), (15, 7)])
     print(f"[qwen3_4b_b16_8k] worst sampled rel L2 {worst:.2e}")
 
@@ -142,6 +172,8 @@ def test_qwen3_14b_b4_32k_full_size(beta):
     li = _inputs_14b()
     ctx = make_ctx(w)
     cache = gpu_encode(ctx, w, li)
+    if beta == 16:
+        _check_encode(w, li, cache, samples=[(3, 6)])
     worst = _run_and_check(w, li, ctx, cache, steps=2, samples=[(0, 1), (3, 6)])
     print(f"[qwen3_14b_b4_32k beta={beta}] worst sampled rel L2 {worst:.2e}")
 

@@ -131,7 +131,7 @@ def test_route_parity(name):
                 row = gsel[b, h]
                 valid = row[row >= 0]
                 assert np.all(np.diff(valid) > 0) and np.all(row[len(valid):] == -1)
-                bad, diff = sel_mismatch(row, osel[b, h], gs[b, h], w.beta)
+                bad, diff = sel_mismatch(row, osel[b, h], oscores[b, h], w.beta)  # band from the oracle's scores
                 assert bad == 0, f"step {s} (b={b}, h={h}): selection differs beyond near-ties"
 
 

@@ -110,3 +110,71 @@ def test_boundary_count_equals_nearest_centroid(bits):
     brute = np.argmin(np.abs(y[..., None] - c), axis=-1)
     far = ~O.near_boundary(y, bits, rel=1e-6)
     np.testing.assert_array_equal(codes[far], brute[far])
+
+
+# The near-tie band of the acceptance rule: a coordinate within
+# 1e-5 * max(|tau_k|, 1/sqrt(d)) of a boundary tau_k.  Its half-width at the
+# zero boundary is 1e-5 / sqrt(128) = 8.8388e-7; at the outermost 4-bit
+# boundary, about (2.0459 + 2.6889) / 2 / sqrt(128) = 0.20929 (the positive
+# levels sqrt(d) c of the d = 128 codebook, computed independently of the
+# oracle), it is 2.09e-6.  near_boundary takes coordinates of d = 128
+# vectors (the last axis), so each probe value fills one such vector.
+ZERO_BAND = 8.838834764831845e-07
+
+
+def _nb(values, bits):
+    y = np.repeat(np.asarray(values, np.float64)[:, None], 128, axis=1)
+    got = O.near_boundary(y, bits)
+    assert got.shape == y.shape and np.all(got == got[:, :1])
+    return got[:, 0]
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_near_boundary_band_at_every_boundary(bits):
+    _, tau = O.codebook(bits)
+    for t in tau:
+        tol = 1e-5 * max(abs(t), ZERO_BAND / 1e-5)
+        inside = [t - 0.5 * tol, t, t + 0.5 * tol, t + 0.99 * tol, t - 0.99 * tol]
+        outside = [t - 2 * tol, t + 2 * tol, t + 1.05 * tol, t - 1.05 * tol]
+        assert np.all(_nb(inside, bits)), (bits, t)
+        assert not np.any(_nb(outside, bits)), (bits, t)
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_near_boundary_is_relative_not_absolute(bits):
+    _, tau = O.codebook(bits)
+    assert tau[len(tau) // 2] == 0.0
+    # the zero boundary: half-width 1e-5 / sqrt(128), not 1e-5
+    assert _nb([0.9 * ZERO_BAND, -0.9 * ZERO_BAND], bits).all()
+    assert not _nb([1.1 * ZERO_BAND, -1.1 * ZERO_BAND, 2e-6, 9e-6], bits).any()
+    # the outermost boundary: half-width 1e-5 |tau|, wider than the zero boundary's
+    t = tau[-1]
+    assert t > 0.15
+    assert _nb([t + 1.5 * ZERO_BAND, -t - 1.5 * ZERO_BAND], bits).all()
+    assert not _nb([t + 1.2e-5 * t, -t - 1.2e-5 * t], bits).any()
+
+
+def test_near_boundary_outermost_4bit_band_literal():
+    # half-width at the outermost 4-bit boundary from the independently
+    # computed levels above (0.20929 * 1e-5 = 2.093e-6)
+    _, tau = O.codebook(4)
+    assert abs(tau[-1] - (2.0459 + 2.6889) / 2 / np.sqrt(128)) < 1e-4
+    assert _nb([tau[-1] + 2.07e-6, tau[-1] - 2.07e-6], 4).all()
+    assert not _nb([tau[-1] + 2.12e-6, tau[-1] - 2.12e-6], 4).any()
+
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_near_boundary_far_values_and_shapes(bits):
+    c, tau = O.codebook(bits)
+    # centroids and the ends of the range lie far from every boundary
+    assert not _nb(c, bits).any()
+    assert not _nb([-1.0, 1.0, 0.5, -0.5], bits).any()
+    # elementwise over any leading shape: a vector holding every boundary
+    # and every centroid is flagged exactly at the boundaries
+    y = np.zeros((2, 3, 128))
+    y[:, :, : len(tau)] = tau
+    y[:, :, len(tau): len(tau) + len(c)] = c
+    y[:, :, len(tau) + len(c):] = 0.5
+    got = O.near_boundary(y, bits)
+    assert got.shape == (2, 3, 128)
+    assert got[..., : len(tau)].all() and not got[..., len(tau):].any()

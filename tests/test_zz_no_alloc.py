@@ -12,8 +12,9 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle as O
 import workloads as W
-from hsq_harness import ensure_built, gpu_encode, make_ctx, sel_mismatch
+from hsq_harness import abi_buffers, ensure_built, gpu_encode, make_ctx, oracle_view, sel_mismatch
 
 pytestmark = pytest.mark.gpu
 
@@ -24,9 +25,10 @@ def test_route_noalloc_matches_route_on_consecutive_calls(name):
     ensure_built()
     import hierarchical_kv_cache_hsq_gb300 as H
     w = W.get_workload(name)
-    li = W.layer_inputs(w)
+    li = W.layer_inputs(w, rope=lambda x, p: O.rope(x, p, w.theta))
     ctx = make_ctx(w)
     cache = gpu_encode(ctx, w, li)
+    gview = oracle_view(abi_buffers(cache), li, w)
     q, pos = W.queries(w, steps=2)
     for s in range(2):  # two calls in a row: the shared scratch keeps the previous call's contents
         qd, pd = torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda()
@@ -36,13 +38,41 @@ def test_route_noalloc_matches_route_on_consecutive_calls(name):
         got = torch.full((w.B, w.Hkv, w.beta), -7, dtype=torch.int32, device="cuda")
         H.hsq_route_noalloc(ctx.cfg, cache, qd, pd, got)
         torch.cuda.synchronize()
-        r, g, sc = ref.cpu().numpy(), got.cpu().numpy(), scores.cpu().numpy()
+        r, g = ref.cpu().numpy(), got.cpu().numpy()
+        # the float64 oracle on the same cache decides which differences are near-ties
+        osel, oscores = O.route(gview, q[s], pos[s], w.beta)
         for b in range(w.B):
             for h in range(w.Hkv):
                 valid = g[b, h][g[b, h] >= 0]
                 assert np.all(np.diff(valid) > 0) and np.all(g[b, h][len(valid):] == -1)
-                bad, _ = sel_mismatch(g[b, h], r[b, h], sc[b, h], w.beta)
-                assert bad == 0, f"call {s}: selection differs beyond near-ties at (b={b}, h={h})"
+                bad, _ = sel_mismatch(g[b, h], osel[b, h], oscores[b, h], w.beta)
+                assert bad == 0, f"call {s}: selection differs from the oracle beyond near-ties at (b={b}, h={h})"
+                bad, _ = sel_mismatch(g[b, h], r[b, h], oscores[b, h], w.beta)
+                assert bad == 0, f"call {s}: selection differs from hsq_route beyond near-ties at (b={b}, h={h})"
+    ctx.close()
+
+
+def test_route_noalloc_clamps_positions_like_hsq_route():
+    """A position outside [0, max_pos) routes as the nearest valid position
+    (hsq_route clamps it the same way and also flags it)."""
+    import torch
+    ensure_built()
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = W.get_workload("tiny_1k")
+    li = W.layer_inputs(w)
+    ctx = make_ctx(w)
+    cache = gpu_encode(ctx, w, li)
+    q, _ = W.queries(w, steps=1)
+    qd = torch.from_numpy(q[0]).cuda()
+    max_pos = ctx.cfg.max_pos
+    outs = {}
+    for p in (-5, 0, max_pos - 1, max_pos + 50):
+        got = torch.full((w.B, w.Hkv, w.beta), -7, dtype=torch.int32, device="cuda")
+        H.hsq_route_noalloc(ctx.cfg, cache, qd, torch.full((w.B,), p, dtype=torch.int32, device="cuda"), got)
+        outs[p] = got.cpu().numpy()
+    assert np.array_equal(outs[-5], outs[0])
+    assert np.array_equal(outs[max_pos + 50], outs[max_pos - 1])
+    assert not np.array_equal(outs[0], outs[max_pos - 1])
     ctx.close()
 
 
