@@ -65,6 +65,11 @@ Readings where the pages are silent (each also listed in the design notes):
     direction error as cosine similarity): relMSE = sum_t |x^_t - x_t|^2 /
     sum_t |x_t|^2 over a set of vectors; cosine = the mean over vectors of
     nonzero norm of x^_t . x_t / (|x^_t| |x_t|).
+  * Prefill ([HSQ] section 4, results: the prefill overhead of compressing
+    the prompt, 1.2-1.3x at 32K): the prompt's attention is the model's
+    ordinary dense causal softmax attention over RoPE'd queries and keys
+    (GQA, scale 1/sqrt(d)); HSQ changes only what is kept for decoding, the
+    encode of the same K/V.  A fused prefill returns both.
   * Decode-time growth (the pages describe the tiers of a context and leave
     their growth open): a cache grown by appended tokens is, by definition,
     the encode of the longer context under the grown L1 set (grown_l1_mask):
@@ -118,6 +123,8 @@ __all__ = [
     "key_residuals",
     "codec_errors",
     "CODECS",
+    "prefill_attn",
+    "prefill",
 ]
 
 D = 128
@@ -781,3 +788,39 @@ def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T
         out.l3_qjl = Sketch(bits=unpack_sketch_words(np.asarray(bufs["l3_qs"])[:, :, :T], m),
                             norm=np.asarray(bufs["l3_qn"])[:, :, :T].astype(np.float32))
     return out
+
+
+# ---------------------------------------------------------------------------
+# Prefill ([HSQ] section 4, results: prefill overhead at 32K).
+# ---------------------------------------------------------------------------
+
+def prefill_attn(Q: np.ndarray, K: np.ndarray, V: np.ndarray, theta: float = 1.0e6) -> np.ndarray:
+    """Dense causal attention of a prompt: Q [B, Hq, T, d] and K, V [B, Hkv, T, d]
+    pre-RoPE at positions 0..T-1; query t of head j attends to keys 0..t of KV
+    head j // (Hq / Hkv) with weights softmax(RoPE(q_t, t) . RoPE(k_s, s) / sqrt(d)).
+    Returns O [B, Hq, T, d] in float64."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    B, Hq, T, d = Q.shape
+    Hkv = K.shape[1]
+    t = np.arange(T)
+    Qr = rope(Q, t, theta)
+    Kr = rope(K, t, theta)
+    causal = t[None, :] <= t[:, None]                    # [query, key]
+    O = np.zeros_like(Q)
+    for b in range(B):
+        for h, js in enumerate(_heads(Hq, Hkv)):
+            for j in js:
+                logits = (Qr[b, j] @ Kr[b, h].T) / np.sqrt(d)
+                logits = np.where(causal, logits, -np.inf)
+                w = np.exp(logits - logits.max(axis=1, keepdims=True))
+                O[b, j] = (w / w.sum(axis=1, keepdims=True)) @ V[b, h]
+    return O
+
+
+def prefill(Q: np.ndarray, K: np.ndarray, V: np.ndarray, l1_mask: np.ndarray, signs: np.ndarray, N: int,
+            theta: float = 1.0e6, **encode_kw):
+    """A prompt's prefill with HSQ: the dense causal attention output and the
+    three-tier cache of the same K/V (encode)."""
+    return prefill_attn(Q, K, V, theta), encode(K, V, l1_mask, signs, N, theta, **encode_kw)
