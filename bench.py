@@ -502,6 +502,67 @@ def measure_codecs(H, torch, w, li):
     return out
 
 
+def measure_prefill(H, torch, w, li, reps=5):
+    """The prompt's prefill on this layer: hsq_prefill with the cache (the
+    attention plus the encode that also writes the attention's K/V operands,
+    K/V read once), the attention alone (hsq_prefill without a cache), and
+    hsq_encode alone; CUDA events, median of `reps`, bf16 Q drawn N(0, 1).
+    Tensor roofline: the causal attention's useful flops 4 Hq T^2 d / 2 (the
+    logit and value products) over the measured bf16 peak; the kernel issues
+    2.5x those flops (three products for the logits, two for the values, to
+    keep fp32-level accuracy)."""
+    import json as _json
+    rng = np.random.default_rng(99)
+    Qn = rng.standard_normal((w.B, w.Hq, w.T, 128), dtype=np.float32)
+    Q = torch.from_numpy(Qn).cuda().to(torch.bfloat16).contiguous()
+    del Qn
+    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta)
+    ctx = H.Context(cfg)
+    cache = H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False)
+    H.set_layer_inputs(cache, li.l1_mask, li.signs)
+    ws = torch.empty(H.hsq_prefill_workspace_size(ctx, w.B, w.T), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.B, w.Hq, w.T, 128), device="cuda")
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    fused = timed(lambda: H.hsq_prefill(ctx, cache, Q, K, V, out, ws))
+    attn = timed(lambda: H.hsq_prefill(ctx, None, Q, K, V, out, ws))
+    enc = timed(lambda: H.hsq_encode(ctx, cache, K, V))
+    assert H.hsq_sync_status(ctx) == 0
+    peaks = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peaks = _json.load(f)
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    flops = 4.0 * w.B * w.Hq * w.T * w.T * 128 / 2
+    achieved = flops / (attn * 1e-3) / 1e12
+    ctx.close()
+    return {"ms_fused": fused, "ms_attention_only": attn, "ms_encode_only": enc,
+            "ms_separate": attn + enc, "overhead_fused": fused / attn, "overhead_separate": (attn + enc) / attn,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "kernel": "prefill_attn_kernel (tcgen05, TMEM accumulators)",
+                         "flops_per_launch": flops, "issued_flops_per_launch": 2.5 * flops,
+                         "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)" if peaks
+                         else "fallback 1900 TFLOP/s"},
+            "how": f"{w.name} layer, bf16 Q/K/V, L3 pinned; fused = hsq_prefill with the cache, attention only = "
+                   f"hsq_prefill without a cache, separate = attention only + hsq_encode; CUDA events, median of "
+                   f"{reps}"}
+
+
 SMALL_WORKLOADS = ("tiny_1k", "qwen3_0p6b_4k")
 
 
@@ -725,6 +786,7 @@ def run_hsq(args, rank, world, local):
         lp = link_peak(torch)
     assert H.hsq_sync_status(ctx) == 0
     growth = None if args.quick else measure_growth(H, torch, w, li, flush, clean, sink)
+    prefill = None if args.quick else measure_prefill(H, torch, w, li)
     small = None if args.quick or world > 1 else measure_small_workloads(
         H, torch, lp, flush, clean, sink, min(args.steps, 200), max(args.warmup, 3),
         0.0 if args.no_cpu_baseline else 3.0)
@@ -804,6 +866,7 @@ def run_hsq(args, rank, world, local):
                    "l3_link_gbs": w.B * w.Hkv * w.G * w.N * 136 / (enc["host"] * 1e-3) / 1e9},
         "link_peak": lp,
         "growth": growth,
+        "prefill": prefill,
         "small_workloads": small,
         "codec": codecs,
         "gpu_launches": args.steps,

@@ -83,6 +83,9 @@ _SIGS = {
     "hsq_append": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, ctypes.c_int, _vp]),
     "hsq_sync_status": (ctypes.c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int)]),
     "hsq_route_noalloc": (ctypes.c_int, [ctypes.POINTER(hsq_config), ctypes.POINTER(hsq_cache), _vp, _vp, _vp, _vp]),
+    "hsq_prefill_workspace_size": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "hsq_prefill": (ctypes.c_int, [_vp, ctypes.POINTER(hsq_cache), _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, _vp,
+                                   _vp, ctypes.c_size_t, _vp]),
     "hsq_last_error": (ctypes.c_char_p, [_vp]),
     "hsq_debug_set_fault": (ctypes.c_int, [ctypes.c_uint]),
     "hsq_version": (ctypes.c_char_p, []),
@@ -394,6 +397,28 @@ def hsq_decode_step(ctx: Context, cache: CacheBuffers, q, pos, sel, out, stream=
     c = cache.struct()
     _check(ctx.lib.hsq_decode_step(ctx.handle, ctypes.byref(c), q.data_ptr(), pos.data_ptr(), sel.data_ptr(),
                                    out.data_ptr(), _stream_handle(stream)), ctx.handle)
+
+
+def hsq_prefill_workspace_size(ctx: Context, B: int, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(ctx.lib.hsq_prefill_workspace_size(ctx.handle, B, T, ctypes.byref(n)), ctx.handle)
+    return int(n.value)
+
+
+def hsq_prefill(ctx: Context, cache: Optional[CacheBuffers], Q, K, V, out, workspace, stream=None):
+    """Prefill: causal attention of the prompt into out (float32) and, with a
+    cache, the encode of K/V (bf16 Q [B, Hq, T, 128], K/V [B, Hkv, T, 128])."""
+    import torch
+    for x in (Q, K, V):
+        if x.dtype != torch.bfloat16 or not x.is_contiguous():
+            raise ValueError("Q, K and V must be contiguous bfloat16")
+    if out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32")
+    B, _, T, _ = Q.shape
+    c = ctypes.byref(cache.struct()) if cache is not None else None
+    _check(ctx.lib.hsq_prefill(ctx.handle, c, Q.data_ptr(), K.data_ptr(), V.data_ptr(), B, T, out.data_ptr(),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream)), ctx.handle)
 
 
 def hsq_route_noalloc(cfg: hsq_config, cache: CacheBuffers, q, pos, sel, stream=None):

@@ -22,7 +22,7 @@ LIB = os.path.join(BUILD, "libhsq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["hsq_kernels.cu", "hsq_decode_r4.cu", "hsq_decode_r8.cu", "hsq_decode_r5.cu", "hsq_decode_r2.cu",
+SOURCES = ["hsq_kernels.cu", "hsq_prefill.cu", "hsq_decode_r4.cu", "hsq_decode_r8.cu", "hsq_decode_r5.cu", "hsq_decode_r2.cu",
            "hsq_decode_r1.cu", "hsq_host.cpp"]
 
 

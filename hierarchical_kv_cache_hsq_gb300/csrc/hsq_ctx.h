@@ -54,4 +54,17 @@ HSQ_DECLARE_DECODE(5)
 HSQ_DECLARE_DECODE(8)
 #undef HSQ_DECLARE_DECODE
 
+// Prefill (hsq_prefill.cu): the attention operands as shared-memory images in
+// the caller's workspace (layout in hsq_prefill.cu) and the kernels around them.
+struct PrefillImages {
+    uint8_t *qh, *ql, *kh, *kl, *vt;
+    int nqt, nkt;   // 128-query tiles, 64-key tiles (2 nqt)
+    size_t bytes;   // workspace bytes the images take
+};
+PrefillImages prefill_images(void* ws, int B, int Hq, int Hkv, int T);
+hsq_status prefill_prep_q(hsq_ctx* ctx, const PrefillImages& im, const void* Q, int B, int T, cudaStream_t st);
+hsq_status prefill_prep_kv(hsq_ctx* ctx, const PrefillImages& im, const void* K, const void* V, int B, int T,
+                           cudaStream_t st);
+hsq_status prefill_attention(hsq_ctx* ctx, const PrefillImages& im, float* out, int B, int T, cudaStream_t st);
+
 }  // namespace hsq

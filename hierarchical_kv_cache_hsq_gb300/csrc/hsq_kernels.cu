@@ -23,6 +23,7 @@
 
 #include "hsq_ctx.h"
 #include "hsq_device.cuh"
+#include "hsq_tc.cuh"
 
 namespace {
 
@@ -76,6 +77,9 @@ struct EncodeOut {
     uint8_t* l3;
     const int32_t* prefix;
     float* win_kv; float* gsum; int recent;  // growth state (win_kv NULL: none)
+    // prefill: the attention's key (RoPE'd, bf16 hi + lo) and transposed value
+    // operand images, 64-key tiles (hsq_prefill.cu); used by the kPF variant only
+    uint8_t* pf_kh; uint8_t* pf_kl; uint8_t* pf_vt; int pf_nkt;
 };
 
 // TQ3 of one group summary (this half-warp's 8 dims of the mean; x is
@@ -106,7 +110,8 @@ __device__ __forceinline__ void write_summary(float x[8], const float sg[8], uns
 // kernel is issue bound and the extra warps hide its memory and shared-memory
 // latencies; 32 warps measured 20 % slower)
 // kRot: TurboQuant rotation (false: Plain-KV), fixed at compile time
-template <int N, bool kBF16, bool kRot>
+// kPF: prefill, the same encode also writes the attention's K/V operand images
+template <int N, bool kBF16, bool kRot, bool kPF = false>
 __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c, EncodeOut o, const void* __restrict__ Kp,
                                                         const void* __restrict__ Vp, Tables tb) {
     __shared__ float s_cb[hsq::kCodebookFloats];
@@ -171,6 +176,31 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 #pragma unroll
     for (int i = 0; i < 8; ++i) xr[i] = x[i];
     if (half == 0 && in_ctx) rope(xr, t, tb);
+
+    if (kPF && t < o.pf_nkt * 64) {  // row t & 63 of key tile t >> 6 (zero past T)
+        const int row = t & 63;
+        const size_t img = (((size_t)b * c.Hkv + h) * o.pf_nkt + (t >> 6)) * (64 * kDim * 2);
+        if (half == 0) {
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                uint16_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) hsq_tc::split_bf16(xr[4 * blk + k], hi[k], lo[k]);
+                const uint32_t off = hsq_tc::sw128_row_quad(64, row, blk, l);
+                *reinterpret_cast<uint2*>(o.pf_kh + img + off) =
+                    make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+                *reinterpret_cast<uint2*>(o.pf_kl + img + off) =
+                    make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = (i < 4 ? 4 * l : 64 + 4 * l) + (i & 3);
+                *reinterpret_cast<uint16_t*>(o.pf_vt + img + hsq_tc::sw128_elem(d, row)) =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(x[i]));
+            }
+        }
+    }
 
     if (is_l1 && slot < c.max_l1) {
         const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
@@ -832,6 +862,60 @@ hsq_status check_common(hsq_ctx* ctx, const hsq_cache* cache) {
     return HSQ_OK;
 }
 
+// Encode of a layer (hsq_encode); with pf, also the prefill's K/V operand images.
+hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const void* V, hsq_dtype dtype,
+                      cudaStream_t s, const hsq::PrefillImages* pf) {
+    hsq_status st = check_common(ctx, cache);
+    if (st != HSQ_OK) return st;
+    if (!K || !V) return fail(ctx, HSQ_ERR_INVALID, "K or V is NULL");
+    if (dtype != HSQ_DTYPE_F32 && dtype != HSQ_DTYPE_BF16) return fail(ctx, HSQ_ERR_INVALID, "bad dtype");
+    cudaPointerAttributes pa;
+    HSQ_CUDA(ctx, cudaPointerGetAttributes(&pa, cache->l3));
+    const bool on_host = pa.type == cudaMemoryTypeHost;
+    if (on_host != (cache->l3_on_host != 0))
+        return fail(ctx, HSQ_ERR_INVALID, "l3 location does not match l3_on_host");
+    if (on_host && pa.devicePointer != (void*)cache->l3)
+        return fail(ctx, HSQ_ERR_INVALID, "host l3 is not mapped at the same address on the device");
+    CacheView v = make_view(ctx, cache);
+    if (pf && (size_t)v.G * v.N < (size_t)pf->nkt * 64) {
+        // key rows past the encode's groups: the attention reads them as zeros
+        HSQ_CUDA(ctx, cudaMemsetAsync(pf->kh, 0, pf->bytes - (size_t)(pf->kh - pf->qh), s));
+    }
+    l1_index_kernel<<<v.B, 1024, 0, s>>>(v, cache->l1_pos, cache->l1_count, ctx->d_prefix, ctx->d_err);
+    const bool grow = ctx->cfg.l1_recent > 0 && cache->win_kv && cache->gsum;
+    EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
+                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix,
+                grow ? cache->win_kv : nullptr, grow ? cache->gsum : nullptr, ctx->cfg.l1_recent,
+                pf ? pf->kh : nullptr, pf ? pf->kl : nullptr, pf ? pf->vt : nullptr, pf ? pf->nkt : 0};
+    dim3 grid(v.G, v.Hkv, v.B);
+    const Tables tb = make_tables(ctx);
+    using EncodeFn = void (*)(CacheView, EncodeOut, const void*, const void*, Tables);
+    const bool bf = dtype == HSQ_DTYPE_BF16;
+    EncodeFn fn;  // the variant of the block size, input type and codec
+    if (pf) {     // prefill: bf16 inputs
+        if (v.N == 16) fn = v.rot ? encode_kernel<16, true, true, true> : encode_kernel<16, true, false, true>;
+        else fn = v.rot ? encode_kernel<8, true, true, true> : encode_kernel<8, true, false, true>;
+    } else if (v.N == 16) {
+        fn = v.rot ? (bf ? encode_kernel<16, true, true> : encode_kernel<16, false, true>)
+                   : (bf ? encode_kernel<16, true, false> : encode_kernel<16, false, false>);
+    } else {
+        fn = v.rot ? (bf ? encode_kernel<8, true, true> : encode_kernel<8, false, true>)
+                   : (bf ? encode_kernel<8, true, false> : encode_kernel<8, false, false>);
+    }
+    fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
+    if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
+        const SketchOut so{cache->qjl_s, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
+        if (v.N == 16) {
+            if (bf) qjl_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
+        } else {
+            if (bf) qjl_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
+        }
+    }
+    return after_launch(ctx, "encode");
+}
+
 void free_ctx(hsq_ctx* c) {
     cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
     cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err);
@@ -906,47 +990,37 @@ hsq_status hsq_destroy(hsq_ctx* ctx) {
 
 hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const void* V,
                       hsq_dtype dtype, hsq_stream_t stream) {
-    hsq_status st = check_common(ctx, cache);
-    if (st != HSQ_OK) return st;
-    if (!K || !V) return fail(ctx, HSQ_ERR_INVALID, "K or V is NULL");
-    if (dtype != HSQ_DTYPE_F32 && dtype != HSQ_DTYPE_BF16) return fail(ctx, HSQ_ERR_INVALID, "bad dtype");
-    cudaPointerAttributes pa;
-    HSQ_CUDA(ctx, cudaPointerGetAttributes(&pa, cache->l3));
-    const bool on_host = pa.type == cudaMemoryTypeHost;
-    if (on_host != (cache->l3_on_host != 0))
-        return fail(ctx, HSQ_ERR_INVALID, "l3 location does not match l3_on_host");
-    if (on_host && pa.devicePointer != (void*)cache->l3)
-        return fail(ctx, HSQ_ERR_INVALID, "host l3 is not mapped at the same address on the device");
+    return encode_run(ctx, cache, K, V, dtype, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+hsq_status hsq_prefill_workspace_size(const hsq_ctx* ctx, int B, int T, size_t* bytes) {
+    if (!ctx || !bytes) return fail(nullptr, HSQ_ERR_INVALID, "ctx or bytes is NULL");
+    if (B < 1 || T < 1) return fail(nullptr, HSQ_ERR_INVALID, "B and T must be positive");
+    *bytes = hsq::prefill_images(nullptr, B, ctx->cfg.n_q_heads, ctx->cfg.n_kv_heads, T).bytes;
+    return HSQ_OK;
+}
+
+hsq_status hsq_prefill(hsq_ctx* ctx, const hsq_cache* cache, const void* Q, const void* K, const void* V, int B,
+                       int T, float* out, void* workspace, size_t workspace_bytes, hsq_stream_t stream) {
+    if (!ctx) return fail(nullptr, HSQ_ERR_INVALID, "context is NULL");
+    if (!Q || !K || !V || !out || !workspace) return fail(ctx, HSQ_ERR_INVALID, "Q, K, V, out or workspace is NULL");
+    if (B < 1 || T < 1 || B > ctx->cfg.max_batch || T > ctx->cfg.max_pos)
+        return fail(ctx, HSQ_ERR_INVALID, "B or T outside the context's limits (max_batch, max_pos)");
+    if (cache && (cache->B != B || cache->T != T)) return fail(ctx, HSQ_ERR_INVALID, "cache B / T differ from B / T");
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return fail(ctx, HSQ_ERR_INVALID, "workspace must be 256-byte aligned");
+    const hsq::PrefillImages im = hsq::prefill_images(workspace, B, ctx->cfg.n_q_heads, ctx->cfg.n_kv_heads, T);
+    if (workspace_bytes < im.bytes) return fail(ctx, HSQ_ERR_INVALID, "workspace smaller than hsq_prefill_workspace_size");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    CacheView v = make_view(ctx, cache);
-    l1_index_kernel<<<v.B, 1024, 0, s>>>(v, cache->l1_pos, cache->l1_count, ctx->d_prefix, ctx->d_err);
-    const bool grow = ctx->cfg.l1_recent > 0 && cache->win_kv && cache->gsum;
-    EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
-                cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix,
-                grow ? cache->win_kv : nullptr, grow ? cache->gsum : nullptr, ctx->cfg.l1_recent};
-    dim3 grid(v.G, v.Hkv, v.B);
-    const Tables tb = make_tables(ctx);
-    using EncodeFn = void (*)(CacheView, EncodeOut, const void*, const void*, Tables);
-    const bool bf = dtype == HSQ_DTYPE_BF16;
-    EncodeFn fn;  // the variant of the block size, input type and codec
-    if (v.N == 16)
-        fn = v.rot ? (bf ? encode_kernel<16, true, true> : encode_kernel<16, false, true>)
-                   : (bf ? encode_kernel<16, true, false> : encode_kernel<16, false, false>);
-    else
-        fn = v.rot ? (bf ? encode_kernel<8, true, true> : encode_kernel<8, false, true>)
-                   : (bf ? encode_kernel<8, true, false> : encode_kernel<8, false, false>);
-    fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
-    if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
-        const SketchOut so{cache->qjl_s, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
-        if (v.N == 16) {
-            if (bf) qjl_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
-        } else {
-            if (bf) qjl_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
-        }
+    hsq_status st;
+    if (cache) {
+        st = encode_run(ctx, cache, K, V, HSQ_DTYPE_BF16, s, &im);  // the encode writes the K/V operands
+    } else {
+        st = hsq::prefill_prep_kv(ctx, im, K, V, B, T, s);
     }
-    return after_launch(ctx, "encode");
+    if (st != HSQ_OK) return st;
+    if ((st = hsq::prefill_prep_q(ctx, im, Q, B, T, s)) != HSQ_OK) return st;
+    return hsq::prefill_attention(ctx, im, out, B, T, s);
 }
 
 hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void* v, hsq_dtype dtype,

@@ -1,0 +1,384 @@
+// Prefill: the prompt's dense causal attention on the tensor cores.
+//
+// "Tamarin (HSQ)" technical summary, section 4 (results): compressing the
+// prompt's K/V costs a prefill overhead of 1.2-1.3x at 32K.  The prompt's
+// attention itself is the model's ordinary causal softmax attention over
+// RoPE'd queries and keys (GQA, scale 1/sqrt(d)); HSQ only decides what is
+// kept for decoding.  hsq_prefill runs the encode of K/V (hsq_encode's
+// kernel, which then also writes the attention's K/V operands, so K/V are
+// read once) and this attention.
+//
+// Operands.  Queries and keys are RoPE'd in fp32 and each split into two
+// bf16 terms x = hi + lo; logits use hi.hi + lo.hi + hi.lo (three MMAs, the
+// dropped lo.lo term is below 2^-16 of the product), probabilities p =
+// ph + pl multiply the bf16 values (exact: the inputs are bf16).  So the
+// tensor cores give fp32-level logits and outputs.  Every operand tile is
+// stored in global memory as the exact shared-memory image the MMA reads
+// (K-major, 128-byte swizzle), so one 1-D bulk copy per tile fills shared
+// memory:
+//   Q  [B][Hq][ceil(T/128)] images of 128 rows x 128 dims (hi and lo, 32 KB each)
+//   K  [B][Hkv][2 ceil(T/128)] images of 64 rows x 128 dims (hi and lo, 16 KB each)
+//   Vt [B][Hkv][2 ceil(T/128)] images of 128 dims x 64 keys (16 KB), V transposed
+//      so that it is the K-major B operand of P V.
+// Rows past T are zero.
+//
+// Attention kernel: one CTA of 128 threads per (128-query tile, query head,
+// sequence); thread i owns query row i, which is TMEM lane i.  Per 64-key
+// tile (up to the diagonal): thread 0 waits for the tile's bulk copies and
+// issues S = Q K^T (128 x 64, fp32 in TMEM columns 0-63); every thread
+// reads its row of S, applies the causal mask and the online softmax (log2
+// domain; the running maximum is raised only when a logit exceeds it by
+// more than 8, then the O row in TMEM is rescaled), writes its row of P
+// (hi, lo) to shared memory; thread 0 issues O += P V (128 x 128, TMEM
+// columns 128-255) and, once it completed, refills the tile's stage with
+// the tile two ahead.  The output is O / l in fp32.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "hsq_ctx.h"
+#include "hsq_device.cuh"
+#include "hsq_tc.cuh"
+
+namespace {
+
+using namespace hsq_tc;
+
+constexpr int kPfRows = 128;                          // query rows per CTA (TMEM lanes)
+constexpr int kPfKeys = 64;                           // keys per tile
+constexpr int kPfThreads = 128;
+constexpr uint32_t kQImg = kPfRows * kDim * 2;        // 32 KB
+constexpr uint32_t kKImg = kPfKeys * kDim * 2;        // 16 KB
+constexpr uint32_t kVImg = kDim * kPfKeys * 2;        // 16 KB
+constexpr uint32_t kPImg = kPfRows * kPfKeys * 2;     // 16 KB
+constexpr uint32_t kStageBytes = 2 * kKImg + kVImg;   // Kh | Kl | Vt
+constexpr int kStages = 2;
+constexpr uint32_t kOffQh = 0, kOffQl = kQImg, kOffStage = 2 * kQImg;
+constexpr uint32_t kOffPh = kOffStage + kStages * kStageBytes, kOffPl = kOffPh + kPImg;
+constexpr uint32_t kOffBar = kOffPl + kPImg;          // q, kv[0], kv[1], mma barriers; TMEM address
+constexpr uint32_t kPfSmem = kOffBar + 64 + 1024;     // + slack to align the base to 1024 bytes
+constexpr uint32_t kTmemCols = 256;                   // S: columns 0-63, O: 128-255
+
+struct PrefillArgs {
+    const uint8_t* qh; const uint8_t* ql; const uint8_t* kh; const uint8_t* kl; const uint8_t* vt;
+    float* out;  // [B][Hq][T][128]
+    int* err;
+    int Hq, Hkv, T, nqt, nkt;
+};
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs a) {
+    extern __shared__ uint8_t pf_raw[];
+    __shared__ int s_abort;
+    const uint32_t raw = smem_addr(pf_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = pf_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int qt = a.nqt - 1 - (int)blockIdx.x;  // the longest rows first
+    const int j = blockIdx.y, b = blockIdx.z;
+    const int h = j / (a.Hq / a.Hkv);
+    const uint32_t bar_q = base + kOffBar, bar_kv = bar_q + 8, bar_mma = bar_q + 24, slot = bar_q + 32;
+
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        mbar_init(bar_kv, 1);
+        mbar_init(bar_kv + 8, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+        s_abort = 0;
+    }
+    if (warp == 0) {
+        tmem_alloc(slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 32);
+    const uint32_t tS = tmem, tO = tmem + 128;
+    const uint32_t lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+
+    const int nkv = 2 * qt + 2;  // key tiles up to the diagonal
+    const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
+    auto load_kv = [&](int kt, int st) {
+        const uint32_t dst = base + kOffStage + st * kStageBytes, bar = bar_kv + 8 * st;
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_g2s(dst, a.kh + (kv0 + kt) * kKImg, kKImg, bar);
+        bulk_g2s(dst + kKImg, a.kl + (kv0 + kt) * kKImg, kKImg, bar);
+        bulk_g2s(dst + 2 * kKImg, a.vt + (kv0 + kt) * kVImg, kVImg, bar);
+    };
+    if (tid == 0) {
+        const size_t qi = ((size_t)b * a.Hq + j) * a.nqt + qt;
+        mbar_expect_tx(bar_q, 2 * kQImg);
+        bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
+        bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
+        load_kv(0, 0);
+        if (nkv > 1) load_kv(1, 1);
+    }
+
+    const int t = qt * kPfRows + tid;  // this thread's query position
+    float m_used = -INFINITY, lsum = 0.f;
+    uint32_t ph_mma = 0;
+    constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys), idO = idesc_bf16_f32(kPfRows, kDim);
+#pragma unroll 1
+    for (int kt = 0; kt < nkv; ++kt) {
+        const int st = kt & 1;
+        const uint32_t stage = base + kOffStage + st * kStageBytes;
+        if (tid == 0) {
+            bool okw = (kt > 0 || mbar_wait(bar_q, 0)) && mbar_wait(bar_kv + 8 * st, (kt >> 1) & 1);
+            if (okw) {
+                tc_fence_after();
+                // S = Qh Kh^T + Ql Kh^T + Qh Kl^T over the 128 dims (8 slices of 16)
+#pragma unroll 1
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t qo = (k >> 2) * (kQImg / 2) + (k & 3) * 32;
+                    const uint32_t ko = (k >> 2) * (kKImg / 2) + (k & 3) * 32;
+                    const uint64_t dqh = sw128_desc(base + kOffQh + qo), dql = sw128_desc(base + kOffQl + qo);
+                    const uint64_t dkh = sw128_desc(stage + ko), dkl = sw128_desc(stage + kKImg + ko);
+                    mma_bf16(tS, dqh, dkh, idS, k > 0);
+                    mma_bf16(tS, dql, dkh, idS, 1);
+                    mma_bf16(tS, dqh, dkl, idS, 1);
+                }
+                mma_commit(bar_mma);
+                okw = mbar_wait(bar_mma, ph_mma);
+            }
+            if (!okw) {
+                s_abort = 1;
+                atomicOr(a.err, HSQ_DEVERR_WAIT);
+            }
+        }
+        ph_mma ^= 1u;
+        __syncthreads();
+        if (s_abort) break;
+        tc_fence_after();
+
+        // this row of S: scaled logits (log2 domain), causal mask
+        float x[64];
+        {
+            float v[32];
+            tmem_ld32(tS + lane, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] = v[c];
+            tmem_ld32(tS + lane + 32, v);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
+        }
+        const int key0 = kt * kPfKeys;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            x[c] = key0 + c <= t ? x[c] * kLogitScaleLog2 : -INFINITY;
+            mt = fmaxf(mt, x[c]);
+        }
+        const float m_new = fmaxf(m_used, mt);
+        const bool raise = m_new > m_used + 8.f;  // (always on the first tile: key 0 is unmasked)
+        const float alpha = raise ? (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new)) : 1.f;
+        if (raise) {
+            lsum *= alpha;
+            m_used = m_new;
+        }
+        if (kt > 0 && __any_sync(0xffffffffu, raise)) {  // rescale this warp's rows of O (TMEM)
+#pragma unroll 1
+            for (int c0 = 0; c0 < kDim; c0 += 32) {
+                float o[32];
+                tmem_ld32(tO + lane + c0, o);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                tmem_st32(tO + lane + c0, o);
+            }
+        }
+        // P = exp2(x - m) as bf16 hi + lo, this thread's row of the two P images
+        float psum = 0.f;
+        uint8_t* prow_h = gbase + kOffPh + tid * 128;
+        uint8_t* prow_l = gbase + kOffPl + tid * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float p0 = exp2f(x[8 * c8 + 2 * e] - m_used), p1 = exp2f(x[8 * c8 + 2 * e + 1] - m_used);
+                psum += p0 + p1;
+                uint16_t h0, l0, h1, l1;
+                split_bf16(p0, h0, l0);
+                split_bf16(p1, h1, l1);
+                wh[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                wl[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+            }
+            const uint32_t off = (uint32_t)((c8 ^ (tid & 7)) << 4);
+            *reinterpret_cast<uint4*>(prow_h + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(prow_l + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+        lsum += psum;
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // O += Ph V + Pl V over the 64 keys (4 slices of 16)
+#pragma unroll 1
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t dv = sw128_desc(stage + 2 * kKImg + k * 32);
+                mma_bf16(tO, sw128_desc(base + kOffPh + k * 32), dv, idO, (kt > 0) | (k > 0));
+                mma_bf16(tO, sw128_desc(base + kOffPl + k * 32), dv, idO, 1);
+            }
+            mma_commit(bar_mma);
+            if (mbar_wait(bar_mma, ph_mma)) {
+                if (kt + 2 < nkv) load_kv(kt + 2, st);  // the stage is free again
+            } else {
+                s_abort = 1;
+                atomicOr(a.err, HSQ_DEVERR_WAIT);
+            }
+        }
+        ph_mma ^= 1u;
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+        tc_fence_after();
+    }
+
+    if (!s_abort) {
+        tc_fence_after();
+        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+        float* orow = a.out + (((size_t)b * a.Hq + j) * a.T + (t < a.T ? t : 0)) * kDim;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kDim; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + lane + c0, o);
+            if (t < a.T) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4*>(orow + c0 + c) =
+                        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Query operand images: RoPE at the query's position in fp32, split into
+// bf16 hi + lo.  One CTA of 256 threads per (128-row tile, query head,
+// sequence); each half-warp handles 8 rows.
+__global__ void __launch_bounds__(256) prefill_q_kernel(const uint16_t* __restrict__ Q, uint8_t* qh, uint8_t* ql,
+                                                        int Hq, int T, int nqt, Tables tb) {
+    const int qt = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const size_t img = (((size_t)b * Hq + j) * nqt + qt) * kQImg;
+#pragma unroll 1
+    for (int r = hw; r < kPfRows; r += 16) {
+        const int t = qt * kPfRows + r;
+        float x[8];
+        if (t < T) {
+            load_bf16x8(Q + (((size_t)b * Hq + j) * T + t) * kDim, x);
+            rope(x, t, tb);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) split_bf16(x[4 * blk + k], hi[k], lo[k]);
+            const uint32_t off = sw128_row_quad(kPfRows, r, blk, l);
+            *reinterpret_cast<uint2*>(qh + img + off) =
+                make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+            *reinterpret_cast<uint2*>(ql + img + off) =
+                make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+        }
+    }
+}
+
+// Key and value operand images without the encode (attention on its own):
+// one CTA of 256 threads per (64-key tile, KV head, sequence); half-warps
+// take the tile's keys (RoPE'd, split) and values (transposed) in turn.
+__global__ void __launch_bounds__(256) prefill_kv_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V,
+                                                         uint8_t* kh, uint8_t* kl, uint8_t* vt, int Hkv, int T, int nkt,
+                                                         Tables tb) {
+    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hw = threadIdx.x >> 4, l = hlane();
+    const size_t img = (((size_t)b * Hkv + h) * nkt + kt) * kKImg;
+#pragma unroll 1
+    for (int r = hw; r < 2 * kPfKeys; r += 16) {
+        const int row = r & (kPfKeys - 1), t = kt * kPfKeys + row;
+        const bool val = r >= kPfKeys;
+        float x[8];
+        if (t < T) {
+            load_bf16x8((val ? V : K) + (((size_t)b * Hkv + h) * T + t) * kDim, x);
+            if (!val) rope(x, t, tb);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        if (!val) {
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+                uint16_t hi[4], lo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) split_bf16(x[4 * blk + k], hi[k], lo[k]);
+                const uint32_t off = sw128_row_quad(kPfKeys, row, blk, l);
+                *reinterpret_cast<uint2*>(kh + img + off) =
+                    make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+                *reinterpret_cast<uint2*>(kl + img + off) =
+                    make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int d = (i < 4 ? 4 * l : 64 + 4 * l) + (i & 3);
+                *reinterpret_cast<uint16_t*>(vt + img + sw128_elem(d, row)) =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(x[i]));
+            }
+        }
+    }
+}
+
+}  // namespace
+
+namespace hsq {
+
+PrefillImages prefill_images(void* ws, int B, int Hq, int Hkv, int T) {
+    PrefillImages im{};
+    im.nqt = (T + kPfRows - 1) / kPfRows;
+    im.nkt = 2 * im.nqt;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    const size_t q = (size_t)B * Hq * im.nqt * kQImg, k = (size_t)B * Hkv * im.nkt * kKImg;
+    im.qh = p;
+    im.ql = p + q;
+    im.kh = p + 2 * q;
+    im.kl = p + 2 * q + k;
+    im.vt = p + 2 * q + 2 * k;
+    im.bytes = 2 * q + 3 * k;
+    return im;
+}
+
+hsq_status prefill_prep_q(hsq_ctx* ctx, const PrefillImages& im, const void* Q, int B, int T, cudaStream_t st) {
+    const dim3 grid(im.nqt, ctx->cfg.n_q_heads, B);
+    prefill_q_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(Q), im.qh, im.ql, ctx->cfg.n_q_heads, T,
+                                           im.nqt, make_tables(ctx));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? HSQ_OK : cuda_fail(ctx, e, "prefill_q_kernel");
+}
+
+hsq_status prefill_prep_kv(hsq_ctx* ctx, const PrefillImages& im, const void* K, const void* V, int B, int T,
+                           cudaStream_t st) {
+    const dim3 grid(im.nkt, ctx->cfg.n_kv_heads, B);
+    prefill_kv_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V), im.kh,
+                                            im.kl, im.vt, ctx->cfg.n_kv_heads, T, im.nkt, make_tables(ctx));
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? HSQ_OK : cuda_fail(ctx, e, "prefill_kv_kernel");
+}
+
+hsq_status prefill_attention(hsq_ctx* ctx, const PrefillImages& im, float* out, int B, int T, cudaStream_t st) {
+    const void* fn = (const void*)prefill_attn_kernel;
+    cudaError_t e = raise_smem_limit(fn, ctx->device, kPfSmem);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(prefill)");
+    PrefillArgs a{im.qh, im.ql, im.kh, im.kl, im.vt, out, ctx->d_err, ctx->cfg.n_q_heads, ctx->cfg.n_kv_heads, T,
+                  im.nqt, im.nkt};
+    const dim3 grid(im.nqt, ctx->cfg.n_q_heads, B);
+    prefill_attn_kernel<<<grid, kPfThreads, kPfSmem, st>>>(a);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? HSQ_OK : cuda_fail(ctx, e, "prefill_attn_kernel");
+}
+
+}  // namespace hsq

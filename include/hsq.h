@@ -77,8 +77,9 @@ enum {
     HSQ_DEVERR_SEL = 1,       /* selection entry out of range or not ascending: treated as -1 */
     HSQ_DEVERR_POS = 2,       /* position outside [0, max_pos): clamped */
     HSQ_DEVERR_L1_OVER = 4,   /* more L1 tokens than max_l1: extra tokens dropped from L1 */
-    HSQ_DEVERR_WAIT = 8,      /* reserved: no kernel of this version waits on another CTA
-                                 outside its own thread-block cluster */
+    HSQ_DEVERR_WAIT = 8,      /* a bounded wait of the prefill attention kernel (on its bulk
+                                 copies or its tensor-core work) ran out: its output is not
+                                 written */
     HSQ_DEVERR_GROW = 16      /* hsq_append: the token leaving the recent window was not in L1
                                  (the cache was not encoded with that window): L1 left as is */
 };
@@ -396,6 +397,33 @@ hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  *   *device_word when it is not NULL), HSQ_ERR_CUDA on a CUDA error.
  */
 hsq_status hsq_sync_status(hsq_ctx* ctx, hsq_stream_t stream, int* device_word);
+
+/*
+ * hsq_prefill -- a prompt's prefill with HSQ: the dense causal attention of
+ *   the prompt and, when cache is not NULL, the encode of its K/V into the
+ *   cache ("Tamarin (HSQ)" technical summary, section 4, results: the prefill
+ *   overhead of compressing the prompt).  The attention is the model's
+ *   ordinary one: out[b, j, t] = sum over s <= t of
+ *   softmax_s(RoPE(q_{j,t}, t) . RoPE(k_{h,s}, s) / sqrt(128)) v_{h,s},
+ *   h = j / (Hq / Hkv), computed on the tensor cores with fp32-level
+ *   accuracy (queries, keys and probabilities split into two bf16 terms).
+ *   With a cache, the encode is hsq_encode's (the same codes) and the same
+ *   pass over K/V writes the attention's key and value operands, so K/V are
+ *   read once.  With cache NULL only the attention runs.
+ *   Q: [B, Hq, T, 128] bf16 pre-RoPE queries at positions 0..T-1; K, V:
+ *   [B, Hkv, T, 128] bf16 pre-RoPE keys and values (device memory); out:
+ *   [B, Hq, T, 128] float32 (device).  workspace: device memory of at least
+ *   hsq_prefill_workspace_size bytes, 256-byte aligned, caller-owned, holding
+ *   the operand images between the calls' kernels (its contents are not
+ *   needed afterwards).  B <= max_batch, T <= max_pos; with a cache, B and T
+ *   equal the cache's.  Asynchronous on `stream`.  Errors: HSQ_ERR_INVALID
+ *   (NULL pointers, sizes, alignment, a small workspace, L3 placement as for
+ *   hsq_encode), HSQ_ERR_CUDA.  A bounded wait inside the attention kernel
+ *   that runs out sets HSQ_DEVERR_WAIT (hsq_sync_status).
+ */
+hsq_status hsq_prefill_workspace_size(const hsq_ctx* ctx, int B, int T, size_t* bytes);
+hsq_status hsq_prefill(hsq_ctx* ctx, const hsq_cache* cache, const void* Q, const void* K, const void* V, int B,
+                       int T, float* out, void* workspace, size_t workspace_bytes, hsq_stream_t stream);
 
 /*
  * hsq_route_noalloc -- hsq_route for callers that cannot allocate device memory.
