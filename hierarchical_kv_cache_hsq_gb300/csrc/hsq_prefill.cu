@@ -22,16 +22,19 @@
 //      so that it is the K-major B operand of P V.
 // Rows past T are zero.
 //
-// Attention kernel: one CTA of 128 threads per (128-query tile, query head,
-// sequence); thread i owns query row i, which is TMEM lane i.  Per 64-key
+// Attention kernel: one CTA of 256 threads per (128-query tile, query head,
+// sequence).  Query row r of the tile is TMEM lane r; warp w reads lanes
+// 32 (w & 3) .. + 31 (a warp can only reach its quarter of the lanes) and
+// the half w >> 2 of the columns, so two threads share a row.  Per 64-key
 // tile (up to the diagonal): thread 0 waits for the tile's bulk copies and
 // issues S = Q K^T (128 x 64, fp32 in TMEM columns 0-63); every thread
-// reads its row of S, applies the causal mask and the online softmax (log2
-// domain; the running maximum is raised only when a logit exceeds it by
-// more than 8, then the O row in TMEM is rescaled), writes its row of P
-// (hi, lo) to shared memory; thread 0 issues O += P V (128 x 128, TMEM
-// columns 128-255) and, once it completed, refills the tile's stage with
-// the tile two ahead.  The output is O / l in fp32.
+// reads its 32 logits of S, applies the causal mask and the online softmax
+// (log2 domain; the two halves of a row exchange their maxima through
+// shared memory; the running maximum is raised only when a logit exceeds
+// it by more than 8, then the row's O in TMEM is rescaled), writes its half
+// row of P (hi, lo) to shared memory; thread 0 issues O += P V (128 x 128,
+// TMEM columns 128-255) and, once it completed, refills the tile's stage
+// with the tile two ahead.  The output is O / l in fp32.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -46,7 +49,7 @@ using namespace hsq_tc;
 
 constexpr int kPfRows = 128;                          // query rows per CTA (TMEM lanes)
 constexpr int kPfKeys = 64;                           // keys per tile
-constexpr int kPfThreads = 128;
+constexpr int kPfThreads = 256;
 constexpr uint32_t kQImg = kPfRows * kDim * 2;        // 32 KB
 constexpr uint32_t kKImg = kPfKeys * kDim * 2;        // 16 KB
 constexpr uint32_t kVImg = kDim * kPfKeys * 2;        // 16 KB
@@ -69,11 +72,14 @@ struct PrefillArgs {
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs a) {
     extern __shared__ uint8_t pf_raw[];
     __shared__ int s_abort;
+    __shared__ float s_mx[2][kPfRows];   // per column half: the row's tile maximum
     const uint32_t raw = smem_addr(pf_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = pf_raw + (base - raw);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int qt = a.nqt - 1 - (int)blockIdx.x;  // the longest rows first
+    const int tid = threadIdx.x, warp = tid >> 5, lanei = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = 32 * quarter + lanei;          // query row of the tile = TMEM lane
+    const int qt = a.nqt - 1 - (int)blockIdx.x;    // the longest rows first
     const int j = blockIdx.y, b = blockIdx.z;
     const int h = j / (a.Hq / a.Hkv);
     const uint32_t bar_q = base + kOffBar, bar_kv = bar_q + 8, bar_mma = bar_q + 24, slot = bar_q + 32;
@@ -94,8 +100,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 32);
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+    const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+    const uint32_t tS = tmem + lanes + 32 * half;           // this thread's 32 columns of S
+    const uint32_t tO = tmem + lanes + 128 + 64 * half;     // and its 64 columns of O
 
     const int nkv = 2 * qt + 2;  // key tiles up to the diagonal
     const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
@@ -115,7 +122,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         if (nkv > 1) load_kv(1, 1);
     }
 
-    const int t = qt * kPfRows + tid;  // this thread's query position
+    const int t = qt * kPfRows + row;  // this thread's query position
     float m_used = -INFINITY, lsum = 0.f;
     uint32_t ph_mma = 0;
     constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys), idO = idesc_bf16_f32(kPfRows, kDim);
@@ -134,9 +141,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                     const uint32_t ko = (k >> 2) * (kKImg / 2) + (k & 3) * 32;
                     const uint64_t dqh = sw128_desc(base + kOffQh + qo), dql = sw128_desc(base + kOffQl + qo);
                     const uint64_t dkh = sw128_desc(stage + ko), dkl = sw128_desc(stage + kKImg + ko);
-                    mma_bf16(tS, dqh, dkh, idS, k > 0);
-                    mma_bf16(tS, dql, dkh, idS, 1);
-                    mma_bf16(tS, dqh, dkl, idS, 1);
+                    mma_bf16(tmem, dqh, dkh, idS, k > 0);
+                    mma_bf16(tmem, dql, dkh, idS, 1);
+                    mma_bf16(tmem, dqh, dkl, idS, 1);
                 }
                 mma_commit(bar_mma);
                 okw = mbar_wait(bar_mma, ph_mma);
@@ -151,59 +158,53 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         if (s_abort) break;
         tc_fence_after();
 
-        // this row of S: scaled logits (log2 domain), causal mask
-        float x[64];
-        {
-            float v[32];
-            tmem_ld32(tS + lane, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[c] = v[c];
-            tmem_ld32(tS + lane + 32, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
-        }
-        const int key0 = kt * kPfKeys;
+        // this thread's 32 logits of the row (log2 domain), causal mask
+        float x[32];
+        tmem_ld32(tS, x);
+        const int key0 = kt * kPfKeys + 32 * half;
         float mt = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 32; ++c) {
             x[c] = key0 + c <= t ? x[c] * kLogitScaleLog2 : -INFINITY;
             mt = fmaxf(mt, x[c]);
         }
+        s_mx[half][row] = mt;
+        __syncthreads();
+        mt = fmaxf(mt, s_mx[half ^ 1][row]);
         const float m_new = fmaxf(m_used, mt);
         const bool raise = m_new > m_used + 8.f;  // (always on the first tile: key 0 is unmasked)
-        const float alpha = raise ? (m_used == -INFINITY ? 0.f : exp2f(m_used - m_new)) : 1.f;
+        const float alpha = raise ? (m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new)) : 1.f;
         if (raise) {
             lsum *= alpha;
             m_used = m_new;
         }
-        if (kt > 0 && __any_sync(0xffffffffu, raise)) {  // rescale this warp's rows of O (TMEM)
+        if (kt > 0 && __any_sync(0xffffffffu, raise)) {  // rescale this thread's half row of O (TMEM)
 #pragma unroll 1
-            for (int c0 = 0; c0 < kDim; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 float o[32];
-                tmem_ld32(tO + lane + c0, o);
+                tmem_ld32(tO + c0, o);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                tmem_st32(tO + lane + c0, o);
+                tmem_st32(tO + c0, o);
             }
         }
-        // P = exp2(x - m) as bf16 hi + lo, this thread's row of the two P images
+        // P = exp2(x - m) as bf16 hi + lo: this thread's 4 chunks of its row of the P images
         float psum = 0.f;
-        uint8_t* prow_h = gbase + kOffPh + tid * 128;
-        uint8_t* prow_l = gbase + kOffPl + tid * 128;
+        uint8_t* prow_h = gbase + kOffPh + row * 128;
+        uint8_t* prow_l = gbase + kOffPl + row * 128;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int cc = 0; cc < 4; ++cc) {
             uint32_t wh[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float p0 = exp2f(x[8 * c8 + 2 * e] - m_used), p1 = exp2f(x[8 * c8 + 2 * e + 1] - m_used);
+                const float p0 = ex2_approx(x[8 * cc + 2 * e] - m_used), p1 = ex2_approx(x[8 * cc + 2 * e + 1] - m_used);
                 psum += p0 + p1;
-                uint16_t h0, l0, h1, l1;
-                split_bf16(p0, h0, l0);
-                split_bf16(p1, h1, l1);
-                wh[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                wl[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+                const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
+                const __nv_bfloat162 lp = __floats2bfloat162_rn(p0 - __low2float(hp), p1 - __high2float(hp));
+                wh[e] = *reinterpret_cast<const uint32_t*>(&hp);
+                wl[e] = *reinterpret_cast<const uint32_t*>(&lp);
             }
-            const uint32_t off = (uint32_t)((c8 ^ (tid & 7)) << 4);
+            const uint32_t off = (uint32_t)(((4 * half + cc) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(prow_h + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
             *reinterpret_cast<uint4*>(prow_l + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
@@ -217,8 +218,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
 #pragma unroll 1
             for (int k = 0; k < 4; ++k) {
                 const uint64_t dv = sw128_desc(stage + 2 * kKImg + k * 32);
-                mma_bf16(tO, sw128_desc(base + kOffPh + k * 32), dv, idO, (kt > 0) | (k > 0));
-                mma_bf16(tO, sw128_desc(base + kOffPl + k * 32), dv, idO, 1);
+                mma_bf16(tmem + 128, sw128_desc(base + kOffPh + k * 32), dv, idO, (kt > 0) | (k > 0));
+                mma_bf16(tmem + 128, sw128_desc(base + kOffPl + k * 32), dv, idO, 1);
             }
             mma_commit(bar_mma);
             if (mbar_wait(bar_mma, ph_mma)) {
@@ -235,14 +236,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         tc_fence_after();
     }
 
+    // the row's sum: this half's plus the other half's (same rescalings)
+    s_mx[half][row] = lsum;
+    __syncthreads();
     if (!s_abort) {
         tc_fence_after();
-        const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-        float* orow = a.out + (((size_t)b * a.Hq + j) * a.T + (t < a.T ? t : 0)) * kDim;
+        const float l = lsum + s_mx[half ^ 1][row];
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        float* orow = a.out + (((size_t)b * a.Hq + j) * a.T + (t < a.T ? t : 0)) * kDim + 64 * half;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kDim; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
             float o[32];
-            tmem_ld32(tO + lane + c0, o);
+            tmem_ld32(tO + c0, o);
             if (t < a.T) {
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)

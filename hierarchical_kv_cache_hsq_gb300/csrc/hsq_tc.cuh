@@ -152,6 +152,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         : "memory");
 }
 
+// 2^x by the special-function unit (relative error about 2^-22); -inf gives 0
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- operand images --------------------------------------------------------
 
 // byte offset of dims [4 * l, 4 * l + 4) (block 0) or [64 + 4 l, ...) (block 1)
