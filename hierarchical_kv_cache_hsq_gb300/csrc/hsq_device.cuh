@@ -538,13 +538,11 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     // count, max and min of the non-empty keys
     int ne = 0;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    if (stats) {
-#pragma unroll 1
-        for (int r = 0; r < nstats; ++r) {
-            ne += (int)stats[4 * r];
-            hi = max(hi, stats[4 * r + 1]);
-            lo = min(lo, stats[4 * r + 2]);
-        }
+    if (stats) {  // lane r reads part r (nstats <= 32)
+        const bool mine = lane < nstats;
+        ne = __reduce_add_sync(kFull, mine ? (int)stats[4 * lane] : 0);
+        hi = __reduce_max_sync(kFull, mine ? stats[4 * lane + 1] : 0u);
+        lo = __reduce_min_sync(kFull, mine ? stats[4 * lane + 2] : 0xFFFFFFFFu);
     } else {
         int cn = 0;
         uint32_t mx = 0u, mn = 0xFFFFFFFFu;
@@ -684,11 +682,11 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                     const uint32_t ck = lane < bcnt ? ss.cand_key[lane] : 0u;
                     const int cg = lane < bcnt ? ss.cand_g[lane] : 0x7FFFFFFF;
                     int rank = 0;
-#pragma unroll 1
-                    for (int j = 0; j < bcnt; ++j) {
-                        const uint32_t kj = __shfl_sync(kFull, ck, j);
-                        const int gj = __shfl_sync(kFull, cg, j);
-                        rank += (kj > ck) || (kj == ck && gj < cg);
+#pragma unroll 8
+                    for (int j = 0; j < kSelCand; ++j) {  // (broadcast reads; entries past bcnt masked)
+                        const uint32_t kj = ss.cand_key[j];
+                        const int gj = ss.cand_g[j];
+                        rank += (j < bcnt) & ((kj > ck) | ((kj == ck) & (gj < cg)));
                     }
                     if (lane < bcnt && rank == need - 1) { ss.tkey = ck; ss.tg = cg; }
                 }
