@@ -895,31 +895,32 @@ def layer_bytes(w, beta: int, l1_counts, nonempty):
 
 
 def layers_oracle_sample(w, L, li, q, pos, beta, nsteps=4):
-    """The float64 oracle on the multi-layer workload's stated sample: one
-    full-layer encode (every sequence and KV head of layer 0) and `nsteps`
-    decode steps of layers 0 and L - 1 (every sequence and KV head, routing
-    and attention), reported per layer-step."""
+    """The float64 oracle on the multi-layer workload's stated sample: the
+    encode of sequence 0 of layer 0 (all its KV heads) and `nsteps` decode
+    steps of sequence 0 on layers 0 and L - 1 (routing and attention of all
+    its KV heads); a full layer-step is that time x B sequences."""
     import oracle as O
+    sub = slice(0, 1)
     t0 = time.perf_counter()
-    caches = {0: O.encode(li.K, li.V, li.l1_mask, li.signs, w.N, w.theta)}
+    caches = {0: O.encode(li.K[sub], li.V[sub], li.l1_mask[sub], li.signs, w.N, w.theta)}
     enc_s = time.perf_counter() - t0
     if L > 1:
         mask, signs = W.layer_meta(w, L - 1)
-        caches[L - 1] = O.encode(li.K, li.V, mask, signs, w.N, w.theta)
+        caches[L - 1] = O.encode(li.K[sub], li.V[sub], mask[sub], signs, w.N, w.theta)
     per = []
     for l, c in caches.items():
         for s in range(nsteps):
             t0 = time.perf_counter()
-            sel, _ = O.route(c, q[s], pos[s], beta)
-            O.decode_attn(c, q[s], pos[s], sel)
+            sel, _ = O.route(c, q[s][sub], pos[s][sub], beta)
+            O.decode_attn(c, q[s][sub], pos[s][sub], sel)
             per.append(time.perf_counter() - t0)
-    t_layer = sum(per) / len(per)
+    t_layer = sum(per) / len(per) * w.B
     return {"value": 1.0 / (t_layer * L), "unit": UNIT, "us_per_layer": t_layer * 1e6,
-            "encode_s_per_layer": enc_s, "cores": len(os.sched_getaffinity(0)), "blas_threads": blas_threads(),
-            "kind": "oracle",
-            "sample": f"one full-layer encode of layer 0 ({w.B * w.Hkv} (sequence, KV head) pairs, {enc_s:.1f} s) "
-                      f"and {nsteps} decode steps of layers {sorted(caches)} (every pair, beta {beta}); "
-                      f"value = 1 / (mean layer-step time x {L} layers)"}
+            "encode_s_per_layer": enc_s * w.B, "cores": len(os.sched_getaffinity(0)),
+            "blas_threads": blas_threads(), "kind": "oracle",
+            "sample": f"sequence 0 (all {w.Hkv} KV heads): its encode of layer 0 ({enc_s:.1f} s) and {nsteps} "
+                      f"decode steps on layers {sorted(caches)} (beta {beta}); layer-step and encode times x "
+                      f"{w.B} sequences; value = 1 / (layer-step time x {L} layers)"}
 
 
 def run_layers(args, rank, world, local):

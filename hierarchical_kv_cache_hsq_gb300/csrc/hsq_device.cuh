@@ -456,19 +456,18 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-constexpr int kSelBins = 256;           // histogram bins per pass of the bucket select
+constexpr int kSelBins = 2048;          // histogram bins of the bucket select (8 per thread)
 constexpr int kSelMaxGroups = 32768;
 constexpr int kSelCand = 32;            // boundary candidates ranked by one warp
 
 struct __align__(16) SelectSmem {
     int hist[kSelBins + 4];  // + a sink bin for keys out of play (branch-free histogram)
+    uint32_t taken[kSelMaxGroups / 32];
     uint32_t cand_key[kSelCand];
     int cand_g[kSelCand];
     uint32_t red[3][32];  // per warp (up to 32 warps)
     int wsum[32];
     int bstar, above, bcnt, ncand;
-    uint32_t tkey;  // threshold pair: the selection is every (key, g) with key > tkey,
-    int tg;         // or key == tkey and g <= tg
 };
 
 // Block-wide exclusive scan of one int per thread (NT threads) with a single
@@ -496,35 +495,35 @@ __device__ __forceinline__ int block_scan_1(int v, int* wsum, int& total) {
 }
 
 // Top-beta selection by the whole block (NT threads, a multiple of 32, at
-// least kSelBins).  s_keys[0..G) are order-preserving keys of the fp32 group
-// scores (0 = empty group, never selected).  The groups of the beta largest
-// keys (ties to the lower group) go to out[0..beta) in ascending group order,
-// -1 padded (out may be shared or global memory; the caller synchronises
-// before reading it).  stats, when not null, holds nstats partial (count,
-// max, min) statistics of the non-empty keys (4 words each) that together
-// cover all G keys; otherwise they are computed here.
+// least 256).  s_keys[0..G) are
+// order-preserving keys of the fp32 group scores (0 = empty group, never
+// selected).  The groups of the beta largest keys (ties to the lower group)
+// go to out[0..beta) in ascending group order, -1 padded (out may be shared
+// or global memory; the caller synchronises before reading it).  stats, when
+// not null, holds nstats partial (count, max, min) statistics of the
+// non-empty keys (4 words each) that together cover all G keys; otherwise
+// they are computed here.
 //
-// The selection is found as a threshold pair (tkey, tg): the beta-th largest
-// (key, group) pair in the order "larger key first, then lower group"; a
-// group is selected when its key is larger than tkey, or equal with a group
-// index up to tg.  To find it, the keys still in play [lo, hi] are
-// histogrammed into kSelBins bins (first pass: equal-width bins of the fp32
-// score; later passes: power-of-two-wide bins of the key), one warp scans
-// the bins from the top for the bin holding the wanted rank, and when that
-// bin has at most kSelCand keys one warp ranks them exactly; otherwise the
-// keys in play shrink to that bin's exact range and the pass repeats (a
-// range of equal keys is resolved by a scan in group order).  Both bin
-// functions are monotone in the key, so every bin is a contiguous key range.
+// Bucket select: the keys still in play, [lo, hi], are histogrammed (first
+// pass: kSelBins equal-width bins of the fp32 score; later passes: power-of-
+// two-wide bins of the key), a blocked scan from the top finds the bin that
+// holds the beta-th key, every key of a higher bin is taken, and the
+// boundary bin's keys are ranked exactly (key, then group index) when there
+// are at most 32 of them; otherwise [lo, hi] shrinks to that bin and the
+// pass repeats.  If all keys left are equal, the lowest groups are taken.
+// Both bin functions are monotone in the key, so a bin is a contiguous key
+// range and the result is exact.
 //
 // Layout: warp w owns the contiguous keys [w W, (w + 1) W), W = 32 kpw;
 // step j of a warp reads keys w W + 32 j + lane (conflict-free), and the
 // ordered placement counts with one ballot per step.  Every loop bound is
-// uniform and the per-key work is branch-free (clamped loads, bitwise flags,
-// a sink bin).
+// uniform, so all warp-level operations are converged, and the per-key work
+// is branch-free (clamped loads, bitwise flags, a sink bin): a divergent
+// branch around a load or an atomic costs several hundred cycles per step.
 template <int NT>
 __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* out, SelectSmem& ss,
                                 const uint32_t* stats = nullptr, int nstats = 0) {
-    static_assert(NT % 32 == 0 && NT >= kSelBins, "block size");
+    static_assert(NT % 32 == 0 && NT >= kSelBins / 8, "block size");
     constexpr int NW = NT / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kpw = (G + NT - 1) / NT;  // steps per warp
@@ -538,11 +537,16 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
     // count, max and min of the non-empty keys
     int ne = 0;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    if (stats) {  // lane r reads part r (nstats <= 32)
-        const bool mine = lane < nstats;
-        ne = __reduce_add_sync(kFull, mine ? (int)stats[4 * lane] : 0);
-        hi = __reduce_max_sync(kFull, mine ? stats[4 * lane + 1] : 0u);
-        lo = __reduce_min_sync(kFull, mine ? stats[4 * lane + 2] : 0xFFFFFFFFu);
+    if (stats) {
+#pragma unroll 1
+        for (int w = tid; w < (G + 31) / 32; w += NT) ss.taken[w] = 0u;
+#pragma unroll 1
+        for (int r = 0; r < nstats; ++r) {
+            ne += (int)stats[4 * r];
+            hi = max(hi, stats[4 * r + 1]);
+            lo = min(lo, stats[4 * r + 2]);
+        }
+        __syncthreads();
     } else {
         int cn = 0;
         uint32_t mx = 0u, mn = 0xFFFFFFFFu;
@@ -558,6 +562,8 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         mx = __reduce_max_sync(kFull, mx);
         mn = __reduce_min_sync(kFull, mn);
         if (lane == 0) { ss.red[0][warp] = (uint32_t)cn; ss.red[1][warp] = mx; ss.red[2][warp] = mn; }
+#pragma unroll 1
+        for (int w = tid; w < (G + 31) / 32; w += NT) ss.taken[w] = 0u;
         __syncthreads();
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
@@ -567,55 +573,25 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
         }
     }
 
-    // the threshold pair; every non-empty group when beta >= the non-empty count
-    uint32_t tkey = 1u;
-    int tg = 0x7FFFFFFF;
+    // mode 0: take every non-empty group; 1: keys > bhi plus the ranked
+    // boundary candidates; 2: keys > kstar plus the first `need` equal to kstar
+    int mode = 0, above = 0, need = 0, mode1_base = 0;
+    uint32_t bhi = 0u, kstar = 0u;
     if (ne > beta) {
-        int need = beta;  // rank wanted among the keys in play
         const float smin = key_to_float(lo), smax = key_to_float(hi);
         const float fscale = (float)kSelBins / (smax - smin);
         const bool float_ok = isfinite(fscale) && smax > smin;
 #pragma unroll 1
         for (int level = 0; level < 8; ++level) {
-            if (lo == hi) {
-                // every key in play equals lo: the need-th of them in group order
-                int cnt = 0;
-#pragma unroll 1
-                for (int j = 0; j < kpw; ++j) {
-                    int i;
-                    cnt += __popc(__ballot_sync(kFull, key_at(j, i) == lo));
-                }
-                int tot;
-                const int before = __shfl_sync(kFull, block_scan_1<NT>(lane == 0 ? cnt : 0, ss.wsum, tot), 0);
-                if (before < need && before + cnt >= need) {  // this warp holds the need-th
-                    int run = before;
-#pragma unroll 1
-                    for (int j = 0; j < kpw; ++j) {
-                        int i;
-                        const unsigned bm = __ballot_sync(kFull, key_at(j, i) == lo);
-                        const int c = __popc(bm);
-                        if (run + c >= need) {
-                            const int k = need - run;  // k-th set bit of bm (1-based)
-                            const bool mine = ((bm >> lane) & 1u) && __popc(bm & ((1u << lane) - 1u)) == k - 1;
-                            if (mine) { ss.tkey = lo; ss.tg = i; }
-                            break;
-                        }
-                        run += c;
-                    }
-                }
-                __syncthreads();
-                tkey = ss.tkey;
-                tg = ss.tg;
-                break;
-            }
+            if (lo == hi) { mode = 2; kstar = lo; need = beta - above; break; }
             const bool fl = level == 0 && float_ok;
             const int bits = 32 - __clz(hi - lo);
-            const int shift = bits > 8 ? bits - 8 : 0;
+            const int shift = bits > 11 ? bits - 11 : 0;
             auto bin_of = [&](uint32_t v) -> int {
                 if (fl) return min(max((int)((key_to_float(v) - smin) * fscale), 0), kSelBins - 1);
                 return (int)((v - lo) >> shift);
             };
-            if (tid <= kSelBins) ss.hist[tid] = 0;
+            for (int q = tid; q < kSelBins / 4; q += NT) reinterpret_cast<int4*>(ss.hist)[q] = make_int4(0, 0, 0, 0);
             __syncthreads();
 #pragma unroll 1
             for (int j = 0; j < kpw; ++j) {
@@ -625,48 +601,46 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                 atomicAdd(&ss.hist[play ? bin_of(v) : kSelBins], 1);
             }
             __syncthreads();
-            if (warp == 0) {
-                // lane L scans bins 255 - 8 L .. 248 - 8 L (descending)
-                int h[8], t = 0;
+            // blocked scan from the top: thread t < B/8 owns bins [B - 8(t+1), B - 8t)
+            const bool owns = tid < kSelBins / 8;
+            const int top = kSelBins - 8 * min(tid, kSelBins / 8 - 1);
+            const int4 h0 = *reinterpret_cast<const int4*>(&ss.hist[top - 8]);
+            const int4 h1 = *reinterpret_cast<const int4*>(&ss.hist[top - 4]);
+            int hv[8] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};  // descending bins
+            int local = 0;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    h[k] = ss.hist[kSelBins - 1 - 8 * lane - k];
-                    t += h[k];
-                }
-                int inc = t;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(kFull, inc, o);
-                    if (lane >= o) inc += y;
-                }
-                int run = inc - t;
-                if (run < need && inc >= need) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (run < need && run + h[k] >= need) {
-                            ss.bstar = kSelBins - 1 - 8 * lane - k;
-                            ss.above = run;
-                            ss.bcnt = h[k];
-                        }
-                        run += h[k];
-                    }
-                }
-                if (lane == 0) ss.ncand = 0;
+            for (int i = 0; i < 8; ++i) {
+                hv[i] = owns ? hv[i] : 0;
+                local += hv[i];
             }
+            int tot;
+            int run = above + block_scan_1<NT>(local, ss.wsum, tot);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (run < beta && run + hv[i] >= beta) { ss.bstar = top - 1 - i; ss.above = run; ss.bcnt = hv[i]; }
+                run += hv[i];
+            }
+            if (tid == 0) ss.ncand = 0;
             __syncthreads();
             const int bstar = ss.bstar, bcnt = ss.bcnt;
-            need -= ss.above;
-            // the boundary bin's members: gathered when few, else their exact key range
+            above = ss.above;
+            need = beta - above;
+            // the boundary bin's members: gathered (when few) and their exact key
+            // range; and per warp the keys above the boundary bin (all taken)
             uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+            int wsure = 0;
 #pragma unroll 1
             for (int j = 0; j < kpw; ++j) {
                 int i;
                 const uint32_t v = key_at(j, i);
-                const bool inb = (v != 0u) & (v >= lo) & (v <= hi) & (bin_of(v) == bstar);
+                const bool inr = (v != 0u) & (v >= lo) & (v <= hi);
+                const int bn = bin_of(v);
+                const bool inb = inr & (bn == bstar);
+                wsure += __popc(__ballot_sync(kFull, (v > hi) | (inr & (bn > bstar))));
                 bmx = max(bmx, inb ? v : 0u);
                 bmn = min(bmn, inb ? v : 0xFFFFFFFFu);
                 const unsigned bm = __ballot_sync(kFull, inb);
-                if (bm != 0u && bcnt <= kSelCand) {
+                if (bm != 0u && bcnt <= kSelCand) {  // rare: the boundary bin's few keys
                     int slot = 0;
                     if (lane == 0) slot = atomicAdd(&ss.ncand, __popc(bm));
                     slot = __shfl_sync(kFull, slot, 0) + __popc(bm & ((1u << lane) - 1u));
@@ -676,67 +650,94 @@ __device__ void select_top_beta(const uint32_t* s_keys, int G, int beta, int* ou
                     }
                 }
             }
-            if (bcnt <= kSelCand) {
-                __syncthreads();
-                if (warp == 0) {
-                    const uint32_t ck = lane < bcnt ? ss.cand_key[lane] : 0u;
-                    const int cg = lane < bcnt ? ss.cand_g[lane] : 0x7FFFFFFF;
-                    int rank = 0;
-#pragma unroll 8
-                    for (int j = 0; j < kSelCand; ++j) {  // (broadcast reads; entries past bcnt masked)
-                        const uint32_t kj = ss.cand_key[j];
-                        const int gj = ss.cand_g[j];
-                        rank += (j < bcnt) & ((kj > ck) | ((kj == ck) & (gj < cg)));
-                    }
-                    if (lane < bcnt && rank == need - 1) { ss.tkey = ck; ss.tg = cg; }
-                }
-                __syncthreads();
-                tkey = ss.tkey;
-                tg = ss.tg;
-                break;
-            }
-            // crowded boundary bin: continue inside its exact key range
             bmx = __reduce_max_sync(kFull, bmx);
             bmn = __reduce_min_sync(kFull, bmn);
-            if (lane == 0) { ss.red[1][warp] = bmx; ss.red[2][warp] = bmn; }
+            if (lane == 0) { ss.red[0][warp] = (uint32_t)wsure; ss.red[1][warp] = bmx; ss.red[2][warp] = bmn; }
             __syncthreads();
-            lo = 0xFFFFFFFFu;
-            hi = 0u;
+            uint32_t blo_b = 0xFFFFFFFFu, bhi_b = 0u;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                hi = max(hi, ss.red[1][w]);
-                lo = min(lo, ss.red[2][w]);
+                bhi_b = max(bhi_b, ss.red[1][w]);
+                blo_b = min(blo_b, ss.red[2][w]);
             }
+            if (bcnt <= kSelCand) {
+                // every warp ranks the candidates (same result); warp 0 records the taken ones
+                const uint32_t ck = lane < bcnt ? ss.cand_key[lane] : 0u;
+                const int cg = lane < bcnt ? ss.cand_g[lane] : -1;
+                int rank = 0;
+#pragma unroll 1
+                for (int j = 0; j < bcnt; ++j) {
+                    const uint32_t kj = __shfl_sync(kFull, ck, j);
+                    const int gj = __shfl_sync(kFull, cg, j);
+                    rank += (kj > ck) || (kj == ck && gj < cg);
+                }
+                const bool tk = lane < bcnt && rank < need;
+                if (warp == 0 && tk) atomicOr(&ss.taken[cg >> 5], 1u << (cg & 31));
+                // where this warp's taken keys start: keys above the bin plus taken
+                // candidates, over the warps before it (the placement needs no count pass)
+                const int ow = cg >= 0 ? cg / (32 * kpw) : -1;
+                int base = 0;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) {
+                    const int cw = (int)ss.red[0][w] + __popc(__ballot_sync(kFull, tk & (ow == w)));
+                    base += w < warp ? cw : 0;
+                }
+                mode1_base = base;
+                mode = 1;
+                bhi = bhi_b;
+                __syncthreads();
+                break;
+            }
+            lo = blo_b;  // crowded boundary bin: continue inside it
+            hi = bhi_b;
             __syncthreads();
         }
     }
 
-    // ordered placement: a warp's taken count, one exclusive scan over the
-    // warps, then per step the ballot of taken keys
-    auto taken = [&](int j, int& i) -> bool {
+    // ordered placement: per step a ballot of taken (mode 2: greater) and of
+    // equal keys; a warp's counts, then one exclusive scan over the warps
+    // (mode is uniform; the per-key expressions are bitwise, without branches)
+    const uint32_t thr = mode == 0 ? 0u : mode == 1 ? bhi : kstar;
+    auto flags_at = [&](int j, int& i, bool& gt, bool& eq) {
         const uint32_t v = key_at(j, i);
-        return (v != 0u) & ((v > tkey) | ((v == tkey) & (i <= tg)));
+        const uint32_t tw = ss.taken[min(i, G - 1) >> 5];
+        const bool tk = (mode == 1) & (v != 0u) & (((tw >> (i & 31)) & 1u) != 0u);
+        gt = (v > thr) | tk;
+        eq = (mode == 2) & (v == kstar);
     };
-    int wcnt = 0;
+    int pos_gt = mode1_base, eq_before = 0;
+    if (mode != 1) {
+        int wgt = 0, weq = 0;
 #pragma unroll 1
-    for (int j = 0; j < kpw; ++j) {
-        int i;
-        wcnt += __popc(__ballot_sync(kFull, taken(j, i)));
+        for (int j = 0; j < kpw; ++j) {
+            int i;
+            bool gt, eq;
+            flags_at(j, i, gt, eq);
+            wgt += __popc(__ballot_sync(kFull, gt));
+            weq += __popc(__ballot_sync(kFull, eq));
+        }
+        int total;
+        const int packed = block_scan_1<NT>(lane == 0 ? (wgt | (weq << 16)) : 0, ss.wsum, total);
+        pos_gt = __shfl_sync(kFull, packed, 0) & 0xFFFF;
+        eq_before = __shfl_sync(kFull, packed, 0) >> 16;
     }
-    int total;
-    int pos = __shfl_sync(kFull, block_scan_1<NT>(lane == 0 ? wcnt : 0, ss.wsum, total), 0);
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll 1
     for (int j = 0; j < kpw; ++j) {
         int i;
-        const bool tk = taken(j, i);
-        const unsigned bm = __ballot_sync(kFull, tk);
-        const int p = pos + __popc(bm & lt);
-        if (tk & (p < beta)) out[p] = i;
-        pos += __popc(bm);
+        bool gt, eq;
+        flags_at(j, i, gt, eq);
+        const unsigned bg = __ballot_sync(kFull, gt), be = __ballot_sync(kFull, eq);
+        const int pg = pos_gt + __popc(bg & lt), pe = eq_before + __popc(be & lt);
+        const int p = gt ? pg + (mode == 2 ? min(pe, need) : 0) : pg + pe;
+        const bool put = (gt | (eq & (pe < need))) & (p < beta);
+        if (put) out[p] = i;
+        pos_gt += __popc(bg);
+        eq_before += __popc(be);
     }
+    const int n_sel = mode == 0 ? ne : beta;
 #pragma unroll 1
-    for (int i = total + tid; i < beta; i += NT) out[i] = -1;
+    for (int i = n_sel + tid; i < beta; i += NT) out[i] = -1;
 }
 
 // Dot products of two 128-vectors (a, b; this lane's 8 dims each) with the R
