@@ -71,6 +71,8 @@ def parse_args():
                    help="per-layer mode: every query head routes, fetches and attends with its own beta groups")
     p.add_argument("--route-max", action="store_true",
                    help="per-layer mode: route by each KV head's best query head (route + attention)")
+    p.add_argument("--prefill-only", type=int, default=0, metavar="T",
+                   help="only the prefill measurement, on the 8B-shaped layer cut to T tokens (profiler captures)")
     return p.parse_args()
 
 
@@ -1099,10 +1101,23 @@ def run_layers(args, rank, world, local):
     return line if rank == 0 else None
 
 
+def run_prefill_only(args):
+    import torch
+
+    import hierarchical_kv_cache_hsq_gb300 as H
+    H.load_library()
+    w = W.get_workload(WORKLOAD).with_(T=args.prefill_only, marked=int(0.01 * args.prefill_only))
+    li = W.layer_inputs(w, rope=lambda x, p: input_rope(x, p, w.theta))
+    return {"prefill": measure_prefill(H, torch, w, li, reps=max(args.steps, 1)),
+            "config": {"workload": f"{w.name} cut to T={w.T}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128"}}
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.prefill_only:
+        line = run_prefill_only(args) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     elif (args.workload != WORKLOAD or args.betas or args.group_n or args.layers or args.route_max
           or args.route_per_head):
