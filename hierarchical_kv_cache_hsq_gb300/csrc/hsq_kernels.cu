@@ -369,10 +369,19 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
         if (active) (half == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
     }
     __syncthreads();
-    // S rho for all 2N residuals of the CTA: thread (i, grp) forms row i of S against
+    // S rho for the 2N residuals of the CTA: thread (i, grp) forms row i of S against
     // 8 residuals, reading its row of S once; a warp's 32 consecutive rows are one
-    // sketch word per residual (ballot)
+    // sketch word per residual (ballot).  Residual r is half r / N of token r % N, so
+    // the groups of L1 residuals (half 1) skip their rows when none of their tokens
+    // is in L1 (most groups: L1 holds ~2 % of the tokens).
     const int i = threadIdx.x & (kDim - 1), grp = threadIdx.x >> 7;
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = grp * 8 + j;
+        any |= s_dst[r % N][r / N] >= 0;
+    }
+    if (!any) return;  // (uniform per CTA group: every thread of the group read the same slots)
     const float4* srow = reinterpret_cast<const float4*>(o.S + (size_t)i * kDim);
     float acc[8];
 #pragma unroll
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int r = grp * 8 + j;
-            const float4 rv = *reinterpret_cast<const float4*>(&s_rho[r >> 1][r & 1][4 * d4]);
+            const float4 rv = *reinterpret_cast<const float4*>(&s_rho[r % N][r / N][4 * d4]);
             acc[j] = fmaf(sv.x, rv.x, acc[j]);
             acc[j] = fmaf(sv.y, rv.y, acc[j]);
             acc[j] = fmaf(sv.z, rv.z, acc[j]);
@@ -395,8 +404,8 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
     for (int j = 0; j < 8; ++j) {
         const uint32_t bits = __ballot_sync(kFull, acc[j] >= 0.f);
         const int r = grp * 8 + j;
-        const long long e = s_dst[r >> 1][r & 1];
-        if (lane == 0 && e >= 0) ((r & 1) == 0 ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
+        const long long e = s_dst[r % N][r / N];
+        if (lane == 0 && e >= 0) (r < N ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
     }
 }
 
