@@ -794,20 +794,27 @@ def cache_from_abi(bufs: dict, l1_mask: np.ndarray, signs: np.ndarray, N: int, T
 # Prefill ([HSQ] section 4, results: prefill overhead at 32K).
 # ---------------------------------------------------------------------------
 
-def prefill_attn(Q: np.ndarray, K: np.ndarray, V: np.ndarray, theta: float = 1.0e6) -> np.ndarray:
-    """Dense causal attention of a prompt: Q [B, Hq, T, d] and K, V [B, Hkv, T, d]
-    pre-RoPE at positions 0..T-1; query t of head j attends to keys 0..t of KV
-    head j // (Hq / Hkv) with weights softmax(RoPE(q_t, t) . RoPE(k_s, s) / sqrt(d)).
-    Returns O [B, Hq, T, d] in float64."""
+def prefill_attn(Q: np.ndarray, K: np.ndarray, V: np.ndarray, theta: float = 1.0e6,
+                 q_start: int = 0) -> np.ndarray:
+    """Dense causal attention of a prompt: K, V [B, Hkv, Tk, d] pre-RoPE at
+    positions 0..Tk-1 and Q [B, Hq, Tq, d] pre-RoPE at positions q_start ..
+    q_start + Tq - 1 (q_start = 0, Tq = Tk: the whole prompt; a later start
+    gives those rows of the whole prompt's output); the query at position p of
+    head j attends to keys 0..p of KV head j // (Hq / Hkv) with weights
+    softmax(RoPE(q, p) . RoPE(k_s, s) / sqrt(d)).  Returns O [B, Hq, Tq, d] in
+    float64."""
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)
-    B, Hq, T, d = Q.shape
-    Hkv = K.shape[1]
-    t = np.arange(T)
-    Qr = rope(Q, t, theta)
-    Kr = rope(K, t, theta)
-    causal = t[None, :] <= t[:, None]                    # [query, key]
+    B, Hq, Tq, d = Q.shape
+    Hkv, Tk = K.shape[1], K.shape[2]
+    if q_start < 0 or q_start + Tq > Tk:
+        raise ValueError("queries must sit at positions covered by the keys")
+    tq = q_start + np.arange(Tq)
+    tk = np.arange(Tk)
+    Qr = rope(Q, tq, theta)
+    Kr = rope(K, tk, theta)
+    causal = tk[None, :] <= tq[:, None]                  # [query, key]
     O = np.zeros_like(Q)
     for b in range(B):
         for h, js in enumerate(_heads(Hq, Hkv)):

@@ -87,3 +87,22 @@ def test_prefill_returns_the_encode_of_its_kv():
     np.testing.assert_array_equal(o, O.prefill_attn(Q, K, V))
     for tier in ("l1_k", "l1_v", "l2_k", "l2_v", "l3_k", "l3_v"):
         np.testing.assert_array_equal(getattr(cache, tier).codes, getattr(ref, tier).codes)
+
+
+def test_prefill_query_rows_from_a_later_start():
+    # rows a..b of the whole prompt's output equal the attention of those queries alone
+    Q, K, V = _inputs(B=1, Hq=4, Hkv=2, T=40)
+    full = O.prefill_attn(Q, K, V)
+    part = O.prefill_attn(Q[:, :, 25:33], K[:, :, :33], V[:, :, :33], q_start=25)
+    np.testing.assert_allclose(part, full[:, :, 25:33], rtol=1e-12, atol=1e-13)
+    # against torch SDPA with an explicit mask for the shifted query positions
+    r = 2
+    tq, tk = np.arange(25, 33), np.arange(33)
+    q = _rope_complex(np.concatenate([np.zeros((1, 4, 25, 128)), Q[:, :, 25:33]], axis=2))[:, :, 25:]
+    mask = torch.from_numpy(tk[None, :] <= tq[:, None])
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(np.repeat(_rope_complex(K[:, :, :33]), r, axis=1)),
+        torch.from_numpy(np.repeat(V[:, :, :33], r, axis=1)), attn_mask=mask).numpy()
+    np.testing.assert_allclose(part, ref, rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):
+        O.prefill_attn(Q[:, :, 30:40], K[:, :, :35], V[:, :, :35], q_start=30)
