@@ -101,3 +101,32 @@ def test_prefill_with_cache_encodes_like_hsq_encode(name):
     alone = _run(ctx, w.B, w.T, Q, li.K, li.V)
     np.testing.assert_array_equal(alone, got)
     ctx.close()
+
+
+def test_prefill_full_size_8b_32k_sampled_rows():
+    """The 8B-shaped 32K prompt (B1, Hq 32, Hkv 8) in the launch configuration the
+    benchmark times: the first and the last 128 query rows of query heads 0-3 (KV
+    head 0) and 28-31 (KV head 7) against the oracle (the last rows attend to all
+    32768 keys)."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    B, Hq, Hkv, T = 1, 32, 8, 32768
+    w = W.get_workload("qwen3_8b_32k")
+    ctx = make_ctx(w)
+    rng = np.random.default_rng(77)
+    Q = _bf16(rng.standard_normal((B, Hq, T, 128), dtype=np.float32))
+    K = _bf16(rng.standard_normal((B, Hkv, T, 128), dtype=np.float32))
+    V = _bf16(rng.standard_normal((B, Hkv, T, 128), dtype=np.float32))
+    got = _run(ctx, B, T, Q, K, V)
+    assert np.all(np.isfinite(got))
+    worst = 0.0
+    for h in (0, 7):
+        js = slice(4 * h, 4 * h + 4)
+        for start in (0, T - 128):
+            ref = O.prefill_attn(Q[:, js, start:start + 128], K[:, h:h + 1], V[:, h:h + 1], w.theta,
+                                 q_start=start)
+            err = rel_l2(got[:, js, start:start + 128], ref)
+            worst = max(worst, float(err.max()))
+            assert err.max() <= 1e-3, f"KV head {h}, rows from {start}: rel L2 {err.max():.3e}"
+    print(f"[prefill 8B/32K] worst sampled rel L2 {worst:.2e}")
+    ctx.close()
