@@ -22,19 +22,22 @@
 //      so that it is the K-major B operand of P V.
 // Rows past T are zero.
 //
-// Attention kernel: one CTA of 256 threads per (128-query tile, query head,
-// sequence).  Query row r of the tile is TMEM lane r; warp w reads lanes
-// 32 (w & 3) .. + 31 (a warp can only reach its quarter of the lanes) and
-// the half w >> 2 of the columns, so two threads share a row.  Per 64-key
-// tile (up to the diagonal): thread 0 waits for the tile's bulk copies and
-// issues S = Q K^T (128 x 64, fp32 in TMEM columns 0-63); every thread
-// reads its 32 logits of S, applies the causal mask and the online softmax
-// (log2 domain; the two halves of a row exchange their maxima through
-// shared memory; the running maximum is raised only when a logit exceeds
-// it by more than 8, then the row's O in TMEM is rescaled), writes its half
-// row of P (hi, lo) to shared memory; thread 0 issues O += P V (128 x 128,
-// TMEM columns 128-255) and, once it completed, refills the tile's stage
-// with the tile two ahead.  The output is O / l in fp32.
+// Attention kernel: one CTA per (128-query tile, query head, sequence), warp
+// specialised.  Warp 8 (one thread) is the producer: it issues every bulk
+// copy and every MMA -- S = Q K^T of tile k (128 x 64, into TMEM columns 0-63
+// or 64-127 in turn), then, once the softmax has written P of tile k, O_half
+// += P_half V_half for both key halves (TMEM columns 128-255 and 256-383) --
+// and refills each key / value stage when the MMA that read it completed.
+// Warps 0-7 run the softmax: query row r of the tile is TMEM lane r (a warp
+// reaches only its quarter of the lanes, 32 (w & 3) .. + 31) and warp w
+// handles the key half w >> 2 of every 64-key tile, so two threads share a
+// row; each key half keeps its own online softmax (log2 domain; its running
+// maximum is raised only when a logit exceeds it by more than 8, then its O
+// in TMEM is rescaled) and its own accumulator, combined once at the end.
+// The roles meet only on mbarriers (S full / S read / P full / O done, two of
+// each, one per buffer), so the S of the next tiles runs on the tensor cores
+// while the softmax of this one runs, and P is double-buffered.  The output
+// is the combined O / l in fp32.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -49,18 +52,20 @@ using namespace hsq_tc;
 
 constexpr int kPfRows = 128;                          // query rows per CTA (TMEM lanes)
 constexpr int kPfKeys = 64;                           // keys per tile
-constexpr int kPfThreads = 256;
+constexpr int kPfSoftThreads = 256;                   // softmax warps 0-7
+constexpr int kPfThreads = kPfSoftThreads + 32;       // + the producer warp
 constexpr uint32_t kQImg = kPfRows * kDim * 2;        // 32 KB
 constexpr uint32_t kKImg = kPfKeys * kDim * 2;        // 16 KB
 constexpr uint32_t kVImg = kDim * kPfKeys * 2;        // 16 KB
 constexpr uint32_t kPImg = kPfRows * kPfKeys * 2;     // 16 KB
-constexpr uint32_t kStageBytes = 2 * kKImg + kVImg;   // Kh | Kl | Vt
-constexpr int kStages = 2;
-constexpr uint32_t kOffQh = 0, kOffQl = kQImg, kOffStage = 2 * kQImg;
-constexpr uint32_t kOffPh = kOffStage + kStages * kStageBytes, kOffPl = kOffPh + kPImg;
-constexpr uint32_t kOffBar = kOffPl + kPImg;          // q, kv[0], kv[1], mma barriers; TMEM address
-constexpr uint32_t kPfSmem = kOffBar + 64 + 1024;     // + slack to align the base to 1024 bytes
-constexpr uint32_t kTmemCols = 256;                   // S: columns 0-63, O: 128-255
+constexpr uint32_t kOffQh = 0, kOffQl = kQImg, kOffK = 2 * kQImg;   // K stage b: Kh | Kl
+constexpr uint32_t kOffV = kOffK + 2 * 2 * kKImg;                    // V stage b
+constexpr uint32_t kOffP = kOffV + 2 * kVImg;                        // P buffer b: Ph | Pl
+constexpr uint32_t kOffBar = kOffP + 2 * 2 * kPImg;
+// barriers (8 bytes each): q | k[2] | v[2] | s_full[2] | s_free[2] | p_full[2] | o_done[2]; TMEM address
+constexpr int kNumBars = 13;
+constexpr uint32_t kPfSmem = kOffBar + 8 * kNumBars + 8 + 1024;
+constexpr uint32_t kTmemCols = 512;  // S buffers: 0-63, 64-127; O of key half k: 128 + 128 k
 
 struct PrefillArgs {
     const uint8_t* qh; const uint8_t* ql; const uint8_t* kh; const uint8_t* kl; const uint8_t* vt;
@@ -71,26 +76,29 @@ struct PrefillArgs {
 
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs a) {
     extern __shared__ uint8_t pf_raw[];
-    __shared__ int s_abort;
-    __shared__ float s_mx[2][kPfRows];   // per column half: the row's tile maximum
     const uint32_t raw = smem_addr(pf_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = pf_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lanei = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = 32 * quarter + lanei;          // query row of the tile = TMEM lane
     const int qt = a.nqt - 1 - (int)blockIdx.x;    // the longest rows first
     const int j = blockIdx.y, b = blockIdx.z;
     const int h = j / (a.Hq / a.Hkv);
-    const uint32_t bar_q = base + kOffBar, bar_kv = bar_q + 8, bar_mma = bar_q + 24, slot = bar_q + 32;
+    const uint32_t bar0 = base + kOffBar;
+    const uint32_t bar_q = bar0, bar_k = bar0 + 8, bar_v = bar0 + 24, s_full = bar0 + 40, s_free = bar0 + 56;
+    const uint32_t p_full = bar0 + 72, o_done = bar0 + 88, slot = bar0 + 8 * kNumBars;
+    const int nkv = 2 * qt + 2;  // key tiles up to the diagonal
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        mbar_init(bar_kv, 1);
-        mbar_init(bar_kv + 8, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_k + 8 * i, 1);
+            mbar_init(bar_v + 8 * i, 1);
+            mbar_init(s_full + 8 * i, 1);
+            mbar_init(s_free + 8 * i, kPfSoftThreads);
+            mbar_init(p_full + 8 * i, kPfSoftThreads);
+            mbar_init(o_done + 8 * i, 1);
+        }
         mbar_init_fence();
-        s_abort = 0;
     }
     if (warp == 0) {
         tmem_alloc(slot, kTmemCols);
@@ -99,160 +107,202 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 32);
-    const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
-    const uint32_t tS = tmem + lanes + 32 * half;           // this thread's 32 columns of S
-    const uint32_t tO = tmem + lanes + 128 + 64 * half;     // and its 64 columns of O
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 8 * kNumBars);
+    bool ok = true;
 
-    const int nkv = 2 * qt + 2;  // key tiles up to the diagonal
-    const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
-    auto load_kv = [&](int kt, int st) {
-        const uint32_t dst = base + kOffStage + st * kStageBytes, bar = bar_kv + 8 * st;
-        mbar_expect_tx(bar, kStageBytes);
-        bulk_g2s(dst, a.kh + (kv0 + kt) * kKImg, kKImg, bar);
-        bulk_g2s(dst + kKImg, a.kl + (kv0 + kt) * kKImg, kKImg, bar);
-        bulk_g2s(dst + 2 * kKImg, a.vt + (kv0 + kt) * kVImg, kVImg, bar);
-    };
-    if (tid == 0) {
-        const size_t qi = ((size_t)b * a.Hq + j) * a.nqt + qt;
-        mbar_expect_tx(bar_q, 2 * kQImg);
-        bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
-        bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
-        load_kv(0, 0);
-        if (nkv > 1) load_kv(1, 1);
-    }
-
-    const int t = qt * kPfRows + row;  // this thread's query position
-    float m_used = -INFINITY, lsum = 0.f;
-    uint32_t ph_mma = 0;
-    constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys), idO = idesc_bf16_f32(kPfRows, kDim);
-#pragma unroll 1
-    for (int kt = 0; kt < nkv; ++kt) {
-        const int st = kt & 1;
-        const uint32_t stage = base + kOffStage + st * kStageBytes;
-        if (tid == 0) {
-            bool okw = (kt > 0 || mbar_wait(bar_q, 0)) && mbar_wait(bar_kv + 8 * st, (kt >> 1) & 1);
-            if (okw) {
-                tc_fence_after();
-                // S = Qh Kh^T + Ql Kh^T + Qh Kl^T over the 128 dims (8 slices of 16)
+    if (warp == kPfSoftThreads / 32) {
+        // ---- producer: bulk copies and MMAs, one thread ----
+        if (lanei == 0) {
+            const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
+            auto load_k = [&](int kt) {
+                const int st = kt & 1;
+                const uint32_t dst = base + kOffK + st * 2 * kKImg, bar = bar_k + 8 * st;
+                mbar_expect_tx(bar, 2 * kKImg);
+                bulk_g2s(dst, a.kh + (kv0 + kt) * kKImg, kKImg, bar);
+                bulk_g2s(dst + kKImg, a.kl + (kv0 + kt) * kKImg, kKImg, bar);
+            };
+            auto load_v = [&](int kt) {
+                const int st = kt & 1;
+                mbar_expect_tx(bar_v + 8 * st, kVImg);
+                bulk_g2s(base + kOffV + st * kVImg, a.vt + (kv0 + kt) * kVImg, kVImg, bar_v + 8 * st);
+            };
+            constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys), idO = idesc_bf16_f32(kPfRows, kDim);
+            auto issue_s = [&](int kt) {  // S of tile kt into buffer kt & 1: Qh Kh^T + Ql Kh^T + Qh Kl^T
+                const uint32_t ks = base + kOffK + (kt & 1) * 2 * kKImg, dS = tmem + 64 * (kt & 1);
 #pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t qo = (k >> 2) * (kQImg / 2) + (k & 3) * 32;
                     const uint32_t ko = (k >> 2) * (kKImg / 2) + (k & 3) * 32;
                     const uint64_t dqh = sw128_desc(base + kOffQh + qo), dql = sw128_desc(base + kOffQl + qo);
-                    const uint64_t dkh = sw128_desc(stage + ko), dkl = sw128_desc(stage + kKImg + ko);
-                    mma_bf16(tmem, dqh, dkh, idS, k > 0);
-                    mma_bf16(tmem, dql, dkh, idS, 1);
-                    mma_bf16(tmem, dqh, dkl, idS, 1);
+                    const uint64_t dkh = sw128_desc(ks + ko), dkl = sw128_desc(ks + kKImg + ko);
+                    mma_bf16(dS, dqh, dkh, idS, k > 0);
+                    mma_bf16(dS, dql, dkh, idS, 1);
+                    mma_bf16(dS, dqh, dkl, idS, 1);
                 }
-                mma_commit(bar_mma);
-                okw = mbar_wait(bar_mma, ph_mma);
+                mma_commit(s_full + 8 * (kt & 1));
+            };
+            const size_t qi = ((size_t)b * a.Hq + j) * a.nqt + qt;
+            mbar_expect_tx(bar_q, 2 * kQImg);
+            bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
+            bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
+            for (int kt = 0; kt < min(nkv, 2); ++kt) {
+                load_k(kt);
+                load_v(kt);
             }
-            if (!okw) {
-                s_abort = 1;
-                atomicOr(a.err, HSQ_DEVERR_WAIT);
+            ok = mbar_wait(bar_q, 0);
+            for (int kt = 0; kt < min(nkv, 2) && ok; ++kt) {
+                ok = mbar_wait(bar_k + 8 * kt, 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(kt);
+                }
             }
-        }
-        ph_mma ^= 1u;
-        __syncthreads();
-        if (s_abort) break;
-        tc_fence_after();
-
-        // this thread's 32 logits of the row (log2 domain), causal mask
-        float x[32];
-        tmem_ld32(tS, x);
-        const int key0 = kt * kPfKeys + 32 * half;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            x[c] = key0 + c <= t ? x[c] * kLogitScaleLog2 : -INFINITY;
-            mt = fmaxf(mt, x[c]);
-        }
-        s_mx[half][row] = mt;
-        __syncthreads();
-        mt = fmaxf(mt, s_mx[half ^ 1][row]);
-        const float m_new = fmaxf(m_used, mt);
-        const bool raise = m_new > m_used + 8.f;  // (always on the first tile: key 0 is unmasked)
-        const float alpha = raise ? (m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new)) : 1.f;
-        if (raise) {
-            lsum *= alpha;
-            m_used = m_new;
-        }
-        if (kt > 0 && __any_sync(0xffffffffu, raise)) {  // rescale this thread's half row of O (TMEM)
 #pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float o[32];
-                tmem_ld32(tO + c0, o);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                tmem_st32(tO + c0, o);
+            for (int kt = 0; kt < nkv && ok; ++kt) {
+                const int bb = kt & 1;
+                const uint32_t ph = (kt >> 1) & 1;
+                if (kt + 2 < nkv) {  // S(kt) has read key stage bb: refill it
+                    ok = mbar_wait(s_full + 8 * bb, ph);
+                    if (ok) load_k(kt + 2);
+                }
+                ok = ok && mbar_wait(p_full + 8 * bb, ph) && mbar_wait(bar_v + 8 * bb, ph);
+                if (!ok) break;
+                tc_fence_after();
+                // O_k += Ph_k V_k + Pl_k V_k for key half k (keys 32 k .. + 31: two slices of 16)
+                const uint32_t vs = base + kOffV + bb * kVImg, pb = base + kOffP + bb * 2 * kPImg;
+#pragma unroll 1
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll 1
+                    for (int k = 0; k < 2; ++k) {
+                        const uint32_t o = (2 * hf + k) * 32;
+                        const uint64_t dv = sw128_desc(vs + o);
+                        mma_bf16(tmem + 128 + 128 * hf, sw128_desc(pb + o), dv, idO, (kt > 0) | (k > 0));
+                        mma_bf16(tmem + 128 + 128 * hf, sw128_desc(pb + kPImg + o), dv, idO, 1);
+                    }
+                }
+                mma_commit(o_done + 8 * bb);
+                if (kt + 2 < nkv) {
+                    ok = mbar_wait(s_free + 8 * bb, ph) && mbar_wait(bar_k + 8 * bb, ((kt + 2) >> 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(kt + 2);
+                    ok = mbar_wait(o_done + 8 * bb, ph);  // P V of tile kt has read value stage bb
+                    if (ok) load_v(kt + 2);
+                }
             }
+            if (!ok) atomicOr(a.err, HSQ_DEVERR_WAIT);
         }
-        // P = exp2(x - m) as bf16 hi + lo: this thread's 4 chunks of its row of the P images
-        float psum = 0.f;
-        uint8_t* prow_h = gbase + kOffPh + row * 128;
-        uint8_t* prow_l = gbase + kOffPl + row * 128;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            uint32_t wh[4], wl[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p0 = ex2_approx(x[8 * cc + 2 * e] - m_used), p1 = ex2_approx(x[8 * cc + 2 * e + 1] - m_used);
-                psum += p0 + p1;
-                const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
-                const __nv_bfloat162 lp = __floats2bfloat162_rn(p0 - __low2float(hp), p1 - __high2float(hp));
-                wh[e] = *reinterpret_cast<const uint32_t*>(&hp);
-                wl[e] = *reinterpret_cast<const uint32_t*>(&lp);
-            }
-            const uint32_t off = (uint32_t)(((4 * half + cc) ^ (row & 7)) << 4);
-            *reinterpret_cast<uint4*>(prow_h + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-            *reinterpret_cast<uint4*>(prow_l + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        }
-        lsum += psum;
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
+    } else {
+        // ---- softmax: 8 warps, query row = TMEM lane, key half = warp >> 2 ----
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = 32 * quarter + lanei;
+        const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+        const uint32_t tO = tmem + lanes + 128 + 128 * half;
+        const int t = qt * kPfRows + row;
+        float m_used = -INFINITY, lsum = 0.f;
+#pragma unroll 1
+        for (int kt = 0; kt < nkv; ++kt) {
+            const int bb = kt & 1;
+            const uint32_t ph = (kt >> 1) & 1;
+            ok = mbar_wait(s_full + 8 * bb, ph);
+            if (!ok) break;
             tc_fence_after();
-            // O += Ph V + Pl V over the 64 keys (4 slices of 16)
+            float x[32];
+            tmem_ld32(tmem + lanes + 64 * bb + 32 * half, x);
+            tc_fence_before();
+            mbar_arrive(s_free + 8 * bb);
+            const int key0 = kt * kPfKeys + 32 * half;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                x[c] = key0 + c <= t ? x[c] * kLogitScaleLog2 : -INFINITY;
+                mt = fmaxf(mt, x[c]);
+            }
+            const float m_new = fmaxf(m_used, mt);
+            const bool raise = m_new > m_used + 8.f;  // (the half's first unmasked key raises it from -inf)
+            const float alpha = raise ? (m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new)) : 1.f;
+            if (raise) {
+                lsum *= alpha;
+                m_used = m_new;
+            }
+            if (kt > 0 && __any_sync(0xffffffffu, raise)) {  // rescale this half's O row: P V of tile kt - 1 first
+                ok = mbar_wait(o_done + 8 * (bb ^ 1), ((kt - 1) >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll 1
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t dv = sw128_desc(stage + 2 * kKImg + k * 32);
-                mma_bf16(tmem + 128, sw128_desc(base + kOffPh + k * 32), dv, idO, (kt > 0) | (k > 0));
-                mma_bf16(tmem + 128, sw128_desc(base + kOffPl + k * 32), dv, idO, 1);
+                for (int c0 = 0; c0 < kDim; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tO + c0, o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                    tmem_st32(tO + c0, o);
+                }
             }
-            mma_commit(bar_mma);
-            if (mbar_wait(bar_mma, ph_mma)) {
-                if (kt + 2 < nkv) load_kv(kt + 2, st);  // the stage is free again
-            } else {
-                s_abort = 1;
-                atomicOr(a.err, HSQ_DEVERR_WAIT);
+            if (kt >= 2) {  // P buffer bb: P V of tile kt - 2 has read it
+                ok = mbar_wait(o_done + 8 * bb, ph ^ 1u);
+                if (!ok) break;
             }
+            const float m_eff = m_used == -INFINITY ? 0.f : m_used;  // (no key yet: every p is 0)
+            float psum = 0.f;
+            uint8_t* prow_h = gbase + kOffP + bb * 2 * kPImg + row * 128;
+            uint8_t* prow_l = prow_h + kPImg;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t wh[4], wl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(x[8 * cc + 2 * e] - m_eff), p1 = ex2_approx(x[8 * cc + 2 * e + 1] - m_eff);
+                    psum += p0 + p1;
+                    const __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
+                    const __nv_bfloat162 lp = __floats2bfloat162_rn(p0 - __low2float(hp), p1 - __high2float(hp));
+                    wh[e] = *reinterpret_cast<const uint32_t*>(&hp);
+                    wl[e] = *reinterpret_cast<const uint32_t*>(&lp);
+                }
+                const uint32_t off = (uint32_t)(((4 * half + cc) ^ (row & 7)) << 4);
+                *reinterpret_cast<uint4*>(prow_h + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4*>(prow_l + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+            }
+            lsum += psum;
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full + 8 * bb);
         }
-        ph_mma ^= 1u;
-        tc_fence_before();
-        __syncthreads();
-        if (s_abort) break;
+        if (ok) ok = mbar_wait(o_done + 8 * ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1);  // the last P V
+        if (!ok) atomicOr(a.err, HSQ_DEVERR_WAIT);
+        // the row's two halves: maxima and sums, then each thread writes output columns
+        // 64 half .. + 63 from its own O there plus the other half's (through the key stages)
+        named_bar_sync(1, kPfSoftThreads);
+        float (*s_ml)[2][kPfRows] = reinterpret_cast<float (*)[2][kPfRows]>(gbase + kOffV);
+        s_ml[half][0][row] = m_used;
+        s_ml[half][1][row] = lsum;
+        named_bar_sync(1, kPfSoftThreads);
         tc_fence_after();
-    }
-
-    // the row's sum: this half's plus the other half's (same rescalings)
-    s_mx[half][row] = lsum;
-    __syncthreads();
-    if (!s_abort) {
-        tc_fence_after();
-        const float l = lsum + s_mx[half ^ 1][row];
-        const float inv = l > 0.f ? 1.0f / l : 0.f;
+        const float m_o = s_ml[half ^ 1][0][row], l_o = s_ml[half ^ 1][1][row];
+        const float M = fmaxf(m_used, m_o);
+        const float w_me = m_used == -INFINITY ? 0.f : ex2_approx(m_used - M);
+        const float w_ot = m_o == -INFINITY ? 0.f : ex2_approx(m_o - M);
+        const float L = lsum * w_me + l_o * w_ot;
+        const float inv = L > 0.f ? 1.0f / L : 0.f;
+        float* xch = reinterpret_cast<float*>(gbase + kOffK);  // [2 halves][128 rows][64 columns]
+        float o[32];
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            tmem_ld32(tO + 64 * (half ^ 1) + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) xch[((half ^ 1) * kPfRows + row) * 64 + c0 + c] = o[c] * w_me;
+        }
+        named_bar_sync(1, kPfSoftThreads);
         float* orow = a.out + (((size_t)b * a.Hq + j) * a.T + (t < a.T ? t : 0)) * kDim + 64 * half;
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
-            float o[32];
-            tmem_ld32(tO + c0, o);
-            if (t < a.T) {
+            tmem_ld32(tO + 64 * half + c0, o);
+            if (t < a.T && ok) {
+                const float* other = xch + ((size_t)half * kPfRows + row) * 64 + c0;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)
                     *reinterpret_cast<float4*>(orow + c0 + c) =
-                        make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+                        make_float4((o[c] * w_me + other[c]) * inv, (o[c + 1] * w_me + other[c + 1]) * inv,
+                                    (o[c + 2] * w_me + other[c + 2]) * inv, (o[c + 3] * w_me + other[c + 3]) * inv);
             }
         }
     }

@@ -52,6 +52,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int max
     return false;
 }
 
+// one arrival on the barrier's current phase
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// barrier `id` (1..15) among `count` threads (a multiple of 32) of the CTA
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- bulk copy (1-D, no tensor map): both addresses 16-byte aligned, size a multiple of 16
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
