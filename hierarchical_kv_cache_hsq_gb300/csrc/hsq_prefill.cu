@@ -23,21 +23,24 @@
 // Rows past T are zero.
 //
 // Attention kernel: one CTA per (128-query tile, query head, sequence), warp
-// specialised.  Warp 8 (one thread) is the producer: it issues every bulk
-// copy and every MMA -- S = Q K^T of tile k (128 x 64, into TMEM columns 0-63
-// or 64-127 in turn), then, once the softmax has written P of tile k, O_half
-// += P_half V_half for both key halves (TMEM columns 128-255 and 256-383) --
-// and refills each key / value stage when the MMA that read it completed.
-// Warps 0-7 run the softmax: query row r of the tile is TMEM lane r (a warp
-// reaches only its quarter of the lanes, 32 (w & 3) .. + 31) and warp w
-// handles the key half w >> 2 of every 64-key tile, so two threads share a
-// row; each key half keeps its own online softmax (log2 domain; its running
-// maximum is raised only when a logit exceeds it by more than 8, then its O
-// in TMEM is rescaled) and its own accumulator, combined once at the end.
-// The roles meet only on mbarriers (S full / S read / P full / O done, two of
-// each, one per buffer), so the S of the next tiles runs on the tensor cores
-// while the softmax of this one runs, and P is double-buffered.  The output
-// is the combined O / l in fp32.
+// specialised.  Two producer warps, one thread each: warp 8 loads the key
+// tiles and issues S = Q K^T of tile k (128 x 64, into TMEM columns 0-63 or
+// 64-127 in turn) as soon as the tile's keys have landed and the softmax has
+// read the buffer's previous S; warp 9 loads the value tiles and, once the
+// softmax has written P of tile k, issues O_half += P_half V_half for both
+// key halves (TMEM columns 128-255 and 256-383).  Each refills its stage when
+// the MMA that read it completed.  Warps 0-7 run the softmax: query row r of
+// the tile is TMEM lane r (a warp reaches only its quarter of the lanes,
+// 32 (w & 3) .. + 31) and warp w handles the key half w >> 2 of every 64-key
+// tile, so two threads share a row; each key half keeps its own online
+// softmax (log2 domain: the queries carry the scale log2(e) / sqrt(d); its
+// running maximum is raised only when a logit exceeds it by more than 8,
+// then its O in TMEM is rescaled) and its own accumulator, combined once at
+// the end; only the two diagonal tiles apply the causal mask.  The roles
+// meet only on mbarriers (S full / S read / P full / O done, two of each,
+// one per buffer), so the S of the next tiles runs on the tensor cores while
+// the softmax of this one runs, and P is double-buffered.  The output is the
+// combined O / l in fp32.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -53,7 +56,7 @@ using namespace hsq_tc;
 constexpr int kPfRows = 128;                          // query rows per CTA (TMEM lanes)
 constexpr int kPfKeys = 64;                           // keys per tile
 constexpr int kPfSoftThreads = 256;                   // softmax warps 0-7
-constexpr int kPfThreads = kPfSoftThreads + 32;       // + the producer warp
+constexpr int kPfThreads = kPfSoftThreads + 64;       // + the two producer warps
 constexpr uint32_t kQImg = kPfRows * kDim * 2;        // 32 KB
 constexpr uint32_t kKImg = kPfKeys * kDim * 2;        // 16 KB
 constexpr uint32_t kVImg = kDim * kPfKeys * 2;        // 16 KB
@@ -110,10 +113,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 8 * kNumBars);
     bool ok = true;
 
-    if (warp == kPfSoftThreads / 32) {
-        // ---- producer: bulk copies and MMAs, one thread ----
-        if (lanei == 0) {
-            const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
+    if (warp >= kPfSoftThreads / 32) {
+        // ---- producers, one thread each: warp 8 the keys and S, warp 9 the values and P V ----
+        const size_t kv0 = ((size_t)b * a.Hkv + h) * a.nkt;
+        if (warp == kPfSoftThreads / 32 && lanei == 0) {
             auto load_k = [&](int kt) {
                 const int st = kt & 1;
                 const uint32_t dst = base + kOffK + st * 2 * kKImg, bar = bar_k + 8 * st;
@@ -121,14 +124,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                 bulk_g2s(dst, a.kh + (kv0 + kt) * kKImg, kKImg, bar);
                 bulk_g2s(dst + kKImg, a.kl + (kv0 + kt) * kKImg, kKImg, bar);
             };
-            auto load_v = [&](int kt) {
-                const int st = kt & 1;
-                mbar_expect_tx(bar_v + 8 * st, kVImg);
-                bulk_g2s(base + kOffV + st * kVImg, a.vt + (kv0 + kt) * kVImg, kVImg, bar_v + 8 * st);
-            };
-            constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys), idO = idesc_bf16_f32(kPfRows, kDim);
-            auto issue_s = [&](int kt) {  // S of tile kt into buffer kt & 1: Qh Kh^T + Ql Kh^T + Qh Kl^T
-                const uint32_t ks = base + kOffK + (kt & 1) * 2 * kKImg, dS = tmem + 64 * (kt & 1);
+            constexpr uint32_t idS = idesc_bf16_f32(kPfRows, kPfKeys);
+            const size_t qi = ((size_t)b * a.Hq + j) * a.nqt + qt;
+            mbar_expect_tx(bar_q, 2 * kQImg);
+            bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
+            bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
+            for (int kt = 0; kt < min(nkv, 2); ++kt) load_k(kt);
+            ok = mbar_wait(bar_q, 0);
+#pragma unroll 1
+            for (int kt = 0; kt < nkv && ok; ++kt) {
+                const int bb = kt & 1;
+                const uint32_t ph = (kt >> 1) & 1;
+                if (kt >= 2) ok = mbar_wait(s_free + 8 * bb, ph ^ 1u);  // the softmax has read S(kt - 2)
+                ok = ok && mbar_wait(bar_k + 8 * bb, ph);
+                if (!ok) break;
+                tc_fence_after();
+                // S of tile kt into buffer bb: Qh Kh^T + Ql Kh^T + Qh Kl^T over the 128 dims
+                const uint32_t ks = base + kOffK + bb * 2 * kKImg, dS = tmem + 64 * bb;
 #pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
                     const uint32_t qo = (k >> 2) * (kQImg / 2) + (k & 3) * 32;
@@ -139,33 +151,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                     mma_bf16(dS, dql, dkh, idS, 1);
                     mma_bf16(dS, dqh, dkl, idS, 1);
                 }
-                mma_commit(s_full + 8 * (kt & 1));
-            };
-            const size_t qi = ((size_t)b * a.Hq + j) * a.nqt + qt;
-            mbar_expect_tx(bar_q, 2 * kQImg);
-            bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
-            bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
-            for (int kt = 0; kt < min(nkv, 2); ++kt) {
-                load_k(kt);
-                load_v(kt);
-            }
-            ok = mbar_wait(bar_q, 0);
-            for (int kt = 0; kt < min(nkv, 2) && ok; ++kt) {
-                ok = mbar_wait(bar_k + 8 * kt, 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(kt);
-                }
-            }
-#pragma unroll 1
-            for (int kt = 0; kt < nkv && ok; ++kt) {
-                const int bb = kt & 1;
-                const uint32_t ph = (kt >> 1) & 1;
+                mma_commit(s_full + 8 * bb);
                 if (kt + 2 < nkv) {  // S(kt) has read key stage bb: refill it
                     ok = mbar_wait(s_full + 8 * bb, ph);
                     if (ok) load_k(kt + 2);
                 }
-                ok = ok && mbar_wait(p_full + 8 * bb, ph) && mbar_wait(bar_v + 8 * bb, ph);
+            }
+            if (!ok) atomicOr(a.err, HSQ_DEVERR_WAIT);
+        } else if (warp == kPfSoftThreads / 32 + 1 && lanei == 0) {
+            auto load_v = [&](int kt) {
+                const int st = kt & 1;
+                mbar_expect_tx(bar_v + 8 * st, kVImg);
+                bulk_g2s(base + kOffV + st * kVImg, a.vt + (kv0 + kt) * kVImg, kVImg, bar_v + 8 * st);
+            };
+            constexpr uint32_t idO = idesc_bf16_f32(kPfRows, kDim);
+            for (int kt = 0; kt < min(nkv, 2); ++kt) load_v(kt);
+#pragma unroll 1
+            for (int kt = 0; kt < nkv && ok; ++kt) {
+                const int bb = kt & 1;
+                const uint32_t ph = (kt >> 1) & 1;
+                ok = mbar_wait(p_full + 8 * bb, ph) && mbar_wait(bar_v + 8 * bb, ph);
                 if (!ok) break;
                 tc_fence_after();
                 // O_k += Ph_k V_k + Pl_k V_k for key half k (keys 32 k .. + 31: two slices of 16)
@@ -181,12 +186,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                     }
                 }
                 mma_commit(o_done + 8 * bb);
-                if (kt + 2 < nkv) {
-                    ok = mbar_wait(s_free + 8 * bb, ph) && mbar_wait(bar_k + 8 * bb, ((kt + 2) >> 1) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(kt + 2);
-                    ok = mbar_wait(o_done + 8 * bb, ph);  // P V of tile kt has read value stage bb
+                if (kt + 2 < nkv) {  // P V of tile kt has read value stage bb: refill it
+                    ok = mbar_wait(o_done + 8 * bb, ph);
                     if (ok) load_v(kt + 2);
                 }
             }
@@ -211,13 +212,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
             tmem_ld32(tmem + lanes + 64 * bb + 32 * half, x);
             tc_fence_before();
             mbar_arrive(s_free + 8 * bb);
-            const int key0 = kt * kPfKeys + 32 * half;
+            // (the queries carry the log2-domain softmax scale; only the two diagonal
+            // tiles have keys after some of the tile's queries)
             float mt = -INFINITY;
+            if (kt >= nkv - 2) {
+                const int key0 = kt * kPfKeys + 32 * half;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                x[c] = key0 + c <= t ? x[c] * kLogitScaleLog2 : -INFINITY;
-                mt = fmaxf(mt, x[c]);
+                for (int c = 0; c < 32; ++c) x[c] = key0 + c <= t ? x[c] : -INFINITY;
             }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
             const float m_new = fmaxf(m_used, mt);
             const bool raise = m_new > m_used + 8.f;  // (the half's first unmasked key raises it from -inf)
             const float alpha = raise ? (m_used == -INFINITY ? 0.f : ex2_approx(m_used - m_new)) : 1.f;
@@ -311,9 +315,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Query operand images: RoPE at the query's position in fp32, split into
-// bf16 hi + lo.  One CTA of 256 threads per (128-row tile, query head,
-// sequence); each half-warp handles 8 rows.
+// Query operand images: RoPE at the query's position in fp32, times the
+// softmax scale log2(e) / sqrt(d), split into bf16 hi + lo.  One CTA of 256
+// threads per (128-row tile, query head, sequence); each half-warp handles 8
+// rows.
 __global__ void __launch_bounds__(256) prefill_q_kernel(const uint16_t* __restrict__ Q, uint8_t* qh, uint8_t* ql,
                                                         int Hq, int T, int nqt, Tables tb) {
     const int qt = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
@@ -326,6 +331,8 @@ __global__ void __launch_bounds__(256) prefill_q_kernel(const uint16_t* __restri
         if (t < T) {
             load_bf16x8(Q + (((size_t)b * Hq + j) * T + t) * kDim, x);
             rope(x, t, tb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] *= kLogitScaleLog2;  // logits come out in the log2 domain
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = 0.f;
