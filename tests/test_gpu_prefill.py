@@ -50,6 +50,8 @@ CASES = {
     "r1_b2_t384": dict(B=2, Hq=2, Hkv=2, T=384),
     "r5_ragged_t200": dict(B=1, Hq=5, Hkv=1, T=200),
     "r4_ragged_t1001": dict(B=1, Hq=4, Hkv=1, T=1001),
+    "r2_b2_tiny_t37": dict(B=2, Hq=4, Hkv=2, T=37),   # one query tile, one partial key tile
+    "r8_t640": dict(B=1, Hq=8, Hkv=1, T=640),
 }
 
 
