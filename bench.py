@@ -71,6 +71,12 @@ def parse_args():
                    help="per-layer mode: every query head routes, fetches and attends with its own beta groups")
     p.add_argument("--route-max", action="store_true",
                    help="per-layer mode: route by each KV head's best query head (route + attention)")
+    p.add_argument("--hot-slots", type=int, default=0,
+                   help="per-layer mode: give the fused step a hot-group table of this many slots per "
+                        "(sequence, KV head) (a power of two in [16, 1024])")
+    p.add_argument("--correlated", action="store_true",
+                   help="per-layer mode: queries correlated across steps (the needle law of the 8B workload: "
+                        "a planted group per (b, KV head), every step's queries sqrt(0.8) q0 + sqrt(0.2) z)")
     p.add_argument("--prefill-only", type=int, default=0, metavar="T",
                    help="only the prefill measurement, on the 8B-shaped layer cut to T tokens (profiler captures)")
     return p.parse_args()
@@ -414,6 +420,66 @@ def measure_growth(H, torch, w, li, flush, clean, sink):
             "steps_per_s_with_append": 1e6 / med(t_step), "steps": n - 4,
             "how": f"hsq_append (one kernel) then hsq_decode_step per token, {n} tokens appended to the "
                    f"{w.T}-token layer (capacity {w.T + n}), recent window {w.recent}, L2 flushed per step"}
+
+
+HOT_SLOTS = 256
+
+
+def table_hit_rate(H, torch, ctx, cache, qd, pd, sel, out, slots, nsteps):
+    """Share of the selected groups found in the hot-group table over nsteps
+    decode steps (the table read back before each step)."""
+    hits = tot = 0
+    for i in range(nsteps):
+        tag = cache.view("hot_tag").cpu().numpy().copy()
+        H.hsq_decode_step(ctx, cache, qd[i % qd.shape[0]], pd[i % pd.shape[0]], sel, out)
+        s = sel.cpu().numpy()
+        for b in range(s.shape[0]):
+            for h in range(s.shape[1]):
+                g = s[b, h][s[b, h] >= 0]
+                hits += int(np.sum(tag[b, h, g % slots] == g))
+                tot += len(g)
+    return hits / max(tot, 1)
+
+
+def measure_hot_table(H, torch, w, li, qd, pd, flush, clean, sink, steps, warmup, table_free_us):
+    """The fused step with a hot-group table (HOT_SLOTS slots per (b, KV
+    head)) on the same layer, pinned L3, the same queries and L2 flush as the
+    headline loop; its hit rate over the first steps after an encode."""
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta, 0,
+                        hot_slots=HOT_SLOTS)
+    hctx = H.Context(cfg)
+    cache = H.allocate_cache(hctx, w.B, w.T, l3_on_host=True, with_staging=False)
+    H.set_layer_inputs(cache, li.l1_mask, li.signs)
+    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+    H.hsq_encode(hctx, cache, K, V)
+    del K, V
+    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+    out = torch.empty((w.B, w.Hq, 128), device="cuda")
+    ts = []
+    for i in range(warmup + steps):
+        s = i % qd.shape[0]
+        flush.fill_(i & 255)
+        torch.sum(clean, dim=0, out=sink)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record()
+        H.hsq_decode_step(hctx, cache, qd[s], pd[s], sel, out)
+        e[1].record()
+        e[1].synchronize()
+        if i >= warmup:
+            ts.append(e[0].elapsed_time(e[1]) * 1e3)
+    hit = table_hit_rate(H, torch, hctx, cache, qd, pd, sel, out, HOT_SLOTS, 16)  # steady state
+    assert H.hsq_sync_status(hctx) == 0
+    hctx.close()
+    med = statistics.median(ts)
+    rb = w.N * 136
+    return {"slots": HOT_SLOTS, "us_per_step_median": med, "us_per_step_mean": sum(ts) / len(ts),
+            "steps_per_s": 1e6 / (sum(ts) / len(ts)), "table_free_us_per_step_mean": table_free_us,
+            "hit_rate": hit, "hit_rate_how": "16 steps after the timed loop (the table warm)",
+            "l3_link_bytes_per_step": (1 - hit) * w.B * w.Hkv * w.beta * rb,
+            "how": "hsq_decode_step with hsq_config.hot_slots on a second cache of this layer; queries of the "
+                   "workload (correlated across steps), L2 flushed per step, each step synchronised; "
+                   "results bit-identical to the table-free step (GPU tests)"}
 
 
 def measure_codecs(H, torch, w, li):
@@ -795,6 +861,8 @@ def run_hsq(args, rank, world, local):
     codecs = None if args.quick else measure_codecs(H, torch, w, li)
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
+    hot = None if args.quick or args.codec != "tq" or args.qjl else measure_hot_table(
+        H, torch, w, li, qd, pd, flush, clean, sink, min(args.steps, 300), max(args.warmup, 3), ms_per_step * 1e3)
     mean = lambda x: sum(x) / len(x)
     hbm_peak, peak_src = measured_peaks()
     link_gbs = lp["h2d_gbs"]
@@ -871,6 +939,7 @@ def run_hsq(args, rank, world, local):
         "prefill": prefill,
         "small_workloads": small,
         "codec": codecs,
+        "hot_table": hot,
         "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,
@@ -944,6 +1013,8 @@ def run_layers(args, rank, world, local):
     w = W.get_workload(args.workload)
     if args.group_n:
         w = w.with_(N=args.group_n)
+    if args.correlated:
+        w = w.with_(needle=True)
     L = args.layers or w.layers
     betas = tuple(int(b) for b in args.betas.split(",")) if args.betas else (tuple(w.betas) or (w.beta,))
     placements = ("host", "device") if w.name == "qwen3_4b_b16_8k" else ("host",)
@@ -951,7 +1022,7 @@ def run_layers(args, rank, world, local):
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
                              args.n_splits, route_max=args.route_max, codec=args.codec,
-                             route_per_head=args.route_per_head) for b in betas}
+                             route_per_head=args.route_per_head, hot_slots=args.hot_slots) for b in betas}
     ctxs = {b: H.Context(c) for b, c in cfgs.items()}
     ctx0 = ctxs[betas[0]]
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
@@ -1055,7 +1126,18 @@ def run_layers(args, rank, world, local):
                 s0 = s_r.cpu().numpy()
                 per = rows_sel // w.Hkv
                 needle = all(int(li.needle_group[b, j // per]) in s0[b, j] for b in range(w.B) for j in range(rows_sel))
+            hot = None
+            if args.hot_slots:  # layer 0's table in steady state: 16 more steps after the timed loop
+                s_h = torch.empty((w.B, rows_sel, beta), dtype=torch.int32, device="cuda")
+                hit = table_hit_rate(H, torch, ctxs[beta], caches[pl][0], qd, pd, s_h, out, args.hot_slots, 16)
+                # the roofline of the bytes that move: records found in the table are read from HBM
+                hbm_h, link_h = hbm_avg + hit * link, (1 - hit) * link
+                t_h = (max(hbm_h / (hbm_peak * 1e9), link_h / (lp["h2d_gbs"] * 1e9)) if pl == "host"
+                       else (hbm_h + link_h) / (hbm_peak * 1e9))
+                hot = {"slots": args.hot_slots, "hit_rate_layer0": hit, "l3_link_bytes_per_layer": link_h,
+                       "hbm_bytes_per_layer": hbm_h, "t_star_us_per_layer": t_h * 1e6, "frac": t_h / t_layer}
             rows.append({"beta": beta, "l3": "pinned host" if pl == "host" else "device", "needle_routed": needle,
+                         "hot_table": hot,
                          "ms_per_step": ms, "steps_per_s": world * 1e3 / ms, "us_per_layer": t_layer * 1e6,
                          "hbm_bytes_per_layer": hbm_avg, "l3_bytes_per_layer": link,
                          "hbm_gbs": hbm_avg / t_layer / 1e9, "l3_gbs": link / t_layer / 1e9,
@@ -1077,6 +1159,8 @@ def run_layers(args, rank, world, local):
                    "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
                    "launch": "one CUDA graph per step (all layers)" if args.graph else "one call per layer",
                    "codec": args.codec,
+                   "hot_slots": args.hot_slots,
+                   "queries": "correlated across steps (needle law)" if w.needle else "independent per step",
                    "routing": "max over each KV head's query heads (route + attention)" if args.route_max
                               else "per query head: own selection, fetch and attention (fused step)"
                               if args.route_per_head else "sum over each KV head's query heads (fused step)",

@@ -29,7 +29,8 @@ HSQ_FAULT_ALLOC, HSQ_FAULT_FETCH = 1, 2
 HSQ_DEVERR_SEL, HSQ_DEVERR_POS, HSQ_DEVERR_L1_OVER, HSQ_DEVERR_WAIT, HSQ_DEVERR_GROW = 1, 2, 4, 8, 16
 
 BUFFERS = ["l1_kc", "l1_vc", "l1_kn", "l1_vn", "l1_pos", "l1_count", "l2_kc", "l2_vc", "l2_kn",
-           "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging", "win_kv", "gsum", "l1_qs", "l1_qn", "l3_qs", "l3_qn"]
+           "l2_vn", "l2_cnt", "l3", "l1_bitmap", "staging", "win_kv", "gsum", "l1_qs", "l1_qn", "l3_qs", "l3_qn",
+           "hot_rec", "hot_tag"]
 HSQ_NBUF = len(BUFFERS)
 CODECS = {"tq": 0, "plain": 1}  # hsq_codec
 
@@ -48,7 +49,7 @@ class hsq_config(ctypes.Structure):
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
         ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
         ("route_max", ctypes.c_int), ("codec", ctypes.c_int), ("route_per_head", ctypes.c_int),
-        ("qjl", ctypes.c_int),
+        ("qjl", ctypes.c_int), ("hot_slots", ctypes.c_int),
     ]
 
 
@@ -64,6 +65,7 @@ class hsq_cache(ctypes.Structure):
         ("t_cap", ctypes.c_int), ("win_kv", ctypes.c_void_p), ("gsum", ctypes.c_void_p),
         ("qjl_s", ctypes.c_void_p), ("l1_qs", ctypes.c_void_p), ("l1_qn", ctypes.c_void_p),
         ("l3_qs", ctypes.c_void_p), ("l3_qn", ctypes.c_void_p),
+        ("hot_rec", ctypes.c_void_p), ("hot_tag", ctypes.c_void_p),
     ]
 
 
@@ -141,21 +143,24 @@ def hsq_codebook(bits: int, dim: int = 128):
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
                 max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
                 recent: int = 0, route_max: bool = False, codec: str = "tq",
-                route_per_head: bool = False, qjl: bool = False) -> hsq_config:
+                route_per_head: bool = False, qjl: bool = False, hot_slots: int = 0) -> hsq_config:
     """recent > 0 makes caches of this context growable (hsq_append) with an
     L1 recent window of that length and `sinks` permanent sink positions;
     route_max scores a group by its best query head instead of their sum;
     codec "plain" quantises the unrotated unit vectors (Plain-KV) instead of
     TurboQuant's rotated ones; route_per_head gives every query head its own
     selection (sel [B, Hq, beta]); qjl adds TQ-QKV's 1-bit sketches of the key
-    residuals (set the sketch matrix with set_qjl_matrix)."""
+    residuals (set the sketch matrix with set_qjl_matrix); hot_slots > 0 gives
+    the fused decode step a device table of that many recently fetched L3
+    records per (sequence, KV head)."""
     if codec not in CODECS:
         raise ValueError(f"codec must be one of {tuple(CODECS)}")
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
                       bits_l1l3=4, bits_l2=3, rope_theta=theta, max_batch=max_batch,
                       max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
                       l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0,
-                      codec=CODECS[codec], route_per_head=1 if route_per_head else 0, qjl=1 if qjl else 0)
+                      codec=CODECS[codec], route_per_head=1 if route_per_head else 0, qjl=1 if qjl else 0,
+                      hot_slots=hot_slots)
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:
@@ -261,13 +266,16 @@ class CacheBuffers:
             "staging": (B, self.sel_heads or H, self.beta, N * 136),
             "win_kv": (B, H, self.recent, 2, 128), "gsum": (B, H, 260),
             "l1_qs": (B, H, L1, 4), "l1_qn": (B, H, L1), "l3_qs": (B, H, G * N, 4), "l3_qn": (B, H, G * N),
+            "hot_rec": (B, H, -1, N * 136), "hot_tag": (B, H, -1),
         }
         import torch
         dt = {"l1_kn": torch.float32, "l1_vn": torch.float32, "l2_kn": torch.float32,
               "l2_vn": torch.float32, "l1_pos": torch.int32, "l1_count": torch.int32,
               "l1_bitmap": torch.int32, "win_kv": torch.float32, "gsum": torch.float32,
               "l1_qs": torch.int32, "l1_qn": torch.float32, "l3_qs": torch.int32,
-              "l3_qn": torch.float32}.get(name, torch.uint8)
+              "l3_qn": torch.float32, "hot_tag": torch.int32}.get(name, torch.uint8)
+        if name.startswith("hot_"):
+            return t.view(dt).view(shapes[name])
         n = int(np.prod(shapes[name]))
         return t.view(dt)[:n].view(shapes[name])
 
@@ -296,9 +304,11 @@ def allocate_cache(ctx: Context, B: int, T: int, l3_on_host: bool = True, with_s
         n = max(sizes[name], 16)
         if name == "staging" and not with_staging:
             continue
-        if name in ("win_kv", "gsum", "l1_qs", "l1_qn", "l3_qs", "l3_qn") and sizes[name] == 0:
+        if name in ("win_kv", "gsum", "l1_qs", "l1_qn", "l3_qs", "l3_qn", "hot_rec", "hot_tag") and sizes[name] == 0:
             continue
-        if name == "l3" and l3_on_host:
+        if name == "hot_tag":  # every slot empty (-1)
+            t[name] = torch.full((n,), 255, dtype=torch.uint8, device=dev)
+        elif name == "l3" and l3_on_host:
             t[name] = torch.zeros(n, dtype=torch.uint8, pin_memory=True)
         else:
             t[name] = torch.zeros(n, dtype=torch.uint8, device=dev)

@@ -236,7 +236,14 @@ __device__ __forceinline__ void cluster_wait() {
 
 // kRot: TurboQuant (rotated frame); false: Plain-KV (identity, no signs).
 // kQJL: TQ-QKV, the logits of L1 and fetched tokens carry the residual-sketch term.
-template <int R, int N, bool kRoute, bool kStaged, bool kRot, bool kQJL = false>
+// kHot: the hot-group table -- a selected group whose slot g & hot_mask is
+// tagged g is read from the device copy instead of L3; a group fetched from L3
+// is copied into its slot, and tagged, when it is the only selected group of
+// this step mapping there (so a step never reads and writes one slot; every
+// slot is written by the one CTA that fetched its record).  Tags are staged
+// before the cluster barrier that precedes selection, so no CTA writes a tag
+// that another CTA of the cluster is still staging.
+template <int R, int N, bool kRoute, bool kStaged, bool kRot, bool kQJL = false, bool kHot = false>
 __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c, DecodeArgs a, Tables tb) {
     namespace cgx = cooperative_groups;
     constexpr int NT = dec_threads<R>(), NH = NT / 16, NW = NT / 32;
@@ -249,6 +256,10 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     __shared__ __align__(16) float s_x[NH][16];
     __shared__ SelectSmem s_ss;
     __shared__ __align__(16) uint32_t s_stats[kMaxSplits][4];  // per split: non-empty keys, max key, min key
+    static_assert(!kHot || kRoute, "the hot-group table belongs to the fused (routing) step");
+    constexpr int kHotSlots = kHot ? hsq::kMaxHotSlots : 32;
+    __shared__ __align__(16) int32_t s_htag[kHot ? hsq::kMaxHotSlots : 4];  // the table's tags at launch
+    __shared__ uint32_t s_hone[kHotSlots / 32], s_htwo[kHotSlots / 32];   // slots selected once / again
 
     constexpr int RB = N * 136;
     constexpr int kBatchRecs = kFetchBatchBytes / RB;
@@ -355,8 +366,12 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     for (int i = tid; i < L.nb0 * 32; i += NT)
         cp_async16(s_b0 + 4 * i, tb.rope_lo + (size_t)(N * (i >> 5)) * kDim + 4 * (i & 31));
     stage16(s_off, tb.rope_lo, N * kDim * 4);
+    if constexpr (kHot) stage16(s_htag, c.hot_tag + bb * (c.hot_mask + 1), (c.hot_mask + 1) * 4);
     cp_async_commit();
     for (int i = tid; i < (L.span + 31) / 32; i += NT) s_mask[i] = 0u;
+    if constexpr (kHot) {
+        for (int i = tid; i < kHotSlots / 32; i += NT) s_hone[i] = s_htwo[i] = 0u;
+    }
     if constexpr (st2) {
         if (tid < n2) s_dyn[L.cnt + tid] = cnt0;
 #pragma unroll 1
@@ -498,6 +513,13 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     for (int i = tid; i < c.beta; i += NT) {
         const int g = s_sel[i];
         if (g >= g0 && g < g1) atomicOr(&s_mask[(g - g0) >> 5], 1u << ((g - g0) & 31));
+        if constexpr (kHot) {
+            if (g >= 0) {
+                const int sl = g & c.hot_mask;
+                const uint32_t bit = 1u << (sl & 31);
+                if (atomicOr(&s_hone[sl >> 5], bit) & bit) atomicOr(&s_htwo[sl >> 5], bit);
+            }
+        }
     }
 
     // 4. gather this split's records (batch k: records f0 + k B .., loaded into
@@ -520,6 +542,10 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                 if (g >= 0) {
                     const uint8_t* src = a.from_staging ? c.staging + ((size_t)bh * c.beta + i) * RB
                                                         : c.l3 + (bb * c.G + g) * RB;
+                    if constexpr (kHot) {
+                        const int sl = g & c.hot_mask;
+                        if (s_htag[sl] == g) src = c.hot_rec + (bb * (c.hot_mask + 1) + sl) * RB;
+                    }
                     pre[u] = __ldcg(reinterpret_cast<const uint4*>(src) + off);
                 }
             }
@@ -651,6 +677,26 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                 for (int u = 0; u < kChunksPT; ++u) {
                     const int ch = tid + u * NT;
                     if (ch < kFetchBatchBytes / 16) dstb[ch] = pre[u];
+                }
+                if constexpr (kHot) {  // records fetched from L3 into their free slots
+                    const int hr0 = f0 + kb_ * kBatchRecs;
+                    const int hnb = min(kBatchRecs, f1 - hr0);
+#pragma unroll
+                    for (int u = 0; u < kChunksPT; ++u) {
+                        const int ch = tid + u * NT;
+                        if (ch < hnb * kRecChunks) {
+                            const int rec = ch / kRecChunks, off = ch - rec * kRecChunks;
+                            const int g = s_sel[hr0 + rec];
+                            const int sl = g & c.hot_mask;
+                            const uint32_t bit = 1u << (sl & 31);
+                            const bool once = ((s_hone[sl >> 5] & ~s_htwo[sl >> 5]) & bit) != 0u;
+                            if ((g >= 0) & once & (s_htag[sl] != g)) {
+                                const size_t slot = bb * (c.hot_mask + 1) + sl;
+                                __stcg(reinterpret_cast<uint4*>(c.hot_rec + slot * RB) + off, pre[u]);
+                                if (off == 0) c.hot_tag[slot] = g;
+                            }
+                        }
+                    }
                 }
             }
             __syncthreads();  // batch kb_ and its meta are in shared memory
@@ -845,14 +891,18 @@ cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaSt
 // fixed n_splits takes the largest launchable S.  0: nothing launchable.
 // The kernel variant of the context's codec.
 template <int R, int N, bool kRoute, bool kStaged>
-DecodeFn decode_fn(bool rot, bool qjl) {
+DecodeFn decode_fn(bool rot, bool qjl, bool hot) {
+    if constexpr (kRoute) {  // the hot-group table: TurboQuant, TQ-KV, fused step only
+        if (hot) return decode_kernel<R, N, kRoute, kStaged, true, false, true>;
+    }
     if (qjl) return decode_kernel<R, N, kRoute, kStaged, true, true>;  // TQ-QKV: TurboQuant only
     return rot ? decode_kernel<R, N, kRoute, kStaged, true> : decode_kernel<R, N, kRoute, kStaged, false>;
 }
 
 template <int R, int N, bool kRoute, bool kStaged>
 int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
-    const void* fn = (const void*)decode_fn<R, N, kRoute, kStaged>(ctx->cfg.codec != HSQ_CODEC_PLAIN, ctx->cfg.qjl != 0);
+    const void* fn = (const void*)decode_fn<R, N, kRoute, kStaged>(ctx->cfg.codec != HSQ_CODEC_PLAIN, ctx->cfg.qjl != 0,
+                                                                   ctx->cfg.hot_slots > 0);
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
     if (hsq::allow_big_clusters(fn, ctx->device) != cudaSuccess) return 0;
@@ -898,7 +948,7 @@ template <int R, int N, bool kRoute, bool kStaged>
 hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
     const DecodeLayout L =
         decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
-    const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0, v.qjl_s != nullptr);
+    const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0, v.qjl_s != nullptr, v.hot_tag != nullptr);
     const void* fn = (const void*)kern;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");

@@ -73,6 +73,11 @@ struct CacheView {
     const uint32_t* l1_bitmap;
     const int8_t* signs;
     const uint8_t* staging;
+    // hot-group table (fused decode step; NULL without one): slot i of view head bh
+    // at hot_rec + (bh * (hot_mask + 1) + i) * N * 136, its group in hot_tag
+    uint8_t* hot_rec;
+    int32_t* hot_tag;
+    int hot_mask;  // slots - 1
 };
 
 // ---------------------------------------------------------------------------
@@ -895,6 +900,9 @@ inline CacheView make_view(const hsq_ctx* ctx, const hsq_cache* c) {
     v.hdiv = 1; v.Hb = v.Hkv;
     if (ctx->cfg.qjl) {
         v.qjl_s = c->qjl_s; v.l1_qs = c->l1_qs; v.l1_qn = c->l1_qn; v.l3_qs = c->l3_qs; v.l3_qn = c->l3_qn;
+    }
+    if (ctx->cfg.hot_slots > 0) {
+        v.hot_rec = c->hot_rec; v.hot_tag = c->hot_tag; v.hot_mask = ctx->cfg.hot_slots - 1;
     }
     return v;
 }

@@ -182,6 +182,12 @@ std::string check_config(const hsq_config* c) {
     if (c->route_per_head && c->route_max) return "route_per_head and route_max exclude each other";
     if (c->qjl != 0 && c->qjl != 1) return "qjl must be 0 or 1";
     if (c->qjl && c->codec != HSQ_CODEC_TQ) return "qjl (TQ-QKV) needs the TurboQuant codec";
+    if (c->hot_slots != 0) {
+        if (c->hot_slots < 16 || c->hot_slots > hsq::kMaxHotSlots || (c->hot_slots & (c->hot_slots - 1)))
+            return "hot_slots must be 0 or a power of two in [16, 1024]";
+        if (c->codec != HSQ_CODEC_TQ || c->qjl || c->route_per_head)
+            return "hot_slots needs codec HSQ_CODEC_TQ, qjl 0 and route_per_head 0";
+    }
     return "";
 }
 
@@ -198,6 +204,9 @@ std::string check_cache_shape(const hsq_config* cfg, const hsq_cache* c) {
     if (!c->signs && cfg->codec != HSQ_CODEC_PLAIN) return "signs is NULL";
     if (cfg->qjl && (!c->qjl_s || !c->l1_qs || !c->l1_qn || !c->l3_qs || !c->l3_qn))
         return "a key-residual sketch buffer is NULL (cfg.qjl)";
+    if (cfg->hot_slots && (!c->hot_rec || !c->hot_tag)) return "hot_rec or hot_tag is NULL (cfg.hot_slots)";
+    if (cfg->hot_slots && (((uintptr_t)c->hot_rec | (uintptr_t)c->hot_tag) & 15u))
+        return "hot_rec and hot_tag must be 16-byte aligned";
     return "";
 }
 
@@ -249,6 +258,9 @@ hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ
     bytes[HSQ_BUF_L1_QN] = q * B * H * L1 * 4;
     bytes[HSQ_BUF_L3_QS] = q * B * H * G * N * 16;
     bytes[HSQ_BUF_L3_QN] = q * B * H * G * N * 4;
+    const size_t hs = (size_t)cfg->hot_slots;  // hot-group table: records and tags
+    bytes[HSQ_BUF_HOT_REC] = B * H * hs * hsq::record_bytes((int)N);
+    bytes[HSQ_BUF_HOT_TAG] = B * H * hs * 4;
     return HSQ_OK;
 }
 

@@ -17,6 +17,7 @@ constexpr int kRopeRowFloats = kDim;        // cos[64] | sin[64]
 constexpr int kCodebookFloats = 48;         // c4[16] | t4[15] pad | c3[8] | t3[7] pad
 constexpr int kGsumFloats = 2 * 128 + 4;    // growth sums: RoPE'd keys | values | count | pad
 constexpr int kPartStride = 132;            // acc[128] | m | l | pad | pad
+constexpr int kMaxHotSlots = 1024;          // largest hot-group table per (b, KV head)
 
 inline int groups_of(int T, int N) { return (T + N - 1) / N; }
 inline int bitmap_words(int T) { return (T + 31) / 32; }

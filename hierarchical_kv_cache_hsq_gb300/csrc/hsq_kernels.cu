@@ -512,6 +512,10 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
         reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
         if (l == 0) reinterpret_cast<float*>(rec + N * 128)[half * N + t % N] = n;
     }
+    if (c.hot_tag && threadIdx.x == 32 * h) {  // the hot-group table's copy of group t / N is stale
+        int32_t* tag = c.hot_tag + bh * (c.hot_mask + 1) + ((t / N) & c.hot_mask);
+        if (*tag == t / N) *tag = -1;
+    }
     // L1 entry (RoPE'd key, value as coded for L3)
     if (slot >= 0) {
         const size_t so = bh * c.max_l1 + slot;
@@ -890,6 +894,8 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
         // key rows past the encode's groups: the attention reads them as zeros
         HSQ_CUDA(ctx, cudaMemsetAsync(pf->kh, 0, pf->bytes - (size_t)(pf->kh - pf->qh), s));
     }
+    if (v.hot_tag)  // the hot-group table holds copies of the old records: empty it
+        HSQ_CUDA(ctx, cudaMemsetAsync(v.hot_tag, 0xFF, (size_t)v.B * v.Hkv * (v.hot_mask + 1) * 4, s));
     l1_index_kernel<<<v.B, 1024, 0, s>>>(v, cache->l1_pos, cache->l1_count, ctx->d_prefix, ctx->d_err);
     const bool grow = ctx->cfg.l1_recent > 0 && cache->win_kv && cache->gsum;
     EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,

@@ -149,6 +149,20 @@ typedef struct hsq_config {
        input is read a second time); hsq_append refuses it (HSQ_ERR_UNSUPPORTED).
        0: TQ-KV. */
     int qjl;
+    /* Hot-group table of the fused decode step (hsq_decode_step only): 0 = none;
+       else a power of two in [16, 1024], the slots of a direct-mapped device
+       copy of recently fetched L3 records per (sequence, KV head).  Group g
+       lives in slot g mod hot_slots.  A step reads a selected group's record
+       from its slot when the slot's tag is g (no host-link transfer); a record
+       it fetched from L3 is copied into its slot, and the tag set, when no
+       other group of the step's selection maps to that slot (so a step never
+       reads and writes one slot).  Results are bit-identical with and without
+       the table.  The cache then needs hot_rec and hot_tag; hsq_encode empties
+       the table, hsq_append drops the group it writes.  An engineering
+       addition (the pages describe no such cache): it saves host-link bytes
+       when consecutive steps select overlapping groups.  Needs codec
+       HSQ_CODEC_TQ, qjl 0 and route_per_head 0. */
+    int hot_slots;
 } hsq_config;
 
 /*
@@ -202,13 +216,17 @@ typedef struct hsq_cache {
     float* l1_qn;             /* [B][Hkv][max_l1] device: their norms */
     uint32_t* l3_qs;          /* [B][Hkv][G*N][4] device: sketches of every token's key residual */
     float* l3_qn;             /* [B][Hkv][G*N] device: their norms */
+    /* Hot-group table (cfg.hot_slots > 0; else ignored). */
+    uint8_t* hot_rec;         /* [B][Hkv][hot_slots][N*136] device: copies of L3 records */
+    int32_t* hot_tag;         /* [B][Hkv][hot_slots] device: the group in each slot, -1 = empty */
 } hsq_cache;
 
 typedef enum {
     HSQ_BUF_L1_KC = 0, HSQ_BUF_L1_VC, HSQ_BUF_L1_KN, HSQ_BUF_L1_VN, HSQ_BUF_L1_POS,
     HSQ_BUF_L1_COUNT, HSQ_BUF_L2_KC, HSQ_BUF_L2_VC, HSQ_BUF_L2_KN, HSQ_BUF_L2_VN,
     HSQ_BUF_L2_CNT, HSQ_BUF_L3, HSQ_BUF_L1_BITMAP, HSQ_BUF_STAGING, HSQ_BUF_WIN_KV,
-    HSQ_BUF_GSUM, HSQ_BUF_L1_QS, HSQ_BUF_L1_QN, HSQ_BUF_L3_QS, HSQ_BUF_L3_QN, HSQ_NBUF
+    HSQ_BUF_GSUM, HSQ_BUF_L1_QS, HSQ_BUF_L1_QN, HSQ_BUF_L3_QS, HSQ_BUF_L3_QN,
+    HSQ_BUF_HOT_REC, HSQ_BUF_HOT_TAG, HSQ_NBUF
 } hsq_buffer;
 
 typedef struct hsq_ctx hsq_ctx;   /* opaque, library-owned */
@@ -263,7 +281,8 @@ hsq_status hsq_destroy(hsq_ctx* ctx);
  *   records past T (up to t_cap) are written empty.  With cfg.qjl it also
  *   writes the key-residual sketches (l1_qs / l1_qn, l3_qs / l3_qn) from
  *   cache->qjl_s, reading K a second time.  Under HSQ_CODEC_PLAIN every "Pi"
- *   here is the identity and signs is not read.
+ *   here is the identity and signs is not read.  With cfg.hot_slots it empties
+ *   the hot-group table (every hot_tag -1).
  *   Errors: HSQ_ERR_INVALID (null pointer, B/T out of range, L3 location not
  *   matching l3_on_host), HSQ_ERR_CUDA.  An L1 set larger than max_l1 sets
  *   HSQ_DEVERR_L1_OVER.
@@ -283,7 +302,9 @@ hsq_status hsq_encode(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
  *       that leaves the window (a new slot when p < max(l1_sinks, 0));
  *     p joins group p / N: its summary is re-quantised from the members'
  *       running float sums (position order, as hsq_encode sums them);
- *     the L1 bitmap, positions and counts and l2_cnt follow.
+ *     the L1 bitmap, positions and counts and l2_cnt follow;
+ *     with cfg.hot_slots, the hot-group table drops group T / N of every
+ *       (b, h) if it holds it (its record changed).
  *   k, v: device [B][Hkv][128] of dtype, pre-RoPE.  Needs cfg.l1_recent > 0,
  *   cache->win_kv and cache->gsum (filled by hsq_encode under this cfg),
  *   T < t_cap and T < max_pos.  L1 slots are then no longer in position
@@ -386,7 +407,10 @@ hsq_status hsq_decode_attn(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
  *   cluster shape can be launched.  Per-query-head routing and TQ-QKV stay
  *   one launch.  q, pos, sel, out: as for those calls (device memory,
  *   or mapped page-locked host memory for a step with no separate copies).
- *   Errors as the two calls.
+ *   With cfg.hot_slots the fused launch reads and fills the cache's hot-group
+ *   table (hsq_config.hot_slots); the separate calls do not use it.
+ *   Errors as the two calls, and HSQ_ERR_INVALID when cfg.hot_slots is set and
+ *   hot_rec or hot_tag is NULL.
  */
 hsq_status hsq_decode_step(hsq_ctx* ctx, const hsq_cache* cache, const float* q,
                            const int32_t* pos, int32_t* sel, float* out, hsq_stream_t stream);

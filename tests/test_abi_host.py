@@ -162,3 +162,17 @@ def test_qjl_sizes_and_codec_requirement(H):
     assert q["l1_qs"] == 2 * 8 * 100 * 16 and q["l1_qn"] == 2 * 8 * 100 * 4
     with pytest.raises(H.HSQError):
         H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, codec="plain", qjl=True), 2, 4096)
+
+
+def test_hot_table_sizes_and_requirements(H):
+    base = H.hsq_cache_sizes(H.make_config(40, 8, 16, 256, 4, 32768, 600, 40000), 4, 32768)
+    hot = H.hsq_cache_sizes(H.make_config(40, 8, 16, 256, 4, 32768, 600, 40000, hot_slots=1024), 4, 32768)
+    assert base["hot_rec"] == 0 and base["hot_tag"] == 0
+    assert hot["hot_rec"] == 4 * 8 * 1024 * 16 * 136 and hot["hot_tag"] == 4 * 8 * 1024 * 4
+    assert {k: v for k, v in hot.items() if not k.startswith("hot_")} == \
+        {k: v for k, v in base.items() if not k.startswith("hot_")}
+    for bad in (dict(hot_slots=8), dict(hot_slots=100), dict(hot_slots=2048), dict(hot_slots=-16),
+                dict(hot_slots=64, qjl=True), dict(hot_slots=64, codec="plain"),
+                dict(hot_slots=64, route_per_head=True)):
+        with pytest.raises(H.HSQError):
+            H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, **bad), 2, 4096)
