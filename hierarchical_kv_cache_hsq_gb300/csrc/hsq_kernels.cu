@@ -278,25 +278,34 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 
 // ---------------------------------------------------------------------------
 // TQ-QKV, encode side: the 1-bit sketches of the key residuals.  One CTA per
-// (group g, KV head h, sequence b), one warp per token: half 0 sketches the
-// L3 key's residual, half 1 the L1 key's when the token is in L1.  Both
-// halves redo the quantiser decision of encode_kernel with the same
+// (group g, KV head h, sequence b), one half-warp per token (N / 2 warps):
+// every token's L3 key residual, then, for the tokens in L1, the L1 key's.
+// Both redo the quantiser decision of encode_kernel with the same
 // arithmetic, so the residual is that of the stored codes.
 // ---------------------------------------------------------------------------
 
 struct SketchOut {
-    const float* S; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
+    // S blocked: element (i, 4 j + k) of the row-major [128][128] sketch matrix at
+    // (j * 128 + i) * 4 + k, so the 32 lanes of a warp, one row each, read 512
+    // contiguous bytes per float4 step
+    const float* Sb; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
 };
 
+__global__ void __launch_bounds__(256) qjl_block_kernel(const float* __restrict__ S, float* __restrict__ Sb) {
+    const int e = blockIdx.x * 256 + threadIdx.x;  // destination float4 (j, i)
+    const int j = e >> 7, i = e & (kDim - 1);
+    reinterpret_cast<float4*>(Sb)[e] = __ldg(reinterpret_cast<const float4*>(S + (size_t)i * kDim) + j);
+}
+
 template <int N, bool kBF16>
-__global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp, Tables tb) {
+__global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp, Tables tb) {
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
-    __shared__ __align__(16) float s_rho[N][2][kDim];
+    __shared__ __align__(16) float s_rho[N][2][kDim];  // [token][L3, L1]
     __shared__ long long s_dst[N][2];
 
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1, l = hlane();
+    const int tk = threadIdx.x >> 4, l = hlane();  // token of this half-warp
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
     __syncthreads();
@@ -305,7 +314,7 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
     float sg[8];
     load_signs(sg, s_sign);
 
-    const int t = g * N + warp;
+    const int t = g * N + tk;
     const bool in_ctx = t < c.T;
     bool is_l1 = false;
     int slot = 0;
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
         is_l1 = (w >> (t & 31)) & 1u;
         if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
     }
-    const bool active = in_ctx && (half == 0 || (is_l1 && slot < c.max_l1));  // uniform per half-warp
+    const bool l1_active = in_ctx && is_l1 && slot < c.max_l1;  // uniform per half-warp
 
     float x[8];
     if (in_ctx) {
@@ -325,12 +334,13 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = 0.f;
     }
+    // L3: e = n (y - c4[code]) is Pi (k - k^); back to the original frame, RoPE to
+    // position t, and into the rotated frame again
     float rho[8];
-    if (half == 0) {
-        // L3: e = n (y - c4[code]) is Pi (k - k^); back to the original frame, RoPE to
-        // position t, and into the rotated frame again
+    float n;
+    {
         float y[8];
-        const float n = tq_rotate(x, y, sg, m, true);
+        n = tq_rotate(x, y, sg, m, true);
 #pragma unroll
         for (int i = 0; i < 8; ++i) rho[i] = n * (y[i] - c4[quant4(y[i], t4)]);
         fwht(rho, m);
@@ -342,70 +352,68 @@ __global__ void __launch_bounds__(N * 32) qjl_kernel(CacheView c, SketchOut o, c
         fwht(rho, m);
 #pragma unroll
         for (int i = 0; i < 8; ++i) rho[i] *= kRsqrtD;
-    } else {
-        // L1: the stored key is TQ4 of RoPE(k, t) with the raw key's norm n
+    }
+    auto put = [&](int hf, bool active, long long e) {  // residual norm, smem row, destination
         float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-        const float n = sqrtf(half_sum(ss, m));
-        rope(x, in_ctx ? t : 0, tb);
+        for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
+        const float gamma = sqrtf(half_sum(ss, m));
+        float* row = s_rho[tk][hf];
+        *reinterpret_cast<float4*>(row + 4 * l) = make_float4(rho[0], rho[1], rho[2], rho[3]);
+        *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(rho[4], rho[5], rho[6], rho[7]);
+        if (l == 0) {
+            s_dst[tk][hf] = active ? e : -1;  // destination sketch slot, -1: none
+            if (active) (hf == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
+        }
+    };
+    put(0, in_ctx, ((long long)b * c.Hkv + h) * c.G * N + t);
+    if (l1_active) {
+        // L1: the stored key is TQ4 of RoPE(k, t) with the raw key's norm n
+        rope(x, t, tb);
         float yr[8];
         const float nr = tq_rotate(x, yr, sg, m, true);
 #pragma unroll
         for (int i = 0; i < 8; ++i) rho[i] = nr * yr[i] - n * c4[quant4(yr[i], t4)];
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
-    const float gamma = sqrtf(half_sum(ss, m));
-    float* row = s_rho[warp][half];
-    *reinterpret_cast<float4*>(row + 4 * l) = make_float4(rho[0], rho[1], rho[2], rho[3]);
-    *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(rho[4], rho[5], rho[6], rho[7]);
-    if (l == 0) {
-        long long e = -1;  // destination sketch slot of this (token, half), -1: none
-        if (active) e = half == 0 ? (((long long)b * c.Hkv + h) * c.G * N + t)
-                                  : (((long long)b * c.Hkv + h) * c.max_l1 + slot);
-        s_dst[warp][half] = e;
-        if (active) (half == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
+        put(1, true, ((long long)b * c.Hkv + h) * c.max_l1 + slot);
+    } else if (l == 0) {
+        s_dst[tk][1] = -1;
     }
     __syncthreads();
-    // S rho for the 2N residuals of the CTA: thread (i, grp) forms row i of S against
-    // 8 residuals, reading its row of S once; a warp's 32 consecutive rows are one
-    // sketch word per residual (ballot).  Residual r is half r / N of token r % N, so
-    // the groups of L1 residuals (half 1) skip their rows when none of their tokens
-    // is in L1 (most groups: L1 holds ~2 % of the tokens).
+    // S rho for the residuals of the CTA, the N L3 ones, then the L1 ones (few: L1
+    // holds ~2 % of the tokens): thread (i, grp) forms row i of S against 8 residuals
+    // (N / 8 groups of 128 threads), reading its row of S once per pass; a warp's 32
+    // consecutive rows are one sketch word per residual (ballot).  A group whose 8
+    // residuals all have no destination skips the pass (uniform per group).
     const int i = threadIdx.x & (kDim - 1), grp = threadIdx.x >> 7;
-    bool any = false;
+    const int lane = threadIdx.x & 31, word = i >> 5;
+    const float4* srow = reinterpret_cast<const float4*>(o.Sb) + i;  // step d4 at srow[d4 * 128]
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        bool any = false;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int r = grp * 8 + j;
-        any |= s_dst[r % N][r / N] >= 0;
-    }
-    if (!any) return;  // (uniform per CTA group: every thread of the group read the same slots)
-    const float4* srow = reinterpret_cast<const float4*>(o.S + (size_t)i * kDim);
-    float acc[8];
+        for (int j = 0; j < 8; ++j) any |= s_dst[grp * 8 + j][hf] >= 0;
+        if (!any) continue;
+        float acc[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll 4
-    for (int d4 = 0; d4 < kDim / 4; ++d4) {
-        const float4 sv = __ldg(srow + d4);
+        for (int d4 = 0; d4 < kDim / 4; ++d4) {
+            const float4 sv = __ldg(srow + d4 * kDim);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 rv = *reinterpret_cast<const float4*>(&s_rho[grp * 8 + j][hf][4 * d4]);
+                acc[j] = fmaf(sv.x, rv.x, acc[j]);
+                acc[j] = fmaf(sv.y, rv.y, acc[j]);
+                acc[j] = fmaf(sv.z, rv.z, acc[j]);
+                acc[j] = fmaf(sv.w, rv.w, acc[j]);
+            }
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int r = grp * 8 + j;
-            const float4 rv = *reinterpret_cast<const float4*>(&s_rho[r % N][r / N][4 * d4]);
-            acc[j] = fmaf(sv.x, rv.x, acc[j]);
-            acc[j] = fmaf(sv.y, rv.y, acc[j]);
-            acc[j] = fmaf(sv.z, rv.z, acc[j]);
-            acc[j] = fmaf(sv.w, rv.w, acc[j]);
+            const uint32_t bits = __ballot_sync(kFull, acc[j] >= 0.f);
+            const long long e = s_dst[grp * 8 + j][hf];
+            if (lane == 0 && e >= 0) (hf == 0 ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
         }
-    }
-    const int lane = threadIdx.x & 31, word = i >> 5;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t bits = __ballot_sync(kFull, acc[j] >= 0.f);
-        const int r = grp * 8 + j;
-        const long long e = s_dst[r % N][r / N];
-        if (lane == 0 && e >= 0) (r < N ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
     }
 }
 
@@ -919,13 +927,14 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
     }
     fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
     if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
-        const SketchOut so{cache->qjl_s, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
+        qjl_block_kernel<<<kDim * kDim / 4 / 256, 256, 0, s>>>(cache->qjl_s, ctx->d_qjl_sb);
+        const SketchOut so{ctx->d_qjl_sb, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
         if (v.N == 16) {
-            if (bf) qjl_kernel<16, true><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<16, false><<<grid, 16 * 32, 0, s>>>(v, so, K, tb);
+            if (bf) qjl_kernel<16, true><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<16, false><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
         } else {
-            if (bf) qjl_kernel<8, true><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<8, false><<<grid, 8 * 32, 0, s>>>(v, so, K, tb);
+            if (bf) qjl_kernel<8, true><<<grid, 8 * 16, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<8, false><<<grid, 8 * 16, 0, s>>>(v, so, K, tb);
         }
     }
     return after_launch(ctx, "encode");
@@ -933,7 +942,7 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
 
 void free_ctx(hsq_ctx* c) {
     cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
-    cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err);
+    cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err); cudaFree(c->d_qjl_sb);
     delete c;
 }
 
@@ -984,6 +993,8 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMalloc(&c->d_prefix, (size_t)cfg->max_batch * c->W_max * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(prefix)");
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
+    if (cfg->qjl && (e = cudaMalloc(&c->d_qjl_sb, hsq::kDim * hsq::kDim * 4)) != cudaSuccess)
+        return bail(e, "cudaMalloc(sketch matrix)");
     if ((e = cudaMemcpy(c->d_cb, cb, sizeof(cb), cudaMemcpyHostToDevice)) != cudaSuccess) return bail(e, "upload");
     if ((e = cudaMemcpy(c->d_rope_hi, hi.data(), hi.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(e, "upload");
