@@ -20,7 +20,7 @@ struct hsq_ctx {
     int* d_route_ctr = nullptr;
     int* d_prefix = nullptr;
     int* d_err = nullptr;
-    float* d_qjl_sb = nullptr;  // TQ-QKV: the sketch matrix of the last encode, blocked [32][128][4]
+    float* d_qjl_sb = nullptr;  // TQ-QKV: the last encode's sketch matrix as tensor-core B fragments (64 KB)
     // Decode launch plan per cache shape: cluster size S (0 = no launchable
     // shape) and whether the split's inputs are staged in shared memory.
     struct Plan { int B, T, route, S, staged; };

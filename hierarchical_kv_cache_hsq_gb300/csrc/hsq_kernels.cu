@@ -285,29 +285,69 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 // ---------------------------------------------------------------------------
 
 struct SketchOut {
-    // S blocked: element (i, 4 j + k) of the row-major [128][128] sketch matrix at
-    // (j * 128 + i) * 4 + k, so the 32 lanes of a warp, one row each, read 512
-    // contiguous bytes per float4 step
-    const float* Sb; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
+    // S as the B operand of the m16n8k16 tensor-core product (k = dimension d,
+    // n = sketch row i), in fragment order: for n-tile nt (rows 8 nt ..) and
+    // k-step ks (dims 16 ks ..), lane (g, q) = (lane / 4, lane % 4) holds at
+    // [(nt * 8 + ks) * 32 + lane] the bf16 pairs {S[i][d], S[i][d + 1]} and
+    // {S[i][d + 8], S[i][d + 9]}, i = 8 nt + g, d = 16 ks + 2 q, of S's bf16
+    // rounding (hi) and of the bf16 rounding of the remainder (lo)
+    const uint4* Sf; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
 };
 
-__global__ void __launch_bounds__(256) qjl_block_kernel(const float* __restrict__ S, float* __restrict__ Sb) {
-    const int e = blockIdx.x * 256 + threadIdx.x;  // destination float4 (j, i)
-    const int j = e >> 7, i = e & (kDim - 1);
-    reinterpret_cast<float4*>(Sb)[e] = __ldg(reinterpret_cast<const float4*>(S + (size_t)i * kDim) + j);
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    const __nv_bfloat16 la = __float2bfloat16_rn(a - __bfloat162float(ha));
+    const __nv_bfloat16 lb = __float2bfloat16_rn(b - __bfloat162float(hb));
+    hi = (uint32_t)__bfloat16_as_ushort(ha) | ((uint32_t)__bfloat16_as_ushort(hb) << 16);
+    lo = (uint32_t)__bfloat16_as_ushort(la) | ((uint32_t)__bfloat16_as_ushort(lb) << 16);
+}
+
+__global__ void __launch_bounds__(256) qjl_pack_kernel(const float* __restrict__ S, uint4* __restrict__ Sf) {
+    const int e = blockIdx.x * 256 + threadIdx.x;  // (nt * 8 + ks) * 32 + lane
+    const int lane = e & 31, ks = (e >> 5) & 7, nt = e >> 8;
+    const int i = 8 * nt + (lane >> 2), d = 16 * ks + 2 * (lane & 3);
+    const float* row = S + (size_t)i * kDim + d;
+    uint4 f;
+    split_pair(__ldg(row), __ldg(row + 1), f.x, f.z);
+    split_pair(__ldg(row + 8), __ldg(row + 9), f.y, f.w);
+    Sf[e] = f;
+}
+
+// D += A B for one m16n8k16 tile: bf16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bits 0..3 of x to bits 0, 2, 4, 6
+__device__ __forceinline__ uint32_t spread4(uint32_t x) {
+    return (x & 1u) | ((x & 2u) << 1) | ((x & 4u) << 2) | ((x & 8u) << 3);
 }
 
 template <int N, bool kBF16>
 __global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp, Tables tb) {
+    constexpr int kRS = kDim / 2 + 4;  // 32-bit words per residual row (bf16 pairs; 4 words of pad)
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
-    __shared__ __align__(16) float s_rho[N][2][kDim];  // [token][L3, L1]
+    // residuals as the A operand: [L3, L1][row = token, 16 rows][bf16 pairs], hi and lo parts
+    __shared__ __align__(16) uint32_t s_rh[2][16][kRS], s_rl[2][16][kRS];
     __shared__ long long s_dst[N][2];
+    __shared__ uint32_t s_bits[2][16][4];
 
     const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int tk = threadIdx.x >> 4, l = hlane();  // token of this half-warp
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
+    for (int i = threadIdx.x; i < 2 * 16 * 4; i += blockDim.x) (&s_bits[0][0][0])[i] = 0u;
+    for (int i = threadIdx.x; i < 2 * (16 - N) * kRS; i += blockDim.x) {  // rows past the tokens: zero
+        const int hf = i / ((16 - N) * kRS), k = i % ((16 - N) * kRS);
+        (&s_rh[hf][N][0])[k] = 0u;
+        (&s_rl[hf][N][0])[k] = 0u;
+    }
     __syncthreads();
     const float* c4 = s_cb;
     const float* t4 = s_cb + 16;
@@ -358,9 +398,17 @@ __global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, Sketch
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
         const float gamma = sqrtf(half_sum(ss, m));
-        float* row = s_rho[tk][hf];
-        *reinterpret_cast<float4*>(row + 4 * l) = make_float4(rho[0], rho[1], rho[2], rho[3]);
-        *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(rho[4], rho[5], rho[6], rho[7]);
+        uint32_t* rh = s_rh[hf][tk];
+        uint32_t* rl = s_rl[hf][tk];
+        uint2 h0, l0, h1, l1;
+        split_pair(rho[0], rho[1], h0.x, l0.x);
+        split_pair(rho[2], rho[3], h0.y, l0.y);
+        split_pair(rho[4], rho[5], h1.x, l1.x);
+        split_pair(rho[6], rho[7], h1.y, l1.y);
+        *reinterpret_cast<uint2*>(rh + 2 * l) = h0;  // dims 4 l .. 4 l + 3
+        *reinterpret_cast<uint2*>(rl + 2 * l) = l0;
+        *reinterpret_cast<uint2*>(rh + 32 + 2 * l) = h1;  // dims 64 + 4 l ..
+        *reinterpret_cast<uint2*>(rl + 32 + 2 * l) = l1;
         if (l == 0) {
             s_dst[tk][hf] = active ? e : -1;  // destination sketch slot, -1: none
             if (active) (hf == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
@@ -379,41 +427,55 @@ __global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, Sketch
         s_dst[tk][1] = -1;
     }
     __syncthreads();
-    // S rho for the residuals of the CTA, the N L3 ones, then the L1 ones (few: L1
-    // holds ~2 % of the tokens): thread (i, grp) forms row i of S against 8 residuals
-    // (N / 8 groups of 128 threads), reading its row of S once per pass; a warp's 32
-    // consecutive rows are one sketch word per residual (ballot).  A group whose 8
-    // residuals all have no destination skips the pass (uniform per group).
-    const int i = threadIdx.x & (kDim - 1), grp = threadIdx.x >> 7;
-    const int lane = threadIdx.x & 31, word = i >> 5;
-    const float4* srow = reinterpret_cast<const float4*>(o.Sb) + i;  // step d4 at srow[d4 * 128]
+    // S rho on the tensor cores: D[r][i] = sum_d rho_r[d] S[i][d] for the 16-row tile
+    // of residuals (the N L3 ones, then the L1 ones when a token of the CTA is in
+    // L1), with operands split into bf16 hi + lo and the three products hi hi,
+    // hi lo, lo hi accumulated in fp32 (about 2^-16 relative per term).  Warp w
+    // takes n-tiles (sketch rows 8 nt ..) w * kNT .. ; bit i of a residual's
+    // sketch (word i / 32, bit i % 32) is set when D >= 0.
+    constexpr int kWarps = N / 2, kNT = 16 / kWarps;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
         bool any = false;
+        for (int r = 0; r < N; ++r) any |= s_dst[r][hf] >= 0;
+        if (!any) continue;  // (uniform: every thread read the same slots)
+        float d[kNT][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) any |= s_dst[grp * 8 + j][hf] >= 0;
-        if (!any) continue;
-        float acc[8];
+        for (int j = 0; j < kNT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll 2
+        for (int ks = 0; ks < 8; ++ks) {
+            const int c0 = 8 * ks + tq;  // word of dims 16 ks + 2 q, + 1
+            const uint32_t ah0 = s_rh[hf][gq][c0], ah1 = s_rh[hf][gq + 8][c0];
+            const uint32_t ah2 = s_rh[hf][gq][c0 + 4], ah3 = s_rh[hf][gq + 8][c0 + 4];
+            const uint32_t al0 = s_rl[hf][gq][c0], al1 = s_rl[hf][gq + 8][c0];
+            const uint32_t al2 = s_rl[hf][gq][c0 + 4], al3 = s_rl[hf][gq + 8][c0 + 4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 4
-        for (int d4 = 0; d4 < kDim / 4; ++d4) {
-            const float4 sv = __ldg(srow + d4 * kDim);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float4 rv = *reinterpret_cast<const float4*>(&s_rho[grp * 8 + j][hf][4 * d4]);
-                acc[j] = fmaf(sv.x, rv.x, acc[j]);
-                acc[j] = fmaf(sv.y, rv.y, acc[j]);
-                acc[j] = fmaf(sv.z, rv.z, acc[j]);
-                acc[j] = fmaf(sv.w, rv.w, acc[j]);
+            for (int j = 0; j < kNT; ++j) {
+                const uint4 bf = __ldg(o.Sf + ((warp * kNT + j) * 8 + ks) * 32 + lane);
+                mma_bf16_16816(d[j], al0, al1, al2, al3, bf.x, bf.y);  // lo hi
+                mma_bf16_16816(d[j], ah0, ah1, ah2, ah3, bf.z, bf.w);  // hi lo
+                mma_bf16_16816(d[j], ah0, ah1, ah2, ah3, bf.x, bf.y);  // hi hi
             }
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t bits = __ballot_sync(kFull, acc[j] >= 0.f);
-            const long long e = s_dst[grp * 8 + j][hf];
-            if (lane == 0 && e >= 0) (hf == 0 ? o.l3_qs : o.l1_qs)[e * 4 + word] = bits;
+        for (int j = 0; j < kNT; ++j) {  // D[g][2q + c], D[g + 8][2q + c] -> bytes of rows g, g + 8
+            const int nt = warp * kNT + j;
+            const uint32_t b0 = __ballot_sync(kFull, d[j][0] >= 0.f), b1 = __ballot_sync(kFull, d[j][1] >= 0.f);
+            const uint32_t b2 = __ballot_sync(kFull, d[j][2] >= 0.f), b3 = __ballot_sync(kFull, d[j][3] >= 0.f);
+            if (tq == 0) {
+                const uint32_t lo = spread4((b0 >> (4 * gq)) & 15u) | (spread4((b1 >> (4 * gq)) & 15u) << 1);
+                const uint32_t hi = spread4((b2 >> (4 * gq)) & 15u) | (spread4((b3 >> (4 * gq)) & 15u) << 1);
+                atomicOr(&s_bits[hf][gq][nt >> 2], lo << (8 * (nt & 3)));
+                atomicOr(&s_bits[hf][gq + 8][nt >> 2], hi << (8 * (nt & 3)));
+            }
         }
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < 2 * N * 4; k += blockDim.x) {
+        const int hf = k / (N * 4), r = (k >> 2) % N, wd = k & 3;
+        const long long e = s_dst[r][hf];
+        if (e >= 0) (hf == 0 ? o.l3_qs : o.l1_qs)[e * 4 + wd] = s_bits[hf][r][wd];
     }
 }
 
@@ -927,8 +989,9 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
     }
     fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
     if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
-        qjl_block_kernel<<<kDim * kDim / 4 / 256, 256, 0, s>>>(cache->qjl_s, ctx->d_qjl_sb);
-        const SketchOut so{ctx->d_qjl_sb, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
+        uint4* sf = reinterpret_cast<uint4*>(ctx->d_qjl_sb);
+        qjl_pack_kernel<<<16 * 8 * 32 / 256, 256, 0, s>>>(cache->qjl_s, sf);
+        const SketchOut so{sf, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
         if (v.N == 16) {
             if (bf) qjl_kernel<16, true><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
             else qjl_kernel<16, false><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
