@@ -108,7 +108,12 @@ __device__ __forceinline__ void write_summary(float x[8], const float sg[8], uns
 
 // (48 resident warps per SM -- 3 CTAs of 16 warps or 6 of 8, 40 registers: the
 // kernel is issue bound and the extra warps hide its memory and shared-memory
-// latencies; 32 warps measured 20 % slower)
+// latencies; 32 warps measured 20 % slower.)  A CTA takes kEncGroups
+// consecutive groups: each warp encodes its token of every group in turn, then
+// warp j forms group j's summary, so the summaries run side by side.
+constexpr int kEncGroups = 4;
+// dynamic shared memory of the encode kernel: the member rows s_sum[kEncGroups][N][2][128]
+constexpr size_t enc_dyn_smem(int N) { return (size_t)kEncGroups * N * 2 * 128 * 4; }
 // kRot: TurboQuant rotation (false: Plain-KV), fixed at compile time
 // kPF: prefill, the same encode also writes the attention's K/V operand images
 template <int N, bool kBF16, bool kRot, bool kPF = false>
@@ -116,135 +121,144 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
                                                         const void* __restrict__ Vp, Tables tb) {
     __shared__ float s_cb[hsq::kCodebookFloats];
     __shared__ float s_sign[kDim];
-    __shared__ __align__(16) uint8_t s_rec[N * 136];
-    __shared__ __align__(16) float s_sum[N][2][kDim];
-    __shared__ int s_member[N];
-    __shared__ uint32_t s_l2[2][12];
+    __shared__ __align__(16) uint8_t s_rec[kEncGroups][N * 136];
+    extern __shared__ __align__(16) float s_dyn_enc[];
+    auto s_sum = reinterpret_cast<float (*)[N][2][kDim]>(s_dyn_enc);  // [kEncGroups][N][2][128]
+    __shared__ int s_member[kEncGroups][N];
+    __shared__ uint32_t s_l2[kEncGroups][2][12];
 
-    const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, half = (threadIdx.x >> 4) & 1, l = hlane();
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
-    if (threadIdx.x < 24) (&s_l2[0][0])[threadIdx.x] = 0u;
+    if (threadIdx.x < kEncGroups * 24) (&s_l2[0][0][0])[threadIdx.x] = 0u;
     __syncthreads();
     const float* t4 = s_cb + 16;
     const float* t3 = s_cb + 40;
     float sg[8];
     load_signs(sg, s_sign);
 
-    const int t = g * N + warp;
-    const bool in_ctx = t < c.T;
-    bool is_l1 = false;
-    int slot = 0;
-    if (in_ctx) {
-        const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
-        is_l1 = (w >> (t & 31)) & 1u;
-        if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
-    }
+#pragma unroll 1
+    for (int j = 0; j < kEncGroups; ++j) {  // token `warp` of each of the CTA's groups
+        const int g = blockIdx.x * kEncGroups + j;
+        if (g >= c.G) break;
+        const int t = g * N + warp;
+        const bool in_ctx = t < c.T;
+        bool is_l1 = false;
+        int slot = 0;
+        if (in_ctx) {
+            const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
+            is_l1 = (w >> (t & 31)) & 1u;
+            if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
+        }
 
-    float x[8];
-    if (in_ctx) {
-        const size_t off = (((size_t)b * c.Hkv + h) * c.T + t) * kDim;
-        if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? Vp : Kp) + off, x);
-        else load_f32x8(static_cast<const float*>(half ? Vp : Kp) + off, x);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
-
-    // the recent window's inputs, for decode-time growth (slot t mod recent)
-    if (o.win_kv && in_ctx && t >= c.T - o.recent) {
-        float* wp = o.win_kv + ((((size_t)b * c.Hkv + h) * o.recent + t % o.recent) * 2 + half) * kDim;
-        *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
-        *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
-    }
-
-    // L3: TQ4 of the raw (pre-RoPE) key / value
-    float y[8];
-    const float n = tq_rotate(x, y, sg, m, kRot);
-    uint16_t lo, hi;
-    pack4(y, t4, lo, hi);
-    {
-        uint8_t* row = s_rec + (half ? N * 64 : 0) + warp * 64;
-        reinterpret_cast<uint16_t*>(row)[l] = lo;
-        reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
-        if (l == 0) reinterpret_cast<float*>(s_rec + N * 128)[half * N + warp] = n;
-    }
-
-    // RoPE'd key (half 0) for L1 and for the group summary; values as they are
-    float xr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xr[i] = x[i];
-    if (half == 0 && in_ctx) rope(xr, t, tb);
-
-    if (kPF && t < o.pf_nkt * 64) {  // row t & 63 of key tile t >> 6 (zero past T)
-        const int row = t & 63;
-        const size_t img = (((size_t)b * c.Hkv + h) * o.pf_nkt + (t >> 6)) * (64 * kDim * 2);
-        if (half == 0) {
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-                uint16_t hi[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) hsq_tc::split_bf16(xr[4 * blk + k], hi[k], lo[k]);
-                const uint32_t off = hsq_tc::sw128_row_quad(64, row, blk, l);
-                *reinterpret_cast<uint2*>(o.pf_kh + img + off) =
-                    make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
-                *reinterpret_cast<uint2*>(o.pf_kl + img + off) =
-                    make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
-            }
+        float x[8];
+        if (in_ctx) {
+            const size_t off = (((size_t)b * c.Hkv + h) * c.T + t) * kDim;
+            if (kBF16) load_bf16x8(static_cast<const uint16_t*>(half ? Vp : Kp) + off, x);
+            else load_f32x8(static_cast<const float*>(half ? Vp : Kp) + off, x);
         } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int d = (i < 4 ? 4 * l : 64 + 4 * l) + (i & 3);
-                *reinterpret_cast<uint16_t*>(o.pf_vt + img + hsq_tc::sw128_elem(d, row)) =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(x[i]));
+    #pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+
+        // the recent window's inputs, for decode-time growth (slot t mod recent)
+        if (o.win_kv && in_ctx && t >= c.T - o.recent) {
+            float* wp = o.win_kv + ((((size_t)b * c.Hkv + h) * o.recent + t % o.recent) * 2 + half) * kDim;
+            *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+
+        // L3: TQ4 of the raw (pre-RoPE) key / value
+        float y[8];
+        const float n = tq_rotate(x, y, sg, m, kRot);
+        uint16_t lo, hi;
+        pack4(y, t4, lo, hi);
+        {
+            uint8_t* row = s_rec[j] + (half ? N * 64 : 0) + warp * 64;
+            reinterpret_cast<uint16_t*>(row)[l] = lo;
+            reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
+            if (l == 0) reinterpret_cast<float*>(s_rec[j] + N * 128)[half * N + warp] = n;
+        }
+
+        // RoPE'd key (half 0) for L1 and for the group summary; values as they are
+        float xr[8];
+    #pragma unroll
+        for (int i = 0; i < 8; ++i) xr[i] = x[i];
+        if (half == 0 && in_ctx) rope(xr, t, tb);
+
+        if (kPF && t < o.pf_nkt * 64) {  // row t & 63 of key tile t >> 6 (zero past T)
+            const int row = t & 63;
+            const size_t img = (((size_t)b * c.Hkv + h) * o.pf_nkt + (t >> 6)) * (64 * kDim * 2);
+            if (half == 0) {
+    #pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    uint16_t hi[4], lo[4];
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) hsq_tc::split_bf16(xr[4 * blk + k], hi[k], lo[k]);
+                    const uint32_t off = hsq_tc::sw128_row_quad(64, row, blk, l);
+                    *reinterpret_cast<uint2*>(o.pf_kh + img + off) =
+                        make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+                    *reinterpret_cast<uint2*>(o.pf_kl + img + off) =
+                        make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
+                }
+            } else {
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int d = (i < 4 ? 4 * l : 64 + 4 * l) + (i & 3);
+                    *reinterpret_cast<uint16_t*>(o.pf_vt + img + hsq_tc::sw128_elem(d, row)) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(x[i]));
+                }
             }
         }
-    }
 
-    if (is_l1 && slot < c.max_l1) {
-        const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
-        if (half == 0) {
-            float yr[8];
-            tq_rotate(xr, yr, sg, m, kRot);  // same norm as the raw key (RoPE is norm preserving)
-            uint16_t klo, khi;
-            pack4(yr, t4, klo, khi);
-            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
-            reinterpret_cast<uint16_t*>(o.l1_kc + so * 64 + 32)[l] = khi;
-            if (l == 0) o.l1_kn[so] = n;
-        } else {
-            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64)[l] = lo;
-            reinterpret_cast<uint16_t*>(o.l1_vc + so * 64 + 32)[l] = hi;
-            if (l == 0) o.l1_vn[so] = n;
+        if (is_l1 && slot < c.max_l1) {
+            const size_t so = ((size_t)b * c.Hkv + h) * c.max_l1 + slot;
+            if (half == 0) {
+                float yr[8];
+                tq_rotate(xr, yr, sg, m, kRot);  // same norm as the raw key (RoPE is norm preserving)
+                uint16_t klo, khi;
+                pack4(yr, t4, klo, khi);
+                reinterpret_cast<uint16_t*>(o.l1_kc + so * 64)[l] = klo;
+                reinterpret_cast<uint16_t*>(o.l1_kc + so * 64 + 32)[l] = khi;
+                if (l == 0) o.l1_kn[so] = n;
+            } else {
+                reinterpret_cast<uint16_t*>(o.l1_vc + so * 64)[l] = lo;
+                reinterpret_cast<uint16_t*>(o.l1_vc + so * 64 + 32)[l] = hi;
+                if (l == 0) o.l1_vn[so] = n;
+            }
         }
-    }
 
-    const bool member = in_ctx && !is_l1;
-    if (member) {
-        float* row = &s_sum[warp][half][0];
-        *reinterpret_cast<float4*>(row + 4 * l) = make_float4(xr[0], xr[1], xr[2], xr[3]);
-        *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(xr[4], xr[5], xr[6], xr[7]);
+        const bool member = in_ctx && !is_l1;
+        if (member) {
+            float* row = &s_sum[j][warp][half][0];
+            *reinterpret_cast<float4*>(row + 4 * l) = make_float4(xr[0], xr[1], xr[2], xr[3]);
+            *reinterpret_cast<float4*>(row + 64 + 4 * l) = make_float4(xr[4], xr[5], xr[6], xr[7]);
+        }
+        if (threadIdx.x == warp * 32) s_member[j][warp] = member ? 1 : 0;
     }
-    if (threadIdx.x == warp * 32) s_member[warp] = member ? 1 : 0;
     __syncthreads();
 
-    // L3 record out (16-byte chunks; through the host link when L3 is pinned host memory)
+    // L3 records out (16-byte chunks; through the host link when L3 is pinned host memory)
     {
-        uint4* dst = reinterpret_cast<uint4*>(o.l3 + (((size_t)b * c.Hkv + h) * c.G + g) * (N * 136));
-        const uint4* src = reinterpret_cast<const uint4*>(s_rec);
-        for (int i = threadIdx.x; i < N * 136 / 16; i += blockDim.x) dst[i] = src[i];
+        const int g0 = blockIdx.x * kEncGroups;
+        const int ng = min(kEncGroups, c.G - g0);
+        uint4* dst = reinterpret_cast<uint4*>(o.l3 + (((size_t)b * c.Hkv + h) * c.G + g0) * (N * 136));
+        const uint4* src = reinterpret_cast<const uint4*>(&s_rec[0][0]);
+        for (int i = threadIdx.x; i < ng * (N * 136 / 16); i += blockDim.x) dst[i] = src[i];
     }
 
-    // L2 summary: mean over members in token order, then TQ3
-    if (warp == 0) {
+    // L2 summaries, group j by warp j: mean over members in token order, then TQ3
+    const int j = warp, g = blockIdx.x * kEncGroups + warp;
+    if (j < kEncGroups && g < c.G) {
         int cnt = 0;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
         for (int k = 0; k < N; ++k) {
-            if (!s_member[k]) continue;
+            if (!s_member[j][k]) continue;
             ++cnt;
-            const float* row = &s_sum[k][half][0];
+            const float* row = &s_sum[j][k][half][0];
             const float4 a = *reinterpret_cast<const float4*>(row + 4 * l);
             const float4 bq = *reinterpret_cast<const float4*>(row + 64 + 4 * l);
             acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
@@ -260,7 +274,7 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
                 keep ? make_float4(acc[0], acc[1], acc[2], acc[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
             *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) =
                 keep ? make_float4(acc[4], acc[5], acc[6], acc[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (threadIdx.x == 0) {
+            if ((threadIdx.x & 31) == 0) {
                 gs[2 * kDim] = keep ? (float)cnt : 0.f;
                 gs[2 * kDim + 1] = (float)p_next;  // the window's first position at encode
             }
@@ -270,9 +284,9 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
             for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
         }
         const size_t go = ((size_t)b * c.Hkv + h) * c.G + g;
-        write_summary(acc, sg, m, kRot, t3, s_l2[half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+        write_summary(acc, sg, m, kRot, t3, s_l2[j][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
                       (half ? o.l2_vn : o.l2_kn) + go);
-        if (threadIdx.x == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
+        if ((threadIdx.x & 31) == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + g] = (uint8_t)cnt;
     }
 }
 
@@ -343,10 +357,12 @@ __global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, Sketch
     const unsigned m = half_mask();
     load_tables(s_cb, s_sign, tb, c.signs);
     for (int i = threadIdx.x; i < 2 * 16 * 4; i += blockDim.x) (&s_bits[0][0][0])[i] = 0u;
-    for (int i = threadIdx.x; i < 2 * (16 - N) * kRS; i += blockDim.x) {  // rows past the tokens: zero
-        const int hf = i / ((16 - N) * kRS), k = i % ((16 - N) * kRS);
-        (&s_rh[hf][N][0])[k] = 0u;
-        (&s_rl[hf][N][0])[k] = 0u;
+    if constexpr (N < 16) {  // MMA rows past the tokens: zero
+        constexpr int kPad = (16 - N) * kRS;
+        for (int i = threadIdx.x; i < 2 * kPad; i += blockDim.x) {
+            (&s_rh[i / kPad][N][0])[i % kPad] = 0u;
+            (&s_rl[i / kPad][N][0])[i % kPad] = 0u;
+        }
     }
     __syncthreads();
     const float* c4 = s_cb;
@@ -987,7 +1003,9 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
         fn = v.rot ? (bf ? encode_kernel<8, true, true> : encode_kernel<8, false, true>)
                    : (bf ? encode_kernel<8, true, false> : encode_kernel<8, false, false>);
     }
-    fn<<<grid, v.N * 32, 0, s>>>(v, o, K, V, tb);
+    const size_t dyn = enc_dyn_smem(v.N);
+    HSQ_CUDA(ctx, raise_smem_limit((const void*)fn, ctx->device, dyn));
+    fn<<<dim3((v.G + kEncGroups - 1) / kEncGroups, v.Hkv, v.B), v.N * 32, dyn, s>>>(v, o, K, V, tb);
     if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
         uint4* sf = reinterpret_cast<uint4*>(ctx->d_qjl_sb);
         qjl_pack_kernel<<<16 * 8 * 32 / 256, 256, 0, s>>>(cache->qjl_s, sf);
