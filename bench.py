@@ -441,10 +441,12 @@ def table_hit_rate(H, torch, ctx, cache, qd, pd, sel, out, slots, nsteps):
     return hits / max(tot, 1)
 
 
-def measure_hot_table(H, torch, w, li, qd, pd, flush, clean, sink, steps, warmup, table_free_us):
+def measure_hot_table(H, torch, w, li, qd, pd, flush, clean, sink, steps, warmup, free_ctx, free_cache):
     """The fused step with a hot-group table (HOT_SLOTS slots per (b, KV
-    head)) on the same layer, pinned L3, the same queries and L2 flush as the
-    headline loop; its hit rate over the first steps after an encode."""
+    head)) on a second cache of the same layer, pinned L3, the same queries
+    and L2 flush as the headline loop, timed in alternating blocks with the
+    table-free step on the headline's cache (same conditions, same process);
+    the table's hit rate in steady state."""
     cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta, 0,
                         hot_slots=HOT_SLOTS)
     hctx = H.Context(cfg)
@@ -456,7 +458,7 @@ def measure_hot_table(H, torch, w, li, qd, pd, flush, clean, sink, steps, warmup
     del K, V
     sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
     out = torch.empty((w.B, w.Hq, 128), device="cuda")
-    def run(n, off):  # as the headline loop: steps queued ahead, events around each step
+    def run(ctx, c, n, off):  # as the headline loop: steps queued ahead, events around each step
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         torch.cuda._sleep(20_000_000)
         for i in range(n):
@@ -464,24 +466,30 @@ def measure_hot_table(H, torch, w, li, qd, pd, flush, clean, sink, steps, warmup
             flush.fill_(i & 255)
             torch.sum(clean, dim=0, out=sink)
             ev[i][0].record()
-            H.hsq_decode_step(hctx, cache, qd[s], pd[s], sel, out)
+            H.hsq_decode_step(ctx, c, qd[s], pd[s], sel, out)
             ev[i][1].record()
         torch.cuda.synchronize()
         return [e[0].elapsed_time(e[1]) * 1e3 for e in ev]
-    run(warmup, 0)
-    ts = run(steps, warmup)
+    ts = {"table": [], "free": []}
+    blk = max(steps // 4, 1)
+    for rep in range(4):
+        for key, ctx, c in (("table", hctx, cache), ("free", free_ctx, free_cache)):
+            run(ctx, c, warmup, rep * blk)
+            ts[key] += run(ctx, c, blk, rep * blk + warmup)
     hit = table_hit_rate(H, torch, hctx, cache, qd, pd, sel, out, HOT_SLOTS, 16)  # steady state
     assert H.hsq_sync_status(hctx) == 0
     hctx.close()
-    med = statistics.median(ts)
+    med, mean = statistics.median, (lambda x: sum(x) / len(x))
     rb = w.N * 136
-    return {"slots": HOT_SLOTS, "us_per_step_median": med, "us_per_step_mean": sum(ts) / len(ts),
-            "steps_per_s": 1e6 / (sum(ts) / len(ts)), "table_free_us_per_step_mean": table_free_us,
+    return {"slots": HOT_SLOTS, "us_per_step_median": med(ts["table"]), "us_per_step_mean": mean(ts["table"]),
+            "steps_per_s": 1e6 / mean(ts["table"]),
+            "table_free_us_per_step_median": med(ts["free"]), "table_free_us_per_step_mean": mean(ts["free"]),
             "hit_rate": hit, "hit_rate_how": "16 steps after the timed loop (the table warm)",
             "l3_link_bytes_per_step": (1 - hit) * w.B * w.Hkv * w.beta * rb,
-            "how": "hsq_decode_step with hsq_config.hot_slots on a second cache of this layer, timed as the "
-                   "headline loop (queries of the workload, correlated across steps; L2 flushed per step; "
-                   "steps queued ahead); results bit-identical to the table-free step (GPU tests)"}
+            "how": "hsq_decode_step with hsq_config.hot_slots on a second cache of this layer against the "
+                   "table-free step on the headline's cache, 4 alternating blocks each, timed as the headline "
+                   "loop (queries of the workload, correlated across steps; L2 flushed and refilled clean per "
+                   "step; steps queued ahead); results bit-identical (GPU tests)"}
 
 
 def measure_codecs(H, torch, w, li):
@@ -864,7 +872,7 @@ def run_hsq(args, rank, world, local):
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
     hot = None if args.quick or args.codec != "tq" or args.qjl else measure_hot_table(
-        H, torch, w, li, qd, pd, flush, clean, sink, min(args.steps, 300), max(args.warmup, 3), ms_per_step * 1e3)
+        H, torch, w, li, qd, pd, flush, clean, sink, min(args.steps, 400), max(args.warmup, 3), ctx, caches["host"])
     mean = lambda x: sum(x) / len(x)
     hbm_peak, peak_src = measured_peaks()
     link_gbs = lp["h2d_gbs"]

@@ -14,7 +14,8 @@ with the first step's, so consecutive selections overlap):
   * selected groups hit the table (the correlated steps re-select groups);
   * hsq_encode empties the table; hsq_append drops the group it writes, and
     decoding continues bit-identical to the table-free cache.
-Shapes: the 8B head layout (r = 4, N = 16); r = 5 with beta = 256 over four
+Shapes: the 8B head layout (r = 4, N = 16), also at full size (the 8B/32K layer in the
+benchmark's launch configuration); r = 5 with beta = 256 over four
 splits (64 records per split: eight record batches per step) and a
 1024-slot table; N = 8 with a 16-slot table (many slots shared within a
 step) and L3 in device memory.
@@ -197,3 +198,42 @@ def test_hot_table_with_growth():
             np.testing.assert_array_equal(rec2[b, h, k], l3[b, h, tag2[b, h, k]])
     assert H.hsq_sync_status(ctx0) == 0 and H.hsq_sync_status(ctx1) == 0
     assert hits > 0
+
+
+def test_hot_table_full_size_8b_32k():
+    """The 8B/32K layer in the benchmark's launch configuration (B 1, Hkv 8, T 32768,
+    N 16, beta 64, L3 in pinned host memory, 256 slots) over 8 correlated steps:
+    out and sel bit-identical to the table-free step, the table following its rule."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = W.get_workload("qwen3_8b_32k").with_(steps=8)
+    c = dict(slots=256, n_splits=0)
+    li = W.layer_inputs(w, rope=lambda x, p: O.rope(x, p, w.theta))
+    q, pos = W.queries(w)
+    ctx0, ctx1 = _contexts(w, c)
+    K = torch.from_numpy(np.ascontiguousarray(li.K, np.float32)).cuda().to(torch.bfloat16)
+    V = torch.from_numpy(np.ascontiguousarray(li.V, np.float32)).cuda().to(torch.bfloat16)
+    caches = []
+    for ctx in (ctx0, ctx1):
+        cache = H.allocate_cache(ctx, w.B, w.T, l3_on_host=True, with_staging=False)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        H.hsq_encode(ctx, cache, K, V)
+        caches.append(cache)
+    torch.cuda.synchronize()
+    ref, hot = caches
+    l3 = hot.view("l3").cpu().numpy()
+    qd, pd = torch.from_numpy(q).cuda(), torch.from_numpy(pos).cuda()
+    sel = [torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda") for _ in range(2)]
+    out = [torch.empty((w.B, w.Hq, 128), device="cuda") for _ in range(2)]
+    hits = 0
+    for s in range(w.steps):
+        tag0, _ = _table(hot)
+        H.hsq_decode_step(ctx0, ref, qd[s], pd[s], sel[0], out[0])
+        H.hsq_decode_step(ctx1, hot, qd[s], pd[s], sel[1], out[1])
+        assert H.hsq_sync_status(ctx1) == 0
+        np.testing.assert_array_equal(sel[1].cpu().numpy(), sel[0].cpu().numpy())
+        np.testing.assert_array_equal(out[1].cpu().numpy(), out[0].cpu().numpy())
+        tag1, rec1 = _table(hot)
+        hits += _check_rule(tag0, tag1, rec1, l3, sel[1].cpu().numpy(), c["slots"])
+    assert hits > 0
+    print(f"8B/32K: {hits} of {w.steps * w.Hkv * w.beta} selected groups hit the table")
