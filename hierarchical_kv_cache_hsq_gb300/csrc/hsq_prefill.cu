@@ -23,10 +23,14 @@
 // Rows past T are zero.
 //
 // Attention kernel: one CTA per (128-query tile, query head, sequence), warp
-// specialised.  Two producer warps, one thread each: warp 8 loads the key
-// tiles and issues S = Q K^T of tile k (128 x 64, into TMEM columns 0-63 or
-// 64-127 in turn) as soon as the tile's keys have landed and the softmax has
-// read the buffer's previous S; warp 9 loads the value tiles and, once the
+// specialised.  The query tile is loaded once and moved by the softmax warps
+// into TMEM columns 384-511 (hi, lo; row = lane, dims in pairs along the
+// columns), so the S products take their A operand from tensor memory and
+// only the key tiles are read from shared memory.  Two producer warps, one
+// thread each: warp 8 loads the key tiles and issues S = Q K^T of tile k
+// (128 x 64, into TMEM columns 0-63 or 64-127 in turn) as soon as the tile's
+// keys have landed and the softmax has read the buffer's previous S; warp 9
+// loads the value tiles and, once the
 // softmax has written P of tile k, issues O_half += P_half V_half for both
 // key halves (TMEM columns 128-255 and 256-383).  Each refills its stage when
 // the MMA that read it completed.  Warps 0-7 run the softmax: query row r of
@@ -66,9 +70,10 @@ constexpr uint32_t kOffV = kOffK + 2 * 2 * kKImg;                    // V stage 
 constexpr uint32_t kOffP = kOffV + 2 * kVImg;                        // P buffer b: Ph | Pl
 constexpr uint32_t kOffBar = kOffP + 2 * 2 * kPImg;
 // barriers (8 bytes each): q | k[2] | v[2] | s_full[2] | s_free[2] | p_full[2] | o_done[2]; TMEM address
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 14;
 constexpr uint32_t kPfSmem = kOffBar + 8 * kNumBars + 8 + 1024;
-constexpr uint32_t kTmemCols = 512;  // S buffers: 0-63, 64-127; O of key half k: 128 + 128 k
+constexpr uint32_t kTmemCols = 512;  // S buffers: 0-63, 64-127; O of key half k: 128 + 128 k; Q hi 384, lo 448
+constexpr uint32_t kTmQh = 384, kTmQl = 448;
 
 struct PrefillArgs {
     const uint8_t* qh; const uint8_t* ql; const uint8_t* kh; const uint8_t* kl; const uint8_t* vt;
@@ -88,11 +93,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
     const int h = j / (a.Hq / a.Hkv);
     const uint32_t bar0 = base + kOffBar;
     const uint32_t bar_q = bar0, bar_k = bar0 + 8, bar_v = bar0 + 24, s_full = bar0 + 40, s_free = bar0 + 56;
-    const uint32_t p_full = bar0 + 72, o_done = bar0 + 88, slot = bar0 + 8 * kNumBars;
+    const uint32_t p_full = bar0 + 72, o_done = bar0 + 88, q_tm = bar0 + 104, slot = bar0 + 8 * kNumBars;
     const int nkv = 2 * qt + 2;  // key tiles up to the diagonal
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
+        mbar_init(q_tm, kPfSoftThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_k + 8 * i, 1);
             mbar_init(bar_v + 8 * i, 1);
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
             bulk_g2s(base + kOffQh, a.qh + qi * kQImg, kQImg, bar_q);
             bulk_g2s(base + kOffQl, a.ql + qi * kQImg, kQImg, bar_q);
             for (int kt = 0; kt < min(nkv, 2); ++kt) load_k(kt);
-            ok = mbar_wait(bar_q, 0);
+            ok = mbar_wait(q_tm, 0);  // Q hi and lo are in tensor memory
 #pragma unroll 1
             for (int kt = 0; kt < nkv && ok; ++kt) {
                 const int bb = kt & 1;
@@ -143,13 +149,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                 const uint32_t ks = base + kOffK + bb * 2 * kKImg, dS = tmem + 64 * bb;
 #pragma unroll 1
                 for (int k = 0; k < 8; ++k) {
-                    const uint32_t qo = (k >> 2) * (kQImg / 2) + (k & 3) * 32;
                     const uint32_t ko = (k >> 2) * (kKImg / 2) + (k & 3) * 32;
-                    const uint64_t dqh = sw128_desc(base + kOffQh + qo), dql = sw128_desc(base + kOffQl + qo);
                     const uint64_t dkh = sw128_desc(ks + ko), dkl = sw128_desc(ks + kKImg + ko);
-                    mma_bf16(dS, dqh, dkh, idS, k > 0);
-                    mma_bf16(dS, dql, dkh, idS, 1);
-                    mma_bf16(dS, dqh, dkl, idS, 1);
+                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkh, idS, k > 0);
+                    mma_bf16_ts(dS, tmem + kTmQl + 8 * k, dkh, idS, 1);
+                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkl, idS, 1);
                 }
                 mma_commit(s_full + 8 * bb);
                 if (kt + 2 < nkv) {  // S(kt) has read key stage bb: refill it
@@ -200,6 +204,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
         const uint32_t tO = tmem + lanes + 128 + 128 * half;
         const int t = qt * kPfRows + row;
+        {   // Q (hi: warps 0-3, lo: warps 4-7) from its shared-memory image into tensor memory,
+            // row = lane, dims in pairs along the columns
+            ok = mbar_wait(bar_q, 0);
+            if (!ok) atomicOr(a.err, HSQ_DEVERR_WAIT);  // (arrives all the same: no one waits forever)
+            const uint8_t* img = gbase + (half ? kOffQl : kOffQh) + row * 128;
+            float w[32];
+#pragma unroll
+            for (int blk = 0; blk < 2 && ok; ++blk) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(img + blk * (kQImg / 2) + ((c ^ (row & 7)) << 4));
+                    w[4 * c] = __uint_as_float(v.x);
+                    w[4 * c + 1] = __uint_as_float(v.y);
+                    w[4 * c + 2] = __uint_as_float(v.z);
+                    w[4 * c + 3] = __uint_as_float(v.w);
+                }
+                tmem_st32(tmem + lanes + (half ? kTmQl : kTmQh) + 32 * blk, w);
+            }
+            tc_fence_before();
+            mbar_arrive(q_tm);
+        }
         float m_used = -INFINITY, lsum = 0.f;
 #pragma unroll 1
         for (int kt = 0; kt < nkv; ++kt) {
