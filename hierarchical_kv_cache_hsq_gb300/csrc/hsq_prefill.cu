@@ -312,13 +312,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         const float w_ot = m_o == -INFINITY ? 0.f : ex2_approx(m_o - M);
         const float L = lsum * w_me + l_o * w_ot;
         const float inv = L > 0.f ? 1.0f / L : 0.f;
-        float* xch = reinterpret_cast<float*>(gbase + kOffK);  // [2 halves][128 rows][64 columns]
+        // [2 halves][64 columns][128 rows]: the 32 rows of a warp are consecutive words
+        // for every column, so the stores and loads below are free of bank conflicts
+        float* xch = reinterpret_cast<float*>(gbase + kOffK);
         float o[32];
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
             tmem_ld32(tO + 64 * (half ^ 1) + c0, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) xch[((half ^ 1) * kPfRows + row) * 64 + c0 + c] = o[c] * w_me;
+            for (int c = 0; c < 32; ++c) xch[((half ^ 1) * 64 + c0 + c) * kPfRows + row] = o[c] * w_me;
         }
         named_bar_sync(1, kPfSoftThreads);
         float* orow = a.out + (((size_t)b * a.Hq + j) * a.T + (t < a.T ? t : 0)) * kDim + 64 * half;
@@ -326,12 +328,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
         for (int c0 = 0; c0 < 64; c0 += 32) {
             tmem_ld32(tO + 64 * half + c0, o);
             if (t < a.T && ok) {
-                const float* other = xch + ((size_t)half * kPfRows + row) * 64 + c0;
+                const float* other = xch + ((size_t)half * 64 + c0) * kPfRows + row;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4)
-                    *reinterpret_cast<float4*>(orow + c0 + c) =
-                        make_float4((o[c] * w_me + other[c]) * inv, (o[c + 1] * w_me + other[c + 1]) * inv,
-                                    (o[c + 2] * w_me + other[c + 2]) * inv, (o[c + 3] * w_me + other[c + 3]) * inv);
+                    *reinterpret_cast<float4*>(orow + c0 + c) = make_float4(
+                        (o[c] * w_me + other[c * kPfRows]) * inv, (o[c + 1] * w_me + other[(c + 1) * kPfRows]) * inv,
+                        (o[c + 2] * w_me + other[(c + 2) * kPfRows]) * inv,
+                        (o[c + 3] * w_me + other[(c + 3) * kPfRows]) * inv);
             }
         }
     }
