@@ -147,13 +147,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                 tc_fence_after();
                 // S of tile kt into buffer bb: Qh Kh^T + Ql Kh^T + Qh Kl^T over the 128 dims
                 const uint32_t ks = base + kOffK + bb * 2 * kKImg, dS = tmem + 64 * bb;
-#pragma unroll 1
+                // the 24 MMAs issued back to back (one thread issues one MMA per ~50 cycles
+                // only when nothing else sits between them): descriptors of the k-steps are
+                // the stage's base descriptor plus the step's offset in 16-byte units
+                const uint64_t dkh0 = sw128_desc(ks), dkl0 = sw128_desc(ks + kKImg);
+#pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const uint32_t ko = (k >> 2) * (kKImg / 2) + (k & 3) * 32;
-                    const uint64_t dkh = sw128_desc(ks + ko), dkl = sw128_desc(ks + kKImg + ko);
-                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkh, idS, k > 0);
-                    mma_bf16_ts(dS, tmem + kTmQl + 8 * k, dkh, idS, 1);
-                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkl, idS, 1);
+                    const uint32_t ko = ((k >> 2) * (kKImg / 2) + (k & 3) * 32) >> 4;
+                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkh0 + ko, idS, k > 0);
+                    mma_bf16_ts(dS, tmem + kTmQl + 8 * k, dkh0 + ko, idS, 1);
+                    mma_bf16_ts(dS, tmem + kTmQh + 8 * k, dkl0 + ko, idS, 1);
                 }
                 mma_commit(s_full + 8 * bb);
                 if (kt + 2 < nkv) {  // S(kt) has read key stage bb: refill it
@@ -179,14 +182,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(PrefillArgs
                 tc_fence_after();
                 // O_k += Ph_k V_k + Pl_k V_k for key half k (keys 32 k .. + 31: two slices of 16)
                 const uint32_t vs = base + kOffV + bb * kVImg, pb = base + kOffP + bb * 2 * kPImg;
-#pragma unroll 1
+                const uint64_t dv0 = sw128_desc(vs), dph0 = sw128_desc(pb), dpl0 = sw128_desc(pb + kPImg);
+#pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll 1
+#pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        const uint32_t o = (2 * hf + k) * 32;
-                        const uint64_t dv = sw128_desc(vs + o);
-                        mma_bf16(tmem + 128 + 128 * hf, sw128_desc(pb + o), dv, idO, (kt > 0) | (k > 0));
-                        mma_bf16(tmem + 128 + 128 * hf, sw128_desc(pb + kPImg + o), dv, idO, 1);
+                        const uint32_t o = ((2 * hf + k) * 32) >> 4;
+                        mma_bf16(tmem + 128 + 128 * hf, dph0 + o, dv0 + o, idO, (kt > 0) | (k > 0));
+                        mma_bf16(tmem + 128 + 128 * hf, dpl0 + o, dv0 + o, idO, 1);
                     }
                 }
                 mma_commit(o_done + 8 * bb);
