@@ -36,9 +36,10 @@ namespace {
 //   5. recovered tokens: dequantise, inverse WHT, RoPE at the token's
 //      position (per-record base angle plus a small offset), logits against
 //      the RoPE'd queries, values kept in the rotated frame;
-//   6. the CTA's softmax partial of query head j is pushed to split j mod S,
-//      which merges the S partials after the last barrier, rotates the
-//      output back to the original frame and stores it.
+//   6. the CTA's softmax partial of each query head, rotated back to the
+//      original frame (a linear map, so it commutes with the merge), is pushed
+//      in pieces: split r owns a slice of 4-dim quads of every head, merges the
+//      S partials of its quads after the last barrier and stores them.
 // Each half-warp runs its own online softmax over its entries, two entries
 // per step.  Every loop has warp-uniform bounds (entries past the end are
 // computed on a clamped index and masked), so all shuffles run on full
@@ -78,6 +79,13 @@ __host__ __device__ inline int rope_levels(int T) {
     return n;
 }
 
+// The output merge: split r of S owns the 4-dim quads [quad0(r), quad0(r + 1)) of every
+// query head; each split pushes, per head, its partial's quads to their owners and its
+// (max, sum) to every split.  Inbox row (head j, source split): the owner's quads, then
+// max and sum (a stride of whole quads).
+__host__ __device__ inline int quad0(int r, int S) { return (32 * r) / S; }
+__host__ __device__ inline int inbox_stride(int S) { return 4 * ((32 + S - 1) / S + 1); }
+
 template <int R, int N>
 __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int max_l1, int beta, bool route,
                                                       int flags) {
@@ -112,7 +120,7 @@ __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int m
     L.off = (unsigned)o; o = al16(o + (size_t)N * row);
     L.base = (unsigned)o; o = al16(o + (size_t)2 * kBatchRecs * row);   // two batches in flight
     L.rbits = (unsigned)o; o = al16(o + (size_t)2 * kBatchRecs * 4);
-    L.inbox = (unsigned)o; o = al16(o + (size_t)((R + S - 1) / S) * S * hsq::kPartStride * 4);
+    L.inbox = (unsigned)o; o = al16(o + (size_t)R * S * inbox_stride(S) * 4);
     // one region, used in turn for: every split's routing keys (until the
     // selection is made), two batches of gathered L3 records, the warp partials
     size_t rec = 2 * (size_t)kFetchBatchBytes;
@@ -177,6 +185,22 @@ __device__ __forceinline__ void angle_add4(float4& c1, float4& s1, const float4 
                                  fmaf(s1.z, c2.z, c1.z * s2.z), fmaf(s1.w, c2.w, c1.w * s2.w));
     c1 = c;
     s1 = s;
+}
+
+// Walsh-Hadamard transform of 128 values held 4 per lane (dims 4 lane .. 4 lane + 3)
+// across a full warp: index bits 0-1 in registers, bits 2-6 across the lanes
+__device__ __forceinline__ void fwht_quad(float4& v) {
+    const float a = v.x + v.y, b = v.x - v.y, c = v.z + v.w, d = v.z - v.w;
+    v = make_float4(a + c, b + d, a - c, b - d);
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const float sgn = (lane & m) ? -1.f : 1.f;  // upper lane: p - v, lower lane: v + p
+        v.x = fmaf(sgn, v.x, __shfl_xor_sync(0xffffffffu, v.x, m));
+        v.y = fmaf(sgn, v.y, __shfl_xor_sync(0xffffffffu, v.y, m));
+        v.z = fmaf(sgn, v.z, __shfl_xor_sync(0xffffffffu, v.z, m));
+        v.w = fmaf(sgn, v.w, __shfl_xor_sync(0xffffffffu, v.w, m));
+    }
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -781,7 +805,8 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     }
 
     // 6. merge the two halves of each warp, then the warps, into this split's
-    //    partial, and push query head j's partial to split j mod S
+    //    partial of each query head, rotate it back to the original frame, and
+    //    push its quads to the splits that own them
 #pragma unroll
     for (int j = 0; j < R; ++j) {
         const float mo = __shfl_xor_sync(kFull, sm.m[j], 16);
@@ -809,7 +834,8 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     }
     __syncthreads();
     if (!kRoute) cluster_wait();  // every CTA of the cluster runs: remote stores may start
-    if (tid < R * 32) {
+    const int P = inbox_stride(S);
+    if (tid < R * 32) {  // warp j: this split's partial of query head j, 4 dims (a quad) per lane
         const int j = tid >> 5, q4 = tid & 31;
         float M = -INFINITY;
 #pragma unroll
@@ -824,42 +850,43 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
             Lsum += p[129] * wt;
             A.x += v.x * wt; A.y += v.y * wt; A.z += v.z * wt; A.w += v.w * wt;
         }
-        float* dst = cluster.map_shared_rank(s_inbox, j % S) + ((size_t)(j / S) * S + s) * hsq::kPartStride;
-        *reinterpret_cast<float4*>(dst + 4 * q4) = A;
-        if (q4 == 0) { dst[128] = M; dst[129] = Lsum; }
+        if constexpr (kRot) {  // back to the original frame (linear, so before the merge): Pi^T = diag(s) H / sqrt(d)
+            fwht_quad(A);
+            const float* sq = sg + (q4 < 16 ? 0 : 4);  // this thread's signs of dims 4 q4 .. 4 q4 + 3
+            A.x *= sq[0] * kRsqrtD; A.y *= sq[1] * kRsqrtD; A.z *= sq[2] * kRsqrtD; A.w *= sq[3] * kRsqrtD;
+        }
+        const int owner = ((q4 + 1) * S + 31) / 32 - 1;  // the split whose quads include quad q4
+        float* dst = cluster.map_shared_rank(s_inbox, owner) + ((size_t)j * S + s) * P;
+        *reinterpret_cast<float4*>(dst + 4 * (q4 - quad0(owner, S))) = A;
+        if (q4 < S) {
+            float* row = cluster.map_shared_rank(s_inbox, q4) + ((size_t)j * S + s) * P;
+            row[P - 4] = M;
+            row[P - 3] = Lsum;
+        }
     }
-    cluster.sync();  // every partial is in its owner's inbox; no remote access follows
+    cluster.sync();  // every partial is in its owners' inboxes; no remote access follows
 
-    // query heads s, s + S, ...: merge the S partials (warp k: head s + k S, 4 dims per lane)
-    float* s_o = s_qr[0];  // [R][128]; the RoPE'd queries are no longer needed
-    const int nmine = (R - s + S - 1) / S;
-    if (nmine > 0) {
-        const int k = min(warp, nmine - 1);
-        const float* in = s_inbox + (size_t)k * S * hsq::kPartStride;
-        const float mr = lane < S ? in[lane * hsq::kPartStride + 128] : -INFINITY;
-        const float lr = lane < S ? in[lane * hsq::kPartStride + 129] : 0.f;
-        const float M = warp_max(mr);
-        const float wr = merge_weight(mr, M);
-        const float Lsum = warp_sum(lr * wr);
+    // this split's quads of every query head: merge the S partials and store
+    const int nq = quad0(s + 1, S) - quad0(s, S);
+#pragma unroll 1
+    for (int i = tid; i < R * nq; i += NT) {
+        const int j = i / nq, kq = i - j * nq;
+        const float* in = s_inbox + (size_t)j * S * P;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int r = 0; r < S; ++r) M = fmaxf(M, in[r * P + P - 4]);
+        float Lsum = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
         for (int r = 0; r < S; ++r) {
-            const float wt = __shfl_sync(kFull, wr, r);
-            const float4 x = *reinterpret_cast<const float4*>(in + r * hsq::kPartStride + 4 * lane);
+            const float wt = merge_weight(in[r * P + P - 4], M);
+            const float4 x = *reinterpret_cast<const float4*>(in + r * P + 4 * kq);
+            Lsum += in[r * P + P - 3] * wt;
             o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
         }
         const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-        if (warp < nmine)
-            *reinterpret_cast<float4*>(s_o + k * kDim + 4 * lane) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-        __syncthreads();
-        const int kk = min(hw, nmine - 1);
-        float ov[8];
-        load_f32x8_smem(s_o + kk * kDim, ov);
-        if constexpr (kRot) fwht(ov, kFull);  // back to the original frame: Pi^T o = diag(s) H o / sqrt(d)
-        const float sc = kRot ? kRsqrtD : 1.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ov[i] *= sg[i] * sc;
-        if (hw < nmine) store_f32x8(a.out + ((size_t)b * c.Hq + h * R + s + kk * S) * kDim, ov);
+        *reinterpret_cast<float4*>(a.out + ((size_t)b * c.Hq + h * R + j) * kDim + 4 * (quad0(s, S) + kq)) =
+            make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
     }
 }
 
