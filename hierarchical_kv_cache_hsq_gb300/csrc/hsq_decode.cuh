@@ -55,7 +55,7 @@ constexpr int kMaxSplits = 16;   // largest (non-portable) cluster
 // which still fit the R <= 5 softmax state in registers) measured slower.
 template <int R>
 __host__ __device__ constexpr int dec_threads() { return 256; }
-enum : int { kStageL2 = 1, kKeepLogits = 2, kStageL1 = 4, kStageBitmap = 8 };
+enum : int { kStageL2 = 1, kKeepLogits = 2, kStageL1 = 4, kStageBitmap = 8, kStageSketch = 16 };
 
 struct DecodeArgs {
     const float* q; const int32_t* pos; int32_t* sel; float* out; int* err; int from_staging;
@@ -65,7 +65,7 @@ constexpr int kStagedFlags = kStageL2 | kKeepLogits | kStageL1 | kStageBitmap;
 
 struct DecodeLayout {
     int span, l1span, nlev, nb0;
-    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, sel, mask, bitmap;
+    unsigned l2k, l2v, l2kn, l2vn, cnt, l1k, l1v, l1kn, l1vn, logit, sel, mask, bitmap, l1qs, l1qn;
     unsigned lev, b0, off, base, rbits, inbox, rec, total;
 };
 
@@ -98,6 +98,7 @@ __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int m
     const size_t row = (size_t)kDim * 4;
     size_t o = 0;
     L.l2k = L.l2v = L.l2kn = L.l2vn = L.cnt = L.l1k = L.l1v = L.l1kn = L.l1vn = L.logit = L.bitmap = 0;
+    L.l1qs = L.l1qn = 0;
     if (flags & kStageL2) {
         L.l2k = (unsigned)o; o = al16(o + (size_t)L.span * 48);
         L.l2v = (unsigned)o; o = al16(o + (size_t)L.span * 48);
@@ -110,6 +111,10 @@ __host__ __device__ inline DecodeLayout decode_layout(int G, int T, int S, int m
         L.l1v = (unsigned)o; o = al16(o + (size_t)L.l1span * 64);
         L.l1kn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
         L.l1vn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
+    }
+    if (flags & kStageSketch) {  // TQ-QKV: the sketches of the split's L1 keys
+        L.l1qs = (unsigned)o; o = al16(o + (size_t)L.l1span * 16);
+        L.l1qn = (unsigned)o; o = al16(o + (size_t)L.l1span * 4);
     }
     if (flags & kKeepLogits) { L.logit = (unsigned)o; o = al16(o + (size_t)L.span * R * 4); }
     if (flags & kStageBitmap) { L.bitmap = (unsigned)o; o = al16(o + (size_t)((T + 31) / 32) * 4); }
@@ -277,6 +282,9 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     __shared__ __align__(16) float s_qt[R][kDim];
     __shared__ __align__(16) float s_qr[R][kDim];
     __shared__ __align__(16) float s_sq[kQJL ? R : 1][kDim];  // S Pi q^r_j (TQ-QKV)
+    // TQ-QKV: the sketch words and norms of a batch's fetched tokens, gathered with its records
+    __shared__ __align__(16) uint4 s_tsk[kQJL ? 2 : 1][kQJL ? kFetchBatchBytes / 136 : 1];
+    __shared__ float s_tnm[kQJL ? 2 : 1][kQJL ? kFetchBatchBytes / 136 : 1];
     __shared__ __align__(16) float s_x[NH][16];
     __shared__ SelectSmem s_ss;
     __shared__ __align__(16) uint32_t s_stats[kMaxSplits][4];  // per split: non-empty keys, max key, min key
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     // tier buffers of this head: bh, except under per-query-head routing (run with R = 1)
     const size_t bb = R == 1 ? buf_head(c, b, h) : (size_t)bh;
     const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
-    constexpr int fl = kStaged ? kStagedFlags : 0;
+    constexpr int fl = kStaged ? (kStagedFlags | (kQJL ? kStageSketch : 0)) : 0;
     const DecodeLayout L = decode_layout<R, N>(c.G, c.cap, S, c.max_l1, c.beta, kRoute, fl);
 
     const int g0 = (int)((long long)c.G * s / S), g1 = (int)((long long)c.G * (s + 1) / S);
@@ -378,6 +386,10 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
         stage4(reinterpret_cast<float*>(s_dyn + L.l1vn), g_l1vn, n1);
     }
     if constexpr (stb) stage4(reinterpret_cast<float*>(s_dyn + L.bitmap), reinterpret_cast<const float*>(g_bitmap), c.W);
+    if constexpr (kQJL && st1) {
+        stage16(s_dyn + L.l1qs, c.l1_qs + (bb * c.max_l1 + e0) * 4, n1 * 16);
+        stage4(reinterpret_cast<float*>(s_dyn + L.l1qn), c.l1_qn + bb * c.max_l1 + e0, n1);
+    }
     // RoPE rows: level k row j = hi[j * 16^k] (angle 256 j 16^k omega), b0 row j = lo[N j], off row n = lo[n]
     const int n_hi = (tb.max_pos + 255) / 256;
 #pragma unroll 1
@@ -407,40 +419,36 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     prepare_queries<R>(qx, pos, sg, tb, s_qt, s_qr, kRot);
     cp_async_wait_group<1>();  // the L2 pass's inputs
     __syncthreads();
-    if constexpr (kQJL) {
-        // the sketched rotated queries S q~_j (read after the barriers that precede the
-        // L1 pass): thread t takes half of row t mod 128 of S for every head, its 16
-        // loads issued together; the two halves meet in shared memory
-        static_assert(NT == 2 * kDim, "one row half per thread");
-        const int i = tid & (kDim - 1), part = tid >> 7;
-        const float4* srow = reinterpret_cast<const float4*>(c.qjl_s + (size_t)i * kDim) + part * (kDim / 8);
-        float4 sv[kDim / 8];
+    // TQ-QKV: rows [i0, i1) of the sketched rotated queries S q~_j, 16 threads per row (8
+    // dims each, a fixed half-warp reduction), every head; with `push` each row goes to
+    // every split of the cluster (remote stores), else to this CTA's s_sq only
+    auto sq_rows = [&](int i0, int i1, bool push) {
+        const unsigned hm = half_mask();
+#pragma unroll 1
+        for (int i = i0 + hw; i < i1; i += NH) {
+            const float4* srow = reinterpret_cast<const float4*>(c.qjl_s + (size_t)i * kDim) + 2 * l;
+            const float4 s0 = __ldg(srow), s1 = __ldg(srow + 1);
+            float v[R];
 #pragma unroll
-        for (int k = 0; k < kDim / 8; ++k) sv[k] = __ldg(srow + k);
-        float acc[R];
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const float* qj = s_qt[j] + part * (kDim / 2);
-            float a = 0.f;
-#pragma unroll
-            for (int k = 0; k < kDim / 8; ++k) {
-                a = fmaf(sv[k].x, qj[4 * k], a);
-                a = fmaf(sv[k].y, qj[4 * k + 1], a);
-                a = fmaf(sv[k].z, qj[4 * k + 2], a);
-                a = fmaf(sv[k].w, qj[4 * k + 3], a);
+            for (int j = 0; j < R; ++j) {
+                const float* qj = s_qt[j] + 8 * l;
+                float a = s0.x * qj[0];
+                a = fmaf(s0.y, qj[1], a); a = fmaf(s0.z, qj[2], a); a = fmaf(s0.w, qj[3], a);
+                a = fmaf(s1.x, qj[4], a); a = fmaf(s1.y, qj[5], a); a = fmaf(s1.z, qj[6], a); a = fmaf(s1.w, qj[7], a);
+                v[j] = half_sum(a, hm);
             }
-            acc[j] = a;
-        }
-        if (part == 1) {
+            if (push) {
+                if (l < S) {
 #pragma unroll
-            for (int j = 0; j < R; ++j) s_sq[j][i] = acc[j];
-        }
-        __syncthreads();
-        if (part == 0) {
+                    for (int j = 0; j < R; ++j) *cluster.map_shared_rank(&s_sq[j][i], l) = v[j];
+                }
+            } else if (l == 0) {
 #pragma unroll
-            for (int j = 0; j < R; ++j) s_sq[j][i] += acc[j];
+                for (int j = 0; j < R; ++j) s_sq[j][i] = v[j];
+            }
         }
-    }
+    };
+    if constexpr (kQJL && !kRoute) sq_rows(0, kDim, false);  // (read after the barriers that precede the L1 pass)
 
     const float* c4 = s_cb;
     const float* c3 = s_cb + 32;
@@ -454,6 +462,7 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
         }
     }
     if (kRoute) cluster_wait();  // every CTA of the cluster runs: remote stores may start
+    if constexpr (kQJL && kRoute) sq_rows(kDim * s / S, kDim * (s + 1) / S, true);  // (in every split after the selection barrier)
     if constexpr (kRoute || keep) {
         // routing keys (each goes to every split, and so do this split's key
         // statistics) and the L2 logits per query head, one pass
@@ -552,9 +561,27 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     //    unselected summaries.  Per record, its base angle g N omega (staged
     //    rows only) and its L1 bits go to slot k & 1.
     uint4 pre[kChunksPT];
+    // TQ-QKV: thread u < kBatchRecs * N also gathers token u of the batch's records:
+    // its sketch words and norm (norm 0 for a slot that is no token)
+    uint4 psk = make_uint4(0u, 0u, 0u, 0u);
+    float pnm = 0.f;
     auto issue = [&](int k) {
         const int r0 = f0 + k * kBatchRecs;
         const int nrec = min(kBatchRecs, f1 - r0);
+        if constexpr (kQJL) {
+            psk = make_uint4(0u, 0u, 0u, 0u);
+            pnm = 0.f;
+            if (tid < nrec * N) {
+                const int rec = tid / N, n = tid - rec * N;
+                const int g = s_sel[r0 + rec];
+                const int t = g * N + n;
+                if ((g >= 0) & (t < c.T)) {
+                    const size_t ti = bb * (size_t)c.G * N + (size_t)t;
+                    psk = __ldg(reinterpret_cast<const uint4*>(c.l3_qs) + ti);
+                    pnm = __ldg(c.l3_qn + ti);
+                }
+            }
+        }
 #pragma unroll
         for (int u = 0; u < kChunksPT; ++u) {
             const int ch = tid + u * NT;
@@ -621,12 +648,18 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     uint4 nwa = make_uint4(0, 0, 0, 0), nwb = nwa;
     float nga = 0.f, ngb = 0.f;
     auto l1_sketch = [&](int blk_) {
-        const size_t ia = bb * c.max_l1 + e0 + min(blk_ + hw, n1 - 1);
-        const size_t ib = bb * c.max_l1 + e0 + min(blk_ + hw + NH, n1 - 1);
-        nwa = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ia);
-        nwb = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ib);
-        nga = __ldg(c.l1_qn + ia);
-        ngb = __ldg(c.l1_qn + ib);
+        const int ja_ = min(blk_ + hw, n1 - 1), jb_ = min(blk_ + hw + NH, n1 - 1);
+        if constexpr (st1) {  // staged with the split's other L1 inputs
+            const uint4* qs = reinterpret_cast<const uint4*>(s_dyn + L.l1qs);
+            const float* qn = reinterpret_cast<const float*>(s_dyn + L.l1qn);
+            nwa = qs[ja_]; nwb = qs[jb_]; nga = qn[ja_]; ngb = qn[jb_];
+        } else {
+            const size_t ia = bb * c.max_l1 + e0 + ja_, ib = bb * c.max_l1 + e0 + jb_;
+            nwa = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ia);
+            nwb = __ldg(reinterpret_cast<const uint4*>(c.l1_qs) + ib);
+            nga = __ldg(c.l1_qn + ia);
+            ngb = __ldg(c.l1_qn + ib);
+        }
     };
     if constexpr (kQJL) {
         if (n1 > 0) l1_sketch(0);
@@ -702,6 +735,12 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
                     const int ch = tid + u * NT;
                     if (ch < kFetchBatchBytes / 16) dstb[ch] = pre[u];
                 }
+                if constexpr (kQJL) {
+                    if (tid < kBatchRecs * N) {
+                        s_tsk[kb_ & 1][tid] = psk;
+                        s_tnm[kb_ & 1][tid] = pnm;
+                    }
+                }
                 if constexpr (kHot) {  // records fetched from L3 into their free slots
                     const int hr0 = f0 + kb_ * kBatchRecs;
                     const int hnb = min(kBatchRecs, f1 - hr0);
@@ -731,14 +770,9 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
             const float* sbase = s_base + (kb_ & 1) * kBatchRecs * kDim;
             const uint32_t* rbits = s_rbits + (kb_ & 1) * kBatchRecs;
             // TQ-QKV: token u's sketch words and weight (0 for a slot that is no token)
-            auto tok_sketch = [&](int u, uint4& wd, float& wt) {
-                const int rec = u / N, n = u - rec * N;
-                const int g = s_sel[r0 + rec];
-                const int t = g * N + n;
-                const bool ok = (g >= 0) & (t < c.T);
-                const size_t ti = bb * (size_t)c.G * N + (size_t)(ok ? t : 0);
-                wd = __ldg(reinterpret_cast<const uint4*>(c.l3_qs) + ti);
-                wt = ok ? kQjlScale * __ldg(c.l3_qn + ti) : 0.f;
+            auto tok_sketch = [&](int u, uint4& wd, float& wt) {  // (gathered with the batch)
+                wd = s_tsk[kb_ & 1][u];
+                wt = kQjlScale * s_tnm[kb_ & 1][u];
             };
             // one recovered token: validity, RoPE'd key and rotated-frame value
             auto token = [&](int u, float kv[8], float vv[8]) -> bool {
@@ -934,7 +968,7 @@ int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
     if (hsq::allow_big_clusters(fn, ctx->device) != cudaSuccess) return 0;
     const size_t cap = (size_t)ctx->smem_optin > fa.sharedSizeBytes ? ctx->smem_optin - fa.sharedSizeBytes : 0;
-    const int fl = kStaged ? kStagedFlags : 0;
+    const int fl = kStaged ? (kStagedFlags | (ctx->cfg.qjl ? kStageSketch : 0)) : 0;
     int last = 0;
     for (int S = s_hi; S >= 1; --S) {
         const size_t smem = decode_layout<R, N>(G, T, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute, fl).total;
@@ -973,8 +1007,8 @@ hsq_ctx::Plan decode_plan(hsq_ctx* ctx, int B, int T, int heads) {
 
 template <int R, int N, bool kRoute, bool kStaged>
 hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, int S, cudaStream_t st) {
-    const DecodeLayout L =
-        decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute, kStaged ? kStagedFlags : 0);
+    const DecodeLayout L = decode_layout<R, N>(v.G, v.cap, S, v.max_l1, v.beta, kRoute,
+                                               kStaged ? (kStagedFlags | (v.qjl_s ? kStageSketch : 0)) : 0);
     const DecodeFn kern = decode_fn<R, N, kRoute, kStaged>(v.rot != 0, v.qjl_s != nullptr, v.hot_tag != nullptr);
     const void* fn = (const void*)kern;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
