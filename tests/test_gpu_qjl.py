@@ -157,3 +157,40 @@ def test_qjl_refused_by_append_and_needs_turboquant():
     assert ei.value.status == 6
     with pytest.raises(H.HSQError):
         H.Context(H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, 100, w.T + 8, w.theta, codec="plain", qjl=True))
+
+
+def test_qjl_in_place_variant_equals_staged():
+    """An L1 capacity of 40000 slots does not fit a split's shared memory, so the launch
+    plan takes the variant that reads the tiers and the L1 sketches in place (and forms
+    every row of S q~ itself); its selection and output equal the staged variant's."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = WL["tiny_1k"]
+    li = W.layer_inputs(w, rope=lambda x, p: O.rope(x, p, w.theta))
+    S = W.qjl_matrix(w)
+    dt = torch.bfloat16 if w.storage == "bf16" else torch.float32
+    K = torch.from_numpy(np.ascontiguousarray(li.K, np.float32)).cuda().to(dt).contiguous()
+    V = torch.from_numpy(np.ascontiguousarray(li.V, np.float32)).cuda().to(dt).contiguous()
+    q, pos = W.queries(w, steps=3)
+    outs, sels = [], []
+    for max_l1 in (40000, max(w.l1_size, 1)):
+        cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, max_l1, w.T + w.steps + 1, w.theta, qjl=True)
+        ctx = H.Context(cfg)
+        cache = H.allocate_cache(ctx, w.B, w.T)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        H.set_qjl_matrix(cache, S)
+        H.hsq_encode(ctx, cache, K, V)
+        o_steps, s_steps = [], []
+        for s in range(3):
+            sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+            out = torch.empty((w.B, w.Hq, 128), device="cuda")
+            H.hsq_decode_step(ctx, cache, torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda(), sel, out)
+            o_steps.append(out.cpu().numpy())
+            s_steps.append(sel.cpu().numpy())
+        assert H.hsq_sync_status(ctx) == 0
+        outs.append(o_steps)
+        sels.append(s_steps)
+        ctx.close()
+    for s in range(3):
+        np.testing.assert_array_equal(sels[0][s], sels[1][s])
+        assert np.all(rel_l2(outs[0][s], outs[1][s]) <= 1e-5)
