@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--group-n", type=int, default=0, help="group size N override for the per-layer mode")
     p.add_argument("--graph", action="store_true",
                    help="per-layer mode: replay each decode step (all layers) as one captured CUDA graph")
+    p.add_argument("--overlap-launch", action="store_true",
+                   help="per-layer mode: launch the decode kernels with programmatic stream serialization "
+                        "(hsq_config.overlap_launch: each layer's launch overlaps the previous layer's tail)")
     p.add_argument("--codec", choices=["tq", "plain"], default="tq",
                    help="codec of the timed caches: TurboQuant (default) or Plain-KV (no rotation)")
     p.add_argument("--qjl", action="store_true",
@@ -1032,7 +1035,8 @@ def run_layers(args, rank, world, local):
     q, pos = W.queries(w, steps=w.steps)
     cfgs = {b: H.make_config(w.Hq, w.Hkv, w.N, b, w.B, w.T, w.l1_size, w.T + w.steps + 1, w.theta,
                              args.n_splits, route_max=args.route_max, codec=args.codec,
-                             route_per_head=args.route_per_head, hot_slots=args.hot_slots) for b in betas}
+                             route_per_head=args.route_per_head, hot_slots=args.hot_slots,
+                             overlap_launch=args.overlap_launch) for b in betas}
     ctxs = {b: H.Context(c) for b, c in cfgs.items()}
     ctx0 = ctxs[betas[0]]
     K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
@@ -1167,7 +1171,9 @@ def run_layers(args, rank, world, local):
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d128 T{w.T} N{w.N} L1={w.l1_size} "
                                f"{L} layers, beta {'/'.join(map(str, betas))}",
                    "layers": "layer 0's K/V draw for every layer; per-layer seeded L1 membership and signs",
-                   "launch": "one CUDA graph per step (all layers)" if args.graph else "one call per layer",
+                   "launch": ("one CUDA graph per step (all layers)" if args.graph else "one call per layer")
+                             + (", programmatic stream serialization (overlap_launch)" if args.overlap_launch
+                                else ""),
                    "codec": args.codec,
                    "hot_slots": args.hot_slots,
                    "queries": "correlated across steps (needle law)" if w.needle else "independent per step",

@@ -49,7 +49,7 @@ class hsq_config(ctypes.Structure):
         ("max_ctx", ctypes.c_int), ("max_l1", ctypes.c_int), ("max_pos", ctypes.c_int),
         ("n_splits", ctypes.c_int), ("l1_sinks", ctypes.c_int), ("l1_recent", ctypes.c_int),
         ("route_max", ctypes.c_int), ("codec", ctypes.c_int), ("route_per_head", ctypes.c_int),
-        ("qjl", ctypes.c_int), ("hot_slots", ctypes.c_int),
+        ("qjl", ctypes.c_int), ("hot_slots", ctypes.c_int), ("overlap_launch", ctypes.c_int),
     ]
 
 
@@ -143,7 +143,8 @@ def hsq_codebook(bits: int, dim: int = 128):
 def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: int, max_l1: int,
                 max_pos: int, theta: float = 1.0e6, n_splits: int = 0, sinks: int = 0,
                 recent: int = 0, route_max: bool = False, codec: str = "tq",
-                route_per_head: bool = False, qjl: bool = False, hot_slots: int = 0) -> hsq_config:
+                route_per_head: bool = False, qjl: bool = False, hot_slots: int = 0,
+                overlap_launch: bool = False) -> hsq_config:
     """recent > 0 makes caches of this context growable (hsq_append) with an
     L1 recent window of that length and `sinks` permanent sink positions;
     route_max scores a group by its best query head instead of their sum;
@@ -152,7 +153,9 @@ def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: i
     selection (sel [B, Hq, beta]); qjl adds TQ-QKV's 1-bit sketches of the key
     residuals (set the sketch matrix with set_qjl_matrix); hot_slots > 0 gives
     the fused decode step a device table of that many recently fetched L3
-    records per (sequence, KV head)."""
+    records per (sequence, KV head); overlap_launch launches the decode kernels
+    with programmatic stream serialization (the next layer's launch overlaps
+    this one's tail; results unchanged)."""
     if codec not in CODECS:
         raise ValueError(f"codec must be one of {tuple(CODECS)}")
     return hsq_config(n_q_heads=Hq, n_kv_heads=Hkv, head_dim=128, group_n=N, beta=beta,
@@ -160,7 +163,7 @@ def make_config(Hq: int, Hkv: int, N: int, beta: int, max_batch: int, max_ctx: i
                       max_ctx=max_ctx, max_l1=max_l1, max_pos=max_pos, n_splits=n_splits,
                       l1_sinks=sinks, l1_recent=recent, route_max=1 if route_max else 0,
                       codec=CODECS[codec], route_per_head=1 if route_per_head else 0, qjl=1 if qjl else 0,
-                      hot_slots=hot_slots)
+                      hot_slots=hot_slots, overlap_launch=1 if overlap_launch else 0)
 
 
 def hsq_cache_sizes(cfg: hsq_config, B: int, T: int) -> Dict[str, int]:

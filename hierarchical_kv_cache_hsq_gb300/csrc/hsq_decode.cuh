@@ -307,6 +307,11 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     // tier buffers of this head: bh, except under per-query-head routing (run with R = 1)
     const size_t bb = R == 1 ? buf_head(c, b, h) : (size_t)bh;
     const int tid = threadIdx.x, hw = tid >> 4, l = hlane(), lane = tid & 31, warp = tid >> 5;
+    // Under a programmatic (overlapped) launch: wait for the stream's preceding
+    // kernel to complete before touching global memory, then let the next one be
+    // scheduled.  Both are no-ops under ordinary stream order.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int fl = kStaged ? (kStagedFlags | (kQJL ? kStageSketch : 0)) : 0;
     const DecodeLayout L = decode_layout<R, N>(c.G, c.cap, S, c.max_l1, c.beta, kRoute, fl);
 
@@ -931,7 +936,10 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
 
 using DecodeFn = void (*)(CacheView, DecodeArgs, Tables);
 
-cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaStream_t st, cudaLaunchAttribute* at) {
+// at: room for two attributes (the cluster shape, and with overlap the
+// programmatic stream serialization of hsq_config.overlap_launch).
+cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaStream_t st, cudaLaunchAttribute* at,
+                                 bool overlap = false) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(S, bh, 1);
     lc.blockDim = dim3(threads, 1, 1);
@@ -943,6 +951,11 @@ cudaLaunchConfig_t decode_config(int S, int bh, int threads, size_t smem, cudaSt
     at[0].val.clusterDim.z = 1;
     lc.attrs = at;
     lc.numAttrs = 1;
+    if (overlap) {
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
+        lc.numAttrs = 2;
+    }
     return lc;
 }
 
@@ -974,7 +987,7 @@ int best_splits(hsq_ctx* ctx, int G, int T, int bh, int s_hi) {
         const size_t smem = decode_layout<R, N>(G, T, S, ctx->cfg.max_l1, ctx->cfg.beta, kRoute, fl).total;
         if (smem > cap) continue;
         if (hsq::raise_smem_limit(fn, ctx->device, smem) != cudaSuccess) continue;
-        cudaLaunchAttribute at[1];
+        cudaLaunchAttribute at[2];
         cudaLaunchConfig_t lc = decode_config(S, bh, dec_threads<R>(), smem, 0, at);
         int nc = 0;
         if (cudaOccupancyMaxActiveClusters(&nc, fn, &lc) != cudaSuccess || nc < 1) continue;
@@ -1013,8 +1026,9 @@ hsq_status launch_decode(hsq_ctx* ctx, const CacheView& v, const DecodeArgs& a, 
     const void* fn = (const void*)kern;
     cudaError_t e = hsq::raise_smem_limit(fn, ctx->device, L.total);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "cudaFuncSetAttribute(decode)");
-    cudaLaunchAttribute at[1];
-    const cudaLaunchConfig_t lc = decode_config(S, v.B * v.Hkv, dec_threads<R>(), L.total, st, at);
+    cudaLaunchAttribute at[2];
+    const cudaLaunchConfig_t lc =
+        decode_config(S, v.B * v.Hkv, dec_threads<R>(), L.total, st, at, ctx->cfg.overlap_launch != 0);
     const Tables tb = make_tables(ctx);
     e = cudaLaunchKernelEx(&lc, kern, v, a, tb);
     if (e != cudaSuccess) return hsq::cuda_fail(ctx, e, "decode launch");

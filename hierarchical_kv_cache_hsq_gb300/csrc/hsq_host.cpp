@@ -188,6 +188,7 @@ std::string check_config(const hsq_config* c) {
         if (c->codec != HSQ_CODEC_TQ || c->qjl || c->route_per_head)
             return "hot_slots needs codec HSQ_CODEC_TQ, qjl 0 and route_per_head 0";
     }
+    if (c->overlap_launch != 0 && c->overlap_launch != 1) return "overlap_launch must be 0 or 1";
     return "";
 }
 

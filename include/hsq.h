@@ -163,6 +163,17 @@ typedef struct hsq_config {
        when consecutive steps select overlapping groups.  Needs codec
        HSQ_CODEC_TQ, qjl 0 and route_per_head 0. */
     int hot_slots;
+    /* 1: launch the decode kernels (hsq_decode_step, hsq_decode_attn) with
+       programmatic stream serialization.  Such a launch may be scheduled onto
+       the GPU while the stream's preceding kernel still runs; the kernel then
+       waits, before its first read or write of global memory, until that
+       kernel has completed and its writes are visible, so results are the
+       same as with 0.  Once all of its own CTAs are running it lets the
+       stream's next kernel be scheduled the same way (that kernel, when it is
+       another library's, must wait on its own).  It hides the launch gap
+       between decode steps issued back to back (one per layer), directly or
+       captured in a CUDA graph.  0: ordinary stream order. */
+    int overlap_launch;
 } hsq_config;
 
 /*

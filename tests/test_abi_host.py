@@ -176,3 +176,12 @@ def test_hot_table_sizes_and_requirements(H):
                 dict(hot_slots=64, route_per_head=True)):
         with pytest.raises(H.HSQError):
             H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, **bad), 2, 4096)
+
+
+def test_overlap_launch_flag_is_checked(H):
+    ok = H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000, overlap_launch=True), 2, 4096)
+    assert ok == H.hsq_cache_sizes(H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000), 2, 4096)
+    cfg = H.make_config(32, 8, 16, 64, 2, 4096, 100, 5000)
+    cfg.overlap_launch = 2
+    with pytest.raises(H.HSQError):
+        H.hsq_cache_sizes(cfg, 2, 4096)
