@@ -20,7 +20,10 @@ struct hsq_ctx {
     int* d_route_ctr = nullptr;
     int* d_prefix = nullptr;
     int* d_err = nullptr;
-    float* d_qjl_sb = nullptr;  // TQ-QKV: the last encode's sketch matrix as tensor-core B fragments (64 KB)
+    float* d_qjl_sb = nullptr;  // TQ-QKV: the last encode's S Pi as tensor-core B fragments (64 KB)
+    // TQ-QKV: the last encode's L3 key codes and norms in device memory,
+    // [max_batch][Hkv][G_max][N * 64 codes | N f32 norms], read by the sketch pass
+    uint8_t* d_qjl_kc = nullptr;
     // Decode launch plan per cache shape: cluster size S (0 = no launchable
     // shape) and whether the split's inputs are staged in shared memory.
     struct Plan { int B, T, route, S, staged; };

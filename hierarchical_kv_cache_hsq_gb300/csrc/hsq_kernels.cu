@@ -80,6 +80,9 @@ struct EncodeOut {
     // prefill: the attention's key (RoPE'd, bf16 hi + lo) and transposed value
     // operand images, 64-key tiles (hsq_prefill.cu); used by the kPF variant only
     uint8_t* pf_kh; uint8_t* pf_kl; uint8_t* pf_vt; int pf_nkt;
+    // TQ-QKV: a device copy of every L3 record's key codes and norms,
+    // [B][Hkv][G][N * 64 | N * 4] (NULL: none)
+    uint8_t* kc3;
 };
 
 // TQ3 of one group summary (this half-warp's 8 dims of the mean; x is
@@ -246,6 +249,14 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
         uint4* dst = reinterpret_cast<uint4*>(o.l3 + (((size_t)b * c.Hkv + h) * c.G + g0) * (N * 136));
         const uint4* src = reinterpret_cast<const uint4*>(&s_rec[0][0]);
         for (int i = threadIdx.x; i < ng * (N * 136 / 16); i += blockDim.x) dst[i] = src[i];
+        if (o.kc3) {  // the key codes (chunks 0 .. 4N) and key norms (chunks 8N .. 8N + N/4) again
+            constexpr int kKC = N * 68 / 16;
+            uint4* kd = reinterpret_cast<uint4*>(o.kc3 + (((size_t)b * c.Hkv + h) * c.G + g0) * (N * 68));
+            for (int i = threadIdx.x; i < ng * kKC; i += blockDim.x) {
+                const int j = i / kKC, r = i - j * kKC;
+                kd[i] = src[j * (N * 136 / 16) + (r < 4 * N ? r : 4 * N + r)];
+            }
+        }
     }
 
     // L2 summaries, group j by warp j: mean over members in token order, then TQ3
@@ -291,21 +302,28 @@ __global__ void __launch_bounds__(N * 32, 16 * 3 / N) encode_kernel(CacheView c,
 }
 
 // ---------------------------------------------------------------------------
-// TQ-QKV, encode side: the 1-bit sketches of the key residuals.  One CTA per
-// (group g, KV head h, sequence b), one half-warp per token (N / 2 warps):
-// every token's L3 key residual, then, for the tokens in L1, the L1 key's.
-// Both redo the quantiser decision of encode_kernel with the same
-// arithmetic, so the residual is that of the stored codes.
+// TQ-QKV, encode side: the 1-bit sketches of the key residuals, one half-warp
+// per residual (qjl_kernel: L3, qjl_l1_kernel: L1).  The sketch of a residual rho taken in the rotated frame is sign(S Pi rho');
+// with rho' the residual in the original frame, S Pi is one fixed matrix per
+// layer, so the kernel forms rho' and multiplies by S Pi (formed once per
+// encode, `qjl_pack_kernel`):
+//   L3: rho' = RoPE(k_t - k^_t, t),  k^_t = n Pi^T c^ (c^: the stored codes'
+//       codebook values, n: the stored norm);
+//   L1: rho' = RoPE(k_t, t) - n Pi^T c^1 (c^1: the stored L1 codes).
+// Both read the codes encode_kernel wrote (the L3 key codes from a device
+// copy, the L1 codes from the tier), so the residual is that of the stored
+// codes by construction; one inverse transform per residual.
 // ---------------------------------------------------------------------------
 
 struct SketchOut {
-    // S as the B operand of the m16n8k16 tensor-core product (k = dimension d,
+    // S Pi as the B operand of the m16n8k16 tensor-core product (k = dimension d,
     // n = sketch row i), in fragment order: for n-tile nt (rows 8 nt ..) and
     // k-step ks (dims 16 ks ..), lane (g, q) = (lane / 4, lane % 4) holds at
-    // [(nt * 8 + ks) * 32 + lane] the bf16 pairs {S[i][d], S[i][d + 1]} and
-    // {S[i][d + 8], S[i][d + 9]}, i = 8 nt + g, d = 16 ks + 2 q, of S's bf16
-    // rounding (hi) and of the bf16 rounding of the remainder (lo)
-    const uint4* Sf; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn; const int32_t* prefix;
+    // [(nt * 8 + ks) * 32 + lane] the bf16 pairs {M[i][d], M[i][d + 1]} and
+    // {M[i][d + 8], M[i][d + 9]}, M = S Pi, i = 8 nt + g, d = 16 ks + 2 q, of
+    // M's bf16 rounding (hi) and of the bf16 rounding of the remainder (lo)
+    const uint4* Sf; uint32_t* l1_qs; float* l1_qn; uint32_t* l3_qs; float* l3_qn;
+    const uint8_t* kc3;  // the L3 key codes and norms, [B][Hkv][G][N * 64 | N * 4]
 };
 
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -316,15 +334,36 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
     lo = (uint32_t)__bfloat16_as_ushort(la) | ((uint32_t)__bfloat16_as_ushort(lb) << 16);
 }
 
-__global__ void __launch_bounds__(256) qjl_pack_kernel(const float* __restrict__ S, uint4* __restrict__ Sf) {
-    const int e = blockIdx.x * 256 + threadIdx.x;  // (nt * 8 + ks) * 32 + lane
-    const int lane = e & 31, ks = (e >> 5) & 7, nt = e >> 8;
-    const int i = 8 * nt + (lane >> 2), d = 16 * ks + 2 * (lane & 3);
-    const float* row = S + (size_t)i * kDim + d;
+// M = S Pi = S H diag(s) / sqrt(d): row i of M is s / sqrt(d) times the
+// Hadamard transform of row i of S (H is symmetric); M = S without rotation.
+// One CTA per n-tile (8 rows), one warp per row (4 dims per lane), then the
+// tile's 256 fragments.
+__global__ void __launch_bounds__(256) qjl_pack_kernel(const float* __restrict__ S, const int8_t* __restrict__ signs,
+                                                       int rot, uint4* __restrict__ Sf) {
+    __shared__ float s_m[8][kDim + 4];
+    const int nt = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float4 v = __ldg(reinterpret_cast<const float4*>(S + (size_t)(8 * nt + w) * kDim) + lane);
+    if (rot) {
+        float a[4] = {v.x + v.y, v.x - v.y, v.z + v.w, v.z - v.w};  // index bit 0
+        float t[4] = {a[0] + a[2], a[1] + a[3], a[0] - a[2], a[1] - a[3]};  // index bit 1
+#pragma unroll
+        for (int sft = 1; sft < 32; sft <<= 1) {  // index bits 2..6 = lane bits 0..4
+            const float sgn = (lane & sft) ? -1.f : 1.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) t[k] = fmaf(sgn, t[k], __shfl_xor_sync(kFull, t[k], sft));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] *= (float)__ldg(signs + 4 * lane + k) * kRsqrtD;
+        v = make_float4(t[0], t[1], t[2], t[3]);
+    }
+    *reinterpret_cast<float4*>(&s_m[w][4 * lane]) = v;
+    __syncthreads();
+    const int ks = threadIdx.x >> 5, gq = lane >> 2, d = 16 * ks + 2 * (lane & 3);
+    const float* row = &s_m[gq][d];
     uint4 f;
-    split_pair(__ldg(row), __ldg(row + 1), f.x, f.z);
-    split_pair(__ldg(row + 8), __ldg(row + 9), f.y, f.w);
-    Sf[e] = f;
+    split_pair(row[0], row[1], f.x, f.z);
+    split_pair(row[8], row[9], f.y, f.w);
+    Sf[(nt * 8 + ks) * 32 + lane] = f;
 }
 
 // D += A B for one m16n8k16 tile: bf16 operands, fp32 accumulators
@@ -342,157 +381,180 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
     return (x & 1u) | ((x & 2u) << 1) | ((x & 4u) << 2) | ((x & 8u) << 3);
 }
 
-template <int N, bool kBF16>
-__global__ void __launch_bounds__(N * 16, 64 / N) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp, Tables tb) {
-    constexpr int kRS = kDim / 2 + 4;  // 32-bit words per residual row (bf16 pairs; 4 words of pad)
-    __shared__ float s_cb[hsq::kCodebookFloats];
-    __shared__ float s_sign[kDim];
-    // residuals as the A operand: [L3, L1][row = token, 16 rows][bf16 pairs], hi and lo parts
-    __shared__ __align__(16) uint32_t s_rh[2][16][kRS], s_rl[2][16][kRS];
-    __shared__ long long s_dst[N][2];
-    __shared__ uint32_t s_bits[2][16][4];
+// Residual rows of the sketch pass, the A operand of M rho': [row][bf16 pairs],
+// kQRS words per row (4 words of pad: the fragment loads hit distinct banks).
+constexpr int kQRS = kDim / 2 + 4;
+constexpr int kQjlThreads = 256;  // 8 warps: warp w takes sketch rows 16 w .. 16 w + 15
 
-    const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int tk = threadIdx.x >> 4, l = hlane();  // token of this half-warp
-    const unsigned m = half_mask();
-    load_tables(s_cb, s_sign, tb, c.signs);
-    for (int i = threadIdx.x; i < 2 * 16 * 4; i += blockDim.x) (&s_bits[0][0][0])[i] = 0u;
-    if constexpr (N < 16) {  // MMA rows past the tokens: zero
-        constexpr int kPad = (16 - N) * kRS;
-        for (int i = threadIdx.x; i < 2 * kPad; i += blockDim.x) {
-            (&s_rh[i / kPad][N][0])[i % kPad] = 0u;
-            (&s_rl[i / kPad][N][0])[i % kPad] = 0u;
-        }
-    }
-    __syncthreads();
-    const float* c4 = s_cb;
-    const float* t4 = s_cb + 16;
-    float sg[8];
-    load_signs(sg, s_sign);
+// This half-warp's 8 dims of one residual into its hi / lo operand rows; returns |rho'|.
+__device__ __forceinline__ float qjl_row(const float rho[8], uint32_t* rh, uint32_t* rl, unsigned m) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
+    const int l = hlane();
+    uint2 h0, l0, h1, l1;
+    split_pair(rho[0], rho[1], h0.x, l0.x);
+    split_pair(rho[2], rho[3], h0.y, l0.y);
+    split_pair(rho[4], rho[5], h1.x, l1.x);
+    split_pair(rho[6], rho[7], h1.y, l1.y);
+    *reinterpret_cast<uint2*>(rh + 2 * l) = h0;  // dims 4 l .. 4 l + 3
+    *reinterpret_cast<uint2*>(rl + 2 * l) = l0;
+    *reinterpret_cast<uint2*>(rh + 32 + 2 * l) = h1;  // dims 64 + 4 l ..
+    *reinterpret_cast<uint2*>(rl + 32 + 2 * l) = l1;
+    return sqrtf(half_sum(ss, m));
+}
 
-    const int t = g * N + tk;
-    const bool in_ctx = t < c.T;
-    bool is_l1 = false;
-    int slot = 0;
-    if (in_ctx) {
-        const uint32_t w = __ldg(c.l1_bitmap + (size_t)b * c.W + (t >> 5));
-        is_l1 = (w >> (t & 31)) & 1u;
-        if (is_l1) slot = o.prefix[(size_t)b * c.W + (t >> 5)] + __popc(w & ((1u << (t & 31)) - 1u));
-    }
-    const bool l1_active = in_ctx && is_l1 && slot < c.max_l1;  // uniform per half-warp
-
-    float x[8];
-    if (in_ctx) {
-        const size_t off = (((size_t)b * c.Hkv + h) * c.T + t) * kDim;
-        if (kBF16) load_bf16x8(static_cast<const uint16_t*>(Kp) + off, x);
-        else load_f32x8(static_cast<const float*>(Kp) + off, x);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.f;
-    }
-    // L3: e = n (y - c4[code]) is Pi (k - k^); back to the original frame, RoPE to
-    // position t, and into the rotated frame again
-    float rho[8];
-    float n;
-    {
-        float y[8];
-        n = tq_rotate(x, y, sg, m, true);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rho[i] = n * (y[i] - c4[quant4(y[i], t4)]);
-        fwht(rho, m);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rho[i] *= sg[i] * kRsqrtD;
-        rope(rho, in_ctx ? t : 0, tb);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rho[i] *= sg[i];
-        fwht(rho, m);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rho[i] *= kRsqrtD;
-    }
-    auto put = [&](int hf, bool active, long long e) {  // residual norm, smem row, destination
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(rho[i], rho[i], ss);
-        const float gamma = sqrtf(half_sum(ss, m));
-        uint32_t* rh = s_rh[hf][tk];
-        uint32_t* rl = s_rl[hf][tk];
-        uint2 h0, l0, h1, l1;
-        split_pair(rho[0], rho[1], h0.x, l0.x);
-        split_pair(rho[2], rho[3], h0.y, l0.y);
-        split_pair(rho[4], rho[5], h1.x, l1.x);
-        split_pair(rho[6], rho[7], h1.y, l1.y);
-        *reinterpret_cast<uint2*>(rh + 2 * l) = h0;  // dims 4 l .. 4 l + 3
-        *reinterpret_cast<uint2*>(rl + 2 * l) = l0;
-        *reinterpret_cast<uint2*>(rh + 32 + 2 * l) = h1;  // dims 64 + 4 l ..
-        *reinterpret_cast<uint2*>(rl + 32 + 2 * l) = l1;
-        if (l == 0) {
-            s_dst[tk][hf] = active ? e : -1;  // destination sketch slot, -1: none
-            if (active) (hf == 0 ? o.l3_qn : o.l1_qn)[e] = gamma;
-        }
-    };
-    put(0, in_ctx, ((long long)b * c.Hkv + h) * c.G * N + t);
-    if (l1_active) {
-        // L1: the stored key is TQ4 of RoPE(k, t) with the raw key's norm n
-        rope(x, t, tb);
-        float yr[8];
-        const float nr = tq_rotate(x, yr, sg, m, true);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rho[i] = nr * yr[i] - n * c4[quant4(yr[i], t4)];
-        put(1, true, ((long long)b * c.Hkv + h) * c.max_l1 + slot);
-    } else if (l == 0) {
-        s_dst[tk][1] = -1;
-    }
-    __syncthreads();
-    // S rho on the tensor cores: D[r][i] = sum_d rho_r[d] S[i][d] for the 16-row tile
-    // of residuals (the N L3 ones, then the L1 ones when a token of the CTA is in
-    // L1), with operands split into bf16 hi + lo and the three products hi hi,
-    // hi lo, lo hi accumulated in fp32 (about 2^-16 relative per term).  Warp w
-    // takes n-tiles (sketch rows 8 nt ..) w * kNT .. ; bit i of a residual's
-    // sketch (word i / 32, bit i % 32) is set when D >= 0.
-    constexpr int kWarps = N / 2, kNT = 16 / kWarps;
+// D[r][i] = sum_d rho'_r[d] M[i][d] for kM 16-row tiles of residual rows on the
+// tensor cores, operands split into bf16 hi + lo and the three products hi hi,
+// hi lo, lo hi accumulated in fp32 (about 2^-16 relative per term); bit i of row
+// r's sketch (word i / 32, bit i % 32) is set in s_bits[r] (zero on entry) when
+// D >= 0.  Each B fragment is loaded once for the kM tiles.
+template <int kM>
+__device__ __forceinline__ void qjl_products(const uint32_t (*rh)[kQRS], const uint32_t (*rl)[kQRS],
+                                             const uint4* __restrict__ Sf, uint32_t (*s_bits)[4]) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
-        bool any = false;
-        for (int r = 0; r < N; ++r) any |= s_dst[r][hf] >= 0;
-        if (!any) continue;  // (uniform: every thread read the same slots)
-        float d[kNT][4];
+    float d[kM][2][4];
 #pragma unroll
-        for (int j = 0; j < kNT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+    for (int mt = 0; mt < kM; ++mt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) d[mt][j][0] = d[mt][j][1] = d[mt][j][2] = d[mt][j][3] = 0.f;
 #pragma unroll 2
-        for (int ks = 0; ks < 8; ++ks) {
-            const int c0 = 8 * ks + tq;  // word of dims 16 ks + 2 q, + 1
-            const uint32_t ah0 = s_rh[hf][gq][c0], ah1 = s_rh[hf][gq + 8][c0];
-            const uint32_t ah2 = s_rh[hf][gq][c0 + 4], ah3 = s_rh[hf][gq + 8][c0 + 4];
-            const uint32_t al0 = s_rl[hf][gq][c0], al1 = s_rl[hf][gq + 8][c0];
-            const uint32_t al2 = s_rl[hf][gq][c0 + 4], al3 = s_rl[hf][gq + 8][c0 + 4];
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint4 bf0 = __ldg(Sf + ((2 * warp) * 8 + ks) * 32 + lane);
+        const uint4 bf1 = __ldg(Sf + ((2 * warp + 1) * 8 + ks) * 32 + lane);
+        const int c0 = 8 * ks + tq;  // word of dims 16 ks + 2 q, + 1
 #pragma unroll
-            for (int j = 0; j < kNT; ++j) {
-                const uint4 bf = __ldg(o.Sf + ((warp * kNT + j) * 8 + ks) * 32 + lane);
-                mma_bf16_16816(d[j], al0, al1, al2, al3, bf.x, bf.y);  // lo hi
-                mma_bf16_16816(d[j], ah0, ah1, ah2, ah3, bf.z, bf.w);  // hi lo
-                mma_bf16_16816(d[j], ah0, ah1, ah2, ah3, bf.x, bf.y);  // hi hi
-            }
+        for (int mt = 0; mt < kM; ++mt) {
+            const int r0 = 16 * mt + gq;
+            const uint32_t ah0 = rh[r0][c0], ah1 = rh[r0 + 8][c0], ah2 = rh[r0][c0 + 4], ah3 = rh[r0 + 8][c0 + 4];
+            const uint32_t al0 = rl[r0][c0], al1 = rl[r0 + 8][c0], al2 = rl[r0][c0 + 4], al3 = rl[r0 + 8][c0 + 4];
+            mma_bf16_16816(d[mt][0], al0, al1, al2, al3, bf0.x, bf0.y);  // lo hi
+            mma_bf16_16816(d[mt][0], ah0, ah1, ah2, ah3, bf0.z, bf0.w);  // hi lo
+            mma_bf16_16816(d[mt][0], ah0, ah1, ah2, ah3, bf0.x, bf0.y);  // hi hi
+            mma_bf16_16816(d[mt][1], al0, al1, al2, al3, bf1.x, bf1.y);
+            mma_bf16_16816(d[mt][1], ah0, ah1, ah2, ah3, bf1.z, bf1.w);
+            mma_bf16_16816(d[mt][1], ah0, ah1, ah2, ah3, bf1.x, bf1.y);
         }
+    }
 #pragma unroll
-        for (int j = 0; j < kNT; ++j) {  // D[g][2q + c], D[g + 8][2q + c] -> bytes of rows g, g + 8
-            const int nt = warp * kNT + j;
-            const uint32_t b0 = __ballot_sync(kFull, d[j][0] >= 0.f), b1 = __ballot_sync(kFull, d[j][1] >= 0.f);
-            const uint32_t b2 = __ballot_sync(kFull, d[j][2] >= 0.f), b3 = __ballot_sync(kFull, d[j][3] >= 0.f);
+    for (int mt = 0; mt < kM; ++mt) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // D[g][2q + c], D[g + 8][2q + c] -> bytes of rows g, g + 8
+            const int nt = 2 * warp + j;
+            const uint32_t b0 = __ballot_sync(kFull, d[mt][j][0] >= 0.f), b1 = __ballot_sync(kFull, d[mt][j][1] >= 0.f);
+            const uint32_t b2 = __ballot_sync(kFull, d[mt][j][2] >= 0.f), b3 = __ballot_sync(kFull, d[mt][j][3] >= 0.f);
             if (tq == 0) {
                 const uint32_t lo = spread4((b0 >> (4 * gq)) & 15u) | (spread4((b1 >> (4 * gq)) & 15u) << 1);
                 const uint32_t hi = spread4((b2 >> (4 * gq)) & 15u) | (spread4((b3 >> (4 * gq)) & 15u) << 1);
-                atomicOr(&s_bits[hf][gq][nt >> 2], lo << (8 * (nt & 3)));
-                atomicOr(&s_bits[hf][gq + 8][nt >> 2], hi << (8 * (nt & 3)));
+                atomicOr(&s_bits[16 * mt + gq][nt >> 2], lo << (8 * (nt & 3)));
+                atomicOr(&s_bits[16 * mt + gq + 8][nt >> 2], hi << (8 * (nt & 3)));
             }
         }
     }
+}
+
+// The L3 sketches: 64 consecutive tokens of one (sequence b, KV head h) per CTA,
+// four per half-warp.  Token t's residual is rho' = RoPE(k_t - n Pi^T c^, t), c^ and n
+// its stored L3 codes' codebook values and norm.
+constexpr int kQjlTok = 64;
+
+template <int N, bool kBF16>
+__global__ void __launch_bounds__(kQjlThreads, 4) qjl_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp,
+                                                            Tables tb) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) uint32_t s_rh[kQjlTok][kQRS], s_rl[kQjlTok][kQRS];
+    __shared__ uint32_t s_bits[kQjlTok][4];
+
+    const int h = blockIdx.y, b = blockIdx.z, hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    const int t0 = blockIdx.x * kQjlTok;
+    const size_t bh = (size_t)b * c.Hkv + h;
+    load_tables(s_cb, s_sign, tb, c.signs);
+    (&s_bits[0][0])[threadIdx.x] = 0u;  // kQjlTok * 4 == kQjlThreads
     __syncthreads();
-    for (int k = threadIdx.x; k < 2 * N * 4; k += blockDim.x) {
-        const int hf = k / (N * 4), r = (k >> 2) % N, wd = k & 3;
-        const long long e = s_dst[r][hf];
-        if (e >= 0) (hf == 0 ? o.l3_qs : o.l1_qs)[e * 4 + wd] = s_bits[hf][r][wd];
+    const float* c4 = s_cb;
+    float sg[8];
+    load_signs(sg, s_sign);
+#pragma unroll 2
+    for (int i = 0; i < kQjlTok / 16; ++i) {
+        const int r = hw + 16 * i, t = t0 + r;
+        const bool valid = t < c.T;  // rows past the context: zero
+        const int tc = valid ? t : c.T - 1;
+        const int g = tc / N, k = tc - g * N;
+        const uint8_t* kr = o.kc3 + (bh * c.G + g) * (N * 68);
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(kr + k * 64 + 2 * l);
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(kr + k * 64 + 32 + 2 * l);
+        const float n = *reinterpret_cast<const float*>(kr + N * 64 + 4 * k);
+        float x[8];
+        const size_t off = (bh * c.T + tc) * kDim;
+        if (kBF16) load_bf16x8(static_cast<const uint16_t*>(Kp) + off, x);
+        else load_f32x8(static_cast<const float*>(Kp) + off, x);
+        const RopeRows rr = rope_rows(tc, tb);
+        float rho[8];  // k^ = n Pi^T c^ = diag(s) H (n / sqrt(d) c^)
+        unpack4(lo, hi, c4, n * kRsqrtD, rho);
+        fwht(rho, m);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) rho[j] = valid ? x[j] - sg[j] * rho[j] : 0.f;
+        rope_apply(rho, rr);
+        const float gamma = qjl_row(rho, s_rh[r], s_rl[r], m);
+        if (valid && l == 0) o.l3_qn[bh * c.G * N + t] = gamma;
     }
+    __syncthreads();
+    qjl_products<kQjlTok / 16>(s_rh, s_rl, o.Sf, s_bits);
+    __syncthreads();
+    const int r = threadIdx.x >> 2;
+    if (t0 + r < c.T) o.l3_qs[(bh * c.G * N + t0 + r) * 4 + (threadIdx.x & 3)] = s_bits[r][threadIdx.x & 3];
+}
+
+// The L1 sketches: 16 L1 slots of one (b, h) per CTA, one per half-warp.  Slot e
+// holds position p = l1_pos[b][e]; its residual is rho' = RoPE(k_p, p) - n Pi^T c^1,
+// c^1 its stored L1 codes' codebook values and n its stored norm.
+template <bool kBF16>
+__global__ void __launch_bounds__(kQjlThreads) qjl_l1_kernel(CacheView c, SketchOut o, const void* __restrict__ Kp,
+                                                           Tables tb) {
+    __shared__ float s_cb[hsq::kCodebookFloats];
+    __shared__ float s_sign[kDim];
+    __shared__ __align__(16) uint32_t s_rh[16][kQRS], s_rl[16][kQRS];
+    __shared__ uint32_t s_bits[16][4];
+
+    const int h = blockIdx.y, b = blockIdx.z, hw = threadIdx.x >> 4, l = hlane();
+    const unsigned m = half_mask();
+    const int cnt = min(c.l1_count[b], c.max_l1);
+    const int e0 = blockIdx.x * 16;
+    if (e0 >= cnt) return;  // (uniform over the CTA, before any barrier)
+    const size_t bh = (size_t)b * c.Hkv + h;
+    load_tables(s_cb, s_sign, tb, c.signs);
+    if (threadIdx.x < 64) (&s_bits[0][0])[threadIdx.x] = 0u;
+    __syncthreads();
+    const float* c4 = s_cb;
+    float sg[8];
+    load_signs(sg, s_sign);
+    const int e = e0 + hw;
+    const bool valid = e < cnt;
+    const int ec = valid ? e : cnt - 1;
+    const int p = c.l1_pos[(size_t)b * c.max_l1 + ec];
+    const size_t so = bh * c.max_l1 + ec;
+    const uint32_t lo = *reinterpret_cast<const uint16_t*>(c.l1_kc + so * 64 + 2 * l);
+    const uint32_t hi = *reinterpret_cast<const uint16_t*>(c.l1_kc + so * 64 + 32 + 2 * l);
+    const float n = c.l1_kn[so];
+    float x[8];
+    const size_t off = (bh * c.T + p) * kDim;
+    if (kBF16) load_bf16x8(static_cast<const uint16_t*>(Kp) + off, x);
+    else load_f32x8(static_cast<const float*>(Kp) + off, x);
+    rope(x, p, tb);
+    float rho[8];
+    unpack4(lo, hi, c4, n * kRsqrtD, rho);
+    fwht(rho, m);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rho[j] = valid ? x[j] - sg[j] * rho[j] : 0.f;
+    const float gamma = qjl_row(rho, s_rh[hw], s_rl[hw], m);
+    if (valid && l == 0) o.l1_qn[bh * c.max_l1 + e] = gamma;
+    __syncthreads();
+    qjl_products<1>(s_rh, s_rl, o.Sf, s_bits);
+    __syncthreads();
+    if (threadIdx.x < 64 && e0 + (threadIdx.x >> 2) < cnt)
+        o.l1_qs[(bh * c.max_l1 + e0 + (threadIdx.x >> 2)) * 4 + (threadIdx.x & 3)] = s_bits[threadIdx.x >> 2][threadIdx.x & 3];
 }
 
 // ---------------------------------------------------------------------------
@@ -987,8 +1049,8 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
     EncodeOut o{cache->l1_kc, cache->l1_vc, cache->l1_kn, cache->l1_vn, cache->l2_kc, cache->l2_vc,
                 cache->l2_kn, cache->l2_vn, cache->l2_cnt, cache->l3, ctx->d_prefix,
                 grow ? cache->win_kv : nullptr, grow ? cache->gsum : nullptr, ctx->cfg.l1_recent,
-                pf ? pf->kh : nullptr, pf ? pf->kl : nullptr, pf ? pf->vt : nullptr, pf ? pf->nkt : 0};
-    dim3 grid(v.G, v.Hkv, v.B);
+                pf ? pf->kh : nullptr, pf ? pf->kl : nullptr, pf ? pf->vt : nullptr, pf ? pf->nkt : 0,
+                ctx->cfg.qjl ? ctx->d_qjl_kc : nullptr};
     const Tables tb = make_tables(ctx);
     using EncodeFn = void (*)(CacheView, EncodeOut, const void*, const void*, Tables);
     const bool bf = dtype == HSQ_DTYPE_BF16;
@@ -1008,15 +1070,18 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
     fn<<<dim3((v.G + kEncGroups - 1) / kEncGroups, v.Hkv, v.B), v.N * 32, dyn, s>>>(v, o, K, V, tb);
     if (ctx->cfg.qjl) {  // TQ-QKV: the key-residual sketches (after the L1 slot prefix is known)
         uint4* sf = reinterpret_cast<uint4*>(ctx->d_qjl_sb);
-        qjl_pack_kernel<<<16 * 8 * 32 / 256, 256, 0, s>>>(cache->qjl_s, sf);
-        const SketchOut so{sf, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_prefix};
+        qjl_pack_kernel<<<16, 256, 0, s>>>(cache->qjl_s, cache->signs, v.rot, sf);
+        const SketchOut so{sf, cache->l1_qs, cache->l1_qn, cache->l3_qs, cache->l3_qn, ctx->d_qjl_kc};
+        const dim3 g3((v.T + kQjlTok - 1) / kQjlTok, v.Hkv, v.B), g1((v.max_l1 + 15) / 16, v.Hkv, v.B);
         if (v.N == 16) {
-            if (bf) qjl_kernel<16, true><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<16, false><<<grid, 16 * 16, 0, s>>>(v, so, K, tb);
+            if (bf) qjl_kernel<16, true><<<g3, kQjlThreads, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<16, false><<<g3, kQjlThreads, 0, s>>>(v, so, K, tb);
         } else {
-            if (bf) qjl_kernel<8, true><<<grid, 8 * 16, 0, s>>>(v, so, K, tb);
-            else qjl_kernel<8, false><<<grid, 8 * 16, 0, s>>>(v, so, K, tb);
+            if (bf) qjl_kernel<8, true><<<g3, kQjlThreads, 0, s>>>(v, so, K, tb);
+            else qjl_kernel<8, false><<<g3, kQjlThreads, 0, s>>>(v, so, K, tb);
         }
+        if (bf) qjl_l1_kernel<true><<<g1, kQjlThreads, 0, s>>>(v, so, K, tb);
+        else qjl_l1_kernel<false><<<g1, kQjlThreads, 0, s>>>(v, so, K, tb);
     }
     return after_launch(ctx, "encode");
 }
@@ -1024,6 +1089,7 @@ hsq_status encode_run(hsq_ctx* ctx, const hsq_cache* cache, const void* K, const
 void free_ctx(hsq_ctx* c) {
     cudaFree(c->d_cb); cudaFree(c->d_rope_hi); cudaFree(c->d_rope_lo); cudaFree(c->d_scores);
     cudaFree(c->d_route_ctr); cudaFree(c->d_prefix); cudaFree(c->d_err); cudaFree(c->d_qjl_sb);
+    cudaFree(c->d_qjl_kc);
     delete c;
 }
 
@@ -1076,6 +1142,9 @@ hsq_status hsq_create(const hsq_config* cfg, hsq_ctx** out) {
     if ((e = cudaMalloc(&c->d_err, 4)) != cudaSuccess) return bail(e, "cudaMalloc(err)");
     if (cfg->qjl && (e = cudaMalloc(&c->d_qjl_sb, hsq::kDim * hsq::kDim * 4)) != cudaSuccess)
         return bail(e, "cudaMalloc(sketch matrix)");
+    if (cfg->qjl && (e = cudaMalloc(&c->d_qjl_kc, (size_t)cfg->max_batch * cfg->n_kv_heads * c->G_max *
+                                                      cfg->group_n * 68)) != cudaSuccess)
+        return bail(e, "cudaMalloc(key codes)");
     if ((e = cudaMemcpy(c->d_cb, cb, sizeof(cb), cudaMemcpyHostToDevice)) != cudaSuccess) return bail(e, "upload");
     if ((e = cudaMemcpy(c->d_rope_hi, hi.data(), hi.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess)
         return bail(e, "upload");
