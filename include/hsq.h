@@ -266,7 +266,10 @@ hsq_status hsq_cache_sizes(const hsq_config* cfg, int B, int T, size_t bytes[HSQ
  * hsq_create -- validate cfg, build both codebooks (float64, rounded to
  *   float32 for the device) and the RoPE angle tables (float64 angles,
  *   float32 cos/sin of 256*a*omega and c*omega, combined on the device by
- *   angle addition), allocate scratch on the current device.
+ *   angle addition), allocate scratch on the current device (with cfg.qjl
+ *   also 64 KB for S Pi and max_batch * n_kv_heads * ceil(max_ctx / group_n)
+ *   * group_n * 68 bytes for a copy of the last encode's L3 key codes and
+ *   norms, read by the sketch pass).
  *   *out receives the context.  Errors: HSQ_ERR_INVALID, HSQ_ERR_NOMEM,
  *   HSQ_ERR_CUDA, HSQ_ERR_UNSUPPORTED.
  */
