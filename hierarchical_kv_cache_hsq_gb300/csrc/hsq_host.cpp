@@ -201,6 +201,7 @@ std::string check_cache_shape(const hsq_config* cfg, const hsq_cache* c) {
         return "an L1 buffer is NULL";
     if (!c->l2_kc || !c->l2_vc || !c->l2_kn || !c->l2_vn || !c->l2_cnt) return "an L2 buffer is NULL";
     if (!c->l3) return "l3 is NULL";
+    if ((uintptr_t)c->l3 & 15u) return "l3 must be 16-byte aligned";
     if (!c->l1_bitmap) return "l1_bitmap is NULL";
     if (!c->signs && cfg->codec != HSQ_CODEC_PLAIN) return "signs is NULL";
     if (cfg->qjl && (!c->qjl_s || !c->l1_qs || !c->l1_qn || !c->l3_qs || !c->l3_qn))

@@ -181,7 +181,8 @@ typedef struct hsq_config {
  * in the order of enum hsq_buffer.  All device buffers are plain device
  * memory; l3 is either device memory or page-locked host memory mapped into
  * the device address space (cudaHostAlloc / torch pin_memory), read by the
- * GPU in place (zero copy).
+ * GPU in place (zero copy); l3 must be 16-byte aligned (HSQ_ERR_INVALID
+ * otherwise: records are read in 16-byte chunks).
  */
 typedef struct hsq_cache {
     int B;                    /* sequences in this cache, 1..max_batch */
