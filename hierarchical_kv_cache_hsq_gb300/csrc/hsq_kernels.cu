@@ -366,6 +366,14 @@ __global__ void __launch_bounds__(256) qjl_pack_kernel(const float* __restrict__
     Sf[(nt * 8 + ks) * 32 + lane] = f;
 }
 
+// Four 8 x 8 b16 matrices from shared memory (ldmatrix.x4): lanes 8 j .. 8 j + 7
+// give the row addresses of matrix j; register j holds this lane's pair of it.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
 // D += A B for one m16n8k16 tile: bf16 operands, fp32 accumulators
 __device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -418,16 +426,22 @@ __device__ __forceinline__ void qjl_products(const uint32_t (*rh)[kQRS], const u
     for (int mt = 0; mt < kM; ++mt)
 #pragma unroll
         for (int j = 0; j < 2; ++j) d[mt][j][0] = d[mt][j][1] = d[mt][j][2] = d[mt][j][3] = 0.f;
+    // ldmatrix.x4 row addresses: lane L gives row (L & 7) + 8 ((L >> 3) & 1) of the
+    // tile and the 8-dim half (L >> 4) of the k-step: matrices 0..3 are the A
+    // fragment's a0..a3 (rows 0-7 / 8-15, dims 0-7 / 8-15 of the 16 x 16 block)
+    const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1), lcol = 4 * (lane >> 4);
+    const uint32_t rh0 = (uint32_t)__cvta_generic_to_shared(&rh[lrow][lcol]);
+    const uint32_t rl0 = (uint32_t)__cvta_generic_to_shared(&rl[lrow][lcol]);
 #pragma unroll 2
     for (int ks = 0; ks < 8; ++ks) {
         const uint4 bf0 = __ldg(Sf + ((2 * warp) * 8 + ks) * 32 + lane);
         const uint4 bf1 = __ldg(Sf + ((2 * warp + 1) * 8 + ks) * 32 + lane);
-        const int c0 = 8 * ks + tq;  // word of dims 16 ks + 2 q, + 1
 #pragma unroll
         for (int mt = 0; mt < kM; ++mt) {
-            const int r0 = 16 * mt + gq;
-            const uint32_t ah0 = rh[r0][c0], ah1 = rh[r0 + 8][c0], ah2 = rh[r0][c0 + 4], ah3 = rh[r0 + 8][c0 + 4];
-            const uint32_t al0 = rl[r0][c0], al1 = rl[r0 + 8][c0], al2 = rl[r0][c0 + 4], al3 = rl[r0 + 8][c0 + 4];
+            const uint32_t off = (uint32_t)((16 * mt * kQRS + 8 * ks) * 4);
+            uint32_t ah0, ah1, ah2, ah3, al0, al1, al2, al3;
+            ldmatrix_x4(rh0 + off, ah0, ah1, ah2, ah3);
+            ldmatrix_x4(rl0 + off, al0, al1, al2, al3);
             mma_bf16_16816(d[mt][0], al0, al1, al2, al3, bf0.x, bf0.y);  // lo hi
             mma_bf16_16816(d[mt][0], ah0, ah1, ah2, ah3, bf0.z, bf0.w);  // hi lo
             mma_bf16_16816(d[mt][0], ah0, ah1, ah2, ah3, bf0.x, bf0.y);  // hi hi
