@@ -361,8 +361,13 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     // 0. the few values read straight into registers, issued before anything
     //    waits on them: position, this half-warp's query head, signs, counts
     const int pos_raw = __ldcg(a.pos + b);  // (q, pos, sel, out may be host-mapped)
-    float qx[8];
-    load_f32x8_cg(a.q + ((size_t)b * c.Hq + h * R + min(hw, R - 1)) * kDim, qx);
+    float qx[8];  // (only the R half-warps of the heads read; the rest compute on zeros)
+    if (hw < R) {
+        load_f32x8_cg(a.q + ((size_t)b * c.Hq + h * R + hw) * kDim, qx);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qx[i] = 0.f;
+    }
     float sg[8];
     if constexpr (kRot) {
         load_signs_global(sg, c.signs);

@@ -851,8 +851,13 @@ template <int R>
 __device__ __forceinline__ void prepare_queries(const float* __restrict__ q, int pos, const float sg[8],
                                                 const Tables& tb, float (*s_qt)[kDim], float (*s_qr)[kDim],
                                                 bool rot) {
-    float x[8];
-    load_f32x8_cg(q + (size_t)min((int)threadIdx.x >> 4, R - 1) * kDim, x);
+    float x[8];  // (only the R half-warps of the heads read; the rest compute on zeros)
+    if ((int)threadIdx.x >> 4 < R) {
+        load_f32x8_cg(q + (size_t)(threadIdx.x >> 4) * kDim, x);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = 0.f;
+    }
     prepare_queries<R>(x, pos, sg, tb, s_qt, s_qr, rot);
 }
 
