@@ -185,3 +185,19 @@ def test_overlap_launch_flag_is_checked(H):
     cfg.overlap_launch = 2
     with pytest.raises(H.HSQError):
         H.hsq_cache_sizes(cfg, 2, 4096)
+
+
+def test_unaligned_l3_rejected_before_any_cuda_call(H):
+    # every pointer non-NULL (never dereferenced: validation fails first), l3 off a 16-byte boundary
+    cfg = H.make_config(32, 8, 16, 64, 1, 4096, 100, 5000)
+    c = H._binding.hsq_cache()
+    c.B, c.T = 1, 4096
+    fake = 1 << 20
+    for name, _ in H._binding.hsq_cache._fields_:
+        if name not in ("B", "T", "l3_on_host", "t_cap"):
+            setattr(c, name, fake)
+    c.l3 = fake + 8
+    lib = H.load_library()
+    buf = np.zeros(64, dtype=np.int32)
+    assert lib.hsq_route_noalloc(ctypes.byref(cfg), ctypes.byref(c), fake, fake, buf.ctypes.data, None) == 1
+    assert b"16-byte aligned" in lib.hsq_last_error(None)
