@@ -425,3 +425,72 @@ def test_pageable_host_buffer_is_refused():
         H.hsq_decode_step(L.ctx, L.cache, qh, pd, sel, out)
     assert ei.value.status == B.HSQ_ERR_INVALID
     assert H.hsq_sync_status(L.ctx) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=16384, N=16, B=1, Hq=8, Hkv=2),   # G = 1024: the top half of the groups
+    dict(T=5000, N=8, B=2, Hq=10, Hkv=2),    # G = 625, ragged, r = 5
+])
+def test_maximum_beta(kw):
+    """beta = HSQ_MAX_BETA (512): the fused step selects what the routing call
+    selects, that selection equals the oracle's up to near-ties of its
+    beta-th score, and the attention over 512 fetched groups is within 1e-3
+    of the oracle's on the GPU's cache and selection."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = WL["tiny_1k"].with_(name="beta_max", beta=512, recent=64, marked=40, storage="bf16", seed_tag=61, **kw)
+    li = W.layer_inputs(w)
+    ctx = make_ctx(w)
+    cache = gpu_encode(ctx, w, li)
+    g = oracle_view(abi_buffers(cache), li, w)
+    q, pos = W.queries(w, steps=2)
+    for s in range(2):
+        qd, pd = torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos[s]).cuda()
+        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        out = torch.empty((w.B, w.Hq, 128), device="cuda")
+        H.hsq_decode_step(ctx, cache, qd, pd, sel, out)
+        sel_r = torch.empty_like(sel)
+        H.hsq_route(ctx, cache, qd, pd, sel_r)
+        assert H.hsq_sync_status(ctx) == 0
+        assert torch.equal(sel, sel_r)
+        gsel = sel.cpu().numpy().astype(np.int64)
+        osel, oscores = O.route(g, q[s], pos[s], w.beta)
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                assert (gsel[b, h] >= 0).sum() == min(w.beta, int((g.l2_cnt[b] > 0).sum()))
+                bad, _ = sel_mismatch(gsel[b, h], osel[b, h], oscores[b, h], w.beta)
+                assert bad == 0, f"step {s} (b={b}, h={h}): {bad} selection differences outside the band"
+        ref = O.decode_attn(g, q[s], pos[s], gsel)
+        err = rel_l2(out.cpu().numpy(), ref)
+        assert np.all(err <= 1e-3), f"step {s}: max rel L2 {err.max():.3e}"
+    ctx.close()
+
+
+def test_query_positions_up_to_max_pos():
+    """max_pos = 2^24, the largest the configuration allows: the query's RoPE
+    at positions near it (angle tables of 65536 + 256 rows combined by angle
+    addition) routes and attends like the float64 oracle."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = WL["tiny_1k"].with_(name="far_positions", seed_tag=62)
+    li = W.layer_inputs(w)
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, max(w.l1_size, 1), 1 << 24, w.theta)
+    ctx = H.Context(cfg)
+    cache = gpu_encode(ctx, w, li)
+    g = oracle_view(abi_buffers(cache), li, w)
+    q, _ = W.queries(w, steps=3)
+    for s, p in enumerate(((1 << 24) - 1, (1 << 23) + 12345, 65536 * 255 + 17)):
+        pos = np.full((w.B,), p, dtype=np.int32)
+        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        out = torch.empty((w.B, w.Hq, 128), device="cuda")
+        H.hsq_decode_step(ctx, cache, torch.from_numpy(q[s]).cuda(), torch.from_numpy(pos).cuda(), sel, out)
+        assert H.hsq_sync_status(ctx) == 0
+        gsel = sel.cpu().numpy().astype(np.int64)
+        osel, oscores = O.route(g, q[s], pos, w.beta)
+        for b in range(w.B):
+            for h in range(w.Hkv):
+                bad, _ = sel_mismatch(gsel[b, h], osel[b, h], oscores[b, h], w.beta)
+                assert bad == 0, f"position {p} (b={b}, h={h})"
+        err = rel_l2(out.cpu().numpy(), O.decode_attn(g, q[s], pos, gsel))
+        assert np.all(err <= 1e-3), f"position {p}: max rel L2 {err.max():.3e}"
+    ctx.close()
