@@ -380,6 +380,45 @@ def run_reference(args, rank, world):
 GROW_STEPS = 64
 
 
+def measure_dense_context(torch, w, li, q, pos, flush, clean, sink, steps=200, warmup=10):
+    """Context, not part of the library: one decode step of dense attention over
+    this layer's uncompressed cache (post-RoPE keys and values in bf16 device
+    memory), torch's scaled_dot_product_attention with each KV head's r query
+    heads as r query rows (the GQA decode), L2 flushed before every step as for
+    the HSQ step.  The pages state HSQ's decode throughput as a percentage of
+    such an uncompressed baseline."""
+    import torch.nn.functional as F
+    r = w.Hq // w.Hkv
+    Kr = torch.empty((w.B, w.Hkv, w.T, 128), dtype=torch.bfloat16, device="cuda")
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            kr = input_rope(li.K[b, h], np.arange(w.T), w.theta).astype(np.float32)
+            Kr[b, h].copy_(torch.from_numpy(kr).to(torch.bfloat16))
+    V = torch.from_numpy(np.ascontiguousarray(li.V, np.float32)).cuda().to(torch.bfloat16)
+    qs = [torch.from_numpy(input_rope(q[s], pos[s][:, None], w.theta).astype(np.float32)).cuda()
+          .to(torch.bfloat16).reshape(w.B, w.Hkv, r, 128) for s in range(q.shape[0])]
+    ts = []
+    for i in range(warmup + steps):
+        flush.fill_(i & 255)
+        torch.sum(clean, dim=0, out=sink)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        F.scaled_dot_product_attention(qs[i % len(qs)], Kr, V)
+        b.record()
+        b.synchronize()
+        if i >= warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    nbytes = 2 * w.B * w.Hkv * w.T * 128 * 2
+    us = statistics.median(ts)
+    del Kr, V
+    return {"us_per_step_median": us, "us_per_step_mean": sum(ts) / len(ts), "steps_per_s": 1e6 / us,
+            "kv_bytes": nbytes, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+            "how": "torch scaled_dot_product_attention (bf16, non-causal) of the r query heads of each KV head "
+                   "as r query rows against that head's 32K post-RoPE keys and values (uncompressed, device "
+                   "memory); L2 flushed and refilled clean before every step; CUDA events, median of "
+                   f"{steps} steps; a library kernel, timed for context only"}
+
+
 def measure_growth(H, torch, w, li, flush, clean, sink):
     """Decode with cache growth on the same layer: a growable copy of the cache
     (recent window and sinks of the workload, capacity T + GROW_STEPS), then
@@ -872,6 +911,7 @@ def run_hsq(args, rank, world, local):
         H, torch, lp, flush, clean, sink, min(args.steps, 200), max(args.warmup, 3),
         0.0 if args.no_cpu_baseline else 3.0)
     codecs = None if args.quick else measure_codecs(H, torch, w, li)
+    dense = None if args.quick else measure_dense_context(torch, w, li, q, pos, flush, clean, sink)
 
     ms_per_step, value = aggregate(sum(res["step_ms"]), args.steps, world, device="cuda")
     hot = None if args.quick or args.codec != "tq" or args.qjl else measure_hot_table(
@@ -953,6 +993,8 @@ def run_hsq(args, rank, world, local):
         "small_workloads": small,
         "codec": codecs,
         "hot_table": hot,
+        "dense_attention_context": None if dense is None else dict(
+            dense, hsq_steps_per_s=value, hsq_over_dense=value / dense["steps_per_s"]),
         "gpu_launches": args.steps,
         "tokens_per_s": value * w.B,
         "needle_routed_step0": needle_ok,
