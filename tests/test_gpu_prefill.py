@@ -132,3 +132,37 @@ def test_prefill_full_size_8b_32k_sampled_rows():
             assert err.max() <= 1e-3, f"KV head {h}, rows from {start}: rel L2 {err.max():.3e}"
     print(f"[prefill 8B/32K] worst sampled rel L2 {worst:.2e}")
     ctx.close()
+
+
+def test_prefill_with_tq_qkv_cache_sketches_like_hsq_encode():
+    """With cfg.qjl the fused prefill also writes the key-residual sketches, and
+    they equal hsq_encode's bit for bit (the same codes, the same sketch pass)."""
+    import torch
+    import hierarchical_kv_cache_hsq_gb300 as H
+    w = W.get_workload("tiny_1k").with_(name="ragged_pf_qjl", T=1000, N=8, Hq=8, Hkv=2, storage="bf16",
+                                        seed_tag=22)
+    li = W.layer_inputs(w)
+    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T, max(w.l1_size, 1), w.T + w.steps + 1, w.theta,
+                        qjl=True)
+    ctx = H.Context(cfg)
+    S = W.qjl_matrix(w)
+    Q = _bf16(np.random.default_rng(6).standard_normal((w.B, w.Hq, w.T, 128)))
+    got = []
+    for fused in (True, False):
+        cache = H.allocate_cache(ctx, w.B, w.T, l3_on_host=True)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        H.set_qjl_matrix(cache, S)
+        if fused:
+            _run(ctx, w.B, w.T, Q, li.K, li.V, cache=cache)
+        else:
+            H.hsq_encode(ctx, cache, torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous(),
+                         torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous())
+            torch.cuda.synchronize()
+        bufs = abi_buffers(cache)
+        for n in ("l1_qs", "l1_qn", "l3_qs", "l3_qn"):
+            bufs[n] = cache.view(n).cpu().numpy()
+        got.append(bufs)
+    assert H.hsq_sync_status(ctx) == 0
+    for k in got[0]:
+        np.testing.assert_array_equal(got[0][k], got[1][k], err_msg=k)
+    ctx.close()
