@@ -424,44 +424,61 @@ def measure_growth(H, torch, w, li, flush, clean, sink):
     (recent window and sinks of the workload, capacity T + GROW_STEPS), then
     per step hsq_append of the new token's K/V (seeded N(0,1) draws) followed
     by the decode step of that token (query at the new position); L2 flushed
-    before every step, outside the events."""
+    before every step, outside the events.  Run twice: in ordinary stream
+    order, and with hsq_config.overlap_launch (the decode step's launch
+    overlapping the append).  The pair is timed without an event between the
+    two calls; in stream order every other step records one there, to time the
+    append alone."""
     n = GROW_STEPS
-    cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T + n, w.l1_size, w.T + n + 1, w.theta, 0,
-                        sinks=w.sinks, recent=w.recent)
-    gctx = H.Context(cfg)
-    cache = H.allocate_cache(gctx, w.B, w.T, l3_on_host=True, with_staging=False, t_cap=w.T + n)
-    H.set_layer_inputs(cache, li.l1_mask, li.signs)
-    K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
-    V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
-    H.hsq_encode(gctx, cache, K, V)
-    del K, V
-    rng = np.random.default_rng(12345)
-    kv = torch.from_numpy(rng.standard_normal((n, 2, w.B, w.Hkv, 128)).astype(np.float32)).cuda().to(torch.bfloat16)
-    q = torch.from_numpy(rng.standard_normal((n, w.B, w.Hq, 128)).astype(np.float32)).cuda()
-    pos = torch.arange(w.T, w.T + n, dtype=torch.int32, device="cuda").view(n, 1).expand(n, w.B).contiguous()
-    sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
-    out = torch.empty((w.B, w.Hq, 128), device="cuda")
-    t_app, t_step = [], []
-    for i in range(n):
-        flush.fill_(i & 255)
-        torch.sum(clean, dim=0, out=sink)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record()
-        H.hsq_append(gctx, cache, kv[i, 0], kv[i, 1])
-        e[1].record()
-        H.hsq_decode_step(gctx, cache, q[i], pos[i], sel, out)
-        e[2].record()
-        e[2].synchronize()
-        if i >= 4:
-            t_app.append(e[0].elapsed_time(e[1]) * 1e3)
-            t_step.append(e[0].elapsed_time(e[2]) * 1e3)
-    assert H.hsq_sync_status(gctx) == 0 and cache.T == w.T + n
-    gctx.close()
+    res = {}
+    for overlap in (False, True):
+        cfg = H.make_config(w.Hq, w.Hkv, w.N, w.beta, w.B, w.T + n, w.l1_size, w.T + n + 1, w.theta, 0,
+                            sinks=w.sinks, recent=w.recent, overlap_launch=overlap)
+        gctx = H.Context(cfg)
+        cache = H.allocate_cache(gctx, w.B, w.T, l3_on_host=True, with_staging=False, t_cap=w.T + n)
+        H.set_layer_inputs(cache, li.l1_mask, li.signs)
+        K = torch.from_numpy(li.K).cuda().to(torch.bfloat16).contiguous()
+        V = torch.from_numpy(li.V).cuda().to(torch.bfloat16).contiguous()
+        H.hsq_encode(gctx, cache, K, V)
+        del K, V
+        rng = np.random.default_rng(12345)
+        kv = torch.from_numpy(rng.standard_normal((n, 2, w.B, w.Hkv, 128)).astype(np.float32)).cuda().to(
+            torch.bfloat16)
+        q = torch.from_numpy(rng.standard_normal((n, w.B, w.Hq, 128)).astype(np.float32)).cuda()
+        pos = torch.arange(w.T, w.T + n, dtype=torch.int32, device="cuda").view(n, 1).expand(n, w.B).contiguous()
+        sel = torch.empty((w.B, w.Hkv, w.beta), dtype=torch.int32, device="cuda")
+        out = torch.empty((w.B, w.Hq, 128), device="cuda")
+        t_app, t_step = [], []
+        for i in range(n):
+            flush.fill_(i & 255)
+            torch.sum(clean, dim=0, out=sink)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            split = not overlap and i % 2 == 1  # (this step times the append alone)
+            e[0].record()
+            H.hsq_append(gctx, cache, kv[i, 0], kv[i, 1])
+            if split:
+                e[1].record()
+            H.hsq_decode_step(gctx, cache, q[i], pos[i], sel, out)
+            e[2].record()
+            e[2].synchronize()
+            if i >= 4:
+                if split:
+                    t_app.append(e[0].elapsed_time(e[1]) * 1e3)
+                else:
+                    t_step.append(e[0].elapsed_time(e[2]) * 1e3)
+        assert H.hsq_sync_status(gctx) == 0 and cache.T == w.T + n
+        gctx.close()
+        res[overlap] = (t_app, t_step)
     med = statistics.median
-    return {"append_us": med(t_app), "append_plus_step_us": med(t_step),
-            "steps_per_s_with_append": 1e6 / med(t_step), "steps": n - 4,
+    return {"append_us": med(res[False][0]), "append_plus_step_us": med(res[False][1]),
+            "steps_per_s_with_append": 1e6 / med(res[False][1]),
+            "append_plus_step_overlapped_us": med(res[True][1]),
+            "steps_per_s_with_append_overlapped": 1e6 / med(res[True][1]), "steps": n - 4,
+            "overlap": "hsq_config.overlap_launch: the decode kernel is launched with programmatic stream "
+                       "serialization, so its launch overlaps the append kernel (which it then waits for)",
             "how": f"hsq_append (one kernel) then hsq_decode_step per token, {n} tokens appended to the "
-                   f"{w.T}-token layer (capacity {w.T + n}), recent window {w.recent}, L2 flushed per step"}
+                   f"{w.T}-token layer (capacity {w.T + n}), recent window {w.recent}, L2 flushed per step; "
+                   f"'overlapped': the same with hsq_config.overlap_launch"}
 
 
 HOT_SLOTS = 256
