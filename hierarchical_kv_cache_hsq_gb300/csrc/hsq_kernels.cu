@@ -573,14 +573,18 @@ __global__ void __launch_bounds__(kQjlThreads) qjl_l1_kernel(CacheView c, Sketch
 
 // ---------------------------------------------------------------------------
 // Decode-time growth: append one token per sequence at position T.  One CTA
-// per sequence b, one warp per KV head.  Warp 0 first finds the L1 slot of the
-// new token -- the slot of the token p = T - recent that leaves the window,
-// or a new slot when nothing leaves -- and updates the sequence's L1 list,
-// count and bitmap (no other CTA touches them).  Then warp h (half 0 the key,
-// half 1 the value) writes the new token's L3 record slot and L1 entry, and,
-// when p leaves, adds p's input (from the window ring) to the running sums
-// of its group in position order and re-quantises the group's summary, as the
-// encode of the longer context computes it.
+// per sequence b: warp h < Hkv for KV head h (half 0 the key, half 1 the
+// value), and one more warp (warp 0 when there are 32 KV heads) for the
+// sequence's L1 bookkeeping: the L1 slot of the new token -- the slot of the
+// token p = T - recent that leaves the window, or a new slot when nothing
+// leaves -- and the sequence's L1 list, count and bitmap (no other CTA touches
+// them).  While that warp searches, the head warps write the new token's L3
+// record slot and, when p leaves (p >= sinks), add p's input (from the window
+// ring) to the running sums of its group in position order and re-quantise
+// the group's summary, as the encode of the longer context computes it; once
+// the slot is known they write the L1 entry.  (A p >= sinks that is not in L1
+// cannot happen in a cache built by hsq_encode and hsq_append; the search
+// flags it, HSQ_DEVERR_GROW.)
 // ---------------------------------------------------------------------------
 
 template <int N, bool kBF16>
@@ -592,10 +596,14 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
     __shared__ float s_sign[kDim];
     __shared__ uint32_t s_l2[32][2][12];
     __shared__ int s_slot;
-    const int b = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int keeper = c.Hkv < 32 ? c.Hkv : 0;  // the bookkeeping warp
+    const bool head = warp < c.Hkv;
+    const int h = head ? warp : 0;
     const int half = (threadIdx.x >> 4) & 1, l = hlane();
     const unsigned m = half_mask();
     const int t = c.T, p = t - recent;
+    const bool leaves = p >= 0 && p >= sinks;  // p leaves the window (a sink stays)
     const size_t bh = (size_t)b * c.Hkv + h;
     // loads that depend on nothing, issued first
     float x[8];
@@ -613,11 +621,11 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
     load_tables(s_cb, s_sign, tb, c.signs);
     if (threadIdx.x < 24 * c.Hkv) (&s_l2[0][0][0])[threadIdx.x] = 0u;
 
-    if (h == 0) {  // the slot, and the sequence's L1 bookkeeping
+    auto bookkeeping = [&]() {  // the slot, and the sequence's L1 bookkeeping
         int32_t* pos = l1_pos + (size_t)b * c.max_l1;
         const int cnt = min(__ldcg(l1_count + b), c.max_l1);
-        int slot = -1, leaves = 0;
-        if (p >= 0 && p >= sinks) {
+        int slot = -1, found_p = 0;
+        if (leaves) {
             // the window fills the last `recent` slots, rotated: the token at
             // position x0 + j (x0 its first position at encode) is in slot
             // cnt - recent + j mod recent -- checked, else every slot is scanned
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
             }
             if (found >= 0) {
                 slot = found;
-                leaves = 1;
+                found_p = 1;
             } else if (lane == 0) {
                 atomicOr(err, HSQ_DEVERR_GROW);
             }
@@ -649,37 +657,64 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
                 pos[slot] = t;
                 atomicOr(bm + (t >> 5), 1u << (t & 31));
             }
-            if (leaves) atomicAnd(bm + (p >> 5), ~(1u << (p & 31)));
-            s_slot = slot >= 0 ? (slot | (leaves << 30)) : -1;
+            if (found_p) atomicAnd(bm + (p >> 5), ~(1u << (p & 31)));
+            s_slot = slot;
         }
-    }
-    __syncthreads();
+    };
+    __syncthreads();  // the tables are in shared memory
+    // (a warp of its own runs beside the heads; with 32 KV heads warp 0 does both)
+    if (warp == keeper) bookkeeping();
     const float* t4 = s_cb + 16;
     const float* t3 = s_cb + 40;
     float sg[8];
     load_signs(sg, s_sign);
-    const int sc = s_slot;
-    const int slot = sc < 0 ? -1 : (sc & 0x3FFFFFFF);
-    const bool leaves = sc >= 0 && ((sc >> 30) & 1);
 
-    // L3 record slot t: TQ4 of the raw key / value
-    float y[8];
-    const float n = tq_rotate(x, y, sg, m, c.rot);
-    uint16_t lo, hi;
-    pack4(y, t4, lo, hi);
-    {
+    float n = 0.f;
+    uint16_t lo = 0, hi = 0;
+    if (head) {
+        // L3 record slot t: TQ4 of the raw key / value
+        float y[8];
+        n = tq_rotate(x, y, sg, m, c.rot);
+        pack4(y, t4, lo, hi);
         uint8_t* rec = o.l3 + (bh * c.G + t / N) * (N * 136);
         uint8_t* row = rec + (half ? N * 64 : 0) + (t % N) * 64;
         reinterpret_cast<uint16_t*>(row)[l] = lo;
         reinterpret_cast<uint16_t*>(row + 32)[l] = hi;
         if (l == 0) reinterpret_cast<float*>(rec + N * 128)[half * N + t % N] = n;
+        if (c.hot_tag && lane == 0) {  // the hot-group table's copy of group t / N is stale
+            int32_t* tag = c.hot_tag + bh * (c.hot_mask + 1) + ((t / N) & c.hot_mask);
+            if (*tag == t / N) *tag = -1;
+        }
+        if (leaves) {
+            if (half == 0) rope_apply(xp, rope_p);
+            float* gs = o.gsum + bh * hsq::kGsumFloats;
+            const bool fresh = p % N == 0;  // p opens its group: nothing summed before it
+            float acc[8];
+            const float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_a;
+            const float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_b;
+            acc[0] = a.x + xp[0]; acc[1] = a.y + xp[1]; acc[2] = a.z + xp[2]; acc[3] = a.w + xp[3];
+            acc[4] = bq.x + xp[4]; acc[5] = bq.y + xp[5]; acc[6] = bq.z + xp[6]; acc[7] = bq.w + xp[7];
+            const int cnt = (fresh ? 0 : (int)gs_n) + 1;
+            __syncwarp();  // every lane has read the count before lane 0 rewrites it
+            *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (lane == 0) gs[2 * kDim] = (float)cnt;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
+            const int gp = p / N;
+            const size_t go = bh * c.G + gp;
+            write_summary(acc, sg, m, c.rot, t3, s_l2[h][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
+                          (half ? o.l2_vn : o.l2_kn) + go);
+            if (lane == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
+        }
+        // t's inputs replace p's in the ring (p's were read at the start)
+        *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
     }
-    if (c.hot_tag && threadIdx.x == 32 * h) {  // the hot-group table's copy of group t / N is stale
-        int32_t* tag = c.hot_tag + bh * (c.hot_mask + 1) + ((t / N) & c.hot_mask);
-        if (*tag == t / N) *tag = -1;
-    }
+    __syncthreads();  // the slot is known
+    const int slot = s_slot;
     // L1 entry (RoPE'd key, value as coded for L3)
-    if (slot >= 0) {
+    if (head && slot >= 0) {
         const size_t so = bh * c.max_l1 + slot;
         if (half == 0) {
             float xr[8], yr[8];
@@ -698,31 +733,6 @@ __global__ void __launch_bounds__(1024) append_kernel(CacheView c, EncodeOut o, 
             if (l == 0) o.l1_vn[so] = n;
         }
     }
-    if (leaves) {
-        if (half == 0) rope_apply(xp, rope_p);
-        float* gs = o.gsum + bh * hsq::kGsumFloats;
-        const bool fresh = p % N == 0;  // p opens its group: nothing summed before it
-        float acc[8];
-        const float4 a = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_a;
-        const float4 bq = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : gs_b;
-        acc[0] = a.x + xp[0]; acc[1] = a.y + xp[1]; acc[2] = a.z + xp[2]; acc[3] = a.w + xp[3];
-        acc[4] = bq.x + xp[4]; acc[5] = bq.y + xp[5]; acc[6] = bq.z + xp[6]; acc[7] = bq.w + xp[7];
-        const int cnt = (fresh ? 0 : (int)gs_n) + 1;
-        __syncwarp();  // every lane has read the count before lane 0 rewrites it
-        *reinterpret_cast<float4*>(gs + half * kDim + 4 * l) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4*>(gs + half * kDim + 64 + 4 * l) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        if (lane == 0) gs[2 * kDim] = (float)cnt;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (float)cnt;
-        const int gp = p / N;
-        const size_t go = bh * c.G + gp;
-        write_summary(acc, sg, m, c.rot, t3, s_l2[h][half], (half ? o.l2_vc : o.l2_kc) + go * 48,
-                      (half ? o.l2_vn : o.l2_kn) + go);
-        if (lane == 0 && h == 0) o.l2_cnt[(size_t)b * c.G + gp] = (uint8_t)cnt;
-    }
-    // t's inputs replace p's in the ring (p's were read at the start)
-    *reinterpret_cast<float4*>(wp + 4 * l) = make_float4(x[0], x[1], x[2], x[3]);
-    *reinterpret_cast<float4*>(wp + 64 + 4 * l) = make_float4(x[4], x[5], x[6], x[7]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1234,7 +1244,7 @@ hsq_status hsq_append(hsq_ctx* ctx, hsq_cache* cache, const void* k, const void*
                 recent};
     const Tables tb = make_tables(ctx);
     const bool bf = dtype == HSQ_DTYPE_BF16;
-    const int threads = 32 * vw.Hkv, sinks = ctx->cfg.l1_sinks;
+    const int threads = 32 * std::min(vw.Hkv + 1, 32), sinks = ctx->cfg.l1_sinks;  // + the bookkeeping warp
     int32_t* pos = cache->l1_pos;
     int32_t* cnt = cache->l1_count;
     uint32_t* bm = cache->l1_bitmap;
