@@ -910,27 +910,50 @@ __global__ void __launch_bounds__(dec_threads<R>(), 1) decode_kernel(CacheView c
     }
     cluster.sync();  // every partial is in its owners' inboxes; no remote access follows
 
-    // this split's quads of every query head: merge the S partials and store
+    // this split's quads of every query head: merge the S partials and store,
+    // four threads per (head, quad), each over every fourth split, combined by
+    // shuffles (loop bounds uniform: a partial past S weighs nothing)
     const int nq = quad0(s + 1, S) - quad0(s, S);
+    const int nitems = R * nq;
 #pragma unroll 1
-    for (int i = tid; i < R * nq; i += NT) {
-        const int j = i / nq, kq = i - j * nq;
+    for (int base = 0; base < 4 * nitems; base += NT) {
+        if (base + (tid & ~31) >= 4 * nitems) break;  // (whole warps)
+        const int u = base + tid, item = u >> 2, sub = u & 3;
+        const bool live = item < nitems;
+        const int it = live ? item : nitems - 1;
+        const int j = it / nq, kq = it - j * nq;
         const float* in = s_inbox + (size_t)j * S * P;
         float M = -INFINITY;
-#pragma unroll 4
-        for (int r = 0; r < S; ++r) M = fmaxf(M, in[r * P + P - 4]);
+#pragma unroll 1
+        for (int r0 = 0; r0 < S; r0 += 4) {
+            const int r = min(r0 + sub, S - 1);
+            M = fmaxf(M, r0 + sub < S ? in[r * P + P - 4] : -INFINITY);
+        }
+        M = fmaxf(M, __shfl_xor_sync(kFull, M, 1));
+        M = fmaxf(M, __shfl_xor_sync(kFull, M, 2));
         float Lsum = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int r = 0; r < S; ++r) {
-            const float wt = merge_weight(in[r * P + P - 4], M);
+#pragma unroll 1
+        for (int r0 = 0; r0 < S; r0 += 4) {
+            const int r = min(r0 + sub, S - 1);
+            const float wt = r0 + sub < S ? merge_weight(in[r * P + P - 4], M) : 0.f;
             const float4 x = *reinterpret_cast<const float4*>(in + r * P + 4 * kq);
             Lsum += in[r * P + P - 3] * wt;
             o.x += x.x * wt; o.y += x.y * wt; o.z += x.z * wt; o.w += x.w * wt;
         }
-        const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-        *reinterpret_cast<float4*>(a.out + ((size_t)b * c.Hq + h * R + j) * kDim + 4 * (quad0(s, S) + kq)) =
-            make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+#pragma unroll
+        for (int d = 1; d < 4; d <<= 1) {
+            Lsum += __shfl_xor_sync(kFull, Lsum, d);
+            o.x += __shfl_xor_sync(kFull, o.x, d);
+            o.y += __shfl_xor_sync(kFull, o.y, d);
+            o.z += __shfl_xor_sync(kFull, o.z, d);
+            o.w += __shfl_xor_sync(kFull, o.w, d);
+        }
+        if (live && sub == 0) {
+            const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+            *reinterpret_cast<float4*>(a.out + ((size_t)b * c.Hq + h * R + j) * kDim + 4 * (quad0(s, S) + kq)) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        }
     }
 }
 
